@@ -1,0 +1,267 @@
+"""CPU oracle for the packed Mamba-1 conv1d + selective scan -- TEST INFRASTRUCTURE.
+
+This package wraps ``varlen_ssm_oracle.c`` (plain C, double precision, one
+sequence at a time).  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import it.  The product path
+(``selective_ssm_packed_gb300``) never does: it shares no code, header, table
+or helper with this file.
+
+Arrays are numpy float64 (values) and int32 (``cu_seqlens``), laid out as in
+the C file's header comment.  ``d_range`` picks a channel range; the
+``*_threaded`` helpers split the channel axis into blocks run on a thread
+pool (the C calls release the GIL) and add the per-block dB/dC partials in
+block order, so the result does not depend on the thread count.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "varlen_ssm_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libvarlen_ssm_oracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int32)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math: IEEE double throughout)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
+             _SRC, "-o", tmp, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.oracle_position_indices.argtypes = [_ip, ctypes.c_int32, ctypes.c_int64, _ip]
+            lib.oracle_conv1d_fwd.argtypes = [_dp, _dp, _dp, _ip, ctypes.c_int32, ctypes.c_int64,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, _dp]
+            lib.oracle_conv1d_bwd.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int32, ctypes.c_int64,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, _dp, _dp, _dp]
+            lib.oracle_scan_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int32,
+                                            _ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _dp, _dp]
+            lib.oracle_scan_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int32,
+                                            _dp, _ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+            for name in ("oracle_position_indices", "oracle_conv1d_fwd", "oracle_conv1d_bwd",
+                         "oracle_scan_fwd", "oracle_scan_bwd"):
+                getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a):
+    if a is None:
+        return None
+    if a.dtype == np.int32:
+        return a.ctypes.data_as(_ip)
+    return a.ctypes.data_as(_dp)
+
+
+def _cu(cu):
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    return cu, int(cu.shape[0] - 1), int(cu[-1]) if cu.shape[0] else 0
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise OracleError(f"{what} failed with code {rc} (malformed cu_seqlens?)")
+
+
+def position_indices(cu_seqlens, total_tokens=None):
+    cu, S, T = _cu(cu_seqlens)
+    if total_tokens is not None:
+        T = int(total_tokens)
+    pos = np.empty(T, dtype=np.int32)
+    _check(_load().oracle_position_indices(_p(cu), S, T, _p(pos)), "position_indices")
+    return pos
+
+
+def conv1d_fwd(x, weight, bias, cu_seqlens, apply_silu=True, d_range=None):
+    x, w, b = _f64(x), _f64(weight), _f64(bias)
+    cu, S, T = _cu(cu_seqlens)
+    D, W = w.shape
+    d0, d1 = d_range if d_range is not None else (0, D)
+    u = np.zeros((T, D), dtype=np.float64)
+    _check(_load().oracle_conv1d_fwd(_p(x), _p(w), _p(b), _p(cu), S, T, D, W, int(apply_silu),
+                                     d0, d1, _p(u)), "conv1d_fwd")
+    return u
+
+
+def conv1d_bwd(x, weight, bias, du, cu_seqlens, apply_silu=True, d_range=None):
+    x, w, b, du = _f64(x), _f64(weight), _f64(bias), _f64(du)
+    cu, S, T = _cu(cu_seqlens)
+    D, W = w.shape
+    d0, d1 = d_range if d_range is not None else (0, D)
+    dx = np.zeros((T, D), dtype=np.float64)
+    dw = np.zeros((D, W), dtype=np.float64)
+    db = np.zeros(D, dtype=np.float64)
+    _check(_load().oracle_conv1d_bwd(_p(x), _p(w), _p(b), _p(du), _p(cu), S, T, D, W,
+                                     int(apply_silu), d0, d1, _p(dx), _p(dw), _p(db)), "conv1d_bwd")
+    return dx, dw, db
+
+
+def scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens, delta_softplus=True,
+             d_range=None, return_last_state=False):
+    u, dr, A, B, C = _f64(u), _f64(delta_raw), _f64(A), _f64(B), _f64(C)
+    Dskip, z, dt_bias = _f64(Dskip), _f64(z), _f64(dt_bias)
+    cu, S, T = _cu(cu_seqlens)
+    D, N = A.shape
+    d0, d1 = d_range if d_range is not None else (0, D)
+    out = np.zeros((T, D), dtype=np.float64)
+    hl = np.zeros((S, D, N), dtype=np.float64) if return_last_state else None
+    _check(_load().oracle_scan_fwd(_p(u), _p(dr), _p(A), _p(B), _p(C), _p(Dskip), _p(z),
+                                   _p(dt_bias), int(delta_softplus), _p(cu), S, T, D, N, d0, d1,
+                                   _p(out), _p(hl)), "scan_fwd")
+    return (out, hl) if return_last_state else out
+
+
+def scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens, delta_softplus=True,
+             d_range=None):
+    """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias (float64)."""
+    u, dr, A, B, C = _f64(u), _f64(delta_raw), _f64(A), _f64(B), _f64(C)
+    Dskip, z, dt_bias, dout = _f64(Dskip), _f64(z), _f64(dt_bias), _f64(dout)
+    cu, S, T = _cu(cu_seqlens)
+    D, N = A.shape
+    d0, d1 = d_range if d_range is not None else (0, D)
+    g = {
+        "du": np.zeros((T, D)), "ddelta_raw": np.zeros((T, D)), "dA": np.zeros((D, N)),
+        "dB": np.zeros((T, N)), "dC": np.zeros((T, N)),
+        "dDskip": np.zeros(D) if Dskip is not None else None,
+        "dz": np.zeros((T, D)) if z is not None else None,
+        "d_dt_bias": np.zeros(D) if dt_bias is not None else None,
+    }
+    _check(_load().oracle_scan_bwd(_p(u), _p(dr), _p(A), _p(B), _p(C), _p(Dskip), _p(z),
+                                   _p(dt_bias), int(delta_softplus), _p(dout), _p(cu), S, T, D, N,
+                                   d0, d1, _p(g["du"]), _p(g["ddelta_raw"]), _p(g["dA"]),
+                                   _p(g["dB"]), _p(g["dC"]), _p(g["dDskip"]), _p(g["dz"]),
+                                   _p(g["d_dt_bias"])), "scan_bwd")
+    return g
+
+
+def _blocks(d0, d1, nblocks):
+    nblocks = max(1, min(nblocks, d1 - d0))
+    edges = np.linspace(d0, d1, nblocks + 1).round().astype(int)
+    return [(int(edges[i]), int(edges[i + 1])) for i in range(nblocks) if edges[i + 1] > edges[i]]
+
+
+def default_threads():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def scan_fwd_threaded(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens, delta_softplus=True,
+                      channels=None, threads=None):
+    """Forward scan over a channel range (default all) split across threads."""
+    D = np.asarray(A).shape[0]
+    d0, d1 = channels if channels is not None else (0, D)
+    threads = threads or default_threads()
+    args = [_f64(a) for a in (u, delta_raw, A, B, C, Dskip, z, dt_bias)]
+    outs = []
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [ex.submit(scan_fwd, *args, cu_seqlens, delta_softplus, blk)
+                for blk in _blocks(d0, d1, threads * 2)]
+        for blk, f in zip(_blocks(d0, d1, threads * 2), futs):
+            outs.append((blk, f.result()))
+    T = args[0].shape[0]
+    out = np.zeros((T, D))
+    for (b0, b1), o in outs:
+        out[:, b0:b1] = o[:, b0:b1]
+    return out
+
+
+def scan_bwd_threaded(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,
+                      delta_softplus=True, channels=None, threads=None):
+    """Backward scan over a channel range split across threads; dB/dC are the
+    sum over that range, added block by block in channel order."""
+    D = np.asarray(A).shape[0]
+    d0, d1 = channels if channels is not None else (0, D)
+    threads = threads or default_threads()
+    args = [_f64(a) for a in (u, delta_raw, A, B, C, Dskip, z, dt_bias, dout)]
+    blocks = _blocks(d0, d1, threads * 2)
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [ex.submit(scan_bwd, *args, cu_seqlens, delta_softplus, blk) for blk in blocks]
+        parts = [f.result() for f in futs]
+    res = {k: (None if v is None else np.zeros_like(v)) for k, v in parts[0].items()}
+    for (b0, b1), g in zip(blocks, parts):
+        for k in ("du", "ddelta_raw", "dz"):
+            if g[k] is not None:
+                res[k][:, b0:b1] = g[k][:, b0:b1]
+        for k in ("dA", "dDskip", "d_dt_bias"):
+            if g[k] is not None:
+                res[k][b0:b1] = g[k][b0:b1]
+        res["dB"] += g["dB"]
+        res["dC"] += g["dC"]
+    return res
+
+
+def conv1d_fwd_threaded(x, weight, bias, cu_seqlens, apply_silu=True, channels=None, threads=None):
+    D = np.asarray(weight).shape[0]
+    d0, d1 = channels if channels is not None else (0, D)
+    threads = threads or default_threads()
+    x, w, b = _f64(x), _f64(weight), _f64(bias)
+    blocks = _blocks(d0, d1, threads * 2)
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [ex.submit(conv1d_fwd, x, w, b, cu_seqlens, apply_silu, blk) for blk in blocks]
+        parts = [f.result() for f in futs]
+    u = np.zeros_like(x)
+    for (b0, b1), o in zip(blocks, parts):
+        u[:, b0:b1] = o[:, b0:b1]
+    return u
+
+
+def conv1d_bwd_threaded(x, weight, bias, du, cu_seqlens, apply_silu=True, channels=None,
+                        threads=None):
+    D = np.asarray(weight).shape[0]
+    d0, d1 = channels if channels is not None else (0, D)
+    threads = threads or default_threads()
+    x, w, b, du = _f64(x), _f64(weight), _f64(bias), _f64(du)
+    blocks = _blocks(d0, d1, threads * 2)
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [ex.submit(conv1d_bwd, x, w, b, du, cu_seqlens, apply_silu, blk) for blk in blocks]
+        parts = [f.result() for f in futs]
+    dx = np.zeros_like(x)
+    dw = np.zeros_like(w)
+    db = np.zeros(w.shape[0])
+    for (b0, b1), (pdx, pdw, pdb) in zip(blocks, parts):
+        dx[:, b0:b1] = pdx[:, b0:b1]
+        dw[b0:b1] = pdw[b0:b1]
+        db[b0:b1] = pdb[b0:b1]
+    return dx, dw, db
