@@ -1,0 +1,199 @@
+/*
+ * varlen_ssm.h -- C ABI of libvarlen_ssm.so: Mamba-1's two sequence-wise
+ * operators (depthwise causal conv1d and the selective scan), forward and
+ * backward, on PACKED variable-length batches, for NVIDIA GB300 (sm_103a).
+ *
+ * The operators follow the article "Shanghai AI Lab: packed variable-length
+ * Mamba training" (gitcode.csdn).  Its section "Mamba block 中的步骤" sorts
+ * the block's steps into element-wise, token-wise and sequence-wise ones and
+ * names conv1d and the SSM as the only sequence-wise steps; the sections
+ * "conv1d_pack 算子" and "SSM_pack算子" ask that these two steps keep the
+ * sequences of one pack from interfering.  The packed input is the
+ * FlashAttention-style pair (total_tokens, D) tensor + int32 cu_seqlens that
+ * the same article's section "基本原理" describes for its cu_seqlens version.
+ *
+ * ---------------------------------------------------------------- conventions
+ * Layouts   (T, D) tensors are row-major, channel index fastest (token t,
+ *           channel d at t*D + d).  B and C are (T, N); A is (D, N); the conv
+ *           weight is (D, W) with weight[d][W-1] multiplying the current
+ *           token (PyTorch's depthwise Conv1d layout).
+ * Dtypes    "I/O" tensors (x, u, delta_raw, z, B, C, out, dout and their
+ *           gradients du, ddelta_raw, dz, dx) are VSSM_F32 or VSSM_BF16 as the
+ *           call's `dtype` says.  Parameters (A, Dskip, dt_bias, conv weight
+ *           and bias) and their gradients are always float32.  All arithmetic,
+ *           the scan state and every accumulation are float32; bf16 results are
+ *           rounded to nearest-even once, at the store.
+ * Pointers  Every data pointer is a DEVICE pointer.  (T, D) tensors, B, C and
+ *           the workspace must be 16-byte aligned and D * sizeof(io) and
+ *           N * sizeof(io) must be multiples of 16; otherwise the call returns
+ *           VSSM_ERR_ALIGN without launching (there is no slow fallback).
+ * Ownership The caller allocates and frees everything: inputs, outputs,
+ *           gradients and the workspace, sized by the matching
+ *           *_workspace_size query.  The library never allocates, frees or
+ *           synchronises, except vssm_read_status, which synchronises `stream`.
+ * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *           stream).  Calls are enqueued on it and return before the GPU work
+ *           finishes.  Calls sharing a workspace must not overlap on the GPU.
+ * Outputs   Outputs and gradients are overwritten, never accumulated into.
+ * Edge cases T == 0 is a no-op that still zeroes parameter gradients.
+ *           Zero-length sequences are allowed (repeated cu_seqlens values).
+ * Supported N in {4, 8, 16} (N * sizeof(io) must be a multiple of 16), conv
+ *           width W in 1..4, T < 2^31, D >= 1.
+ * Errors    Every call validates its arguments on the host and returns a
+ *           negative VSSM_ERR_* code without launching anything.  Conditions
+ *           only the GPU can see (malformed cu_seqlens, a look-back wait that
+ *           ran out of time) are recorded in a status word inside the
+ *           workspace; read it with vssm_read_status.  A per-thread message
+ *           describing the last host-side error is kept (vssm_last_error).
+ * position_indices
+ *           Each call takes cu_seqlens AND an optional position_indices array
+ *           (int32, T): the per-token position inside its own sequence, built
+ *           once per pack by varlen_position_indices and reusable by every
+ *           call on that pack.  Pass NULL to have the call build it in its
+ *           workspace first.  A non-NULL array must be the one built from the
+ *           same cu_seqlens.
+ */
+#ifndef VARLEN_SSM_H
+#define VARLEN_SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { VSSM_F32 = 0, VSSM_BF16 = 1 } vssm_dtype;
+
+/* Status codes.  0 is success; host-detected errors are -1..-15; errors the
+ * GPU detected (reported by vssm_read_status) are -16 and below. */
+#define VSSM_OK 0
+#define VSSM_ERR_ARG (-1)              /* bad size, NULL where required, bad flag */
+#define VSSM_ERR_DTYPE (-2)            /* dtype not VSSM_F32 / VSSM_BF16 */
+#define VSSM_ERR_ALIGN (-3)            /* pointer or row pitch not 16-byte aligned */
+#define VSSM_ERR_WORKSPACE (-4)        /* workspace NULL or smaller than the query */
+#define VSSM_ERR_CUDA (-5)             /* a CUDA runtime / driver call failed */
+#define VSSM_ERR_UNSUPPORTED (-6)      /* N or W outside the supported set */
+#define VSSM_ERR_BAD_CU_SEQLENS (-16)  /* cu_seqlens[0] != 0, decreasing, or cu[S] != T */
+#define VSSM_ERR_LOOKBACK_TIMEOUT (-17)/* a cross-chunk wait gave up; results invalid */
+
+/* Tokens per saved scan-state chunk: the forward scan can save the state at
+ * every multiple of this many tokens for the backward scan. */
+#define VSSM_STATE_CHUNK 32
+
+/* ------------------------------------------------------------ position indices
+ * position_indices[t] = t - cu_seqlens[s] for cu_seqlens[s] <= t < cu_seqlens[s+1]:
+ * the token's position inside its own sequence, the auxiliary structure the
+ * article's pack() builds ("conv1d_pack 算子", figure (a): lengths [4,2,3,7]
+ * give 0 1 2 3 0 1 0 1 2 0 1 2 3 4 5 6).
+ *   cu_seqlens        device int32[num_seqs + 1]
+ *   position_indices  device int32[total_tokens], written
+ *   status            device int32, nullable; the kernel ORs a nonzero value
+ *                     into it when cu_seqlens is malformed (see
+ *                     vssm_status_code to turn it into a VSSM_ERR_* code).
+ */
+int varlen_position_indices(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                            int32_t* position_indices, int32_t* status, void* stream);
+
+/* Maps a raw status word written by the GPU to VSSM_OK or a VSSM_ERR_* code. */
+int vssm_status_code(int32_t status_word);
+
+/* ------------------------------------------------------------ conv1d_pack
+ * Forward ("conv1d_pack 算子", Algorithm 1): depthwise causal conv of width W
+ * whose taps stop early at each sequence's first token; tap k reaches back k
+ * tokens and is used only if position_indices[t] >= k:
+ *   pre[t,d] = bias[d] + sum_{k=0}^{W-1} [pos[t] >= k] weight[d][W-1-k] x[t-k,d]
+ *   u[t,d]   = apply_silu ? pre * sigmoid(pre) : pre
+ * x, u: (T, D) io; weight: (D, W) f32; bias: (D) f32, nullable (zero).
+ */
+size_t varlen_conv1d_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t W);
+int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                      const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+                      int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
+                      vssm_dtype dtype, void* u, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Backward (same section: the backward pass stops dx and dweight at sequence
+ * edges too, reading the position W-1 tokens LATER to know where a sequence
+ * ends).  With g[t] = du[t] * d(u)/d(pre) at t:
+ *   dx[t,d]        = sum_k [t+k < T and pos[t+k] >= k] weight[d][W-1-k] g[t+k,d]
+ *   dweight[d][W-1-k] = sum_t [pos[t] >= k] g[t,d] x[t-k,d]
+ *   dbias[d]       = sum_t g[t,d]
+ * x, du, dx: (T, D) io; dweight (D, W) f32; dbias (D) f32, nullable.  The
+ * reductions over tokens run in a fixed order (bitwise repeatable).
+ */
+size_t varlen_conv1d_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t W);
+int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, const void* du,
+                      const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+                      int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
+                      vssm_dtype dtype, void* dx, float* dweight, float* dbias,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ SSM_pack
+ * Forward ("SSM_pack算子": the state must not pass from one packed sequence to
+ * the next; the transition factor is zeroed at every sequence start, which is
+ * the same as starting each sequence from h = 0):
+ *   r      = delta_raw[t,d] + dt_bias[d]
+ *   delta  = delta_softplus ? log(1 + exp(r)) : r
+ *   h_t[n] = exp(delta A[d,n]) h_{t-1}[n] + delta B[t,n] u[t,d],  h = 0 before a start
+ *   y      = sum_n C[t,n] h_t[n] + Dskip[d] u[t,d]
+ *   out    = z ? y * SiLU(z[t,d]) : y
+ * u, delta_raw, z, out: (T, D) io; B, C: (T, N) io; A: (D, N) f32;
+ * Dskip, dt_bias: (D) f32.  Dskip, z, dt_bias are nullable (zero / no gate).
+ * chunk_states: nullable f32 (ceil(T / VSSM_STATE_CHUNK), D, N); when given,
+ * entry [c][d][n] receives the state just before token c*VSSM_STATE_CHUNK,
+ * which the backward call needs.
+ */
+size_t varlen_selective_scan_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
+size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, int32_t N);
+int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float* A,
+                              const void* B, const void* C, const float* Dskip, const void* z,
+                              const float* dt_bias, int32_t delta_softplus,
+                              const int32_t* cu_seqlens, const int32_t* position_indices,
+                              int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
+                              vssm_dtype dtype, void* out, float* chunk_states,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward: the reverse scan of the state gradient, which resets at every
+ * sequence END (the article's "SSM_pack" backward), recomputing the forward
+ * states from chunk_states.  Gradients (all overwritten):
+ *   du, ddelta_raw (w.r.t. delta_raw, i.e. before softplus), dz: (T, D) io
+ *   dA (D, N), dB (T, N), dC (T, N), dDskip (D), d_dt_bias (D): f32
+ * dz, dDskip, d_dt_bias may be NULL.  dz is written only when z is given.
+ * chunk_states is the array the forward call filled.  Every reduction (over
+ * channels for dB/dC, over tokens for dA/dDskip/d_dt_bias) is atomic-free and
+ * runs in a fixed order, so results are bitwise repeatable.
+ */
+size_t varlen_selective_scan_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
+int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
+                              const void* B, const void* C, const float* Dskip, const void* z,
+                              const float* dt_bias, int32_t delta_softplus, const void* dout,
+                              const int32_t* cu_seqlens, const int32_t* position_indices,
+                              int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
+                              vssm_dtype dtype, const float* chunk_states,
+                              void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
+                              float* dDskip, void* dz, float* d_dt_bias,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ status, errors, knobs
+ * vssm_read_status: synchronises `stream`, reads the status word the last call
+ * using `workspace` left there, and stores VSSM_OK or a VSSM_ERR_* code in
+ * *status.  Returns VSSM_OK or VSSM_ERR_CUDA / VSSM_ERR_ARG.
+ */
+int vssm_read_status(const void* workspace, void* stream, int* status);
+const char* vssm_strerror(int code);
+const char* vssm_last_error(void);      /* thread-local; "" if none */
+
+/* Test knobs (process-wide).  VSSM_DBG_DROP_FLAG: the scan work item with this
+ * ticket never publishes its look-back flag (-1 = off), so the waits behind it
+ * run out of time and report VSSM_ERR_LOOKBACK_TIMEOUT instead of hanging.
+ * VSSM_DBG_WAIT_NS: the time limit of each look-back wait in nanoseconds
+ * (default 1e9).  Returns VSSM_OK or VSSM_ERR_ARG. */
+#define VSSM_DBG_DROP_FLAG 1
+#define VSSM_DBG_WAIT_NS 2
+int vssm_debug_set(int knob, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VARLEN_SSM_H */

@@ -1,0 +1,268 @@
+"""Thin ctypes binding of libvarlen_ssm.so (argument marshalling only).
+
+Each function carries the name of the C entry point it calls (see
+include/varlen_ssm.h for the definitions, layouts and error behaviour).  It
+checks that the torch tensors it is handed are contiguous CUDA tensors of the
+right dtype, allocates outputs and workspaces the caller did not pass (with
+torch, i.e. the caching allocator), passes raw device pointers and torch's
+current stream, and raises VssmError on a non-zero status.  All arithmetic
+happens in the library's CUDA kernels; if the library is missing, every call
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+VSSM_F32, VSSM_BF16 = 0, 1
+VSSM_STATE_CHUNK = 32
+VSSM_DBG_DROP_FLAG, VSSM_DBG_WAIT_NS = 1, 2
+ERR = {0: "VSSM_OK", -1: "VSSM_ERR_ARG", -2: "VSSM_ERR_DTYPE", -3: "VSSM_ERR_ALIGN",
+       -4: "VSSM_ERR_WORKSPACE", -5: "VSSM_ERR_CUDA", -6: "VSSM_ERR_UNSUPPORTED",
+       -16: "VSSM_ERR_BAD_CU_SEQLENS", -17: "VSSM_ERR_LOOKBACK_TIMEOUT"}
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "varlen_position_indices": (ctypes.c_int, [_vp, _i32, _i64, _vp, _vp, _vp]),
+    "vssm_status_code": (ctypes.c_int, [_i32]),
+    "varlen_conv1d_fwd_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "varlen_conv1d_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                         ctypes.c_int, _vp, _vp, _sz, _vp]),
+    "varlen_conv1d_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "varlen_conv1d_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                         ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "varlen_selective_scan_fwd_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "varlen_selective_scan_chunk_states_size": (_sz, [_i64, _i32, _i32]),
+    "varlen_selective_scan_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                                 _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
+                                                 _vp, _vp, _vp, _sz, _vp]),
+    "varlen_selective_scan_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "varlen_selective_scan_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                                 _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int, _vp,
+                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                                 _vp]),
+    "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
+    "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "vssm_last_error": (ctypes.c_char_p, []),
+    "vssm_debug_set": (ctypes.c_int, [ctypes.c_int, _i64]),
+}
+
+_lib = None
+
+
+class VssmError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {ERR.get(code, code)} ({code}): {last_error()}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first with "
+                               "selective_ssm_packed_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().vssm_last_error().decode()
+
+
+def strerror(code: int) -> str:
+    return lib().vssm_strerror(code).decode()
+
+
+def debug_set(knob: int, value: int) -> None:
+    _check(lib().vssm_debug_set(knob, value), "vssm_debug_set")
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise VssmError(rc, what)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return VSSM_F32
+    if t.dtype == torch.bfloat16:
+        return VSSM_BF16
+    raise TypeError(f"I/O tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr() or None
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ws(workspace, nbytes, device):
+    if workspace is None:
+        return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace too small: {workspace.numel()} < {nbytes} bytes")
+    return workspace
+
+
+def read_status(workspace: torch.Tensor, stream=None) -> int:
+    st = ctypes.c_int(0)
+    _check(lib().vssm_read_status(_ptr(workspace, "workspace"), _stream(stream), ctypes.byref(st)),
+           "vssm_read_status")
+    return st.value
+
+
+def status_code(word: int) -> int:
+    return lib().vssm_status_code(int(word))
+
+
+# ------------------------------------------------------------------ position indices
+def varlen_position_indices(cu_seqlens, total_tokens, out=None, status=None, stream=None):
+    cu = cu_seqlens
+    _ptr(cu, "cu_seqlens", torch.int32)
+    T = int(total_tokens)
+    if out is None:
+        out = torch.empty(T, dtype=torch.int32, device=cu.device)
+    _check(lib().varlen_position_indices(_ptr(cu, "cu_seqlens"), cu.numel() - 1, T,
+                                         _ptr(out, "out", torch.int32),
+                                         _ptr(status, "status", torch.int32), _stream(stream)),
+           "varlen_position_indices")
+    return out
+
+
+# ------------------------------------------------------------------ conv1d
+def conv1d_fwd_workspace_size(T, D, W):
+    return lib().varlen_conv1d_fwd_workspace_size(int(T), int(D), int(W))
+
+
+def conv1d_bwd_workspace_size(T, D, W):
+    return lib().varlen_conv1d_bwd_workspace_size(int(T), int(D), int(W))
+
+
+def varlen_conv1d_fwd(x, weight, bias, cu_seqlens, position_indices=None, apply_silu=True,
+                      out=None, workspace=None, stream=None):
+    T, D = x.shape
+    W = weight.shape[1]
+    out = torch.empty_like(x) if out is None else out
+    ws = _ws(workspace, conv1d_fwd_workspace_size(T, D, W), x.device)
+    _check(lib().varlen_conv1d_fwd(
+        _ptr(x, "x"), _ptr(weight, "weight", torch.float32), _ptr(bias, "bias", torch.float32),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
+        cu_seqlens.numel() - 1, T, D, W, int(bool(apply_silu)), _dt(x), _ptr(out, "out", x.dtype),
+        _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_conv1d_fwd")
+    return out
+
+
+def varlen_conv1d_bwd(x, weight, bias, du, cu_seqlens, position_indices=None, apply_silu=True,
+                      dx=None, dweight=None, dbias=None, workspace=None, stream=None):
+    T, D = x.shape
+    W = weight.shape[1]
+    dx = torch.empty_like(x) if dx is None else dx
+    dweight = torch.empty_like(weight) if dweight is None else dweight
+    if dbias is None and bias is not None:
+        dbias = torch.empty_like(bias)
+    ws = _ws(workspace, conv1d_bwd_workspace_size(T, D, W), x.device)
+    _check(lib().varlen_conv1d_bwd(
+        _ptr(x, "x"), _ptr(weight, "weight", torch.float32), _ptr(bias, "bias", torch.float32),
+        _ptr(du, "du", x.dtype), _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+        _ptr(position_indices, "position_indices", torch.int32), cu_seqlens.numel() - 1, T, D, W,
+        int(bool(apply_silu)), _dt(x), _ptr(dx, "dx", x.dtype), _ptr(dweight, "dweight", torch.float32),
+        _ptr(dbias, "dbias", torch.float32), _ptr(ws, "workspace"), ws.numel(), _stream(stream)),
+        "varlen_conv1d_bwd")
+    return dx, dweight, dbias
+
+
+# ------------------------------------------------------------------ selective scan
+def scan_fwd_workspace_size(T, D, N):
+    return lib().varlen_selective_scan_fwd_workspace_size(int(T), int(D), int(N))
+
+
+def scan_bwd_workspace_size(T, D, N):
+    return lib().varlen_selective_scan_bwd_workspace_size(int(T), int(D), int(N))
+
+
+def chunk_states_shape(T, D, N):
+    return ((int(T) + VSSM_STATE_CHUNK - 1) // VSSM_STATE_CHUNK, int(D), int(N))
+
+
+def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens,
+                              position_indices=None, delta_softplus=True, out=None,
+                              chunk_states=True, workspace=None, stream=None):
+    """Returns (out, chunk_states).  chunk_states=True allocates the saved-state
+    array the backward call needs, False/None skips it, a tensor is filled."""
+    T, D = u.shape
+    N = A.shape[1]
+    out = torch.empty_like(u) if out is None else out
+    if chunk_states is True:
+        chunk_states = torch.empty(chunk_states_shape(T, D, N), dtype=torch.float32, device=u.device)
+    elif chunk_states is False:
+        chunk_states = None
+    ws = _ws(workspace, scan_fwd_workspace_size(T, D, N), u.device)
+    dt = u.dtype
+    _check(lib().varlen_selective_scan_fwd(
+        _ptr(u, "u"), _ptr(delta_raw, "delta_raw", dt), _ptr(A, "A", torch.float32),
+        _ptr(B, "B", dt), _ptr(C, "C", dt), _ptr(Dskip, "Dskip", torch.float32), _ptr(z, "z", dt),
+        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
+        cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(out, "out", dt),
+        _ptr(chunk_states, "chunk_states", torch.float32), _ptr(ws, "workspace"), ws.numel(),
+        _stream(stream)), "varlen_selective_scan_fwd")
+    return out, chunk_states
+
+
+def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,
+                              chunk_states, position_indices=None, delta_softplus=True,
+                              grads=None, workspace=None, stream=None):
+    """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias."""
+    T, D = u.shape
+    N = A.shape[1]
+    dt = u.dtype
+    g = dict(grads or {})
+    g.setdefault("du", torch.empty_like(u))
+    g.setdefault("ddelta_raw", torch.empty_like(u))
+    g.setdefault("dA", torch.empty_like(A))
+    g.setdefault("dB", torch.empty((T, N), dtype=torch.float32, device=u.device))
+    g.setdefault("dC", torch.empty((T, N), dtype=torch.float32, device=u.device))
+    g.setdefault("dDskip", torch.empty_like(Dskip) if Dskip is not None else None)
+    g.setdefault("dz", torch.empty_like(z) if z is not None else None)
+    g.setdefault("d_dt_bias", torch.empty_like(dt_bias) if dt_bias is not None else None)
+    ws = _ws(workspace, scan_bwd_workspace_size(T, D, N), u.device)
+    _check(lib().varlen_selective_scan_bwd(
+        _ptr(u, "u"), _ptr(delta_raw, "delta_raw", dt), _ptr(A, "A", torch.float32),
+        _ptr(B, "B", dt), _ptr(C, "C", dt), _ptr(Dskip, "Dskip", torch.float32), _ptr(z, "z", dt),
+        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)), _ptr(dout, "dout", dt),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
+        cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(chunk_states, "chunk_states", torch.float32),
+        _ptr(g["du"], "du", dt), _ptr(g["ddelta_raw"], "ddelta_raw", dt),
+        _ptr(g["dA"], "dA", torch.float32), _ptr(g["dB"], "dB", torch.float32),
+        _ptr(g["dC"], "dC", torch.float32), _ptr(g["dDskip"], "dDskip", torch.float32),
+        _ptr(g["dz"], "dz", dt), _ptr(g["d_dt_bias"], "d_dt_bias", torch.float32),
+        _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_selective_scan_bwd")
+    return g

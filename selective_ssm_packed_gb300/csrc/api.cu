@@ -1,0 +1,469 @@
+// api.cu -- the C ABI of libvarlen_ssm.so (declared in include/varlen_ssm.h):
+// argument validation, workspace layout, TMA descriptors, kernel launches,
+// device status words and error reporting.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+#include "varlen_ssm.h"
+
+using namespace vssm;
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<long long> g_drop_ticket{-1};
+std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(VSSM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- workspace layout
+// [header 256 B: status int @0, ticket uint @4][flags][pos][...call specific]
+// header + flags are cleared by one memset at the start of every call.
+struct Layout {
+  size_t flags = 0, pos = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, conv_part = 0;
+  size_t clear_bytes = 0, total = 0;
+};
+
+Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
+  Layout l;
+  const int64_t n_tiles = cdiv(D, kTile);
+  const int64_t n_chunks = cdiv(T, chunk);
+  const int64_t slots = n_tiles * n_chunks;
+  size_t off = kAlign;
+  l.flags = off;
+  off += up(sizeof(int) * (size_t)slots);
+  l.clear_bytes = off;
+  l.pos = off;
+  off += up(sizeof(int32_t) * (size_t)T);
+  l.agg = off;
+  off += up(sizeof(float) * (size_t)slots * N * kTile);
+  l.agg_sd = off;
+  off += up(sizeof(float) * (size_t)slots * kTile);
+  l.incl = off;
+  off += up(sizeof(float) * (size_t)slots * N * kTile);
+  if (bwd) {
+    l.part_bc = off;
+    off += up(sizeof(float) * (size_t)n_tiles * T * 2 * N);
+    l.part_a = off;
+    off += up(sizeof(float) * (size_t)n_chunks * D * N);
+    l.part_d = off;
+    off += up(sizeof(float) * (size_t)n_chunks * D);
+    l.part_b = off;
+    off += up(sizeof(float) * (size_t)n_chunks * D);
+  }
+  l.total = off;
+  return l;
+}
+
+Layout conv_layout(int64_t T, int D, int W, bool bwd) {
+  Layout l;
+  size_t off = kAlign;
+  l.clear_bytes = off;
+  l.pos = off;
+  off += up(sizeof(int32_t) * (size_t)T);
+  if (bwd) {
+    l.conv_part = off;
+    off += up(sizeof(float) * (size_t)conv_bwd_partial_rows(T) * D * (W + 1));
+  }
+  l.total = off;
+  return l;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a (T, D) row-major tensor, box = box_x channels x box_y tokens.
+int make_map(CUtensorMap* m, const void* base, IO io, int64_t T, int D, int box_x, int box_y) {
+  std::memset(m, 0, sizeof(*m));
+  if (!base) return VSSM_OK;
+  auto enc = encoder();
+  if (!enc) return fail(VSSM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * (cuuint64_t)io_bytes(io)};
+  const cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_y};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, io == IO::F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(VSSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return VSSM_OK;
+}
+
+// ---------------------------------------------------------------- validation
+int check_dtype(vssm_dtype dt, IO* io) {
+  if (dt == VSSM_F32) { *io = IO::F32; return VSSM_OK; }
+  if (dt == VSSM_BF16) { *io = IO::BF16; return VSSM_OK; }
+  return fail(VSSM_ERR_DTYPE, "dtype %d is neither VSSM_F32 nor VSSM_BF16", (int)dt);
+}
+
+int check_shape(int64_t T, int D, int32_t num_seqs, const int32_t* cu) {
+  if (T < 0 || T > 2147483647LL) return fail(VSSM_ERR_ARG, "total_tokens %lld out of range", (long long)T);
+  if (D <= 0) return fail(VSSM_ERR_ARG, "D must be positive (got %d)", D);
+  if (num_seqs < 0) return fail(VSSM_ERR_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
+  if (!cu) return fail(VSSM_ERR_ARG, "cu_seqlens is NULL");
+  return VSSM_OK;
+}
+
+int check_io(const void* p, const char* name, int64_t T) {
+  if (T == 0) return VSSM_OK;
+  if (!p) return fail(VSSM_ERR_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(VSSM_ERR_ALIGN, "%s is not 16-byte aligned", name);
+  return VSSM_OK;
+}
+
+int check_ws(const void* ws, size_t have, size_t need) {
+  if (have < need) return fail(VSSM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", have, need);
+  if (!ws) return fail(VSSM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned16(ws)) return fail(VSSM_ERR_ALIGN, "workspace is not 16-byte aligned");
+  return VSSM_OK;
+}
+
+// Resolves the position indices a call uses: the caller's array, or one built
+// in the workspace from cu_seqlens (status bits land in the workspace header).
+int resolve_pos(const int32_t* cu, const int32_t* pos_in, int32_t S, int64_t T, void* ws,
+                const Layout& l, cudaStream_t st, const int32_t** pos_out) {
+  if (pos_in) { *pos_out = pos_in; return VSSM_OK; }
+  int32_t* p = at<int32_t>(ws, l.pos);
+  cudaError_t e = launch_position_indices(cu, S, T, p, at<int32_t>(ws, 0), st);
+  if (e != cudaSuccess) return cuda_fail(e, "position_indices launch");
+  *pos_out = p;
+  return VSSM_OK;
+}
+
+#define VSSM_TRY(expr)              \
+  do {                              \
+    const int rc_ = (expr);         \
+    if (rc_ != VSSM_OK) return rc_; \
+  } while (0)
+
+}  // namespace
+
+// ============================================================================ C ABI
+extern "C" {
+
+int vssm_status_code(int32_t w) {
+  if (w & kStatusBadCu) return VSSM_ERR_BAD_CU_SEQLENS;
+  if (w & (kStatusLookbackTimeout | kStatusTmaTimeout)) return VSSM_ERR_LOOKBACK_TIMEOUT;
+  return VSSM_OK;
+}
+
+const char* vssm_strerror(int code) {
+  switch (code) {
+    case VSSM_OK: return "success";
+    case VSSM_ERR_ARG: return "invalid argument";
+    case VSSM_ERR_DTYPE: return "unsupported dtype";
+    case VSSM_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case VSSM_ERR_WORKSPACE: return "workspace missing or too small";
+    case VSSM_ERR_CUDA: return "CUDA runtime or driver error";
+    case VSSM_ERR_UNSUPPORTED: return "unsupported N or conv width";
+    case VSSM_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens (device check)";
+    case VSSM_ERR_LOOKBACK_TIMEOUT: return "cross-chunk wait timed out (device check)";
+  }
+  return "unknown status code";
+}
+
+const char* vssm_last_error(void) { return g_last_error.c_str(); }
+
+int vssm_debug_set(int knob, int64_t value) {
+  if (knob == VSSM_DBG_DROP_FLAG) { g_drop_ticket.store(value); return VSSM_OK; }
+  if (knob == VSSM_DBG_WAIT_NS) {
+    if (value <= 0) return fail(VSSM_ERR_ARG, "wait limit must be positive");
+    g_wait_ns.store((unsigned long long)value);
+    return VSSM_OK;
+  }
+  return fail(VSSM_ERR_ARG, "unknown debug knob %d", knob);
+}
+
+int vssm_read_status(const void* workspace, void* stream, int* status) {
+  if (!workspace || !status) return fail(VSSM_ERR_ARG, "workspace and status must be non-NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t w = 0;
+  cudaError_t e = cudaMemcpyAsync(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  *status = vssm_status_code(w);
+  return VSSM_OK;
+}
+
+// ---------------------------------------------------------------- position indices
+int varlen_position_indices(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                            int32_t* position_indices, int32_t* status, void* stream) {
+  VSSM_TRY(check_shape(total_tokens, 1, num_seqs, cu_seqlens));
+  if (total_tokens > 0 && !position_indices) return fail(VSSM_ERR_ARG, "position_indices is NULL");
+  cudaError_t e = launch_position_indices(cu_seqlens, num_seqs, total_tokens, position_indices,
+                                          status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "position_indices launch");
+}
+
+// ---------------------------------------------------------------- conv1d
+size_t varlen_conv1d_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t W) {
+  if (total_tokens < 0 || D <= 0 || W < 1 || W > 4) return 0;
+  return conv_layout(total_tokens, D, W, false).total;
+}
+
+size_t varlen_conv1d_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t W) {
+  if (total_tokens < 0 || D <= 0 || W < 1 || W > 4) return 0;
+  return conv_layout(total_tokens, D, W, true).total;
+}
+
+static int conv_common(const void* x, const float* weight, const int32_t* cu, int32_t num_seqs,
+                       int64_t T, int32_t D, int32_t W, vssm_dtype dtype, IO* io) {
+  VSSM_TRY(check_dtype(dtype, io));
+  VSSM_TRY(check_shape(T, D, num_seqs, cu));
+  if (W < 1 || W > 4) return fail(VSSM_ERR_UNSUPPORTED, "conv width %d not in 1..4", W);
+  if (((int64_t)D * io_bytes(*io)) % 16 != 0)
+    return fail(VSSM_ERR_ALIGN, "D * sizeof(io) = %lld is not a multiple of 16",
+                (long long)D * io_bytes(*io));
+  if (!weight) return fail(VSSM_ERR_ARG, "weight is NULL");
+  VSSM_TRY(check_io(x, "x", T));
+  return VSSM_OK;
+}
+
+int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                      const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+                      int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
+                      vssm_dtype dtype, void* u, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  IO io;
+  VSSM_TRY(conv_common(x, weight, cu_seqlens, num_seqs, total_tokens, D, W, dtype, &io));
+  VSSM_TRY(check_io(u, "u", total_tokens));
+  const Layout l = conv_layout(total_tokens, D, W, false);
+  VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  if (total_tokens == 0) return VSSM_OK;
+  const int32_t* pos = nullptr;
+  VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, total_tokens, workspace, l, st, &pos));
+  ConvArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.pos = pos; a.out = u;
+  a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
+  e = launch_conv1d_fwd(a, io, st);
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_fwd launch");
+}
+
+int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, const void* du,
+                      const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+                      int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
+                      vssm_dtype dtype, void* dx, float* dweight, float* dbias,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  IO io;
+  VSSM_TRY(conv_common(x, weight, cu_seqlens, num_seqs, total_tokens, D, W, dtype, &io));
+  VSSM_TRY(check_io(du, "du", total_tokens));
+  VSSM_TRY(check_io(dx, "dx", total_tokens));
+  if (!dweight) return fail(VSSM_ERR_ARG, "dweight is NULL");
+  const Layout l = conv_layout(total_tokens, D, W, true);
+  VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  const int32_t* pos = nullptr;
+  if (total_tokens > 0)
+    VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, total_tokens, workspace, l, st, &pos));
+  ConvArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.pos = pos; a.du = du; a.out = dx;
+  a.partial = at<float>(workspace, l.conv_part);
+  a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
+  e = launch_conv1d_bwd(a, io, dweight, dbias, st);
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_bwd launch");
+}
+
+// ---------------------------------------------------------------- selective scan
+size_t varlen_selective_scan_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N) {
+  if (total_tokens < 0 || D <= 0 || N <= 0) return 0;
+  return scan_layout(total_tokens, D, N, kFwdChunk, false).total;
+}
+
+size_t varlen_selective_scan_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N) {
+  if (total_tokens < 0 || D <= 0 || N <= 0) return 0;
+  return scan_layout(total_tokens, D, N, kBwdChunk, true).total;
+}
+
+size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, int32_t N) {
+  if (total_tokens < 0 || D <= 0 || N <= 0) return 0;
+  return sizeof(float) * (size_t)cdiv(total_tokens, kStateChunk) * (size_t)D * (size_t)N;
+}
+
+static int scan_common(const void* u, const void* delta_raw, const float* A, const void* B,
+                       const void* C, const void* z, const int32_t* cu, int32_t num_seqs,
+                       int64_t T, int32_t D, int32_t N, vssm_dtype dtype, IO* io) {
+  VSSM_TRY(check_dtype(dtype, io));
+  VSSM_TRY(check_shape(T, D, num_seqs, cu));
+  if (N != 4 && N != 8 && N != 16) return fail(VSSM_ERR_UNSUPPORTED, "N = %d not in {4, 8, 16}", N);
+  const int e = io_bytes(*io);
+  if (((int64_t)D * e) % 16 != 0)
+    return fail(VSSM_ERR_ALIGN, "D * sizeof(io) = %lld is not a multiple of 16", (long long)D * e);
+  if ((N * e) % 16 != 0)
+    return fail(VSSM_ERR_ALIGN, "N * sizeof(io) = %d is not a multiple of 16", N * e);
+  if (!A) return fail(VSSM_ERR_ARG, "A is NULL");
+  VSSM_TRY(check_io(u, "u", T));
+  VSSM_TRY(check_io(delta_raw, "delta_raw", T));
+  VSSM_TRY(check_io(B, "B", T));
+  VSSM_TRY(check_io(C, "C", T));
+  if (z && !aligned16(z)) return fail(VSSM_ERR_ALIGN, "z is not 16-byte aligned");
+  return VSSM_OK;
+}
+
+int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float* A,
+                              const void* B, const void* C, const float* Dskip, const void* z,
+                              const float* dt_bias, int32_t delta_softplus,
+                              const int32_t* cu_seqlens, const int32_t* position_indices,
+                              int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
+                              vssm_dtype dtype, void* out, float* chunk_states,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  IO io;
+  VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, cu_seqlens, num_seqs, total_tokens, D, N, dtype, &io));
+  VSSM_TRY(check_io(out, "out", total_tokens));
+  if (chunk_states && !aligned16(chunk_states))
+    return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
+  const int64_t T = total_tokens;
+  const Layout l = scan_layout(T, D, N, kFwdChunk, false);
+  VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  if (T == 0) return VSSM_OK;
+  const int32_t* pos = nullptr;
+  VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, T, workspace, l, st, &pos));
+
+  ScanArgs a{};
+  a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
+  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out;
+  a.status = at<int>(workspace, 0);
+  a.ticket = at<unsigned>(workspace, 4);
+  a.flags = at<int>(workspace, l.flags);
+  a.agg = at<float>(workspace, l.agg);
+  a.agg_sd = at<float>(workspace, l.agg_sd);
+  a.incl = at<float>(workspace, l.incl);
+  a.T = T; a.D = D; a.N = N;
+  a.n_tiles = (int)cdiv(D, kTile);
+  a.n_chunks = (int)cdiv(T, kFwdChunk);
+  a.delta_softplus = delta_softplus ? 1 : 0;
+  a.has_z = z ? 1 : 0;
+  a.has_skip = Dskip ? 1 : 0;
+  a.box_x = D < kTile ? D : kTile;
+  a.box_y = T < kFwdChunk ? (int)T : kFwdChunk;
+  a.drop_ticket = g_drop_ticket.load();
+  a.wait_ns = g_wait_ns.load();
+  CUtensorMap mu, mdr, mz;
+  VSSM_TRY(make_map(&mu, u, io, T, D, a.box_x, a.box_y));
+  VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
+  VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
+  e = launch_scan_fwd(a, io, mu, mdr, mz, st);
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_fwd launch");
+}
+
+int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
+                              const void* B, const void* C, const float* Dskip, const void* z,
+                              const float* dt_bias, int32_t delta_softplus, const void* dout,
+                              const int32_t* cu_seqlens, const int32_t* position_indices,
+                              int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
+                              vssm_dtype dtype, const float* chunk_states,
+                              void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
+                              float* dDskip, void* dz, float* d_dt_bias,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  IO io;
+  VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, cu_seqlens, num_seqs, total_tokens, D, N, dtype, &io));
+  const int64_t T = total_tokens;
+  VSSM_TRY(check_io(dout, "dout", T));
+  VSSM_TRY(check_io(du, "du", T));
+  VSSM_TRY(check_io(ddelta_raw, "ddelta_raw", T));
+  VSSM_TRY(check_io(dB, "dB", T));
+  VSSM_TRY(check_io(dC, "dC", T));
+  if (!dA) return fail(VSSM_ERR_ARG, "dA is NULL");
+  if (T > 0 && !chunk_states) return fail(VSSM_ERR_ARG, "chunk_states is NULL");
+  if (z && T > 0 && !dz) return fail(VSSM_ERR_ARG, "dz is NULL although z is given");
+  if (dz && !aligned16(dz)) return fail(VSSM_ERR_ALIGN, "dz is not 16-byte aligned");
+  const Layout l = scan_layout(T, D, N, kBwdChunk, true);
+  VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+
+  ScanArgs a{};
+  a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
+  a.dt_bias = dt_bias; a.dout = dout; a.chunk_states = const_cast<float*>(chunk_states);
+  a.du = du; a.ddr = ddelta_raw; a.dz = z ? dz : nullptr;
+  a.status = at<int>(workspace, 0);
+  a.ticket = at<unsigned>(workspace, 4);
+  a.flags = at<int>(workspace, l.flags);
+  a.agg = at<float>(workspace, l.agg);
+  a.agg_sd = at<float>(workspace, l.agg_sd);
+  a.incl = at<float>(workspace, l.incl);
+  a.part_dBC = at<float>(workspace, l.part_bc);
+  a.part_dA = at<float>(workspace, l.part_a);
+  a.part_dD = at<float>(workspace, l.part_d);
+  a.part_dbias = at<float>(workspace, l.part_b);
+  a.T = T; a.D = D; a.N = N;
+  a.n_tiles = (int)cdiv(D, kTile);
+  a.n_chunks = (int)cdiv(T, kBwdChunk);
+  a.delta_softplus = delta_softplus ? 1 : 0;
+  a.has_z = z ? 1 : 0;
+  a.has_skip = Dskip ? 1 : 0;
+  a.box_x = D < kTile ? D : kTile;
+  a.box_y = T < kBwdChunk ? (int)T : kBwdChunk;
+  a.drop_ticket = g_drop_ticket.load();
+  a.wait_ns = g_wait_ns.load();
+  CUtensorMap mu, mdr, mz, mdo;
+  std::memset(&mu, 0, sizeof(mu));
+  std::memset(&mdr, 0, sizeof(mdr));
+  std::memset(&mz, 0, sizeof(mz));
+  std::memset(&mdo, 0, sizeof(mdo));
+  if (T > 0) {
+    const int32_t* pos = nullptr;
+    VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, T, workspace, l, st, &pos));
+    a.pos = pos;
+    VSSM_TRY(make_map(&mu, u, io, T, D, a.box_x, a.box_y));
+    VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
+    VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
+    VSSM_TRY(make_map(&mdo, dout, io, T, D, a.box_x, a.box_y));
+  }
+  e = launch_scan_bwd(a, io, mu, mdr, mz, mdo, dA, dB, dC, dDskip, d_dt_bias, st);
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_bwd launch");
+}
+
+}  // extern "C"

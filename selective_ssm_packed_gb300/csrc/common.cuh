@@ -1,0 +1,172 @@
+// common.cuh -- device helpers shared by the libvarlen_ssm kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace vssm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// look-back flag values
+enum : int { kFlagNone = 0, kFlagAggregate = 1, kFlagInclusive = 2 };
+
+// ------------------------------------------------------------------ I/O types
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// ------------------------------------------------------------------ math
+// 2^x on the MUFU unit (PTX ex2.approx, flush-to-zero): exp(x) = ex2(x * log2 e).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float sigmoidf_fast(float x) {
+  return __fdividef(1.0f, 1.0f + ex2(-x * kLog2e));
+}
+
+// SiLU(x) = x * sigmoid(x)
+__device__ __forceinline__ float siluf(float x) { return x * sigmoidf_fast(x); }
+
+// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^-|x|); above 20 the second
+// term is below fp32 resolution of x.
+__device__ __forceinline__ float softplusf(float x) {
+  if (x > 20.0f) return x;
+  return fmaxf(x, 0.0f) + log1pf(ex2(-fabsf(x) * kLog2e));
+}
+
+// ------------------------------------------------------------------ timers, memory order
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Spin (with backoff) until *flag != 0 or `limit_ns` passes.  Returns the flag
+// value, or 0 after a timeout (the caller records the error and carries on).
+__device__ __forceinline__ int wait_flag(const int* flag, uint64_t limit_ns) {
+  int v = ld_acquire_gpu(flag);
+  if (v != 0) return v;
+  const uint64_t t0 = globaltimer_ns();
+  unsigned backoff = 32;
+  for (;;) {
+    __nanosleep(backoff);
+    v = ld_acquire_gpu(flag);
+    if (v != 0) return v;
+    if (globaltimer_ns() - t0 > limit_ns) return 0;
+    if (backoff < 1024) backoff <<= 1;
+  }
+}
+
+// ------------------------------------------------------------------ mbarrier + TMA
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier; gives up after limit_ns (returns false).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// 2-D tiled TMA load of box (x = inner coordinate, y = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------------ vector loads of N values
+// Loads N consecutive io values from shared memory (16-byte aligned) as floats.
+template <int N>
+__device__ __forceinline__ void lds_row(float (&v)[N], const float* p) {
+  static_assert(N % 4 == 0, "N must be a multiple of 4");
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p + i);
+    v[i] = q.x; v[i + 1] = q.y; v[i + 2] = q.z; v[i + 3] = q.w;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void lds_row(float (&v)[N], const __nv_bfloat16* p) {
+  static_assert(N % 8 == 0, "N must be a multiple of 8 for bf16");
+#pragma unroll
+  for (int i = 0; i < N; i += 8) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[i + 2 * j] = f.x;
+      v[i + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+}  // namespace vssm

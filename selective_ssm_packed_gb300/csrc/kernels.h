@@ -1,0 +1,101 @@
+// kernels.h -- internal launcher interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vssm {
+
+enum class IO { F32 = 0, BF16 = 1 };
+
+inline int io_bytes(IO t) { return t == IO::F32 ? 4 : 2; }
+
+constexpr int kStateChunk = 32;  // tokens per saved scan-state chunk
+
+// status-word bits written by kernels (the host maps them to VSSM_ERR_* codes)
+enum : int { kStatusBadCu = 1, kStatusLookbackTimeout = 2, kStatusTmaTimeout = 4 };
+
+// ---------------------------------------------------------------- position indices
+cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
+                                    int32_t* status, cudaStream_t st);
+
+// ---------------------------------------------------------------- conv1d
+struct ConvArgs {
+  const void* x;
+  const float* w;      // (D, W)
+  const float* bias;   // (D) or null
+  const int32_t* pos;  // (T)
+  const void* du;      // bwd only
+  void* out;           // fwd: u; bwd: dx
+  float* partial;      // bwd: [rows_of_ctas][D*W + D]
+  int64_t T;
+  int D;
+  int W;
+  int apply_silu;
+};
+// Number of token-rows of CTAs the backward kernel uses (partial buffer rows).
+int64_t conv_bwd_partial_rows(int64_t T);
+cudaError_t launch_conv1d_fwd(const ConvArgs& a, IO io, cudaStream_t st);
+cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, float* dweight, float* dbias,
+                              cudaStream_t st);
+
+// ---------------------------------------------------------------- selective scan
+constexpr int kFwdChunk = 128;   // tokens per forward work item (look-back granule)
+constexpr int kBwdChunk = 32;    // tokens per backward work item (= saved-state chunk)
+constexpr int kTile = 32;        // channels per work item
+
+struct ScanArgs {
+  const void* u;
+  const void* dr;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* Dskip;
+  const void* z;
+  const float* dt_bias;
+  const void* dout;           // bwd
+  const int32_t* pos;
+  float* chunk_states;        // fwd: written (nullable); bwd: read
+  void* out;                  // fwd
+  void* du;                   // bwd
+  void* ddr;                  // bwd
+  void* dz;                   // bwd (nullable)
+  float* part_dBC;            // bwd [n_tiles][T][2N]
+  float* part_dA;             // bwd [n_chunks][D][N]
+  float* part_dD;             // bwd [n_chunks][D]
+  float* part_dbias;          // bwd [n_chunks][D]
+  int* status;
+  unsigned* ticket;
+  int* flags;                 // [n_tiles][n_chunks]
+  float* agg;                 // [n_tiles][n_chunks][N][kTile]
+  float* agg_sd;              // [n_tiles][n_chunks][kTile]
+  float* incl;                // [n_tiles][n_chunks][N][kTile]
+  int64_t T;
+  int D;
+  int N;
+  int n_tiles;
+  int n_chunks;
+  int delta_softplus;
+  int has_z;
+  int has_skip;
+  int box_x;                  // tile row pitch in elements: min(kTile, D)
+  int box_y;                  // tile rows: min(chunk, T)
+  long long drop_ticket;
+  unsigned long long wait_ns;
+};
+
+cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
+                            const CUtensorMap& tm_dr, const CUtensorMap& tm_z, cudaStream_t st);
+cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
+                            const CUtensorMap& tm_dr, const CUtensorMap& tm_z,
+                            const CUtensorMap& tm_dout, float* dA, float* dB, float* dC,
+                            float* dDskip, float* d_dt_bias, cudaStream_t st);
+
+// ---------------------------------------------------------------- reductions
+// out[m] = sum_{p < P} in[p * ld + m] for m < M, p in increasing order.
+cudaError_t launch_sum_rows(const float* in, int64_t P, int64_t M, int64_t ld, float* out,
+                            cudaStream_t st);
+
+}  // namespace vssm

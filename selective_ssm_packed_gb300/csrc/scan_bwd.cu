@@ -1,0 +1,504 @@
+// scan_bwd.cu -- packed selective scan, backward (sm_103a).
+//
+// Work item = (chunk of kBwdChunk = 32 tokens, the saved-state granule) x
+// (tile of kTile = 32 channels); items are taken in DESCENDING chunk order
+// from an atomic ticket because the state gradient flows from the end of a
+// sequence to its start.  CTA = 8 warps; warp s owns K = 4 tokens, lane l owns
+// channel d0 + l with all N states.
+//
+// With a_t = exp(delta_t A) (0 at a sequence start), g_t = dout_t SiLU(z_t),
+// the state gradient obeys dh_t = a_{t+1} dh_{t+1} + C_t g_t and is zero after
+// the last token of every sequence (a_{t+1} = 0 when t+1 starts a sequence):
+// the reverse scan that resets at sequence ends.
+//
+//   1. TMA: u, delta_raw, dout, z tiles (32 x 32), B and C rows; per-token
+//      delta, SiLU(z), g kept in registers.
+//   2. Forward states: pass over the K tokens from h = 0 -> sub-chunk
+//      aggregates; exclusive scan seeded with the chunk's saved state
+//      (chunk_states from the forward call) gives each thread its start state.
+//   3. Reverse aggregates: pass over the K tokens backwards from dh = 0; the
+//      left-going carry of a block is (prod a) * carry_in + G, with G the carry
+//      out when nothing comes in; exclusive reverse scan in shared memory.
+//   4. Decoupled look-back towards HIGHER chunks for the carry entering the
+//      chunk from the right, re-applied in a fixed order (bitwise repeatable),
+//      time-bounded waits.
+//   5. Recompute the K forward states into shared memory, then walk the K
+//      tokens backwards producing du, d(delta_raw), dz and per-token partial
+//      dB, dC (reduced over the warp's 32 channels with a butterfly
+//      reduce-scatter, no atomics) and per-thread partial dA, dDskip, d_dt_bias.
+//   6. Fixed-order CTA reduction of the partials; separate fixed-order kernels
+//      sum them over channel tiles (dB, dC) and chunks (dA, dDskip, d_dt_bias).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace vssm {
+
+namespace {
+
+constexpr int kL = kBwdChunk;   // 32
+constexpr int kS = 8;
+constexpr int kK = kL / kS;     // 4
+constexpr int kThreads = kS * 32;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T, int N>
+struct BwdSmem {
+  alignas(128) T u[kL * kTile];
+  alignas(128) T dr[kL * kTile];
+  alignas(128) T z[kL * kTile];
+  alignas(128) T dout[kL * kTile];
+  alignas(128) T B[kL * N];
+  alignas(128) T C[kL * N];
+  alignas(16) float hist[kK * N * kThreads];  // [k][n][tid]
+  alignas(16) float agg[kS * N * kTile];
+  float tot[N * kTile];
+  float rin[N * kTile];
+  float aggSD[kS * kTile];
+  float redD[kS * kTile];
+  float redB[kS * kTile];
+  int pos[kL];
+  int aggRS[kS];
+  int ticket;
+  alignas(8) uint64_t bar;
+};
+
+// Butterfly reduce-scatter over the 32 lanes of a warp: on entry each lane
+// holds C values; on exit v[0] of lane l is the sum over all lanes of value
+// l >> (5 - log2 C).  Fixed pairing order, so the sums are reproducible.
+template <int C, int M>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (C > 1) {
+      constexpr int H = C / 2;
+      const bool up = (lane & M) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
+    }
+    if constexpr (M > 1) ReduceScatter<(C > 1 ? C / 2 : 1), M / 2>::run(v, lane);
+  }
+};
+
+template <typename T, int N>
+__global__ void __launch_bounds__(kThreads, 2)
+scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
+                const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
+                const ScanArgs a) {
+  using SM = BwdSmem<T, N>;
+  constexpr int V = 2 * N;                       // dB and dC values per token
+  constexpr int kRep = 32 / (V < 32 ? V : 32);   // lanes holding the same value
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, s = tid >> 5;
+
+  if (tid == 0) {
+    sm.ticket = (int)atomicAdd(a.ticket, 1u);
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int tk = sm.ticket;
+  const int rev = tk / a.n_tiles;
+  const int tile = tk - rev * a.n_tiles;
+  const int chunk = a.n_chunks - 1 - rev;
+  const int64_t t0 = (int64_t)chunk * kL;
+  const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
+  const int d0 = tile * kTile;
+  const int bx = a.box_x;
+
+  if (tid == 0) {
+    const uint32_t box = (uint32_t)bx * (uint32_t)a.box_y * sizeof(T);
+    const uint32_t bc = (uint32_t)rows * N * sizeof(T);
+    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 4u : 3u) + 2u * bc);
+    tma_load_2d(sm.u, &tm_u, d0, (int)t0, &sm.bar);
+    tma_load_2d(sm.dr, &tm_dr, d0, (int)t0, &sm.bar);
+    tma_load_2d(sm.dout, &tm_dout, d0, (int)t0, &sm.bar);
+    if (a.has_z) tma_load_2d(sm.z, &tm_z, d0, (int)t0, &sm.bar);
+    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + t0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + t0 * N, bc, &sm.bar);
+  }
+  if (tid < kL) sm.pos[tid] = (tid < rows) ? __ldg(a.pos + t0 + tid) : 1;
+
+  const int d = d0 + lane;
+  const bool valid = lane < bx && d < a.D;
+  float A2[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) A2[n] = valid ? __ldg(a.A + (int64_t)d * N + n) * kLog2e : 0.0f;
+  const float bias = (valid && a.dt_bias) ? __ldg(a.dt_bias + d) : 0.0f;
+  const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
+
+  if (!mbar_wait(&sm.bar, 0, a.wait_ns) && lane == 0) atomicOr(a.status, kStatusTmaTimeout);
+  __syncthreads();
+
+  const int tb = s * kK;
+  // ---- 1. per-token values (registers)
+  float dl[kK], sg[kK], uu[kK], g[kK], dzf[kK];
+  int rst = 0;  // bit k: token tb+k starts a sequence (warp-uniform)
+#pragma unroll
+  for (int k = 0; k < kK; ++k) {
+    const int t = tb + k;
+    dl[k] = sg[k] = uu[k] = g[k] = dzf[k] = 0.0f;
+    if (t < rows) {
+      const float r = to_f(sm.dr[t * bx + lane]) + bias;
+      if (a.delta_softplus) {
+        dl[k] = softplusf(r);
+        sg[k] = sigmoidf_fast(r);
+      } else {
+        dl[k] = r;
+        sg[k] = 1.0f;
+      }
+      uu[k] = to_f(sm.u[t * bx + lane]);
+      const float go = to_f(sm.dout[t * bx + lane]);
+      if (a.has_z) {
+        const float zz = to_f(sm.z[t * bx + lane]);
+        const float sz = sigmoidf_fast(zz);
+        g[k] = go * (zz * sz);
+        dzf[k] = go * sz * fmaf(zz, 1.0f - sz, 1.0f);
+      } else {
+        g[k] = go;
+      }
+      if (sm.pos[t] == 0) rst |= 1 << k;
+    }
+  }
+
+  // ---- 2. forward aggregates, scan seeded with the saved chunk state
+  float h[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) h[n] = 0.0f;
+  float sd = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kK; ++k) {
+    const int t = tb + k;
+    if (t >= rows) break;
+    if (rst & (1 << k)) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+      sd = 0.0f;
+    }
+    const float du = dl[k] * uu[k];
+    float Bv[N];
+    lds_row<N>(Bv, sm.B + t * N);
+#pragma unroll
+    for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dl[k] * A2[n]), h[n], du * Bv[n]);
+    sd += dl[k];
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) sm.agg[(s * N + n) * kTile + lane] = h[n];
+  sm.aggSD[s * kTile + lane] = sd;
+  if (lane == 0) sm.aggRS[s] = rst != 0;
+  __syncthreads();
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    if (n % kS != s) continue;
+    float x = valid ? __ldg(a.chunk_states + ((int64_t)chunk * a.D + d) * N + n) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      float* slot = &sm.agg[(j * N + n) * kTile + lane];
+      const float Hj = *slot;
+      *slot = x;
+      const float P = sm.aggRS[j] ? 0.0f : ex2(A2[n] * sm.aggSD[j * kTile + lane]);
+      x = fmaf(P, x, Hj);
+    }
+  }
+  __syncthreads();
+  float hs[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) hs[n] = sm.agg[(s * N + n) * kTile + lane];
+  __syncthreads();
+
+  // ---- 3. reverse aggregates (carry out to the left when nothing comes in)
+  float dh[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) dh[n] = 0.0f;
+#pragma unroll
+  for (int k = kK - 1; k >= 0; --k) {
+    const int t = tb + k;
+    if (t >= rows) continue;
+    float Cv[N];
+    lds_row<N>(Cv, sm.C + t * N);
+    const bool start = rst & (1 << k);
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      const float at = start ? 0.0f : ex2(dl[k] * A2[n]);
+      dh[n] = at * fmaf(Cv[n], g[k], dh[n]);
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) sm.agg[(s * N + n) * kTile + lane] = dh[n];
+  __syncthreads();
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    if (n % kS != s) continue;
+    float y = 0.0f;
+#pragma unroll
+    for (int j = kS - 1; j >= 0; --j) {
+      float* slot = &sm.agg[(j * N + n) * kTile + lane];
+      const float Gj = *slot;
+      *slot = y;
+      const float P = sm.aggRS[j] ? 0.0f : ex2(A2[n] * sm.aggSD[j * kTile + lane]);
+      y = fmaf(P, y, Gj);
+    }
+    sm.tot[n * kTile + lane] = y;
+  }
+  __syncthreads();
+
+  // ---- 4. decoupled look-back towards higher chunks (warp 0)
+  if (s == 0) {
+    int rs_any = 0;
+    float sd_tot = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      rs_any |= sm.aggRS[j];
+      sd_tot += sm.aggSD[j * kTile + lane];
+    }
+    const int64_t base = (int64_t)tile * a.n_chunks;
+    const int64_t slot = base + chunk;
+    const bool publish = (long long)tk != a.drop_ticket;
+    float* my_agg = a.agg + slot * (N * kTile);
+    float* my_inc = a.incl + slot * (N * kTile);
+    if (rs_any) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.tot[n * kTile + lane];
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+    } else {
+#pragma unroll
+      for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.tot[n * kTile + lane];
+      a.agg_sd[slot * kTile + lane] = sd_tot;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagAggregate);
+    }
+    float x[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) x[n] = 0.0f;
+    if (chunk < a.n_chunks - 1) {
+      int j = chunk + 1, found = -1, timed_out = 0;
+      while (j < a.n_chunks) {
+        int f = 0;
+        if (lane == 0) f = wait_flag(a.flags + base + j, a.wait_ns);
+        f = __shfl_sync(0xffffffffu, f, 0);
+        if (f == kFlagInclusive) { found = j; break; }
+        if (f == kFlagNone) { timed_out = 1; break; }
+        ++j;
+      }
+      __syncwarp();  // orders lane 0's acquire before every lane's payload reads
+      if (timed_out && lane == 0) atomicOr(a.status, kStatusLookbackTimeout);
+      int last = j - 1;
+      if (found >= 0) {
+        const float* inc = a.incl + (base + found) * (N * kTile);
+#pragma unroll
+        for (int n = 0; n < N; ++n) x[n] = __ldcg(inc + n * kTile + lane);
+        last = found - 1;
+      }
+      for (int i = last; i > chunk; --i) {
+        const float* ag = a.agg + (base + i) * (N * kTile);
+        const float sdi = __ldcg(a.agg_sd + (base + i) * kTile + lane);
+#pragma unroll
+        for (int n = 0; n < N; ++n) x[n] = fmaf(ex2(A2[n] * sdi), x[n], __ldcg(ag + n * kTile + lane));
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
+    if (!rs_any) {
+#pragma unroll
+      for (int n = 0; n < N; ++n)
+        my_inc[n * kTile + lane] = fmaf(ex2(A2[n] * sd_tot), x[n], sm.tot[n * kTile + lane]);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+    }
+  }
+  __syncthreads();
+
+  // ---- 5. carry entering my last token from the right
+  {
+    int rs_post = 0;
+    float sd_post = 0.0f;
+    for (int j = s + 1; j < kS; ++j) {
+      rs_post |= sm.aggRS[j];
+      sd_post += sm.aggSD[j * kTile + lane];
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      const float E = sm.agg[(s * N + n) * kTile + lane];
+      dh[n] = rs_post ? E : fmaf(ex2(A2[n] * sd_post), sm.rin[n * kTile + lane], E);
+    }
+  }
+  // recompute forward states of my K tokens into shared memory
+  float yk[kK];
+#pragma unroll
+  for (int n = 0; n < N; ++n) h[n] = hs[n];
+#pragma unroll
+  for (int k = 0; k < kK; ++k) {
+    const int t = tb + k;
+    yk[k] = 0.0f;
+    if (t >= rows) continue;
+    if (rst & (1 << k)) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+    }
+    const float du = dl[k] * uu[k];
+    float Bv[N], Cv[N];
+    lds_row<N>(Bv, sm.B + t * N);
+    lds_row<N>(Cv, sm.C + t * N);
+    float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      h[n] = fmaf(ex2(dl[k] * A2[n]), h[n], du * Bv[n]);
+      sm.hist[(k * N + n) * kThreads + tid] = h[n];
+      if (n & 1) y1 = fmaf(Cv[n], h[n], y1); else y0 = fmaf(Cv[n], h[n], y0);
+    }
+    yk[k] = fmaf(Dsk, uu[k], y0 + y1);
+  }
+
+  // reverse walk
+  float dA[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) dA[n] = 0.0f;
+  float sDD = 0.0f, sDB = 0.0f;
+  T* gdu = static_cast<T*>(a.du);
+  T* gddr = static_cast<T*>(a.ddr);
+  T* gdz = static_cast<T*>(a.dz);
+#pragma unroll
+  for (int k = kK - 1; k >= 0; --k) {
+    const int t = tb + k;
+    if (t >= rows) continue;  // warp-uniform
+    float Bv[N], Cv[N];
+    lds_row<N>(Bv, sm.B + t * N);
+    lds_row<N>(Cv, sm.C + t * N);
+    const bool start = rst & (1 << k);
+    const float du = dl[k] * uu[k];
+    float v[V];
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      const float hcur = sm.hist[(k * N + n) * kThreads + tid];
+      const float hprev = k > 0 ? sm.hist[((k - 1) * N + n) * kThreads + tid] : hs[n];
+      dh[n] = fmaf(Cv[n], g[k], dh[n]);  // total gradient w.r.t. h_t
+      const float at = start ? 0.0f : ex2(dl[k] * A2[n]);
+      const float dhq = dh[n] * (at * hprev);
+      dA[n] = fmaf(dl[k], dhq, dA[n]);
+      s2 = fmaf(A2[n], dhq, s2);
+      s1 = fmaf(dh[n], Bv[n], s1);
+      v[n] = valid ? dh[n] * du : 0.0f;
+      v[N + n] = valid ? g[k] * hcur : 0.0f;
+      dh[n] *= at;                       // carry to h_{t-1}
+    }
+    const float gdu_t = fmaf(dl[k], s1, Dsk * g[k]);
+    const float gdl_t = fmaf(uu[k], s1, s2 * kLn2);
+    const float gdr_t = gdl_t * sg[k];
+    sDD = fmaf(g[k], uu[k], sDD);
+    sDB += gdr_t;
+    const int64_t off = (t0 + t) * a.D + d;
+    if (valid) {
+      gdu[off] = from_f<T>(gdu_t);
+      gddr[off] = from_f<T>(gdr_t);
+      if (gdz) gdz[off] = from_f<T>(dzf[k] * yk[k]);
+    }
+    ReduceScatter<V, 16>::run(v, lane);
+    if ((lane & (kRep - 1)) == 0)
+      a.part_dBC[((int64_t)tile * a.T + t0 + t) * V + lane / kRep] = v[0];
+  }
+
+  // ---- 6. fixed-order CTA reduction of dA, dDskip, d_dt_bias partials
+  __syncthreads();
+#pragma unroll
+  for (int n = 0; n < N; ++n) sm.agg[(s * N + n) * kTile + lane] = dA[n];
+  sm.redD[s * kTile + lane] = sDD;
+  sm.redB[s * kTile + lane] = sDB;
+  __syncthreads();
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    if (n % kS != s) continue;
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) acc += sm.agg[(j * N + n) * kTile + lane];
+    if (valid) a.part_dA[((int64_t)chunk * a.D + d) * N + n] = acc;
+  }
+  if (s == 0 && valid) {
+    float accD = 0.0f, accB = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      accD += sm.redD[j * kTile + lane];
+      accB += sm.redB[j * kTile + lane];
+    }
+    a.part_dD[(int64_t)chunk * a.D + d] = accD;
+    a.part_dbias[(int64_t)chunk * a.D + d] = accB;
+  }
+}
+
+// dB[t][n] = sum over tiles of part[tile][t][n]; dC[t][n] likewise from
+// part[tile][t][N + n].  One thread per output, tiles summed in order.
+__global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restrict__ part,
+                                                           int n_tiles, int64_t T, int N,
+                                                           float* __restrict__ dB,
+                                                           float* __restrict__ dC) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t M = T * 2 * N;
+  if (i >= M) return;
+  float acc = 0.0f;
+  for (int k = 0; k < n_tiles; ++k) acc += __ldcs(part + (int64_t)k * M + i);
+  const int64_t t = i / (2 * N);
+  const int j = (int)(i - t * 2 * N);
+  if (j < N) dB[t * N + j] = acc; else dC[t * N + (j - N)] = acc;
+}
+
+template <typename T, int N>
+cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, cudaStream_t st) {
+  const size_t smem = sizeof(BwdSmem<T, N>);
+  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
+  scan_bwd_kernel<T, N><<<(unsigned)items, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, cudaStream_t st) {
+  if (a.N == 16) return launch_n<T, 16>(a, tm_u, tm_dr, tm_z, tm_dout, st);
+  if (a.N == 8) return launch_n<T, 8>(a, tm_u, tm_dr, tm_z, tm_dout, st);
+  if constexpr (sizeof(T) == 4) {
+    if (a.N == 4) return launch_n<T, 4>(a, tm_u, tm_dr, tm_z, tm_dout, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
+                            const CUtensorMap& tm_dr, const CUtensorMap& tm_z,
+                            const CUtensorMap& tm_dout, float* dA, float* dB, float* dC,
+                            float* dDskip, float* d_dt_bias, cudaStream_t st) {
+  const int64_t DN = (int64_t)a.D * a.N;
+  if (a.T <= 0) {
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * DN, st);
+    if (e == cudaSuccess && dDskip) e = cudaMemsetAsync(dDskip, 0, sizeof(float) * a.D, st);
+    if (e == cudaSuccess && d_dt_bias) e = cudaMemsetAsync(d_dt_bias, 0, sizeof(float) * a.D, st);
+    return e;
+  }
+  cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, st)
+                                : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, st);
+  if (e != cudaSuccess) return e;
+  const int64_t M = a.T * 2 * a.N;
+  sum_tiles_bc_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(a.part_dBC, a.n_tiles, a.T, a.N,
+                                                                   dB, dC);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_sum_rows(a.part_dA, a.n_chunks, DN, DN, dA, st);
+  if (e == cudaSuccess && dDskip) e = launch_sum_rows(a.part_dD, a.n_chunks, a.D, a.D, dDskip, st);
+  if (e == cudaSuccess && d_dt_bias)
+    e = launch_sum_rows(a.part_dbias, a.n_chunks, a.D, a.D, d_dt_bias, st);
+  return e;
+}
+
+}  // namespace vssm

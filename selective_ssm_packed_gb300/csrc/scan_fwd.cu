@@ -1,0 +1,310 @@
+// scan_fwd.cu -- packed selective scan, forward (sm_103a).
+//
+// Work item = (chunk of kFwdChunk = 128 tokens) x (tile of kTile = 32 channels).
+// A CTA of 256 threads = 8 warps; warp s owns sub-chunk s (K = 16 tokens) and
+// lane l owns channel d0 + l with all N states in registers.
+//
+//   1. TMA: u, delta_raw, z tiles (128 x 32) with 2-D tensor maps, B and C
+//      rows (128 x N, contiguous) with 1-D bulk copies, one mbarrier.
+//   2. delta = softplus(delta_raw + dt_bias) once per (token, channel) -> smem.
+//   3. Pass 1: every thread scans its K tokens from h = 0 and records the
+//      sub-chunk aggregate: H (the state reached) and the sum of delta since
+//      the last sequence start; the product of the transition factors over the
+//      sub-chunk is then exp2(A*log2e * sum) or exactly 0 if a sequence starts
+//      inside it (the article's SSM_pack zeroes the factor at a start).
+//   4. Exclusive scan of the 8 sub-chunk aggregates per (channel, state) in
+//      shared memory.
+//   5. Decoupled look-back across chunks (warp 0): publish the chunk aggregate
+//      (or, if a sequence starts inside the chunk, the inclusive state at once),
+//      walk back over predecessors' flags to the nearest inclusive state, then
+//      re-apply the aggregates FORWARD from there in chunk order, which gives
+//      the same floating-point result whatever the timing (bitwise repeatable).
+//      Work items take chunk ids from an atomic ticket, so a CTA only ever waits
+//      on items already running; every wait is time-bounded and a timeout is
+//      reported through the status word instead of hanging.
+//   6. Pass 2: each thread starts from its exact state, recomputes its K tokens
+//      and writes out = (C.h + Dskip u) * SiLU(z); states at multiples of 32
+//      tokens go to chunk_states for the backward pass.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace vssm {
+
+namespace {
+
+constexpr int kL = kFwdChunk;   // 128
+constexpr int kS = 8;           // sub-chunks (warps)
+constexpr int kK = kL / kS;     // 16 tokens per thread
+constexpr int kThreads = kS * 32;
+
+template <typename T, int N>
+struct FwdSmem {
+  alignas(128) T u[kL * kTile];
+  alignas(128) T dr[kL * kTile];
+  alignas(128) T z[kL * kTile];
+  alignas(128) T B[kL * N];
+  alignas(128) T C[kL * N];
+  alignas(16) float dlt[kL * kTile];
+  alignas(16) float aggH[kS * N * kTile];
+  float totH[N * kTile];
+  float hin[N * kTile];
+  float aggSD[kS * kTile];
+  int pos[kL];
+  int aggRS[kS];
+  int ticket;
+  alignas(8) uint64_t bar;
+};
+
+template <typename T, int N>
+__global__ void __launch_bounds__(kThreads, 2)
+scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
+                const __grid_constant__ CUtensorMap tm_z, const ScanArgs a) {
+  using SM = FwdSmem<T, N>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, s = tid >> 5;
+
+  if (tid == 0) {
+    sm.ticket = (int)atomicAdd(a.ticket, 1u);
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int tk = sm.ticket;
+  const int chunk = tk / a.n_tiles;
+  const int tile = tk - chunk * a.n_tiles;
+  const int64_t t0 = (int64_t)chunk * kL;
+  const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
+  const int d0 = tile * kTile;
+  const int bx = a.box_x;
+
+  if (tid == 0) {
+    const uint32_t box = (uint32_t)bx * (uint32_t)a.box_y * sizeof(T);
+    const uint32_t bc = (uint32_t)rows * N * sizeof(T);
+    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 3u : 2u) + 2u * bc);
+    tma_load_2d(sm.u, &tm_u, d0, (int)t0, &sm.bar);
+    tma_load_2d(sm.dr, &tm_dr, d0, (int)t0, &sm.bar);
+    if (a.has_z) tma_load_2d(sm.z, &tm_z, d0, (int)t0, &sm.bar);
+    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + t0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + t0 * N, bc, &sm.bar);
+  }
+  for (int i = tid; i < kL; i += kThreads) sm.pos[i] = (i < rows) ? __ldg(a.pos + t0 + i) : 1;
+
+  const int d = d0 + lane;
+  const bool valid = lane < bx && d < a.D;
+  float A2[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) A2[n] = valid ? __ldg(a.A + (int64_t)d * N + n) * kLog2e : 0.0f;
+  const float bias = (valid && a.dt_bias) ? __ldg(a.dt_bias + d) : 0.0f;
+  const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
+
+  if (!mbar_wait(&sm.bar, 0, a.wait_ns) && lane == 0) atomicOr(a.status, kStatusTmaTimeout);
+  __syncthreads();
+
+  const int tb = s * kK;  // first token (within the chunk) of this thread
+  // ---- step 2: delta for my tokens
+#pragma unroll
+  for (int k = 0; k < kK; ++k) {
+    const int t = tb + k;
+    const float r = to_f(sm.dr[t * bx + lane]) + bias;
+    sm.dlt[t * kTile + lane] = a.delta_softplus ? softplusf(r) : r;
+  }
+
+  // ---- step 3: pass 1, sub-chunk aggregate from h = 0
+  float h[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) h[n] = 0.0f;
+  float sd = 0.0f;
+  int rs = 0;
+#pragma unroll
+  for (int k = 0; k < kK; ++k) {
+    const int t = tb + k;
+    if (t >= rows) break;
+    if (sm.pos[t] == 0) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+      sd = 0.0f;
+      rs = 1;
+    }
+    const float dl = sm.dlt[t * kTile + lane];
+    const float du = dl * to_f(sm.u[t * bx + lane]);
+    float Bv[N];
+    lds_row<N>(Bv, sm.B + t * N);
+#pragma unroll
+    for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dl * A2[n]), h[n], du * Bv[n]);
+    sd += dl;
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) sm.aggH[(s * N + n) * kTile + lane] = h[n];
+  sm.aggSD[s * kTile + lane] = sd;
+  if (lane == 0) sm.aggRS[s] = rs;
+  __syncthreads();
+
+  // ---- step 4: exclusive scan over sub-chunks; chain (lane, n) with n % kS == s
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    if (n % kS != s) continue;
+    float x = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      float* slot = &sm.aggH[(j * N + n) * kTile + lane];
+      const float Hj = *slot;
+      *slot = x;
+      const float P = sm.aggRS[j] ? 0.0f : ex2(A2[n] * sm.aggSD[j * kTile + lane]);
+      x = fmaf(P, x, Hj);
+    }
+    sm.totH[n * kTile + lane] = x;
+  }
+  __syncthreads();
+
+  // ---- step 5: decoupled look-back (warp 0)
+  if (s == 0) {
+    int rs_any = 0;
+    float sd_tot = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      rs_any |= sm.aggRS[j];
+      sd_tot += sm.aggSD[j * kTile + lane];
+    }
+    const int64_t slot = (int64_t)tile * a.n_chunks + chunk;
+    const bool publish = (long long)tk != a.drop_ticket;
+    float* my_agg = a.agg + slot * (N * kTile);
+    float* my_inc = a.incl + slot * (N * kTile);
+    if (rs_any) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.totH[n * kTile + lane];
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+    } else {
+#pragma unroll
+      for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.totH[n * kTile + lane];
+      a.agg_sd[slot * kTile + lane] = sd_tot;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagAggregate);
+    }
+
+    float x[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) x[n] = 0.0f;
+    if (chunk > 0 && sm.pos[0] != 0) {
+      const int64_t base = (int64_t)tile * a.n_chunks;
+      int j = chunk - 1, found = -1, timed_out = 0;
+      while (j >= 0) {
+        int f = 0;
+        if (lane == 0) f = wait_flag(a.flags + base + j, a.wait_ns);
+        f = __shfl_sync(0xffffffffu, f, 0);
+        if (f == kFlagInclusive) { found = j; break; }
+        if (f == kFlagNone) { timed_out = 1; break; }
+        --j;
+      }
+      __syncwarp();  // orders lane 0's acquire before every lane's payload reads
+      if (timed_out && lane == 0) atomicOr(a.status, kStatusLookbackTimeout);
+      int first = j + 1;
+      if (found >= 0) {
+        const float* inc = a.incl + (base + found) * (N * kTile);
+#pragma unroll
+        for (int n = 0; n < N; ++n) x[n] = __ldcg(inc + n * kTile + lane);
+        first = found + 1;
+      }
+      for (int i = first; i < chunk; ++i) {
+        const float* ag = a.agg + (base + i) * (N * kTile);
+        const float sdi = __ldcg(a.agg_sd + (base + i) * kTile + lane);
+#pragma unroll
+        for (int n = 0; n < N; ++n) x[n] = fmaf(ex2(A2[n] * sdi), x[n], __ldcg(ag + n * kTile + lane));
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = x[n];
+    if (!rs_any) {
+#pragma unroll
+      for (int n = 0; n < N; ++n)
+        my_inc[n * kTile + lane] = fmaf(ex2(A2[n] * sd_tot), x[n], sm.totH[n * kTile + lane]);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+    }
+  }
+  __syncthreads();
+
+  // ---- step 6: exact start state, pass 2
+  int rs_pre = 0;
+  float sd_pre = 0.0f;
+  for (int j = 0; j < s; ++j) {
+    rs_pre |= sm.aggRS[j];
+    sd_pre += sm.aggSD[j * kTile + lane];
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    const float E = sm.aggH[(s * N + n) * kTile + lane];
+    h[n] = rs_pre ? E : fmaf(ex2(A2[n] * sd_pre), sm.hin[n * kTile + lane], E);
+  }
+  const int64_t ts = t0 + tb;
+  if (a.chunk_states && valid && ts < a.T && (ts % kStateChunk) == 0) {
+    float* cs = a.chunk_states + ((ts / kStateChunk) * a.D + d) * N;
+#pragma unroll
+    for (int n = 0; n < N; n += 4)
+      *reinterpret_cast<float4*>(cs + n) = make_float4(h[n], h[n + 1], h[n + 2], h[n + 3]);
+  }
+
+  T* out = static_cast<T*>(a.out);
+#pragma unroll
+  for (int k = 0; k < kK; ++k) {
+    const int t = tb + k;
+    if (t >= rows) break;
+    if (sm.pos[t] == 0) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+    }
+    const float dl = sm.dlt[t * kTile + lane];
+    const float uu = to_f(sm.u[t * bx + lane]);
+    const float du = dl * uu;
+    float Bv[N], Cv[N];
+    lds_row<N>(Bv, sm.B + t * N);
+    lds_row<N>(Cv, sm.C + t * N);
+    float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      h[n] = fmaf(ex2(dl * A2[n]), h[n], du * Bv[n]);
+      if (n & 1) y1 = fmaf(Cv[n], h[n], y1); else y0 = fmaf(Cv[n], h[n], y0);
+    }
+    float y = fmaf(Dsk, uu, y0 + y1);
+    if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane]));
+    if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
+  }
+}
+
+template <typename T, int N>
+cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, cudaStream_t st) {
+  const size_t smem = sizeof(FwdSmem<T, N>);
+  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<T, N>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
+  scan_fwd_kernel<T, N><<<(unsigned)items, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, cudaStream_t st) {
+  if (a.N == 16) return launch_n<T, 16>(a, tm_u, tm_dr, tm_z, st);
+  if (a.N == 8) return launch_n<T, 8>(a, tm_u, tm_dr, tm_z, st);
+  if constexpr (sizeof(T) == 4) {
+    if (a.N == 4) return launch_n<T, 4>(a, tm_u, tm_dr, tm_z, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
+                            const CUtensorMap& tm_dr, const CUtensorMap& tm_z, cudaStream_t st) {
+  if (a.T <= 0) return cudaSuccess;
+  return io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, st)
+                       : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, st);
+}
+
+}  // namespace vssm

@@ -169,11 +169,21 @@ def make(name: str, backward: bool | None = None, scan_input: bool = True) -> di
     return dict(workload=wl, lengths=lengths, cu_seqlens=cu, T=T, **vals)
 
 
+ACTIVATIONS = ("x", "u", "delta_raw", "z", "B", "C", "dout")
+
+
 def round_to(a: np.ndarray, dtype: str) -> np.ndarray:
-    """Values exactly as a device buffer of `dtype` holds them, as float64
-    (bf16 uses round-to-nearest-even, the conversion torch applies)."""
+    """Values exactly as a device buffer of `dtype` holds them, returned as
+    float32 (every bf16 value is exact in float32); bf16 uses
+    round-to-nearest-even, the conversion torch applies."""
     if dtype == "f32":
-        return np.asarray(a, dtype=np.float32).astype(np.float64)
+        return np.ascontiguousarray(a, dtype=np.float32)
     import torch
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16) \
-        .to(torch.float64).numpy()
+        .to(torch.float32).numpy()
+
+
+def rounded(values: dict, dtype: str) -> dict:
+    """Round the activations of a draw_values() dict to the I/O dtype; the
+    parameters stay float32 (they are float32 on the device too)."""
+    return {k: (round_to(v, dtype) if k in ACTIVATIONS else v) for k, v in values.items()}

@@ -1,0 +1,374 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Tolerances (per output tensor, from the scan's arithmetic: fp32 state and
+accumulation, MUFU ex2 with ~2^-22 relative error, bf16 rounding once at the
+store):  fp32 I/O  max|gpu - ref| <= 2e-4 * max|ref|;  bf16 I/O  <= 1e-2 *
+max|ref|.  Integer outputs (position indices, status codes) are compared
+exactly, and the packing invariants (a sequence's outputs do not depend on its
+neighbours; repeated runs agree) bit for bit.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_ssm_packed_gb300 as vs
+from selective_ssm_packed_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TOL = {"f32": 2e-4, "bf16": 1e-2}
+TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from selective_ssm_packed_gb300 import build
+    build.build()
+    oracle.build()
+    binding.lib()
+
+
+def dev(a, dtype="f32"):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda().to(TDT[dtype])
+
+
+def f32(a):
+    return dev(a, "f32")
+
+
+def host(t):
+    return t.double().cpu().numpy()
+
+
+def assert_close(name, got, ref, tol):
+    got = host(got) if isinstance(got, torch.Tensor) else np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    if ref.size == 0:
+        return
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    err = float(np.max(np.abs(got - ref)))
+    scale = float(np.max(np.abs(ref)))
+    assert err <= tol * max(scale, 1e-30), f"{name}: max|err| {err:.3e} > {tol:g} * max|ref| {scale:.3e}"
+
+
+def rand_case(lengths, D, N, dtype, seed, W=4):
+    cu = workloads.cu_seqlens_from_lengths(lengths)
+    T = int(cu[-1])
+    r = workloads.rounded(workloads.draw_values(T, D, N, W, seed, scan_input=False), dtype)
+    return cu, T, r
+
+
+def run_chain(cu_np, T, r, dtype, with_bwd=True, z=True, skip=True, bias=True, softplus=True):
+    """conv fwd -> scan fwd (-> scan bwd -> conv bwd) through the C ABI."""
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    x = dev(r["x"], dtype)
+    u = vs.varlen_conv1d_fwd(x, f32(r["conv_w"]), f32(r["conv_b"]), cu, pos)
+    args = dict(u=u, delta_raw=dev(r["delta_raw"], dtype), A=f32(r["A"]), B=dev(r["B"], dtype),
+                C=dev(r["C"], dtype), Dskip=f32(r["Dskip"]) if skip else None,
+                z=dev(r["z"], dtype) if z else None, dt_bias=f32(r["dt_bias"]) if bias else None)
+    out, states = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos,
+                                               delta_softplus=softplus)
+    res = dict(pos=pos, u=u, out=out, states=states)
+    if with_bwd:
+        g = vs.varlen_selective_scan_bwd(**args, dout=dev(r["dout"], dtype), cu_seqlens=cu,
+                                         chunk_states=states, position_indices=pos,
+                                         delta_softplus=softplus)
+        dx, dw, db = vs.varlen_conv1d_bwd(x, f32(r["conv_w"]), f32(r["conv_b"]), g["du"], cu, pos)
+        res.update(g)
+        res.update(dx=dx, dweight=dw, dbias=db)
+    torch.cuda.synchronize()
+    return res
+
+
+def check_chain(cu_np, r, res, dtype, with_bwd=True, z=True, skip=True, bias=True, softplus=True,
+                channels=None):
+    """Compare a run_chain result with the oracle, optionally on a channel subset
+    (every channel is an independent computation, so a column subset of the
+    inputs gives exactly those columns of every per-channel output)."""
+    tol = TOL[dtype]
+    idx = np.arange(r["A"].shape[0]) if channels is None else np.asarray(channels)
+    col = lambda a: a[:, idx]  # noqa: E731
+    u_gpu = host(res["u"])
+    assert_close("u", col(u_gpu),
+                 oracle.conv1d_fwd_threaded(col(r["x"]), r["conv_w"][idx], r["conv_b"][idx], cu_np), tol)
+    sargs = [col(u_gpu), col(r["delta_raw"]), r["A"][idx], r["B"], r["C"],
+             r["Dskip"][idx] if skip else None, col(r["z"]) if z else None,
+             r["dt_bias"][idx] if bias else None]
+    assert_close("out", col(host(res["out"])),
+                 oracle.scan_fwd_threaded(*sargs, cu_np, delta_softplus=softplus), tol)
+    if not with_bwd:
+        return
+    g = oracle.scan_bwd_threaded(*sargs, col(r["dout"]), cu_np, delta_softplus=softplus)
+    for k in ("du", "ddelta_raw", "dz"):
+        if g[k] is not None:
+            assert_close(k, col(host(res[k])), g[k], tol)
+    assert_close("dA", host(res["dA"])[idx], g["dA"], tol)
+    if skip:
+        assert_close("dDskip", host(res["dDskip"])[idx], g["dDskip"], tol)
+    if bias:
+        assert_close("d_dt_bias", host(res["d_dt_bias"])[idx], g["d_dt_bias"], tol)
+    if channels is None:
+        assert_close("dB", res["dB"], g["dB"], tol)
+        assert_close("dC", res["dC"], g["dC"], tol)
+    dx, dw, db = oracle.conv1d_bwd_threaded(col(r["x"]), r["conv_w"][idx], r["conv_b"][idx],
+                                            col(host(res["du"])), cu_np)
+    assert_close("dx", col(host(res["dx"])), dx, tol)
+    assert_close("dweight", host(res["dweight"])[idx], dw, tol)
+    assert_close("dbias", host(res["dbias"])[idx], db, tol)
+
+
+# ------------------------------------------------------------------ position indices
+
+def test_position_indices_golden_example():
+    with open(os.path.join(GOLDEN, "position_indices_4_2_3_7.txt")) as f:
+        rows = [list(map(int, ln.split())) for ln in f if ln.strip() and not ln.startswith("#")]
+    cu = torch.tensor(rows[1], dtype=torch.int32, device="cuda")
+    pos = vs.varlen_position_indices(cu, 16)
+    assert pos.cpu().tolist() == rows[2]
+
+
+def test_position_indices_random_with_empty_sequences():
+    rng = np.random.default_rng(3)
+    lengths = [int(v) for v in rng.integers(0, 300, size=2000)]
+    lengths[5:15] = [0] * 10
+    cu_np = workloads.cu_seqlens_from_lengths(lengths)
+    T = int(cu_np[-1])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pos = vs.varlen_position_indices(torch.from_numpy(cu_np).cuda(), T, status=status)
+    assert np.array_equal(pos.cpu().numpy(), oracle.position_indices(cu_np))
+    assert binding.status_code(int(status.item())) == 0
+
+
+@pytest.mark.parametrize("cu", [[1, 4, 6], [0, 4, 3, 6], [0, 2, 5]])
+def test_position_indices_reports_malformed_cu_seqlens(cu):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vs.varlen_position_indices(torch.tensor(cu, dtype=torch.int32, device="cuda"), 6, status=status)
+    assert binding.status_code(int(status.item())) == -16
+
+
+def test_malformed_cu_seqlens_reach_the_call_status():
+    # the scan call builds its own position indices and reports through the workspace
+    cu = torch.tensor([0, 5, 3, 16], dtype=torch.int32, device="cuda")
+    T, D, N = 16, 8, 4
+    u = torch.randn(T, D, device="cuda")
+    ws = torch.empty(binding.scan_fwd_workspace_size(T, D, N), dtype=torch.uint8, device="cuda")
+    vs.varlen_selective_scan_fwd(u, u, -torch.ones(D, N, device="cuda"), torch.randn(T, N, device="cuda"),
+                                 torch.randn(T, N, device="cuda"), None, None, None, cu, workspace=ws)
+    assert binding.read_status(ws) == -16
+
+
+# ------------------------------------------------------------------ small exact-parity cases
+
+def test_tiny_worked_example_fwd_bwd():
+    w = workloads.make("tiny")
+    r = workloads.rounded(w, "f32")
+    res = run_chain(w["cu_seqlens"], w["T"], r, "f32")
+    assert res["pos"].cpu().tolist() == [0, 1, 2, 3, 0, 1, 0, 1, 2, 0, 1, 2, 3, 4, 5, 6]
+    check_chain(w["cu_seqlens"], r, res, "f32")
+
+
+CASES = [
+    # lengths, D, N, dtype
+    ([1, 1, 2, 3, 700, 1, 40, 129, 5], 40, 4, "f32"),
+    ([300, 0, 1, 257, 0, 0, 33, 128, 2], 72, 8, "f32"),
+    ([1000, 31, 1, 64, 200], 48, 16, "f32"),
+    ([513, 1, 7, 90, 300, 1], 64, 8, "bf16"),
+    ([129, 1, 1, 1, 640, 77], 104, 16, "bf16"),
+]
+
+
+@pytest.mark.parametrize("lengths,D,N,dtype", CASES)
+def test_ragged_packs_fwd_bwd(lengths, D, N, dtype):
+    cu, T, r = rand_case(lengths, D, N, dtype, seed=sum(lengths) + D + N)
+    res = run_chain(cu, T, r, dtype)
+    check_chain(cu, r, res, dtype)
+
+
+@pytest.mark.parametrize("flags", [dict(z=False), dict(skip=False), dict(bias=False),
+                                   dict(softplus=False), dict(z=False, skip=False, bias=False)])
+def test_optional_inputs(flags):
+    cu, T, r = rand_case([100, 3, 260, 1], 40, 8, "f32", seed=11)
+    if flags.get("softplus") is False:
+        r["delta_raw"] = np.abs(r["delta_raw"]) * np.float32(0.1)   # a positive step without softplus
+    res = run_chain(cu, T, r, "f32", **flags)
+    check_chain(cu, r, res, "f32", **flags)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3])
+def test_conv_widths(W):
+    cu, T, r = rand_case([5, 1, 2, 90, 3], 24, 4, "f32", seed=W, W=W)
+    cu_t = torch.from_numpy(cu).cuda()
+    x = f32(r["x"])
+    u = vs.varlen_conv1d_fwd(x, f32(r["conv_w"]), f32(r["conv_b"]), cu_t)
+    du = f32(r["dout"])
+    dx, dw, db = vs.varlen_conv1d_bwd(x, f32(r["conv_w"]), f32(r["conv_b"]), du, cu_t)
+    assert_close("u", u, oracle.conv1d_fwd(r["x"], r["conv_w"], r["conv_b"], cu), 2e-4)
+    rdx, rdw, rdb = oracle.conv1d_bwd(r["x"], r["conv_w"], r["conv_b"], r["dout"], cu)
+    assert_close("dx", dx, rdx, 2e-4)
+    assert_close("dweight", dw, rdw, 2e-4)
+    assert_close("dbias", db, rdb, 2e-4)
+
+
+def test_zero_tokens_is_a_noop_that_zeroes_parameter_grads():
+    D, N = 8, 4
+    cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e = torch.empty(0, D, device="cuda")
+    eb = torch.empty(0, N, device="cuda")
+    A = -torch.ones(D, N, device="cuda")
+    out, st = vs.varlen_selective_scan_fwd(e, e, A, eb, eb, torch.ones(D, device="cuda"), e,
+                                           torch.zeros(D, device="cuda"), cu)
+    g = vs.varlen_selective_scan_bwd(e, e, A, eb, eb, torch.ones(D, device="cuda"), e,
+                                     torch.zeros(D, device="cuda"), e, cu, st,
+                                     grads=dict(dA=torch.full((D, N), 7.0, device="cuda"),
+                                                dDskip=torch.full((D,), 7.0, device="cuda"),
+                                                d_dt_bias=torch.full((D,), 7.0, device="cuda")))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(g["dA"]) == 0 and torch.count_nonzero(g["dDskip"]) == 0
+    assert torch.count_nonzero(g["d_dt_bias"]) == 0
+
+
+# ------------------------------------------------------------------ packing invariants on the GPU
+
+def _per_token_outputs(res):
+    return {k: res[k].clone() for k in ("u", "out", "du", "ddelta_raw", "dz", "dB", "dC", "dx")}
+
+
+def test_sequences_do_not_interact_bitwise():
+    lengths = [300, 1, 129, 4, 600, 2]
+    cu, T, r = rand_case(lengths, 64, 16, "bf16", seed=21)
+    base = _per_token_outputs(run_chain(cu, T, r, "bf16"))
+    victim = 2
+    r2 = {k: v.copy() for k, v in r.items()}
+    sl = slice(int(cu[victim]), int(cu[victim + 1]))
+    for k in ("x", "delta_raw", "z", "B", "C", "dout"):
+        r2[k][sl] = workloads.round_to(r2[k][sl] * -1.5 + 0.25, "bf16")
+    pert = _per_token_outputs(run_chain(cu, T, r2, "bf16"))
+    for k in base:
+        for s in range(len(lengths)):
+            a, b = int(cu[s]), int(cu[s + 1])
+            same = torch.equal(base[k][a:b], pert[k][a:b])
+            assert same == (s != victim), (k, s)
+
+
+def test_repeated_runs_are_bitwise_identical():
+    cu, T, r = rand_case([2000, 1, 3, 1500, 600], 256, 16, "bf16", seed=5)
+    first = run_chain(cu, T, r, "bf16")
+    keys = ("u", "out", "du", "ddelta_raw", "dz", "dA", "dB", "dC", "dDskip", "d_dt_bias", "dx",
+            "dweight", "dbias", "states")
+    ref = {k: first[k].clone() for k in keys}
+    for _ in range(4):
+        again = run_chain(cu, T, r, "bf16")
+        for k in keys:
+            assert torch.equal(again[k], ref[k]), k
+
+
+def test_right_padded_layout_matches_packed_on_real_tokens():
+    lengths = [700, 1, 5, 300, 1100]
+    cu, T, r = rand_case(lengths, 64, 16, "f32", seed=8)
+    packed = run_chain(cu, T, r, "f32")
+    cu_pad, idx = workloads.padded_layout(lengths)
+    Tp = int(cu_pad[-1])
+    rp = dict(r)
+    rng = np.random.default_rng(99)
+    for k in ("x", "delta_raw", "z", "B", "C", "dout"):
+        arr = rng.standard_normal((Tp,) + r[k].shape[1:]).astype(np.float32) * 3
+        arr[idx] = r[k]
+        if k == "dout":
+            arr[np.setdiff1d(np.arange(Tp), idx)] = 0.0   # padding carries no loss
+        rp[k] = workloads.round_to(arr, "f32")
+    padded = run_chain(cu_pad, Tp, rp, "f32")
+    ii = torch.from_numpy(idx).cuda()
+    assert torch.equal(padded["u"][ii], packed["u"])          # conv is per token: exact
+    for k in ("out", "du", "ddelta_raw", "dz", "dB", "dC", "dx"):
+        assert_close(k, padded[k][ii], host(packed[k]), 2e-4)
+    for k in ("dA", "dDskip", "d_dt_bias", "dweight", "dbias"):
+        assert_close(k, padded[k], host(packed[k]), 2e-4)
+
+
+# ------------------------------------------------------------------ failure reporting
+
+def test_lookback_wait_timeout_is_reported_not_hung():
+    """A work item that never publishes its flag makes the next one's wait run
+    out (after 1 ms); the call still completes and reports the timeout."""
+    cu_np = np.array([0, 1024], dtype=np.int32)
+    T, D, N = 1024, 32, 8
+    rng = np.random.default_rng(1)
+    u = f32(rng.standard_normal((T, D)))
+    B = f32(rng.standard_normal((T, N)))
+    A = -torch.ones(D, N, device="cuda")
+    cu = torch.from_numpy(cu_np).cuda()
+    ws = torch.empty(binding.scan_fwd_workspace_size(T, D, N), dtype=torch.uint8, device="cuda")
+    try:
+        binding.debug_set(binding.VSSM_DBG_WAIT_NS, 1_000_000)
+        binding.debug_set(binding.VSSM_DBG_DROP_FLAG, 3)
+        vs.varlen_selective_scan_fwd(u, u, A, B, B, None, None, None, cu, workspace=ws)
+        assert binding.read_status(ws) == -17
+        wsb = torch.empty(binding.scan_bwd_workspace_size(T, D, N), dtype=torch.uint8, device="cuda")
+        binding.debug_set(binding.VSSM_DBG_DROP_FLAG, -1)
+        out, st = vs.varlen_selective_scan_fwd(u, u, A, B, B, None, None, None, cu)
+        binding.debug_set(binding.VSSM_DBG_DROP_FLAG, 5)
+        vs.varlen_selective_scan_bwd(u, u, A, B, B, None, None, None, u, cu, st, workspace=wsb)
+        assert binding.read_status(wsb) == -17
+    finally:
+        binding.debug_set(binding.VSSM_DBG_DROP_FLAG, -1)
+        binding.debug_set(binding.VSSM_DBG_WAIT_NS, 1_000_000_000)
+    # and the context is still healthy
+    vs.varlen_selective_scan_fwd(u, u, A, B, B, None, None, None, cu, workspace=ws)
+    assert binding.read_status(ws) == 0
+
+
+# ------------------------------------------------------------------ the named workloads
+
+def test_workload_m130m_forward_full_parity():
+    w = workloads.make("m130m", backward=False, scan_input=False)
+    r = workloads.rounded(w, "f32")
+    res = run_chain(w["cu_seqlens"], w["T"], r, "f32", with_bwd=False)
+    check_chain(w["cu_seqlens"], r, res, "f32", with_bwd=False)
+
+
+def _big_case(name):
+    w = workloads.make(name, backward=True, scan_input=False)
+    r = workloads.rounded(w, "bf16")
+    for k in workloads.ACTIVATIONS:
+        w.pop(k, None)
+    return w, r
+
+
+def _sampled_checks(w, r, res, seq_pick):
+    cu = w["cu_seqlens"]
+    D = r["A"].shape[0]
+    rng = np.random.default_rng(7)
+    chans = np.unique(np.concatenate([np.arange(0, 8), np.arange(D - 8, D), rng.choice(D, 32, replace=False)]))
+    check_chain(cu, r, res, "bf16", channels=chans)
+    # dB / dC sum over every channel: check whole sequences, run alone through the oracle
+    u_gpu = res["u"]
+    for s in seq_pick:
+        a, b = int(cu[s]), int(cu[s + 1])
+        sl = slice(a, b)
+        one = np.array([0, b - a], dtype=np.int32)
+        g = oracle.scan_bwd_threaded(host(u_gpu[a:b]), r["delta_raw"][sl], r["A"], r["B"][sl], r["C"][sl],
+                                     r["Dskip"], r["z"][sl], r["dt_bias"], r["dout"][sl], one)
+        assert_close(f"dB[seq {s}]", res["dB"][a:b], g["dB"], 1e-2)
+        assert_close(f"dC[seq {s}]", res["dC"][a:b], g["dC"], 1e-2)
+
+
+def test_workload_m14b_fwd_bwd_sampled_parity():
+    w, r = _big_case("m14b")
+    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16")
+    lengths = np.diff(w["cu_seqlens"])
+    picks = [int(np.argmax(lengths)), int(np.argmin(lengths)), len(lengths) // 2]
+    _sampled_checks(w, r, res, picks)
+
+
+def test_workload_longtail_fwd_bwd_sampled_parity():
+    w, r = _big_case("longtail")
+    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16")
+    lengths = np.diff(w["cu_seqlens"])
+    picks = [int(np.argmax(lengths)), int(np.argmin(lengths)), int(np.argmax(lengths < 9))]
+    _sampled_checks(w, r, res, picks)
