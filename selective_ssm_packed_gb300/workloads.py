@@ -17,6 +17,7 @@ log-normal mixes instead of a real corpus):
   m14b_fwd   8 packs x 4096, LogN(ln 800, 1) clipped [32,4096],
              D=4096, N=16, bf16, seed 2, fwd
   m14b       as m14b_fwd, seed 3, fwd+bwd
+  m14b_small the first 2 packs of m14b (8192 tokens), for profiler captures
   longtail   2 packs x 65536, each: 2000 lengths U{1..8}, one 32768-token
              sequence, LogN(ln 800, 1) bulk filling the rest; order shuffled;
              D=4096, N=16, bf16, seed 4, fwd+bwd
@@ -57,6 +58,8 @@ WORKLOADS = {
                          "Mamba-1.4B layer: 8 packs x 4096 tokens, lengths LogN(median 800), D=4096, N=16, bf16"),
     "m14b": Workload("m14b", 4096, 16, 4, "bf16", 3, True,
                      "Mamba-1.4B layer: 8 packs x 4096 tokens, lengths LogN(median 800), D=4096, N=16, bf16, fwd+bwd"),
+    "m14b_small": Workload("m14b_small", 4096, 16, 4, "bf16", 3, True,
+                           "Mamba-1.4B layer, 2 packs x 4096 tokens (profiling size), D=4096, N=16, bf16, fwd+bwd"),
     "longtail": Workload("longtail", 4096, 16, 4, "bf16", 4, True,
                          "long tail: 2 packs x 65536 tokens (2000 short, one 32768, LogN bulk), D=4096, N=16, bf16, fwd+bwd"),
 }
@@ -84,9 +87,9 @@ def pack_lengths(name: str, seed: int | None = None) -> list[int]:
         return [4, 2, 3, 7]
     if name == "m130m":
         return _lognormal_fill(rng, 4096, 300, 16, 2048)
-    if name in ("m14b_fwd", "m14b"):
+    if name in ("m14b_fwd", "m14b", "m14b_small"):
         out = []
-        for _ in range(8):
+        for _ in range(2 if name == "m14b_small" else 8):
             out += _lognormal_fill(rng, 4096, 800, 32, 4096)
         return out
     if name == "longtail":
