@@ -45,6 +45,16 @@ def per_token_counts(D, N, e, W=4):
     }
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the last ncu
+# capture of a kernel, per token; reset an entry to nothing as soon as the
+# kernel changes (profiles/ keeps the capture summaries).
+LAST_CAPTURE_TRAFFIC = {
+    ("m14b", "scan_bwd"): {"bytes_per_token": (336.948992e6 + 521.399040e6) / 8192,
+                           "source": "ncu capture on m14b_small (T=8192), scaled by tokens; "
+                                     "profiles/scan_bwd_m14b_small.md"},
+}
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -55,7 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    p.add_argument("--cpu-channels", type=int, default=256)
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target wall time of the CPU-oracle baseline sample")
     return p.parse_args(argv)
 
 
@@ -196,13 +207,23 @@ def config_of(w, world):
 
 
 # ---------------------------------------------------------------- reference arm
+def sized_sample(w, r, seconds):
+    """Channel count whose oracle run takes about `seconds` (calibrated on 16)."""
+    D = w["workload"].D
+    ch0 = min(16, D)
+    sec0, _ = oracle_sample(w, r, ch0)
+    ch = int(ch0 * seconds / max(sec0, 1e-3))
+    return max(ch0, min(D, (ch // 16) * 16 or ch0))
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     w, r = load_workload(args.workload)
     D, T = w["workload"].D, w["T"]
-    ch = max(1, min(16, D))
+    # each step: a channel sample sized so that all steps together take ~2 minutes
+    ch = sized_sample(w, r, 120.0 / max(1, args.steps + args.warmup))
     times, threads = [], 1
     for i in range(args.warmup + args.steps):
         sec, threads = oracle_sample(w, r, ch)
@@ -407,7 +428,10 @@ def run_ours(args):
         roof = {"kernel": dom, "bound": "hbm", "achieved": stages[dom]["GB/s"], "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    tr = LAST_CAPTURE_TRAFFIC.get((args.workload if args.workload != "m14b_small" else "m14b", dom))
+    roof["traffic"] = tr["bytes_per_token"] * T if tr else None
+    if tr:
+        roof["traffic_source"] = tr["source"]
     roof["algorithmic_per_token"] = c
     # whole-step roofline (the metric's definition): slowest of HBM, FP32, MUFU bounds
     tot = {k: sum(counts[s][k] for s in counts) for k in ("bytes", "fp32", "mufu")}
@@ -424,7 +448,7 @@ def run_ours(args):
     # --- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        ch = max(1, min(args.cpu_channels, D))
+        ch = sized_sample(w, r, args.cpu_seconds)
         csec, threads = oracle_sample(w, r, ch)
         cpu = {"value": T * (ch / D) / csec, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{ch} of {D} channels over all {T} tokens (conv1d + selective scan fwd + bwd, "
