@@ -175,6 +175,44 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------ allocation-free forward scan
+ * The article has no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory where they run the scan: code
+ * running inside an allocator's own callbacks, runtimes that reserved the whole
+ * device for their own pool up front, or hot paths where allocation is not
+ * allowed because it could stall or fail mid-step.
+ *
+ * It computes exactly what varlen_selective_scan_fwd computes, with the same
+ * arguments minus the workspace: the look-back scratch lives in one static
+ * device array of VSSM_NOALLOC_SCRATCH_BYTES built into the library, held by
+ * every GPU that loads it until the process exits.  The call allocates nothing
+ * (no cudaMalloc, no library allocator); the caller still provides every input
+ * and output.
+ *   - The first call made with a given device current looks up the array's
+ *     device address (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture on that device.
+ *   - A problem whose scratch would not fit (about T*D*(2N+1)/32 + 4*T
+ *     bytes: T = 8192 tokens at D = 4096, N = 16 needs 35 MB and fits;
+ *     T = 16384 needs 69 MB and does not) is rejected with
+ *     VSSM_ERR_WORKSPACE and a message naming both sizes, before anything is
+ *     launched.
+ *   - Every call on a device shares the array and finds the previous call's
+ *     contents; the call clears what must start at zero (status, ticket,
+ *     look-back flags) on `stream` before its kernels.  Calls that overlap on
+ *     the GPU (other streams, other host threads) race on the array.
+ *   - status: nullable device int32 the call zeroes and into which device-side
+ *     errors are OR-ed (decode with vssm_status_code); NULL keeps them in the
+ *     scratch, where they cannot be read back.
+ */
+#define VSSM_NOALLOC_SCRATCH_BYTES (64u << 20)
+int varlen_selective_scan_fwd_noalloc(const void* u, const void* delta_raw, const float* A,
+                                      const void* B, const void* C, const float* Dskip,
+                                      const void* z, const float* dt_bias, int32_t delta_softplus,
+                                      const int32_t* cu_seqlens, const int32_t* position_indices,
+                                      int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
+                                      vssm_dtype dtype, void* out, float* chunk_states,
+                                      int32_t* status, void* stream);
+
 /* ------------------------------------------------------------ status, errors, knobs
  * vssm_read_status: synchronises `stream`, reads the status word the last call
  * using `workspace` left there, and stores VSSM_OK or a VSSM_ERR_* code in

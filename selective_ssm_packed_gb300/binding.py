@@ -47,6 +47,9 @@ SIGNATURES = {
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int, _vp,
                                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                                  _vp]),
+    "varlen_selective_scan_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                                         _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
+                                                         _vp, _vp, _vp, _vp]),
     "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "vssm_last_error": (ctypes.c_char_p, []),

@@ -182,6 +182,13 @@ int resolve_pos(const int32_t* cu, const int32_t* pos_in, int32_t S, int64_t T, 
 
 }  // namespace
 
+// Lets other translation units of the library report a host-side error
+// through vssm_last_error().
+int vssm::record_error(int code, const char* message) {
+  g_last_error = message ? message : "";
+  return code;
+}
+
 // ============================================================================ C ABI
 extern "C" {
 

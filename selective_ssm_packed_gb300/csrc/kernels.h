@@ -93,6 +93,9 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dout, float* dA, float* dB, float* dC,
                             float* dDskip, float* d_dt_bias, cudaStream_t st);
 
+// Sets the message vssm_last_error() returns on this thread; returns `code`.
+int record_error(int code, const char* message);
+
 // ---------------------------------------------------------------- reductions
 // out[m] = sum_{p < P} in[p * ld + m] for m < M, p in increasing order.
 cudaError_t launch_sum_rows(const float* in, int64_t P, int64_t M, int64_t ld, float* out,

@@ -1,0 +1,207 @@
+// noalloc.cu -- the forward selective scan for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocator) at the point where
+// they run the scan: code that runs inside a host allocator's own callbacks, a
+// runtime that has handed every byte of the device to its own pool up front,
+// or an embedding that forbids allocation on its hot path so that a step never
+// stalls on the allocator.  varlen_selective_scan_fwd needs a caller-supplied
+// workspace for its cross-chunk look-back state; this variant keeps that
+// scratch in a fixed-size array compiled into the library instead, so the
+// caller passes only inputs and outputs.
+//
+// The scratch is one file-scope __device__ array of VSSM_NOALLOC_SCRATCH_BYTES
+// (64 MiB).  Every GPU that loads this part of the library keeps it until the
+// process exits, and every call on a device uses the same array, which keeps
+// whatever the previous call left: the call clears the part that must start at
+// zero (status, work ticket, look-back flags) before launching, and calls that
+// overlap on the GPU (two streams, or two host threads on one device) race on
+// it.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "varlen_ssm.h"
+
+namespace vssm {
+namespace {
+
+constexpr size_t kScratchBytes = VSSM_NOALLOC_SCRATCH_BYTES;
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+// The scratch itself.  In host code this name is only a host-side stand-in for
+// the device array; kernels must be given the device address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+namespace {
+
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int err(int code, const char* fmt, long long a = 0, long long b = 0) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), fmt, a, b);
+  return record_error(code, buf);
+}
+
+// Device address of the scratch on the current device, looked up on the first
+// call made with that device current and cached per device afterwards.
+int scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return err(VSSM_ERR_CUDA, "device ordinal %lld out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      char buf[256];
+      snprintf(buf, sizeof(buf), "cudaGetSymbolAddress of the built-in scratch failed: %s",
+               cudaGetErrorString(e));
+      return record_error(VSSM_ERR_CUDA, buf);
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return VSSM_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int map2d(CUtensorMap* m, const void* base, IO io, int64_t T, int D, int bx, int by) {
+  std::memset(m, 0, sizeof(*m));
+  if (!base) return VSSM_OK;
+  auto enc = encoder();
+  if (!enc) return record_error(VSSM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * (cuuint64_t)io_bytes(io)};
+  const cuuint32_t box[2] = {(cuuint32_t)bx, (cuuint32_t)by};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, io == IO::F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return err(VSSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%lld)", (long long)r);
+  return VSSM_OK;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace vssm
+
+using namespace vssm;
+
+extern "C" int varlen_selective_scan_fwd_noalloc(
+    const void* u, const void* delta_raw, const float* A, const void* B, const void* C,
+    const float* Dskip, const void* z, const float* dt_bias, int32_t delta_softplus,
+    const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+    int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* out, float* chunk_states,
+    int32_t* status, void* stream) {
+  // ---- argument checks (same rules as varlen_selective_scan_fwd)
+  if (dtype != VSSM_F32 && dtype != VSSM_BF16) return err(VSSM_ERR_DTYPE, "dtype %lld not supported", dtype);
+  const IO io = dtype == VSSM_F32 ? IO::F32 : IO::BF16;
+  const int64_t T = total_tokens;
+  if (T < 0 || T > 2147483647LL) return err(VSSM_ERR_ARG, "total_tokens %lld out of range", T);
+  if (D <= 0) return err(VSSM_ERR_ARG, "D must be positive (got %lld)", D);
+  if (num_seqs < 0 || !cu_seqlens) return record_error(VSSM_ERR_ARG, "bad num_seqs or NULL cu_seqlens");
+  if (N != 4 && N != 8 && N != 16) return err(VSSM_ERR_UNSUPPORTED, "N = %lld not in {4, 8, 16}", N);
+  const int e = io_bytes(io);
+  if (((int64_t)D * e) % 16 != 0 || (N * e) % 16 != 0)
+    return record_error(VSSM_ERR_ALIGN, "D * sizeof(io) and N * sizeof(io) must be multiples of 16");
+  if (!A) return record_error(VSSM_ERR_ARG, "A is NULL");
+  if (T > 0) {
+    const void* need[] = {u, delta_raw, B, C, out};
+    for (const void* p : need) {
+      if (!p) return record_error(VSSM_ERR_ARG, "u, delta_raw, B, C and out must be non-NULL");
+      if (!al16(p)) return record_error(VSSM_ERR_ALIGN, "u, delta_raw, B, C, out must be 16-byte aligned");
+    }
+  }
+  if ((z && !al16(z)) || (chunk_states && !al16(chunk_states)))
+    return record_error(VSSM_ERR_ALIGN, "z and chunk_states must be 16-byte aligned");
+
+  // ---- scratch layout: [header: status, ticket][flags][pos][agg][agg_sd][incl]
+  const int64_t n_tiles = cdiv(D, kTile), n_chunks = cdiv(T, kFwdChunk);
+  const size_t slots = (size_t)(n_tiles * n_chunks);
+  const size_t o_flags = kAlign;
+  const size_t o_pos = o_flags + up(sizeof(int) * slots);
+  const size_t o_agg = o_pos + up(sizeof(int32_t) * (size_t)T);
+  const size_t o_sd = o_agg + up(sizeof(float) * slots * N * kTile);
+  const size_t o_incl = o_sd + up(sizeof(float) * slots * kTile);
+  const size_t need = o_incl + up(sizeof(float) * slots * N * kTile);
+  if (need > kScratchBytes)
+    return err(VSSM_ERR_WORKSPACE,
+               "this problem needs %lld bytes of scratch but the built-in scratch holds %lld bytes; "
+               "use varlen_selective_scan_fwd with a caller-allocated workspace",
+               (long long)need, (long long)kScratchBytes);
+
+  void* base = nullptr;
+  const int rc = scratch_address(&base);
+  if (rc != VSSM_OK) return rc;
+  char* s = static_cast<char*>(base);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemsetAsync(s, 0, o_pos, st);  // status, ticket, look-back flags
+  if (ce == cudaSuccess && status) ce = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+  if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
+  if (T == 0) return VSSM_OK;
+  int32_t* status_word = status ? status : reinterpret_cast<int32_t*>(s);
+
+  const int32_t* pos = position_indices;
+  if (!pos) {
+    int32_t* p = reinterpret_cast<int32_t*>(s + o_pos);
+    ce = launch_position_indices(cu_seqlens, num_seqs, T, p, status_word, st);
+    if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
+    pos = p;
+  }
+
+  ScanArgs a{};
+  a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
+  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out;
+  a.status = status_word;
+  a.ticket = reinterpret_cast<unsigned*>(s + 4);
+  a.flags = reinterpret_cast<int*>(s + o_flags);
+  a.agg = reinterpret_cast<float*>(s + o_agg);
+  a.agg_sd = reinterpret_cast<float*>(s + o_sd);
+  a.incl = reinterpret_cast<float*>(s + o_incl);
+  a.T = T; a.D = D; a.N = N;
+  a.n_tiles = (int)n_tiles;
+  a.n_chunks = (int)n_chunks;
+  a.delta_softplus = delta_softplus ? 1 : 0;
+  a.has_z = z ? 1 : 0;
+  a.has_skip = Dskip ? 1 : 0;
+  a.box_x = D < kTile ? D : kTile;
+  a.box_y = T < kFwdChunk ? (int)T : kFwdChunk;
+  a.drop_ticket = -1;
+  a.wait_ns = 1000000000ull;
+  CUtensorMap mu, mdr, mz;
+  int r = map2d(&mu, u, io, T, D, a.box_x, a.box_y);
+  if (r == VSSM_OK) r = map2d(&mdr, delta_raw, io, T, D, a.box_x, a.box_y);
+  if (r == VSSM_OK) r = map2d(&mz, z, io, T, D, a.box_x, a.box_y);
+  if (r != VSSM_OK) return r;
+  ce = launch_scan_fwd(a, io, mu, mdr, mz, st);
+  if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
+  return VSSM_OK;
+}
