@@ -169,4 +169,20 @@ __device__ __forceinline__ void lds_row(float (&v)[N], const __nv_bfloat16* p) {
   }
 }
 
+// Widens `count` bf16 values staged in shared memory into an fp32 copy (all
+// threads of the block take part; the caller synchronises before reading).
+// For fp32 I/O the staged values are used as they are.
+template <typename T>
+__device__ __forceinline__ const float* widen_rows(const T* src, float* dst, int count, int tid,
+                                                   int nthreads) {
+  if constexpr (sizeof(T) == 4) {
+    return reinterpret_cast<const float*>(src);
+  } else {
+    const __nv_bfloat162* s2 = reinterpret_cast<const __nv_bfloat162*>(src);
+    float2* d2 = reinterpret_cast<float2*>(dst);
+    for (int i = tid; i < count / 2; i += nthreads) d2[i] = __bfloat1622float2(s2[i]);
+    return dst;
+  }
+}
+
 }  // namespace vssm

@@ -1,7 +1,8 @@
 // conv.cu -- packed depthwise causal conv1d (width W <= 4), forward and backward.
 //
-// Layout: thread block = 32 threads along channels x 8 along tokens; the grid's
-// x axis walks token rows, its y axis channel columns.  Each
+// Layout: thread block = 32 threads along channels x 8 along tokens; a 1-D grid
+// where consecutive blocks cover consecutive channel columns of the same token
+// rows, so the blocks running together read and write whole rows.  Each
 // thread owns V consecutive channels (one 16-byte vector in the forward, an
 // 8/16-byte vector in the backward) and a short run of R consecutive tokens,
 // so every warp reads and writes whole contiguous row segments.  The
@@ -81,8 +82,10 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvArgs a) {
   constexpr int V = 16 / sizeof(T);
   constexpr int R = kFwdRun;
   constexpr int E = R + W - 1;  // rows loaded: t0-(W-1) .. t0+R-1
-  const int d0 = (blockIdx.y * 32 + threadIdx.x) * V;
-  const int64_t t0 = ((int64_t)blockIdx.x * kRowsPerBlock + threadIdx.y) * R;
+  const int ncols = (a.D / V + 31) / 32;
+  const int64_t row = blockIdx.x / ncols;
+  const int d0 = ((int)(blockIdx.x - row * ncols) * 32 + threadIdx.x) * V;
+  const int64_t t0 = (row * kRowsPerBlock + threadIdx.y) * R;
   if (d0 >= a.D || t0 >= a.T) return;
   const T* __restrict__ x = static_cast<const T*>(a.x);
   T* __restrict__ u = static_cast<T*>(a.out);
@@ -135,8 +138,10 @@ template <typename T, int W>
 __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvArgs a) {
   constexpr int V = 4;
   constexpr int R = kBwdRun;
-  const int d0 = (blockIdx.y * 32 + threadIdx.x) * V;
-  const int64_t t0 = ((int64_t)blockIdx.x * kRowsPerBlock + threadIdx.y) * R;
+  const int ncols = (a.D / V + 31) / 32;
+  const int64_t row = blockIdx.x / ncols;
+  const int d0 = ((int)(blockIdx.x - row * ncols) * 32 + threadIdx.x) * V;
+  const int64_t t0 = (row * kRowsPerBlock + threadIdx.y) * R;
   const bool active = d0 < a.D && t0 < a.T;
   const T* __restrict__ x = static_cast<const T*>(a.x);
   const T* __restrict__ du = static_cast<const T*>(a.du);
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvArgs a) {
   }
   __syncthreads();
   if (threadIdx.y == 0 && d0 < a.D) {
-    float* part = a.partial + (int64_t)blockIdx.x * (D * (W + 1));
+    float* part = a.partial + row * (D * (W + 1));
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       float s[W + 1];
@@ -273,8 +278,8 @@ cudaError_t fwd_w(const ConvArgs& a, cudaStream_t st) {
   constexpr int V = 16 / sizeof(T);
   const int64_t cols = (a.D / V + 31) / 32;
   const int64_t rows = (a.T + kRowsPerBlock * kFwdRun - 1) / (kRowsPerBlock * kFwdRun);
-  if (cols > 65535) return cudaErrorInvalidConfiguration;
-  conv_fwd_kernel<T, W><<<dim3((unsigned)rows, (unsigned)cols), dim3(32, kRowsPerBlock), 0, st>>>(a);
+  if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
+  conv_fwd_kernel<T, W><<<(unsigned)(rows * cols), dim3(32, kRowsPerBlock), 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -282,8 +287,8 @@ template <typename T, int W>
 cudaError_t bwd_w(const ConvArgs& a, cudaStream_t st) {
   const int64_t cols = (a.D / 4 + 31) / 32;
   const int64_t rows = conv_bwd_partial_rows(a.T);
-  if (cols > 65535) return cudaErrorInvalidConfiguration;
-  conv_bwd_kernel<T, W><<<dim3((unsigned)rows, (unsigned)cols), dim3(32, kRowsPerBlock), 0, st>>>(a);
+  if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
+  conv_bwd_kernel<T, W><<<(unsigned)(rows * cols), dim3(32, kRowsPerBlock), 0, st>>>(a);
   return cudaGetLastError();
 }
 

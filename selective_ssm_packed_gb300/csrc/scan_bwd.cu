@@ -49,7 +49,10 @@ struct BwdSmem {
   alignas(128) T dout[kL * kTile];
   alignas(128) T B[kL * N];
   alignas(128) T C[kL * N];
-  alignas(16) float hist[kK * N * kThreads];  // [k][n][tid]
+  // B and C widened to fp32 once per work item (bf16 I/O only; fp32 I/O reads B, C directly)
+  alignas(16) float Bf[sizeof(T) == 2 ? kL * N : 4];
+  alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
+  alignas(16) float4 hist[kK * (N / 4) * kThreads];  // [k][n/4][tid], 16-byte accesses
   alignas(16) float agg[kS * N * kTile];
   float tot[N * kTile];
   float rin[N * kTile];
@@ -133,10 +136,13 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
 
   if (!mbar_wait(&sm.bar, 0, a.wait_ns) && lane == 0) atomicOr(a.status, kStatusTmaTimeout);
+  const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
+  const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
   __syncthreads();
 
   const int tb = s * kK;
-  // ---- 1. per-token values (registers)
+  // ---- 1. per-token values (registers); lanes without a channel get u = g = 0
+  //         so that every partial they feed into a channel sum is exactly 0
   float dl[kK], sg[kK], uu[kK], g[kK], dzf[kK];
   int rst = 0;  // bit k: token tb+k starts a sequence (warp-uniform)
 #pragma unroll
@@ -152,8 +158,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         dl[k] = r;
         sg[k] = 1.0f;
       }
-      uu[k] = to_f(sm.u[t * bx + lane]);
-      const float go = to_f(sm.dout[t * bx + lane]);
+      uu[k] = valid ? to_f(sm.u[t * bx + lane]) : 0.0f;
+      const float go = valid ? to_f(sm.dout[t * bx + lane]) : 0.0f;
       if (a.has_z) {
         const float zz = to_f(sm.z[t * bx + lane]);
         const float sz = sigmoidf_fast(zz);
@@ -182,7 +188,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     const float du = dl[k] * uu[k];
     float Bv[N];
-    lds_row<N>(Bv, sm.B + t * N);
+    lds_row<N>(Bv, Bf + t * N);
 #pragma unroll
     for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dl[k] * A2[n]), h[n], du * Bv[n]);
     sd += dl[k];
@@ -220,11 +226,12 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int t = tb + k;
     if (t >= rows) continue;
     float Cv[N];
-    lds_row<N>(Cv, sm.C + t * N);
-    const bool start = rst & (1 << k);
+    lds_row<N>(Cv, Cf + t * N);
+    // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
+    const float off = (rst & (1 << k)) ? -INFINITY : 0.0f;
 #pragma unroll
     for (int n = 0; n < N; ++n) {
-      const float at = start ? 0.0f : ex2(dl[k] * A2[n]);
+      const float at = ex2(fmaf(dl[k], A2[n], off));
       dh[n] = at * fmaf(Cv[n], g[k], dh[n]);
     }
   }
@@ -315,23 +322,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
     }
   }
-  __syncthreads();
 
-  // ---- 5. carry entering my last token from the right
-  {
-    int rs_post = 0;
-    float sd_post = 0.0f;
-    for (int j = s + 1; j < kS; ++j) {
-      rs_post |= sm.aggRS[j];
-      sd_post += sm.aggSD[j * kTile + lane];
-    }
-#pragma unroll
-    for (int n = 0; n < N; ++n) {
-      const float E = sm.agg[(s * N + n) * kTile + lane];
-      dh[n] = rs_post ? E : fmaf(ex2(A2[n] * sd_post), sm.rin[n * kTile + lane], E);
-    }
-  }
-  // recompute forward states of my K tokens into shared memory
+  // ---- 5. recompute the forward states of my K tokens into shared memory; it
+  //         needs no carry from the right, so warps 1..7 do it while warp 0 is
+  //         still in the look-back above
   float yk[kK];
 #pragma unroll
   for (int n = 0; n < N; ++n) h[n] = hs[n];
@@ -346,16 +340,34 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     const float du = dl[k] * uu[k];
     float Bv[N], Cv[N];
-    lds_row<N>(Bv, sm.B + t * N);
-    lds_row<N>(Cv, sm.C + t * N);
+    lds_row<N>(Bv, Bf + t * N);
+    lds_row<N>(Cv, Cf + t * N);
     float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
     for (int n = 0; n < N; ++n) {
       h[n] = fmaf(ex2(dl[k] * A2[n]), h[n], du * Bv[n]);
-      sm.hist[(k * N + n) * kThreads + tid] = h[n];
       if (n & 1) y1 = fmaf(Cv[n], h[n], y1); else y0 = fmaf(Cv[n], h[n], y0);
     }
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q)
+      sm.hist[(k * (N / 4) + q) * kThreads + tid] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
     yk[k] = fmaf(Dsk, uu[k], y0 + y1);
+  }
+  __syncthreads();
+
+  // ---- 6. carry entering my last token from the right
+  {
+    int rs_post = 0;
+    float sd_post = 0.0f;
+    for (int j = s + 1; j < kS; ++j) {
+      rs_post |= sm.aggRS[j];
+      sd_post += sm.aggSD[j * kTile + lane];
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      const float E = sm.agg[(s * N + n) * kTile + lane];
+      dh[n] = rs_post ? E : fmaf(ex2(A2[n] * sd_post), sm.rin[n * kTile + lane], E);
+    }
   }
 
   // reverse walk
@@ -371,36 +383,43 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int t = tb + k;
     if (t >= rows) continue;  // warp-uniform
     float Bv[N], Cv[N];
-    lds_row<N>(Bv, sm.B + t * N);
-    lds_row<N>(Cv, sm.C + t * N);
-    const bool start = rst & (1 << k);
+    lds_row<N>(Bv, Bf + t * N);
+    lds_row<N>(Cv, Cf + t * N);
+    const float off = (rst & (1 << k)) ? -INFINITY : 0.0f;
     const float du = dl[k] * uu[k];
     float v[V];
     float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      const float hcur = sm.hist[(k * N + n) * kThreads + tid];
-      const float hprev = k > 0 ? sm.hist[((k - 1) * N + n) * kThreads + tid] : hs[n];
-      dh[n] = fmaf(Cv[n], g[k], dh[n]);  // total gradient w.r.t. h_t
-      const float at = start ? 0.0f : ex2(dl[k] * A2[n]);
-      const float dhq = dh[n] * (at * hprev);
-      dA[n] = fmaf(dl[k], dhq, dA[n]);
-      s2 = fmaf(A2[n], dhq, s2);
-      s1 = fmaf(dh[n], Bv[n], s1);
-      v[n] = valid ? dh[n] * du : 0.0f;
-      v[N + n] = valid ? g[k] * hcur : 0.0f;
-      dh[n] *= at;                       // carry to h_{t-1}
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 hc4 = sm.hist[(k * (N / 4) + q) * kThreads + tid];
+      const float4 hp4 = k > 0 ? sm.hist[((k - 1) * (N / 4) + q) * kThreads + tid]
+                               : make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
+      const float hcur[4] = {hc4.x, hc4.y, hc4.z, hc4.w};
+      const float hprev[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = 4 * q + i;
+        dh[n] = fmaf(Cv[n], g[k], dh[n]);  // total gradient w.r.t. h_t
+        const float at = ex2(fmaf(dl[k], A2[n], off));
+        const float dhq = dh[n] * (at * hprev[i]);
+        dA[n] = fmaf(dl[k], dhq, dA[n]);
+        s2 = fmaf(A2[n], dhq, s2);
+        s1 = fmaf(dh[n], Bv[n], s1);
+        v[n] = dh[n] * du;               // 0 on lanes without a channel (u = 0)
+        v[N + n] = g[k] * hcur[i];       // 0 on lanes without a channel (g = 0)
+        dh[n] *= at;                     // carry to h_{t-1}
+      }
     }
     const float gdu_t = fmaf(dl[k], s1, Dsk * g[k]);
     const float gdl_t = fmaf(uu[k], s1, s2 * kLn2);
     const float gdr_t = gdl_t * sg[k];
     sDD = fmaf(g[k], uu[k], sDD);
     sDB += gdr_t;
-    const int64_t off = (t0 + t) * a.D + d;
+    const int64_t at_td = (t0 + t) * a.D + d;
     if (valid) {
-      gdu[off] = from_f<T>(gdu_t);
-      gddr[off] = from_f<T>(gdr_t);
-      if (gdz) gdz[off] = from_f<T>(dzf[k] * yk[k]);
+      gdu[at_td] = from_f<T>(gdu_t);
+      gddr[at_td] = from_f<T>(gdr_t);
+      if (gdz) gdz[at_td] = from_f<T>(dzf[k] * yk[k]);
     }
     ReduceScatter<V, 16>::run(v, lane);
     if ((lane & (kRep - 1)) == 0)

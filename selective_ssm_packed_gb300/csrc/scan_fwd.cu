@@ -44,6 +44,9 @@ struct FwdSmem {
   alignas(128) T z[kL * kTile];
   alignas(128) T B[kL * N];
   alignas(128) T C[kL * N];
+  // B and C widened to fp32 once per work item (bf16 I/O only)
+  alignas(16) float Bf[sizeof(T) == 2 ? kL * N : 4];
+  alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
   alignas(16) float dlt[kL * kTile];
   alignas(16) float aggH[kS * N * kTile];
   float totH[N * kTile];
@@ -99,6 +102,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
 
   if (!mbar_wait(&sm.bar, 0, a.wait_ns) && lane == 0) atomicOr(a.status, kStatusTmaTimeout);
+  const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
+  const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
   __syncthreads();
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
@@ -129,7 +134,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float dl = sm.dlt[t * kTile + lane];
     const float du = dl * to_f(sm.u[t * bx + lane]);
     float Bv[N];
-    lds_row<N>(Bv, sm.B + t * N);
+    lds_row<N>(Bv, Bf + t * N);
 #pragma unroll
     for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dl * A2[n]), h[n], du * Bv[n]);
     sd += dl;
@@ -261,8 +266,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float uu = to_f(sm.u[t * bx + lane]);
     const float du = dl * uu;
     float Bv[N], Cv[N];
-    lds_row<N>(Bv, sm.B + t * N);
-    lds_row<N>(Cv, sm.C + t * N);
+    lds_row<N>(Bv, Bf + t * N);
+    lds_row<N>(Cv, Cf + t * N);
     float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
     for (int n = 0; n < N; ++n) {
