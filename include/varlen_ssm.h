@@ -191,8 +191,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
  *   - The first call made with a given device current looks up the array's
  *     device address (cudaGetSymbolAddress) and caches it; make that first call
  *     before any stream capture on that device.
- *   - A problem whose scratch would not fit (about T*D*(2N+1)/32 + 4*T
- *     bytes: T = 8192 tokens at D = 4096, N = 16 needs 35 MB and fits;
+ *   - A problem whose scratch would not fit (about T*D*(N+1)/16 + 4*T
+ *     bytes: T = 8192 tokens at D = 4096, N = 16 needs 36 MB and fits;
  *     T = 16384 needs 69 MB and does not) is rejected with
  *     VSSM_ERR_WORKSPACE and a message naming both sizes, before anything is
  *     launched.

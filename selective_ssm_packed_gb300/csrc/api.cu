@@ -42,7 +42,7 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------- workspace layout
-// [header 256 B: status int @0, ticket uint @4][flags][pos][...call specific]
+// [header 256 B: status int @0, ticket uint @4][flags, one per (slot, lane)][pos][...call specific]
 // header + flags are cleared by one memset at the start of every call.
 struct Layout {
   size_t flags = 0, pos = 0, agg = 0, agg_sd = 0, incl = 0;
@@ -57,7 +57,7 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   const int64_t slots = n_tiles * n_chunks;
   size_t off = kAlign;
   l.flags = off;
-  off += up(sizeof(int) * (size_t)slots);
+  off += up(sizeof(int) * (size_t)slots * kTile);
   l.clear_bytes = off;
   l.pos = off;
   off += up(sizeof(int32_t) * (size_t)T);

@@ -47,6 +47,50 @@ __device__ __forceinline__ float softplusf(float x) {
   return fmaxf(x, 0.0f) + log1pf(ex2(-fabsf(x) * kLog2e));
 }
 
+// ------------------------------------------------------------------ packed FP32 pairs
+// Two lanes of FP32 per instruction (fma/mul.rn.f32x2): the FMA pipe does the
+// same work, but the pair costs one issue slot.  Each component is rounded
+// exactly as the scalar instruction would round it.
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2(x.x), ex2(x.y)); }
+
+// Loads N fp32 values (16-byte aligned shared memory) as N/2 pairs.
+template <int N>
+__device__ __forceinline__ void lds_pairs(float2 (&v)[N / 2], const float* p) {
+#pragma unroll
+  for (int i = 0; i < N / 2; i += 2) {
+    const float4 q = *reinterpret_cast<const float4*>(p + 2 * i);
+    v[i] = make_float2(q.x, q.y);
+    v[i + 1] = make_float2(q.z, q.w);
+  }
+}
+
+// Copies the rows d0 .. d0+31 of a row-major (D, N) fp32 array into shared
+// memory with row pitch N + 4 (coalesced global reads; the padding makes the
+// per-lane 16-byte row reads conflict-free); rows past D are zero.
+template <int N>
+__device__ __forceinline__ void stage_rows(float* dst, const float* src, int d0, int D, int tid,
+                                           int nthreads) {
+  const float* base = src + (int64_t)d0 * N;
+  for (int i = tid; i < 32 * N; i += nthreads) {
+    const int r = i / N, c = i - r * N;
+    dst[r * (N + 4) + c] = (d0 + r < D) ? __ldg(base + i) : 0.0f;
+  }
+}
+
+// Reads one staged row of N values as N/2 pairs, each value times `scale`.
+template <int N>
+__device__ __forceinline__ void load_scaled_pairs(float2 (&v)[N / 2], const float* row, float scale) {
+#pragma unroll
+  for (int i = 0; i < N / 2; i += 2) {
+    const float4 q = *reinterpret_cast<const float4*>(row + 2 * i);
+    v[i] = make_float2(q.x * scale, q.y * scale);
+    v[i + 1] = make_float2(q.z * scale, q.w * scale);
+  }
+}
+
 // ------------------------------------------------------------------ timers, memory order
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

@@ -18,33 +18,16 @@ namespace vssm {
 namespace {
 
 constexpr int kRowsPerBlock = 8;  // threadIdx.y extent
-constexpr int kFwdRun = 4;        // tokens per thread, forward
+constexpr int kFwdRun = 8;        // tokens per thread, forward
 constexpr int kBwdRun = 8;        // tokens per thread, backward
 
-template <typename T, int V>
-__device__ __forceinline__ void ldv(const T* p, float (&v)[V]);
 template <typename T, int V>
 __device__ __forceinline__ void stv(T* p, const float (&v)[V]);
 
 // 16-byte loads / stores
 template <>
-__device__ __forceinline__ void ldv<float, 4>(const float* p, float (&v)[4]) {
-  const float4 q = __ldg(reinterpret_cast<const float4*>(p));
-  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-}
-template <>
 __device__ __forceinline__ void stv<float, 4>(float* p, const float (&v)[4]) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-}
-template <>
-__device__ __forceinline__ void ldv<__nv_bfloat16, 8>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 f = __bfloat1622float2(h[j]);
-    v[2 * j] = f.x; v[2 * j + 1] = f.y;
-  }
 }
 template <>
 __device__ __forceinline__ void stv<__nv_bfloat16, 8>(__nv_bfloat16* p, const float (&v)[8]) {
@@ -55,13 +38,6 @@ __device__ __forceinline__ void stv<__nv_bfloat16, 8>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint4*>(p) = q;
 }
 // 8-byte bf16 loads / stores (backward, 4 channels per thread)
-template <>
-__device__ __forceinline__ void ldv<__nv_bfloat16, 4>(const __nv_bfloat16* p, float (&v)[4]) {
-  const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
-  const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
-  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-}
 template <>
 __device__ __forceinline__ void stv<__nv_bfloat16, 4>(__nv_bfloat16* p, const float (&v)[4]) {
   uint2 q;
@@ -76,32 +52,77 @@ __device__ __forceinline__ float silu_grad(float x) {
   return s * fmaf(x, 1.0f - s, 1.0f);
 }
 
+// Raw (still packed) row segments: loaded in one vector access, widened later.
+template <typename T, int V> struct RawRow;
+template <> struct RawRow<float, 4> { uint4 r; };
+template <> struct RawRow<__nv_bfloat16, 8> { uint4 r; };
+template <> struct RawRow<__nv_bfloat16, 4> { uint2 r; };
+
+template <typename T, int V>
+__device__ __forceinline__ void ld_raw(const T* p, RawRow<T, V>& out) {
+  if constexpr (sizeof(out.r) == 16) out.r = __ldg(reinterpret_cast<const uint4*>(p));
+  else out.r = __ldg(reinterpret_cast<const uint2*>(p));
+}
+template <typename T, int V>
+__device__ __forceinline__ void zero_raw(RawRow<T, V>& out) {
+  if constexpr (sizeof(out.r) == 16) out.r = make_uint4(0, 0, 0, 0);
+  else out.r = make_uint2(0, 0);
+}
+template <typename T, int V>
+__device__ __forceinline__ void widen(const RawRow<T, V>& in, float (&v)[V]) {
+  if constexpr (sizeof(T) == 4) {
+    v[0] = __uint_as_float(in.r.x); v[1] = __uint_as_float(in.r.y);
+    v[2] = __uint_as_float(in.r.z); v[3] = __uint_as_float(in.r.w);
+  } else {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&in.r);
+#pragma unroll
+    for (int j = 0; j < V / 2; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[2 * j] = f.x; v[2 * j + 1] = f.y;
+    }
+  }
+}
+
+// Stages the block's conv weights ([tap][channel], channel-contiguous) and
+// biases in shared memory with coalesced loads.
+template <int W, int CH>
+__device__ __forceinline__ void stage_weights(const ConvArgs& a, int c0, float (*wS)[CH], float* bS,
+                                              int tid) {
+  for (int i = tid; i < CH * W; i += 256) {
+    const int c = i / W, k = i - c * W;
+    wS[k][c] = (c0 + c < a.D) ? __ldg(a.w + (int64_t)c0 * W + i) : 0.0f;
+  }
+  for (int i = tid; i < CH; i += 256) bS[i] = (a.bias && c0 + i < a.D) ? __ldg(a.bias + c0 + i) : 0.0f;
+}
+
 // ------------------------------------------------------------------ forward
 template <typename T, int W>
-__global__ void __launch_bounds__(256) conv_fwd_kernel(ConvArgs a) {
+__global__ void __launch_bounds__(256, 2) conv_fwd_kernel(ConvArgs a) {
   constexpr int V = 16 / sizeof(T);
   constexpr int R = kFwdRun;
   constexpr int E = R + W - 1;  // rows loaded: t0-(W-1) .. t0+R-1
+  constexpr int CH = 32 * V;    // channels per block
+  __shared__ __align__(16) float wS[W][CH];
+  __shared__ __align__(16) float bS[CH];
   const int ncols = (a.D / V + 31) / 32;
   const int64_t row = blockIdx.x / ncols;
-  const int d0 = ((int)(blockIdx.x - row * ncols) * 32 + threadIdx.x) * V;
+  const int c0 = (int)(blockIdx.x - row * ncols) * CH;
+  stage_weights<W, CH>(a, c0, wS, bS, threadIdx.y * 32 + threadIdx.x);
+  __syncthreads();
+  const int d0 = c0 + threadIdx.x * V;
   const int64_t t0 = (row * kRowsPerBlock + threadIdx.y) * R;
   if (d0 >= a.D || t0 >= a.T) return;
   const T* __restrict__ x = static_cast<const T*>(a.x);
   T* __restrict__ u = static_cast<T*>(a.out);
   const int64_t D = a.D;
 
-  float xr[E][V];
+  // every load of the thread is issued before any arithmetic
+  RawRow<T, V> xr[E];
   int p[R];
 #pragma unroll
   for (int i = 0; i < E; ++i) {
     const int64_t t = t0 - (W - 1) + i;
-    if (t >= 0 && t < a.T) {
-      ldv<T, V>(x + t * D + d0, xr[i]);
-    } else {
-#pragma unroll
-      for (int v = 0; v < V; ++v) xr[i][v] = 0.0f;
-    }
+    if (t >= 0 && t < a.T) ld_raw<T, V>(x + t * D + d0, xr[i]); else zero_raw<T, V>(xr[i]);
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) p[r] = (t0 + r < a.T) ? __ldg(a.pos + t0 + r) : 0;
@@ -110,21 +131,24 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvArgs a) {
 #pragma unroll
   for (int v = 0; v < V; ++v) {
 #pragma unroll
-    for (int k = 0; k < W; ++k) w[k][v] = __ldg(a.w + (int64_t)(d0 + v) * W + k);
-    b[v] = a.bias ? __ldg(a.bias + d0 + v) : 0.0f;
+    for (int k = 0; k < W; ++k) w[k][v] = wS[k][threadIdx.x * V + v];
+    b[v] = bS[threadIdx.x * V + v];
   }
 
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int64_t t = t0 + r;
     if (t >= a.T) break;
+    float xs[W][V];
+#pragma unroll
+    for (int k = 0; k < W; ++k) widen<T, V>(xr[r + W - 1 - k], xs[k]);   // xs[k] = x[t - k]
     float o[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      float pre = fmaf(w[W - 1][v], xr[r + W - 1][v], b[v]);
+      float pre = fmaf(w[W - 1][v], xs[0][v], b[v]);
 #pragma unroll
       for (int k = 1; k < W; ++k)
-        if (p[r] >= k) pre = fmaf(w[W - 1 - k][v], xr[r + W - 1 - k][v], pre);
+        if (p[r] >= k) pre = fmaf(w[W - 1 - k][v], xs[k][v], pre);
       o[v] = a.apply_silu ? siluf(pre) : pre;
     }
     stv<T, V>(u + t * D + d0, o);
@@ -132,15 +156,26 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvArgs a) {
 }
 
 // ------------------------------------------------------------------ backward
-// Each thread streams over tokens t' = t0 .. t0+R+W-2, keeping windows of x,
-// of g = du * du/dpre and of pos, and emits dx[t'-(W-1)] once g[t'] is known.
+// Each thread loads all of its rows up front (x for t0-(W-1) .. t0+R+W-2, du
+// and pos for t0 .. t0+R+W-2), then streams over t' = t0 .. t0+R+W-2 keeping
+// windows of g = du * du/dpre and of pos, and emits dx[t'-(W-1)] once g[t'] is
+// known.
 template <typename T, int W>
-__global__ void __launch_bounds__(256) conv_bwd_kernel(ConvArgs a) {
+__global__ void __launch_bounds__(256, 2) conv_bwd_kernel(ConvArgs a) {
   constexpr int V = 4;
   constexpr int R = kBwdRun;
+  constexpr int CH = 32 * V;
+  constexpr int EG = R + W - 1;        // tokens t0 .. t0+R+W-2 (g, du, pos)
+  constexpr int EX = EG + W - 1;       // x rows t0-(W-1) .. t0+R+W-2
+  __shared__ __align__(16) float wS[W][CH];
+  __shared__ __align__(16) float bS[CH];
+  __shared__ float red[kRowsPerBlock][32][V * (W + 1)];
   const int ncols = (a.D / V + 31) / 32;
   const int64_t row = blockIdx.x / ncols;
-  const int d0 = ((int)(blockIdx.x - row * ncols) * 32 + threadIdx.x) * V;
+  const int c0 = (int)(blockIdx.x - row * ncols) * CH;
+  stage_weights<W, CH>(a, c0, wS, bS, threadIdx.y * 32 + threadIdx.x);
+  __syncthreads();
+  const int d0 = c0 + threadIdx.x * V;
   const int64_t t0 = (row * kRowsPerBlock + threadIdx.y) * R;
   const bool active = d0 < a.D && t0 < a.T;
   const T* __restrict__ x = static_cast<const T*>(a.x);
@@ -157,79 +192,70 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvArgs a) {
   }
 
   if (active) {
+    RawRow<T, V> xr[EX], dr[EG];
+    int p[EG];
+#pragma unroll
+    for (int i = 0; i < EX; ++i) {
+      const int64_t t = t0 - (W - 1) + i;
+      if (t >= 0 && t < a.T) ld_raw<T, V>(x + t * D + d0, xr[i]); else zero_raw<T, V>(xr[i]);
+    }
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+      const int64_t t = t0 + j;
+      if (t < a.T) {
+        ld_raw<T, V>(du + t * D + d0, dr[j]);
+        p[j] = __ldg(a.pos + t);
+      } else {
+        zero_raw<T, V>(dr[j]);
+        p[j] = 0;
+      }
+    }
     float w[W][V], b[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
 #pragma unroll
-      for (int k = 0; k < W; ++k) w[k][v] = __ldg(a.w + (int64_t)(d0 + v) * W + k);
-      b[v] = a.bias ? __ldg(a.bias + d0 + v) : 0.0f;
+      for (int k = 0; k < W; ++k) w[k][v] = wS[k][threadIdx.x * V + v];
+      b[v] = bS[threadIdx.x * V + v];
     }
-    float xw[W][V];   // after the shift at step t': xw[k] = x[t' - k]
-    float gw[W][V];   // after step t': gw[k] = g[t' - (W-1) + k]
-    int pw[W];        // after step t': pw[k] = pos[t' - (W-1) + k]
+    float gw[W][V];   // after step j: gw[k] = g[t0 + j - (W-1) + k]
 #pragma unroll
-    for (int k = 0; k < W; ++k) {
-      pw[k] = 0;
+    for (int k = 0; k < W; ++k)
 #pragma unroll
-      for (int v = 0; v < V; ++v) { xw[k][v] = 0.0f; gw[k][v] = 0.0f; }
-    }
-    // before the first step xw[k-1] holds x[t0 - k], so the shift lines it up
+      for (int v = 0; v < V; ++v) gw[k][v] = 0.0f;
 #pragma unroll
-    for (int k = 1; k < W; ++k) {
-      const int64_t t = t0 - k;
-      if (t >= 0) ldv<T, V>(x + t * D + d0, xw[k - 1]);
-    }
-#pragma unroll
-    for (int j = 0; j < R + W - 1; ++j) {
+    for (int j = 0; j < EG; ++j) {
       const int64_t tp = t0 + j;
-      const bool in = tp < a.T;
-      float xc[V], dc[V];
-      int p = 0;
-      if (in) {
-        ldv<T, V>(x + tp * D + d0, xc);
-        ldv<T, V>(du + tp * D + d0, dc);
-        p = __ldg(a.pos + tp);
-      } else {
+      float xs[W][V];   // xs[k] = x[t' - k]
 #pragma unroll
-        for (int v = 0; v < V; ++v) { xc[v] = 0.0f; dc[v] = 0.0f; }
-      }
-      // shift the windows by one token
+      for (int k = 0; k < W; ++k) widen<T, V>(xr[j + W - 1 - k], xs[k]);
+      float dc[V];
+      widen<T, V>(dr[j], dc);
 #pragma unroll
-      for (int k = W - 1; k > 0; --k) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) xw[k][v] = xw[k - 1][v];
-      }
-#pragma unroll
-      for (int v = 0; v < V; ++v) xw[0][v] = xc[v];
-#pragma unroll
-      for (int k = 0; k < W - 1; ++k) {
-        pw[k] = pw[k + 1];
+      for (int k = 0; k < W - 1; ++k)
 #pragma unroll
         for (int v = 0; v < V; ++v) gw[k][v] = gw[k + 1][v];
-      }
-      pw[W - 1] = p;
-      // g at t'
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         float g = 0.0f;
-        if (in) {
-          float pre = fmaf(w[W - 1][v], xw[0][v], b[v]);
+        if (tp < a.T) {
+          float pre = fmaf(w[W - 1][v], xs[0][v], b[v]);
 #pragma unroll
           for (int k = 1; k < W; ++k)
-            if (p >= k) pre = fmaf(w[W - 1 - k][v], xw[k][v], pre);
+            if (p[j] >= k) pre = fmaf(w[W - 1 - k][v], xs[k][v], pre);
           g = a.apply_silu ? dc[v] * silu_grad(pre) : dc[v];
         }
         gw[W - 1][v] = g;
-        if (j < R && in) {
+        if (j < R && tp < a.T) {
           db[v] += g;
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            if (p >= k) dw[W - 1 - k][v] = fmaf(g, xw[k][v], dw[W - 1 - k][v]);
+            if (p[j] >= k) dw[W - 1 - k][v] = fmaf(g, xs[k][v], dw[W - 1 - k][v]);
         }
       }
       // dx at t = t' - (W-1), complete now that g[t .. t+W-1] is known
       if (j >= W - 1) {
         const int64_t t = tp - (W - 1);
+        const int r = j - (W - 1);
         if (t < a.T) {
           float o[V];
 #pragma unroll
@@ -237,7 +263,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvArgs a) {
             float acc = 0.0f;
 #pragma unroll
             for (int k = 0; k < W; ++k)
-              if (t + k < a.T && pw[k] >= k) acc = fmaf(w[W - 1 - k][v], gw[k][v], acc);
+              if (t + k < a.T && p[r + k] >= k) acc = fmaf(w[W - 1 - k][v], gw[k][v], acc);
             o[v] = acc;
           }
           stv<T, V>(dx + t * D + d0, o);
@@ -247,7 +273,6 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvArgs a) {
   }
 
   // reduce dw / db over the 8 token rows of the block, write one partial row
-  __shared__ float red[kRowsPerBlock][32][V * (W + 1)];
 #pragma unroll
   for (int v = 0; v < V; ++v) {
 #pragma unroll

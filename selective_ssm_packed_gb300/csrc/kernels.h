@@ -68,7 +68,7 @@ struct ScanArgs {
   float* part_dbias;          // bwd [n_chunks][D]
   int* status;
   unsigned* ticket;
-  int* flags;                 // [n_tiles][n_chunks]
+  int* flags;                 // [n_tiles][n_chunks][kTile]: one per channel chain
   float* agg;                 // [n_tiles][n_chunks][N][kTile]
   float* agg_sd;              // [n_tiles][n_chunks][kTile]
   float* incl;                // [n_tiles][n_chunks][N][kTile]

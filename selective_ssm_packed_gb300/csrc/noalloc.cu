@@ -147,7 +147,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   const int64_t n_tiles = cdiv(D, kTile), n_chunks = cdiv(T, kFwdChunk);
   const size_t slots = (size_t)(n_tiles * n_chunks);
   const size_t o_flags = kAlign;
-  const size_t o_pos = o_flags + up(sizeof(int) * slots);
+  const size_t o_pos = o_flags + up(sizeof(int) * slots * kTile);
   const size_t o_agg = o_pos + up(sizeof(int32_t) * (size_t)T);
   const size_t o_sd = o_agg + up(sizeof(float) * slots * N * kTile);
   const size_t o_incl = o_sd + up(sizeof(float) * slots * kTile);

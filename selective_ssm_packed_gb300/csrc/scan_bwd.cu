@@ -52,13 +52,18 @@ struct BwdSmem {
   // B and C widened to fp32 once per work item (bf16 I/O only; fp32 I/O reads B, C directly)
   alignas(16) float Bf[sizeof(T) == 2 ? kL * N : 4];
   alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
-  alignas(16) float4 hist[kK * (N / 4) * kThreads];  // [k][n/4][tid], 16-byte accesses
-  alignas(16) float agg[kS * N * kTile];
+  // states after a thread's first K-1 tokens ([k][n/4][tid]); the state after
+  // its last token stays in registers
+  alignas(16) float4 hist[(kK - 1) * (N / 4) * kThreads];
+  alignas(16) float aggH[kS * N * kTile];  // forward aggregates, then each warp's start state
+  alignas(16) float aggG[kS * N * kTile];  // reverse aggregates, then exclusive suffixes
   float tot[N * kTile];
   float rin[N * kTile];
   float aggSD[kS * kTile];
   float redD[kS * kTile];
   float redB[kS * kTile];
+  alignas(16) float At[kTile * (N + 4)];  // A rows of the tile (padded), later the dA partial block
+  alignas(16) float Ht[kTile * (N + 4)];  // saved states of the chunk for the tile's channels
   int pos[kL];
   int aggRS[kS];
   int ticket;
@@ -93,6 +98,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
                 const ScanArgs a) {
   using SM = BwdSmem<T, N>;
+  constexpr int P = N / 2;                       // state pairs
   constexpr int V = 2 * N;                       // dB and dC values per token
   constexpr int kRep = 32 / (V < 32 ? V : 32);   // lanes holding the same value
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -126,12 +132,29 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     bulk_load_1d(sm.C, static_cast<const T*>(a.C) + t0 * N, bc, &sm.bar);
   }
   if (tid < kL) sm.pos[tid] = (tid < rows) ? __ldg(a.pos + t0 + tid) : 1;
+  stage_rows<N>(sm.At, a.A, d0, a.D, tid, kThreads);
+  // Early look-back (warp 0, while the tiles are in flight): the carry entering
+  // this chunk from the right does not depend on this chunk's data, and the
+  // next chunk of the tile has usually published its inclusive carry already.
+  // Take it now if it is there; otherwise step 4 does the full look-back.
+  int early = 0;
+  if (s == 0) {
+    const int64_t base = (int64_t)tile * a.n_chunks;
+    if (chunk == a.n_chunks - 1) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = 0.0f;
+      early = 1;
+    } else if (ld_acquire_gpu(a.flags + (base + chunk + 1) * kTile + lane) == kFlagInclusive) {
+      const float* inc = a.incl + (base + chunk + 1) * (N * kTile);
+#pragma unroll
+      for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = __ldcg(inc + n * kTile + lane);
+      early = 1;
+    }
+  }
+  stage_rows<N>(sm.Ht, a.chunk_states + (int64_t)chunk * a.D * N, d0, a.D, tid, kThreads);
 
   const int d = d0 + lane;
   const bool valid = lane < bx && d < a.D;
-  float A2[N];
-#pragma unroll
-  for (int n = 0; n < N; ++n) A2[n] = valid ? __ldg(a.A + (int64_t)d * N + n) * kLog2e : 0.0f;
   const float bias = (valid && a.dt_bias) ? __ldg(a.dt_bias + d) : 0.0f;
   const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
 
@@ -139,6 +162,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
   const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
   __syncthreads();
+  float2 A2[P];
+  load_scaled_pairs<N>(A2, sm.At + lane * (N + 4), kLog2e);
 
   const int tb = s * kK;
   // ---- 1. per-token values (registers); lanes without a channel get u = g = 0
@@ -172,89 +197,97 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
   }
 
-  // ---- 2. forward aggregates, scan seeded with the saved chunk state
-  float h[N];
+  // ---- 2. both aggregates of my K tokens: forward (state from 0) and reverse
+  //         (carry leaving to the left when nothing enters from the right)
+  {
+    float2 h[P];
 #pragma unroll
-  for (int n = 0; n < N; ++n) h[n] = 0.0f;
-  float sd = 0.0f;
+    for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
+    float sd = 0.0f;
 #pragma unroll
-  for (int k = 0; k < kK; ++k) {
-    const int t = tb + k;
-    if (t >= rows) break;
-    if (rst & (1 << k)) {
+    for (int k = 0; k < kK; ++k) {
+      const int t = tb + k;
+      if (t >= rows) break;
+      if (rst & (1 << k)) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) h[n] = 0.0f;
-      sd = 0.0f;
+        for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
+        sd = 0.0f;
+      }
+      const float2 dl2 = splat2(dl[k]), du2 = splat2(dl[k] * uu[k]);
+      float2 Bv[P];
+      lds_pairs<N>(Bv, Bf + t * N);
+#pragma unroll
+      for (int i = 0; i < P; ++i) h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
+      sd += dl[k];
     }
-    const float du = dl[k] * uu[k];
-    float Bv[N];
-    lds_row<N>(Bv, Bf + t * N);
+    float2 q[P];
 #pragma unroll
-    for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dl[k] * A2[n]), h[n], du * Bv[n]);
-    sd += dl[k];
+    for (int i = 0; i < P; ++i) q[i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = kK - 1; k >= 0; --k) {
+      const int t = tb + k;
+      if (t >= rows) continue;
+      float2 Cv[P];
+      lds_pairs<N>(Cv, Cf + t * N);
+      // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
+      const float2 off2 = splat2((rst & (1 << k)) ? -INFINITY : 0.0f);
+      const float2 dl2 = splat2(dl[k]), g2 = splat2(g[k]);
+#pragma unroll
+      for (int i = 0; i < P; ++i) q[i] = mul2(ex2x2(fma2(dl2, A2[i], off2)), fma2(Cv[i], g2, q[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      sm.aggH[(s * N + 2 * i) * kTile + lane] = h[i].x;
+      sm.aggH[(s * N + 2 * i + 1) * kTile + lane] = h[i].y;
+      sm.aggG[(s * N + 2 * i) * kTile + lane] = q[i].x;
+      sm.aggG[(s * N + 2 * i + 1) * kTile + lane] = q[i].y;
+    }
+    sm.aggSD[s * kTile + lane] = sd;
+    if (lane == 0) sm.aggRS[s] = rst != 0;
   }
-#pragma unroll
-  for (int n = 0; n < N; ++n) sm.agg[(s * N + n) * kTile + lane] = h[n];
-  sm.aggSD[s * kTile + lane] = sd;
-  if (lane == 0) sm.aggRS[s] = rst != 0;
   __syncthreads();
-#pragma unroll
-  for (int n = 0; n < N; ++n) {
-    if (n % kS != s) continue;
-    float x = valid ? __ldg(a.chunk_states + ((int64_t)chunk * a.D + d) * N + n) : 0.0f;
+
+  // ---- 3. both in-CTA scans over the kS sub-chunks; chain (lane, n), n % kS == s.
+  //         Forward: exclusive prefix seeded with the saved state of the chunk.
+  //         Reverse: exclusive suffix with nothing entering from the right.
+  {
+    float sdj[kS];
+    int rsj[kS];
 #pragma unroll
     for (int j = 0; j < kS; ++j) {
-      float* slot = &sm.agg[(j * N + n) * kTile + lane];
-      const float Hj = *slot;
-      *slot = x;
-      const float P = sm.aggRS[j] ? 0.0f : ex2(A2[n] * sm.aggSD[j * kTile + lane]);
-      x = fmaf(P, x, Hj);
+      sdj[j] = sm.aggSD[j * kTile + lane];
+      rsj[j] = sm.aggRS[j];
     }
-  }
-  __syncthreads();
-  float hs[N];
-#pragma unroll
-  for (int n = 0; n < N; ++n) hs[n] = sm.agg[(s * N + n) * kTile + lane];
-  __syncthreads();
-
-  // ---- 3. reverse aggregates (carry out to the left when nothing comes in)
-  float dh[N];
-#pragma unroll
-  for (int n = 0; n < N; ++n) dh[n] = 0.0f;
-#pragma unroll
-  for (int k = kK - 1; k >= 0; --k) {
-    const int t = tb + k;
-    if (t >= rows) continue;
-    float Cv[N];
-    lds_row<N>(Cv, Cf + t * N);
-    // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
-    const float off = (rst & (1 << k)) ? -INFINITY : 0.0f;
 #pragma unroll
     for (int n = 0; n < N; ++n) {
-      const float at = ex2(fmaf(dl[k], A2[n], off));
-      dh[n] = at * fmaf(Cv[n], g[k], dh[n]);
+      if (n % kS != s) continue;
+      const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+      float Pj[kS], Hj[kS], Gj[kS];
+#pragma unroll
+      for (int j = 0; j < kS; ++j) {
+        Pj[j] = rsj[j] ? 0.0f : ex2(a2 * sdj[j]);
+        Hj[j] = sm.aggH[(j * N + n) * kTile + lane];
+        Gj[j] = sm.aggG[(j * N + n) * kTile + lane];
+      }
+      float x = sm.Ht[lane * (N + 4) + n];
+#pragma unroll
+      for (int j = 0; j < kS; ++j) {
+        sm.aggH[(j * N + n) * kTile + lane] = x;
+        x = fmaf(Pj[j], x, Hj[j]);
+      }
+      float y = 0.0f;
+#pragma unroll
+      for (int j = kS - 1; j >= 0; --j) {
+        sm.aggG[(j * N + n) * kTile + lane] = y;
+        y = fmaf(Pj[j], y, Gj[j]);
+      }
+      sm.tot[n * kTile + lane] = y;
     }
-  }
-#pragma unroll
-  for (int n = 0; n < N; ++n) sm.agg[(s * N + n) * kTile + lane] = dh[n];
-  __syncthreads();
-#pragma unroll
-  for (int n = 0; n < N; ++n) {
-    if (n % kS != s) continue;
-    float y = 0.0f;
-#pragma unroll
-    for (int j = kS - 1; j >= 0; --j) {
-      float* slot = &sm.agg[(j * N + n) * kTile + lane];
-      const float Gj = *slot;
-      *slot = y;
-      const float P = sm.aggRS[j] ? 0.0f : ex2(A2[n] * sm.aggSD[j * kTile + lane]);
-      y = fmaf(P, y, Gj);
-    }
-    sm.tot[n * kTile + lane] = y;
   }
   __syncthreads();
 
-  // ---- 4. decoupled look-back towards higher chunks (warp 0)
+  // ---- 4. decoupled look-back towards higher chunks (warp 0); the other warps
+  //         go straight on to step 5, which needs no carry from the right
   if (s == 0) {
     int rs_any = 0;
     float sd_tot = 0.0f;
@@ -268,35 +301,39 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const bool publish = (long long)tk != a.drop_ticket;
     float* my_agg = a.agg + slot * (N * kTile);
     float* my_inc = a.incl + slot * (N * kTile);
+    // every lane is its own chain (one channel): it publishes its payload and
+    // then its own flag with a release store, and readers acquire that flag
+    int* my_flag = a.flags + slot * kTile + lane;
     if (rs_any) {
 #pragma unroll
       for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.tot[n * kTile + lane];
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+      if (publish) st_release_gpu(my_flag, kFlagInclusive);
+    } else if (early) {
+      // carry already known: publish the inclusive carry straight away
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), sm.rin[n * kTile + lane], sm.tot[n * kTile + lane]);
+      }
+      if (publish) st_release_gpu(my_flag, kFlagInclusive);
     } else {
 #pragma unroll
       for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.tot[n * kTile + lane];
       a.agg_sd[slot * kTile + lane] = sd_tot;
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagAggregate);
+      if (publish) st_release_gpu(my_flag, kFlagAggregate);
     }
     float x[N];
 #pragma unroll
     for (int n = 0; n < N; ++n) x[n] = 0.0f;
-    if (chunk < a.n_chunks - 1) {
+    if (!early && chunk < a.n_chunks - 1) {
       int j = chunk + 1, found = -1, timed_out = 0;
       while (j < a.n_chunks) {
-        int f = 0;
-        if (lane == 0) f = wait_flag(a.flags + base + j, a.wait_ns);
-        f = __shfl_sync(0xffffffffu, f, 0);
+        const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
         if (f == kFlagInclusive) { found = j; break; }
         if (f == kFlagNone) { timed_out = 1; break; }
         ++j;
       }
-      __syncwarp();  // orders lane 0's acquire before every lane's payload reads
-      if (timed_out && lane == 0) atomicOr(a.status, kStatusLookbackTimeout);
+      if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int last = j - 1;
       if (found >= 0) {
         const float* inc = a.incl + (base + found) * (N * kTile);
@@ -308,27 +345,33 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         const float* ag = a.agg + (base + i) * (N * kTile);
         const float sdi = __ldcg(a.agg_sd + (base + i) * kTile + lane);
 #pragma unroll
-        for (int n = 0; n < N; ++n) x[n] = fmaf(ex2(A2[n] * sdi), x[n], __ldcg(ag + n * kTile + lane));
+        for (int n = 0; n < N; ++n) {
+          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+          x[n] = fmaf(ex2(a2 * sdi), x[n], __ldcg(ag + n * kTile + lane));
+        }
       }
     }
+    if (!early) {
 #pragma unroll
-    for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
-    if (!rs_any) {
+      for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
+      if (!rs_any) {
 #pragma unroll
-      for (int n = 0; n < N; ++n)
-        my_inc[n * kTile + lane] = fmaf(ex2(A2[n] * sd_tot), x[n], sm.tot[n * kTile + lane]);
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+        for (int n = 0; n < N; ++n) {
+          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+          my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.tot[n * kTile + lane]);
+        }
+        if (publish) st_release_gpu(my_flag, kFlagInclusive);
+      }
     }
   }
 
-  // ---- 5. recompute the forward states of my K tokens into shared memory; it
-  //         needs no carry from the right, so warps 1..7 do it while warp 0 is
-  //         still in the look-back above
-  float yk[kK];
+  // ---- 5. recompute the forward states of my K tokens from my start state;
+  //         the first K-1 go to shared memory, the last stays in registers
+  float2 h[P];
 #pragma unroll
-  for (int n = 0; n < N; ++n) h[n] = hs[n];
+  for (int i = 0; i < P; ++i)
+    h[i] = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
+  float yk[kK];
 #pragma unroll
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
@@ -336,26 +379,29 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (t >= rows) continue;
     if (rst & (1 << k)) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+      for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
     }
-    const float du = dl[k] * uu[k];
-    float Bv[N], Cv[N];
-    lds_row<N>(Bv, Bf + t * N);
-    lds_row<N>(Cv, Cf + t * N);
-    float y0 = 0.0f, y1 = 0.0f;
+    const float2 dl2 = splat2(dl[k]), du2 = splat2(dl[k] * uu[k]);
+    float2 Bv[P], Cv[P];
+    lds_pairs<N>(Bv, Bf + t * N);
+    lds_pairs<N>(Cv, Cf + t * N);
+    float2 y2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      h[n] = fmaf(ex2(dl[k] * A2[n]), h[n], du * Bv[n]);
-      if (n & 1) y1 = fmaf(Cv[n], h[n], y1); else y0 = fmaf(Cv[n], h[n], y0);
+    for (int i = 0; i < P; ++i) {
+      h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
+      y2 = fma2(Cv[i], h[i], y2);
     }
+    if (k < kK - 1) {
 #pragma unroll
-    for (int q = 0; q < N / 4; ++q)
-      sm.hist[(k * (N / 4) + q) * kThreads + tid] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    yk[k] = fmaf(Dsk, uu[k], y0 + y1);
+      for (int i = 0; i < P; i += 2)
+        sm.hist[(k * (N / 4) + i / 2) * kThreads + tid] = make_float4(h[i].x, h[i].y, h[i + 1].x, h[i + 1].y);
+    }
+    yk[k] = fmaf(Dsk, uu[k], y2.x + y2.y);
   }
   __syncthreads();
 
   // ---- 6. carry entering my last token from the right
+  float2 dh[P];
   {
     int rs_post = 0;
     float sd_post = 0.0f;
@@ -364,16 +410,18 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       sd_post += sm.aggSD[j * kTile + lane];
     }
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      const float E = sm.agg[(s * N + n) * kTile + lane];
-      dh[n] = rs_post ? E : fmaf(ex2(A2[n] * sd_post), sm.rin[n * kTile + lane], E);
+    for (int i = 0; i < P; ++i) {
+      const float2 E = make_float2(sm.aggG[(s * N + 2 * i) * kTile + lane],
+                                   sm.aggG[(s * N + 2 * i + 1) * kTile + lane]);
+      const float2 R = make_float2(sm.rin[(2 * i) * kTile + lane], sm.rin[(2 * i + 1) * kTile + lane]);
+      dh[i] = rs_post ? E : fma2(ex2x2(mul2(A2[i], splat2(sd_post))), R, E);
     }
   }
 
-  // reverse walk
-  float dA[N];
+  // ---- 7. reverse walk over my tokens
+  float2 dA[P];
 #pragma unroll
-  for (int n = 0; n < N; ++n) dA[n] = 0.0f;
+  for (int i = 0; i < P; ++i) dA[i] = make_float2(0.0f, 0.0f);
   float sDD = 0.0f, sDB = 0.0f;
   T* gdu = static_cast<T*>(a.du);
   T* gddr = static_cast<T*>(a.ddr);
@@ -382,36 +430,53 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int k = kK - 1; k >= 0; --k) {
     const int t = tb + k;
     if (t >= rows) continue;  // warp-uniform
-    float Bv[N], Cv[N];
-    lds_row<N>(Bv, Bf + t * N);
-    lds_row<N>(Cv, Cf + t * N);
-    const float off = (rst & (1 << k)) ? -INFINITY : 0.0f;
-    const float du = dl[k] * uu[k];
+    float2 Bv[P], Cv[P];
+    lds_pairs<N>(Bv, Bf + t * N);
+    lds_pairs<N>(Cv, Cf + t * N);
+    const float2 off2 = splat2((rst & (1 << k)) ? -INFINITY : 0.0f);
+    const float2 dl2 = splat2(dl[k]), g2 = splat2(g[k]), du2 = splat2(dl[k] * uu[k]);
     float v[V];
-    float s1 = 0.0f, s2 = 0.0f;
+    float2 s1 = make_float2(0.0f, 0.0f), s2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int q = 0; q < N / 4; ++q) {
-      const float4 hc4 = sm.hist[(k * (N / 4) + q) * kThreads + tid];
-      const float4 hp4 = k > 0 ? sm.hist[((k - 1) * (N / 4) + q) * kThreads + tid]
-                               : make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
-      const float hcur[4] = {hc4.x, hc4.y, hc4.z, hc4.w};
-      const float hprev[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
+    for (int i = 0; i < P; i += 2) {
+      float2 hc[2], hp[2];
+      if (k == kK - 1) {
+        hc[0] = h[i];
+        hc[1] = h[i + 1];
+      } else {
+        const float4 c4 = sm.hist[(k * (N / 4) + i / 2) * kThreads + tid];
+        hc[0] = make_float2(c4.x, c4.y);
+        hc[1] = make_float2(c4.z, c4.w);
+      }
+      if (k > 0) {
+        const float4 p4 = sm.hist[((k - 1) * (N / 4) + i / 2) * kThreads + tid];
+        hp[0] = make_float2(p4.x, p4.y);
+        hp[1] = make_float2(p4.z, p4.w);
+      } else {
+        hp[0] = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
+        hp[1] = make_float2(sm.aggH[(s * N + 2 * i + 2) * kTile + lane], sm.aggH[(s * N + 2 * i + 3) * kTile + lane]);
+      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int n = 4 * q + i;
-        dh[n] = fmaf(Cv[n], g[k], dh[n]);  // total gradient w.r.t. h_t
-        const float at = ex2(fmaf(dl[k], A2[n], off));
-        const float dhq = dh[n] * (at * hprev[i]);
-        dA[n] = fmaf(dl[k], dhq, dA[n]);
-        s2 = fmaf(A2[n], dhq, s2);
-        s1 = fmaf(dh[n], Bv[n], s1);
-        v[n] = dh[n] * du;               // 0 on lanes without a channel (u = 0)
-        v[N + n] = g[k] * hcur[i];       // 0 on lanes without a channel (g = 0)
-        dh[n] *= at;                     // carry to h_{t-1}
+      for (int e = 0; e < 2; ++e) {
+        const int j = i + e;
+        dh[j] = fma2(Cv[j], g2, dh[j]);  // total gradient w.r.t. h_t
+        const float2 at = ex2x2(fma2(dl2, A2[j], off2));
+        const float2 dhq = mul2(dh[j], mul2(at, hp[e]));
+        dA[j] = fma2(dl2, dhq, dA[j]);
+        s2 = fma2(A2[j], dhq, s2);
+        s1 = fma2(dh[j], Bv[j], s1);
+        const float2 vb = mul2(dh[j], du2);   // 0 on lanes without a channel (u = 0)
+        const float2 vc = mul2(g2, hc[e]);    // 0 on lanes without a channel (g = 0)
+        v[2 * j] = vb.x;
+        v[2 * j + 1] = vb.y;
+        v[N + 2 * j] = vc.x;
+        v[N + 2 * j + 1] = vc.y;
+        dh[j] = mul2(dh[j], at);               // carry to h_{t-1}
       }
     }
-    const float gdu_t = fmaf(dl[k], s1, Dsk * g[k]);
-    const float gdl_t = fmaf(uu[k], s1, s2 * kLn2);
+    const float s1t = s1.x + s1.y, s2t = s2.x + s2.y;
+    const float gdu_t = fmaf(dl[k], s1t, Dsk * g[k]);
+    const float gdl_t = fmaf(uu[k], s1t, s2t * kLn2);
     const float gdr_t = gdl_t * sg[k];
     sDD = fmaf(g[k], uu[k], sDD);
     sDB += gdr_t;
@@ -426,10 +491,13 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       a.part_dBC[((int64_t)tile * a.T + t0 + t) * V + lane / kRep] = v[0];
   }
 
-  // ---- 6. fixed-order CTA reduction of dA, dDskip, d_dt_bias partials
+  // ---- 8. fixed-order CTA reduction of dA, dDskip, d_dt_bias partials
   __syncthreads();
 #pragma unroll
-  for (int n = 0; n < N; ++n) sm.agg[(s * N + n) * kTile + lane] = dA[n];
+  for (int i = 0; i < P; ++i) {
+    sm.aggH[(s * N + 2 * i) * kTile + lane] = dA[i].x;
+    sm.aggH[(s * N + 2 * i + 1) * kTile + lane] = dA[i].y;
+  }
   sm.redD[s * kTile + lane] = sDD;
   sm.redB[s * kTile + lane] = sDB;
   __syncthreads();
@@ -438,8 +506,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (n % kS != s) continue;
     float acc = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kS; ++j) acc += sm.agg[(j * N + n) * kTile + lane];
-    if (valid) a.part_dA[((int64_t)chunk * a.D + d) * N + n] = acc;
+    for (int j = 0; j < kS; ++j) acc += sm.aggH[(j * N + n) * kTile + lane];
+    sm.At[lane * (N + 4) + n] = acc;   // A is no longer needed: reuse its rows
   }
   if (s == 0 && valid) {
     float accD = 0.0f, accB = 0.0f;
@@ -450,6 +518,13 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     a.part_dD[(int64_t)chunk * a.D + d] = accD;
     a.part_dbias[(int64_t)chunk * a.D + d] = accB;
+  }
+  __syncthreads();
+  // the tile's dA partial block is contiguous in part_dA: write it coalesced
+  {
+    float* dst = a.part_dA + ((int64_t)chunk * a.D + d0) * N;
+    const int nvalid = (a.D - d0 < kTile ? a.D - d0 : kTile) * N;
+    for (int i = tid; i < nvalid; i += kThreads) dst[i] = sm.At[(i / N) * (N + 4) + (i % N)];
   }
 }
 

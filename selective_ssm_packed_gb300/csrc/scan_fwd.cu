@@ -52,6 +52,7 @@ struct FwdSmem {
   float totH[N * kTile];
   float hin[N * kTile];
   float aggSD[kS * kTile];
+  alignas(16) float At[kTile * (N + 4)];  // A rows of the tile, padded for conflict-free 16-byte reads
   int pos[kL];
   int aggRS[kS];
   int ticket;
@@ -92,12 +93,30 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     bulk_load_1d(sm.C, static_cast<const T*>(a.C) + t0 * N, bc, &sm.bar);
   }
   for (int i = tid; i < kL; i += kThreads) sm.pos[i] = (i < rows) ? __ldg(a.pos + t0 + i) : 1;
+  stage_rows<N>(sm.At, a.A, d0, a.D, tid, kThreads);
+  // Early look-back (warp 0, while the tiles are in flight): the state entering
+  // this chunk does not depend on this chunk's data, and the previous chunk of
+  // the tile has usually published its inclusive state already.  Take it now if
+  // it is there (or if a sequence starts at this chunk's first token); otherwise
+  // step 5 does the full look-back.
+  int early = 0;
+  if (s == 0) {
+    const int64_t base = (int64_t)tile * a.n_chunks;
+    if (chunk == 0 || __ldg(a.pos + t0) == 0) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = 0.0f;
+      early = 1;
+    } else if (ld_acquire_gpu(a.flags + (base + chunk - 1) * kTile + lane) == kFlagInclusive) {
+      const float* inc = a.incl + (base + chunk - 1) * (N * kTile);
+#pragma unroll
+      for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = __ldcg(inc + n * kTile + lane);
+      early = 1;
+    }
+  }
 
   const int d = d0 + lane;
   const bool valid = lane < bx && d < a.D;
-  float A2[N];
-#pragma unroll
-  for (int n = 0; n < N; ++n) A2[n] = valid ? __ldg(a.A + (int64_t)d * N + n) * kLog2e : 0.0f;
+  constexpr int P = N / 2;  // state pairs
   const float bias = (valid && a.dt_bias) ? __ldg(a.dt_bias + d) : 0.0f;
   const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
 
@@ -105,6 +124,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
   const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
   __syncthreads();
+  float2 A2[P];
+  load_scaled_pairs<N>(A2, sm.At + lane * (N + 4), kLog2e);
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
   // ---- step 2: delta for my tokens
@@ -116,9 +137,9 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
 
   // ---- step 3: pass 1, sub-chunk aggregate from h = 0
-  float h[N];
+  float2 h[P];
 #pragma unroll
-  for (int n = 0; n < N; ++n) h[n] = 0.0f;
+  for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
   float sd = 0.0f;
   int rs = 0;
 #pragma unroll
@@ -127,38 +148,54 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (t >= rows) break;
     if (sm.pos[t] == 0) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+      for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
       sd = 0.0f;
       rs = 1;
     }
     const float dl = sm.dlt[t * kTile + lane];
-    const float du = dl * to_f(sm.u[t * bx + lane]);
-    float Bv[N];
-    lds_row<N>(Bv, Bf + t * N);
+    const float2 dl2 = splat2(dl), du2 = splat2(dl * to_f(sm.u[t * bx + lane]));
+    float2 Bv[P];
+    lds_pairs<N>(Bv, Bf + t * N);
 #pragma unroll
-    for (int n = 0; n < N; ++n) h[n] = fmaf(ex2(dl * A2[n]), h[n], du * Bv[n]);
+    for (int i = 0; i < P; ++i) h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
     sd += dl;
   }
 #pragma unroll
-  for (int n = 0; n < N; ++n) sm.aggH[(s * N + n) * kTile + lane] = h[n];
+  for (int i = 0; i < P; ++i) {
+    sm.aggH[(s * N + 2 * i) * kTile + lane] = h[i].x;
+    sm.aggH[(s * N + 2 * i + 1) * kTile + lane] = h[i].y;
+  }
   sm.aggSD[s * kTile + lane] = sd;
   if (lane == 0) sm.aggRS[s] = rs;
   __syncthreads();
 
   // ---- step 4: exclusive scan over sub-chunks; chain (lane, n) with n % kS == s
-#pragma unroll
-  for (int n = 0; n < N; ++n) {
-    if (n % kS != s) continue;
-    float x = 0.0f;
+  {
+    float sdj[kS];
+    int rsj[kS];
 #pragma unroll
     for (int j = 0; j < kS; ++j) {
-      float* slot = &sm.aggH[(j * N + n) * kTile + lane];
-      const float Hj = *slot;
-      *slot = x;
-      const float P = sm.aggRS[j] ? 0.0f : ex2(A2[n] * sm.aggSD[j * kTile + lane]);
-      x = fmaf(P, x, Hj);
+      sdj[j] = sm.aggSD[j * kTile + lane];
+      rsj[j] = sm.aggRS[j];
     }
-    sm.totH[n * kTile + lane] = x;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      if (n % kS != s) continue;
+      const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+      float Pj[kS], Hj[kS];
+#pragma unroll
+      for (int j = 0; j < kS; ++j) {
+        Pj[j] = rsj[j] ? 0.0f : ex2(a2 * sdj[j]);
+        Hj[j] = sm.aggH[(j * N + n) * kTile + lane];
+      }
+      float x = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kS; ++j) {
+        sm.aggH[(j * N + n) * kTile + lane] = x;
+        x = fmaf(Pj[j], x, Hj[j]);
+      }
+      sm.totH[n * kTile + lane] = x;
+    }
   }
   __syncthreads();
 
@@ -175,37 +212,41 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const bool publish = (long long)tk != a.drop_ticket;
     float* my_agg = a.agg + slot * (N * kTile);
     float* my_inc = a.incl + slot * (N * kTile);
+    // every lane is its own chain (one channel): it publishes its payload and
+    // then its own flag with a release store, and readers acquire that flag
+    int* my_flag = a.flags + slot * kTile + lane;
     if (rs_any) {
 #pragma unroll
       for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.totH[n * kTile + lane];
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+      if (publish) st_release_gpu(my_flag, kFlagInclusive);
+    } else if (early) {
+      // entering state already known: publish the inclusive state straight away
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), sm.hin[n * kTile + lane], sm.totH[n * kTile + lane]);
+      }
+      if (publish) st_release_gpu(my_flag, kFlagInclusive);
     } else {
 #pragma unroll
       for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.totH[n * kTile + lane];
       a.agg_sd[slot * kTile + lane] = sd_tot;
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagAggregate);
+      if (publish) st_release_gpu(my_flag, kFlagAggregate);
     }
 
     float x[N];
 #pragma unroll
     for (int n = 0; n < N; ++n) x[n] = 0.0f;
-    if (chunk > 0 && sm.pos[0] != 0) {
+    if (!early) {
       const int64_t base = (int64_t)tile * a.n_chunks;
       int j = chunk - 1, found = -1, timed_out = 0;
       while (j >= 0) {
-        int f = 0;
-        if (lane == 0) f = wait_flag(a.flags + base + j, a.wait_ns);
-        f = __shfl_sync(0xffffffffu, f, 0);
+        const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
         if (f == kFlagInclusive) { found = j; break; }
         if (f == kFlagNone) { timed_out = 1; break; }
         --j;
       }
-      __syncwarp();  // orders lane 0's acquire before every lane's payload reads
-      if (timed_out && lane == 0) atomicOr(a.status, kStatusLookbackTimeout);
+      if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int first = j + 1;
       if (found >= 0) {
         const float* inc = a.incl + (base + found) * (N * kTile);
@@ -217,18 +258,23 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         const float* ag = a.agg + (base + i) * (N * kTile);
         const float sdi = __ldcg(a.agg_sd + (base + i) * kTile + lane);
 #pragma unroll
-        for (int n = 0; n < N; ++n) x[n] = fmaf(ex2(A2[n] * sdi), x[n], __ldcg(ag + n * kTile + lane));
+        for (int n = 0; n < N; ++n) {
+          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+          x[n] = fmaf(ex2(a2 * sdi), x[n], __ldcg(ag + n * kTile + lane));
+        }
       }
     }
+    if (!early) {
 #pragma unroll
-    for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = x[n];
-    if (!rs_any) {
+      for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = x[n];
+      if (!rs_any) {
 #pragma unroll
-      for (int n = 0; n < N; ++n)
-        my_inc[n * kTile + lane] = fmaf(ex2(A2[n] * sd_tot), x[n], sm.totH[n * kTile + lane]);
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish) st_release_gpu(a.flags + slot, kFlagInclusive);
+        for (int n = 0; n < N; ++n) {
+          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+          my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.totH[n * kTile + lane]);
+        }
+        if (publish) st_release_gpu(my_flag, kFlagInclusive);
+      }
     }
   }
   __syncthreads();
@@ -241,16 +287,17 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     sd_pre += sm.aggSD[j * kTile + lane];
   }
 #pragma unroll
-  for (int n = 0; n < N; ++n) {
-    const float E = sm.aggH[(s * N + n) * kTile + lane];
-    h[n] = rs_pre ? E : fmaf(ex2(A2[n] * sd_pre), sm.hin[n * kTile + lane], E);
+  for (int i = 0; i < P; ++i) {
+    const float2 E = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
+    const float2 R = make_float2(sm.hin[(2 * i) * kTile + lane], sm.hin[(2 * i + 1) * kTile + lane]);
+    h[i] = rs_pre ? E : fma2(ex2x2(mul2(A2[i], splat2(sd_pre))), R, E);
   }
   const int64_t ts = t0 + tb;
   if (a.chunk_states && valid && ts < a.T && (ts % kStateChunk) == 0) {
     float* cs = a.chunk_states + ((ts / kStateChunk) * a.D + d) * N;
 #pragma unroll
-    for (int n = 0; n < N; n += 4)
-      *reinterpret_cast<float4*>(cs + n) = make_float4(h[n], h[n + 1], h[n + 2], h[n + 3]);
+    for (int i = 0; i < P; i += 2)
+      *reinterpret_cast<float4*>(cs + 2 * i) = make_float4(h[i].x, h[i].y, h[i + 1].x, h[i + 1].y);
   }
 
   T* out = static_cast<T*>(a.out);
@@ -260,21 +307,21 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (t >= rows) break;
     if (sm.pos[t] == 0) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+      for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
     }
     const float dl = sm.dlt[t * kTile + lane];
     const float uu = to_f(sm.u[t * bx + lane]);
-    const float du = dl * uu;
-    float Bv[N], Cv[N];
-    lds_row<N>(Bv, Bf + t * N);
-    lds_row<N>(Cv, Cf + t * N);
-    float y0 = 0.0f, y1 = 0.0f;
+    const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+    float2 Bv[P], Cv[P];
+    lds_pairs<N>(Bv, Bf + t * N);
+    lds_pairs<N>(Cv, Cf + t * N);
+    float2 y2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      h[n] = fmaf(ex2(dl * A2[n]), h[n], du * Bv[n]);
-      if (n & 1) y1 = fmaf(Cv[n], h[n], y1); else y0 = fmaf(Cv[n], h[n], y0);
+    for (int i = 0; i < P; ++i) {
+      h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
+      y2 = fma2(Cv[i], h[i], y2);
     }
-    float y = fmaf(Dsk, uu, y0 + y1);
+    float y = fmaf(Dsk, uu, y2.x + y2.y);
     if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane]));
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
   }
