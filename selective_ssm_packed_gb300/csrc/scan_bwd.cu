@@ -133,24 +133,6 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   if (tid < kL) sm.pos[tid] = (tid < rows) ? __ldg(a.pos + t0 + tid) : 1;
   stage_rows<N>(sm.At, a.A, d0, a.D, tid, kThreads);
-  // Early look-back (warp 0, while the tiles are in flight): the carry entering
-  // this chunk from the right does not depend on this chunk's data, and the
-  // next chunk of the tile has usually published its inclusive carry already.
-  // Take it now if it is there; otherwise step 4 does the full look-back.
-  int early = 0;
-  if (s == 0) {
-    const int64_t base = (int64_t)tile * a.n_chunks;
-    if (chunk == a.n_chunks - 1) {
-#pragma unroll
-      for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = 0.0f;
-      early = 1;
-    } else if (ld_acquire_gpu(a.flags + (base + chunk + 1) * kTile + lane) == kFlagInclusive) {
-      const float* inc = a.incl + (base + chunk + 1) * (N * kTile);
-#pragma unroll
-      for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = __ldcg(inc + n * kTile + lane);
-      early = 1;
-    }
-  }
   stage_rows<N>(sm.Ht, a.chunk_states + (int64_t)chunk * a.D * N, d0, a.D, tid, kThreads);
 
   const int d = d0 + lane;
@@ -288,6 +270,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
   // ---- 4. decoupled look-back towards higher chunks (warp 0); the other warps
   //         go straight on to step 5, which needs no carry from the right
+  bool release_incl = false;  // warp 0: inclusive carry stored, flag not yet released
   if (s == 0) {
     int rs_any = 0;
     float sd_tot = 0.0f;
@@ -305,33 +288,35 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // then its own flag with a release store, and readers acquire that flag
     int* my_flag = a.flags + slot * kTile + lane;
     if (rs_any) {
+      // a sequence starts in this chunk: the carry leaving it to the left does
+      // not depend on what enters from the right, publish it at once
 #pragma unroll
       for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.tot[n * kTile + lane];
       if (publish) st_release_gpu(my_flag, kFlagInclusive);
-    } else if (early) {
-      // carry already known: publish the inclusive carry straight away
-#pragma unroll
-      for (int n = 0; n < N; ++n) {
-        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), sm.rin[n * kTile + lane], sm.tot[n * kTile + lane]);
-      }
-      if (publish) st_release_gpu(my_flag, kFlagInclusive);
-    } else {
-#pragma unroll
-      for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.tot[n * kTile + lane];
-      a.agg_sd[slot * kTile + lane] = sd_tot;
-      if (publish) st_release_gpu(my_flag, kFlagAggregate);
     }
     float x[N];
 #pragma unroll
     for (int n = 0; n < N; ++n) x[n] = 0.0f;
-    if (!early && chunk < a.n_chunks - 1) {
+    if (chunk < a.n_chunks - 1) {
+      // the next chunk of the tile started long before this one and has
+      // usually published its inclusive carry: look first, and publish this
+      // chunk's aggregate only when the walk has to go further
       int j = chunk + 1, found = -1, timed_out = 0;
-      while (j < a.n_chunks) {
-        const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
-        if (f == kFlagInclusive) { found = j; break; }
-        if (f == kFlagNone) { timed_out = 1; break; }
-        ++j;
+      if (ld_acquire_gpu(a.flags + (base + j) * kTile + lane) == kFlagInclusive) {
+        found = j;
+      } else {
+        if (!rs_any) {
+#pragma unroll
+          for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.tot[n * kTile + lane];
+          a.agg_sd[slot * kTile + lane] = sd_tot;
+          if (publish) st_release_gpu(my_flag, kFlagAggregate);
+        }
+        while (j < a.n_chunks) {
+          const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
+          if (f == kFlagInclusive) { found = j; break; }
+          if (f == kFlagNone) { timed_out = 1; break; }
+          ++j;
+        }
       }
       if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int last = j - 1;
@@ -351,17 +336,17 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         }
       }
     }
-    if (!early) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
-      if (!rs_any) {
+    for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
+    if (!rs_any) {
+      // payload now; its flag is released after step 5, by which time these
+      // stores have drained and the release costs little
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-          my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.tot[n * kTile + lane]);
-        }
-        if (publish) st_release_gpu(my_flag, kFlagInclusive);
+      for (int n = 0; n < N; ++n) {
+        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.tot[n * kTile + lane]);
       }
+      release_incl = publish;
     }
   }
 
@@ -398,6 +383,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     yk[k] = fmaf(Dsk, uu[k], y2.x + y2.y);
   }
+  if (release_incl)
+    st_release_gpu(a.flags + ((int64_t)tile * a.n_chunks + chunk) * kTile + lane, kFlagInclusive);
   __syncthreads();
 
   // ---- 6. carry entering my last token from the right

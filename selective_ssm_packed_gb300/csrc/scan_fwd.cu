@@ -94,25 +94,6 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   for (int i = tid; i < kL; i += kThreads) sm.pos[i] = (i < rows) ? __ldg(a.pos + t0 + i) : 1;
   stage_rows<N>(sm.At, a.A, d0, a.D, tid, kThreads);
-  // Early look-back (warp 0, while the tiles are in flight): the state entering
-  // this chunk does not depend on this chunk's data, and the previous chunk of
-  // the tile has usually published its inclusive state already.  Take it now if
-  // it is there (or if a sequence starts at this chunk's first token); otherwise
-  // step 5 does the full look-back.
-  int early = 0;
-  if (s == 0) {
-    const int64_t base = (int64_t)tile * a.n_chunks;
-    if (chunk == 0 || __ldg(a.pos + t0) == 0) {
-#pragma unroll
-      for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = 0.0f;
-      early = 1;
-    } else if (ld_acquire_gpu(a.flags + (base + chunk - 1) * kTile + lane) == kFlagInclusive) {
-      const float* inc = a.incl + (base + chunk - 1) * (N * kTile);
-#pragma unroll
-      for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = __ldcg(inc + n * kTile + lane);
-      early = 1;
-    }
-  }
 
   const int d = d0 + lane;
   const bool valid = lane < bx && d < a.D;
@@ -200,6 +181,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   __syncthreads();
 
   // ---- step 5: decoupled look-back (warp 0)
+  bool release_incl = false;  // warp 0: inclusive state stored, flag not yet released
   if (s == 0) {
     int rs_any = 0;
     float sd_tot = 0.0f;
@@ -216,35 +198,37 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // then its own flag with a release store, and readers acquire that flag
     int* my_flag = a.flags + slot * kTile + lane;
     if (rs_any) {
+      // a sequence starts in this chunk: the state leaving it does not depend
+      // on the state entering, publish it at once
 #pragma unroll
       for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.totH[n * kTile + lane];
       if (publish) st_release_gpu(my_flag, kFlagInclusive);
-    } else if (early) {
-      // entering state already known: publish the inclusive state straight away
-#pragma unroll
-      for (int n = 0; n < N; ++n) {
-        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), sm.hin[n * kTile + lane], sm.totH[n * kTile + lane]);
-      }
-      if (publish) st_release_gpu(my_flag, kFlagInclusive);
-    } else {
-#pragma unroll
-      for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.totH[n * kTile + lane];
-      a.agg_sd[slot * kTile + lane] = sd_tot;
-      if (publish) st_release_gpu(my_flag, kFlagAggregate);
     }
-
     float x[N];
 #pragma unroll
     for (int n = 0; n < N; ++n) x[n] = 0.0f;
-    if (!early) {
+    // no entering state is needed when a sequence starts at the first token
+    if (chunk > 0 && sm.pos[0] != 0) {
+      // the previous chunk of the tile started long before this one and has
+      // usually published its inclusive state: look first, and publish this
+      // chunk's aggregate only when the walk has to go further
       const int64_t base = (int64_t)tile * a.n_chunks;
       int j = chunk - 1, found = -1, timed_out = 0;
-      while (j >= 0) {
-        const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
-        if (f == kFlagInclusive) { found = j; break; }
-        if (f == kFlagNone) { timed_out = 1; break; }
-        --j;
+      if (ld_acquire_gpu(a.flags + (base + j) * kTile + lane) == kFlagInclusive) {
+        found = j;
+      } else {
+        if (!rs_any) {
+#pragma unroll
+          for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.totH[n * kTile + lane];
+          a.agg_sd[slot * kTile + lane] = sd_tot;
+          if (publish) st_release_gpu(my_flag, kFlagAggregate);
+        }
+        while (j >= 0) {
+          const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
+          if (f == kFlagInclusive) { found = j; break; }
+          if (f == kFlagNone) { timed_out = 1; break; }
+          --j;
+        }
       }
       if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int first = j + 1;
@@ -264,20 +248,21 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         }
       }
     }
-    if (!early) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = x[n];
-      if (!rs_any) {
+    for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = x[n];
+    if (!rs_any) {
+      // payload now, flag after the barrier below, when these stores have drained
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-          my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.totH[n * kTile + lane]);
-        }
-        if (publish) st_release_gpu(my_flag, kFlagInclusive);
+      for (int n = 0; n < N; ++n) {
+        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.totH[n * kTile + lane]);
       }
+      release_incl = publish;
     }
   }
   __syncthreads();
+  if (release_incl)
+    st_release_gpu(a.flags + ((int64_t)tile * a.n_chunks + chunk) * kTile + lane, kFlagInclusive);
 
   // ---- step 6: exact start state, pass 2
   int rs_pre = 0;
