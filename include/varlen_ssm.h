@@ -23,8 +23,10 @@
  *           and bias) and their gradients are always float32.  All arithmetic,
  *           the scan state and every accumulation are float32; bf16 results are
  *           rounded to nearest-even once, at the store.
- * Pointers  Every data pointer is a DEVICE pointer.  (T, D) tensors, B, C and
- *           the workspace must be 16-byte aligned and D * sizeof(io) and
+ * Pointers  Every data pointer is a DEVICE pointer.  (T, D) tensors, B, C,
+ *           the workspace and, for the scan calls, A, Dskip, dt_bias,
+ *           chunk_states and position_indices must be 16-byte aligned (the
+ *           kernels fetch them with bulk copies), and D * sizeof(io) and
  *           N * sizeof(io) must be multiples of 16; otherwise the call returns
  *           VSSM_ERR_ALIGN without launching (there is no slow fallback).
  * Ownership The caller allocates and frees everything: inputs, outputs,

@@ -336,8 +336,13 @@ size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, 
 }
 
 static int scan_common(const void* u, const void* delta_raw, const float* A, const void* B,
-                       const void* C, const void* z, const int32_t* cu, int32_t num_seqs,
+                       const void* C, const void* z, const float* Dskip, const float* dt_bias,
+                       const int32_t* pos, const int32_t* cu, int32_t num_seqs,
                        int64_t T, int32_t D, int32_t N, vssm_dtype dtype, IO* io) {
+  // the kernels copy these with 16-byte bulk copies
+  if (Dskip && !aligned16(Dskip)) return fail(VSSM_ERR_ALIGN, "Dskip is not 16-byte aligned");
+  if (dt_bias && !aligned16(dt_bias)) return fail(VSSM_ERR_ALIGN, "dt_bias is not 16-byte aligned");
+  if (pos && !aligned16(pos)) return fail(VSSM_ERR_ALIGN, "position_indices is not 16-byte aligned");
   VSSM_TRY(check_dtype(dtype, io));
   VSSM_TRY(check_shape(T, D, num_seqs, cu));
   if (N != 4 && N != 8 && N != 16) return fail(VSSM_ERR_UNSUPPORTED, "N = %d not in {4, 8, 16}", N);
@@ -347,6 +352,7 @@ static int scan_common(const void* u, const void* delta_raw, const float* A, con
   if ((N * e) % 16 != 0)
     return fail(VSSM_ERR_ALIGN, "N * sizeof(io) = %d is not a multiple of 16", N * e);
   if (!A) return fail(VSSM_ERR_ARG, "A is NULL");
+  if (!aligned16(A)) return fail(VSSM_ERR_ALIGN, "A is not 16-byte aligned");
   VSSM_TRY(check_io(u, "u", T));
   VSSM_TRY(check_io(delta_raw, "delta_raw", T));
   VSSM_TRY(check_io(B, "B", T));
@@ -363,7 +369,8 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
                               vssm_dtype dtype, void* out, float* chunk_states,
                               void* workspace, size_t workspace_bytes, void* stream) {
   IO io;
-  VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, cu_seqlens, num_seqs, total_tokens, D, N, dtype, &io));
+  VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
+                        num_seqs, total_tokens, D, N, dtype, &io));
   VSSM_TRY(check_io(out, "out", total_tokens));
   if (chunk_states && !aligned16(chunk_states))
     return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
@@ -414,7 +421,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream) {
   IO io;
-  VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, cu_seqlens, num_seqs, total_tokens, D, N, dtype, &io));
+  VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
+                        num_seqs, total_tokens, D, N, dtype, &io));
   const int64_t T = total_tokens;
   VSSM_TRY(check_io(dout, "dout", T));
   VSSM_TRY(check_io(du, "du", T));

@@ -143,6 +143,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Arrival without data (completes the phase once every expected byte is in).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -227,6 +232,21 @@ __device__ __forceinline__ const float* widen_rows(const T* src, float* dst, int
     for (int i = tid; i < count / 2; i += nthreads) d2[i] = __bfloat1622float2(s2[i]);
     return dst;
   }
+}
+
+// ------------------------------------------------------------------ launch shape
+// Grid of a persistent kernel: as many CTAs as fit on the device at once (all
+// SMs x resident CTAs per SM), never more than there are work items.
+template <typename K>
+inline cudaError_t persistent_grid(K kernel, int threads, size_t smem, int64_t items, int* grid) {
+  int dev = 0, n_sm = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t cap = (int64_t)(per_sm > 0 ? per_sm : 1) * (n_sm > 0 ? n_sm : 1);
+  *grid = (int)(items < cap ? items : cap);
+  return cudaSuccess;
 }
 
 }  // namespace vssm

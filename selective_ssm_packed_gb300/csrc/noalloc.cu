@@ -140,8 +140,10 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
       if (!al16(p)) return record_error(VSSM_ERR_ALIGN, "u, delta_raw, B, C, out must be 16-byte aligned");
     }
   }
-  if ((z && !al16(z)) || (chunk_states && !al16(chunk_states)))
-    return record_error(VSSM_ERR_ALIGN, "z and chunk_states must be 16-byte aligned");
+  if ((z && !al16(z)) || (chunk_states && !al16(chunk_states)) || !al16(A) || (Dskip && !al16(Dskip)) ||
+      (dt_bias && !al16(dt_bias)) || (position_indices && !al16(position_indices)))
+    return record_error(VSSM_ERR_ALIGN,
+                        "z, chunk_states, A, Dskip, dt_bias and position_indices must be 16-byte aligned");
 
   // ---- scratch layout: [header: status, ticket][flags][pos][agg][agg_sd][incl]
   const int64_t n_tiles = cdiv(D, kTile), n_chunks = cdiv(T, kFwdChunk);

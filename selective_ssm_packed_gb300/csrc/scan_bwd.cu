@@ -3,16 +3,20 @@
 // Work item = (chunk of kBwdChunk = 32 tokens, the saved-state granule) x
 // (tile of kTile = 32 channels); items are taken in DESCENDING chunk order
 // from an atomic ticket because the state gradient flows from the end of a
-// sequence to its start.  CTA = 8 warps; warp s owns K = 4 tokens, lane l owns
-// channel d0 + l with all N states.
+// sequence to its start.  The kernel is persistent (one CTA per resident slot,
+// looping over tickets); each item's inputs are requested by one thread with
+// tensor / bulk copies on one mbarrier while the previous item finishes.
+// CTA = 8 warps; warp s owns K = 4 tokens, lane l owns channel d0 + l with
+// all N states.
 //
 // With a_t = exp(delta_t A) (0 at a sequence start), g_t = dout_t SiLU(z_t),
 // the state gradient obeys dh_t = a_{t+1} dh_{t+1} + C_t g_t and is zero after
 // the last token of every sequence (a_{t+1} = 0 when t+1 starts a sequence):
 // the reverse scan that resets at sequence ends.
 //
-//   1. TMA: u, delta_raw, dout, z tiles (32 x 32), B and C rows; per-token
-//      delta, SiLU(z), g kept in registers.
+//   1. Copies (issued during the previous item): u, delta_raw, dout, z tiles
+//      (32 x 32), B and C rows, A rows, dt_bias, Dskip, saved states,
+//      position indices; per-token delta, SiLU(z), g kept in registers.
 //   2. Forward states: pass over the K tokens from h = 0 -> sub-chunk
 //      aggregates; exclusive scan seeded with the chunk's saved state
 //      (chunk_states from the forward call) gives each thread its start state.
@@ -43,12 +47,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T, int N>
 struct BwdSmem {
+  // ---- inputs of one work item, written by tensor / bulk copies and refilled
+  //      for the next item while this one is still being processed
   alignas(128) T u[kL * kTile];
   alignas(128) T dr[kL * kTile];
   alignas(128) T z[kL * kTile];
   alignas(128) T dout[kL * kTile];
   alignas(128) T B[kL * N];
   alignas(128) T C[kL * N];
+  alignas(16) float Araw[kTile * N];   // A rows d0 .. d0+31
+  alignas(16) float Hraw[kTile * N];   // saved states at the chunk start, same rows
+  alignas(16) float bias[kTile];
+  alignas(16) float dsk[kTile];
+  alignas(16) int pos[kL];
+  // ---- working set of the item being processed
   // B and C widened to fp32 once per work item (bf16 I/O only; fp32 I/O reads B, C directly)
   alignas(16) float Bf[sizeof(T) == 2 ? kL * N : 4];
   alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
@@ -56,15 +68,12 @@ struct BwdSmem {
   // its last token stays in registers
   alignas(16) float4 hist[(kK - 1) * (N / 4) * kThreads];
   alignas(16) float aggH[kS * N * kTile];  // forward aggregates, then each warp's start state
-  alignas(16) float aggG[kS * N * kTile];  // reverse aggregates, then exclusive suffixes
+  alignas(16) float aggG[kS * N * kTile];  // reverse aggregates, then exclusive suffixes, then the dA block
   float tot[N * kTile];
   float rin[N * kTile];
   float aggSD[kS * kTile];
   float redD[kS * kTile];
   float redB[kS * kTile];
-  alignas(16) float At[kTile * (N + 4)];  // A rows of the tile (padded), later the dA partial block
-  alignas(16) float Ht[kTile * (N + 4)];  // saved states of the chunk for the tile's channels
-  int pos[kL];
   int aggRS[kS];
   int ticket;
   alignas(8) uint64_t bar;
@@ -105,47 +114,84 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, s = tid >> 5;
 
+  const int n_items = a.n_chunks * a.n_tiles;
+
+  // Requests every input of work item `tkn` on the barrier: u, delta_raw,
+  // dout, z tiles; B and C rows; A rows, dt_bias, Dskip and the saved states
+  // of the tile's channels; position indices (whole groups of 4 tokens).
+  auto issue = [&](int tkn) {
+    const int rv = tkn / a.n_tiles;
+    const int tl = tkn - rv * a.n_tiles;
+    const int ch = a.n_chunks - 1 - rv;
+    const int64_t tt0 = (int64_t)ch * kL;
+    const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
+    const int dd0 = tl * kTile;
+    const uint32_t nval = (uint32_t)(a.D - dd0 < kTile ? a.D - dd0 : kTile);
+    const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
+    const uint32_t rows4 = (uint32_t)nrows & ~3u;
+    const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
+    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 4u : 3u) + 2u * bc + 2u * nval * N * 4u +
+                                       rows4 * 4u + (a.dt_bias ? nval * 4u : 0u) +
+                                       (a.Dskip ? nval * 4u : 0u));
+    tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+    tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
+    tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
+    if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
+    bulk_load_1d(sm.Hraw, a.chunk_states + ((int64_t)ch * a.D + dd0) * N, nval * N * 4u, &sm.bar);
+    if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
+    if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
+    if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
+  };
+
   if (tid == 0) {
-    sm.ticket = (int)atomicAdd(a.ticket, 1u);
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
+    const int first = (int)atomicAdd(a.ticket, 1u);
+    sm.ticket = first;
+    if (first < n_items) issue(first);
   }
   __syncthreads();
+
+  // Persistent loop: one work item per pass.  The next ticket is drawn once
+  // this item has read its inputs for the last time (after step 7) and its
+  // copies land while this item finishes its reductions.  An earlier draw
+  // would hold tickets back from the look-back chains (an item whose
+  // neighbour sits reserved behind a running item waits for both), which
+  // measurably slows the whole kernel.  Items only ever wait on items with
+  // smaller tickets, all of which are done or in hand of a running CTA, so
+  // the loop cannot deadlock.
+  for (uint32_t it = 0;; ++it) {
   const int tk = sm.ticket;
+  if (tk >= n_items) break;
   const int rev = tk / a.n_tiles;
   const int tile = tk - rev * a.n_tiles;
   const int chunk = a.n_chunks - 1 - rev;
   const int64_t t0 = (int64_t)chunk * kL;
   const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
+  const int rows4 = rows & ~3;
   const int d0 = tile * kTile;
   const int bx = a.box_x;
-
-  if (tid == 0) {
-    const uint32_t box = (uint32_t)bx * (uint32_t)a.box_y * sizeof(T);
-    const uint32_t bc = (uint32_t)rows * N * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 4u : 3u) + 2u * bc);
-    tma_load_2d(sm.u, &tm_u, d0, (int)t0, &sm.bar);
-    tma_load_2d(sm.dr, &tm_dr, d0, (int)t0, &sm.bar);
-    tma_load_2d(sm.dout, &tm_dout, d0, (int)t0, &sm.bar);
-    if (a.has_z) tma_load_2d(sm.z, &tm_z, d0, (int)t0, &sm.bar);
-    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + t0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + t0 * N, bc, &sm.bar);
-  }
-  if (tid < kL) sm.pos[tid] = (tid < rows) ? __ldg(a.pos + t0 + tid) : 1;
-  stage_rows<N>(sm.At, a.A, d0, a.D, tid, kThreads);
-  stage_rows<N>(sm.Ht, a.chunk_states + (int64_t)chunk * a.D * N, d0, a.D, tid, kThreads);
-
   const int d = d0 + lane;
   const bool valid = lane < bx && d < a.D;
-  const float bias = (valid && a.dt_bias) ? __ldg(a.dt_bias + d) : 0.0f;
-  const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
 
-  if (!mbar_wait(&sm.bar, 0, a.wait_ns) && lane == 0) atomicOr(a.status, kStatusTmaTimeout);
+  if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
+    if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
+    break;
+  }
+  const float bias = (valid && a.dt_bias) ? sm.bias[lane] : 0.0f;
+  const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
   const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
   const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
-  __syncthreads();
   float2 A2[P];
-  load_scaled_pairs<N>(A2, sm.At + lane * (N + 4), kLog2e);
+  if (valid) {
+    load_scaled_pairs<N>(A2, sm.Araw + lane * N, kLog2e);
+  } else {
+#pragma unroll
+    for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
+  }
 
   const int tb = s * kK;
   // ---- 1. per-token values (registers); lanes without a channel get u = g = 0
@@ -175,9 +221,11 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       } else {
         g[k] = go;
       }
-      if (sm.pos[t] == 0) rst |= 1 << k;
+      const int pt = t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t);
+      if (pt == 0) rst |= 1 << k;
     }
   }
+  __syncthreads();  // Bf, Cf complete
 
   // ---- 2. both aggregates of my K tokens: forward (state from 0) and reverse
   //         (carry leaving to the left when nothing enters from the right)
@@ -251,7 +299,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         Hj[j] = sm.aggH[(j * N + n) * kTile + lane];
         Gj[j] = sm.aggG[(j * N + n) * kTile + lane];
       }
-      float x = sm.Ht[lane * (N + 4) + n];
+      float x = valid ? sm.Hraw[lane * N + n] : 0.0f;
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
         sm.aggH[(j * N + n) * kTile + lane] = x;
@@ -270,7 +318,6 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
   // ---- 4. decoupled look-back towards higher chunks (warp 0); the other warps
   //         go straight on to step 5, which needs no carry from the right
-  bool release_incl = false;  // warp 0: inclusive carry stored, flag not yet released
   if (s == 0) {
     int rs_any = 0;
     float sd_tot = 0.0f;
@@ -339,14 +386,14 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
     for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
     if (!rs_any) {
-      // payload now; its flag is released after step 5, by which time these
-      // stores have drained and the release costs little
+      // released at once: the next chunk of the tile may already be waiting,
+      // and every link of that chain adds this item's publication delay
 #pragma unroll
       for (int n = 0; n < N; ++n) {
         const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
         my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.tot[n * kTile + lane]);
       }
-      release_incl = publish;
+      if (publish) st_release_gpu(my_flag, kFlagInclusive);
     }
   }
 
@@ -383,10 +430,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     yk[k] = fmaf(Dsk, uu[k], y2.x + y2.y);
   }
-  if (release_incl)
-    st_release_gpu(a.flags + ((int64_t)tile * a.n_chunks + chunk) * kTile + lane, kFlagInclusive);
   __syncthreads();
 
+  // the next ticket, drawn now and used once this item's inputs are consumed
+  // (the atomic's latency hides behind step 7)
   // ---- 6. carry entering my last token from the right
   float2 dh[P];
   {
@@ -480,6 +527,13 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
   // ---- 8. fixed-order CTA reduction of dA, dDskip, d_dt_bias partials
   __syncthreads();
+  // no input buffer is read any more: draw the next item and request its
+  // inputs, which land while this item finishes its reductions
+  if (tid == 0) {
+    const int next = (int)atomicAdd(a.ticket, 1u);
+    sm.ticket = next;
+    if (next < n_items) issue(next);
+  }
 #pragma unroll
   for (int i = 0; i < P; ++i) {
     sm.aggH[(s * N + 2 * i) * kTile + lane] = dA[i].x;
@@ -494,7 +548,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     float acc = 0.0f;
 #pragma unroll
     for (int j = 0; j < kS; ++j) acc += sm.aggH[(j * N + n) * kTile + lane];
-    sm.At[lane * (N + 4) + n] = acc;   // A is no longer needed: reuse its rows
+    sm.aggG[lane * (N + 4) + n] = acc;
   }
   if (s == 0 && valid) {
     float accD = 0.0f, accB = 0.0f;
@@ -511,8 +565,9 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   {
     float* dst = a.part_dA + ((int64_t)chunk * a.D + d0) * N;
     const int nvalid = (a.D - d0 < kTile ? a.D - d0 : kTile) * N;
-    for (int i = tid; i < nvalid; i += kThreads) dst[i] = sm.At[(i / N) * (N + 4) + (i % N)];
+    for (int i = tid; i < nvalid; i += kThreads) dst[i] = sm.aggG[(i / N) * (N + 4) + (i % N)];
   }
+  }  // persistent loop
 }
 
 // dB[t][n] = sum over tiles of part[tile][t][n]; dC[t][n] likewise from
@@ -539,7 +594,10 @@ cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
-  scan_bwd_kernel<T, N><<<(unsigned)items, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, a);
+  int grid = 0;
+  e = persistent_grid(scan_bwd_kernel<T, N>, kThreads, smem, items, &grid);
+  if (e != cudaSuccess) return e;
+  scan_bwd_kernel<T, N><<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, a);
   return cudaGetLastError();
 }
 

@@ -4,8 +4,11 @@
 // A CTA of 256 threads = 8 warps; warp s owns sub-chunk s (K = 16 tokens) and
 // lane l owns channel d0 + l with all N states in registers.
 //
-//   1. TMA: u, delta_raw, z tiles (128 x 32) with 2-D tensor maps, B and C
-//      rows (128 x N, contiguous) with 1-D bulk copies, one mbarrier.
+//   1. Copies: u, delta_raw, z tiles (128 x 32) with 2-D tensor maps; B and C
+//      rows (128 x N, contiguous), A rows, dt_bias, Dskip and position indices
+//      with 1-D bulk copies; one mbarrier.  The kernel is persistent (one CTA
+//      per resident slot, looping over tickets), and one thread requests the
+//      next item's copies as soon as the current item has read its inputs.
 //   2. delta = softplus(delta_raw + dt_bias) once per (token, channel) -> smem.
 //   3. Pass 1: every thread scans its K tokens from h = 0 and records the
 //      sub-chunk aggregate: H (the state reached) and the sum of delta since
@@ -52,8 +55,10 @@ struct FwdSmem {
   float totH[N * kTile];
   float hin[N * kTile];
   float aggSD[kS * kTile];
-  alignas(16) float At[kTile * (N + 4)];  // A rows of the tile, padded for conflict-free 16-byte reads
-  int pos[kL];
+  alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
+  alignas(16) float bias[kTile];
+  alignas(16) float dsk[kTile];
+  alignas(16) int pos[kL];
   int aggRS[kS];
   int ticket;
   alignas(8) uint64_t bar;
@@ -68,45 +73,88 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, s = tid >> 5;
 
+  const int n_items = a.n_chunks * a.n_tiles;
+
+  // Requests every input of work item `tkn` on the barrier: u, delta_raw, z
+  // tiles; B and C rows; A rows, dt_bias, Dskip; position indices (whole
+  // groups of 4 tokens).  With no item left, thread 0 arrives without data so
+  // that the barrier still completes and tells every thread to stop.
+  auto issue = [&](int tkn) {
+    if (tkn >= n_items) {
+      mbar_arrive(&sm.bar);
+      return;
+    }
+    const int ch = tkn / a.n_tiles;
+    const int tl = tkn - ch * a.n_tiles;
+    const int64_t tt0 = (int64_t)ch * kL;
+    const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
+    const int dd0 = tl * kTile;
+    const uint32_t nval = (uint32_t)(a.D - dd0 < kTile ? a.D - dd0 : kTile);
+    const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
+    const uint32_t rows4 = (uint32_t)nrows & ~3u;
+    const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
+    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 3u : 2u) + 2u * bc + nval * N * 4u + rows4 * 4u +
+                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
+    tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+    tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
+    if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
+    if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
+    if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
+    if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
+  };
+
   if (tid == 0) {
-    sm.ticket = (int)atomicAdd(a.ticket, 1u);
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
+    const int first = (int)atomicAdd(a.ticket, 1u);
+    sm.ticket = first;
+    issue(first);
   }
   __syncthreads();
+
+  // Persistent loop: one work item per pass.  The inputs are read until the
+  // end of pass 2, so the next ticket is drawn and its copies requested there;
+  // an earlier draw would hold tickets back from the look-back chains (an
+  // item whose neighbour sits reserved behind a running item waits for both).
+  // Items only ever wait on items with smaller tickets, all of which are done
+  // or in hand of a running CTA, so the loop cannot deadlock.
+  for (uint32_t it = 0;; ++it) {
+  // the barrier's completion also publishes thread 0's write of sm.ticket
+  if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
+    if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
+    break;
+  }
   const int tk = sm.ticket;
+  if (tk >= n_items) break;
   const int chunk = tk / a.n_tiles;
   const int tile = tk - chunk * a.n_tiles;
   const int64_t t0 = (int64_t)chunk * kL;
   const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
+  const int rows4 = rows & ~3;
   const int d0 = tile * kTile;
   const int bx = a.box_x;
-
-  if (tid == 0) {
-    const uint32_t box = (uint32_t)bx * (uint32_t)a.box_y * sizeof(T);
-    const uint32_t bc = (uint32_t)rows * N * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 3u : 2u) + 2u * bc);
-    tma_load_2d(sm.u, &tm_u, d0, (int)t0, &sm.bar);
-    tma_load_2d(sm.dr, &tm_dr, d0, (int)t0, &sm.bar);
-    if (a.has_z) tma_load_2d(sm.z, &tm_z, d0, (int)t0, &sm.bar);
-    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + t0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + t0 * N, bc, &sm.bar);
-  }
-  for (int i = tid; i < kL; i += kThreads) sm.pos[i] = (i < rows) ? __ldg(a.pos + t0 + i) : 1;
-  stage_rows<N>(sm.At, a.A, d0, a.D, tid, kThreads);
-
   const int d = d0 + lane;
   const bool valid = lane < bx && d < a.D;
   constexpr int P = N / 2;  // state pairs
-  const float bias = (valid && a.dt_bias) ? __ldg(a.dt_bias + d) : 0.0f;
-  const float Dsk = (valid && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
+  const float bias = (valid && a.dt_bias) ? sm.bias[lane] : 0.0f;
+  const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
+  // position index of token t < rows of the chunk (the last chunk's ragged
+  // tail, past the last whole group of 4, is read from global memory)
+  auto pos_at = [&](int t) { return t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t); };
 
-  if (!mbar_wait(&sm.bar, 0, a.wait_ns) && lane == 0) atomicOr(a.status, kStatusTmaTimeout);
   const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
   const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
   __syncthreads();
   float2 A2[P];
-  load_scaled_pairs<N>(A2, sm.At + lane * (N + 4), kLog2e);
+  if (valid) {
+    load_scaled_pairs<N>(A2, sm.Araw + lane * N, kLog2e);
+  } else {
+#pragma unroll
+    for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
+  }
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
   // ---- step 2: delta for my tokens
@@ -127,7 +175,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
-    if (sm.pos[t] == 0) {
+    if (pos_at(t) == 0) {
 #pragma unroll
       for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
       sd = 0.0f;
@@ -208,7 +256,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
     for (int n = 0; n < N; ++n) x[n] = 0.0f;
     // no entering state is needed when a sequence starts at the first token
-    if (chunk > 0 && sm.pos[0] != 0) {
+    if (chunk > 0 && pos_at(0) != 0) {
       // the previous chunk of the tile started long before this one and has
       // usually published its inclusive state: look first, and publish this
       // chunk's aggregate only when the walk has to go further
@@ -264,6 +312,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   if (release_incl)
     st_release_gpu(a.flags + ((int64_t)tile * a.n_chunks + chunk) * kTile + lane, kFlagInclusive);
 
+  // the next ticket, drawn now and used once pass 2 has read this item's
+  // inputs (the atomic's latency hides behind pass 2)
   // ---- step 6: exact start state, pass 2
   int rs_pre = 0;
   float sd_pre = 0.0f;
@@ -290,7 +340,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
-    if (sm.pos[t] == 0) {
+    if (pos_at(t) == 0) {
 #pragma unroll
       for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
     }
@@ -310,6 +360,15 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane]));
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
   }
+
+  // every input of this item has been read: draw the next one
+  __syncthreads();
+  if (tid == 0) {
+    const int next = (int)atomicAdd(a.ticket, 1u);
+    sm.ticket = next;
+    issue(next);
+  }
+  }  // persistent loop
 }
 
 template <typename T, int N>
@@ -320,7 +379,10 @@ cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
-  scan_fwd_kernel<T, N><<<(unsigned)items, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
+  int grid = 0;
+  e = persistent_grid(scan_fwd_kernel<T, N>, kThreads, smem, items, &grid);
+  if (e != cudaSuccess) return e;
+  scan_fwd_kernel<T, N><<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
   return cudaGetLastError();
 }
 
