@@ -142,9 +142,9 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
  *   out    = z ? y * SiLU(z[t,d]) : y
  * u, delta_raw, z, out: (T, D) io; B, C: (T, N) io; A: (D, N) f32;
  * Dskip, dt_bias: (D) f32.  Dskip, z, dt_bias are nullable (zero / no gate).
- * chunk_states: nullable f32 (ceil(T / VSSM_STATE_CHUNK), D, N); when given,
- * entry [c][d][n] receives the state just before token c*VSSM_STATE_CHUNK,
- * which the backward call needs.
+ * chunk_states: nullable f32 (ceil(T / VSSM_STATE_CHUNK), N, D); when given,
+ * entry [c][n][d] receives state n of channel d just before token
+ * c*VSSM_STATE_CHUNK, which the backward call needs.
  */
 size_t varlen_selective_scan_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
 size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, int32_t N);

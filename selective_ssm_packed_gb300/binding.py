@@ -212,7 +212,7 @@ def scan_bwd_workspace_size(T, D, N):
 
 
 def chunk_states_shape(T, D, N):
-    return ((int(T) + VSSM_STATE_CHUNK - 1) // VSSM_STATE_CHUNK, int(D), int(N))
+    return ((int(T) + VSSM_STATE_CHUNK - 1) // VSSM_STATE_CHUNK, int(N), int(D))
 
 
 def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens,

@@ -64,7 +64,7 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   l.agg = off;
   off += up(sizeof(float) * (size_t)slots * N * kTile);
   l.agg_sd = off;
-  off += up(sizeof(float) * (size_t)slots * kTile);
+  off += up(sizeof(float) * (size_t)slots * (bwd ? N : 1) * kTile);
   l.incl = off;
   off += up(sizeof(float) * (size_t)slots * N * kTile);
   if (bwd) {
@@ -463,11 +463,12 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.box_y = T < kBwdChunk ? (int)T : kBwdChunk;
   a.drop_ticket = g_drop_ticket.load();
   a.wait_ns = g_wait_ns.load();
-  CUtensorMap mu, mdr, mz, mdo;
+  CUtensorMap mu, mdr, mz, mdo, mcs;
   std::memset(&mu, 0, sizeof(mu));
   std::memset(&mdr, 0, sizeof(mdr));
   std::memset(&mz, 0, sizeof(mz));
   std::memset(&mdo, 0, sizeof(mdo));
+  std::memset(&mcs, 0, sizeof(mcs));
   if (T > 0) {
     const int32_t* pos = nullptr;
     VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, T, workspace, l, st, &pos));
@@ -476,8 +477,11 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
     VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
     VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
     VSSM_TRY(make_map(&mdo, dout, io, T, D, a.box_x, a.box_y));
+    // saved states [chunk][n][d] seen as (chunks * N) rows of D floats; one
+    // copy fetches an item's N rows of its tile's channels
+    VSSM_TRY(make_map(&mcs, chunk_states, IO::F32, cdiv(T, kStateChunk) * N, D, a.box_x, N));
   }
-  e = launch_scan_bwd(a, io, mu, mdr, mz, mdo, dA, dB, dC, dDskip, d_dt_bias, st);
+  e = launch_scan_bwd(a, io, mu, mdr, mz, mdo, mcs, dA, dB, dC, dDskip, d_dt_bias, st);
   return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_bwd launch");
 }
 

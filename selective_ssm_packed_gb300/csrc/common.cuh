@@ -91,6 +91,28 @@ __device__ __forceinline__ void load_scaled_pairs(float2 (&v)[N / 2], const floa
   }
 }
 
+// Same values from an UNPADDED row-major (rows, N) array in shared memory, one
+// row per lane: each lane fetches its four-value blocks in a lane-rotated
+// order, so that the 8 lanes of a 16-byte access phase hit distinct banks.
+template <int N>
+__device__ __forceinline__ void load_row_pairs_rotated(float2 (&v)[N / 2], const float* row, int lane,
+                                                       float scale) {
+  constexpr int NB = N / 4;                     // 16-byte blocks per row
+  const int r = (lane / (8 / NB)) % NB;         // rotation of this lane
+  float4 q[NB];                                 // q[j] = block (j + r) % NB
+#pragma unroll
+  for (int j = 0; j < NB; ++j) q[j] = *reinterpret_cast<const float4*>(row + 4 * ((j + r) % NB));
+#pragma unroll
+  for (int c = 0; c < NB; ++c) {
+    float4 b = q[c];
+#pragma unroll
+    for (int k = 1; k < NB; ++k)
+      if (r == k) b = q[(c - k + NB) % NB];
+    v[2 * c] = make_float2(b.x * scale, b.y * scale);
+    v[2 * c + 1] = make_float2(b.z * scale, b.w * scale);
+  }
+}
+
 // ------------------------------------------------------------------ timers, memory order
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -107,6 +129,14 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+
+__device__ __forceinline__ void st_relaxed_gpu(int* p, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's earlier memory accesses before its later ones, for
+// observers anywhere on the GPU.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Spin (with backoff) until *flag != 0 or `limit_ns` passes.  Returns the flag
 // value, or 0 after a timeout (the caller records the error and carries on).

@@ -62,16 +62,21 @@ struct ScanArgs {
   void* du;                   // bwd
   void* ddr;                  // bwd
   void* dz;                   // bwd (nullable)
-  float* part_dBC;            // bwd [n_tiles][T][2N]
-  float* part_dA;             // bwd [n_chunks][D][N]
+  float* part_dBC;            // bwd [n_tiles][2N][T]
+  float* part_dA;             // bwd [n_chunks][N][D]
   float* part_dD;             // bwd [n_chunks][D]
   float* part_dbias;          // bwd [n_chunks][D]
   int* status;
   unsigned* ticket;
-  int* flags;                 // [n_tiles][n_chunks][kTile]: one per channel chain
-  float* agg;                 // [n_tiles][n_chunks][N][kTile]
-  float* agg_sd;              // [n_tiles][n_chunks][kTile]
-  float* incl;                // [n_tiles][n_chunks][N][kTile]
+  // look-back state.  fwd: one chain per channel, flags [n_tiles][n_chunks][kTile],
+  // agg / incl [n_tiles][n_chunks][N][kTile], agg_sd [n_tiles][n_chunks][kTile]
+  // (sum of delta).  bwd: one chain per (warp = state pair, channel), flags
+  // [n_tiles][n_chunks][N/2], agg / incl / agg_sd [n_tiles][n_chunks][N/2][kTile]
+  // float2, agg_sd holding the products of the transition factors.
+  int* flags;
+  float* agg;
+  float* agg_sd;
+  float* incl;
   int64_t T;
   int D;
   int N;
@@ -90,15 +95,18 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z, cudaStream_t st);
 cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z,
-                            const CUtensorMap& tm_dout, float* dA, float* dB, float* dC,
-                            float* dDskip, float* d_dt_bias, cudaStream_t st);
+                            const CUtensorMap& tm_dout, const CUtensorMap& tm_cs, float* dA,
+                            float* dB, float* dC, float* dDskip, float* d_dt_bias, cudaStream_t st);
 
 // Sets the message vssm_last_error() returns on this thread; returns `code`.
 int record_error(int code, const char* message);
 
 // ---------------------------------------------------------------- reductions
-// out[m] = sum_{p < P} in[p * ld + m] for m < M, p in increasing order.
-cudaError_t launch_sum_rows(const float* in, int64_t P, int64_t M, int64_t ld, float* out,
-                            cudaStream_t st);
+// out[m] = sum_{p < P} in[p * ld + m] for m < M, in a fixed order (rows in
+// order within groups of 32, then the group sums in order); `in` is scratch
+// and is overwritten.  With inner > 0 the M columns form an (M / inner, inner)
+// array that is written out transposed.
+cudaError_t launch_sum_rows(float* in, int64_t P, int64_t M, int64_t ld, float* out, cudaStream_t st,
+                            int64_t inner = 0);
 
 }  // namespace vssm

@@ -39,10 +39,36 @@ cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t
   return cudaGetLastError();
 }
 
-// out[m] = sum over p = 0..P-1 (in order) of in[p*ld + m].  One thread per
-// column, so the summation order is fixed and the result bitwise repeatable.
+// out[m] = sum over p = 0..P-1 of in[p*ld + m], in a fixed order: rows are
+// summed in order within groups of R consecutive rows, then the group sums in
+// order.  One thread per (column, group), so the result is bitwise repeatable.
+//
+// Group pass: the sum of rows g*R .. g*R+R-1 replaces row g*R (the partial
+// buffer is scratch owned by the caller).
+__global__ void __launch_bounds__(256) sum_row_groups_kernel(float* __restrict__ in, int64_t P,
+                                                             int64_t M, int64_t ld, int64_t R,
+                                                             int64_t col_blocks) {
+  const int64_t g = blockIdx.x / col_blocks;
+  const int64_t m = (blockIdx.x - g * col_blocks) * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  const int64_t r0 = g * R, r1 = (r0 + R < P) ? r0 + R : P;
+  float* p = in + m;
+  float acc = 0.0f;
+  int64_t r = r0;
+  for (; r + 4 <= r1; r += 4) {
+    const float a0 = __ldcs(p + (r + 0) * ld), a1 = __ldcs(p + (r + 1) * ld);
+    const float a2 = __ldcs(p + (r + 2) * ld), a3 = __ldcs(p + (r + 3) * ld);
+    acc += a0; acc += a1; acc += a2; acc += a3;
+  }
+  for (; r < r1; ++r) acc += __ldcs(p + r * ld);
+  p[r0 * ld] = acc;
+}
+
+// Final pass: out[m] = sum over p = 0..P-1 (in order) of in[p*ld + m]; with
+// inner > 0 the columns are an (M / inner, inner) array written out
+// transposed: out[(m % inner) * (M / inner) + m / inner].
 __global__ void __launch_bounds__(256) sum_rows_kernel(const float* __restrict__ in, int64_t P,
-                                                       int64_t M, int64_t ld,
+                                                       int64_t M, int64_t ld, int64_t inner,
                                                        float* __restrict__ out) {
   const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
@@ -55,14 +81,31 @@ __global__ void __launch_bounds__(256) sum_rows_kernel(const float* __restrict__
     acc += a0; acc += a1; acc += a2; acc += a3;
   }
   for (; r < P; ++r) acc += __ldcs(p + r * ld);
-  out[m] = acc;
+  if (inner > 0) {
+    const int64_t q = m / inner;
+    out[(m - q * inner) * (M / inner) + q] = acc;
+  } else {
+    out[m] = acc;
+  }
 }
 
-cudaError_t launch_sum_rows(const float* in, int64_t P, int64_t M, int64_t ld, float* out,
-                            cudaStream_t st) {
+cudaError_t launch_sum_rows(float* in, int64_t P, int64_t M, int64_t ld, float* out, cudaStream_t st,
+                            int64_t inner) {
   if (M <= 0) return cudaSuccess;
-  const int64_t blocks = (M + 255) / 256;
-  sum_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(in, P, M, ld, out);
+  const int64_t col_blocks = (M + 255) / 256;
+  constexpr int64_t kGroup = 32;
+  if (P > 2 * kGroup) {
+    // enough groups to fill the GPU, at most 2^31 - 1 blocks in all
+    int64_t R = kGroup;
+    while (((P + R - 1) / R) * col_blocks > 2147483647LL) R *= 2;
+    const int64_t G = (P + R - 1) / R;
+    sum_row_groups_kernel<<<(unsigned)(G * col_blocks), 256, 0, st>>>(in, P, M, ld, R, col_blocks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    P = G;
+    ld *= R;
+  }
+  sum_rows_kernel<<<(unsigned)col_blocks, 256, 0, st>>>(in, P, M, ld, inner, out);
   return cudaGetLastError();
 }
 

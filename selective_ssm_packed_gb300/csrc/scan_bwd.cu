@@ -4,34 +4,43 @@
 // (tile of kTile = 32 channels); items are taken in DESCENDING chunk order
 // from an atomic ticket because the state gradient flows from the end of a
 // sequence to its start.  The kernel is persistent (one CTA per resident slot,
-// looping over tickets); each item's inputs are requested by one thread with
-// tensor / bulk copies on one mbarrier while the previous item finishes.
-// CTA = 8 warps; warp s owns K = 4 tokens, lane l owns channel d0 + l with
-// all N states.
+// looping over tickets); one thread requests each item's inputs with tensor /
+// bulk copies on one mbarrier while the previous item finishes.
 //
-// With a_t = exp(delta_t A) (0 at a sequence start), g_t = dout_t SiLU(z_t),
-// the state gradient obeys dh_t = a_{t+1} dh_{t+1} + C_t g_t and is zero after
-// the last token of every sequence (a_{t+1} = 0 when t+1 starts a sequence):
-// the reverse scan that resets at sequence ends.
+// CTA = N/2 warps.  Warp w owns the state pair (2w, 2w+1) for ALL 32 tokens
+// of the item, lane l owns channel d0 + l.  The forward states therefore need
+// no scan inside the CTA: every warp starts from the saved state of the chunk
+// (chunk_states, written by the forward call) and walks its 32 tokens.
 //
-//   1. Copies (issued during the previous item): u, delta_raw, dout, z tiles
-//      (32 x 32), B and C rows, A rows, dt_bias, Dskip, saved states,
-//      position indices; per-token delta, SiLU(z), g kept in registers.
-//   2. Forward states: pass over the K tokens from h = 0 -> sub-chunk
-//      aggregates; exclusive scan seeded with the chunk's saved state
-//      (chunk_states from the forward call) gives each thread its start state.
-//   3. Reverse aggregates: pass over the K tokens backwards from dh = 0; the
-//      left-going carry of a block is (prod a) * carry_in + G, with G the carry
-//      out when nothing comes in; exclusive reverse scan in shared memory.
-//   4. Decoupled look-back towards HIGHER chunks for the carry entering the
-//      chunk from the right, re-applied in a fixed order (bitwise repeatable),
-//      time-bounded waits.
-//   5. Recompute the K forward states into shared memory, then walk the K
-//      tokens backwards producing du, d(delta_raw), dz and per-token partial
-//      dB, dC (reduced over the warp's 32 channels with a butterfly
-//      reduce-scatter, no atomics) and per-thread partial dA, dDskip, d_dt_bias.
-//   6. Fixed-order CTA reduction of the partials; separate fixed-order kernels
-//      sum them over channel tiles (dB, dC) and chunks (dA, dDskip, d_dt_bias).
+// With a_t = exp(delta_t A) (0 at a sequence start), b_t = delta_t u_t B_t,
+// g_t = dout_t SiLU(z_t):
+//   h_t  = a_t h_{t-1} + b_t                       (forward walk)
+//   dh_t = C_t g_t + a_{t+1} dh_{t+1}              (reverse walk; a_{t+1} = 0
+//                                                   at a sequence start, so the
+//                                                   scan resets at sequence ends)
+// The carry handed to the previous chunk is a_{t0} dh_{t0} = sum_t E_t C_t g_t
+// + E_last * (carry from the next chunk), with E_t = a_{t0} ... a_t: both terms
+// are accumulated during the FORWARD walk, so the look-back needs no extra
+// pass and no extra exponential.
+//
+//   1. Per-(token, channel) values once per item, by all threads: delta,
+//      delta u, g, d delta / d delta_raw, in [channel][token] arrays; B and C
+//      transposed to [state][token] (fp32).
+//   2. Forward walk per warp: states h_t kept in registers (32 tokens x 2
+//      states); E and the carry aggregate accumulated; dC_t[n] contributions
+//      g_t h_t summed over the tile's channels (WarpColumnSum); C_t.h_t
+//      partials for y.
+//   3. Decoupled look-back per warp towards HIGHER chunks for the carry
+//      entering from the right; aggregates re-applied in a fixed order
+//      (bitwise repeatable); time-bounded waits.
+//   4. y = sum of the warps' partials + Dskip u, and dz (all threads).
+//   5. Reverse walk per warp in blocks of 8 tokens: dA (per thread), dB
+//      contributions (WarpColumnSum), partial sums over the warp's states
+//      for du and d delta; after each block all threads add the warps'
+//      partials in a fixed order and write du, d delta_raw.
+//   6. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
+// Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
+// and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,81 +48,114 @@ namespace vssm {
 
 namespace {
 
-constexpr int kL = kBwdChunk;   // 32
-constexpr int kS = 8;
-constexpr int kK = kL / kS;     // 4
-constexpr int kThreads = kS * 32;
+constexpr int kL = kBwdChunk;   // 32 tokens per work item
+constexpr int kP = kL + 4;      // row pitch of the [channel][token] arrays
+constexpr int kRB = 8;          // tokens per block of the reverse walk
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T, int N>
 struct BwdSmem {
+  static constexpr int W = N / 2;  // warps = state pairs
   // ---- inputs of one work item, written by tensor / bulk copies and refilled
-  //      for the next item while this one is still being processed
+  //      for the next item once this one has read them for the last time
   alignas(128) T u[kL * kTile];
   alignas(128) T dr[kL * kTile];
   alignas(128) T z[kL * kTile];
   alignas(128) T dout[kL * kTile];
   alignas(128) T B[kL * N];
   alignas(128) T C[kL * N];
-  alignas(16) float Araw[kTile * N];   // A rows d0 .. d0+31
-  alignas(16) float Hraw[kTile * N];   // saved states at the chunk start, same rows
+  alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
+  alignas(128) float H[N * kTile];    // saved states at the chunk start, [n][channel]
   alignas(16) float bias[kTile];
   alignas(16) float dsk[kTile];
   alignas(16) int pos[kL];
-  // ---- working set of the item being processed
-  // B and C widened to fp32 once per work item (bf16 I/O only; fp32 I/O reads B, C directly)
-  alignas(16) float Bf[sizeof(T) == 2 ? kL * N : 4];
-  alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
-  // states after a thread's first K-1 tokens ([k][n/4][tid]); the state after
-  // its last token stays in registers
-  alignas(16) float4 hist[(kK - 1) * (N / 4) * kThreads];
-  alignas(16) float aggH[kS * N * kTile];  // forward aggregates, then each warp's start state
-  alignas(16) float aggG[kS * N * kTile];  // reverse aggregates, then exclusive suffixes, then the dA block
-  float tot[N * kTile];
-  float rin[N * kTile];
-  float aggSD[kS * kTile];
-  float redD[kS * kTile];
-  float redB[kS * kTile];
-  int aggRS[kS];
+  // ---- per-(token, channel) values, [channel][token] with pitch kP: a lane
+  //      reads 4 tokens of its channel with one conflict-free 16-byte access
+  alignas(16) float dl[kTile * kP];   // delta
+  alignas(16) float dlu[kTile * kP];  // delta * u
+  alignas(16) float g[kTile * kP];    // dout * SiLU(z)
+  alignas(16) float sg[kTile * kP];   // d delta / d delta_raw
+  // ---- B, C as [state][token] with pitch kP, fp32 (zero past the last token)
+  alignas(16) float BT[N * kP];
+  alignas(16) float CT[N * kP];
+  // ---- exponent offset per token: -inf at a sequence start, else 0
+  alignas(16) float off[kL];
+  // ---- per-warp column-sum buffers, 32 rows x 32 floats each
+  alignas(16) float cs[W * 32 * 32];
+  // ---- cross-warp partials: y partials [W][kL][kTile] after the forward
+  //      walk, then (du, d delta) partials [2][W][kRB][kTile] float2 in the
+  //      reverse walk
+  alignas(16) float part[W * kL * kTile];
+  float redD[W * kTile];
+  float redB[W * kTile];
   int ticket;
   alignas(8) uint64_t bar;
 };
 
-// Butterfly reduce-scatter over the 32 lanes of a warp: on entry each lane
-// holds C values; on exit v[0] of lane l is the sum over all lanes of value
-// l >> (5 - log2 C).  Fixed pairing order, so the sums are reproducible.
-template <int C, int M>
-struct ReduceScatter {
-  static __device__ __forceinline__ void run(float* v, int lane) {
-    if constexpr (C > 1) {
-      constexpr int H = C / 2;
-      const bool up = (lane & M) != 0;
+// Column sums over the 32 lanes of a warp (lane = channel) of 32 values per
+// lane, through the warp's shared buffer of 32 rows x 32 floats:
+//   1. every lane stores its row; 16-byte chunk q of row l sits at slot
+//      q ^ (l & 7), so the 8 lanes of each 16-byte access phase hit 8
+//      different bank groups;
+//   2. lane j reads chunk m = j & 7 of the rows g, g + 4, ..., g + 28
+//      (g = j >> 3: conflict-free again) and adds them in order, two values
+//      per instruction;
+//   3. the 4 lanes holding the same chunk combine their sums by two halving
+//      shuffle exchanges (lane bits 4 and 3), after which lane j holds the
+//      sum of column 4 (j & 7) + 2 bit4(j) + bit3(j).
+// The order of every addition is fixed, so the sums are bitwise repeatable.
+struct WarpColumnSum {
+  static __device__ __forceinline__ int column(int lane) {
+    return 4 * (lane & 7) + 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);
+  }
+  // values 4q .. 4q+3 of this lane's row
+  static __device__ __forceinline__ void put(float* buf, int lane, int q, float2 lo, float2 hi) {
+    *reinterpret_cast<float4*>(buf + lane * 32 + 4 * (q ^ (lane & 7))) = make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+  // call with every lane's row in place (after __syncwarp)
+  static __device__ __forceinline__ float reduce(const float* buf, int lane) {
+    const int m = lane & 7, g0 = lane >> 3;
+    float2 lo = make_float2(0.0f, 0.0f), hi = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float send = up ? v[i] : v[i + H];
-        const float keep = up ? v[i + H] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
-      }
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
+    for (int i = 0; i < 8; ++i) {
+      const int r = g0 + 4 * i;
+      const float4 x = *reinterpret_cast<const float4*>(buf + r * 32 + 4 * (m ^ (r & 7)));
+      lo = __fadd2_rn(lo, make_float2(x.x, x.y));
+      hi = __fadd2_rn(hi, make_float2(x.z, x.w));
     }
-    if constexpr (M > 1) ReduceScatter<(C > 1 ? C / 2 : 1), M / 2>::run(v, lane);
+    const bool u4 = (lane & 16) != 0;
+    float2 keep = u4 ? hi : lo;
+    const float2 send = u4 ? lo : hi;
+    keep.x += __shfl_xor_sync(0xffffffffu, send.x, 16);
+    keep.y += __shfl_xor_sync(0xffffffffu, send.y, 16);
+    const bool u3 = (lane & 8) != 0;
+    float v = u3 ? keep.y : keep.x;
+    v += __shfl_xor_sync(0xffffffffu, u3 ? keep.x : keep.y, 8);
+    return v;
   }
 };
 
+// Publishes a warp's look-back payload: every lane has stored its part; the
+// fence orders each lane's stores before the barrier, and lane 0 then sets the
+// warp's flag.
+__device__ __forceinline__ void publish_flag(int* flag, int value, bool publish, int lane) {
+  fence_acq_rel_gpu();
+  __syncwarp();
+  if (lane == 0 && publish) st_relaxed_gpu(flag, value);
+}
+
 template <typename T, int N>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(16 * N, 512 / (16 * N))
 scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
-                const ScanArgs a) {
+                const __grid_constant__ CUtensorMap tm_cs, const ScanArgs a) {
   using SM = BwdSmem<T, N>;
-  constexpr int P = N / 2;                       // state pairs
-  constexpr int V = 2 * N;                       // dB and dC values per token
-  constexpr int kRep = 32 / (V < 32 ? V : 32);   // lanes holding the same value
+  constexpr int W = SM::W;
+  constexpr int kThr = 32 * W;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, s = tid >> 5;
-
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  float* const csw = sm.cs + w * 32 * 32;  // this warp's column-sum buffer
   const int n_items = a.n_chunks * a.n_tiles;
 
   // Requests every input of work item `tkn` on the barrier: u, delta_raw,
@@ -130,9 +172,9 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 4u : 3u) + 2u * bc + 2u * nval * N * 4u +
-                                       rows4 * 4u + (a.dt_bias ? nval * 4u : 0u) +
-                                       (a.Dskip ? nval * 4u : 0u));
+    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 4u : 3u) + 2u * bc + nval * N * 4u +
+                                       (uint32_t)a.box_x * N * 4u + rows4 * 4u +
+                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
     tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
     tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
     tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
@@ -140,7 +182,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
     bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
     bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
-    bulk_load_1d(sm.Hraw, a.chunk_states + ((int64_t)ch * a.D + dd0) * N, nval * N * 4u, &sm.bar);
+    tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
     if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
     if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
     if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
@@ -156,13 +198,12 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   __syncthreads();
 
   // Persistent loop: one work item per pass.  The next ticket is drawn once
-  // this item has read its inputs for the last time (after step 7) and its
-  // copies land while this item finishes its reductions.  An earlier draw
-  // would hold tickets back from the look-back chains (an item whose
-  // neighbour sits reserved behind a running item waits for both), which
-  // measurably slows the whole kernel.  Items only ever wait on items with
-  // smaller tickets, all of which are done or in hand of a running CTA, so
-  // the loop cannot deadlock.
+  // this item has read its inputs for the last time and its copies land while
+  // this item writes its last partials.  An earlier draw would hold tickets
+  // back from the look-back chains (an item whose neighbour sits reserved
+  // behind a running item waits for both).  Items only ever wait on items
+  // with smaller tickets, all of which are done or in hand of a running CTA,
+  // so the loop cannot deadlock.
   for (uint32_t it = 0;; ++it) {
   const int tk = sm.ticket;
   if (tk >= n_items) break;
@@ -181,185 +222,134 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
     break;
   }
-  const float bias = (valid && a.dt_bias) ? sm.bias[lane] : 0.0f;
-  const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
-  const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
-  const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
-  float2 A2[P];
-  if (valid) {
-    load_scaled_pairs<N>(A2, sm.Araw + lane * N, kLog2e);
-  } else {
-#pragma unroll
-    for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
-  }
 
-  const int tb = s * kK;
-  // ---- 1. per-token values (registers); lanes without a channel get u = g = 0
-  //         so that every partial they feed into a channel sum is exactly 0
-  float dl[kK], sg[kK], uu[kK], g[kK], dzf[kK];
-  int rst = 0;  // bit k: token tb+k starts a sequence (warp-uniform)
-#pragma unroll
-  for (int k = 0; k < kK; ++k) {
-    const int t = tb + k;
-    dl[k] = sg[k] = uu[k] = g[k] = dzf[k] = 0.0f;
-    if (t < rows) {
-      const float r = to_f(sm.dr[t * bx + lane]) + bias;
+  // ---- 1. per-(token, channel) values; all zero past the last token and on
+  //         channels past D (a = 1, b = 0, g = 0 there), so that those feed
+  //         exactly 0 into every sum they enter
+  // a warp's 32 lanes take 8 channels x 4 tokens: the [channel][token]
+  // stores then hit 32 different banks
+  for (int i = tid; i < kL * kTile; i += kThr) {
+    const int b = i >> 5, l = i & 31;
+    const int c = 8 * (b & 3) + (l >> 2), t = 4 * (b >> 2) + (l & 3);
+    const bool vt = t < rows, vd = c < bx && d0 + c < a.D;
+    float dlv = 0.0f, sgv = 0.0f, uv = 0.0f, gv = 0.0f;
+    if (vt && vd) {
+      const float r = to_f(sm.dr[t * bx + c]) + (a.dt_bias ? sm.bias[c] : 0.0f);
       if (a.delta_softplus) {
-        dl[k] = softplusf(r);
-        sg[k] = sigmoidf_fast(r);
+        dlv = softplusf(r);
+        sgv = sigmoidf_fast(r);
       } else {
-        dl[k] = r;
-        sg[k] = 1.0f;
+        dlv = r;
+        sgv = 1.0f;
       }
-      uu[k] = valid ? to_f(sm.u[t * bx + lane]) : 0.0f;
-      const float go = valid ? to_f(sm.dout[t * bx + lane]) : 0.0f;
-      if (a.has_z) {
-        const float zz = to_f(sm.z[t * bx + lane]);
-        const float sz = sigmoidf_fast(zz);
-        g[k] = go * (zz * sz);
-        dzf[k] = go * sz * fmaf(zz, 1.0f - sz, 1.0f);
-      } else {
-        g[k] = go;
-      }
-      const int pt = t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t);
-      if (pt == 0) rst |= 1 << k;
+      uv = to_f(sm.u[t * bx + c]);
+      const float go = to_f(sm.dout[t * bx + c]);
+      gv = a.has_z ? go * siluf(to_f(sm.z[t * bx + c])) : go;
     }
+    sm.dl[c * kP + t] = dlv;
+    sm.dlu[c * kP + t] = dlv * uv;
+    sm.g[c * kP + t] = gv;
+    sm.sg[c * kP + t] = sgv;
   }
-  __syncthreads();  // Bf, Cf complete
-
-  // ---- 2. both aggregates of my K tokens: forward (state from 0) and reverse
-  //         (carry leaving to the left when nothing enters from the right)
-  {
-    float2 h[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
-    float sd = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kK; ++k) {
-      const int t = tb + k;
-      if (t >= rows) break;
-      if (rst & (1 << k)) {
-#pragma unroll
-        for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
-        sd = 0.0f;
-      }
-      const float2 dl2 = splat2(dl[k]), du2 = splat2(dl[k] * uu[k]);
-      float2 Bv[P];
-      lds_pairs<N>(Bv, Bf + t * N);
-#pragma unroll
-      for (int i = 0; i < P; ++i) h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
-      sd += dl[k];
-    }
-    float2 q[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) q[i] = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int k = kK - 1; k >= 0; --k) {
-      const int t = tb + k;
-      if (t >= rows) continue;
-      float2 Cv[P];
-      lds_pairs<N>(Cv, Cf + t * N);
-      // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
-      const float2 off2 = splat2((rst & (1 << k)) ? -INFINITY : 0.0f);
-      const float2 dl2 = splat2(dl[k]), g2 = splat2(g[k]);
-#pragma unroll
-      for (int i = 0; i < P; ++i) q[i] = mul2(ex2x2(fma2(dl2, A2[i], off2)), fma2(Cv[i], g2, q[i]));
-    }
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-      sm.aggH[(s * N + 2 * i) * kTile + lane] = h[i].x;
-      sm.aggH[(s * N + 2 * i + 1) * kTile + lane] = h[i].y;
-      sm.aggG[(s * N + 2 * i) * kTile + lane] = q[i].x;
-      sm.aggG[(s * N + 2 * i + 1) * kTile + lane] = q[i].y;
-    }
-    sm.aggSD[s * kTile + lane] = sd;
-    if (lane == 0) sm.aggRS[s] = rst != 0;
+  for (int i = tid; i < N * kL; i += kThr) {
+    const int t = i / N, n = i - t * N;  // consecutive lanes: consecutive states
+    sm.BT[n * kP + t] = t < rows ? to_f(sm.B[t * N + n]) : 0.0f;
+    sm.CT[n * kP + t] = t < rows ? to_f(sm.C[t * N + n]) : 0.0f;
   }
+  // bit t: token t starts a sequence
+  const unsigned rst =
+      __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
+  // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
+  if (w == 0) sm.off[lane] = ((rst >> lane) & 1u) ? -INFINITY : 0.0f;
+  const int n0 = 2 * w;
+  float2 A2 = make_float2(0.0f, 0.0f), h = make_float2(0.0f, 0.0f);
+  if (valid) {
+    A2 = make_float2(sm.Araw[lane * N + n0] * kLog2e, sm.Araw[lane * N + n0 + 1] * kLog2e);
+    h = make_float2(sm.H[n0 * bx + lane], sm.H[(n0 + 1) * bx + lane]);
+  }
+  const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
   __syncthreads();
 
-  // ---- 3. both in-CTA scans over the kS sub-chunks; chain (lane, n), n % kS == s.
-  //         Forward: exclusive prefix seeded with the saved state of the chunk.
-  //         Reverse: exclusive suffix with nothing entering from the right.
+  // ---- 2. forward walk over the 32 tokens (state pair n0, n0+1)
+  float2 hist[kL];
+  float2 E = make_float2(1.0f, 1.0f), tot = make_float2(0.0f, 0.0f);
+  float2 vprev = make_float2(0.0f, 0.0f);  // column-sum values of the previous token
   {
-    float sdj[kS];
-    int rsj[kS];
+    const float* rowc = sm.dl + lane * kP;
 #pragma unroll
-    for (int j = 0; j < kS; ++j) {
-      sdj[j] = sm.aggSD[j * kTile + lane];
-      rsj[j] = sm.aggRS[j];
-    }
+    for (int kb = 0; kb < kL / 4; ++kb) {
+      const float4 dl4 = *reinterpret_cast<const float4*>(rowc + 4 * kb);
+      const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
+      const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
+      const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + n0 * kP + 4 * kb);
+      const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + (n0 + 1) * kP + 4 * kb);
+      const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + n0 * kP + 4 * kb);
+      const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + (n0 + 1) * kP + 4 * kb);
+      const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
+      const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
+      const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
+      const float dua[4] = {du4.x, du4.y, du4.z, du4.w};
+      const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
+      const float bxa[4] = {bx4.x, bx4.y, bx4.z, bx4.w}, bya[4] = {by4.x, by4.y, by4.z, by4.w};
+      const float cxa[4] = {cx4.x, cx4.y, cx4.z, cx4.w}, cya[4] = {cy4.x, cy4.y, cy4.z, cy4.w};
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      if (n % kS != s) continue;
-      const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-      float Pj[kS], Hj[kS], Gj[kS];
-#pragma unroll
-      for (int j = 0; j < kS; ++j) {
-        Pj[j] = rsj[j] ? 0.0f : ex2(a2 * sdj[j]);
-        Hj[j] = sm.aggH[(j * N + n) * kTile + lane];
-        Gj[j] = sm.aggG[(j * N + n) * kTile + lane];
+      for (int e = 0; e < 4; ++e) {
+        const int t = 4 * kb + e;
+        const float2 at = ex2x2(fma2(splat2(dla[e]), A2, splat2(ofa[e])));
+        const float2 Ct = make_float2(cxa[e], cya[e]);
+        h = fma2(at, h, mul2(splat2(dua[e]), make_float2(bxa[e], bya[e])));
+        hist[t] = h;
+        E = mul2(E, at);
+        tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
+        if (a.has_z) sm.part[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
+        const float2 vc = mul2(splat2(ga[e]), h);  // dC contributions
+        if (t & 1) WarpColumnSum::put(csw, lane, (t & 15) >> 1, vprev, vc);
+        vprev = vc;
+        if ((t & 15) == 15) {
+          __syncwarp();
+          const float sum = WarpColumnSum::reduce(csw, lane);
+          const int col = WarpColumnSum::column(lane);
+          const int tt = (t - 15) + (col >> 1);
+          if (tt < rows)
+            a.part_dBC[((int64_t)tile * 2 * N + N + n0 + (col & 1)) * a.T + t0 + tt] = sum;
+          __syncwarp();
+        }
       }
-      float x = valid ? sm.Hraw[lane * N + n] : 0.0f;
-#pragma unroll
-      for (int j = 0; j < kS; ++j) {
-        sm.aggH[(j * N + n) * kTile + lane] = x;
-        x = fmaf(Pj[j], x, Hj[j]);
-      }
-      float y = 0.0f;
-#pragma unroll
-      for (int j = kS - 1; j >= 0; --j) {
-        sm.aggG[(j * N + n) * kTile + lane] = y;
-        y = fmaf(Pj[j], y, Gj[j]);
-      }
-      sm.tot[n * kTile + lane] = y;
     }
   }
-  __syncthreads();
 
-  // ---- 4. decoupled look-back towards higher chunks (warp 0); the other warps
-  //         go straight on to step 5, which needs no carry from the right
-  if (s == 0) {
-    int rs_any = 0;
-    float sd_tot = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kS; ++j) {
-      rs_any |= sm.aggRS[j];
-      sd_tot += sm.aggSD[j * kTile + lane];
-    }
+  // ---- 3. decoupled look-back towards higher chunks (every warp for its pair)
+  float2 x = make_float2(0.0f, 0.0f);
+  {
     const int64_t base = (int64_t)tile * a.n_chunks;
-    const int64_t slot = base + chunk;
+    const int64_t wslot = (base + chunk) * W + w;
     const bool publish = (long long)tk != a.drop_ticket;
-    float* my_agg = a.agg + slot * (N * kTile);
-    float* my_inc = a.incl + slot * (N * kTile);
-    // every lane is its own chain (one channel): it publishes its payload and
-    // then its own flag with a release store, and readers acquire that flag
-    int* my_flag = a.flags + slot * kTile + lane;
+    float2* const agg = reinterpret_cast<float2*>(a.agg);
+    float2* const aggp = reinterpret_cast<float2*>(a.agg_sd);
+    float2* const inc = reinterpret_cast<float2*>(a.incl);
+    int* const my_flag = a.flags + wslot;
+    // a sequence starts in this chunk: E = 0 exactly, and the carry leaving
+    // to the left does not depend on what enters from the right
+    const bool rs_any = (rst & (rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u))) != 0u;
     if (rs_any) {
-      // a sequence starts in this chunk: the carry leaving it to the left does
-      // not depend on what enters from the right, publish it at once
-#pragma unroll
-      for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.tot[n * kTile + lane];
-      if (publish) st_release_gpu(my_flag, kFlagInclusive);
+      inc[wslot * 32 + lane] = tot;
+      publish_flag(my_flag, kFlagInclusive, publish, lane);
     }
-    float x[N];
-#pragma unroll
-    for (int n = 0; n < N; ++n) x[n] = 0.0f;
     if (chunk < a.n_chunks - 1) {
       // the next chunk of the tile started long before this one and has
       // usually published its inclusive carry: look first, and publish this
       // chunk's aggregate only when the walk has to go further
       int j = chunk + 1, found = -1, timed_out = 0;
-      if (ld_acquire_gpu(a.flags + (base + j) * kTile + lane) == kFlagInclusive) {
+      if (__all_sync(0xffffffffu, ld_acquire_gpu(a.flags + (base + j) * W + w) == kFlagInclusive)) {
         found = j;
       } else {
         if (!rs_any) {
-#pragma unroll
-          for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.tot[n * kTile + lane];
-          a.agg_sd[slot * kTile + lane] = sd_tot;
-          if (publish) st_release_gpu(my_flag, kFlagAggregate);
+          agg[wslot * 32 + lane] = tot;
+          aggp[wslot * 32 + lane] = E;
+          publish_flag(my_flag, kFlagAggregate, publish, lane);
         }
         while (j < a.n_chunks) {
-          const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
+          const int f = wait_flag(a.flags + (base + j) * W + w, a.wait_ns);
           if (f == kFlagInclusive) { found = j; break; }
           if (f == kFlagNone) { timed_out = 1; break; }
           ++j;
@@ -368,210 +358,151 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int last = j - 1;
       if (found >= 0) {
-        const float* inc = a.incl + (base + found) * (N * kTile);
-#pragma unroll
-        for (int n = 0; n < N; ++n) x[n] = __ldcg(inc + n * kTile + lane);
+        x = __ldcg(inc + ((base + found) * W + w) * 32 + lane);
         last = found - 1;
       }
       for (int i = last; i > chunk; --i) {
-        const float* ag = a.agg + (base + i) * (N * kTile);
-        const float sdi = __ldcg(a.agg_sd + (base + i) * kTile + lane);
+        const int64_t ws = ((base + i) * W + w) * 32 + lane;
+        x = fma2(__ldcg(aggp + ws), x, __ldcg(agg + ws));
+      }
+    }
+    if (!rs_any) {
+      // released at once: the previous chunk of the tile may already be
+      // waiting, and every link of that chain adds this item's delay
+      inc[wslot * 32 + lane] = fma2(E, x, tot);
+      publish_flag(my_flag, kFlagInclusive, publish, lane);
+    }
+  }
+  __syncthreads();  // y partials complete
+
+  // ---- 4. y = C.h + Dskip u and dz
+  if (a.has_z) {
+    T* gdz = static_cast<T*>(a.dz);
+    for (int i = tid; i < kL * kTile; i += kThr) {
+      const int t = i / kTile, c = i - t * kTile;
+      if (t >= rows || c >= bx || d0 + c >= a.D) continue;
+      float y = 0.0f;
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-          x[n] = fmaf(ex2(a2 * sdi), x[n], __ldcg(ag + n * kTile + lane));
+      for (int v = 0; v < W; ++v) y += sm.part[(v * kL + t) * kTile + c];
+      const float uv = to_f(sm.u[t * bx + c]);
+      y = fmaf(a.Dskip ? sm.dsk[c] : 0.0f, uv, y);
+      const float go = to_f(sm.dout[t * bx + c]);
+      const float zz = to_f(sm.z[t * bx + c]);
+      const float sz = sigmoidf_fast(zz);
+      gdz[(t0 + t) * a.D + d0 + c] = from_f<T>(go * sz * fmaf(zz, 1.0f - sz, 1.0f) * y);
+    }
+  }
+  __syncthreads();  // part is reused below
+
+  // ---- 5. reverse walk in blocks of kRB tokens
+  float2 dA = make_float2(0.0f, 0.0f);
+  int next = 0;  // thread 0: the next ticket, drawn before the last block
+  float sDD = 0.0f, sDB = 0.0f;
+  {
+    float2* const part2 = reinterpret_cast<float2*>(sm.part);  // [2][W][kRB][kTile]
+    T* gdu = static_cast<T*>(a.du);
+    T* gddr = static_cast<T*>(a.ddr);
+    float2 r = x;  // carry entering the current token from the right
+#pragma unroll
+    for (int blk = kL / kRB - 1; blk >= 0; --blk) {
+      const int buf = blk & 1;
+      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
+#pragma unroll
+      for (int kb = (blk + 1) * kRB / 4 - 1; kb >= blk * kRB / 4; --kb) {
+        const float4 dl4 = *reinterpret_cast<const float4*>(sm.dl + lane * kP + 4 * kb);
+        const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
+        const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
+        const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + n0 * kP + 4 * kb);
+        const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + (n0 + 1) * kP + 4 * kb);
+        const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + n0 * kP + 4 * kb);
+        const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + (n0 + 1) * kP + 4 * kb);
+        const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
+        const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
+        const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
+        const float dua[4] = {du4.x, du4.y, du4.z, du4.w};
+        const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
+        const float bxa[4] = {bx4.x, bx4.y, bx4.z, bx4.w}, bya[4] = {by4.x, by4.y, by4.z, by4.w};
+        const float cxa[4] = {cx4.x, cx4.y, cx4.z, cx4.w}, cya[4] = {cy4.x, cy4.y, cy4.z, cy4.w};
+#pragma unroll
+        for (int e = 3; e >= 0; --e) {
+          const int t = 4 * kb + e;
+          const float2 at = ex2x2(fma2(splat2(dla[e]), A2, splat2(ofa[e])));
+          const float2 Bt = make_float2(bxa[e], bya[e]);
+          const float2 dh = fma2(make_float2(cxa[e], cya[e]), splat2(ga[e]), r);  // total gradient w.r.t. h_t
+          // a_t h_{t-1} = h_t - delta u B: no need for the previous state
+          const float2 dhq = mul2(dh, fma2(splat2(-dua[e]), Bt, hist[t]));
+          dA = fma2(splat2(dla[e]), dhq, dA);
+          part2[((buf * W + w) * kRB + (t - blk * kRB)) * kTile + lane] =
+              make_float2(fmaf(dh.x, Bt.x, dh.y * Bt.y), fmaf(A2.x, dhq.x, A2.y * dhq.y));
+          const float2 vb = mul2(dh, splat2(dua[e]));  // dB contributions
+          if (!(t & 1)) WarpColumnSum::put(csw, lane, (t & 15) >> 1, vb, vprev);
+          vprev = vb;
+          r = mul2(dh, at);  // carry to h_{t-1}
+          if ((t & 15) == 0) {
+            __syncwarp();
+            const float sum = WarpColumnSum::reduce(csw, lane);
+            const int col = WarpColumnSum::column(lane);
+            const int tt = t + (col >> 1);
+            if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + n0 + (col & 1)) * a.T + t0 + tt] = sum;
+            __syncwarp();
+          }
+        }
+      }
+      __syncthreads();  // the block's partials are complete
+      // du, d delta_raw of the block: thread i takes token blk*kRB + i / kTile,
+      // channel i % kTile (= lane), and adds the warps' partials in order
+      for (int i = tid; i < kRB * kTile; i += kThr) {
+        const int e = i / kTile;
+        const int t = blk * kRB + e;
+        float2 sp = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int v = 0; v < W; ++v) sp = __fadd2_rn(sp, part2[((buf * W + v) * kRB + e) * kTile + lane]);
+        if (t < rows && valid) {
+          const float dlt = sm.dl[lane * kP + t], gt = sm.g[lane * kP + t];
+          const float uv = to_f(sm.u[t * bx + lane]);
+          const float gdu_t = fmaf(dlt, sp.x, Dsk * gt);
+          const float gdr_t = fmaf(uv, sp.x, sp.y * kLn2) * sm.sg[lane * kP + t];
+          const int64_t at_td = (t0 + t) * a.D + d;
+          gdu[at_td] = from_f<T>(gdu_t);
+          gddr[at_td] = from_f<T>(gdr_t);
+          sDD = fmaf(gt, uv, sDD);
+          sDB += gdr_t;
         }
       }
     }
-#pragma unroll
-    for (int n = 0; n < N; ++n) sm.rin[n * kTile + lane] = x[n];
-    if (!rs_any) {
-      // released at once: the next chunk of the tile may already be waiting,
-      // and every link of that chain adds this item's publication delay
-#pragma unroll
-      for (int n = 0; n < N; ++n) {
-        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.tot[n * kTile + lane]);
-      }
-      if (publish) st_release_gpu(my_flag, kFlagInclusive);
-    }
   }
 
-  // ---- 5. recompute the forward states of my K tokens from my start state;
-  //         the first K-1 go to shared memory, the last stays in registers
-  float2 h[P];
-#pragma unroll
-  for (int i = 0; i < P; ++i)
-    h[i] = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
-  float yk[kK];
-#pragma unroll
-  for (int k = 0; k < kK; ++k) {
-    const int t = tb + k;
-    yk[k] = 0.0f;
-    if (t >= rows) continue;
-    if (rst & (1 << k)) {
-#pragma unroll
-      for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
-    }
-    const float2 dl2 = splat2(dl[k]), du2 = splat2(dl[k] * uu[k]);
-    float2 Bv[P], Cv[P];
-    lds_pairs<N>(Bv, Bf + t * N);
-    lds_pairs<N>(Cv, Cf + t * N);
-    float2 y2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-      h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
-      y2 = fma2(Cv[i], h[i], y2);
-    }
-    if (k < kK - 1) {
-#pragma unroll
-      for (int i = 0; i < P; i += 2)
-        sm.hist[(k * (N / 4) + i / 2) * kThreads + tid] = make_float4(h[i].x, h[i].y, h[i + 1].x, h[i + 1].y);
-    }
-    yk[k] = fmaf(Dsk, uu[k], y2.x + y2.y);
+  // ---- 6. dA partials of the chunk ([chunk][n][d]); fixed-order CTA sums of
+  //         the dDskip and d_dt_bias partials
+  if (valid) {
+    a.part_dA[((int64_t)chunk * N + n0) * a.D + d] = dA.x;
+    a.part_dA[((int64_t)chunk * N + n0 + 1) * a.D + d] = dA.y;
   }
-  __syncthreads();
-
-  // the next ticket, drawn now and used once this item's inputs are consumed
-  // (the atomic's latency hides behind step 7)
-  // ---- 6. carry entering my last token from the right
-  float2 dh[P];
-  {
-    int rs_post = 0;
-    float sd_post = 0.0f;
-    for (int j = s + 1; j < kS; ++j) {
-      rs_post |= sm.aggRS[j];
-      sd_post += sm.aggSD[j * kTile + lane];
-    }
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-      const float2 E = make_float2(sm.aggG[(s * N + 2 * i) * kTile + lane],
-                                   sm.aggG[(s * N + 2 * i + 1) * kTile + lane]);
-      const float2 R = make_float2(sm.rin[(2 * i) * kTile + lane], sm.rin[(2 * i + 1) * kTile + lane]);
-      dh[i] = rs_post ? E : fma2(ex2x2(mul2(A2[i], splat2(sd_post))), R, E);
-    }
-  }
-
-  // ---- 7. reverse walk over my tokens
-  float2 dA[P];
-#pragma unroll
-  for (int i = 0; i < P; ++i) dA[i] = make_float2(0.0f, 0.0f);
-  float sDD = 0.0f, sDB = 0.0f;
-  T* gdu = static_cast<T*>(a.du);
-  T* gddr = static_cast<T*>(a.ddr);
-  T* gdz = static_cast<T*>(a.dz);
-#pragma unroll
-  for (int k = kK - 1; k >= 0; --k) {
-    const int t = tb + k;
-    if (t >= rows) continue;  // warp-uniform
-    float2 Bv[P], Cv[P];
-    lds_pairs<N>(Bv, Bf + t * N);
-    lds_pairs<N>(Cv, Cf + t * N);
-    const float2 off2 = splat2((rst & (1 << k)) ? -INFINITY : 0.0f);
-    const float2 dl2 = splat2(dl[k]), g2 = splat2(g[k]), du2 = splat2(dl[k] * uu[k]);
-    float v[V];
-    float2 s1 = make_float2(0.0f, 0.0f), s2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < P; i += 2) {
-      float2 hc[2], hp[2];
-      if (k == kK - 1) {
-        hc[0] = h[i];
-        hc[1] = h[i + 1];
-      } else {
-        const float4 c4 = sm.hist[(k * (N / 4) + i / 2) * kThreads + tid];
-        hc[0] = make_float2(c4.x, c4.y);
-        hc[1] = make_float2(c4.z, c4.w);
-      }
-      if (k > 0) {
-        const float4 p4 = sm.hist[((k - 1) * (N / 4) + i / 2) * kThreads + tid];
-        hp[0] = make_float2(p4.x, p4.y);
-        hp[1] = make_float2(p4.z, p4.w);
-      } else {
-        hp[0] = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
-        hp[1] = make_float2(sm.aggH[(s * N + 2 * i + 2) * kTile + lane], sm.aggH[(s * N + 2 * i + 3) * kTile + lane]);
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = i + e;
-        dh[j] = fma2(Cv[j], g2, dh[j]);  // total gradient w.r.t. h_t
-        const float2 at = ex2x2(fma2(dl2, A2[j], off2));
-        const float2 dhq = mul2(dh[j], mul2(at, hp[e]));
-        dA[j] = fma2(dl2, dhq, dA[j]);
-        s2 = fma2(A2[j], dhq, s2);
-        s1 = fma2(dh[j], Bv[j], s1);
-        const float2 vb = mul2(dh[j], du2);   // 0 on lanes without a channel (u = 0)
-        const float2 vc = mul2(g2, hc[e]);    // 0 on lanes without a channel (g = 0)
-        v[2 * j] = vb.x;
-        v[2 * j + 1] = vb.y;
-        v[N + 2 * j] = vc.x;
-        v[N + 2 * j + 1] = vc.y;
-        dh[j] = mul2(dh[j], at);               // carry to h_{t-1}
-      }
-    }
-    const float s1t = s1.x + s1.y, s2t = s2.x + s2.y;
-    const float gdu_t = fmaf(dl[k], s1t, Dsk * g[k]);
-    const float gdl_t = fmaf(uu[k], s1t, s2t * kLn2);
-    const float gdr_t = gdl_t * sg[k];
-    sDD = fmaf(g[k], uu[k], sDD);
-    sDB += gdr_t;
-    const int64_t at_td = (t0 + t) * a.D + d;
-    if (valid) {
-      gdu[at_td] = from_f<T>(gdu_t);
-      gddr[at_td] = from_f<T>(gdr_t);
-      if (gdz) gdz[at_td] = from_f<T>(dzf[k] * yk[k]);
-    }
-    ReduceScatter<V, 16>::run(v, lane);
-    if ((lane & (kRep - 1)) == 0)
-      a.part_dBC[((int64_t)tile * a.T + t0 + t) * V + lane / kRep] = v[0];
-  }
-
-  // ---- 8. fixed-order CTA reduction of dA, dDskip, d_dt_bias partials
+  sm.redD[w * kTile + lane] = sDD;
+  sm.redB[w * kTile + lane] = sDB;
   __syncthreads();
   // no input buffer is read any more: draw the next item and request its
-  // inputs, which land while this item finishes its reductions
+  // inputs, which land while this item writes its last partials
   if (tid == 0) {
-    const int next = (int)atomicAdd(a.ticket, 1u);
     sm.ticket = next;
     if (next < n_items) issue(next);
   }
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    sm.aggH[(s * N + 2 * i) * kTile + lane] = dA[i].x;
-    sm.aggH[(s * N + 2 * i + 1) * kTile + lane] = dA[i].y;
-  }
-  sm.redD[s * kTile + lane] = sDD;
-  sm.redB[s * kTile + lane] = sDB;
-  __syncthreads();
-#pragma unroll
-  for (int n = 0; n < N; ++n) {
-    if (n % kS != s) continue;
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kS; ++j) acc += sm.aggH[(j * N + n) * kTile + lane];
-    sm.aggG[lane * (N + 4) + n] = acc;
-  }
-  if (s == 0 && valid) {
+  if (w == 0 && valid) {
     float accD = 0.0f, accB = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kS; ++j) {
-      accD += sm.redD[j * kTile + lane];
-      accB += sm.redB[j * kTile + lane];
+    for (int v = 0; v < W; ++v) {
+      accD += sm.redD[v * kTile + lane];
+      accB += sm.redB[v * kTile + lane];
     }
     a.part_dD[(int64_t)chunk * a.D + d] = accD;
     a.part_dbias[(int64_t)chunk * a.D + d] = accB;
   }
-  __syncthreads();
-  // the tile's dA partial block is contiguous in part_dA: write it coalesced
-  {
-    float* dst = a.part_dA + ((int64_t)chunk * a.D + d0) * N;
-    const int nvalid = (a.D - d0 < kTile ? a.D - d0 : kTile) * N;
-    for (int i = tid; i < nvalid; i += kThreads) dst[i] = sm.aggG[(i / N) * (N + 4) + (i % N)];
-  }
+  __syncthreads();  // redD / redB and the ticket are consumed before the next pass
   }  // persistent loop
 }
 
-// dB[t][n] = sum over tiles of part[tile][t][n]; dC[t][n] likewise from
-// part[tile][t][N + n].  One thread per output, tiles summed in order.
+// dB[t][n] = sum over tiles of part[tile][n][t]; dC[t][n] likewise from
+// part[tile][N + n][t].  One thread per output, tiles summed in order.
 __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restrict__ part,
                                                            int n_tiles, int64_t T, int N,
                                                            float* __restrict__ dB,
@@ -581,34 +512,34 @@ __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restri
   if (i >= M) return;
   float acc = 0.0f;
   for (int k = 0; k < n_tiles; ++k) acc += __ldcs(part + (int64_t)k * M + i);
-  const int64_t t = i / (2 * N);
-  const int j = (int)(i - t * 2 * N);
-  if (j < N) dB[t * N + j] = acc; else dC[t * N + (j - N)] = acc;
+  const int64_t v = i / T;
+  const int64_t t = i - v * T;
+  if (v < N) dB[t * N + v] = acc; else dC[t * N + (v - N)] = acc;
 }
 
 template <typename T, int N>
 cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
-                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, cudaStream_t st) {
+                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                     cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem<T, N>);
   cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
   int grid = 0;
-  e = persistent_grid(scan_bwd_kernel<T, N>, kThreads, smem, items, &grid);
+  e = persistent_grid(scan_bwd_kernel<T, N>, 16 * N, smem, items, &grid);
   if (e != cudaSuccess) return e;
-  scan_bwd_kernel<T, N><<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, a);
+  scan_bwd_kernel<T, N><<<grid, 16 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, a);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
-                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, cudaStream_t st) {
-  if (a.N == 16) return launch_n<T, 16>(a, tm_u, tm_dr, tm_z, tm_dout, st);
-  if (a.N == 8) return launch_n<T, 8>(a, tm_u, tm_dr, tm_z, tm_dout, st);
-  if constexpr (sizeof(T) == 4) {
-    if (a.N == 4) return launch_n<T, 4>(a, tm_u, tm_dr, tm_z, tm_dout, st);
-  }
+                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                     cudaStream_t st) {
+  if (a.N == 16) return launch_n<T, 16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
+  if (a.N == 8) return launch_n<T, 8>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
+  if (a.N == 4) return launch_n<T, 4>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
   return cudaErrorInvalidValue;
 }
 
@@ -616,8 +547,8 @@ cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
 
 cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z,
-                            const CUtensorMap& tm_dout, float* dA, float* dB, float* dC,
-                            float* dDskip, float* d_dt_bias, cudaStream_t st) {
+                            const CUtensorMap& tm_dout, const CUtensorMap& tm_cs, float* dA,
+                            float* dB, float* dC, float* dDskip, float* d_dt_bias, cudaStream_t st) {
   const int64_t DN = (int64_t)a.D * a.N;
   if (a.T <= 0) {
     cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * DN, st);
@@ -625,15 +556,16 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
     if (e == cudaSuccess && d_dt_bias) e = cudaMemsetAsync(d_dt_bias, 0, sizeof(float) * a.D, st);
     return e;
   }
-  cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, st)
-                                : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, st);
+  cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st)
+                                : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
   if (e != cudaSuccess) return e;
   const int64_t M = a.T * 2 * a.N;
   sum_tiles_bc_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(a.part_dBC, a.n_tiles, a.T, a.N,
                                                                    dB, dC);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_sum_rows(a.part_dA, a.n_chunks, DN, DN, dA, st);
+  // part_dA is [chunk][n][d]: sum over chunks, written out as dA[d][n]
+  e = launch_sum_rows(a.part_dA, a.n_chunks, DN, DN, dA, st, a.D);
   if (e == cudaSuccess && dDskip) e = launch_sum_rows(a.part_dD, a.n_chunks, a.D, a.D, dDskip, st);
   if (e == cudaSuccess && d_dt_bias)
     e = launch_sum_rows(a.part_dbias, a.n_chunks, a.D, a.D, d_dt_bias, st);

@@ -150,7 +150,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   __syncthreads();
   float2 A2[P];
   if (valid) {
-    load_scaled_pairs<N>(A2, sm.Araw + lane * N, kLog2e);
+    load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, kLog2e);
   } else {
 #pragma unroll
     for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
@@ -158,7 +158,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
   // ---- step 2: delta for my tokens
-#pragma unroll
+#pragma unroll 2  // the tokens come from shared memory: keep the code small
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     const float r = to_f(sm.dr[t * bx + lane]) + bias;
@@ -171,7 +171,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
   float sd = 0.0f;
   int rs = 0;
-#pragma unroll
+#pragma unroll 2  // the tokens come from shared memory: keep the code small
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
@@ -329,14 +329,17 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   const int64_t ts = t0 + tb;
   if (a.chunk_states && valid && ts < a.T && (ts % kStateChunk) == 0) {
-    float* cs = a.chunk_states + ((ts / kStateChunk) * a.D + d) * N;
+    // layout [chunk][n][d]: the 32 lanes store 32 consecutive floats per state
+    float* cs = a.chunk_states + (ts / kStateChunk) * N * a.D + d;
 #pragma unroll
-    for (int i = 0; i < P; i += 2)
-      *reinterpret_cast<float4*>(cs + 2 * i) = make_float4(h[i].x, h[i].y, h[i + 1].x, h[i + 1].y);
+    for (int i = 0; i < P; ++i) {
+      cs[(2 * i) * (int64_t)a.D] = h[i].x;
+      cs[(2 * i + 1) * (int64_t)a.D] = h[i].y;
+    }
   }
 
   T* out = static_cast<T*>(a.out);
-#pragma unroll
+#pragma unroll 2  // the tokens come from shared memory: keep the code small
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
