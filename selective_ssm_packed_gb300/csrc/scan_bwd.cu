@@ -228,6 +228,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   //         exactly 0 into every sum they enter
   // a warp's 32 lanes take 8 channels x 4 tokens: the [channel][token]
   // stores then hit 32 different banks
+#pragma unroll
   for (int i = tid; i < kL * kTile; i += kThr) {
     const int b = i >> 5, l = i & 31;
     const int c = 8 * (b & 3) + (l >> 2), t = 4 * (b >> 2) + (l & 3);
@@ -236,8 +237,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (vt && vd) {
       const float r = to_f(sm.dr[t * bx + c]) + (a.dt_bias ? sm.bias[c] : 0.0f);
       if (a.delta_softplus) {
-        dlv = softplusf(r);
-        sgv = sigmoidf_fast(r);
+        dlv = softplus_sig(r, &sgv);
       } else {
         dlv = r;
         sgv = 1.0f;
@@ -251,6 +251,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     sm.g[c * kP + t] = gv;
     sm.sg[c * kP + t] = sgv;
   }
+#pragma unroll
   for (int i = tid; i < N * kL; i += kThr) {
     const int t = i / N, n = i - t * N;  // consecutive lanes: consecutive states
     sm.BT[n * kP + t] = t < rows ? to_f(sm.B[t * N + n]) : 0.0f;
