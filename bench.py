@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import ctypes
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -65,6 +66,12 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-comparators", action="store_true",
+                   help="skip the no-reset concat bound and the packed-vs-padded comparison")
+    p.add_argument("--comparator-steps", type=int, default=10)
+    p.add_argument("--comparator-d", type=int, default=512,
+                   help="channels for the packed-vs-padded comparison (the padded long-tail layout "
+                        "holds ~2.2 M tokens)")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target wall time of the CPU-oracle baseline sample")
     return p.parse_args(argv)
@@ -261,6 +268,99 @@ def probe_alu():
     return out
 
 
+def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=None):
+    """Seconds per full step (pos, conv fwd, scan fwd, scan bwd, conv bwd) for
+    the packed layout cu_np, on seeded device-generated inputs (timing only)."""
+    import numpy as np
+    tdt = dtype or torch.bfloat16
+    T = int(cu_np[-1])
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def rnd(*shape, scale=1.0):
+        return (scale * torch.randn(*shape, generator=g, device=device)).to(tdt)
+
+    x, dr, z, dout = rnd(T, D), rnd(T, D, scale=0.5), rnd(T, D), rnd(T, D)
+    B, C = rnd(T, N), rnd(T, N)
+    A = (-(torch.arange(N, device=device, dtype=torch.float32) + 1.0)).repeat(D, 1).contiguous()
+    Dsk = torch.ones(D, device=device)
+    dt = torch.exp(torch.empty(D, device=device).uniform_(math.log(1e-3), math.log(1e-1), generator=g))
+    dtb = (dt + torch.log(-torch.expm1(-dt))).contiguous()
+    bound = 1.0 / math.sqrt(Wc)
+    cw = torch.empty(D, Wc, device=device).uniform_(-bound, bound, generator=g)
+    cb = torch.empty(D, device=device).uniform_(-bound, bound, generator=g)
+    cu = torch.from_numpy(np.ascontiguousarray(cu_np, dtype=np.int32)).to(device)
+    pos = torch.empty(T, dtype=torch.int32, device=device)
+    u = torch.empty(T, D, dtype=tdt, device=device)
+    out = torch.empty_like(u)
+    states = torch.empty(vs.chunk_states_shape(T, D, N), dtype=torch.float32, device=device)
+    grads = {"du": torch.empty_like(u), "ddelta_raw": torch.empty_like(u), "dz": torch.empty_like(u),
+             "dA": torch.empty(D, N, device=device), "dB": torch.empty(T, N, device=device),
+             "dC": torch.empty(T, N, device=device), "dDskip": torch.empty(D, device=device),
+             "d_dt_bias": torch.empty(D, device=device)}
+    dx = torch.empty_like(u)
+    dw = torch.empty(D, Wc, device=device)
+    db = torch.empty(D, device=device)
+    ws = {k: torch.empty(n, dtype=torch.uint8, device=device) for k, n in (
+        ("cf", binding.conv1d_fwd_workspace_size(T, D, Wc)), ("cb", binding.conv1d_bwd_workspace_size(T, D, Wc)),
+        ("sf", binding.scan_fwd_workspace_size(T, D, N)), ("sb", binding.scan_bwd_workspace_size(T, D, N)))}
+
+    def step():
+        vs.varlen_position_indices(cu, T, out=pos)
+        vs.varlen_conv1d_fwd(x, cw, cb, cu, pos, out=u, workspace=ws["cf"])
+        vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, chunk_states=states,
+                                     workspace=ws["sf"])
+        vs.varlen_selective_scan_bwd(u, dr, A, B, C, Dsk, z, dtb, dout, cu, states, pos, grads=grads,
+                                     workspace=ws["sb"])
+        vs.varlen_conv1d_bwd(x, cw, cb, grads["du"], cu, pos, dx=dx, dweight=dw, dbias=db, workspace=ws["cb"])
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    for k in ("sf", "sb"):
+        st = binding.read_status(ws[k])
+        if st != 0:
+            raise RuntimeError(f"device status {binding.ERR.get(st, st)} in a comparator run ({k})")
+    return a.elapsed_time(b) / 1e3 / steps
+
+
+def comparators(args, torch, vs, binding, device, w, step_sec):
+    """The no-reset concat bound on the bench workload (cu_seqlens = [0, T],
+    same kernels) and the long-tail packs packed vs right-padded into the
+    buckets [512 .. 8192] (each sequence its own row), real tokens/s."""
+    import numpy as np
+    from selective_ssm_packed_gb300 import workloads as wls
+    wl = w["workload"]
+    T = w["T"]
+    res = {}
+    csec = time_case(torch, vs, binding, device, np.array([0, T], dtype=np.int32), wl.D, wl.N, wl.W,
+                     args.comparator_steps, seed=11)
+    res["concat_no_reset"] = {"value": T / csec, "unit": "tokens/s", "ms_per_step": csec * 1e3,
+                              "packed_over_concat": csec / step_sec,
+                              "config": f"{args.workload} with cu_seqlens = [0, {T}] (one sequence)"}
+    lengths = wls.pack_lengths("longtail")
+    cu_pk = wls.cu_seqlens_from_lengths(lengths)
+    cu_pad, _ = wls.padded_layout(lengths)
+    Dc = args.comparator_d
+    T_real, T_pad = int(cu_pk[-1]), int(cu_pad[-1])
+    psec = time_case(torch, vs, binding, device, cu_pk, Dc, 16, 4, args.comparator_steps, seed=12)
+    qsec = time_case(torch, vs, binding, device, cu_pad, Dc, 16, 4, max(2, args.comparator_steps // 4),
+                     seed=13)
+    res["longtail_packed_vs_padded"] = {
+        "packed_tokens_per_s": T_real / psec, "padded_real_tokens_per_s": T_real / qsec,
+        "speedup": qsec / psec, "real_tokens": T_real, "padded_tokens": T_pad,
+        "padding_rate": 1.0 - T_real / T_pad,
+        "config": f"long-tail packs ({len(lengths)} sequences, {T_real} tokens), D={Dc}, N=16, bf16, "
+                  f"buckets {list(wls.BUCKETS)}; same kernels, fwd+bwd"}
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -402,6 +502,11 @@ def run_ours(args):
         e2e = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": esec * 1e3, "steps": args.e2e_steps}
 
+    # --- comparators: no-reset concat bound, packed vs right-padded (rank 0, one GPU)
+    comp = None
+    if rank == 0 and world == 1 and not args.no_comparators:
+        comp = comparators(args, torch, vs, binding, device, w, sec / args.steps)
+
     # --- roofline of the dominant kernel, plus every stage for context
     counts = per_token_counts(D, N, e, Wc)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
@@ -459,7 +564,7 @@ def run_ours(args):
                 "warmup": args.warmup, "ms_per_step": sec_max * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": config_of(w, world), "roofline": roof, "path_roofline": path_roofline,
-                "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
+                "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "comparators": comp,
                 "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
     return 0
