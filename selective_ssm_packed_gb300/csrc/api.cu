@@ -289,7 +289,10 @@ int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
   ConvArgs a{};
   a.x = x; a.w = weight; a.bias = bias; a.pos = pos; a.out = u;
   a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
-  e = launch_conv1d_fwd(a, io, st);
+  const int bx = D < conv_tile_cols() ? D : conv_tile_cols();
+  CUtensorMap mx;
+  VSSM_TRY(make_map(&mx, x, io, total_tokens, D, bx, conv_tile_rows(W, false, true)));
+  e = launch_conv1d_fwd(a, io, mx, st);
   return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_fwd launch");
 }
 
@@ -315,7 +318,15 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
   a.x = x; a.w = weight; a.bias = bias; a.pos = pos; a.du = du; a.out = dx;
   a.partial = at<float>(workspace, l.conv_part);
   a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
-  e = launch_conv1d_bwd(a, io, dweight, dbias, st);
+  CUtensorMap mx, mdu;
+  std::memset(&mx, 0, sizeof(mx));
+  std::memset(&mdu, 0, sizeof(mdu));
+  if (total_tokens > 0) {
+    const int bx = D < conv_tile_cols() ? D : conv_tile_cols();
+    VSSM_TRY(make_map(&mx, x, io, total_tokens, D, bx, conv_tile_rows(W, true, true)));
+    VSSM_TRY(make_map(&mdu, du, io, total_tokens, D, bx, conv_tile_rows(W, true, false)));
+  }
+  e = launch_conv1d_bwd(a, io, mx, mdu, dweight, dbias, st);
   return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_bwd launch");
 }
 

@@ -1,15 +1,16 @@
 // conv.cu -- packed depthwise causal conv1d (width W <= 4), forward and backward.
 //
-// Layout: thread block = 32 threads along channels x 8 along tokens; a 1-D grid
-// where consecutive blocks cover consecutive channel columns of the same token
-// rows, so the blocks running together read and write whole rows.  Each
-// thread owns V consecutive channels (one 16-byte vector in the forward, an
-// 8/16-byte vector in the backward) and a short run of R consecutive tokens,
-// so every warp reads and writes whole contiguous row segments.  The
-// sequence-boundary mask comes from position_indices: tap k (k tokens back)
-// is used only if pos[t] >= k, and in the backward the tap that token t feeds
-// k tokens later is used only if pos[t+k] >= k (the conv1d_pack early stop of
-// the article "Shanghai AI Lab: packed variable-length Mamba training").
+// One CTA per tile of 64 tokens x 128 channels.  The x rows of the tile (plus
+// the W-1 rows before it, and for the backward the W-1 after it) and the du
+// rows come into shared memory by 2-D tensor copies, so every row is read from
+// HBM about once; rows before the first token or past the last are zero-filled
+// by the copy.  Warp w owns 8 consecutive tokens of the tile, lane l owns 4
+// consecutive channels, so stores are whole 256- or 512-byte row segments per
+// warp.  The sequence-boundary mask comes from position_indices: tap k (k
+// tokens back) is used only if pos[t] >= k, and in the backward the tap that
+// token t feeds k tokens later is used only if pos[t+k] >= k (the conv1d_pack
+// early stop of the article "Shanghai AI Lab: packed variable-length Mamba
+// training").
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,29 +18,9 @@ namespace vssm {
 
 namespace {
 
-constexpr int kRowsPerBlock = 8;  // threadIdx.y extent
-constexpr int kFwdRun = 8;        // tokens per thread, forward
-constexpr int kBwdRun = 8;        // tokens per thread, backward
 
-template <typename T, int V>
-__device__ __forceinline__ void stv(T* p, const float (&v)[V]);
-
-// 16-byte loads / stores
-template <>
-__device__ __forceinline__ void stv<float, 4>(float* p, const float (&v)[4]) {
-  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-}
-template <>
-__device__ __forceinline__ void stv<__nv_bfloat16, 8>(__nv_bfloat16* p, const float (&v)[8]) {
-  uint4 q;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-  *reinterpret_cast<uint4*>(p) = q;
-}
-// 8-byte bf16 loads / stores (backward, 4 channels per thread)
-template <>
-__device__ __forceinline__ void stv<__nv_bfloat16, 4>(__nv_bfloat16* p, const float (&v)[4]) {
+// 8-byte bf16 store of 4 channels
+__device__ __forceinline__ void st_bf16x4(__nv_bfloat16* p, const float (&v)[4]) {
   uint2 q;
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
   h[0] = __floats2bfloat162_rn(v[0], v[1]);
@@ -52,289 +33,310 @@ __device__ __forceinline__ float silu_grad(float x) {
   return s * fmaf(x, 1.0f - s, 1.0f);
 }
 
-// Raw (still packed) row segments: loaded in one vector access, widened later.
-template <typename T, int V> struct RawRow;
-template <> struct RawRow<float, 4> { uint4 r; };
-template <> struct RawRow<__nv_bfloat16, 8> { uint4 r; };
-template <> struct RawRow<__nv_bfloat16, 4> { uint2 r; };
+// ------------------------------------------------------------------ tiled kernels
+// One CTA per tile of kCT = 64 tokens x kCC = 128 channels.  The x rows the
+// tile needs (its tokens plus the W-1 before them, and for the backward the
+// W-1 after them) and the du rows arrive by 2-D tensor copies on one mbarrier;
+// rows before the first token or past the last come back as zeros.  Warp w
+// owns tokens 8w .. 8w+7 of the tile, lane l owns channels 4l .. 4l+3, and
+// every row a thread touches after the copies is read from shared memory.
+constexpr int kCT = 64;    // tokens per tile
+constexpr int kCC = 128;   // channels per tile
+constexpr int kTokPerWarp = kCT / 8;
 
-template <typename T, int V>
-__device__ __forceinline__ void ld_raw(const T* p, RawRow<T, V>& out) {
-  if constexpr (sizeof(out.r) == 16) out.r = __ldg(reinterpret_cast<const uint4*>(p));
-  else out.r = __ldg(reinterpret_cast<const uint2*>(p));
-}
-template <typename T, int V>
-__device__ __forceinline__ void zero_raw(RawRow<T, V>& out) {
-  if constexpr (sizeof(out.r) == 16) out.r = make_uint4(0, 0, 0, 0);
-  else out.r = make_uint2(0, 0);
-}
-template <typename T, int V>
-__device__ __forceinline__ void widen(const RawRow<T, V>& in, float (&v)[V]) {
+template <typename T>
+__device__ __forceinline__ void lds4(const T* p, float (&v)[4]) {
   if constexpr (sizeof(T) == 4) {
-    v[0] = __uint_as_float(in.r.x); v[1] = __uint_as_float(in.r.y);
-    v[2] = __uint_as_float(in.r.z); v[3] = __uint_as_float(in.r.w);
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
   } else {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&in.r);
-#pragma unroll
-    for (int j = 0; j < V / 2; ++j) {
-      const float2 f = __bfloat1622float2(h[j]);
-      v[2 * j] = f.x; v[2 * j + 1] = f.y;
-    }
+    const uint2 q = *reinterpret_cast<const uint2*>(p);
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+    v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y;
   }
 }
 
-// Stages the block's conv weights ([tap][channel], channel-contiguous) and
-// biases in shared memory with coalesced loads.
-template <int W, int CH>
-__device__ __forceinline__ void stage_weights(const ConvArgs& a, int c0, float (*wS)[CH], float* bS,
-                                              int tid) {
-  for (int i = tid; i < CH * W; i += 256) {
-    const int c = i / W, k = i - c * W;
-    wS[k][c] = (c0 + c < a.D) ? __ldg(a.w + (int64_t)c0 * W + i) : 0.0f;
+template <typename T>
+__device__ __forceinline__ void stg4(T* p, const float (&v)[4]) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    st_bf16x4(p, v);
   }
-  for (int i = tid; i < CH; i += 256) bS[i] = (a.bias && c0 + i < a.D) ? __ldg(a.bias + c0 + i) : 0.0f;
 }
 
-// ------------------------------------------------------------------ forward
 template <typename T, int W>
-__global__ void __launch_bounds__(256, 2) conv_fwd_kernel(ConvArgs a) {
-  constexpr int V = 16 / sizeof(T);
-  constexpr int R = kFwdRun;
-  constexpr int E = R + W - 1;  // rows loaded: t0-(W-1) .. t0+R-1
-  constexpr int CH = 32 * V;    // channels per block
-  __shared__ __align__(16) float wS[W][CH];
-  __shared__ __align__(16) float bS[CH];
-  const int ncols = (a.D / V + 31) / 32;
+struct ConvTileSmem {
+  static constexpr int XR = kCT + 2 * (W - 1);  // x rows t0-(W-1) .. t0+kCT+W-2
+  static constexpr int GR = kCT + W - 1;        // du rows t0 .. t0+kCT+W-2
+  static constexpr size_t kIO = sizeof(T) * (size_t)(XR + GR) * kCC;
+  static constexpr size_t kRed = sizeof(float) * 8 * kCC * (W + 1);
+  // x rows, then du rows (both 256-byte multiples: kCC * sizeof(T)); after
+  // the backward's arithmetic, the per-warp dweight / dbias partials
+  alignas(128) unsigned char io[kIO > kRed ? kIO : kRed];
+  __device__ T* x() { return reinterpret_cast<T*>(io); }
+  __device__ T* du() { return reinterpret_cast<T*>(io + sizeof(T) * (size_t)XR * kCC); }
+  __device__ float* red() { return reinterpret_cast<float*>(io); }
+  alignas(16) float w[W][kCC];
+  alignas(16) float b[kCC];
+  int pos[GR];
+  alignas(8) uint64_t bar;
+};
+
+// Forward: u[t] = SiLU(bias + sum_k w[W-1-k] x[t-k] [pos[t] >= k]) for the tile.
+template <typename T, int W>
+__global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                            ConvArgs a) {
+  using SM = ConvTileSmem<T, W>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  const int ncols = (a.D + kCC - 1) / kCC;
   const int64_t row = blockIdx.x / ncols;
-  const int c0 = (int)(blockIdx.x - row * ncols) * CH;
-  stage_weights<W, CH>(a, c0, wS, bS, threadIdx.y * 32 + threadIdx.x);
+  const int c0 = (int)(blockIdx.x - row * ncols) * kCC;
+  const int64_t t0 = row * kCT;
+  const int bx = a.D < kCC ? a.D : kCC;  // row pitch of the staged tile
+  constexpr int FR = kCT + W - 1;        // x rows the forward needs
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&sm.bar, (uint32_t)bx * FR * sizeof(T));
+    tma_load_2d(sm.x(), &tm_x, c0, (int)(t0 - (W - 1)), &sm.bar);
+  }
+  for (int i = tid; i < kCC * W; i += 256) {
+    const int c = i / W, k = i - c * W;
+    sm.w[k][c] = (c0 + c < a.D) ? __ldg(a.w + (int64_t)c0 * W + i) : 0.0f;
+  }
+  for (int i = tid; i < kCC; i += 256) sm.b[i] = (a.bias && c0 + i < a.D) ? __ldg(a.bias + c0 + i) : 0.0f;
+  for (int i = tid; i < kCT; i += 256) sm.pos[i] = (t0 + i < a.T) ? __ldg(a.pos + t0 + i) : 0;
   __syncthreads();
-  const int d0 = c0 + threadIdx.x * V;
-  const int64_t t0 = (row * kRowsPerBlock + threadIdx.y) * R;
-  if (d0 >= a.D || t0 >= a.T) return;
-  const T* __restrict__ x = static_cast<const T*>(a.x);
+  const int c = 4 * lane;
+  const bool active = c < bx && c0 + c < a.D;
+  float w[W][4], bb[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) w[k][v] = sm.w[k][c + v];
+    bb[v] = sm.b[c + v];
+  }
+  if (!mbar_wait(&sm.bar, 0, 1000000000ull)) return;  // copies lost: leave the tile (never expected)
+  if (!active) return;
   T* __restrict__ u = static_cast<T*>(a.out);
-  const int64_t D = a.D;
-
-  // every load of the thread is issued before any arithmetic
-  RawRow<T, V> xr[E];
-  int p[R];
+  float xw[W][4];  // xw[k] = x[t - (W-1) + k]
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const int64_t t = t0 - (W - 1) + i;
-    if (t >= 0 && t < a.T) ld_raw<T, V>(x + t * D + d0, xr[i]); else zero_raw<T, V>(xr[i]);
-  }
+  for (int k = 0; k < W - 1; ++k) lds4<T>(sm.x() + (kTokPerWarp * wp + k) * bx + c, xw[k]);
 #pragma unroll
-  for (int r = 0; r < R; ++r) p[r] = (t0 + r < a.T) ? __ldg(a.pos + t0 + r) : 0;
-
-  float w[W][V], b[V];
+  for (int j = 0; j < kTokPerWarp; ++j) {
+    const int tl = kTokPerWarp * wp + j;
+    lds4<T>(sm.x() + (tl + W - 1) * bx + c, xw[W - 1]);
+    const int p = sm.pos[tl];
+    float o[4];
 #pragma unroll
-  for (int v = 0; v < V; ++v) {
-#pragma unroll
-    for (int k = 0; k < W; ++k) w[k][v] = wS[k][threadIdx.x * V + v];
-    b[v] = bS[threadIdx.x * V + v];
-  }
-
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int64_t t = t0 + r;
-    if (t >= a.T) break;
-    float xs[W][V];
-#pragma unroll
-    for (int k = 0; k < W; ++k) widen<T, V>(xr[r + W - 1 - k], xs[k]);   // xs[k] = x[t - k]
-    float o[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-      float pre = fmaf(w[W - 1][v], xs[0][v], b[v]);
+    for (int v = 0; v < 4; ++v) {
+      float pre = fmaf(w[W - 1][v], xw[W - 1][v], bb[v]);
 #pragma unroll
       for (int k = 1; k < W; ++k)
-        if (p[r] >= k) pre = fmaf(w[W - 1 - k][v], xs[k][v], pre);
+        if (p >= k) pre = fmaf(w[W - 1 - k][v], xw[W - 1 - k][v], pre);
       o[v] = a.apply_silu ? siluf(pre) : pre;
     }
-    stv<T, V>(u + t * D + d0, o);
+    if (t0 + tl < a.T) stg4<T>(u + (t0 + tl) * (int64_t)a.D + c0 + c, o);
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) xw[k][v] = xw[k + 1][v];
   }
 }
 
-// ------------------------------------------------------------------ backward
-// Each thread loads all of its rows up front (x for t0-(W-1) .. t0+R+W-2, du
-// and pos for t0 .. t0+R+W-2), then streams over t' = t0 .. t0+R+W-2 keeping
-// windows of g = du * du/dpre and of pos, and emits dx[t'-(W-1)] once g[t'] is
-// known.
+// Backward: g[t] = du[t] SiLU'(pre[t]) for the tile's tokens and the W-1 after
+// them; dx[t] = sum_k w[W-1-k] g[t+k] [t+k < T and pos[t+k] >= k]; dweight and
+// dbias partials of the tile's own tokens, summed over the 8 warps in a fixed
+// order into one partial row per tile row.  A warp's lanes share their token,
+// so every mask is warp-uniform; the 4 channels of a lane run as 2 packed pairs.
 template <typename T, int W>
-__global__ void __launch_bounds__(256, 2) conv_bwd_kernel(ConvArgs a) {
-  constexpr int V = 4;
-  constexpr int R = kBwdRun;
-  constexpr int CH = 32 * V;
-  constexpr int EG = R + W - 1;        // tokens t0 .. t0+R+W-2 (g, du, pos)
-  constexpr int EX = EG + W - 1;       // x rows t0-(W-1) .. t0+R+W-2
-  __shared__ __align__(16) float wS[W][CH];
-  __shared__ __align__(16) float bS[CH];
-  __shared__ float red[kRowsPerBlock][32][V * (W + 1)];
-  const int ncols = (a.D / V + 31) / 32;
+__global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                               const __grid_constant__ CUtensorMap tm_du,
+                                                               ConvArgs a) {
+  using SM = ConvTileSmem<T, W>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  const int ncols = (a.D + kCC - 1) / kCC;
   const int64_t row = blockIdx.x / ncols;
-  const int c0 = (int)(blockIdx.x - row * ncols) * CH;
-  stage_weights<W, CH>(a, c0, wS, bS, threadIdx.y * 32 + threadIdx.x);
-  __syncthreads();
-  const int d0 = c0 + threadIdx.x * V;
-  const int64_t t0 = (row * kRowsPerBlock + threadIdx.y) * R;
-  const bool active = d0 < a.D && t0 < a.T;
-  const T* __restrict__ x = static_cast<const T*>(a.x);
-  const T* __restrict__ du = static_cast<const T*>(a.du);
-  T* __restrict__ dx = static_cast<T*>(a.out);
-  const int64_t D = a.D;
-
-  float dw[W][V], db[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-    db[v] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < W; ++k) dw[k][v] = 0.0f;
+  const int c0 = (int)(blockIdx.x - row * ncols) * kCC;
+  const int64_t t0 = row * kCT;
+  const int bx = a.D < kCC ? a.D : kCC;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&sm.bar, (uint32_t)bx * (SM::XR + SM::GR) * sizeof(T));
+    tma_load_2d(sm.x(), &tm_x, c0, (int)(t0 - (W - 1)), &sm.bar);
+    tma_load_2d(sm.du(), &tm_du, c0, (int)t0, &sm.bar);
   }
-
-  if (active) {
-    RawRow<T, V> xr[EX], dr[EG];
-    int p[EG];
+  for (int i = tid; i < kCC * W; i += 256) {
+    const int c = i / W, k = i - c * W;
+    sm.w[k][c] = (c0 + c < a.D) ? __ldg(a.w + (int64_t)c0 * W + i) : 0.0f;
+  }
+  for (int i = tid; i < kCC; i += 256) sm.b[i] = (a.bias && c0 + i < a.D) ? __ldg(a.bias + c0 + i) : 0.0f;
+  // pos of tokens past T is 0, so every tap from there is masked off
+  for (int i = tid; i < SM::GR; i += 256) sm.pos[i] = (t0 + i < a.T) ? __ldg(a.pos + t0 + i) : 0;
+  __syncthreads();
+  const int c = 4 * lane;
+  const bool active = c < bx && c0 + c < a.D;
+  float2 w[W][2], bb[2];
 #pragma unroll
-    for (int i = 0; i < EX; ++i) {
-      const int64_t t = t0 - (W - 1) + i;
-      if (t >= 0 && t < a.T) ld_raw<T, V>(x + t * D + d0, xr[i]); else zero_raw<T, V>(xr[i]);
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) w[k][h] = make_float2(sm.w[k][c + 2 * h], sm.w[k][c + 2 * h + 1]);
+    bb[h] = make_float2(sm.b[c + 2 * h], sm.b[c + 2 * h + 1]);
+  }
+  const bool got = mbar_wait(&sm.bar, 0, 1000000000ull);
+  float2 dw[W][2], db[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    db[h] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < W; ++k) dw[k][h] = make_float2(0.0f, 0.0f);
+  }
+  if (got && active) {
+    T* __restrict__ dx = static_cast<T*>(a.out);
+    const int tb = kTokPerWarp * wp;
+    float2 xw[W][2];  // xw[k] = x[t - (W-1) + k] for the g token t
+    float2 gw[W][2];  // gw[k] = g[t - (W-1) + k]
+    int pw[W];        // pw[k] = pos[t - (W-1) + k] (tile-relative tokens >= tb only)
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k) {
+      float v[4];
+      lds4<T>(sm.x() + (tb + k) * bx + c, v);
+      xw[k][0] = make_float2(v[0], v[1]);
+      xw[k][1] = make_float2(v[2], v[3]);
+      gw[k][0] = gw[k][1] = make_float2(0.0f, 0.0f);
+      pw[k] = 0;
     }
 #pragma unroll
-    for (int j = 0; j < EG; ++j) {
-      const int64_t t = t0 + j;
-      if (t < a.T) {
-        ld_raw<T, V>(du + t * D + d0, dr[j]);
-        p[j] = __ldg(a.pos + t);
-      } else {
-        zero_raw<T, V>(dr[j]);
-        p[j] = 0;
+    for (int j = 0; j < kTokPerWarp + W - 1; ++j) {
+      const int tl = tb + j;  // g token (tile-relative); its x row is tl + W - 1
+      {
+        float v[4];
+        lds4<T>(sm.x() + (tl + W - 1) * bx + c, v);
+        xw[W - 1][0] = make_float2(v[0], v[1]);
+        xw[W - 1][1] = make_float2(v[2], v[3]);
       }
-    }
-    float w[W][V], b[V];
+      float dv[4];
+      lds4<T>(sm.du() + tl * bx + c, dv);
+      const int p = sm.pos[tl];
+      pw[W - 1] = p;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
+      for (int h = 0; h < 2; ++h) {
+        float2 pre = fma2(w[W - 1][h], xw[W - 1][h], bb[h]);
 #pragma unroll
-      for (int k = 0; k < W; ++k) w[k][v] = wS[k][threadIdx.x * V + v];
-      b[v] = bS[threadIdx.x * V + v];
-    }
-    float gw[W][V];   // after step j: gw[k] = g[t0 + j - (W-1) + k]
-#pragma unroll
-    for (int k = 0; k < W; ++k)
-#pragma unroll
-      for (int v = 0; v < V; ++v) gw[k][v] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < EG; ++j) {
-      const int64_t tp = t0 + j;
-      float xs[W][V];   // xs[k] = x[t' - k]
-#pragma unroll
-      for (int k = 0; k < W; ++k) widen<T, V>(xr[j + W - 1 - k], xs[k]);
-      float dc[V];
-      widen<T, V>(dr[j], dc);
-#pragma unroll
-      for (int k = 0; k < W - 1; ++k)
-#pragma unroll
-        for (int v = 0; v < V; ++v) gw[k][v] = gw[k + 1][v];
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        float g = 0.0f;
-        if (tp < a.T) {
-          float pre = fmaf(w[W - 1][v], xs[0][v], b[v]);
-#pragma unroll
-          for (int k = 1; k < W; ++k)
-            if (p[j] >= k) pre = fmaf(w[W - 1 - k][v], xs[k][v], pre);
-          g = a.apply_silu ? dc[v] * silu_grad(pre) : dc[v];
-        }
-        gw[W - 1][v] = g;
-        if (j < R && tp < a.T) {
-          db[v] += g;
+        for (int k = 1; k < W; ++k)
+          if (p >= k) pre = fma2(w[W - 1 - k][h], xw[W - 1 - k][h], pre);
+        // rows past T are zero-filled, so g = 0 there
+        const float2 dv2 = make_float2(dv[2 * h], dv[2 * h + 1]);
+        const float2 g = a.apply_silu ? mul2(dv2, make_float2(silu_grad(pre.x), silu_grad(pre.y))) : dv2;
+        gw[W - 1][h] = g;
+        if (j < kTokPerWarp) {
+          db[h] = __fadd2_rn(db[h], g);
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            if (p[j] >= k) dw[W - 1 - k][v] = fmaf(g, xs[k][v], dw[W - 1 - k][v]);
+            if (p >= k) dw[W - 1 - k][h] = fma2(g, xw[W - 1 - k][h], dw[W - 1 - k][h]);
         }
       }
-      // dx at t = t' - (W-1), complete now that g[t .. t+W-1] is known
-      if (j >= W - 1) {
-        const int64_t t = tp - (W - 1);
-        const int r = j - (W - 1);
+      if (j >= W - 1) {  // dx of token tl - (W-1), which now has g[t .. t+W-1]
+        const int to = tl - (W - 1);
+        const int64_t t = t0 + to;
         if (t < a.T) {
-          float o[V];
+          float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-          for (int v = 0; v < V; ++v) {
-            float acc = 0.0f;
+          for (int k = 0; k < W; ++k)
+            if (pw[k] >= k)
 #pragma unroll
-            for (int k = 0; k < W; ++k)
-              if (t + k < a.T && p[r + k] >= k) acc = fmaf(w[W - 1 - k][v], gw[k][v], acc);
-            o[v] = acc;
-          }
-          stv<T, V>(dx + t * D + d0, o);
+              for (int h = 0; h < 2; ++h) acc[h] = fma2(w[W - 1 - k][h], gw[k][h], acc[h]);
+          const float o[4] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y};
+          stg4<T>(dx + t * (int64_t)a.D + c0 + c, o);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < W - 1; ++k) {
+        pw[k] = pw[k + 1];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          xw[k][h] = xw[k + 1][h];
+          gw[k][h] = gw[k + 1][h];
         }
       }
     }
   }
-
-  // reduce dw / db over the 8 token rows of the block, write one partial row
+  // dweight / dbias: sum the 8 warps in order (the input tiles are free now)
+  __syncthreads();
+  float* red = sm.red();  // [8][kCC][W + 1]
 #pragma unroll
-  for (int v = 0; v < V; ++v) {
+  for (int v = 0; v < 4; ++v) {
+    const int h = v >> 1;
 #pragma unroll
-    for (int k = 0; k < W; ++k) red[threadIdx.y][threadIdx.x][v * (W + 1) + k] = dw[k][v];
-    red[threadIdx.y][threadIdx.x][v * (W + 1) + W] = db[v];
+    for (int k = 0; k < W; ++k) red[(wp * kCC + c + v) * (W + 1) + k] = (v & 1) ? dw[k][h].y : dw[k][h].x;
+    red[(wp * kCC + c + v) * (W + 1) + W] = (v & 1) ? db[h].y : db[h].x;
   }
   __syncthreads();
-  if (threadIdx.y == 0 && d0 < a.D) {
-    float* part = a.partial + row * (D * (W + 1));
+  float* part = a.partial + row * ((int64_t)a.D * (W + 1));
+  for (int i = tid; i < kCC * (W + 1); i += 256) {
+    const int cc = i / (W + 1), k = i - cc * (W + 1);
+    if (cc >= bx || c0 + cc >= a.D) continue;
+    float acc = 0.0f;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      float s[W + 1];
-#pragma unroll
-      for (int k = 0; k <= W; ++k) s[k] = 0.0f;
-      for (int r = 0; r < kRowsPerBlock; ++r)
-#pragma unroll
-        for (int k = 0; k <= W; ++k) s[k] += red[r][threadIdx.x][v * (W + 1) + k];
-      // partial row layout: dweight (D, W) first, then dbias (D)
-#pragma unroll
-      for (int k = 0; k < W; ++k) part[(int64_t)(d0 + v) * W + k] = s[k];
-      part[D * W + d0 + v] = s[W];
-    }
+    for (int r = 0; r < 8; ++r) acc += red[(r * kCC + cc) * (W + 1) + k];
+    // partial row layout: dweight (D, W) first, then dbias (D)
+    if (k < W) part[(int64_t)(c0 + cc) * W + k] = acc;
+    else part[(int64_t)a.D * W + c0 + cc] = acc;
   }
 }
 
 template <typename T, int W>
-cudaError_t fwd_w(const ConvArgs& a, cudaStream_t st) {
-  constexpr int V = 16 / sizeof(T);
-  const int64_t cols = (a.D / V + 31) / 32;
-  const int64_t rows = (a.T + kRowsPerBlock * kFwdRun - 1) / (kRowsPerBlock * kFwdRun);
+cudaError_t fwd_tile_w(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t st) {
+  const size_t smem = sizeof(ConvTileSmem<T, W>);
+  cudaError_t e = cudaFuncSetAttribute(conv_fwd_tile_kernel<T, W>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t cols = (a.D + kCC - 1) / kCC;
+  const int64_t rows = (a.T + kCT - 1) / kCT;
   if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
-  conv_fwd_kernel<T, W><<<(unsigned)(rows * cols), dim3(32, kRowsPerBlock), 0, st>>>(a);
+  conv_fwd_tile_kernel<T, W><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, a);
   return cudaGetLastError();
 }
 
 template <typename T, int W>
-cudaError_t bwd_w(const ConvArgs& a, cudaStream_t st) {
-  const int64_t cols = (a.D / 4 + 31) / 32;
-  const int64_t rows = conv_bwd_partial_rows(a.T);
+cudaError_t bwd_tile_w(const ConvArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
+                       cudaStream_t st) {
+  const size_t smem = sizeof(ConvTileSmem<T, W>);
+  cudaError_t e = cudaFuncSetAttribute(conv_bwd_tile_kernel<T, W>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t cols = (a.D + kCC - 1) / kCC;
+  const int64_t rows = (a.T + kCT - 1) / kCT;
   if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
-  conv_bwd_kernel<T, W><<<(unsigned)(rows * cols), dim3(32, kRowsPerBlock), 0, st>>>(a);
+  conv_bwd_tile_kernel<T, W><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, tm_du, a);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t fwd_t(const ConvArgs& a, cudaStream_t st) {
+cudaError_t fwd_t(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t st) {
   switch (a.W) {
-    case 1: return fwd_w<T, 1>(a, st);
-    case 2: return fwd_w<T, 2>(a, st);
-    case 3: return fwd_w<T, 3>(a, st);
-    case 4: return fwd_w<T, 4>(a, st);
+    case 1: return fwd_tile_w<T, 1>(a, tm_x, st);
+    case 2: return fwd_tile_w<T, 2>(a, tm_x, st);
+    case 3: return fwd_tile_w<T, 3>(a, tm_x, st);
+    case 4: return fwd_tile_w<T, 4>(a, tm_x, st);
   }
   return cudaErrorInvalidValue;
 }
 
 template <typename T>
-cudaError_t bwd_t(const ConvArgs& a, cudaStream_t st) {
+cudaError_t bwd_t(const ConvArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_du, cudaStream_t st) {
   switch (a.W) {
-    case 1: return bwd_w<T, 1>(a, st);
-    case 2: return bwd_w<T, 2>(a, st);
-    case 3: return bwd_w<T, 3>(a, st);
-    case 4: return bwd_w<T, 4>(a, st);
+    case 1: return bwd_tile_w<T, 1>(a, tm_x, tm_du, st);
+    case 2: return bwd_tile_w<T, 2>(a, tm_x, tm_du, st);
+    case 3: return bwd_tile_w<T, 3>(a, tm_x, tm_du, st);
+    case 4: return bwd_tile_w<T, 4>(a, tm_x, tm_du, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -342,21 +344,26 @@ cudaError_t bwd_t(const ConvArgs& a, cudaStream_t st) {
 }  // namespace
 
 int64_t conv_bwd_partial_rows(int64_t T) {
-  const int64_t per = kRowsPerBlock * kBwdRun;
+  const int64_t per = kCT;
   const int64_t r = (T + per - 1) / per;
   return r > 0 ? r : 1;
 }
 
-cudaError_t launch_conv1d_fwd(const ConvArgs& a, IO io, cudaStream_t st) {
+int conv_tile_rows(int W, bool bwd, bool x) {
+  return x ? kCT + (bwd ? 2 : 1) * (W - 1) : kCT + W - 1;
+}
+int conv_tile_cols() { return kCC; }
+
+cudaError_t launch_conv1d_fwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
-  return io == IO::F32 ? fwd_t<float>(a, st) : fwd_t<__nv_bfloat16>(a, st);
+  return io == IO::F32 ? fwd_t<float>(a, tm_x, st) : fwd_t<__nv_bfloat16>(a, tm_x, st);
 }
 
-cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, float* dweight, float* dbias,
-                              cudaStream_t st) {
+cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
+                              float* dweight, float* dbias, cudaStream_t st) {
   const int64_t P = conv_bwd_partial_rows(a.T);
   if (a.T > 0) {
-    cudaError_t e = io == IO::F32 ? bwd_t<float>(a, st) : bwd_t<__nv_bfloat16>(a, st);
+    cudaError_t e = io == IO::F32 ? bwd_t<float>(a, tm_x, tm_du, st) : bwd_t<__nv_bfloat16>(a, tm_x, tm_du, st);
     if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = cudaMemsetAsync(a.partial, 0, sizeof(float) * (size_t)a.D * (a.W + 1), st);

@@ -37,9 +37,12 @@ struct ConvArgs {
 };
 // Number of token-rows of CTAs the backward kernel uses (partial buffer rows).
 int64_t conv_bwd_partial_rows(int64_t T);
-cudaError_t launch_conv1d_fwd(const ConvArgs& a, IO io, cudaStream_t st);
-cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, float* dweight, float* dbias,
-                              cudaStream_t st);
+// Tensor-map boxes of the conv tiles: rows of x (fwd or bwd) or of du, and channels.
+int conv_tile_rows(int W, bool bwd, bool x);
+int conv_tile_cols();
+cudaError_t launch_conv1d_fwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x, cudaStream_t st);
+cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
+                              float* dweight, float* dbias, cudaStream_t st);
 
 // ---------------------------------------------------------------- selective scan
 constexpr int kFwdChunk = 128;   // tokens per forward work item (look-back granule)
