@@ -28,14 +28,14 @@
 //      transposed to [state][token] (fp32).
 //   2. Forward walk per warp: states h_t kept in registers (32 tokens x 2
 //      states); E and the carry aggregate accumulated; dC_t[n] contributions
-//      g_t h_t summed over the tile's channels (WarpColumnSum); C_t.h_t
-//      partials for y.
+//      g_t h_t summed over the tile's channels (ColSum16 shuffle butterflies,
+//      fed token by token); C_t.h_t partials for y.
 //   3. Decoupled look-back per warp towards HIGHER chunks for the carry
 //      entering from the right; aggregates re-applied in a fixed order
 //      (bitwise repeatable); time-bounded waits.
 //   4. y = sum of the warps' partials + Dskip u, and dz (all threads).
 //   5. Reverse walk per warp in blocks of 8 tokens: dA (per thread), dB
-//      contributions (WarpColumnSum), partial sums over the warp's states
+//      contributions (ColSum16), partial sums over the warp's states
 //      for du and d delta; after each block all threads add the warps'
 //      partials in a fixed order and write du, d delta_raw.
 //   6. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
@@ -80,8 +80,6 @@ struct BwdSmem {
   alignas(16) float CT[N * kP];
   // ---- exponent offset per token: -inf at a sequence start, else 0
   alignas(16) float off[kL];
-  // ---- per-warp column-sum buffers, 32 rows x 32 floats each
-  alignas(16) float cs[W * 32 * 32];
   // ---- cross-warp partials: y partials [W][kL][kTile] after the forward
   //      walk, then (du, d delta) partials [2][W][kRB][kTile] float2 in the
   //      reverse walk
@@ -92,46 +90,42 @@ struct BwdSmem {
   alignas(8) uint64_t bar;
 };
 
-// Column sums over the 32 lanes of a warp (lane = channel) of 32 values per
-// lane, through the warp's shared buffer of 32 rows x 32 floats:
-//   1. every lane stores its row; 16-byte chunk q of row l sits at slot
-//      q ^ (l & 7), so the 8 lanes of each 16-byte access phase hit 8
-//      different bank groups;
-//   2. lane j reads chunk m = j & 7 of the rows g, g + 4, ..., g + 28
-//      (g = j >> 3: conflict-free again) and adds them in order, two values
-//      per instruction;
-//   3. the 4 lanes holding the same chunk combine their sums by two halving
-//      shuffle exchanges (lane bits 4 and 3), after which lane j holds the
-//      sum of column 4 (j & 7) + 2 bit4(j) + bit3(j).
-// The order of every addition is fixed, so the sums are bitwise repeatable.
-struct WarpColumnSum {
-  static __device__ __forceinline__ int column(int lane) {
-    return 4 * (lane & 7) + 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);
+// Column sums over the 32 lanes of a warp (lane = channel) for groups of 16
+// tokens x 2 states, fed one token at a time by shuffle butterflies.  A lane
+// keeps its state pair in its own order, the "first" state being n0 + bit4:
+//   level 1 (every token): lanes l, l^16 exchange the state the other keeps,
+//   level 2 (every token pair): lanes l, l^8 exchange the token the other
+//     keeps (bit 3 picks the odd token),
+//   levels 3, 4, 5 likewise over lane bits 2, 1, 0 for pairs of pairs, ...
+// After the 16th token, lane l holds the sum over all 32 lanes for token
+// 8 b0 + 4 b1 + 2 b2 + b3 of the group (b_i = bit i of l) and its first
+// state.  The pairing is fixed, so the sums are bitwise repeatable; tokens may
+// come in ascending or descending order.
+struct ColSum16 {
+  float p1[2], p2[2], p3[2], p4[2];  // pending sums, by the parity of the token group at each level
+
+  static __device__ __forceinline__ int token(int lane) {
+    return 8 * (lane & 1) + 4 * ((lane >> 1) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 3) & 1);
   }
-  // values 4q .. 4q+3 of this lane's row
-  static __device__ __forceinline__ void put(float* buf, int lane, int q, float2 lo, float2 hi) {
-    *reinterpret_cast<float4*>(buf + lane * 32 + 4 * (q ^ (lane & 7))) = make_float4(lo.x, lo.y, hi.x, hi.y);
+
+  static __device__ __forceinline__ float combine(float lo, float hi, int lane, int mask) {
+    const bool up = (lane & mask) != 0;
+    return (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, mask);
   }
-  // call with every lane's row in place (after __syncwarp)
-  static __device__ __forceinline__ float reduce(const float* buf, int lane) {
-    const int m = lane & 7, g0 = lane >> 3;
-    float2 lo = make_float2(0.0f, 0.0f), hi = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = g0 + 4 * i;
-      const float4 x = *reinterpret_cast<const float4*>(buf + r * 32 + 4 * (m ^ (r & 7)));
-      lo = __fadd2_rn(lo, make_float2(x.x, x.y));
-      hi = __fadd2_rn(hi, make_float2(x.z, x.w));
-    }
-    const bool u4 = (lane & 16) != 0;
-    float2 keep = u4 ? hi : lo;
-    const float2 send = u4 ? lo : hi;
-    keep.x += __shfl_xor_sync(0xffffffffu, send.x, 16);
-    keep.y += __shfl_xor_sync(0xffffffffu, send.y, 16);
-    const bool u3 = (lane & 8) != 0;
-    float v = u3 ? keep.y : keep.x;
-    v += __shfl_xor_sync(0xffffffffu, u3 ? keep.x : keep.y, 8);
-    return v;
+
+  // Token c (0..15) of the group with this lane's values in its state order;
+  // returns true once the group is complete (*sum then holds the lane's result).
+  __device__ __forceinline__ bool feed(int c, bool ascending, float2 v, int lane, float* sum) {
+    p1[c & 1] = v.x + __shfl_xor_sync(0xffffffffu, v.y, 16);
+    if ((c & 1) != (ascending ? 1 : 0)) return false;
+    p2[(c >> 1) & 1] = combine(p1[0], p1[1], lane, 8);
+    if ((c & 3) != (ascending ? 3 : 0)) return false;
+    p3[(c >> 2) & 1] = combine(p2[0], p2[1], lane, 4);
+    if ((c & 7) != (ascending ? 7 : 0)) return false;
+    p4[(c >> 3) & 1] = combine(p3[0], p3[1], lane, 2);
+    if ((c & 15) != (ascending ? 15 : 0)) return false;
+    *sum = combine(p4[0], p4[1], lane, 1);
+    return true;
   }
 };
 
@@ -155,7 +149,6 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  float* const csw = sm.cs + w * 32 * 32;  // this warp's column-sum buffer
   const int n_items = a.n_chunks * a.n_tiles;
 
   // Requests every input of work item `tkn` on the barrier: u, delta_raw,
@@ -262,11 +255,14 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
   // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
   if (w == 0) sm.off[lane] = ((rst >> lane) & 1u) ? -INFINITY : 0.0f;
+  // the warp's state pair, in this lane's order: "first" = n0 + bit4(lane)
+  // (the column-sum butterflies keep a lane's first state)
   const int n0 = 2 * w;
+  const int nF = n0 + ((lane >> 4) & 1), nS = n0 + 1 - ((lane >> 4) & 1);
   float2 A2 = make_float2(0.0f, 0.0f), h = make_float2(0.0f, 0.0f);
   if (valid) {
-    A2 = make_float2(sm.Araw[lane * N + n0] * kLog2e, sm.Araw[lane * N + n0 + 1] * kLog2e);
-    h = make_float2(sm.H[n0 * bx + lane], sm.H[(n0 + 1) * bx + lane]);
+    A2 = make_float2(sm.Araw[lane * N + nF] * kLog2e, sm.Araw[lane * N + nS] * kLog2e);
+    h = make_float2(sm.H[nF * bx + lane], sm.H[nS * bx + lane]);
   }
   const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
   __syncthreads();
@@ -274,7 +270,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // ---- 2. forward walk over the 32 tokens (state pair n0, n0+1)
   float2 hist[kL];
   float2 E = make_float2(1.0f, 1.0f), tot = make_float2(0.0f, 0.0f);
-  float2 vprev = make_float2(0.0f, 0.0f);  // column-sum values of the previous token
+  ColSum16 colsum;
   {
     const float* rowc = sm.dl + lane * kP;
 #pragma unroll
@@ -282,10 +278,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       const float4 dl4 = *reinterpret_cast<const float4*>(rowc + 4 * kb);
       const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
       const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
-      const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + n0 * kP + 4 * kb);
-      const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + (n0 + 1) * kP + 4 * kb);
-      const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + n0 * kP + 4 * kb);
-      const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + (n0 + 1) * kP + 4 * kb);
+      const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + nF * kP + 4 * kb);
+      const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + nS * kP + 4 * kb);
+      const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + nF * kP + 4 * kb);
+      const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + nS * kP + 4 * kb);
       const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
       const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
       const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
@@ -303,17 +299,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         E = mul2(E, at);
         tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
         if (a.has_z) sm.part[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
-        const float2 vc = mul2(splat2(ga[e]), h);  // dC contributions
-        if (t & 1) WarpColumnSum::put(csw, lane, (t & 15) >> 1, vprev, vc);
-        vprev = vc;
-        if ((t & 15) == 15) {
-          __syncwarp();
-          const float sum = WarpColumnSum::reduce(csw, lane);
-          const int col = WarpColumnSum::column(lane);
-          const int tt = (t - 15) + (col >> 1);
-          if (tt < rows)
-            a.part_dBC[((int64_t)tile * 2 * N + N + n0 + (col & 1)) * a.T + t0 + tt] = sum;
-          __syncwarp();
+        float sum;  // dC contributions g_t h_t, summed over the tile's channels
+        if (colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &sum)) {
+          const int tt = (t - 15) + ColSum16::token(lane);
+          if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + N + nF) * a.T + t0 + tt] = sum;
         }
       }
     }
@@ -413,10 +402,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         const float4 dl4 = *reinterpret_cast<const float4*>(sm.dl + lane * kP + 4 * kb);
         const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
         const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
-        const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + n0 * kP + 4 * kb);
-        const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + (n0 + 1) * kP + 4 * kb);
-        const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + n0 * kP + 4 * kb);
-        const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + (n0 + 1) * kP + 4 * kb);
+        const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + nF * kP + 4 * kb);
+        const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + nS * kP + 4 * kb);
+        const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + nF * kP + 4 * kb);
+        const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + nS * kP + 4 * kb);
         const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
         const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
         const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
@@ -435,18 +424,12 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
           dA = fma2(splat2(dla[e]), dhq, dA);
           part2[((buf * W + w) * kRB + (t - blk * kRB)) * kTile + lane] =
               make_float2(fmaf(dh.x, Bt.x, dh.y * Bt.y), fmaf(A2.x, dhq.x, A2.y * dhq.y));
-          const float2 vb = mul2(dh, splat2(dua[e]));  // dB contributions
-          if (!(t & 1)) WarpColumnSum::put(csw, lane, (t & 15) >> 1, vb, vprev);
-          vprev = vb;
-          r = mul2(dh, at);  // carry to h_{t-1}
-          if ((t & 15) == 0) {
-            __syncwarp();
-            const float sum = WarpColumnSum::reduce(csw, lane);
-            const int col = WarpColumnSum::column(lane);
-            const int tt = t + (col >> 1);
-            if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + n0 + (col & 1)) * a.T + t0 + tt] = sum;
-            __syncwarp();
+          float sum;  // dB contributions dh_t delta u, summed over the tile's channels
+          if (colsum.feed(t & 15, false, mul2(dh, splat2(dua[e])), lane, &sum)) {
+            const int tt = t + ColSum16::token(lane);
+            if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + nF) * a.T + t0 + tt] = sum;
           }
+          r = mul2(dh, at);  // carry to h_{t-1}
         }
       }
       __syncthreads();  // the block's partials are complete
@@ -476,8 +459,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // ---- 6. dA partials of the chunk ([chunk][n][d]); fixed-order CTA sums of
   //         the dDskip and d_dt_bias partials
   if (valid) {
-    a.part_dA[((int64_t)chunk * N + n0) * a.D + d] = dA.x;
-    a.part_dA[((int64_t)chunk * N + n0 + 1) * a.D + d] = dA.y;
+    a.part_dA[((int64_t)chunk * N + nF) * a.D + d] = dA.x;
+    a.part_dA[((int64_t)chunk * N + nS) * a.D + d] = dA.y;
   }
   sm.redD[w * kTile + lane] = sDD;
   sm.redB[w * kTile + lane] = sDB;
