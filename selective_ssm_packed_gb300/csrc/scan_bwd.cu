@@ -220,29 +220,54 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   //         channels past D (a = 1, b = 0, g = 0 there), so that those feed
   //         exactly 0 into every sum they enter
   // a warp's 32 lanes take 8 channels x 4 tokens: the [channel][token]
-  // stores then hit 32 different banks
+  // stores then hit 32 different banks.  Straight-line code over the thread's
+  // kPer elements (no per-element branches), so their exp / log chains overlap;
+  // out-of-range elements are computed on whatever the buffers hold and then
+  // replaced by zeros with selects.
+  {
+    constexpr int kPer = kL * kTile / kThr;
+    float rv[kPer], uv[kPer], gov[kPer], dlv[kPer], sgv[kPer], gv[kPer];
+    int cs[kPer], ts[kPer];
+    bool ok[kPer];
 #pragma unroll
-  for (int i = tid; i < kL * kTile; i += kThr) {
-    const int b = i >> 5, l = i & 31;
-    const int c = 8 * (b & 3) + (l >> 2), t = 4 * (b >> 2) + (l & 3);
-    const bool vt = t < rows, vd = c < bx && d0 + c < a.D;
-    float dlv = 0.0f, sgv = 0.0f, uv = 0.0f, gv = 0.0f;
-    if (vt && vd) {
-      const float r = to_f(sm.dr[t * bx + c]) + (a.dt_bias ? sm.bias[c] : 0.0f);
-      if (a.delta_softplus) {
-        dlv = softplus_sig(r, &sgv);
-      } else {
-        dlv = r;
-        sgv = 1.0f;
-      }
-      uv = to_f(sm.u[t * bx + c]);
-      const float go = to_f(sm.dout[t * bx + c]);
-      gv = a.has_z ? go * siluf(to_f(sm.z[t * bx + c])) : go;
+    for (int q = 0; q < kPer; ++q) {
+      const int i = tid + q * kThr;
+      const int b = i >> 5, l = i & 31;
+      const int c = 8 * (b & 3) + (l >> 2), t = 4 * (b >> 2) + (l & 3);
+      cs[q] = c;
+      ts[q] = t;
+      ok[q] = t < rows && c < bx && d0 + c < a.D;
+      rv[q] = to_f(sm.dr[t * bx + c]) + (a.dt_bias ? sm.bias[c] : 0.0f);
+      uv[q] = to_f(sm.u[t * bx + c]);
+      gov[q] = to_f(sm.dout[t * bx + c]);
+      gv[q] = a.has_z ? to_f(sm.z[t * bx + c]) : 0.0f;
     }
-    sm.dl[c * kP + t] = dlv;
-    sm.dlu[c * kP + t] = dlv * uv;
-    sm.g[c * kP + t] = gv;
-    sm.sg[c * kP + t] = sgv;
+    if (a.delta_softplus) {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) dlv[q] = softplus_sig(rv[q], &sgv[q]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        dlv[q] = rv[q];
+        sgv[q] = 1.0f;
+      }
+    }
+    if (a.has_z) {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) gv[q] = gov[q] * siluf(gv[q]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) gv[q] = gov[q];
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int at = cs[q] * kP + ts[q];
+      const float dl_q = ok[q] ? dlv[q] : 0.0f;
+      sm.dl[at] = dl_q;
+      sm.dlu[at] = ok[q] ? dl_q * uv[q] : 0.0f;
+      sm.g[at] = ok[q] ? gv[q] : 0.0f;
+      sm.sg[at] = ok[q] ? sgv[q] : 0.0f;
+    }
   }
 #pragma unroll
   for (int i = tid; i < N * kL; i += kThr) {
@@ -368,9 +393,9 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // ---- 4. y = C.h + Dskip u and dz
   if (a.has_z) {
     T* gdz = static_cast<T*>(a.dz);
+#pragma unroll
     for (int i = tid; i < kL * kTile; i += kThr) {
       const int t = i / kTile, c = i - t * kTile;
-      if (t >= rows || c >= bx || d0 + c >= a.D) continue;
       float y = 0.0f;
 #pragma unroll
       for (int v = 0; v < W; ++v) y += sm.part[(v * kL + t) * kTile + c];
@@ -379,7 +404,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       const float go = to_f(sm.dout[t * bx + c]);
       const float zz = to_f(sm.z[t * bx + c]);
       const float sz = sigmoidf_fast(zz);
-      gdz[(t0 + t) * a.D + d0 + c] = from_f<T>(go * sz * fmaf(zz, 1.0f - sz, 1.0f) * y);
+      const float dzv = go * sz * fmaf(zz, 1.0f - sz, 1.0f) * y;
+      if (t < rows && c < bx && d0 + c < a.D) gdz[(t0 + t) * a.D + d0 + c] = from_f<T>(dzv);
     }
   }
   __syncthreads();  // part is reused below
