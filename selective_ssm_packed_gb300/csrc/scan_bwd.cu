@@ -296,6 +296,9 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   float2 hist[kL];
   float2 E = make_float2(1.0f, 1.0f), tot = make_float2(0.0f, 0.0f);
   ColSum16 colsum;
+  // the forward walk's dC sums (one per lane and 16-token group), stored only
+  // after the look-back has published, so that its fence does not wait for them
+  float dcs[kL / 16];
   {
     const float* rowc = sm.dl + lane * kP;
 #pragma unroll
@@ -324,11 +327,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         E = mul2(E, at);
         tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
         if (a.has_z) sm.part[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
-        float sum;  // dC contributions g_t h_t, summed over the tile's channels
-        if (colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &sum)) {
-          const int tt = (t - 15) + ColSum16::token(lane);
-          if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + N + nF) * a.T + t0 + tt] = sum;
-        }
+        // dC contributions g_t h_t, summed over the tile's channels
+        colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &dcs[t >> 4]);
       }
     }
   }
@@ -387,6 +387,11 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       inc[wslot * 32 + lane] = fma2(E, x, tot);
       publish_flag(my_flag, kFlagInclusive, publish, lane);
     }
+  }
+#pragma unroll
+  for (int q = 0; q < kL / 16; ++q) {
+    const int tt = 16 * q + ColSum16::token(lane);
+    if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + N + nF) * a.T + t0 + tt] = dcs[q];
   }
   __syncthreads();  // y partials complete
 
