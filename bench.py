@@ -50,7 +50,7 @@ def per_token_counts(D, N, e, W=4):
 # capture of a kernel, per token; reset an entry to nothing as soon as the
 # kernel changes (profiles/ keeps the capture summaries).
 LAST_CAPTURE_TRAFFIC = {
-    ("m14b", "scan_bwd"): {"bytes_per_token": (337.034752e6 + 454.412544e6) / 8192,
+    ("m14b", "scan_bwd"): {"bytes_per_token": (337.196544e6 + 440.187136e6) / 8192,
                            "source": "ncu capture of scan_bwd_kernel on m14b_small (T=8192), "
                                      "scaled by tokens; profiles/scan_bwd_m14b_small.md"},
 }
