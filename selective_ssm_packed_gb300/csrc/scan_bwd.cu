@@ -33,12 +33,12 @@
 //   3. Decoupled look-back per warp towards HIGHER chunks for the carry
 //      entering from the right; aggregates re-applied in a fixed order
 //      (bitwise repeatable); time-bounded waits.
-//   4. y = sum of the warps' partials + Dskip u, and dz (all threads).
-//   5. Reverse walk per warp in blocks of 8 tokens: dA (per thread), dB
+//   4. Reverse walk per warp in blocks of 8 tokens: dA (per thread), dB
 //      contributions (ColSum16), partial sums over the warp's states
 //      for du and d delta; after each block all threads add the warps'
-//      partials in a fixed order and write du, d delta_raw.
-//   6. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
+//      partials in a fixed order and write du, d delta_raw and dz (with
+//      y = the warps' C.h partials + Dskip u).
+//   5. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
 // Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
 // and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
 #include "common.cuh"
@@ -80,9 +80,10 @@ struct BwdSmem {
   alignas(16) float CT[N * kP];
   // ---- exponent offset per token: -inf at a sequence start, else 0
   alignas(16) float off[kL];
-  // ---- cross-warp partials: y partials [W][kL][kTile] after the forward
-  //      walk, then (du, d delta) partials [2][W][kRB][kTile] float2 in the
-  //      reverse walk
+  // ---- cross-warp partials: C.h of each warp's state pair [W][kL][kTile]
+  //      from the forward walk, and (du, d delta) partials
+  //      [2][W][kRB][kTile] float2 from each block of the reverse walk
+  alignas(16) float ypart[W * kL * kTile];
   alignas(16) float part[W * kL * kTile];
   float redD[W * kTile];
   float redB[W * kTile];
@@ -326,7 +327,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         hist[t] = h;
         E = mul2(E, at);
         tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
-        if (a.has_z) sm.part[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
+        if (a.has_z) sm.ypart[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
         // dC contributions g_t h_t, summed over the tile's channels
         colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &dcs[t >> 4]);
       }
@@ -393,27 +394,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int tt = 16 * q + ColSum16::token(lane);
     if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + N + nF) * a.T + t0 + tt] = dcs[q];
   }
-  __syncthreads();  // y partials complete
-
-  // ---- 4. y = C.h + Dskip u and dz
-  if (a.has_z) {
-    T* gdz = static_cast<T*>(a.dz);
-#pragma unroll
-    for (int i = tid; i < kL * kTile; i += kThr) {
-      const int t = i / kTile, c = i - t * kTile;
-      float y = 0.0f;
-#pragma unroll
-      for (int v = 0; v < W; ++v) y += sm.part[(v * kL + t) * kTile + c];
-      const float uv = to_f(sm.u[t * bx + c]);
-      y = fmaf(a.Dskip ? sm.dsk[c] : 0.0f, uv, y);
-      const float go = to_f(sm.dout[t * bx + c]);
-      const float zz = to_f(sm.z[t * bx + c]);
-      const float sz = sigmoidf_fast(zz);
-      const float dzv = go * sz * fmaf(zz, 1.0f - sz, 1.0f) * y;
-      if (t < rows && c < bx && d0 + c < a.D) gdz[(t0 + t) * a.D + d0 + c] = from_f<T>(dzv);
-    }
-  }
-  __syncthreads();  // part is reused below
+  // no barrier here: the reverse walk writes only its own partial buffers,
+  // and the block barriers below order every cross-warp read
 
   // ---- 5. reverse walk in blocks of kRB tokens
   float2 dA = make_float2(0.0f, 0.0f);
@@ -423,6 +405,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     float2* const part2 = reinterpret_cast<float2*>(sm.part);  // [2][W][kRB][kTile]
     T* gdu = static_cast<T*>(a.du);
     T* gddr = static_cast<T*>(a.ddr);
+    T* gdz = static_cast<T*>(a.dz);
     float2 r = x;  // carry entering the current token from the right
 #pragma unroll
     for (int blk = kL / kRB - 1; blk >= 0; --blk) {
@@ -464,22 +447,34 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         }
       }
       __syncthreads();  // the block's partials are complete
-      // du, d delta_raw of the block: thread i takes token blk*kRB + i / kTile,
-      // channel i % kTile (= lane), and adds the warps' partials in order
+      // du, d delta_raw and dz of the block: thread i takes token
+      // blk*kRB + i / kTile, channel i % kTile (= lane), and adds the warps'
+      // partials in order
       for (int i = tid; i < kRB * kTile; i += kThr) {
         const int e = i / kTile;
         const int t = blk * kRB + e;
         float2 sp = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int v = 0; v < W; ++v) sp = __fadd2_rn(sp, part2[((buf * W + v) * kRB + e) * kTile + lane]);
+        float y = 0.0f;  // y = C.h + Dskip u, for dz
+        if (a.has_z) {
+#pragma unroll
+          for (int v = 0; v < W; ++v) y += sm.ypart[(v * kL + t) * kTile + lane];
+        }
+        const float dlt = sm.dl[lane * kP + t], gt = sm.g[lane * kP + t];
+        const float uv = to_f(sm.u[t * bx + lane]);
+        const float gdu_t = fmaf(dlt, sp.x, Dsk * gt);
+        const float gdr_t = fmaf(uv, sp.x, sp.y * kLn2) * sm.sg[lane * kP + t];
         if (t < rows && valid) {
-          const float dlt = sm.dl[lane * kP + t], gt = sm.g[lane * kP + t];
-          const float uv = to_f(sm.u[t * bx + lane]);
-          const float gdu_t = fmaf(dlt, sp.x, Dsk * gt);
-          const float gdr_t = fmaf(uv, sp.x, sp.y * kLn2) * sm.sg[lane * kP + t];
           const int64_t at_td = (t0 + t) * a.D + d;
           gdu[at_td] = from_f<T>(gdu_t);
           gddr[at_td] = from_f<T>(gdr_t);
+          if (a.has_z) {
+            const float go = to_f(sm.dout[t * bx + lane]);
+            const float zz = to_f(sm.z[t * bx + lane]);
+            const float sz = sigmoidf_fast(zz);
+            gdz[at_td] = from_f<T>(go * sz * fmaf(zz, 1.0f - sz, 1.0f) * fmaf(Dsk, uv, y));
+          }
           sDD = fmaf(gt, uv, sDD);
           sDB += gdr_t;
         }
