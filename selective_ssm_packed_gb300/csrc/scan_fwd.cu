@@ -9,7 +9,8 @@
 //      with 1-D bulk copies; one mbarrier.  The kernel is persistent (one CTA
 //      per resident slot, looping over tickets), and one thread requests the
 //      next item's copies as soon as the current item has read its inputs.
-//   2. delta = softplus(delta_raw + dt_bias) once per (token, channel) -> smem.
+//   2. delta = softplus(delta_raw + dt_bias) once per (token, channel), in
+//      pass 1, kept in shared memory for pass 2.
 //   3. Pass 1: every thread scans its K tokens from h = 0 and records the
 //      sub-chunk aggregate: H (the state reached) and the sum of delta since
 //      the last sequence start; the product of the transition factors over the
@@ -157,15 +158,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
-  // ---- step 2: delta for my tokens
-#pragma unroll 2  // the tokens come from shared memory: keep the code small
-  for (int k = 0; k < kK; ++k) {
-    const int t = tb + k;
-    const float r = to_f(sm.dr[t * bx + lane]) + bias;
-    sm.dlt[t * kTile + lane] = a.delta_softplus ? softplusf(r) : r;
-  }
-
-  // ---- step 3: pass 1, sub-chunk aggregate from h = 0
+  // ---- steps 2-3: delta for my tokens (kept for pass 2) and pass 1, the
+  //      sub-chunk aggregate from h = 0
   float2 h[P];
 #pragma unroll
   for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
@@ -175,13 +169,15 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
+    const float r = to_f(sm.dr[t * bx + lane]) + bias;
+    const float dl = a.delta_softplus ? softplusf(r) : r;
+    sm.dlt[t * kTile + lane] = dl;
     if (pos_at(t) == 0) {
 #pragma unroll
       for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
       sd = 0.0f;
       rs = 1;
     }
-    const float dl = sm.dlt[t * kTile + lane];
     const float2 dl2 = splat2(dl), du2 = splat2(dl * to_f(sm.u[t * bx + lane]));
     float2 Bv[P];
     lds_pairs<N>(Bv, Bf + t * N);
