@@ -165,7 +165,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
   float sd = 0.0f;
   int rs = 0;
-#pragma unroll 2  // the tokens come from shared memory: keep the code small
+#pragma unroll 4  // tokens come from shared memory; 4 overlap well without a huge body
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
@@ -335,7 +335,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
 
   T* out = static_cast<T*>(a.out);
-#pragma unroll 2  // the tokens come from shared memory: keep the code small
+#pragma unroll 4  // tokens come from shared memory; 4 overlap well without a huge body
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
