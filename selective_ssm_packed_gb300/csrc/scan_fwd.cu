@@ -194,6 +194,20 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   if (lane == 0) sm.aggRS[s] = rs;
   __syncthreads();
 
+  // Warp 0 acquires the previous chunk's flag and reads its inclusive state
+  // now; the loads land during the scan below.  (That chunk started long
+  // before this one: its state is nearly always published by now.  The reads
+  // follow the acquire in program order, so they see what the flag publishes.)
+  int early_f = kFlagNone;
+  float early_x[N];
+  if (s == 0 && chunk > 0 && pos_at(0) != 0) {
+    const int64_t jslot = (int64_t)tile * a.n_chunks + chunk - 1;
+    early_f = ld_acquire_gpu(a.flags + jslot * kTile + lane);
+    const float* inc = a.incl + jslot * (N * kTile);
+#pragma unroll
+    for (int n = 0; n < N; ++n) early_x[n] = __ldcg(inc + n * kTile + lane);
+  }
+
   // ---- step 4: exclusive scan over sub-chunks; chain (lane, n) with n % kS == s
   {
     float sdj[kS];
@@ -258,7 +272,13 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       // chunk's aggregate only when the walk has to go further
       const int64_t base = (int64_t)tile * a.n_chunks;
       int j = chunk - 1, found = -1, timed_out = 0;
-      if (ld_acquire_gpu(a.flags + (base + j) * kTile + lane) == kFlagInclusive) {
+      bool have_x = false;
+      if (early_f == kFlagInclusive) {
+        found = j;
+        have_x = true;
+#pragma unroll
+        for (int n = 0; n < N; ++n) x[n] = early_x[n];
+      } else if (ld_acquire_gpu(a.flags + (base + j) * kTile + lane) == kFlagInclusive) {
         found = j;
       } else {
         if (!rs_any) {
@@ -277,9 +297,11 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int first = j + 1;
       if (found >= 0) {
-        const float* inc = a.incl + (base + found) * (N * kTile);
+        if (!have_x) {
+          const float* inc = a.incl + (base + found) * (N * kTile);
 #pragma unroll
-        for (int n = 0; n < N; ++n) x[n] = __ldcg(inc + n * kTile + lane);
+          for (int n = 0; n < N; ++n) x[n] = __ldcg(inc + n * kTile + lane);
+        }
         first = found + 1;
       }
       for (int i = first; i < chunk; ++i) {
@@ -308,8 +330,6 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   if (release_incl)
     st_release_gpu(a.flags + ((int64_t)tile * a.n_chunks + chunk) * kTile + lane, kFlagInclusive);
 
-  // the next ticket, drawn now and used once pass 2 has read this item's
-  // inputs (the atomic's latency hides behind pass 2)
   // ---- step 6: exact start state, pass 2
   int rs_pre = 0;
   float sd_pre = 0.0f;
