@@ -47,7 +47,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 struct Layout {
   size_t flags = 0, pos = 0, agg = 0, agg_sd = 0, incl = 0;
   size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, conv_part = 0;
-  size_t clear_bytes = 0, total = 0;
+  size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
 
 Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
@@ -66,7 +66,8 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   l.agg_sd = off;
   off += up(sizeof(float) * (size_t)slots * (bwd ? N : 1) * kTile);
   l.incl = off;
-  off += up(sizeof(float) * (size_t)slots * N * kTile);
+  l.incl_bytes = sizeof(float) * (size_t)slots * N * kTile;
+  off += up(l.incl_bytes);
   if (bwd) {
     l.part_bc = off;
     off += up(sizeof(float) * (size_t)n_tiles * T * 2 * N);
@@ -449,6 +450,10 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  // every carry word starts as the all-ones NaN (bytes 0xff) that the kernel
+  // reads as "not stored yet": a carry is its own flag
+  if (T > 0) e = cudaMemsetAsync(at<char>(workspace, l.incl), 0xff, l.incl_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "filling the look-back carries");
 
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;

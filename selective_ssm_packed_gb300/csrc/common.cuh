@@ -175,6 +175,50 @@ __device__ __forceinline__ int wait_flag(const int* flag, uint64_t limit_ns) {
   }
 }
 
+// A carry word that holds no value yet: the all-ones NaN.  The caller fills a
+// carry array with it before the launch.  FP32 arithmetic never yields it (a
+// NaN result is the canonical 0x7fffffff) and st_carry turns it into that NaN
+// all the same, so a carry word is its own flag: each 32-bit half of a 64-bit
+// access is single-copy atomic, and a reader sees either kCarryUnset or the
+// whole value, with no fence on either side.
+constexpr unsigned kCarryUnset = 0xffffffffu;
+
+__device__ __forceinline__ float2 ld_carry(const float2* p) {
+  unsigned x, y;
+  asm volatile("ld.relaxed.gpu.global.v2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "l"(p) : "memory");
+  return make_float2(__uint_as_float(x), __uint_as_float(y));
+}
+
+__device__ __forceinline__ bool carry_set(float2 v) {
+  return __float_as_uint(v.x) != kCarryUnset && __float_as_uint(v.y) != kCarryUnset;
+}
+
+__device__ __forceinline__ void st_carry(float2* p, float2 v) {
+  unsigned x = __float_as_uint(v.x), y = __float_as_uint(v.y);
+  x = x == kCarryUnset ? 0x7fffffffu : x;
+  y = y == kCarryUnset ? 0x7fffffffu : y;
+  asm volatile("st.relaxed.gpu.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(x), "r"(y) : "memory");
+}
+
+// Warp-wide wait on one look-back slot whose carry words are their own flags
+// and whose aggregate is announced by `flag`.  Returns kFlagInclusive once
+// every lane's carry word holds a value (the value in *v), kFlagAggregate once
+// every lane has acquired the aggregate flag, kFlagNone after `limit_ns`.  The
+// result is the same in every lane.
+__device__ __forceinline__ int wait_carry(const float2* carry, const int* flag, uint64_t limit_ns,
+                                          float2* v) {
+  const uint64_t t0 = globaltimer_ns();
+  unsigned backoff = 32;
+  for (;;) {
+    *v = ld_carry(carry);
+    if (__all_sync(0xffffffffu, carry_set(*v))) return kFlagInclusive;
+    if (__all_sync(0xffffffffu, ld_acquire_gpu(flag) == kFlagAggregate)) return kFlagAggregate;
+    if (__shfl_sync(0xffffffffu, globaltimer_ns() - t0 > limit_ns, 0)) return kFlagNone;
+    __nanosleep(backoff);
+    if (backoff < 1024) backoff <<= 1;
+  }
+}
+
 // ------------------------------------------------------------------ mbarrier + TMA
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -75,7 +75,8 @@ struct ScanArgs {
   // agg / incl [n_tiles][n_chunks][N][kTile], agg_sd [n_tiles][n_chunks][kTile]
   // (sum of delta).  bwd: one chain per (warp = state pair, channel), flags
   // [n_tiles][n_chunks][N/2], agg / incl / agg_sd [n_tiles][n_chunks][N/2][kTile]
-  // float2, agg_sd holding the products of the transition factors.
+  // float2, agg_sd holding the products of the transition factors; the flags
+  // announce aggregates only, and incl starts filled with kCarryUnset words.
   int* flags;
   float* agg;
   float* agg_sd;

@@ -32,7 +32,10 @@
 //      fed token by token); C_t.h_t partials for y.
 //   3. Decoupled look-back per warp towards HIGHER chunks for the carry
 //      entering from the right; aggregates re-applied in a fixed order
-//      (bitwise repeatable); time-bounded waits.
+//      (bitwise repeatable); time-bounded waits.  An inclusive carry is its
+//      own flag (the carry array starts filled with a NaN word that no
+//      stored value equals), so it is stored and read with no fence; only an
+//      aggregate is announced by a flag, behind a fence.
 //   4. Reverse walk per warp in blocks of 8 tokens: dA (per thread), dB
 //      contributions (ColSum16), partial sums over the warp's states
 //      for du and d delta; after each block all threads add the warps'
@@ -298,7 +301,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   float2 E = make_float2(1.0f, 1.0f), tot = make_float2(0.0f, 0.0f);
   ColSum16 colsum;
   // the forward walk's dC sums (one per lane and 16-token group), stored only
-  // after the look-back has published, so that its fence does not wait for them
+  // after the look-back, so that a fence there does not wait for them
   float dcs[kL / 16];
   {
     const float* rowc = sm.dl + lane * kP;
@@ -343,20 +346,21 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     float2* const agg = reinterpret_cast<float2*>(a.agg);
     float2* const aggp = reinterpret_cast<float2*>(a.agg_sd);
     float2* const inc = reinterpret_cast<float2*>(a.incl);
+    // the carry words are their own flags (filled with kCarryUnset before the
+    // launch); only an aggregate, published when the walk must go further,
+    // is announced by the warp's flag
     int* const my_flag = a.flags + wslot;
     // a sequence starts in this chunk: E = 0 exactly, and the carry leaving
     // to the left does not depend on what enters from the right
     const bool rs_any = (rst & (rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u))) != 0u;
-    if (rs_any) {
-      inc[wslot * 32 + lane] = tot;
-      publish_flag(my_flag, kFlagInclusive, publish, lane);
-    }
+    if (rs_any && publish) st_carry(inc + wslot * 32 + lane, tot);
     if (chunk < a.n_chunks - 1) {
       // the next chunk of the tile started long before this one and has
-      // usually published its inclusive carry: look first, and publish this
+      // usually stored its inclusive carry: look first, and publish this
       // chunk's aggregate only when the walk has to go further
       int j = chunk + 1, found = -1, timed_out = 0;
-      if (__all_sync(0xffffffffu, ld_acquire_gpu(a.flags + (base + j) * W + w) == kFlagInclusive)) {
+      float2 v = ld_carry(inc + ((base + j) * W + w) * 32 + lane);
+      if (__all_sync(0xffffffffu, carry_set(v))) {
         found = j;
       } else {
         if (!rs_any) {
@@ -365,7 +369,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
           publish_flag(my_flag, kFlagAggregate, publish, lane);
         }
         while (j < a.n_chunks) {
-          const int f = wait_flag(a.flags + (base + j) * W + w, a.wait_ns);
+          const int f = wait_carry(inc + ((base + j) * W + w) * 32 + lane, a.flags + (base + j) * W + w,
+                                   a.wait_ns, &v);
           if (f == kFlagInclusive) { found = j; break; }
           if (f == kFlagNone) { timed_out = 1; break; }
           ++j;
@@ -374,7 +379,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
       int last = j - 1;
       if (found >= 0) {
-        x = __ldcg(inc + ((base + found) * W + w) * 32 + lane);
+        x = v;
         last = found - 1;
       }
       for (int i = last; i > chunk; --i) {
@@ -382,12 +387,9 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         x = fma2(__ldcg(aggp + ws), x, __ldcg(agg + ws));
       }
     }
-    if (!rs_any) {
-      // released at once: the previous chunk of the tile may already be
-      // waiting, and every link of that chain adds this item's delay
-      inc[wslot * 32 + lane] = fma2(E, x, tot);
-      publish_flag(my_flag, kFlagInclusive, publish, lane);
-    }
+    // stored at once: the previous chunk of the tile may already be waiting,
+    // and every link of that chain adds this item's delay
+    if (!rs_any && publish) st_carry(inc + wslot * 32 + lane, fma2(E, x, tot));
   }
 #pragma unroll
   for (int q = 0; q < kL / 16; ++q) {
