@@ -53,6 +53,7 @@ namespace {
 
 constexpr int kL = kBwdChunk;   // 32 tokens per work item
 constexpr int kP = kL + 4;      // row pitch of the [channel][token] arrays
+constexpr int kPP = kL + 2;     // token pitch (in pairs) of the paired B / C arrays
 constexpr int kRB = 8;          // tokens per block of the reverse walk
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -78,9 +79,13 @@ struct BwdSmem {
   alignas(16) float dlu[kTile * kP];  // delta * u
   alignas(16) float g[kTile * kP];    // dout * SiLU(z)
   alignas(16) float sg[kTile * kP];   // d delta / d delta_raw
-  // ---- B, C as [state][token] with pitch kP, fp32 (zero past the last token)
-  alignas(16) float BT[N * kP];
-  alignas(16) float CT[N * kP];
+  // ---- B, C paired per warp, fp32 (zero past the last token): entry
+  //      [o][w][t] of BP is (B_t[2w], B_t[2w+1]) for o = 0 and the swapped
+  //      pair for o = 1, so a lane loads its state pair, in its own order,
+  //      for 2 tokens with one 16-byte access and feeds it to the paired FP32
+  //      instructions as loaded; the pitch kPP keeps the stores conflict-free
+  alignas(16) float BP[2 * W * kPP * 2];
+  alignas(16) float CP[2 * W * kPP * 2];
   // ---- exponent offset per token: -inf at a sequence start, else 0
   alignas(16) float off[kL];
   // ---- cross-warp partials: C.h of each warp's state pair [W][kL][kTile]
@@ -276,8 +281,13 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
   for (int i = tid; i < N * kL; i += kThr) {
     const int t = i / N, n = i - t * N;  // consecutive lanes: consecutive states
-    sm.BT[n * kP + t] = t < rows ? to_f(sm.B[t * N + n]) : 0.0f;
-    sm.CT[n * kP + t] = t < rows ? to_f(sm.C[t * N + n]) : 0.0f;
+    const int pw = n >> 1, e = n & 1;
+    const float bv = t < rows ? to_f(sm.B[t * N + n]) : 0.0f;
+    const float cv = t < rows ? to_f(sm.C[t * N + n]) : 0.0f;
+    sm.BP[(pw * kPP + t) * 2 + e] = bv;
+    sm.BP[((W + pw) * kPP + t) * 2 + 1 - e] = bv;
+    sm.CP[(pw * kPP + t) * 2 + e] = cv;
+    sm.CP[((W + pw) * kPP + t) * 2 + 1 - e] = cv;
   }
   // bit t: token t starts a sequence
   const unsigned rst =
@@ -288,6 +298,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // (the column-sum butterflies keep a lane's first state)
   const int n0 = 2 * w;
   const int nF = n0 + ((lane >> 4) & 1), nS = n0 + 1 - ((lane >> 4) & 1);
+  const float* const bp = sm.BP + ((((lane >> 4) & 1) * W + w) * kPP) * 2;  // this lane's pairs
+  const float* const cp = sm.CP + ((((lane >> 4) & 1) * W + w) * kPP) * 2;
   float2 A2 = make_float2(0.0f, 0.0f), h = make_float2(0.0f, 0.0f);
   if (valid) {
     A2 = make_float2(sm.Araw[lane * N + nF] * kLog2e, sm.Araw[lane * N + nS] * kLog2e);
@@ -310,23 +322,25 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       const float4 dl4 = *reinterpret_cast<const float4*>(rowc + 4 * kb);
       const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
       const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
-      const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + nF * kP + 4 * kb);
-      const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + nS * kP + 4 * kb);
-      const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + nF * kP + 4 * kb);
-      const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + nS * kP + 4 * kb);
+      const float4 b01 = *reinterpret_cast<const float4*>(bp + 8 * kb);
+      const float4 b23 = *reinterpret_cast<const float4*>(bp + 8 * kb + 4);
+      const float4 c01 = *reinterpret_cast<const float4*>(cp + 8 * kb);
+      const float4 c23 = *reinterpret_cast<const float4*>(cp + 8 * kb + 4);
       const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
       const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
       const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
       const float dua[4] = {du4.x, du4.y, du4.z, du4.w};
       const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
-      const float bxa[4] = {bx4.x, bx4.y, bx4.z, bx4.w}, bya[4] = {by4.x, by4.y, by4.z, by4.w};
-      const float cxa[4] = {cx4.x, cx4.y, cx4.z, cx4.w}, cya[4] = {cy4.x, cy4.y, cy4.z, cy4.w};
+      const float2 Ba[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w), make_float2(b23.x, b23.y),
+                            make_float2(b23.z, b23.w)};
+      const float2 Ca[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
+                            make_float2(c23.z, c23.w)};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = 4 * kb + e;
-        const float2 at = ex2x2(fma2(splat2(dla[e]), A2, splat2(ofa[e])));
-        const float2 Ct = make_float2(cxa[e], cya[e]);
-        h = fma2(at, h, mul2(splat2(dua[e]), make_float2(bxa[e], bya[e])));
+        const float2 at = make_float2(ex2(fmaf(dla[e], A2.x, ofa[e])), ex2(fmaf(dla[e], A2.y, ofa[e])));
+        const float2 Ct = Ca[e];
+        h = fma2(at, h, mul2(splat2(dua[e]), Ba[e]));
         hist[t] = h;
         E = mul2(E, at);
         tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
@@ -418,23 +432,25 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         const float4 dl4 = *reinterpret_cast<const float4*>(sm.dl + lane * kP + 4 * kb);
         const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
         const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
-        const float4 bx4 = *reinterpret_cast<const float4*>(sm.BT + nF * kP + 4 * kb);
-        const float4 by4 = *reinterpret_cast<const float4*>(sm.BT + nS * kP + 4 * kb);
-        const float4 cx4 = *reinterpret_cast<const float4*>(sm.CT + nF * kP + 4 * kb);
-        const float4 cy4 = *reinterpret_cast<const float4*>(sm.CT + nS * kP + 4 * kb);
+        const float4 b01 = *reinterpret_cast<const float4*>(bp + 8 * kb);
+        const float4 b23 = *reinterpret_cast<const float4*>(bp + 8 * kb + 4);
+        const float4 c01 = *reinterpret_cast<const float4*>(cp + 8 * kb);
+        const float4 c23 = *reinterpret_cast<const float4*>(cp + 8 * kb + 4);
         const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
         const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
         const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
         const float dua[4] = {du4.x, du4.y, du4.z, du4.w};
         const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
-        const float bxa[4] = {bx4.x, bx4.y, bx4.z, bx4.w}, bya[4] = {by4.x, by4.y, by4.z, by4.w};
-        const float cxa[4] = {cx4.x, cx4.y, cx4.z, cx4.w}, cya[4] = {cy4.x, cy4.y, cy4.z, cy4.w};
+        const float2 Ba[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w), make_float2(b23.x, b23.y),
+                              make_float2(b23.z, b23.w)};
+        const float2 Ca[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
+                              make_float2(c23.z, c23.w)};
 #pragma unroll
         for (int e = 3; e >= 0; --e) {
           const int t = 4 * kb + e;
-          const float2 at = ex2x2(fma2(splat2(dla[e]), A2, splat2(ofa[e])));
-          const float2 Bt = make_float2(bxa[e], bya[e]);
-          const float2 dh = fma2(make_float2(cxa[e], cya[e]), splat2(ga[e]), r);  // total gradient w.r.t. h_t
+          const float2 at = make_float2(ex2(fmaf(dla[e], A2.x, ofa[e])), ex2(fmaf(dla[e], A2.y, ofa[e])));
+          const float2 Bt = Ba[e];
+          const float2 dh = fma2(Ca[e], splat2(ga[e]), r);  // total gradient w.r.t. h_t
           // a_t h_{t-1} = h_t - delta u B: no need for the previous state
           const float2 dhq = mul2(dh, fma2(splat2(-dua[e]), Bt, hist[t]));
           dA = fma2(splat2(dla[e]), dhq, dA);
