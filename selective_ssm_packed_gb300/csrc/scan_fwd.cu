@@ -165,6 +165,36 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
   float sd = 0.0f;
   int rs = 0;
+  // bit k: token tb + k starts a sequence (tokens past the chunk's end never do)
+  const unsigned rm = __ballot_sync(0xffffffffu, lane < kK && tb + lane < rows && pos_at(tb + lane) == 0);
+  // the common case, a whole sub-chunk of a full-width tile, is walked with
+  // compile-time offsets; the last chunk's ragged tail and narrow tiles take
+  // the general loop
+  const bool whole = tb + kK <= rows && bx == kTile;
+  if (whole) {
+    const T* const drp = sm.dr + tb * kTile + lane;
+    const T* const up = sm.u + tb * kTile + lane;
+    float* const dlp = sm.dlt + tb * kTile + lane;
+    const float* const bp = Bf + tb * N;
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+      const float r = to_f(drp[k * kTile]) + bias;
+      const float dl = a.delta_softplus ? softplusf(r) : r;
+      dlp[k * kTile] = dl;
+      if ((rm >> k) & 1u) {
+#pragma unroll
+        for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
+        sd = 0.0f;
+        rs = 1;
+      }
+      const float2 dl2 = splat2(dl), du2 = splat2(dl * to_f(up[k * kTile]));
+      float2 Bv[P];
+      lds_pairs<N>(Bv, bp + k * N);
+#pragma unroll
+      for (int i = 0; i < P; ++i) h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
+      sd += dl;
+    }
+  } else {
 #pragma unroll 4  // tokens come from shared memory; 4 overlap well without a huge body
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
@@ -184,6 +214,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
     for (int i = 0; i < P; ++i) h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
     sd += dl;
+  }
   }
 #pragma unroll
   for (int i = 0; i < P; ++i) {
@@ -355,6 +386,37 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
 
   T* out = static_cast<T*>(a.out);
+  if (whole) {
+    const T* const up = sm.u + tb * kTile + lane;
+    const T* const zp = sm.z + tb * kTile + lane;
+    const float* const dlp = sm.dlt + tb * kTile + lane;
+    const float* const bp = Bf + tb * N;
+    const float* const cp = Cf + tb * N;
+    T* op = out + (t0 + tb) * a.D + d;
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+      if ((rm >> k) & 1u) {
+#pragma unroll
+        for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
+      }
+      const float dl = dlp[k * kTile];
+      const float uu = to_f(up[k * kTile]);
+      const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+      float2 Bv[P], Cv[P];
+      lds_pairs<N>(Bv, bp + k * N);
+      lds_pairs<N>(Cv, cp + k * N);
+      float2 y2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
+        y2 = fma2(Cv[i], h[i], y2);
+      }
+      float y = fmaf(Dsk, uu, y2.x + y2.y);
+      if (a.has_z) y *= siluf(to_f(zp[k * kTile]));
+      if (valid) *op = from_f<T>(y);
+      op += a.D;
+    }
+  } else {
 #pragma unroll 4  // tokens come from shared memory; 4 overlap well without a huge body
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
@@ -378,6 +440,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     float y = fmaf(Dsk, uu, y2.x + y2.y);
     if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane]));
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
+  }
   }
 
   // every input of this item has been read: draw the next one
