@@ -195,7 +195,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       sd += dl;
     }
   } else {
-#pragma unroll 4  // tokens come from shared memory; 4 overlap well without a huge body
+#pragma unroll 1  // ragged tails and narrow tiles only: kept small for the instruction cache
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
@@ -417,7 +417,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       op += a.D;
     }
   } else {
-#pragma unroll 4  // tokens come from shared memory; 4 overlap well without a huge body
+#pragma unroll 1  // ragged tails and narrow tiles only: kept small for the instruction cache
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
