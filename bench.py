@@ -36,12 +36,14 @@ if ROOT not in sys.path:
 METRIC = "packed tokens/s for varlen conv1d+selective scan fwd+bwd; % of roofline"
 
 # Algorithmic per-token counts of the step (bytes moved, FP32-pipe ops with
-# FMA = 1, MUFU ops), e = bytes per I/O element; see the design doc.
+# FMA = 1, MUFU ops), e = bytes per I/O element; see the design doc.  The forward
+# writes the pre-gate output y and the backward reads it for dz (so it does not
+# recompute C.h).
 def per_token_counts(D, N, e, W=4):
     return {
         "conv_fwd": dict(bytes=2 * e * D + 4, fp32=(W + 3) * D, mufu=2 * D),
-        "scan_fwd": dict(bytes=4 * e * D + 2 * e * N + 4, fp32=4 * D * N + 10 * D, mufu=D * N + 4 * D),
-        "scan_bwd": dict(bytes=7 * e * D + 2 * e * N + 8 * N + 4, fp32=13 * D * N + 24 * D, mufu=D * N + 6 * D),
+        "scan_fwd": dict(bytes=5 * e * D + 2 * e * N + 4, fp32=4 * D * N + 10 * D, mufu=D * N + 4 * D),
+        "scan_bwd": dict(bytes=8 * e * D + 2 * e * N + 8 * N + 4, fp32=12 * D * N + 24 * D, mufu=D * N + 6 * D),
         "conv_bwd": dict(bytes=3 * e * D + 4, fp32=(3 * W + 6) * D, mufu=2 * D),
     }
 
@@ -50,9 +52,6 @@ def per_token_counts(D, N, e, W=4):
 # capture of a kernel, per token; reset an entry to nothing as soon as the
 # kernel changes (profiles/ keeps the capture summaries).
 LAST_CAPTURE_TRAFFIC = {
-    ("m14b", "scan_bwd"): {"bytes_per_token": (337.196544e6 + 440.187136e6) / 8192,
-                           "source": "ncu capture of scan_bwd_kernel on m14b_small (T=8192), "
-                                     "scaled by tokens; profiles/scan_bwd_m14b_small.md"},
 }
 
 
@@ -293,6 +292,7 @@ def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=No
     pos = torch.empty(T, dtype=torch.int32, device=device)
     u = torch.empty(T, D, dtype=tdt, device=device)
     out = torch.empty_like(u)
+    ypre = torch.empty_like(u)  # the forward's pre-gate output, which the backward takes for dz
     states = torch.empty(vs.chunk_states_shape(T, D, N), dtype=torch.float32, device=device)
     grads = {"du": torch.empty_like(u), "ddelta_raw": torch.empty_like(u), "dz": torch.empty_like(u),
              "dA": torch.empty(D, N, device=device), "dB": torch.empty(T, N, device=device),
@@ -309,9 +309,9 @@ def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=No
         vs.varlen_position_indices(cu, T, out=pos)
         vs.varlen_conv1d_fwd(x, cw, cb, cu, pos, out=u, workspace=ws["cf"])
         vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, chunk_states=states,
-                                     workspace=ws["sf"])
+                                     workspace=ws["sf"], y=ypre)
         vs.varlen_selective_scan_bwd(u, dr, A, B, C, Dsk, z, dtb, dout, cu, states, pos, grads=grads,
-                                     workspace=ws["sb"])
+                                     workspace=ws["sb"], y=ypre)
         vs.varlen_conv1d_bwd(x, cw, cb, grads["du"], cu, pos, dx=dx, dweight=dw, dbias=db, workspace=ws["cb"])
 
     for _ in range(3):
@@ -394,6 +394,7 @@ def run_ours(args):
     pos = torch.empty(T, dtype=torch.int32, device=device)
     u = torch.empty(T, D, dtype=tdt, device=device)
     out = torch.empty_like(u)
+    ypre = torch.empty_like(u)  # the forward's pre-gate output, which the backward takes for dz
     states = torch.empty(vs.chunk_states_shape(T, D, N), dtype=torch.float32, device=device)
     grads = {"du": torch.empty_like(u), "ddelta_raw": torch.empty_like(u), "dz": torch.empty_like(u),
              "dA": torch.empty(D, N, device=device), "dB": torch.empty(T, N, device=device),
@@ -419,11 +420,11 @@ def run_ours(args):
         mark(2)
         vs.varlen_selective_scan_fwd(u, inp["delta_raw"], prm["A"], inp["B"], inp["C"], prm["Dskip"],
                                      inp["z"], prm["dt_bias"], cu, pos, out=out, chunk_states=states,
-                                     workspace=ws["sf"])
+                                     workspace=ws["sf"], y=ypre)
         mark(3)
         vs.varlen_selective_scan_bwd(u, inp["delta_raw"], prm["A"], inp["B"], inp["C"], prm["Dskip"],
                                      inp["z"], prm["dt_bias"], inp["dout"], cu, states, pos,
-                                     grads=grads, workspace=ws["sb"])
+                                     grads=grads, workspace=ws["sb"], y=ypre)
         mark(4)
         vs.varlen_conv1d_bwd(inp["x"], prm["conv_w"], prm["conv_b"], grads["du"], cu, pos,
                              dx=dx, dweight=dw, dbias=db, workspace=ws["cb"])
@@ -500,10 +501,10 @@ def run_ours(args):
             vs.varlen_conv1d_fwd(si["x"], prm["conv_w"], prm["conv_b"], c, pos, out=u, workspace=ws["cf"])
             vs.varlen_selective_scan_fwd(u, si["delta_raw"], prm["A"], si["B"], si["C"], prm["Dskip"],
                                          si["z"], prm["dt_bias"], c, pos, out=so["out"], chunk_states=states,
-                                         workspace=ws["sf"])
+                                         workspace=ws["sf"], y=ypre)
             vs.varlen_selective_scan_bwd(u, si["delta_raw"], prm["A"], si["B"], si["C"], prm["Dskip"],
                                          si["z"], prm["dt_bias"], si["dout"], c, states, pos,
-                                         grads=g, workspace=ws["sb"])
+                                         grads=g, workspace=ws["sb"], y=ypre)
             vs.varlen_conv1d_bwd(si["x"], prm["conv_w"], prm["conv_b"], g["du"], c, pos,
                                  dx=so["dx"], dweight=so["dweight"], dbias=so["dbias"], workspace=ws["cb"])
 

@@ -145,6 +145,9 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
  * chunk_states: nullable f32 (ceil(T / VSSM_STATE_CHUNK), N, D); when given,
  * entry [c][n][d] receives state n of channel d just before token
  * c*VSSM_STATE_CHUNK, which the backward call needs.
+ * y: nullable (T, D) io; when given it receives the output before the gate,
+ * y above (equal to out when z is NULL), which the backward call can take
+ * instead of recomputing it for dz.  16-byte aligned like out.
  */
 size_t varlen_selective_scan_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
 size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, int32_t N);
@@ -153,7 +156,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
                               const float* dt_bias, int32_t delta_softplus,
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
-                              vssm_dtype dtype, void* out, float* chunk_states,
+                              vssm_dtype dtype, void* out, void* y, float* chunk_states,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward: the reverse scan of the state gradient, which resets at every
@@ -162,9 +165,13 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
  *   du, ddelta_raw (w.r.t. delta_raw, i.e. before softplus), dz: (T, D) io
  *   dA (D, N), dB (T, N), dC (T, N), dDskip (D), d_dt_bias (D): f32
  * dz, dDskip, d_dt_bias may be NULL.  dz is written only when z is given.
- * chunk_states is the array the forward call filled.  Every reduction (over
- * channels for dB/dC, over tokens for dA/dDskip/d_dt_bias) is atomic-free and
- * runs in a fixed order, so results are bitwise repeatable.
+ * chunk_states is the array the forward call filled.  y is nullable: the
+ * forward call's pre-gate output (its `y` argument); with z given, dz then
+ * uses it (dz = dout * y * SiLU'(z)) instead of recomputing C.h + Dskip u,
+ * which saves the backward that work; with y NULL it is recomputed (in fp32,
+ * so for bf16 io the two ways differ by y's rounding to bf16).  Every
+ * reduction (over channels for dB/dC, over tokens for dA/dDskip/d_dt_bias) is
+ * atomic-free and runs in a fixed order, so results are bitwise repeatable.
  */
 size_t varlen_selective_scan_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
 int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
@@ -172,7 +179,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               const float* dt_bias, int32_t delta_softplus, const void* dout,
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
-                              vssm_dtype dtype, const float* chunk_states,
+                              vssm_dtype dtype, const float* chunk_states, const void* y,
                               void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream);
@@ -212,7 +219,7 @@ int varlen_selective_scan_fwd_noalloc(const void* u, const void* delta_raw, cons
                                       const void* z, const float* dt_bias, int32_t delta_softplus,
                                       const int32_t* cu_seqlens, const int32_t* position_indices,
                                       int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
-                                      vssm_dtype dtype, void* out, float* chunk_states,
+                                      vssm_dtype dtype, void* out, void* y, float* chunk_states,
                                       int32_t* status, void* stream);
 
 /* ------------------------------------------------------------ status, errors, knobs

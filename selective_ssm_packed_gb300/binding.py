@@ -41,15 +41,15 @@ SIGNATURES = {
     "varlen_selective_scan_chunk_states_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
-                                                 _vp, _vp, _vp, _sz, _vp]),
+                                                 _vp, _vp, _vp, _vp, _sz, _vp]),
     "varlen_selective_scan_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int, _vp,
-                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
-                                                 _vp]),
+                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                 _sz, _vp]),
     "varlen_selective_scan_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                          _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
-                                                         _vp, _vp, _vp, _vp]),
+                                                         _vp, _vp, _vp, _vp, _vp]),
     "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "vssm_last_error": (ctypes.c_char_p, []),
@@ -217,12 +217,20 @@ def chunk_states_shape(T, D, N):
 
 def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens,
                               position_indices=None, delta_softplus=True, out=None,
-                              chunk_states=True, workspace=None, stream=None):
-    """Returns (out, chunk_states).  chunk_states=True allocates the saved-state
-    array the backward call needs, False/None skips it, a tensor is filled."""
+                              chunk_states=True, workspace=None, stream=None, y=None):
+    """Returns (out, chunk_states), or (out, chunk_states, y) when y is asked
+    for.  chunk_states=True allocates the saved-state array the backward call
+    needs, False/None skips it, a tensor is filled.  y (the output before the
+    gate, which the backward call can take for dz): None/False skips it, True
+    allocates it, a tensor is filled."""
     T, D = u.shape
     N = A.shape[1]
     out = torch.empty_like(u) if out is None else out
+    want_y = y is not None and y is not False
+    if y is True:
+        y = torch.empty_like(u)
+    elif y is False:
+        y = None
     if chunk_states is True:
         chunk_states = torch.empty(chunk_states_shape(T, D, N), dtype=torch.float32, device=u.device)
     elif chunk_states is False:
@@ -234,16 +242,18 @@ def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqle
         _ptr(B, "B", dt), _ptr(C, "C", dt), _ptr(Dskip, "Dskip", torch.float32), _ptr(z, "z", dt),
         _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
-        cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(out, "out", dt),
+        cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(out, "out", dt), _ptr(y, "y", dt),
         _ptr(chunk_states, "chunk_states", torch.float32), _ptr(ws, "workspace"), ws.numel(),
         _stream(stream)), "varlen_selective_scan_fwd")
-    return out, chunk_states
+    return (out, chunk_states, y) if want_y else (out, chunk_states)
 
 
 def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,
                               chunk_states, position_indices=None, delta_softplus=True,
-                              grads=None, workspace=None, stream=None):
-    """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias."""
+                              grads=None, workspace=None, stream=None, y=None):
+    """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias.  y: the
+    forward call's pre-gate output (optional; dz then reads it instead of
+    recomputing it)."""
     T, D = u.shape
     N = A.shape[1]
     dt = u.dtype
@@ -263,7 +273,7 @@ def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu
         _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)), _ptr(dout, "dout", dt),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
         cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(chunk_states, "chunk_states", torch.float32),
-        _ptr(g["du"], "du", dt), _ptr(g["ddelta_raw"], "ddelta_raw", dt),
+        _ptr(y, "y", dt), _ptr(g["du"], "du", dt), _ptr(g["ddelta_raw"], "ddelta_raw", dt),
         _ptr(g["dA"], "dA", torch.float32), _ptr(g["dB"], "dB", torch.float32),
         _ptr(g["dC"], "dC", torch.float32), _ptr(g["dDskip"], "dDskip", torch.float32),
         _ptr(g["dz"], "dz", dt), _ptr(g["d_dt_bias"], "d_dt_bias", torch.float32),

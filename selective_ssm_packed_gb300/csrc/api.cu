@@ -378,12 +378,13 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
                               const float* dt_bias, int32_t delta_softplus,
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
-                              vssm_dtype dtype, void* out, float* chunk_states,
+                              vssm_dtype dtype, void* out, void* y, float* chunk_states,
                               void* workspace, size_t workspace_bytes, void* stream) {
   IO io;
   VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
                         num_seqs, total_tokens, D, N, dtype, &io));
   VSSM_TRY(check_io(out, "out", total_tokens));
+  if (y) VSSM_TRY(check_io(y, "y", total_tokens));
   if (chunk_states && !aligned16(chunk_states))
     return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
   const int64_t T = total_tokens;
@@ -398,7 +399,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
 
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
-  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out;
+  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);
   a.flags = at<int>(workspace, l.flags);
@@ -428,7 +429,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               const float* dt_bias, int32_t delta_softplus, const void* dout,
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
-                              vssm_dtype dtype, const float* chunk_states,
+                              vssm_dtype dtype, const float* chunk_states, const void* y,
                               void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream) {
@@ -445,6 +446,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   if (T > 0 && !chunk_states) return fail(VSSM_ERR_ARG, "chunk_states is NULL");
   if (z && T > 0 && !dz) return fail(VSSM_ERR_ARG, "dz is NULL although z is given");
   if (dz && !aligned16(dz)) return fail(VSSM_ERR_ALIGN, "dz is not 16-byte aligned");
+  if (y) VSSM_TRY(check_io(y, "y", T));
   const Layout l = scan_layout(T, D, N, kBwdChunk, true);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -459,6 +461,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.dout = dout; a.chunk_states = const_cast<float*>(chunk_states);
   a.du = du; a.ddr = ddelta_raw; a.dz = z ? dz : nullptr;
+  a.y = const_cast<void*>(y);
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);
   a.flags = at<int>(workspace, l.flags);
@@ -474,12 +477,14 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.n_chunks = (int)cdiv(T, kBwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
   a.has_z = z ? 1 : 0;
+  a.has_y = (z && y) ? 1 : 0;
   a.has_skip = Dskip ? 1 : 0;
   a.box_x = D < kTile ? D : kTile;
   a.box_y = T < kBwdChunk ? (int)T : kBwdChunk;
   a.drop_ticket = g_drop_ticket.load();
   a.wait_ns = g_wait_ns.load();
-  CUtensorMap mu, mdr, mz, mdo, mcs;
+  CUtensorMap mu, mdr, mz, mdo, mcs, my;
+  std::memset(&my, 0, sizeof(my));
   std::memset(&mu, 0, sizeof(mu));
   std::memset(&mdr, 0, sizeof(mdr));
   std::memset(&mz, 0, sizeof(mz));
@@ -493,11 +498,12 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
     VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
     VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
     VSSM_TRY(make_map(&mdo, dout, io, T, D, a.box_x, a.box_y));
+    if (a.has_y) VSSM_TRY(make_map(&my, y, io, T, D, a.box_x, a.box_y));
     // saved states [chunk][n][d] seen as (chunks * N) rows of D floats; one
     // copy fetches an item's N rows of its tile's channels
     VSSM_TRY(make_map(&mcs, chunk_states, IO::F32, cdiv(T, kStateChunk) * N, D, a.box_x, N));
   }
-  e = launch_scan_bwd(a, io, mu, mdr, mz, mdo, mcs, dA, dB, dC, dDskip, d_dt_bias, st);
+  e = launch_scan_bwd(a, io, mu, mdr, mz, mdo, mcs, my, dA, dB, dC, dDskip, d_dt_bias, st);
   return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_bwd launch");
 }
 

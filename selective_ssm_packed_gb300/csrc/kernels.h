@@ -62,6 +62,7 @@ struct ScanArgs {
   const int32_t* pos;
   float* chunk_states;        // fwd: written (nullable); bwd: read
   void* out;                  // fwd
+  void* y;                    // fwd: pre-gate output (nullable); bwd: the same, read (nullable)
   void* du;                   // bwd
   void* ddr;                  // bwd
   void* dz;                   // bwd (nullable)
@@ -88,6 +89,7 @@ struct ScanArgs {
   int n_chunks;
   int delta_softplus;
   int has_z;
+  int has_y;                  // bwd: dz from the given y instead of recomputed C.h + Dskip u
   int has_skip;
   int box_x;                  // tile row pitch in elements: min(kTile, D)
   int box_y;                  // tile rows: min(chunk, T)
@@ -99,7 +101,8 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z, cudaStream_t st);
 cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z,
-                            const CUtensorMap& tm_dout, const CUtensorMap& tm_cs, float* dA,
+                            const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                            const CUtensorMap& tm_y, float* dA,
                             float* dB, float* dC, float* dDskip, float* d_dt_bias, cudaStream_t st);
 
 // Sets the message vssm_last_error() returns on this thread; returns `code`.

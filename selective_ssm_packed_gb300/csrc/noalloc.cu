@@ -119,7 +119,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
     const void* u, const void* delta_raw, const float* A, const void* B, const void* C,
     const float* Dskip, const void* z, const float* dt_bias, int32_t delta_softplus,
     const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
-    int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* out, float* chunk_states,
+    int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* out, void* y, float* chunk_states,
     int32_t* status, void* stream) {
   // ---- argument checks (same rules as varlen_selective_scan_fwd)
   if (dtype != VSSM_F32 && dtype != VSSM_BF16) return err(VSSM_ERR_DTYPE, "dtype %lld not supported", dtype);
@@ -140,10 +140,10 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
       if (!al16(p)) return record_error(VSSM_ERR_ALIGN, "u, delta_raw, B, C, out must be 16-byte aligned");
     }
   }
-  if ((z && !al16(z)) || (chunk_states && !al16(chunk_states)) || !al16(A) || (Dskip && !al16(Dskip)) ||
-      (dt_bias && !al16(dt_bias)) || (position_indices && !al16(position_indices)))
+  if ((z && !al16(z)) || (y && !al16(y)) || (chunk_states && !al16(chunk_states)) || !al16(A) ||
+      (Dskip && !al16(Dskip)) || (dt_bias && !al16(dt_bias)) || (position_indices && !al16(position_indices)))
     return record_error(VSSM_ERR_ALIGN,
-                        "z, chunk_states, A, Dskip, dt_bias and position_indices must be 16-byte aligned");
+                        "z, y, chunk_states, A, Dskip, dt_bias and position_indices must be 16-byte aligned");
 
   // ---- scratch layout: [header: status, ticket][flags][pos][agg][agg_sd][incl]
   const int64_t n_tiles = cdiv(D, kTile), n_chunks = cdiv(T, kFwdChunk);
@@ -181,7 +181,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
 
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
-  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out;
+  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
   a.status = status_word;
   a.ticket = reinterpret_cast<unsigned*>(s + 4);
   a.flags = reinterpret_cast<int*>(s + o_flags);

@@ -40,7 +40,8 @@
 //      contributions (ColSum16), partial sums over the warp's states
 //      for du and d delta; after each block all threads add the warps'
 //      partials in a fixed order and write du, d delta_raw and dz (with
-//      y = the warps' C.h partials + Dskip u).
+//      y = the forward's pre-gate output when the call passes it, else the
+//      warps' C.h partials + Dskip u).
 //   5. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
 // Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
 // and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
@@ -66,6 +67,7 @@ struct BwdSmem {
   alignas(128) T dr[kL * kTile];
   alignas(128) T z[kL * kTile];
   alignas(128) T dout[kL * kTile];
+  alignas(128) T y[kL * kTile];  // the forward's pre-gate output, when the call has it
   alignas(128) T B[kL * N];
   alignas(128) T C[kL * N];
   alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
@@ -151,7 +153,8 @@ template <typename T, int N>
 __global__ void __launch_bounds__(16 * N, 512 / (16 * N))
 scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
-                const __grid_constant__ CUtensorMap tm_cs, const ScanArgs a) {
+                const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_y,
+                const ScanArgs a) {
   using SM = BwdSmem<T, N>;
   constexpr int W = SM::W;
   constexpr int kThr = 32 * W;
@@ -161,7 +164,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const int n_items = a.n_chunks * a.n_tiles;
 
   // Requests every input of work item `tkn` on the barrier: u, delta_raw,
-  // dout, z tiles; B and C rows; A rows, dt_bias, Dskip and the saved states
+  // dout, z (and y) tiles; B and C rows; A rows, dt_bias, Dskip and the saved states
   // of the tile's channels; position indices (whole groups of 4 tokens).
   auto issue = [&](int tkn) {
     const int rv = tkn / a.n_tiles;
@@ -174,13 +177,14 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 4u : 3u) + 2u * bc + nval * N * 4u +
+    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bc + nval * N * 4u +
                                        (uint32_t)a.box_x * N * 4u + rows4 * 4u +
                                        (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
     tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
     tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
     tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
     if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+    if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
     bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
     bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
     bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
@@ -344,7 +348,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         hist[t] = h;
         E = mul2(E, at);
         tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
-        if (a.has_z) sm.ypart[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
+        if (a.has_z && !a.has_y) sm.ypart[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
         // dC contributions g_t h_t, summed over the tile's channels
         colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &dcs[t >> 4]);
       }
@@ -474,8 +478,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         float2 sp = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int v = 0; v < W; ++v) sp = __fadd2_rn(sp, part2[((buf * W + v) * kRB + e) * kTile + lane]);
-        float y = 0.0f;  // y = C.h + Dskip u, for dz
-        if (a.has_z) {
+        float y = 0.0f;  // C.h, for dz, when the call has no y to read
+        if (a.has_z && !a.has_y) {
 #pragma unroll
           for (int v = 0; v < W; ++v) y += sm.ypart[(v * kL + t) * kTile + lane];
         }
@@ -491,7 +495,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             const float go = to_f(sm.dout[t * bx + lane]);
             const float zz = to_f(sm.z[t * bx + lane]);
             const float sz = sigmoidf_fast(zz);
-            gdz[at_td] = from_f<T>(go * sz * fmaf(zz, 1.0f - sz, 1.0f) * fmaf(Dsk, uv, y));
+            const float yf = a.has_y ? to_f(sm.y[t * bx + lane]) : fmaf(Dsk, uv, y);
+            gdz[at_td] = from_f<T>(go * sz * fmaf(zz, 1.0f - sz, 1.0f) * yf);
           }
           sDD = fmaf(gt, uv, sDD);
           sDB += gdr_t;
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restri
 template <typename T, int N>
 cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
-                     cudaStream_t st) {
+                     const CUtensorMap& tm_y, cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem<T, N>);
   cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -557,17 +562,17 @@ cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
   int grid = 0;
   e = persistent_grid(scan_bwd_kernel<T, N>, 16 * N, smem, items, &grid);
   if (e != cudaSuccess) return e;
-  scan_bwd_kernel<T, N><<<grid, 16 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, a);
+  scan_bwd_kernel<T, N><<<grid, 16 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, a);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
-                     cudaStream_t st) {
-  if (a.N == 16) return launch_n<T, 16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
-  if (a.N == 8) return launch_n<T, 8>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
-  if (a.N == 4) return launch_n<T, 4>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
+                     const CUtensorMap& tm_y, cudaStream_t st) {
+  if (a.N == 16) return launch_n<T, 16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  if (a.N == 8) return launch_n<T, 8>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  if (a.N == 4) return launch_n<T, 4>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
   return cudaErrorInvalidValue;
 }
 
@@ -575,8 +580,9 @@ cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
 
 cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z,
-                            const CUtensorMap& tm_dout, const CUtensorMap& tm_cs, float* dA,
-                            float* dB, float* dC, float* dDskip, float* d_dt_bias, cudaStream_t st) {
+                            const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                            const CUtensorMap& tm_y, float* dA, float* dB, float* dC, float* dDskip,
+                            float* d_dt_bias, cudaStream_t st) {
   const int64_t DN = (int64_t)a.D * a.N;
   if (a.T <= 0) {
     cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * DN, st);
@@ -584,8 +590,8 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
     if (e == cudaSuccess && d_dt_bias) e = cudaMemsetAsync(d_dt_bias, 0, sizeof(float) * a.D, st);
     return e;
   }
-  cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st)
-                                : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, st);
+  cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+                                : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
   if (e != cudaSuccess) return e;
   const int64_t M = a.T * 2 * a.N;
   sum_tiles_bc_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(a.part_dBC, a.n_tiles, a.T, a.N,

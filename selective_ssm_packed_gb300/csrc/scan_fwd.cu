@@ -386,6 +386,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
 
   T* out = static_cast<T*>(a.out);
+  T* ypre = static_cast<T*>(a.y);  // the output before the gate (nullable)
   if (whole) {
     const T* const up = sm.u + tb * kTile + lane;
     const T* const zp = sm.z + tb * kTile + lane;
@@ -393,6 +394,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float* const bp = Bf + tb * N;
     const float* const cp = Cf + tb * N;
     T* op = out + (t0 + tb) * a.D + d;
+    T* yp = ypre ? ypre + (t0 + tb) * a.D + d : nullptr;
 #pragma unroll
     for (int k = 0; k < kK; ++k) {
       if ((rm >> k) & 1u) {
@@ -412,6 +414,10 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         y2 = fma2(Cv[i], h[i], y2);
       }
       float y = fmaf(Dsk, uu, y2.x + y2.y);
+      if (yp) {
+        if (valid) *yp = from_f<T>(y);
+        yp += a.D;
+      }
       if (a.has_z) y *= siluf(to_f(zp[k * kTile]));
       if (valid) *op = from_f<T>(y);
       op += a.D;
@@ -438,6 +444,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       y2 = fma2(Cv[i], h[i], y2);
     }
     float y = fmaf(Dsk, uu, y2.x + y2.y);
+    if (ypre && valid) ypre[(t0 + t) * a.D + d] = from_f<T>(y);
     if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane]));
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
   }

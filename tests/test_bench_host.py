@@ -61,6 +61,6 @@ def test_per_token_counts_match_the_stated_totals():
     D, N, e = 4096, 16, 2
     c = bench.per_token_counts(D, N, e)
     tot = {k: sum(s[k] for s in c.values()) for k in ("bytes", "fp32", "mufu")}
-    assert tot["bytes"] == 16 * e * D + 4 * e * N + 8 * N + 16
-    assert tot["fp32"] == D * (17 * N + 59)
+    assert tot["bytes"] == 18 * e * D + 4 * e * N + 8 * N + 16
+    assert tot["fp32"] == D * (16 * N + 59)
     assert tot["mufu"] == D * (2 * N + 14)

@@ -190,6 +190,34 @@ def test_ragged_packs_fwd_bwd(lengths, D, N, dtype):
     check_chain(cu, r, res, dtype)
 
 
+@pytest.mark.parametrize("lengths,D,N,dtype", [([300, 1, 2, 257, 40], 72, 8, "f32"),
+                                               ([129, 1, 640, 77, 3], 104, 16, "bf16")])
+def test_backward_reads_the_forward_pre_gate_output(lengths, D, N, dtype):
+    """The forward call's optional y output is the pre-gate output (the oracle's
+    output with no gate); the backward call that takes it computes dz from it
+    and leaves every other gradient bitwise unchanged."""
+    cu_np, T, r = rand_case(lengths, D, N, dtype, seed=sum(lengths) + 7)
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    u = dev(r["x"], dtype)  # any (T, D) input serves as the scan's u here
+    args = dict(u=u, delta_raw=dev(r["delta_raw"], dtype), A=f32(r["A"]), B=dev(r["B"], dtype),
+                C=dev(r["C"], dtype), Dskip=f32(r["Dskip"]), z=dev(r["z"], dtype), dt_bias=f32(r["dt_bias"]))
+    out, states, y = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos, y=True)
+    dout = dev(r["dout"], dtype)
+    g_re = vs.varlen_selective_scan_bwd(**args, dout=dout, cu_seqlens=cu, chunk_states=states,
+                                        position_indices=pos)
+    g_y = vs.varlen_selective_scan_bwd(**args, dout=dout, cu_seqlens=cu, chunk_states=states,
+                                       position_indices=pos, y=y)
+    torch.cuda.synchronize()
+    sargs = [host(u), r["delta_raw"], r["A"], r["B"], r["C"], r["Dskip"], r["z"], r["dt_bias"]]
+    y_ref = oracle.scan_fwd_threaded(*sargs[:6], None, sargs[7], cu_np)
+    assert_close("y", y, y_ref, TOL[dtype])
+    g = oracle.scan_bwd_threaded(*sargs, host(dout), cu_np)
+    assert_close("dz (from y)", g_y["dz"], g["dz"], TOL[dtype])
+    for k in ("du", "ddelta_raw", "dA", "dB", "dC", "dDskip", "d_dt_bias"):
+        assert torch.equal(g_y[k], g_re[k]), k
+
+
 @pytest.mark.parametrize("flags", [dict(z=False), dict(skip=False), dict(bias=False),
                                    dict(softplus=False), dict(z=False, skip=False, bias=False)])
 def test_optional_inputs(flags):

@@ -48,11 +48,11 @@ def _p(x):
     return None if x is None else ctypes.c_void_p(x.data_ptr())
 
 
-def _noalloc(lib, t, T, D, N, dtype, out, states, status, pos=None):
+def _noalloc(lib, t, T, D, N, dtype, out, states, status, pos=None, y=None):
     return lib.varlen_selective_scan_fwd_noalloc(
         _p(t["u"]), _p(t["delta_raw"]), _p(t["A"]), _p(t["B"]), _p(t["C"]), _p(t["Dskip"]), _p(t["z"]),
         _p(t["dt_bias"]), 1, _p(t["cu"]), _p(pos), t["cu"].numel() - 1, T, D, N,
-        binding.VSSM_F32 if dtype == "f32" else binding.VSSM_BF16, _p(out), _p(states), _p(status),
+        binding.VSSM_F32 if dtype == "f32" else binding.VSSM_BF16, _p(out), _p(y), _p(states), _p(status),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
@@ -69,16 +69,18 @@ def test_noalloc_forward_matches_the_workspace_entry_point_on_two_calls(lib):
              ([5, 300, 1, 90], 72, 8, "f32", 42)]                  # second call: smaller
     for lengths, D, N, dtype, seed in cases:
         T, t = _case(lengths, D, N, dtype, seed)
-        ref_out, ref_states = vs.varlen_selective_scan_fwd(
-            t["u"], t["delta_raw"], t["A"], t["B"], t["C"], t["Dskip"], t["z"], t["dt_bias"], t["cu"])
+        ref_out, ref_states, ref_y = vs.varlen_selective_scan_fwd(
+            t["u"], t["delta_raw"], t["A"], t["B"], t["C"], t["Dskip"], t["z"], t["dt_bias"], t["cu"], y=True)
         out = torch.full_like(t["u"], float("nan"))
+        y = torch.full_like(t["u"], float("nan"))
         states = torch.full_like(ref_states, float("nan"))
         status = torch.full((1,), 7, dtype=torch.int32, device="cuda")
-        rc = _noalloc(lib, t, T, D, N, dtype, out, states, status)
+        rc = _noalloc(lib, t, T, D, N, dtype, out, states, status, y=y)
         assert rc == 0, binding.last_error()
         torch.cuda.synchronize()
         assert binding.status_code(int(status.item())) == 0
         _close("out", out, ref_out, TOL[dtype])
+        _close("y", y, ref_y, TOL[dtype])
         _close("chunk_states", states, ref_states, TOL[dtype])
 
 
@@ -88,7 +90,7 @@ def test_noalloc_refuses_a_problem_larger_than_its_scratch(lib):
     # claims 16384 tokens at D = 4096; refused on the host before any launch
     rc = lib.varlen_selective_scan_fwd_noalloc(
         _p(t["u"]), _p(t["delta_raw"]), _p(t["A"]), _p(t["B"]), _p(t["C"]), None, None, None, 1,
-        _p(t["cu"]), None, 1, 16384, 4096, 16, binding.VSSM_BF16, _p(out), None, None, None)
+        _p(t["cu"]), None, 1, 16384, 4096, 16, binding.VSSM_BF16, _p(out), None, None, None, None)
     assert rc == -4
     msg = binding.last_error()
     assert "scratch" in msg and str(64 << 20) in msg
