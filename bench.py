@@ -52,6 +52,9 @@ def per_token_counts(D, N, e, W=4):
 # capture of a kernel, per token; reset an entry to nothing as soon as the
 # kernel changes (profiles/ keeps the capture summaries).
 LAST_CAPTURE_TRAFFIC = {
+    ("m14b", "scan_bwd"): {"bytes_per_token": (404.029184e6 + 439.640064e6) / 8192,
+                           "source": "ncu capture of scan_bwd_kernel on m14b_small (T=8192), "
+                                     "scaled by tokens; profiles/scan_bwd_m14b_small.md"},
 }
 
 
