@@ -146,9 +146,13 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // tail, past the last whole group of 4, is read from global memory)
   auto pos_at = [&](int t) { return t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t); };
 
-  const float* Bf = widen_rows<T>(sm.B, sm.Bf, rows * N, tid, kThreads);
-  const float* Cf = widen_rows<T>(sm.C, sm.Cf, rows * N, tid, kThreads);
-  __syncthreads();
+  const int tb = s * kK;  // first token (within the chunk) of this thread
+  // B and C rows of this warp's own tokens, widened to fp32 by the warp: no
+  // other warp reads them, so a warp barrier is enough
+  const int wr0 = tb < rows ? tb : rows, wr1 = tb + kK < rows ? tb + kK : rows;
+  const float* Bf = widen_rows<T>(sm.B + wr0 * N, sm.Bf + wr0 * N, (wr1 - wr0) * N, lane, 32) - wr0 * N;
+  const float* Cf = widen_rows<T>(sm.C + wr0 * N, sm.Cf + wr0 * N, (wr1 - wr0) * N, lane, 32) - wr0 * N;
+  __syncwarp();
   float2 A2[P];
   if (valid) {
     load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, kLog2e);
@@ -157,7 +161,6 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
   }
 
-  const int tb = s * kK;  // first token (within the chunk) of this thread
   // ---- steps 2-3: delta for my tokens (kept for pass 2) and pass 1, the
   //      sub-chunk aggregate from h = 0
   float2 h[P];
