@@ -63,8 +63,10 @@ def rand_case(lengths, D, N, dtype, seed, W=4):
     return cu, T, r
 
 
-def run_chain(cu_np, T, r, dtype, with_bwd=True, z=True, skip=True, bias=True, softplus=True):
-    """conv fwd -> scan fwd (-> scan bwd -> conv bwd) through the C ABI."""
+def run_chain(cu_np, T, r, dtype, with_bwd=True, z=True, skip=True, bias=True, softplus=True, use_y=False):
+    """conv fwd -> scan fwd (-> scan bwd -> conv bwd) through the C ABI.  use_y:
+    the forward also writes its pre-gate output and the backward takes it (the
+    bench step's configuration)."""
     cu = torch.from_numpy(cu_np).cuda()
     pos = vs.varlen_position_indices(cu, T)
     x = dev(r["x"], dtype)
@@ -72,13 +74,20 @@ def run_chain(cu_np, T, r, dtype, with_bwd=True, z=True, skip=True, bias=True, s
     args = dict(u=u, delta_raw=dev(r["delta_raw"], dtype), A=f32(r["A"]), B=dev(r["B"], dtype),
                 C=dev(r["C"], dtype), Dskip=f32(r["Dskip"]) if skip else None,
                 z=dev(r["z"], dtype) if z else None, dt_bias=f32(r["dt_bias"]) if bias else None)
-    out, states = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos,
-                                               delta_softplus=softplus)
+    y = None
+    if use_y:
+        out, states, y = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos,
+                                                      delta_softplus=softplus, y=True)
+    else:
+        out, states = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos,
+                                                   delta_softplus=softplus)
     res = dict(pos=pos, u=u, out=out, states=states)
+    if y is not None:
+        res["y"] = y
     if with_bwd:
         g = vs.varlen_selective_scan_bwd(**args, dout=dev(r["dout"], dtype), cu_seqlens=cu,
                                          chunk_states=states, position_indices=pos,
-                                         delta_softplus=softplus)
+                                         delta_softplus=softplus, y=y)
         dx, dw, db = vs.varlen_conv1d_bwd(x, f32(r["conv_w"]), f32(r["conv_b"]), g["du"], cu, pos)
         res.update(g)
         res.update(dx=dx, dweight=dw, dbias=db)
@@ -102,6 +111,9 @@ def check_chain(cu_np, r, res, dtype, with_bwd=True, z=True, skip=True, bias=Tru
              r["dt_bias"][idx] if bias else None]
     assert_close("out", col(host(res["out"])),
                  oracle.scan_fwd_threaded(*sargs, cu_np, delta_softplus=softplus), tol)
+    if "y" in res:  # the output before the gate: the oracle's output with no gate
+        assert_close("y", col(host(res["y"])),
+                     oracle.scan_fwd_threaded(*sargs[:6], None, sargs[7], cu_np, delta_softplus=softplus), tol)
     if not with_bwd:
         return
     g = oracle.scan_bwd_threaded(*sargs, col(r["dout"]), cu_np, delta_softplus=softplus)
@@ -391,7 +403,7 @@ def _sampled_checks(w, r, res, seq_pick):
 
 def test_workload_m14b_fwd_bwd_sampled_parity():
     w, r = _big_case("m14b")
-    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16")
+    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16", use_y=True)  # as the bench step runs
     lengths = np.diff(w["cu_seqlens"])
     picks = [int(np.argmax(lengths)), int(np.argmin(lengths)), len(lengths) // 2]
     _sampled_checks(w, r, res, picks)
@@ -399,7 +411,7 @@ def test_workload_m14b_fwd_bwd_sampled_parity():
 
 def test_workload_longtail_fwd_bwd_sampled_parity():
     w, r = _big_case("longtail")
-    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16")
+    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16", use_y=True)
     lengths = np.diff(w["cu_seqlens"])
     picks = [int(np.argmax(lengths)), int(np.argmin(lengths)), int(np.argmax(lengths < 9))]
     _sampled_checks(w, r, res, picks)
