@@ -62,12 +62,14 @@ def _load():
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                               ctypes.c_int32, ctypes.c_int32, _dp, _dp, _dp]
             lib.oracle_scan_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int32,
+                                            ctypes.c_double, _dp,
                                             _ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _dp, _dp]
             lib.oracle_scan_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int32,
+                                            ctypes.c_double, _dp, _dp,
                                             _dp, _ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                            _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+                                            _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
             for name in ("oracle_position_indices", "oracle_conv1d_fwd", "oracle_conv1d_bwd",
                          "oracle_scan_fwd", "oracle_scan_bwd"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -137,25 +139,32 @@ def conv1d_bwd(x, weight, bias, du, cu_seqlens, apply_silu=True, d_range=None):
 
 
 def scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens, delta_softplus=True,
-             d_range=None, return_last_state=False):
+             d_range=None, return_last_state=False, gate_floor=0.0, h_init=None):
+    """out (T, D); with return_last_state, also the state after each sequence's
+    last token (S, D, N).  h_init (S, D, N): each sequence's starting state
+    (zero when None); gate_floor: the GateFloor bias on the gate."""
     u, dr, A, B, C = _f64(u), _f64(delta_raw), _f64(A), _f64(B), _f64(C)
-    Dskip, z, dt_bias = _f64(Dskip), _f64(z), _f64(dt_bias)
+    Dskip, z, dt_bias, h_init = _f64(Dskip), _f64(z), _f64(dt_bias), _f64(h_init)
     cu, S, T = _cu(cu_seqlens)
     D, N = A.shape
     d0, d1 = d_range if d_range is not None else (0, D)
     out = np.zeros((T, D), dtype=np.float64)
     hl = np.zeros((S, D, N), dtype=np.float64) if return_last_state else None
     _check(_load().oracle_scan_fwd(_p(u), _p(dr), _p(A), _p(B), _p(C), _p(Dskip), _p(z),
-                                   _p(dt_bias), int(delta_softplus), _p(cu), S, T, D, N, d0, d1,
-                                   _p(out), _p(hl)), "scan_fwd")
+                                   _p(dt_bias), int(delta_softplus), float(gate_floor), _p(h_init),
+                                   _p(cu), S, T, D, N, d0, d1, _p(out), _p(hl)), "scan_fwd")
     return (out, hl) if return_last_state else out
 
 
 def scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens, delta_softplus=True,
-             d_range=None):
-    """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias (float64)."""
+             d_range=None, gate_floor=0.0, h_init=None, dh_last=None):
+    """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias and
+    dh_init (the gradient reaching each sequence's starting state, (S, D, N)),
+    float64.  dh_last (S, D, N): the gradient reaching each sequence's final
+    state from outside (zero when None)."""
     u, dr, A, B, C = _f64(u), _f64(delta_raw), _f64(A), _f64(B), _f64(C)
     Dskip, z, dt_bias, dout = _f64(Dskip), _f64(z), _f64(dt_bias), _f64(dout)
+    h_init, dh_last = _f64(h_init), _f64(dh_last)
     cu, S, T = _cu(cu_seqlens)
     D, N = A.shape
     d0, d1 = d_range if d_range is not None else (0, D)
@@ -165,12 +174,14 @@ def scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens, delta_s
         "dDskip": np.zeros(D) if Dskip is not None else None,
         "dz": np.zeros((T, D)) if z is not None else None,
         "d_dt_bias": np.zeros(D) if dt_bias is not None else None,
+        "dh_init": np.zeros((S, D, N)),
     }
     _check(_load().oracle_scan_bwd(_p(u), _p(dr), _p(A), _p(B), _p(C), _p(Dskip), _p(z),
-                                   _p(dt_bias), int(delta_softplus), _p(dout), _p(cu), S, T, D, N,
+                                   _p(dt_bias), int(delta_softplus), float(gate_floor), _p(h_init),
+                                   _p(dh_last), _p(dout), _p(cu), S, T, D, N,
                                    d0, d1, _p(g["du"]), _p(g["ddelta_raw"]), _p(g["dA"]),
                                    _p(g["dB"]), _p(g["dC"]), _p(g["dDskip"]), _p(g["dz"]),
-                                   _p(g["d_dt_bias"])), "scan_bwd")
+                                   _p(g["d_dt_bias"]), _p(g["dh_init"])), "scan_bwd")
     return g
 
 
@@ -188,15 +199,16 @@ def default_threads():
 
 
 def scan_fwd_threaded(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens, delta_softplus=True,
-                      channels=None, threads=None):
+                      channels=None, threads=None, gate_floor=0.0, h_init=None):
     """Forward scan over a channel range (default all) split across threads."""
     D = np.asarray(A).shape[0]
     d0, d1 = channels if channels is not None else (0, D)
     threads = threads or default_threads()
     args = [_f64(a) for a in (u, delta_raw, A, B, C, Dskip, z, dt_bias)]
+    h_init = _f64(h_init)
     outs = []
     with ThreadPoolExecutor(threads) as ex:
-        futs = [ex.submit(scan_fwd, *args, cu_seqlens, delta_softplus, blk)
+        futs = [ex.submit(scan_fwd, *args, cu_seqlens, delta_softplus, blk, False, gate_floor, h_init)
                 for blk in _blocks(d0, d1, threads * 2)]
         for blk, f in zip(_blocks(d0, d1, threads * 2), futs):
             outs.append((blk, f.result()))
@@ -208,16 +220,19 @@ def scan_fwd_threaded(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens, delt
 
 
 def scan_bwd_threaded(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,
-                      delta_softplus=True, channels=None, threads=None):
+                      delta_softplus=True, channels=None, threads=None, gate_floor=0.0, h_init=None,
+                      dh_last=None):
     """Backward scan over a channel range split across threads; dB/dC are the
     sum over that range, added block by block in channel order."""
     D = np.asarray(A).shape[0]
     d0, d1 = channels if channels is not None else (0, D)
     threads = threads or default_threads()
     args = [_f64(a) for a in (u, delta_raw, A, B, C, Dskip, z, dt_bias, dout)]
+    h_init, dh_last = _f64(h_init), _f64(dh_last)
     blocks = _blocks(d0, d1, threads * 2)
     with ThreadPoolExecutor(threads) as ex:
-        futs = [ex.submit(scan_bwd, *args, cu_seqlens, delta_softplus, blk) for blk in blocks]
+        futs = [ex.submit(scan_bwd, *args, cu_seqlens, delta_softplus, blk, gate_floor, h_init, dh_last)
+                for blk in blocks]
         parts = [f.result() for f in futs]
     res = {k: (None if v is None else np.zeros_like(v)) for k, v in parts[0].items()}
     for (b0, b1), g in zip(blocks, parts):
@@ -227,6 +242,7 @@ def scan_bwd_threaded(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens
         for k in ("dA", "dDskip", "d_dt_bias"):
             if g[k] is not None:
                 res[k][b0:b1] = g[k][b0:b1]
+        res["dh_init"][:, b0:b1] = g["dh_init"][:, b0:b1]
         res["dB"] += g["dB"]
         res["dC"] += g["dC"]
     return res

@@ -132,18 +132,24 @@ int oracle_conv1d_bwd(const double* x, const double* w, const double* bias, cons
     return ORACLE_OK;
 }
 
-/* Selective scan forward, one sequence at a time (state reset to zero at the
+/* Selective scan forward, one sequence at a time (state reset at the
  * sequence start, the article's "SSM_pack" requirement):
  *     r_t   = delta_raw[t,d] + dt_bias[d]
  *     dlt_t = delta_softplus ? softplus(r_t) : r_t
- *     h_t[n] = exp(dlt_t A[d,n]) h_{t-1}[n] + dlt_t B[t,n] u[t,d],  h_{start-1} = 0
+ *     h_t[n] = exp(dlt_t A[d,n]) h_{t-1}[n] + dlt_t B[t,n] u[t,d],
+ *              h_{start-1} = h_init[s] (or 0 when h_init is NULL)
  *     y_t   = sum_n C[t,n] h_t[n] + Dskip[d] u[t,d]
- *     out_t = z ? y_t SiLU(z[t,d]) : y_t
- * If h_last is non-NULL it receives the state after each sequence's last
- * token, laid out (num_seqs, D, N).                                          */
+ *     out_t = z ? y_t (SiLU(z[t,d]) + gate_floor) : y_t
+ * h_init (num_seqs, D, N) is the state a sequence starts from: the state a
+ * cut sequence's first part ended in, so that a long sequence can be split
+ * across packs and still pass its state on (the article's future work); the
+ * gate floor is the positive bias on the gate of the GateFloor variant.  If
+ * h_last is non-NULL it receives the state after each sequence's last token,
+ * laid out (num_seqs, D, N) (h_init for an empty sequence).                  */
 int oracle_scan_fwd(const double* u, const double* delta_raw, const double* A,
                     const double* B, const double* C, const double* Dskip, const double* z,
-                    const double* dt_bias, int32_t delta_softplus,
+                    const double* dt_bias, int32_t delta_softplus, double gate_floor,
+                    const double* h_init,
                     const int32_t* cu, int32_t num_seqs, int64_t T, int32_t D, int32_t N,
                     int32_t d_begin, int32_t d_end, double* out, double* h_last) {
     if (check_cu(cu, num_seqs, T) != ORACLE_OK) return ORACLE_ERR_CU;
@@ -152,7 +158,7 @@ int oracle_scan_fwd(const double* u, const double* delta_raw, const double* A,
     for (int32_t s = 0; s < num_seqs; ++s) {
         const int64_t start = cu[s], end = cu[s + 1];
         for (int32_t d = d_begin; d < d_end; ++d) {
-            for (int32_t n = 0; n < N; ++n) h[n] = 0.0;
+            for (int32_t n = 0; n < N; ++n) h[n] = h_init ? h_init[((int64_t)s * D + d) * N + n] : 0.0;
             for (int64_t t = start; t < end; ++t) {
                 const double r = delta_raw[t * D + d] + (dt_bias ? dt_bias[d] : 0.0);
                 const double dlt = delta_softplus ? softplus(r) : r;
@@ -164,7 +170,7 @@ int oracle_scan_fwd(const double* u, const double* delta_raw, const double* A,
                     y += C[t * N + n] * h[n];
                 }
                 y += (Dskip ? Dskip[d] : 0.0) * ut;
-                out[t * D + d] = z ? y * silu(z[t * D + d]) : y;
+                out[t * D + d] = z ? y * (silu(z[t * D + d]) + gate_floor) : y;
             }
             if (h_last)
                 for (int32_t n = 0; n < N; ++n) h_last[((int64_t)s * D + d) * N + n] = h[n];
@@ -176,20 +182,25 @@ int oracle_scan_fwd(const double* u, const double* delta_raw, const double* A,
 
 /* Hand-derived reverse-mode adjoint of oracle_scan_fwd, one sequence at a
  * time.  The forward states of the sequence are kept in full, then walked
- * backwards; the state gradient starts at zero after each sequence's last
- * token, which is the reverse scan that resets at sequence ends.
+ * backwards; the state gradient starts after each sequence's last token at
+ * dh_last[s] (the gradient that reaches the final state from outside, e.g.
+ * from the next part of a cut sequence; zero when dh_last is NULL), which is
+ * the reverse scan that resets at sequence ends.
  * Outputs are overwritten (gradients over the channel range):
  *   du, ddelta_raw, dz            (T, D) columns d_begin..d_end-1
  *   dA (D, N), dDskip, d_dt_bias  rows d_begin..d_end-1
  *   dB, dC (T, N)                 sum over the channel range only
+ *   dh_init (num_seqs, D, N)      the gradient reaching each sequence's
+ *                                 starting state (nullable)
  * dz, dDskip, d_dt_bias may be NULL when z, Dskip, dt_bias are NULL.      */
 int oracle_scan_bwd(const double* u, const double* delta_raw, const double* A,
                     const double* B, const double* C, const double* Dskip, const double* z,
-                    const double* dt_bias, int32_t delta_softplus, const double* dout,
+                    const double* dt_bias, int32_t delta_softplus, double gate_floor,
+                    const double* h_init, const double* dh_last, const double* dout,
                     const int32_t* cu, int32_t num_seqs, int64_t T, int32_t D, int32_t N,
                     int32_t d_begin, int32_t d_end,
                     double* du, double* ddelta_raw, double* dA, double* dB, double* dC,
-                    double* dDskip, double* dz, double* d_dt_bias) {
+                    double* dDskip, double* dz, double* d_dt_bias, double* dh_init) {
     if (check_cu(cu, num_seqs, T) != ORACLE_OK) return ORACLE_ERR_CU;
     int64_t max_len = 0;
     for (int32_t s = 0; s < num_seqs; ++s)
@@ -214,6 +225,7 @@ int oracle_scan_bwd(const double* u, const double* delta_raw, const double* A,
         for (int32_t d = d_begin; d < d_end; ++d) {
             const double Dd = Dskip ? Dskip[d] : 0.0;
             const double bias = dt_bias ? dt_bias[d] : 0.0;
+            const int64_t sd = ((int64_t)s * D + d) * N;  /* this (sequence, channel)'s state row */
             /* forward, keeping every state */
             for (int64_t t = start; t < end; ++t) {
                 const int64_t i = t - start;
@@ -222,7 +234,7 @@ int oracle_scan_bwd(const double* u, const double* delta_raw, const double* A,
                 const double ut = u[t * D + d];
                 double y = 0.0;
                 for (int32_t n = 0; n < N; ++n) {
-                    const double hprev = i > 0 ? H[(size_t)(i - 1) * nn + n] : 0.0;
+                    const double hprev = i > 0 ? H[(size_t)(i - 1) * nn + n] : (h_init ? h_init[sd + n] : 0.0);
                     const double a = exp(dlt * A[(int64_t)d * N + n]);
                     const double hn = a * hprev + dlt * B[t * N + n] * ut;
                     H[(size_t)i * nn + n] = hn;
@@ -231,7 +243,7 @@ int oracle_scan_bwd(const double* u, const double* delta_raw, const double* A,
                 Y[i] = y + Dd * ut;
             }
             /* backward */
-            for (int32_t n = 0; n < N; ++n) dh[n] = 0.0;
+            for (int32_t n = 0; n < N; ++n) dh[n] = dh_last ? dh_last[sd + n] : 0.0;
             for (int64_t t = end - 1; t >= start; --t) {
                 const int64_t i = t - start;
                 const double r = delta_raw[t * D + d] + bias;
@@ -241,14 +253,14 @@ int oracle_scan_bwd(const double* u, const double* delta_raw, const double* A,
                 double g = go;                      /* dL/dy_t */
                 if (z) {
                     const double zt = z[t * D + d];
-                    g = go * silu(zt);
+                    g = go * (silu(zt) + gate_floor);
                     dz[t * D + d] = go * Y[i] * silu_grad(zt);
                 }
                 double ddlt = 0.0, dut = 0.0;
                 for (int32_t n = 0; n < N; ++n) {
                     const double An = A[(int64_t)d * N + n];
                     const double a = exp(dlt * An);
-                    const double hprev = i > 0 ? H[(size_t)(i - 1) * nn + n] : 0.0;
+                    const double hprev = i > 0 ? H[(size_t)(i - 1) * nn + n] : (h_init ? h_init[sd + n] : 0.0);
                     dh[n] += C[t * N + n] * g;                 /* total dL/dh_t[n] */
                     dC[t * N + n] += g * H[(size_t)i * nn + n];
                     dB[t * N + n] += dh[n] * dlt * ut;
@@ -264,6 +276,9 @@ int oracle_scan_bwd(const double* u, const double* delta_raw, const double* A,
                 ddelta_raw[t * D + d] = dr;
                 if (d_dt_bias) d_dt_bias[d] += dr;
             }
+            /* dh now holds the gradient reaching the state before the first token */
+            if (dh_init)
+                for (int32_t n = 0; n < N; ++n) dh_init[sd + n] = dh[n];
         }
     }
     free(H); free(Y); free(dh);

@@ -380,6 +380,101 @@ def test_scan_bwd_pack_grads_are_sums_of_sequence_grads():
         np.testing.assert_allclose(gp[k], acc[k], rtol=1e-13, atol=1e-13)
 
 
+# ---------------------------------------------------------------- gate floor, sequence states, A_log
+
+def test_scan_gate_floor_adds_floor_times_the_ungated_output():
+    # out = y (SiLU(z) + delta) = y SiLU(z) + delta y: linear in the floor
+    rng = _rng(40)
+    v = _rand_pack(rng, [4, 2, 3, 7], D=6, N=3)
+    base = _scan(v)
+    ungated = oracle.scan_fwd(v["u"], v["dr"], v["A"], v["B"], v["C"], v["Dskip"], None, v["dt_bias"], v["cu"])
+    np.testing.assert_allclose(_scan(v, gate_floor=0.05), base + 0.05 * ungated, rtol=1e-12, atol=1e-12)
+
+
+def test_scan_bwd_gate_floor_equals_the_ungated_run_on_gated_dout():
+    # with the gate fixed, the scan sees dy = dout (SiLU(z) + delta); dz does not depend on delta
+    rng = _rng(41)
+    v = _rand_pack(rng, [4, 2, 3, 7], D=5, N=3)
+    g = _scan_bwd(v, gate_floor=0.07)
+    g0 = _scan_bwd(v)
+    ref = oracle.scan_bwd(v["u"], v["dr"], v["A"], v["B"], v["C"], v["Dskip"], None, v["dt_bias"],
+                          v["dout"] * (_silu(v["z"]) + 0.07), v["cu"])
+    for k in ("du", "ddelta_raw", "dA", "dB", "dC", "dDskip", "d_dt_bias"):
+        np.testing.assert_allclose(g[k], ref[k], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(g["dz"], g0["dz"])
+
+
+def test_scan_bwd_finite_differences_with_gate_floor_initial_and_final_states():
+    # loss = sum(out * dout) + sum(h_last * dh_last), so that both states enter it
+    rng = _rng(42)
+    v = _rand_pack(rng, [4, 2, 3, 7], D=3, N=2)
+    S = 4
+    h0 = rng.standard_normal((S, 3, 2))
+    dhl = rng.standard_normal((S, 3, 2))
+    g = _scan_bwd(v, gate_floor=0.03, h_init=h0, dh_last=dhl)
+
+    def f():
+        out, hl = _scan(v, gate_floor=0.03, h_init=h0, return_last_state=True)
+        return float(np.sum(out * v["dout"]) + np.sum(hl * dhl))
+
+    _fd_check(f, {"u": v["u"], "dr": v["dr"], "A": v["A"], "B": v["B"], "C": v["C"],
+                  "Dskip": v["Dskip"], "z": v["z"], "dt_bias": v["dt_bias"], "h0": h0},
+              {"u": g["du"], "dr": g["ddelta_raw"], "A": g["dA"], "B": g["dB"], "C": g["dC"],
+               "Dskip": g["dDskip"], "z": g["dz"], "dt_bias": g["d_dt_bias"], "h0": g["dh_init"]})
+
+
+def test_a_cut_sequence_that_passes_its_state_equals_the_whole_sequence():
+    # the article's future work: a long sequence cut into two parts that pass
+    # the state on gives the whole sequence's outputs and gradients
+    rng = _rng(43)
+    L, L1 = 37, 16
+    v = _rand_pack(rng, [L], D=4, N=3)
+    whole = _scan(v)
+    gw = _scan_bwd(v)
+    one = lambda n: np.array([0, n], np.int32)  # noqa: E731
+    p1 = {k: (v[k][:L1] if isinstance(v[k], np.ndarray) and v[k].shape[:1] == (L,) else v[k]) for k in v}
+    p2 = {k: (v[k][L1:] if isinstance(v[k], np.ndarray) and v[k].shape[:1] == (L,) else v[k]) for k in v}
+    p1["cu"], p2["cu"] = one(L1), one(L - L1)
+    out1, h1 = _scan(p1, return_last_state=True)
+    out2 = _scan(p2, h_init=h1)
+    np.testing.assert_allclose(np.concatenate([out1, out2]), whole, rtol=1e-12, atol=1e-12)
+    g2 = _scan_bwd(p2, h_init=h1)
+    g1 = _scan_bwd(p1, dh_last=g2["dh_init"])
+    for k in ("du", "ddelta_raw", "dz"):
+        np.testing.assert_allclose(np.concatenate([g1[k], g2[k]]), gw[k], rtol=1e-11, atol=1e-11)
+    for k in ("dB", "dC"):
+        np.testing.assert_allclose(np.concatenate([g1[k], g2[k]]), gw[k], rtol=1e-11, atol=1e-11)
+    for k in ("dA", "dDskip", "d_dt_bias"):
+        np.testing.assert_allclose(g1[k] + g2[k], gw[k], rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(g1["dh_init"], gw["dh_init"], rtol=1e-11, atol=1e-11)
+
+
+def test_an_empty_sequence_passes_its_state_and_gradient_through():
+    rng = _rng(44)
+    v = _rand_pack(rng, [3, 0, 4], D=2, N=2)
+    h0 = rng.standard_normal((3, 2, 2))
+    dhl = rng.standard_normal((3, 2, 2))
+    _, hl = _scan(v, h_init=h0, return_last_state=True)
+    np.testing.assert_array_equal(hl[1], h0[1])
+    g = _scan_bwd(v, h_init=h0, dh_last=dhl)
+    np.testing.assert_array_equal(g["dh_init"][1], dhl[1])
+
+
+def test_a_log_gradient_is_dA_times_A():
+    # A = -exp(A_log): finite differences in A_log against the chain rule dA * A
+    rng = _rng(45)
+    v = _rand_pack(rng, [4, 2, 3, 7], D=3, N=2)
+    a_log = rng.uniform(-1.0, 1.0, size=(3, 2))
+    v["A"] = -np.exp(a_log)
+    g = _scan_bwd(v)
+
+    def f():
+        w = dict(v, A=-np.exp(a_log))
+        return float(np.sum(_scan(w) * v["dout"]))
+
+    _fd_check(f, {"a_log": a_log}, {"a_log": g["dA"] * v["A"]})
+
+
 # ---------------------------------------------------------------- threaded helpers
 
 def test_threaded_helpers_match_single_call():
