@@ -148,13 +148,19 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
  * y: nullable (T, D) io; when given it receives the output before the gate,
  * y above (equal to out when z is NULL), which the backward call can take
  * instead of recomputing it for dz.  16-byte aligned like out.
+ * Two variants from the article's pages, both off at 0:
+ *   gate_floor: the GateFloor gate, out = y * (SiLU(z) + gate_floor) (a
+ *     positive bias that keeps the gate above zero; no effect without z);
+ *   a_log: nonzero when A holds A_log, the stored parameterisation with
+ *     A = -exp(A_log); the backward then returns dA_log = dA * A in dA.
  */
 size_t varlen_selective_scan_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
 size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, int32_t N);
 int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float* A,
                               const void* B, const void* C, const float* Dskip, const void* z,
-                              const float* dt_bias, int32_t delta_softplus,
-                              const int32_t* cu_seqlens, const int32_t* position_indices,
+                              const float* dt_bias, int32_t delta_softplus, float gate_floor,
+                              int32_t a_log, const int32_t* cu_seqlens,
+                              const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, void* out, void* y, float* chunk_states,
                               void* workspace, size_t workspace_bytes, void* stream);
@@ -176,7 +182,8 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
 size_t varlen_selective_scan_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
 int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
                               const void* B, const void* C, const float* Dskip, const void* z,
-                              const float* dt_bias, int32_t delta_softplus, const void* dout,
+                              const float* dt_bias, int32_t delta_softplus, float gate_floor,
+                              int32_t a_log, const void* dout,
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, const float* chunk_states, const void* y,
@@ -217,6 +224,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
 int varlen_selective_scan_fwd_noalloc(const void* u, const void* delta_raw, const float* A,
                                       const void* B, const void* C, const float* Dskip,
                                       const void* z, const float* dt_bias, int32_t delta_softplus,
+                                      float gate_floor, int32_t a_log,
                                       const int32_t* cu_seqlens, const int32_t* position_indices,
                                       int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                                       vssm_dtype dtype, void* out, void* y, float* chunk_states,

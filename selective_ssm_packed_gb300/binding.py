@@ -40,14 +40,17 @@ SIGNATURES = {
     "varlen_selective_scan_fwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_chunk_states_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                                 ctypes.c_float, _i32,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
                                                  _vp, _vp, _vp, _vp, _sz, _vp]),
     "varlen_selective_scan_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
-    "varlen_selective_scan_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+    "varlen_selective_scan_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                                 ctypes.c_float, _i32, _vp,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int, _vp,
                                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                                  _sz, _vp]),
     "varlen_selective_scan_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                                         ctypes.c_float, _i32,
                                                          _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
                                                          _vp, _vp, _vp, _vp, _vp]),
     "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
@@ -217,12 +220,14 @@ def chunk_states_shape(T, D, N):
 
 def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens,
                               position_indices=None, delta_softplus=True, out=None,
-                              chunk_states=True, workspace=None, stream=None, y=None):
+                              chunk_states=True, workspace=None, stream=None, y=None, gate_floor=0.0,
+                              a_log=False):
     """Returns (out, chunk_states), or (out, chunk_states, y) when y is asked
     for.  chunk_states=True allocates the saved-state array the backward call
     needs, False/None skips it, a tensor is filled.  y (the output before the
     gate, which the backward call can take for dz): None/False skips it, True
-    allocates it, a tensor is filled."""
+    allocates it, a tensor is filled.  gate_floor: the GateFloor gate
+    SiLU(z) + gate_floor; a_log: A holds A_log (A = -exp(A_log))."""
     T, D = u.shape
     N = A.shape[1]
     out = torch.empty_like(u) if out is None else out
@@ -240,7 +245,8 @@ def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqle
     _check(lib().varlen_selective_scan_fwd(
         _ptr(u, "u"), _ptr(delta_raw, "delta_raw", dt), _ptr(A, "A", torch.float32),
         _ptr(B, "B", dt), _ptr(C, "C", dt), _ptr(Dskip, "Dskip", torch.float32), _ptr(z, "z", dt),
-        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)),
+        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)), float(gate_floor),
+        int(bool(a_log)),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
         cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(out, "out", dt), _ptr(y, "y", dt),
         _ptr(chunk_states, "chunk_states", torch.float32), _ptr(ws, "workspace"), ws.numel(),
@@ -250,10 +256,12 @@ def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqle
 
 def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,
                               chunk_states, position_indices=None, delta_softplus=True,
-                              grads=None, workspace=None, stream=None, y=None):
+                              grads=None, workspace=None, stream=None, y=None, gate_floor=0.0,
+                              a_log=False):
     """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias.  y: the
     forward call's pre-gate output (optional; dz then reads it instead of
-    recomputing it)."""
+    recomputing it).  gate_floor, a_log: as in the forward call; with a_log
+    the dA entry holds dA_log = dA * A."""
     T, D = u.shape
     N = A.shape[1]
     dt = u.dtype
@@ -270,7 +278,8 @@ def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu
     _check(lib().varlen_selective_scan_bwd(
         _ptr(u, "u"), _ptr(delta_raw, "delta_raw", dt), _ptr(A, "A", torch.float32),
         _ptr(B, "B", dt), _ptr(C, "C", dt), _ptr(Dskip, "Dskip", torch.float32), _ptr(z, "z", dt),
-        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)), _ptr(dout, "dout", dt),
+        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)), float(gate_floor),
+        int(bool(a_log)), _ptr(dout, "dout", dt),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
         cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(chunk_states, "chunk_states", torch.float32),
         _ptr(y, "y", dt), _ptr(g["du"], "du", dt), _ptr(g["ddelta_raw"], "ddelta_raw", dt),

@@ -375,8 +375,9 @@ static int scan_common(const void* u, const void* delta_raw, const float* A, con
 
 int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float* A,
                               const void* B, const void* C, const float* Dskip, const void* z,
-                              const float* dt_bias, int32_t delta_softplus,
-                              const int32_t* cu_seqlens, const int32_t* position_indices,
+                              const float* dt_bias, int32_t delta_softplus, float gate_floor,
+                              int32_t a_log, const int32_t* cu_seqlens,
+                              const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, void* out, void* y, float* chunk_states,
                               void* workspace, size_t workspace_bytes, void* stream) {
@@ -410,6 +411,8 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   a.n_tiles = (int)cdiv(D, kTile);
   a.n_chunks = (int)cdiv(T, kFwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
+  a.gate_floor = gate_floor;
+  a.a_log = a_log ? 1 : 0;
   a.has_z = z ? 1 : 0;
   a.has_skip = Dskip ? 1 : 0;
   a.box_x = D < kTile ? D : kTile;
@@ -426,7 +429,8 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
 
 int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
                               const void* B, const void* C, const float* Dskip, const void* z,
-                              const float* dt_bias, int32_t delta_softplus, const void* dout,
+                              const float* dt_bias, int32_t delta_softplus, float gate_floor,
+                              int32_t a_log, const void* dout,
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, const float* chunk_states, const void* y,
@@ -476,6 +480,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.n_tiles = (int)cdiv(D, kTile);
   a.n_chunks = (int)cdiv(T, kBwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
+  a.gate_floor = gate_floor;
+  a.a_log = a_log ? 1 : 0;
   a.has_z = z ? 1 : 0;
   a.has_y = (z && y) ? 1 : 0;
   a.has_skip = Dskip ? 1 : 0;

@@ -88,6 +88,8 @@ struct ScanArgs {
   int n_tiles;
   int n_chunks;
   int delta_softplus;
+  float gate_floor;           // GateFloor: the gate is SiLU(z) + gate_floor
+  int a_log;                  // A holds A_log (A = -exp(A_log)); bwd returns dA_log = dA * A
   int has_z;
   int has_y;                  // bwd: dz from the given y instead of recomputed C.h + Dskip u
   int has_skip;

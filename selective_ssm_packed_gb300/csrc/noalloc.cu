@@ -117,7 +117,8 @@ using namespace vssm;
 
 extern "C" int varlen_selective_scan_fwd_noalloc(
     const void* u, const void* delta_raw, const float* A, const void* B, const void* C,
-    const float* Dskip, const void* z, const float* dt_bias, int32_t delta_softplus,
+    const float* Dskip, const void* z, const float* dt_bias, int32_t delta_softplus, float gate_floor,
+    int32_t a_log,
     const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
     int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* out, void* y, float* chunk_states,
     int32_t* status, void* stream) {
@@ -192,6 +193,8 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   a.n_tiles = (int)n_tiles;
   a.n_chunks = (int)n_chunks;
   a.delta_softplus = delta_softplus ? 1 : 0;
+  a.gate_floor = gate_floor;
+  a.a_log = a_log ? 1 : 0;
   a.has_z = z ? 1 : 0;
   a.has_skip = Dskip ? 1 : 0;
   a.box_x = D < kTile ? D : kTile;

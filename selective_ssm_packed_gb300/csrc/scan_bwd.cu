@@ -13,7 +13,7 @@
 // (chunk_states, written by the forward call) and walks its 32 tokens.
 //
 // With a_t = exp(delta_t A) (0 at a sequence start), b_t = delta_t u_t B_t,
-// g_t = dout_t SiLU(z_t):
+// g_t = dout_t (SiLU(z_t) + gate floor):
 //   h_t  = a_t h_{t-1} + b_t                       (forward walk)
 //   dh_t = C_t g_t + a_{t+1} dh_{t+1}              (reverse walk; a_{t+1} = 0
 //                                                   at a sequence start, so the
@@ -267,7 +267,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     if (a.has_z) {
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) gv[q] = gov[q] * siluf(gv[q]);
+      for (int q = 0; q < kPer; ++q) gv[q] = gov[q] * (siluf(gv[q]) + a.gate_floor);
     } else {
 #pragma unroll
       for (int q = 0; q < kPer; ++q) gv[q] = gov[q];
@@ -306,7 +306,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const float* const cp = sm.CP + ((((lane >> 4) & 1) * W + w) * kPP) * 2;
   float2 A2 = make_float2(0.0f, 0.0f), h = make_float2(0.0f, 0.0f);
   if (valid) {
-    A2 = make_float2(sm.Araw[lane * N + nF] * kLog2e, sm.Araw[lane * N + nS] * kLog2e);
+    A2 = make_float2(sm.Araw[lane * N + nF], sm.Araw[lane * N + nS]);
+    // the rows hold A or A_log (A = -exp(A_log)); kept scaled by log2 e for ex2
+    if (a.a_log) A2 = make_float2(-ex2(A2.x * kLog2e), -ex2(A2.y * kLog2e));
+    A2 = make_float2(A2.x * kLog2e, A2.y * kLog2e);
     h = make_float2(sm.H[nF * bx + lane], sm.H[nS * bx + lane]);
   }
   const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
@@ -508,8 +511,11 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // ---- 6. dA partials of the chunk ([chunk][n][d]); fixed-order CTA sums of
   //         the dDskip and d_dt_bias partials
   if (valid) {
-    a.part_dA[((int64_t)chunk * N + nF) * a.D + d] = dA.x;
-    a.part_dA[((int64_t)chunk * N + nS) * a.D + d] = dA.y;
+    // for A_log the chain rule gives dA_log = dA * A (A = A2 ln 2), applied to
+    // every chunk's partial before the fixed-order sum
+    const float2 s = a.a_log ? make_float2(A2.x * kLn2, A2.y * kLn2) : make_float2(1.0f, 1.0f);
+    a.part_dA[((int64_t)chunk * N + nF) * a.D + d] = dA.x * s.x;
+    a.part_dA[((int64_t)chunk * N + nS) * a.D + d] = dA.y * s.y;
   }
   sm.redD[w * kTile + lane] = sDD;
   sm.redB[w * kTile + lane] = sDB;

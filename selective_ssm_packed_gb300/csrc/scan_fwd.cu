@@ -155,7 +155,13 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   __syncwarp();
   float2 A2[P];
   if (valid) {
-    load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, kLog2e);
+    load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, a.a_log ? 1.0f : kLog2e);
+    if (a.a_log) {
+      // the rows hold A_log: A = -exp(A_log), kept scaled by log2 e for ex2
+#pragma unroll
+      for (int i = 0; i < P; ++i)
+        A2[i] = make_float2(-ex2(A2[i].x * kLog2e) * kLog2e, -ex2(A2[i].y * kLog2e) * kLog2e);
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
@@ -421,7 +427,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         if (valid) *yp = from_f<T>(y);
         yp += a.D;
       }
-      if (a.has_z) y *= siluf(to_f(zp[k * kTile]));
+      if (a.has_z) y *= siluf(to_f(zp[k * kTile])) + a.gate_floor;
       if (valid) *op = from_f<T>(y);
       op += a.D;
     }
@@ -448,7 +454,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     float y = fmaf(Dsk, uu, y2.x + y2.y);
     if (ypre && valid) ypre[(t0 + t) * a.D + d] = from_f<T>(y);
-    if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane]));
+    if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane])) + a.gate_floor;
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
   }
   }

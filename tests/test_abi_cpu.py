@@ -81,17 +81,17 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _conv_fwd(lib, ws=None) == -4
     assert _conv_fwd(lib, T=-1) == -1
     scan = lib.varlen_selective_scan_fwd
-    args = [16, 16, 16, 16, 16, None, None, None, 1, 16, None, 1, 16, 8, 3, 0, 16, None, None, 16, 1 << 30,
-            None]
+    args = [16, 16, 16, 16, 16, None, None, None, 1, 0.0, 0, 16, None, 1, 16, 8, 3, 0, 16, None, None, 16,
+            1 << 30, None]
     assert scan(*args) == -6                     # N = 3
-    args[14] = 4
-    args[15] = 1
+    args[16] = 4
+    args[17] = 1
     assert scan(*args) == -3                     # N * 2 bytes = 8
-    args[15] = 0
-    args[17] = 8
+    args[17] = 0
+    args[19] = 8
     assert scan(*args) == -3                     # misaligned y
-    args[17] = None
     args[19] = None
+    args[21] = None
     assert scan(*args) == -4
 
 

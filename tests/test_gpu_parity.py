@@ -230,6 +230,35 @@ def test_backward_reads_the_forward_pre_gate_output(lengths, D, N, dtype):
         assert torch.equal(g_y[k], g_re[k]), k
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gate_floor_and_a_log_variants(dtype):
+    """GateFloor (out = y (SiLU(z) + delta)) and the A_log parameterisation
+    (A = -exp(A_log); the backward returns dA_log = dA * A) against the oracle."""
+    cu_np, T, r = rand_case([300, 1, 2, 257, 0, 40], 72, 8, dtype, seed=29)
+    a_log = np.random.default_rng(30).uniform(-1.0, 1.5, size=r["A"].shape).astype(np.float32)
+    A_ref = -np.exp(a_log.astype(np.float64))
+    floor = 0.05
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    u = dev(r["x"], dtype)
+    args = dict(u=u, delta_raw=dev(r["delta_raw"], dtype), A=f32(a_log), B=dev(r["B"], dtype),
+                C=dev(r["C"], dtype), Dskip=f32(r["Dskip"]), z=dev(r["z"], dtype), dt_bias=f32(r["dt_bias"]))
+    out, states, y = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos, y=True,
+                                                  gate_floor=floor, a_log=True)
+    dout = dev(r["dout"], dtype)
+    g = vs.varlen_selective_scan_bwd(**args, dout=dout, cu_seqlens=cu, chunk_states=states,
+                                     position_indices=pos, y=y, gate_floor=floor, a_log=True)
+    torch.cuda.synchronize()
+    sargs = [host(u), r["delta_raw"], A_ref, r["B"], r["C"], r["Dskip"], r["z"], r["dt_bias"]]
+    tol = TOL[dtype]
+    assert_close("out", out, oracle.scan_fwd_threaded(*sargs, cu_np, gate_floor=floor), tol)
+    assert_close("y", y, oracle.scan_fwd_threaded(*sargs[:6], None, sargs[7], cu_np), tol)
+    ref = oracle.scan_bwd_threaded(*sargs, host(dout), cu_np, gate_floor=floor)
+    ref["dA"] = ref["dA"] * A_ref  # dA_log by the chain rule
+    for k in ("du", "ddelta_raw", "dz", "dA", "dB", "dC", "dDskip", "d_dt_bias"):
+        assert_close(k, g[k], ref[k], tol)
+
+
 @pytest.mark.parametrize("flags", [dict(z=False), dict(skip=False), dict(bias=False),
                                    dict(softplus=False), dict(z=False, skip=False, bias=False)])
 def test_optional_inputs(flags):
