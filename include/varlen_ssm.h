@@ -153,6 +153,13 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
  *     positive bias that keeps the gate above zero; no effect without z);
  *   a_log: nonzero when A holds A_log, the stored parameterisation with
  *     A = -exp(A_log); the backward then returns dA_log = dA * A in dA.
+ * Sequence states (the article's future work: a long sequence cut at the end
+ * of a pack into two parts that still pass data between them), both
+ * nullable f32 (num_seqs, D, N), entry [s][d][n] for state n of channel d:
+ *   initial_states: the state each sequence starts from (h before its first
+ *     token; zero when NULL), e.g. the previous part's final state;
+ *   final_states: receives the state after each sequence's last token (the
+ *     initial state for an empty sequence).
  */
 size_t varlen_selective_scan_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t N);
 size_t varlen_selective_scan_chunk_states_size(int64_t total_tokens, int32_t D, int32_t N);
@@ -163,6 +170,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
                               const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, void* out, void* y, float* chunk_states,
+                              const float* initial_states, float* final_states,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward: the reverse scan of the state gradient, which resets at every
@@ -175,7 +183,13 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
  * forward call's pre-gate output (its `y` argument); with z given, dz then
  * uses it (dz = dout * y * SiLU'(z)) instead of recomputing C.h + Dskip u,
  * which saves the backward that work; with y NULL it is recomputed (in fp32,
- * so for bf16 io the two ways differ by y's rounding to bf16).  Every
+ * so for bf16 io the two ways differ by y's rounding to bf16).
+ * initial_states: the forward call's (nullable; the states are recomputed
+ * from it at every sequence start).  d_final_states: nullable (num_seqs, D,
+ * N), the gradient reaching each sequence's final state from outside (from
+ * the next part of a cut sequence).  d_initial_states: nullable (num_seqs, D,
+ * N), receives the gradient reaching each sequence's starting state (for an
+ * empty sequence, its d_final_states entry).  Every
  * reduction (over channels for dB/dC, over tokens for dA/dDskip/d_dt_bias) is
  * atomic-free and runs in a fixed order, so results are bitwise repeatable.
  */
@@ -187,6 +201,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, const float* chunk_states, const void* y,
+                              const float* initial_states, const float* d_final_states,
+                              float* d_initial_states,
                               void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream);
@@ -207,7 +223,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
  *   - The first call made with a given device current looks up the array's
  *     device address (cudaGetSymbolAddress) and caches it; make that first call
  *     before any stream capture on that device.
- *   - A problem whose scratch would not fit (about T*D*(N+1)/16 + 4*T
+ *   - A problem whose scratch would not fit (about T*D*(N+1)/16 + 8*T
  *     bytes: T = 8192 tokens at D = 4096, N = 16 needs 36 MB and fits;
  *     T = 16384 needs 69 MB and does not) is rejected with
  *     VSSM_ERR_WORKSPACE and a message naming both sizes, before anything is
@@ -228,6 +244,7 @@ int varlen_selective_scan_fwd_noalloc(const void* u, const void* delta_raw, cons
                                       const int32_t* cu_seqlens, const int32_t* position_indices,
                                       int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                                       vssm_dtype dtype, void* out, void* y, float* chunk_states,
+                                      const float* initial_states, float* final_states,
                                       int32_t* status, void* stream);
 
 /* ------------------------------------------------------------ status, errors, knobs

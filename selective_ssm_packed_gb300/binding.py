@@ -42,17 +42,17 @@ SIGNATURES = {
     "varlen_selective_scan_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                  ctypes.c_float, _i32,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
-                                                 _vp, _vp, _vp, _vp, _sz, _vp]),
+                                                 _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "varlen_selective_scan_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                  ctypes.c_float, _i32, _vp,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int, _vp,
-                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                                 _sz, _vp]),
+                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                 _vp, _vp, _sz, _vp]),
     "varlen_selective_scan_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                          ctypes.c_float, _i32,
                                                          _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
-                                                         _vp, _vp, _vp, _vp, _vp]),
+                                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "vssm_last_error": (ctypes.c_char_p, []),
@@ -221,13 +221,16 @@ def chunk_states_shape(T, D, N):
 def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens,
                               position_indices=None, delta_softplus=True, out=None,
                               chunk_states=True, workspace=None, stream=None, y=None, gate_floor=0.0,
-                              a_log=False):
+                              a_log=False, initial_states=None, final_states=None):
     """Returns (out, chunk_states), or (out, chunk_states, y) when y is asked
     for.  chunk_states=True allocates the saved-state array the backward call
     needs, False/None skips it, a tensor is filled.  y (the output before the
     gate, which the backward call can take for dz): None/False skips it, True
     allocates it, a tensor is filled.  gate_floor: the GateFloor gate
-    SiLU(z) + gate_floor; a_log: A holds A_log (A = -exp(A_log))."""
+    SiLU(z) + gate_floor; a_log: A holds A_log (A = -exp(A_log)).
+    initial_states: (S, D, N) f32 state each sequence starts from (None: zero).
+    final_states: None skips them, True allocates, a tensor is filled; when
+    asked for they come last in the returned tuple."""
     T, D = u.shape
     N = A.shape[1]
     out = torch.empty_like(u) if out is None else out
@@ -236,6 +239,12 @@ def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqle
         y = torch.empty_like(u)
     elif y is False:
         y = None
+    S = cu_seqlens.numel() - 1
+    want_final = final_states is not None and final_states is not False
+    if final_states is True:
+        final_states = torch.empty((S, D, N), dtype=torch.float32, device=u.device)
+    elif final_states is False:
+        final_states = None
     if chunk_states is True:
         chunk_states = torch.empty(chunk_states_shape(T, D, N), dtype=torch.float32, device=u.device)
     elif chunk_states is False:
@@ -249,19 +258,25 @@ def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqle
         int(bool(a_log)),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
         cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(out, "out", dt), _ptr(y, "y", dt),
-        _ptr(chunk_states, "chunk_states", torch.float32), _ptr(ws, "workspace"), ws.numel(),
-        _stream(stream)), "varlen_selective_scan_fwd")
-    return (out, chunk_states, y) if want_y else (out, chunk_states)
+        _ptr(chunk_states, "chunk_states", torch.float32),
+        _ptr(initial_states, "initial_states", torch.float32), _ptr(final_states, "final_states", torch.float32),
+        _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_selective_scan_fwd")
+    res = (out, chunk_states) + ((y,) if want_y else ()) + ((final_states,) if want_final else ())
+    return res
 
 
 def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,
                               chunk_states, position_indices=None, delta_softplus=True,
                               grads=None, workspace=None, stream=None, y=None, gate_floor=0.0,
-                              a_log=False):
+                              a_log=False, initial_states=None, d_final_states=None,
+                              d_initial_states=None):
     """Returns dict du, ddelta_raw, dA, dB, dC, dDskip, dz, d_dt_bias.  y: the
     forward call's pre-gate output (optional; dz then reads it instead of
     recomputing it).  gate_floor, a_log: as in the forward call; with a_log
-    the dA entry holds dA_log = dA * A."""
+    the dA entry holds dA_log = dA * A.  initial_states: the forward call's;
+    d_final_states: (S, D, N) gradient reaching each sequence's final state;
+    d_initial_states: True allocates (or a tensor to fill) the gradient
+    reaching each sequence's starting state, returned as "d_initial_states"."""
     T, D = u.shape
     N = A.shape[1]
     dt = u.dtype
@@ -274,6 +289,11 @@ def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu
     g.setdefault("dDskip", torch.empty_like(Dskip) if Dskip is not None else None)
     g.setdefault("dz", torch.empty_like(z) if z is not None else None)
     g.setdefault("d_dt_bias", torch.empty_like(dt_bias) if dt_bias is not None else None)
+    if d_initial_states is True:
+        d_initial_states = torch.empty((cu_seqlens.numel() - 1, D, N), dtype=torch.float32, device=u.device)
+    elif d_initial_states is False:
+        d_initial_states = None
+    g["d_initial_states"] = d_initial_states
     ws = _ws(workspace, scan_bwd_workspace_size(T, D, N), u.device)
     _check(lib().varlen_selective_scan_bwd(
         _ptr(u, "u"), _ptr(delta_raw, "delta_raw", dt), _ptr(A, "A", torch.float32),
@@ -282,7 +302,9 @@ def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu
         int(bool(a_log)), _ptr(dout, "dout", dt),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
         cu_seqlens.numel() - 1, T, D, N, _dt(u), _ptr(chunk_states, "chunk_states", torch.float32),
-        _ptr(y, "y", dt), _ptr(g["du"], "du", dt), _ptr(g["ddelta_raw"], "ddelta_raw", dt),
+        _ptr(y, "y", dt), _ptr(initial_states, "initial_states", torch.float32),
+        _ptr(d_final_states, "d_final_states", torch.float32),
+        _ptr(d_initial_states, "d_initial_states", torch.float32), _ptr(g["du"], "du", dt), _ptr(g["ddelta_raw"], "ddelta_raw", dt),
         _ptr(g["dA"], "dA", torch.float32), _ptr(g["dB"], "dB", torch.float32),
         _ptr(g["dC"], "dC", torch.float32), _ptr(g["dDskip"], "dDskip", torch.float32),
         _ptr(g["dz"], "dz", dt), _ptr(g["d_dt_bias"], "d_dt_bias", torch.float32),

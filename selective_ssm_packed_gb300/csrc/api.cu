@@ -45,7 +45,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // [header 256 B: status int @0, ticket uint @4][flags, one per (slot, lane)][pos][...call specific]
 // header + flags are cleared by one memset at the start of every call.
 struct Layout {
-  size_t flags = 0, pos = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t flags = 0, pos = 0, seq = 0, agg = 0, agg_sd = 0, incl = 0;
   size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, conv_part = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
@@ -60,6 +60,8 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   off += up(sizeof(int) * (size_t)slots * kTile);
   l.clear_bytes = off;
   l.pos = off;
+  off += up(sizeof(int32_t) * (size_t)T);
+  l.seq = off;
   off += up(sizeof(int32_t) * (size_t)T);
   l.agg = off;
   off += up(sizeof(float) * (size_t)slots * N * kTile);
@@ -172,6 +174,12 @@ int resolve_pos(const int32_t* cu, const int32_t* pos_in, int32_t S, int64_t T, 
   cudaError_t e = launch_position_indices(cu, S, T, p, at<int32_t>(ws, 0), st);
   if (e != cudaSuccess) return cuda_fail(e, "position_indices launch");
   *pos_out = p;
+  return VSSM_OK;
+}
+
+// A (num_seqs, D, N) f32 sequence-state array: nullable, 16-byte aligned.
+int check_states(const float* p, const char* name) {
+  if (p && !aligned16(p)) return fail(VSSM_ERR_ALIGN, "%s is not 16-byte aligned", name);
   return VSSM_OK;
 }
 
@@ -380,6 +388,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
                               const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, void* out, void* y, float* chunk_states,
+                              const float* initial_states, float* final_states,
                               void* workspace, size_t workspace_bytes, void* stream) {
   IO io;
   VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
@@ -388,19 +397,31 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   if (y) VSSM_TRY(check_io(y, "y", total_tokens));
   if (chunk_states && !aligned16(chunk_states))
     return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
+  VSSM_TRY(check_states(initial_states, "initial_states"));
+  VSSM_TRY(check_states(final_states, "final_states"));
   const int64_t T = total_tokens;
   const Layout l = scan_layout(T, D, N, kFwdChunk, false);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  // an empty sequence ends in the state it starts from
+  e = launch_empty_sequence_states(cu_seqlens, num_seqs, (int64_t)D * N, initial_states, final_states, st);
+  if (e != cudaSuccess) return cuda_fail(e, "empty-sequence states launch");
   if (T == 0) return VSSM_OK;
   const int32_t* pos = nullptr;
   VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, T, workspace, l, st, &pos));
+  const int32_t* seq = nullptr;
+  if (initial_states || final_states) {
+    e = launch_sequence_index(cu_seqlens, num_seqs, T, at<int32_t>(workspace, l.seq), st);
+    if (e != cudaSuccess) return cuda_fail(e, "sequence index launch");
+    seq = at<int32_t>(workspace, l.seq);
+  }
 
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
+  a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);
   a.flags = at<int>(workspace, l.flags);
@@ -434,6 +455,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               const int32_t* cu_seqlens, const int32_t* position_indices,
                               int32_t num_seqs, int64_t total_tokens, int32_t D, int32_t N,
                               vssm_dtype dtype, const float* chunk_states, const void* y,
+                              const float* initial_states, const float* d_final_states,
+                              float* d_initial_states,
                               void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream) {
@@ -451,6 +474,9 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   if (z && T > 0 && !dz) return fail(VSSM_ERR_ARG, "dz is NULL although z is given");
   if (dz && !aligned16(dz)) return fail(VSSM_ERR_ALIGN, "dz is not 16-byte aligned");
   if (y) VSSM_TRY(check_io(y, "y", T));
+  VSSM_TRY(check_states(initial_states, "initial_states"));
+  VSSM_TRY(check_states(d_final_states, "d_final_states"));
+  VSSM_TRY(check_states(d_initial_states, "d_initial_states"));
   const Layout l = scan_layout(T, D, N, kBwdChunk, true);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -460,12 +486,22 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   // reads as "not stored yet": a carry is its own flag
   if (T > 0) e = cudaMemsetAsync(at<char>(workspace, l.incl), 0xff, l.incl_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "filling the look-back carries");
+  // the gradient reaching an empty sequence's final state reaches its start unchanged
+  e = launch_empty_sequence_states(cu_seqlens, num_seqs, (int64_t)D * N, d_final_states, d_initial_states, st);
+  if (e != cudaSuccess) return cuda_fail(e, "empty-sequence states launch");
+  const bool states = initial_states || d_final_states || d_initial_states;
+  if (T > 0 && states) {
+    e = launch_sequence_index(cu_seqlens, num_seqs, T, at<int32_t>(workspace, l.seq), st);
+    if (e != cudaSuccess) return cuda_fail(e, "sequence index launch");
+  }
 
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.dout = dout; a.chunk_states = const_cast<float*>(chunk_states);
   a.du = du; a.ddr = ddelta_raw; a.dz = z ? dz : nullptr;
   a.y = const_cast<void*>(y);
+  a.seq = states ? at<int32_t>(workspace, l.seq) : nullptr;
+  a.h_init = initial_states; a.dh_final = d_final_states; a.dh_init = d_initial_states;
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);
   a.flags = at<int>(workspace, l.flags);

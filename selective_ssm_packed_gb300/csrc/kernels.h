@@ -18,6 +18,12 @@ constexpr int kStateChunk = 32;  // tokens per saved scan-state chunk
 enum : int { kStatusBadCu = 1, kStatusLookbackTimeout = 2, kStatusTmaTimeout = 4 };
 
 // ---------------------------------------------------------------- position indices
+// seq[t] = the sequence holding token t (read where sequences start or end).
+cudaError_t launch_sequence_index(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* seq,
+                                  cudaStream_t st);
+// dst[s] = src[s] (or zeros) for every empty sequence s; rows of DN floats.
+cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, int64_t DN,
+                                         const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st);
 
@@ -63,6 +69,14 @@ struct ScanArgs {
   float* chunk_states;        // fwd: written (nullable); bwd: read
   void* out;                  // fwd
   void* y;                    // fwd: pre-gate output (nullable); bwd: the same, read (nullable)
+  // sequence states, (num_seqs, D, N) f32, all nullable: fwd reads h_init and
+  // writes h_final; bwd reads h_init and dh_final and writes dh_init.  seq[t]
+  // is the sequence of token t (set whenever one of them is given).
+  const int32_t* seq;
+  const float* h_init;
+  float* h_final;
+  const float* dh_final;
+  float* dh_init;
   void* du;                   // bwd
   void* ddr;                  // bwd
   void* dz;                   // bwd (nullable)

@@ -39,6 +39,51 @@ cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t
   return cudaGetLastError();
 }
 
+// seq[t] = the sequence holding token t: the largest s with cu[s] <= t (the
+// same upper-bound search, so zero-length sequences hold no token).  The scan
+// calls read it only where a sequence starts or ends, to find its state row.
+__global__ void __launch_bounds__(256) sequence_index_kernel(const int32_t* __restrict__ cu,
+                                                             int32_t S, int64_t T,
+                                                             int32_t* __restrict__ seq) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += stride) {
+    int32_t lo = 0, hi = S;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    seq[t] = lo;
+  }
+}
+
+cudaError_t launch_sequence_index(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* seq,
+                                  cudaStream_t st) {
+  int64_t blocks = (T + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) return cudaSuccess;
+  sequence_index_kernel<<<(unsigned)blocks, 256, 0, st>>>(cu, num_seqs, T, seq);
+  return cudaGetLastError();
+}
+
+// For every EMPTY sequence s (cu[s] == cu[s+1]), dst[s] = src[s] (rows of DN
+// floats; zeros when src is NULL): the state, or its gradient, passes a
+// sequence with no token unchanged.  One block per sequence.
+__global__ void __launch_bounds__(256) empty_sequence_states_kernel(const int32_t* __restrict__ cu,
+                                                                    int64_t DN,
+                                                                    const float* __restrict__ src,
+                                                                    float* __restrict__ dst) {
+  const int64_t s = blockIdx.x;
+  if (cu[s] != cu[s + 1]) return;
+  for (int64_t i = threadIdx.x; i < DN; i += blockDim.x) dst[s * DN + i] = src ? src[s * DN + i] : 0.0f;
+}
+
+cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, int64_t DN,
+                                         const float* src, float* dst, cudaStream_t st) {
+  if (num_seqs <= 0 || !dst) return cudaSuccess;
+  empty_sequence_states_kernel<<<(unsigned)num_seqs, 256, 0, st>>>(cu, DN, src, dst);
+  return cudaGetLastError();
+}
+
 // out[m] = sum over p = 0..P-1 of in[p*ld + m], in a fixed order: rows are
 // summed in order within groups of R consecutive rows, then the group sums in
 // order.  One thread per (column, group), so the result is bitwise repeatable.

@@ -121,7 +121,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
     int32_t a_log,
     const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
     int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* out, void* y, float* chunk_states,
-    int32_t* status, void* stream) {
+    const float* initial_states, float* final_states, int32_t* status, void* stream) {
   // ---- argument checks (same rules as varlen_selective_scan_fwd)
   if (dtype != VSSM_F32 && dtype != VSSM_BF16) return err(VSSM_ERR_DTYPE, "dtype %lld not supported", dtype);
   const IO io = dtype == VSSM_F32 ? IO::F32 : IO::BF16;
@@ -142,16 +142,19 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
     }
   }
   if ((z && !al16(z)) || (y && !al16(y)) || (chunk_states && !al16(chunk_states)) || !al16(A) ||
-      (Dskip && !al16(Dskip)) || (dt_bias && !al16(dt_bias)) || (position_indices && !al16(position_indices)))
+      (Dskip && !al16(Dskip)) || (dt_bias && !al16(dt_bias)) || (position_indices && !al16(position_indices)) ||
+      (initial_states && !al16(initial_states)) || (final_states && !al16(final_states)))
     return record_error(VSSM_ERR_ALIGN,
-                        "z, y, chunk_states, A, Dskip, dt_bias and position_indices must be 16-byte aligned");
+                        "z, y, chunk_states, A, Dskip, dt_bias, position_indices, initial_states and "
+                        "final_states must be 16-byte aligned");
 
-  // ---- scratch layout: [header: status, ticket][flags][pos][agg][agg_sd][incl]
+  // ---- scratch layout: [header: status, ticket][flags][pos][seq][agg][agg_sd][incl]
   const int64_t n_tiles = cdiv(D, kTile), n_chunks = cdiv(T, kFwdChunk);
   const size_t slots = (size_t)(n_tiles * n_chunks);
   const size_t o_flags = kAlign;
   const size_t o_pos = o_flags + up(sizeof(int) * slots * kTile);
-  const size_t o_agg = o_pos + up(sizeof(int32_t) * (size_t)T);
+  const size_t o_seq = o_pos + up(sizeof(int32_t) * (size_t)T);
+  const size_t o_agg = o_seq + up(sizeof(int32_t) * (size_t)T);
   const size_t o_sd = o_agg + up(sizeof(float) * slots * N * kTile);
   const size_t o_incl = o_sd + up(sizeof(float) * slots * kTile);
   const size_t need = o_incl + up(sizeof(float) * slots * N * kTile);
@@ -168,9 +171,18 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t ce = cudaMemsetAsync(s, 0, o_pos, st);  // status, ticket, look-back flags
   if (ce == cudaSuccess && status) ce = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+  // an empty sequence ends in the state it starts from
+  if (ce == cudaSuccess)
+    ce = launch_empty_sequence_states(cu_seqlens, num_seqs, (int64_t)D * N, initial_states, final_states, st);
   if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
   if (T == 0) return VSSM_OK;
   int32_t* status_word = status ? status : reinterpret_cast<int32_t*>(s);
+  const int32_t* seq = nullptr;
+  if (initial_states || final_states) {
+    ce = launch_sequence_index(cu_seqlens, num_seqs, T, reinterpret_cast<int32_t*>(s + o_seq), st);
+    if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
+    seq = reinterpret_cast<int32_t*>(s + o_seq);
+  }
 
   const int32_t* pos = position_indices;
   if (!pos) {
@@ -183,6 +195,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
+  a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
   a.status = status_word;
   a.ticket = reinterpret_cast<unsigned*>(s + 4);
   a.flags = reinterpret_cast<int*>(s + o_flags);

@@ -45,6 +45,8 @@
 //   5. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
 // Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
 // and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -313,6 +315,31 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     h = make_float2(sm.H[nF * bx + lane], sm.H[nS * bx + lane]);
   }
   const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
+  // Sequence-state events of this item, bit t for token t of the chunk:
+  //   evH: a sequence starts from a given initial state,
+  //   evG: a sequence starts and the gradient reaching its initial state is asked for,
+  //   evF: a sequence ends and a gradient reaches its final state from outside.
+  // Items without any take the walks without event code.
+  unsigned evH = 0u, evG = 0u, evF = 0u;
+  if (a.seq) {
+    const unsigned live = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
+    const unsigned starts = rst & live;
+    evH = a.h_init ? starts : 0u;
+    evG = a.dh_init ? starts : 0u;
+    if (a.dh_final) {
+      // token t ends a sequence when token t + 1 starts one or does not exist
+      unsigned ends = starts >> 1;
+      if (t0 + rows >= a.T || (rows == 32 && __ldg(a.pos + t0 + 32) == 0)) ends |= 1u << (rows - 1);
+      evF = ends & live;
+    }
+  }
+  const bool events = (evH | evG | evF) != 0u;
+  // the (nF, nS) entries of a sequence-state row for token t's sequence
+  auto state_pair = [&](const float* st, int t) {
+    if (!valid) return make_float2(0.0f, 0.0f);
+    const float2 v = __ldg(reinterpret_cast<const float2*>(st + ((int64_t)a.seq[t0 + t] * a.D + d) * N + n0));
+    return (lane & 16) ? make_float2(v.y, v.x) : v;
+  };
   __syncthreads();
 
   // ---- 2. forward walk over the 32 tokens (state pair n0, n0+1)
@@ -322,7 +349,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // the forward walk's dC sums (one per lane and 16-token group), stored only
   // after the look-back, so that a fence there does not wait for them
   float dcs[kL / 16];
-  {
+  auto fwalk = [&](auto with_events) {
+    constexpr bool kEv = decltype(with_events)::value;
     const float* rowc = sm.dl + lane * kP;
 #pragma unroll
     for (int kb = 0; kb < kL / 4; ++kb) {
@@ -348,15 +376,25 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         const float2 at = make_float2(ex2(fmaf(dla[e], A2.x, ofa[e])), ex2(fmaf(dla[e], A2.y, ofa[e])));
         const float2 Ct = Ca[e];
         h = fma2(at, h, mul2(splat2(dua[e]), Ba[e]));
+        if constexpr (kEv) {
+          if ((evH >> t) & 1u)  // a start from a given state: h = a h_init + b, a's own value
+            h = fma2(make_float2(ex2(dla[e] * A2.x), ex2(dla[e] * A2.y)), state_pair(a.h_init, t), h);
+        }
         hist[t] = h;
         E = mul2(E, at);
         tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
+        if constexpr (kEv) {
+          // the gradient reaching a final state joins dh_t, and the left carry through E_t
+          if ((evF >> t) & 1u) tot = fma2(E, state_pair(a.dh_final, t), tot);
+        }
         if (a.has_z && !a.has_y) sm.ypart[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
         // dC contributions g_t h_t, summed over the tile's channels
         colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &dcs[t >> 4]);
       }
     }
-  }
+  };
+  if (events) fwalk(std::true_type{});
+  else fwalk(std::false_type{});
 
   // ---- 3. decoupled look-back towards higher chunks (every warp for its pair)
   float2 x = make_float2(0.0f, 0.0f);
@@ -430,10 +468,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     T* gddr = static_cast<T*>(a.ddr);
     T* gdz = static_cast<T*>(a.dz);
     float2 r = x;  // carry entering the current token from the right
-#pragma unroll
-    for (int blk = kL / kRB - 1; blk >= 0; --blk) {
+    // the block's tokens, walked down; a second copy carries the event code
+    auto rwalk = [&](const int blk, auto with_events) {
+      constexpr bool kEv = decltype(with_events)::value;
       const int buf = blk & 1;
-      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
 #pragma unroll
       for (int kb = (blk + 1) * kRB / 4 - 1; kb >= blk * kRB / 4; --kb) {
         const float4 dl4 = *reinterpret_cast<const float4*>(sm.dl + lane * kP + 4 * kb);
@@ -457,7 +495,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
           const int t = 4 * kb + e;
           const float2 at = make_float2(ex2(fmaf(dla[e], A2.x, ofa[e])), ex2(fmaf(dla[e], A2.y, ofa[e])));
           const float2 Bt = Ba[e];
-          const float2 dh = fma2(Ca[e], splat2(ga[e]), r);  // total gradient w.r.t. h_t
+          float2 dh = fma2(Ca[e], splat2(ga[e]), r);  // total gradient w.r.t. h_t
+          if constexpr (kEv) {
+            if ((evF >> t) & 1u) dh = __fadd2_rn(dh, state_pair(a.dh_final, t));
+          }
           // a_t h_{t-1} = h_t - delta u B: no need for the previous state
           const float2 dhq = mul2(dh, fma2(splat2(-dua[e]), Bt, hist[t]));
           dA = fma2(splat2(dla[e]), dhq, dA);
@@ -468,9 +509,24 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             const int tt = t + ColSum16::token(lane);
             if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + nF) * a.T + t0 + tt] = sum;
           }
+          if constexpr (kEv) {
+            if (((evG >> t) & 1u) && valid) {
+              // the gradient reaching the starting state: dh_t times a's own value
+              const float2 g0 = mul2(dh, make_float2(ex2(dla[e] * A2.x), ex2(dla[e] * A2.y)));
+              float2* row = reinterpret_cast<float2*>(a.dh_init + ((int64_t)a.seq[t0 + t] * a.D + d) * N + n0);
+              *row = (lane & 16) ? make_float2(g0.y, g0.x) : g0;
+            }
+          }
           r = mul2(dh, at);  // carry to h_{t-1}
         }
       }
+    };
+#pragma unroll
+    for (int blk = kL / kRB - 1; blk >= 0; --blk) {
+      const int buf = blk & 1;
+      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
+      if (events) rwalk(blk, std::true_type{});
+      else rwalk(blk, std::false_type{});
       __syncthreads();  // the block's partials are complete
       // du, d delta_raw and dz of the block: thread i takes token
       // blk*kRB + i / kTile, channel i % kTile (= lane), and adds the warps'

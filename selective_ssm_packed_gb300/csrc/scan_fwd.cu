@@ -29,6 +29,8 @@
 //   6. Pass 2: each thread starts from its exact state, recomputes its K tokens
 //      and writes out = (C.h + Dskip u) * SiLU(z); states at multiples of 32
 //      tokens go to chunk_states for the backward pass.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -145,6 +147,39 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // position index of token t < rows of the chunk (the last chunk's ragged
   // tail, past the last whole group of 4, is read from global memory)
   auto pos_at = [&](int t) { return t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t); };
+  // the state a sequence starting at token t (of the chunk) starts from: its
+  // row of the initial states, or zero
+  auto start_state = [&](float2 (&hs)[N / 2], int t) {
+    if (a.h_init && valid) {
+      const float4* row = reinterpret_cast<const float4*>(a.h_init + ((int64_t)a.seq[t0 + t] * a.D + d) * N);
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) {
+        const float4 q = __ldg(row + i);
+        hs[2 * i] = make_float2(q.x, q.y);
+        hs[2 * i + 1] = make_float2(q.z, q.w);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) hs[i] = make_float2(0.0f, 0.0f);
+    }
+  };
+  // the state after the last token t (of the chunk) of a sequence, into its
+  // row of the final states
+  auto end_state = [&](const float2 (&hs)[N / 2], int t) {
+    if (valid) {
+      float4* row = reinterpret_cast<float4*>(a.h_final + ((int64_t)a.seq[t0 + t] * a.D + d) * N);
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i)
+        row[i] = make_float4(hs[2 * i].x, hs[2 * i].y, hs[2 * i + 1].x, hs[2 * i + 1].y);
+    }
+  };
+  // token t (< rows) is the last of its sequence: the next token starts one,
+  // or there is none
+  auto seq_end = [&](int t) {
+    const int n = t + 1;
+    if (t0 + n >= a.T) return true;
+    return (n < rows ? pos_at(n) : __ldg(a.pos + t0 + n)) == 0;
+  };
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
   // B and C rows of this warp's own tokens, widened to fp32 by the warp: no
@@ -191,8 +226,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       const float dl = a.delta_softplus ? softplusf(r) : r;
       dlp[k * kTile] = dl;
       if ((rm >> k) & 1u) {
-#pragma unroll
-        for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
+        start_state(h, tb + k);
         sd = 0.0f;
         rs = 1;
       }
@@ -212,8 +246,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float dl = a.delta_softplus ? softplusf(r) : r;
     sm.dlt[t * kTile + lane] = dl;
     if (pos_at(t) == 0) {
-#pragma unroll
-      for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
+      start_state(h, t);
       sd = 0.0f;
       rs = 1;
     }
@@ -404,12 +437,14 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float* const cp = Cf + tb * N;
     T* op = out + (t0 + tb) * a.D + d;
     T* yp = ypre ? ypre + (t0 + tb) * a.D + d : nullptr;
+    // bit k: token tb + k ends a sequence whose final state is asked for
+    const unsigned em = a.h_final ? __ballot_sync(0xffffffffu, lane < kK && seq_end(tb + lane)) : 0u;
+    // two copies of the walk: with the final-state stores only where a
+    // sequence ends in this warp's tokens
+    auto walk2 = [&](auto with_ends) {
 #pragma unroll
     for (int k = 0; k < kK; ++k) {
-      if ((rm >> k) & 1u) {
-#pragma unroll
-        for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
-      }
+      if ((rm >> k) & 1u) start_state(h, tb + k);
       const float dl = dlp[k * kTile];
       const float uu = to_f(up[k * kTile]);
       const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
@@ -430,16 +465,19 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (a.has_z) y *= siluf(to_f(zp[k * kTile])) + a.gate_floor;
       if (valid) *op = from_f<T>(y);
       op += a.D;
+      if constexpr (decltype(with_ends)::value) {
+        if ((em >> k) & 1u) end_state(h, tb + k);
+      }
     }
+    };
+    if (em) walk2(std::true_type{});
+    else walk2(std::false_type{});
   } else {
 #pragma unroll 1  // ragged tails and narrow tiles only: kept small for the instruction cache
   for (int k = 0; k < kK; ++k) {
     const int t = tb + k;
     if (t >= rows) break;
-    if (pos_at(t) == 0) {
-#pragma unroll
-      for (int i = 0; i < P; ++i) h[i] = make_float2(0.0f, 0.0f);
-    }
+    if (pos_at(t) == 0) start_state(h, t);
     const float dl = sm.dlt[t * kTile + lane];
     const float uu = to_f(sm.u[t * bx + lane]);
     const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
@@ -456,6 +494,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (ypre && valid) ypre[(t0 + t) * a.D + d] = from_f<T>(y);
     if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane])) + a.gate_floor;
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
+    if (a.h_final && seq_end(t)) end_state(h, t);
   }
   }
 

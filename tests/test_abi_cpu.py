@@ -81,8 +81,8 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _conv_fwd(lib, ws=None) == -4
     assert _conv_fwd(lib, T=-1) == -1
     scan = lib.varlen_selective_scan_fwd
-    args = [16, 16, 16, 16, 16, None, None, None, 1, 0.0, 0, 16, None, 1, 16, 8, 3, 0, 16, None, None, 16,
-            1 << 30, None]
+    args = [16, 16, 16, 16, 16, None, None, None, 1, 0.0, 0, 16, None, 1, 16, 8, 3, 0, 16, None, None, None,
+            None, 16, 1 << 30, None]
     assert scan(*args) == -6                     # N = 3
     args[16] = 4
     args[17] = 1
@@ -91,7 +91,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     args[19] = 8
     assert scan(*args) == -3                     # misaligned y
     args[19] = None
+    args[21] = 8
+    assert scan(*args) == -3                     # misaligned initial_states
     args[21] = None
+    args[23] = None
     assert scan(*args) == -4
 
 

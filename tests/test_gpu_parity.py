@@ -259,6 +259,76 @@ def test_gate_floor_and_a_log_variants(dtype):
         assert_close(k, g[k], ref[k], tol)
 
 
+@pytest.mark.parametrize("D,N,dtype", [(72, 8, "f32"), (104, 16, "bf16")])
+def test_sequence_states_fwd_bwd(D, N, dtype):
+    """Per-sequence initial states in, final states out, and their gradients
+    (the article's future work: cut sequences pass their state on).  The
+    lengths put sequence ends on the forward's 128-token and the backward's
+    32-token chunk edges, and include length-1 and empty sequences."""
+    lengths = [128, 32, 1, 0, 95, 2, 300, 64]
+    cu_np, T, r = rand_case(lengths, D, N, dtype, seed=31)
+    S = len(lengths)
+    rng = np.random.default_rng(32)
+    h0 = rng.standard_normal((S, D, N)).astype(np.float32)
+    dfin = rng.standard_normal((S, D, N)).astype(np.float32)
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    u = dev(r["x"], dtype)
+    args = dict(u=u, delta_raw=dev(r["delta_raw"], dtype), A=f32(r["A"]), B=dev(r["B"], dtype),
+                C=dev(r["C"], dtype), Dskip=f32(r["Dskip"]), z=dev(r["z"], dtype), dt_bias=f32(r["dt_bias"]))
+    h0_t, dfin_t = f32(h0), f32(dfin)
+    out, states, y, fin = vs.varlen_selective_scan_fwd(**args, cu_seqlens=cu, position_indices=pos, y=True,
+                                                       initial_states=h0_t, final_states=True)
+    dout = dev(r["dout"], dtype)
+    g = vs.varlen_selective_scan_bwd(**args, dout=dout, cu_seqlens=cu, chunk_states=states,
+                                     position_indices=pos, y=y, initial_states=h0_t,
+                                     d_final_states=dfin_t, d_initial_states=True)
+    torch.cuda.synchronize()
+    sargs = [host(u), r["delta_raw"], r["A"], r["B"], r["C"], r["Dskip"], r["z"], r["dt_bias"]]
+    tol = TOL[dtype]
+    out_ref, fin_ref = oracle.scan_fwd(*sargs, cu_np, h_init=h0, return_last_state=True)
+    assert_close("out", out, out_ref, tol)
+    assert_close("final_states", fin, fin_ref, tol)
+    assert np.array_equal(host(fin)[3], h0[3].astype(np.float64))  # the empty sequence
+    ref = oracle.scan_bwd_threaded(*sargs, host(dout), cu_np, h_init=h0, dh_last=dfin)
+    for k in ("du", "ddelta_raw", "dz", "dA", "dB", "dC", "dDskip", "d_dt_bias"):
+        assert_close(k, g[k], ref[k], tol)
+    assert_close("d_initial_states", g["d_initial_states"], ref["dh_init"], tol)
+    assert np.array_equal(host(g["d_initial_states"])[3], dfin[3].astype(np.float64))
+
+
+def test_a_cut_sequence_passes_its_state_on_gpu():
+    """One 900-token sequence run whole, and run as two parts (the first 400
+    tokens, then the rest from the first part's final state, the first part's
+    backward taking the second part's starting-state gradient): the same
+    outputs and gradients."""
+    L, L1, D, N = 900, 400, 64, 16
+    cu_np, T, r = rand_case([L], D, N, "f32", seed=33)
+    cu = torch.from_numpy(cu_np).cuda()
+    f = lambda k, sl=slice(None): f32(r[k][sl])  # noqa: E731
+    def call(sl, n, h0=None, dfin=None):
+        c = torch.tensor([0, n], dtype=torch.int32, device="cuda")
+        args = dict(u=f("x", sl), delta_raw=f("delta_raw", sl), A=f("A"), B=f("B", sl), C=f("C", sl),
+                    Dskip=f("Dskip"), z=f("z", sl), dt_bias=f("dt_bias"))
+        out, st, fin = vs.varlen_selective_scan_fwd(**args, cu_seqlens=c, initial_states=h0, final_states=True)
+        g = vs.varlen_selective_scan_bwd(**args, dout=f("dout", sl), cu_seqlens=c, chunk_states=st,
+                                         initial_states=h0, d_final_states=dfin, d_initial_states=True)
+        return out, fin, g
+    out_w, _, g_w = call(slice(None), L)
+    out_2, fin_2, g_2 = None, None, None
+    out_1, fin_1, _ = call(slice(0, L1), L1)
+    out_2, _, g_2 = call(slice(L1, L), L - L1, h0=fin_1)
+    _, _, g_1 = call(slice(0, L1), L1, dfin=g_2["d_initial_states"])
+    torch.cuda.synchronize()
+    tol = TOL["f32"]
+    assert_close("out", torch.cat([out_1, out_2]), host(out_w), tol)
+    for k in ("du", "ddelta_raw", "dz", "dB", "dC"):
+        assert_close(k, torch.cat([g_1[k], g_2[k]]), host(g_w[k]), tol)
+    for k in ("dA", "dDskip", "d_dt_bias"):
+        assert_close(k, g_1[k] + g_2[k], host(g_w[k]), tol)
+    assert_close("d_initial_states", g_1["d_initial_states"], host(g_w["d_initial_states"]), tol)
+
+
 @pytest.mark.parametrize("flags", [dict(z=False), dict(skip=False), dict(bias=False),
                                    dict(softplus=False), dict(z=False, skip=False, bias=False)])
 def test_optional_inputs(flags):

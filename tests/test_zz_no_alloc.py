@@ -52,7 +52,8 @@ def _noalloc(lib, t, T, D, N, dtype, out, states, status, pos=None, y=None):
     return lib.varlen_selective_scan_fwd_noalloc(
         _p(t["u"]), _p(t["delta_raw"]), _p(t["A"]), _p(t["B"]), _p(t["C"]), _p(t["Dskip"]), _p(t["z"]),
         _p(t["dt_bias"]), 1, 0.0, 0, _p(t["cu"]), _p(pos), t["cu"].numel() - 1, T, D, N,
-        binding.VSSM_F32 if dtype == "f32" else binding.VSSM_BF16, _p(out), _p(y), _p(states), _p(status),
+        binding.VSSM_F32 if dtype == "f32" else binding.VSSM_BF16, _p(out), _p(y), _p(states), None, None,
+        _p(status),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
@@ -90,7 +91,8 @@ def test_noalloc_refuses_a_problem_larger_than_its_scratch(lib):
     # claims 16384 tokens at D = 4096; refused on the host before any launch
     rc = lib.varlen_selective_scan_fwd_noalloc(
         _p(t["u"]), _p(t["delta_raw"]), _p(t["A"]), _p(t["B"]), _p(t["C"]), None, None, None, 1, 0.0, 0,
-        _p(t["cu"]), None, 1, 16384, 4096, 16, binding.VSSM_BF16, _p(out), None, None, None, None)
+        _p(t["cu"]), None, 1, 16384, 4096, 16, binding.VSSM_BF16, _p(out), None, None, None, None, None,
+        None)
     assert rc == -4
     msg = binding.last_error()
     assert "scratch" in msg and str(64 << 20) in msg
