@@ -45,8 +45,6 @@
 //   5. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
 // Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
 // and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
-#include <type_traits>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -151,7 +149,9 @@ __device__ __forceinline__ void publish_flag(int* flag, int value, bool publish,
   if (lane == 0 && publish) st_relaxed_gpu(flag, value);
 }
 
-template <typename T, int N>
+// kStates: the call passes sequence states (initial states, final-state or
+// starting-state gradients); without them the kernel carries no code for them.
+template <typename T, int N, bool kStates>
 __global__ void __launch_bounds__(16 * N, 512 / (16 * N))
 scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
@@ -319,9 +319,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   //   evH: a sequence starts from a given initial state,
   //   evG: a sequence starts and the gradient reaching its initial state is asked for,
   //   evF: a sequence ends and a gradient reaches its final state from outside.
-  // Items without any take the walks without event code.
   unsigned evH = 0u, evG = 0u, evF = 0u;
-  if (a.seq) {
+  if (kStates && a.seq) {
     const unsigned live = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
     const unsigned starts = rst & live;
     evH = a.h_init ? starts : 0u;
@@ -333,7 +332,6 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       evF = ends & live;
     }
   }
-  const bool events = (evH | evG | evF) != 0u;
   // the (nF, nS) entries of a sequence-state row for token t's sequence
   auto state_pair = [&](const float* st, int t) {
     if (!valid) return make_float2(0.0f, 0.0f);
@@ -349,8 +347,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // the forward walk's dC sums (one per lane and 16-token group), stored only
   // after the look-back, so that a fence there does not wait for them
   float dcs[kL / 16];
-  auto fwalk = [&](auto with_events) {
-    constexpr bool kEv = decltype(with_events)::value;
+  {
+    constexpr bool kEv = kStates;
     const float* rowc = sm.dl + lane * kP;
 #pragma unroll
     for (int kb = 0; kb < kL / 4; ++kb) {
@@ -392,9 +390,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &dcs[t >> 4]);
       }
     }
-  };
-  if (events) fwalk(std::true_type{});
-  else fwalk(std::false_type{});
+  }
 
   // ---- 3. decoupled look-back towards higher chunks (every warp for its pair)
   float2 x = make_float2(0.0f, 0.0f);
@@ -468,10 +464,11 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     T* gddr = static_cast<T*>(a.ddr);
     T* gdz = static_cast<T*>(a.dz);
     float2 r = x;  // carry entering the current token from the right
-    // the block's tokens, walked down; a second copy carries the event code
-    auto rwalk = [&](const int blk, auto with_events) {
-      constexpr bool kEv = decltype(with_events)::value;
+    constexpr bool kEv = kStates;
+#pragma unroll
+    for (int blk = kL / kRB - 1; blk >= 0; --blk) {
       const int buf = blk & 1;
+      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
 #pragma unroll
       for (int kb = (blk + 1) * kRB / 4 - 1; kb >= blk * kRB / 4; --kb) {
         const float4 dl4 = *reinterpret_cast<const float4*>(sm.dl + lane * kP + 4 * kb);
@@ -520,13 +517,6 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
           r = mul2(dh, at);  // carry to h_{t-1}
         }
       }
-    };
-#pragma unroll
-    for (int blk = kL / kRB - 1; blk >= 0; --blk) {
-      const int buf = blk & 1;
-      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
-      if (events) rwalk(blk, std::true_type{});
-      else rwalk(blk, std::false_type{});
       __syncthreads();  // the block's partials are complete
       // du, d delta_raw and dz of the block: thread i takes token
       // blk*kRB + i / kTile, channel i % kTile (= lane), and adds the warps'
@@ -612,20 +602,28 @@ __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restri
   if (v < N) dB[t * N + v] = acc; else dC[t * N + (v - N)] = acc;
 }
 
-template <typename T, int N>
-cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+template <typename T, int N, bool kStates>
+cudaError_t launch_k(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
                      const CUtensorMap& tm_y, cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem<T, N>);
-  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N>,
+  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, kStates>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
   int grid = 0;
-  e = persistent_grid(scan_bwd_kernel<T, N>, 16 * N, smem, items, &grid);
+  e = persistent_grid(scan_bwd_kernel<T, N, kStates>, 16 * N, smem, items, &grid);
   if (e != cudaSuccess) return e;
-  scan_bwd_kernel<T, N><<<grid, 16 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, a);
+  scan_bwd_kernel<T, N, kStates><<<grid, 16 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, a);
   return cudaGetLastError();
+}
+
+template <typename T, int N>
+cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                     const CUtensorMap& tm_y, cudaStream_t st) {
+  return a.seq ? launch_k<T, N, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+               : launch_k<T, N, false>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
 }
 
 template <typename T>

@@ -29,8 +29,6 @@
 //   6. Pass 2: each thread starts from its exact state, recomputes its K tokens
 //      and writes out = (C.h + Dskip u) * SiLU(z); states at multiples of 32
 //      tokens go to chunk_states for the backward pass.
-#include <type_traits>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -67,7 +65,9 @@ struct FwdSmem {
   alignas(8) uint64_t bar;
 };
 
-template <typename T, int N>
+// kStates: the call passes sequence states (initial and/or final); without
+// them the kernel carries no code for them.
+template <typename T, int N, bool kStates>
 __global__ void __launch_bounds__(kThreads, 2)
 scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
                 const __grid_constant__ CUtensorMap tm_z, const ScanArgs a) {
@@ -150,7 +150,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // the state a sequence starting at token t (of the chunk) starts from: its
   // row of the initial states, or zero
   auto start_state = [&](float2 (&hs)[N / 2], int t) {
-    if (a.h_init && valid) {
+    if (kStates && a.h_init && valid) {
       const float4* row = reinterpret_cast<const float4*>(a.h_init + ((int64_t)a.seq[t0 + t] * a.D + d) * N);
 #pragma unroll
       for (int i = 0; i < N / 4; ++i) {
@@ -437,14 +437,16 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float* const cp = Cf + tb * N;
     T* op = out + (t0 + tb) * a.D + d;
     T* yp = ypre ? ypre + (t0 + tb) * a.D + d : nullptr;
-    // bit k: token tb + k ends a sequence whose final state is asked for
-    const unsigned em = a.h_final ? __ballot_sync(0xffffffffu, lane < kK && seq_end(tb + lane)) : 0u;
-    // two copies of the walk: with the final-state stores only where a
-    // sequence ends in this warp's tokens
-    auto walk2 = [&](auto with_ends) {
 #pragma unroll
     for (int k = 0; k < kK; ++k) {
-      if ((rm >> k) & 1u) start_state(h, tb + k);
+      if ((rm >> k) & 1u) {
+        // the previous token ended a sequence (a token of this warp's when k > 0;
+        // the warp before stores its own last token's state)
+        if constexpr (kStates) {
+          if (a.h_final && k > 0) end_state(h, tb + k - 1);
+        }
+        start_state(h, tb + k);
+      }
       const float dl = dlp[k * kTile];
       const float uu = to_f(up[k * kTile]);
       const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
@@ -465,13 +467,10 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (a.has_z) y *= siluf(to_f(zp[k * kTile])) + a.gate_floor;
       if (valid) *op = from_f<T>(y);
       op += a.D;
-      if constexpr (decltype(with_ends)::value) {
-        if ((em >> k) & 1u) end_state(h, tb + k);
-      }
     }
-    };
-    if (em) walk2(std::true_type{});
-    else walk2(std::false_type{});
+    if constexpr (kStates) {
+      if (a.h_final && seq_end(tb + kK - 1)) end_state(h, tb + kK - 1);
+    }
   } else {
 #pragma unroll 1  // ragged tails and narrow tiles only: kept small for the instruction cache
   for (int k = 0; k < kK; ++k) {
@@ -494,7 +493,9 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (ypre && valid) ypre[(t0 + t) * a.D + d] = from_f<T>(y);
     if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane])) + a.gate_floor;
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
-    if (a.h_final && seq_end(t)) end_state(h, t);
+    if constexpr (kStates) {
+      if (a.h_final && seq_end(t)) end_state(h, t);
+    }
   }
   }
 
@@ -508,19 +509,25 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }  // persistent loop
 }
 
-template <typename T, int N>
-cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+template <typename T, int N, bool kStates>
+cudaError_t launch_k(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, cudaStream_t st) {
   const size_t smem = sizeof(FwdSmem<T, N>);
-  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<T, N>,
+  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<T, N, kStates>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
   int grid = 0;
-  e = persistent_grid(scan_fwd_kernel<T, N>, kThreads, smem, items, &grid);
+  e = persistent_grid(scan_fwd_kernel<T, N, kStates>, kThreads, smem, items, &grid);
   if (e != cudaSuccess) return e;
-  scan_fwd_kernel<T, N><<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
+  scan_fwd_kernel<T, N, kStates><<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
   return cudaGetLastError();
+}
+
+template <typename T, int N>
+cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, cudaStream_t st) {
+  return a.seq ? launch_k<T, N, true>(a, tm_u, tm_dr, tm_z, st) : launch_k<T, N, false>(a, tm_u, tm_dr, tm_z, st);
 }
 
 template <typename T>
