@@ -57,10 +57,10 @@ def _load():
             lib.oracle_position_indices.argtypes = [_ip, ctypes.c_int32, ctypes.c_int64, _ip]
             lib.oracle_conv1d_fwd.argtypes = [_dp, _dp, _dp, _ip, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                              ctypes.c_int32, ctypes.c_int32, _dp]
+                                              ctypes.c_int32, ctypes.c_int32, _dp, _dp, _dp]
             lib.oracle_conv1d_bwd.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                              ctypes.c_int32, ctypes.c_int32, _dp, _dp, _dp]
+                                              ctypes.c_int32, ctypes.c_int32, _dp, _dp, _dp, _dp, _dp, _dp]
             lib.oracle_scan_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int32,
                                             ctypes.c_double, _dp,
                                             _ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
@@ -114,28 +114,39 @@ def position_indices(cu_seqlens, total_tokens=None):
     return pos
 
 
-def conv1d_fwd(x, weight, bias, cu_seqlens, apply_silu=True, d_range=None):
-    x, w, b = _f64(x), _f64(weight), _f64(bias)
+def conv1d_fwd(x, weight, bias, cu_seqlens, apply_silu=True, d_range=None, x_init=None,
+               return_last=False):
+    """u (T, D); with return_last, also each sequence's last W-1 inputs (S, D, W-1).
+    x_init (S, D, W-1): the W-1 inputs before each sequence (zero when None)."""
+    x, w, b, x_init = _f64(x), _f64(weight), _f64(bias), _f64(x_init)
     cu, S, T = _cu(cu_seqlens)
     D, W = w.shape
     d0, d1 = d_range if d_range is not None else (0, D)
     u = np.zeros((T, D), dtype=np.float64)
+    xl = np.zeros((S, D, W - 1), dtype=np.float64) if return_last else None
     _check(_load().oracle_conv1d_fwd(_p(x), _p(w), _p(b), _p(cu), S, T, D, W, int(apply_silu),
-                                     d0, d1, _p(u)), "conv1d_fwd")
-    return u
+                                     d0, d1, _p(x_init), _p(u), _p(xl)), "conv1d_fwd")
+    return (u, xl) if return_last else u
 
 
-def conv1d_bwd(x, weight, bias, du, cu_seqlens, apply_silu=True, d_range=None):
+def conv1d_bwd(x, weight, bias, du, cu_seqlens, apply_silu=True, d_range=None, x_init=None,
+               dx_last=None, return_dx_init=False):
+    """(dx, dweight, dbias), and dx_init (S, D, W-1) last with return_dx_init.
+    dx_last (S, D, W-1): the gradient reaching each sequence's last W-1 inputs
+    from outside (zero when None)."""
     x, w, b, du = _f64(x), _f64(weight), _f64(bias), _f64(du)
+    x_init, dx_last = _f64(x_init), _f64(dx_last)
     cu, S, T = _cu(cu_seqlens)
     D, W = w.shape
     d0, d1 = d_range if d_range is not None else (0, D)
     dx = np.zeros((T, D), dtype=np.float64)
     dw = np.zeros((D, W), dtype=np.float64)
     db = np.zeros(D, dtype=np.float64)
+    dxi = np.zeros((S, D, W - 1), dtype=np.float64) if return_dx_init else None
     _check(_load().oracle_conv1d_bwd(_p(x), _p(w), _p(b), _p(du), _p(cu), S, T, D, W,
-                                     int(apply_silu), d0, d1, _p(dx), _p(dw), _p(db)), "conv1d_bwd")
-    return dx, dw, db
+                                     int(apply_silu), d0, d1, _p(x_init), _p(dx_last), _p(dx), _p(dw),
+                                     _p(db), _p(dxi)), "conv1d_bwd")
+    return (dx, dw, db, dxi) if return_dx_init else (dx, dw, db)
 
 
 def scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens, delta_softplus=True,

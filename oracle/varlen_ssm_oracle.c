@@ -68,67 +68,103 @@ int oracle_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int3
     return ORACLE_OK;
 }
 
-/* Depthwise causal conv1d on one pack.  For token t of a sequence starting at
- * `start`, tap k (k = 0 is the current token) is used only when t-k >= start,
- * which is the early stop of the article's conv1d_pack (taps never reach into
- * the previous sequence):
- *     pre[t,d] = bias[d] + sum_{k=0}^{W-1} [t-k >= start] w[d][W-1-k] x[t-k,d]
- *     u[t,d]   = apply_silu ? SiLU(pre) : pre                                  */
+/* Depthwise causal conv1d on one pack, one sequence at a time.  The taps of
+ * a sequence's token never reach into the previous sequence (the early stop
+ * of the article's conv1d_pack); instead, the W-1 positions before the
+ * sequence's first token hold its tail values: x_init[s][d][0..W-2] (the
+ * last W-1 inputs of a cut sequence's previous part), or zeros when x_init is
+ * NULL, which is the plain per-sequence zero padding.  With xe the
+ * sequence's inputs preceded by that tail (xe[p] for p = -(W-1) .. L-1):
+ *     pre[p,d] = bias[d] + sum_{k=0}^{W-1} w[d][W-1-k] xe[p-k]
+ *     u[p,d]   = apply_silu ? SiLU(pre) : pre
+ * x_last (nullable, (num_seqs, D, W-1)) receives each sequence's last W-1
+ * entries of xe: the tail the sequence's next part starts from.            */
+static void fill_tail(double* xe, const double* x, const double* x_init, int32_t s, int64_t start,
+                      int64_t L, int32_t d, int32_t D, int32_t W) {
+    for (int32_t j = 0; j < W - 1; ++j)
+        xe[j] = x_init ? x_init[((int64_t)s * D + d) * (W - 1) + j] : 0.0;
+    for (int64_t p = 0; p < L; ++p) xe[W - 1 + p] = x[(start + p) * D + d];
+}
+
 int oracle_conv1d_fwd(const double* x, const double* w, const double* bias,
                       const int32_t* cu, int32_t num_seqs, int64_t T, int32_t D, int32_t W,
-                      int32_t apply_silu, int32_t d_begin, int32_t d_end, double* u) {
+                      int32_t apply_silu, int32_t d_begin, int32_t d_end, const double* x_init,
+                      double* u, double* x_last) {
     if (check_cu(cu, num_seqs, T) != ORACLE_OK) return ORACLE_ERR_CU;
+    int64_t max_len = 0;
+    for (int32_t s = 0; s < num_seqs; ++s)
+        if (cu[s + 1] - cu[s] > max_len) max_len = cu[s + 1] - cu[s];
+    double* xe = (double*)malloc(sizeof(double) * (size_t)(W - 1 + max_len + 1));
+    if (!xe) return ORACLE_ERR_ALLOC;
     for (int32_t s = 0; s < num_seqs; ++s) {
-        const int64_t start = cu[s], end = cu[s + 1];
+        const int64_t start = cu[s], L = cu[s + 1] - cu[s];
         for (int32_t d = d_begin; d < d_end; ++d) {
-            for (int64_t t = start; t < end; ++t) {
+            fill_tail(xe, x, x_init, s, start, L, d, D, W);
+            for (int64_t p = 0; p < L; ++p) {
                 double pre = bias ? bias[d] : 0.0;
-                for (int32_t k = 0; k < W; ++k) {
-                    if (t - k < start) break;
-                    pre += w[(int64_t)d * W + (W - 1 - k)] * x[(t - k) * D + d];
-                }
-                u[t * D + d] = apply_silu ? silu(pre) : pre;
+                for (int32_t k = 0; k < W; ++k) pre += w[(int64_t)d * W + (W - 1 - k)] * xe[W - 1 + p - k];
+                u[(start + p) * D + d] = apply_silu ? silu(pre) : pre;
             }
+            if (x_last)
+                for (int32_t j = 0; j < W - 1; ++j) x_last[((int64_t)s * D + d) * (W - 1) + j] = xe[L + j];
         }
     }
+    free(xe);
     return ORACLE_OK;
 }
 
-/* Reverse-mode adjoint of oracle_conv1d_fwd, per sequence.  Gradients are
- * written (not accumulated): dx over the channel range, dw and dbias rows
- * d_begin..d_end-1.  The reverse early stop of the article (read the
- * position of the token conv_width-1 places later) is the same condition as
- * the forward one seen from the other end: x[t-k] feeds pre[t] only if t-k is
- * in t's sequence.                                                          */
+/* Reverse-mode adjoint of oracle_conv1d_fwd, per sequence, on the same
+ * extended inputs xe.  Gradients are written (not accumulated): dx over the
+ * channel range, dw and dbias rows d_begin..d_end-1, and (nullable) dx_init,
+ * the gradient reaching each sequence's tail values.  dx_last (nullable,
+ * (num_seqs, D, W-1)) is the gradient reaching each sequence's x_last from
+ * outside; it adds to the xe entries x_last was read from.  The reverse early
+ * stop of the article (read the position of the token conv_width-1 places
+ * later) is the same condition seen from the other end: xe[q] feeds pre[p]
+ * only when p is a token of q's own sequence.                              */
 int oracle_conv1d_bwd(const double* x, const double* w, const double* bias, const double* du,
                       const int32_t* cu, int32_t num_seqs, int64_t T, int32_t D, int32_t W,
-                      int32_t apply_silu, int32_t d_begin, int32_t d_end,
-                      double* dx, double* dw, double* dbias) {
+                      int32_t apply_silu, int32_t d_begin, int32_t d_end, const double* x_init,
+                      const double* dx_last, double* dx, double* dw, double* dbias, double* dx_init) {
     if (check_cu(cu, num_seqs, T) != ORACLE_OK) return ORACLE_ERR_CU;
+    int64_t max_len = 0;
+    for (int32_t s = 0; s < num_seqs; ++s)
+        if (cu[s + 1] - cu[s] > max_len) max_len = cu[s + 1] - cu[s];
+    const size_t ne = (size_t)(W - 1 + max_len + 1);
+    double* xe = (double*)malloc(sizeof(double) * ne);
+    double* dxe = (double*)malloc(sizeof(double) * ne);
+    if (!xe || !dxe) {
+        free(xe); free(dxe);
+        return ORACLE_ERR_ALLOC;
+    }
     for (int32_t d = d_begin; d < d_end; ++d) {
         for (int32_t k = 0; k < W; ++k) dw[(int64_t)d * W + k] = 0.0;
         if (dbias) dbias[d] = 0.0;
         for (int64_t t = 0; t < T; ++t) dx[t * D + d] = 0.0;
     }
     for (int32_t s = 0; s < num_seqs; ++s) {
-        const int64_t start = cu[s], end = cu[s + 1];
+        const int64_t start = cu[s], L = cu[s + 1] - cu[s];
         for (int32_t d = d_begin; d < d_end; ++d) {
-            for (int64_t t = start; t < end; ++t) {
+            fill_tail(xe, x, x_init, s, start, L, d, D, W);
+            for (size_t i = 0; i < (size_t)(W - 1 + L); ++i) dxe[i] = 0.0;
+            if (dx_last)
+                for (int32_t j = 0; j < W - 1; ++j) dxe[L + j] += dx_last[((int64_t)s * D + d) * (W - 1) + j];
+            for (int64_t p = 0; p < L; ++p) {
                 double pre = bias ? bias[d] : 0.0;
-                for (int32_t k = 0; k < W; ++k) {
-                    if (t - k < start) break;
-                    pre += w[(int64_t)d * W + (W - 1 - k)] * x[(t - k) * D + d];
-                }
-                const double gpre = apply_silu ? du[t * D + d] * silu_grad(pre) : du[t * D + d];
+                for (int32_t k = 0; k < W; ++k) pre += w[(int64_t)d * W + (W - 1 - k)] * xe[W - 1 + p - k];
+                const double gpre = apply_silu ? du[(start + p) * D + d] * silu_grad(pre) : du[(start + p) * D + d];
                 if (dbias) dbias[d] += gpre;
                 for (int32_t k = 0; k < W; ++k) {
-                    if (t - k < start) break;
-                    dw[(int64_t)d * W + (W - 1 - k)] += gpre * x[(t - k) * D + d];
-                    dx[(t - k) * D + d] += w[(int64_t)d * W + (W - 1 - k)] * gpre;
+                    dw[(int64_t)d * W + (W - 1 - k)] += gpre * xe[W - 1 + p - k];
+                    dxe[W - 1 + p - k] += w[(int64_t)d * W + (W - 1 - k)] * gpre;
                 }
             }
+            for (int64_t p = 0; p < L; ++p) dx[(start + p) * D + d] = dxe[W - 1 + p];
+            if (dx_init)
+                for (int32_t j = 0; j < W - 1; ++j) dx_init[((int64_t)s * D + d) * (W - 1) + j] = dxe[j];
         }
     }
+    free(xe); free(dxe);
     return ORACLE_OK;
 }
 

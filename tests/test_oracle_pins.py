@@ -475,6 +475,60 @@ def test_a_log_gradient_is_dA_times_A():
     _fd_check(f, {"a_log": a_log}, {"a_log": g["dA"] * v["A"]})
 
 
+# ---------------------------------------------------------------- conv tails (the conv half of a cut sequence)
+
+def test_conv_bwd_finite_differences_with_tails():
+    # loss = sum(u * g) + sum(x_last * dx_last); the pack has a sequence shorter than W-1,
+    # so its x_last reaches back into its own tail values
+    rng = _rng(46)
+    v = _rand_pack(rng, [4, 2, 3, 7], D=3, N=2)
+    W = v["w"].shape[1]
+    x0 = rng.standard_normal((4, 3, W - 1))
+    dxl = rng.standard_normal((4, 3, W - 1))
+    g = rng.standard_normal(v["x"].shape)
+    dx, dw, db, dxi = oracle.conv1d_bwd(v["x"], v["w"], v["b"], g, v["cu"], x_init=x0, dx_last=dxl,
+                                        return_dx_init=True)
+
+    def f():
+        u, xl = oracle.conv1d_fwd(v["x"], v["w"], v["b"], v["cu"], x_init=x0, return_last=True)
+        return float(np.sum(u * g) + np.sum(xl * dxl))
+
+    _fd_check(f, {"x": v["x"], "w": v["w"], "b": v["b"], "x0": x0},
+              {"x": dx, "w": dw, "b": db, "x0": dxi})
+
+
+def test_a_cut_sequence_that_passes_its_conv_tail_equals_the_whole_sequence():
+    rng = _rng(47)
+    L, L1 = 23, 9
+    v = _rand_pack(rng, [L], D=4, N=2)
+    one = lambda n: np.array([0, n], np.int32)  # noqa: E731
+    g = rng.standard_normal(v["x"].shape)
+    uw = oracle.conv1d_fwd(v["x"], v["w"], v["b"], v["cu"])
+    dxw, dww, dbw = oracle.conv1d_bwd(v["x"], v["w"], v["b"], g, v["cu"])
+    u1, xl1 = oracle.conv1d_fwd(v["x"][:L1], v["w"], v["b"], one(L1), return_last=True)
+    u2 = oracle.conv1d_fwd(v["x"][L1:], v["w"], v["b"], one(L - L1), x_init=xl1)
+    np.testing.assert_allclose(np.concatenate([u1, u2]), uw, rtol=1e-13, atol=1e-13)
+    dx2, dw2, db2, dxi2 = oracle.conv1d_bwd(v["x"][L1:], v["w"], v["b"], g[L1:], one(L - L1), x_init=xl1,
+                                            return_dx_init=True)
+    dx1, dw1, db1 = oracle.conv1d_bwd(v["x"][:L1], v["w"], v["b"], g[:L1], one(L1), dx_last=dxi2)
+    np.testing.assert_allclose(np.concatenate([dx1, dx2]), dxw, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw1 + dw2, dww, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(db1 + db2, dbw, rtol=1e-12, atol=1e-12)
+
+
+def test_an_empty_sequence_passes_its_conv_tail_and_gradient_through():
+    rng = _rng(48)
+    v = _rand_pack(rng, [3, 0, 4], D=2, N=2)
+    W = v["w"].shape[1]
+    x0 = rng.standard_normal((3, 2, W - 1))
+    dxl = rng.standard_normal((3, 2, W - 1))
+    _, xl = oracle.conv1d_fwd(v["x"], v["w"], v["b"], v["cu"], x_init=x0, return_last=True)
+    np.testing.assert_array_equal(xl[1], x0[1])
+    *_, dxi = oracle.conv1d_bwd(v["x"], v["w"], v["b"], v["dout"], v["cu"], x_init=x0, dx_last=dxl,
+                                return_dx_init=True)
+    np.testing.assert_array_equal(dxi[1], dxl[1])
+
+
 # ---------------------------------------------------------------- threaded helpers
 
 def test_threaded_helpers_match_single_call():
