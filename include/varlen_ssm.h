@@ -107,13 +107,21 @@ int vssm_status_code(int32_t status_word);
  *   pre[t,d] = bias[d] + sum_{k=0}^{W-1} [pos[t] >= k] weight[d][W-1-k] x[t-k,d]
  *   u[t,d]   = apply_silu ? pre * sigmoid(pre) : pre
  * x, u: (T, D) io; weight: (D, W) f32; bias: (D) f32, nullable (zero).
+ * Conv tails of cut sequences (the conv half of the article's future work:
+ * a sequence cut across packs keeps passing data), both nullable f32
+ * (num_seqs, D, W-1), entry [s][d][j]:
+ *   x_init: the W-1 inputs before each sequence's first token (the previous
+ *     part's x_last); a tap that reaches before the start reads them instead
+ *     of stopping (zero when NULL: the plain early stop);
+ *   x_last: receives each sequence's last W-1 inputs, reaching back into its
+ *     x_init when the sequence is shorter than W-1.
  */
 size_t varlen_conv1d_fwd_workspace_size(int64_t total_tokens, int32_t D, int32_t W);
 int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
                       const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
                       int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
-                      vssm_dtype dtype, void* u, void* workspace, size_t workspace_bytes,
-                      void* stream);
+                      vssm_dtype dtype, void* u, const float* x_init, float* x_last,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward (same section: the backward pass stops dx and dweight at sequence
  * edges too, reading the position W-1 tokens LATER to know where a sequence
@@ -123,12 +131,17 @@ int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
  *   dbias[d]       = sum_t g[t,d]
  * x, du, dx: (T, D) io; dweight (D, W) f32; dbias (D) f32, nullable.  The
  * reductions over tokens run in a fixed order (bitwise repeatable).
+ * x_init: the forward call's (nullable).  dx_last: nullable (num_seqs, D,
+ * W-1), the gradient reaching each sequence's x_last from outside.  dx_init:
+ * nullable (num_seqs, D, W-1), receives the gradient reaching each sequence's
+ * x_init.
  */
 size_t varlen_conv1d_bwd_workspace_size(int64_t total_tokens, int32_t D, int32_t W);
 int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, const void* du,
                       const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
                       int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
                       vssm_dtype dtype, void* dx, float* dweight, float* dbias,
+                      const float* x_init, const float* dx_last, float* dx_init,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------ SSM_pack

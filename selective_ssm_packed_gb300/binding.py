@@ -33,10 +33,10 @@ SIGNATURES = {
     "vssm_status_code": (ctypes.c_int, [_i32]),
     "varlen_conv1d_fwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_conv1d_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
-                                         ctypes.c_int, _vp, _vp, _sz, _vp]),
+                                         ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
     "varlen_conv1d_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_conv1d_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
-                                         ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
+                                         ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "varlen_selective_scan_fwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_chunk_states_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
@@ -173,36 +173,56 @@ def conv1d_bwd_workspace_size(T, D, W):
 
 
 def varlen_conv1d_fwd(x, weight, bias, cu_seqlens, position_indices=None, apply_silu=True,
-                      out=None, workspace=None, stream=None):
+                      out=None, workspace=None, stream=None, x_init=None, x_last=None):
+    """Returns u, or (u, x_last) when x_last is asked for (True allocates,
+    a tensor is filled).  x_init: (S, D, W-1) f32 inputs before each sequence
+    (a cut sequence's previous part's x_last); None: the plain early stop."""
     T, D = x.shape
     W = weight.shape[1]
     out = torch.empty_like(x) if out is None else out
+    want_last = x_last is not None and x_last is not False
+    if x_last is True:
+        x_last = torch.empty((cu_seqlens.numel() - 1, D, W - 1), dtype=torch.float32, device=x.device)
+    elif x_last is False:
+        x_last = None
     ws = _ws(workspace, conv1d_fwd_workspace_size(T, D, W), x.device)
     _check(lib().varlen_conv1d_fwd(
         _ptr(x, "x"), _ptr(weight, "weight", torch.float32), _ptr(bias, "bias", torch.float32),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
         cu_seqlens.numel() - 1, T, D, W, int(bool(apply_silu)), _dt(x), _ptr(out, "out", x.dtype),
+        _ptr(x_init, "x_init", torch.float32), _ptr(x_last, "x_last", torch.float32),
         _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_conv1d_fwd")
-    return out
+    return (out, x_last) if want_last else out
 
 
 def varlen_conv1d_bwd(x, weight, bias, du, cu_seqlens, position_indices=None, apply_silu=True,
-                      dx=None, dweight=None, dbias=None, workspace=None, stream=None):
+                      dx=None, dweight=None, dbias=None, workspace=None, stream=None, x_init=None,
+                      dx_last=None, dx_init=None):
+    """Returns (dx, dweight, dbias), and dx_init last when it is asked for
+    (True allocates, a tensor is filled).  x_init: the forward call's;
+    dx_last: (S, D, W-1) gradient reaching each sequence's x_last."""
     T, D = x.shape
     W = weight.shape[1]
     dx = torch.empty_like(x) if dx is None else dx
     dweight = torch.empty_like(weight) if dweight is None else dweight
     if dbias is None and bias is not None:
         dbias = torch.empty_like(bias)
+    want_init = dx_init is not None and dx_init is not False
+    if dx_init is True:
+        dx_init = torch.empty((cu_seqlens.numel() - 1, D, W - 1), dtype=torch.float32, device=x.device)
+    elif dx_init is False:
+        dx_init = None
     ws = _ws(workspace, conv1d_bwd_workspace_size(T, D, W), x.device)
     _check(lib().varlen_conv1d_bwd(
         _ptr(x, "x"), _ptr(weight, "weight", torch.float32), _ptr(bias, "bias", torch.float32),
         _ptr(du, "du", x.dtype), _ptr(cu_seqlens, "cu_seqlens", torch.int32),
         _ptr(position_indices, "position_indices", torch.int32), cu_seqlens.numel() - 1, T, D, W,
         int(bool(apply_silu)), _dt(x), _ptr(dx, "dx", x.dtype), _ptr(dweight, "dweight", torch.float32),
-        _ptr(dbias, "dbias", torch.float32), _ptr(ws, "workspace"), ws.numel(), _stream(stream)),
+        _ptr(dbias, "dbias", torch.float32), _ptr(x_init, "x_init", torch.float32),
+        _ptr(dx_last, "dx_last", torch.float32), _ptr(dx_init, "dx_init", torch.float32),
+        _ptr(ws, "workspace"), ws.numel(), _stream(stream)),
         "varlen_conv1d_bwd")
-    return dx, dweight, dbias
+    return (dx, dweight, dbias, dx_init) if want_init else (dx, dweight, dbias)
 
 
 # ------------------------------------------------------------------ selective scan

@@ -90,6 +90,8 @@ Layout conv_layout(int64_t T, int D, int W, bool bwd) {
   l.clear_bytes = off;
   l.pos = off;
   off += up(sizeof(int32_t) * (size_t)T);
+  l.seq = off;
+  off += up(sizeof(int32_t) * (size_t)T);
   if (bwd) {
     l.conv_part = off;
     off += up(sizeof(float) * (size_t)conv_bwd_partial_rows(T) * D * (W + 1));
@@ -282,22 +284,34 @@ static int conv_common(const void* x, const float* weight, const int32_t* cu, in
 int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
                       const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
                       int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
-                      vssm_dtype dtype, void* u, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      vssm_dtype dtype, void* u, const float* x_init, float* x_last,
+                      void* workspace, size_t workspace_bytes, void* stream) {
   IO io;
   VSSM_TRY(conv_common(x, weight, cu_seqlens, num_seqs, total_tokens, D, W, dtype, &io));
   VSSM_TRY(check_io(u, "u", total_tokens));
+  VSSM_TRY(check_states(x_init, "x_init"));
+  VSSM_TRY(check_states(x_last, "x_last"));
   const Layout l = conv_layout(total_tokens, D, W, false);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  ConvArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.out = u;
+  a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
+  a.cu = cu_seqlens; a.num_seqs = num_seqs; a.x_init = W > 1 ? x_init : nullptr; a.x_last = x_last;
+  // every sequence's last W-1 inputs (its tail values when it is shorter)
+  e = launch_conv_tails(a, io, false, st);
+  if (e != cudaSuccess) return cuda_fail(e, "conv tails launch");
   if (total_tokens == 0) return VSSM_OK;
   const int32_t* pos = nullptr;
   VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, total_tokens, workspace, l, st, &pos));
-  ConvArgs a{};
-  a.x = x; a.w = weight; a.bias = bias; a.pos = pos; a.out = u;
-  a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
+  a.pos = pos;
+  if (a.x_init) {
+    e = launch_sequence_index(cu_seqlens, num_seqs, total_tokens, at<int32_t>(workspace, l.seq), st);
+    if (e != cudaSuccess) return cuda_fail(e, "sequence index launch");
+    a.seq = at<int32_t>(workspace, l.seq);
+  }
   const int bx = D < conv_tile_cols() ? D : conv_tile_cols();
   CUtensorMap mx;
   VSSM_TRY(make_map(&mx, x, io, total_tokens, D, bx, conv_tile_rows(W, false, true)));
@@ -309,12 +323,16 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
                       const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
                       int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
                       vssm_dtype dtype, void* dx, float* dweight, float* dbias,
+                      const float* x_init, const float* dx_last, float* dx_init,
                       void* workspace, size_t workspace_bytes, void* stream) {
   IO io;
   VSSM_TRY(conv_common(x, weight, cu_seqlens, num_seqs, total_tokens, D, W, dtype, &io));
   VSSM_TRY(check_io(du, "du", total_tokens));
   VSSM_TRY(check_io(dx, "dx", total_tokens));
   if (!dweight) return fail(VSSM_ERR_ARG, "dweight is NULL");
+  VSSM_TRY(check_states(x_init, "x_init"));
+  VSSM_TRY(check_states(dx_last, "dx_last"));
+  VSSM_TRY(check_states(dx_init, "dx_init"));
   const Layout l = conv_layout(total_tokens, D, W, true);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -327,6 +345,16 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
   a.x = x; a.w = weight; a.bias = bias; a.pos = pos; a.du = du; a.out = dx;
   a.partial = at<float>(workspace, l.conv_part);
   a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
+  a.cu = cu_seqlens; a.num_seqs = num_seqs;
+  if (W > 1) { a.x_init = x_init; a.dx_last = dx_last; a.dx_init = dx_init; }
+  if (total_tokens > 0 && (a.x_init || a.dx_last)) {
+    e = launch_sequence_index(cu_seqlens, num_seqs, total_tokens, at<int32_t>(workspace, l.seq), st);
+    if (e != cudaSuccess) return cuda_fail(e, "sequence index launch");
+    a.seq = at<int32_t>(workspace, l.seq);
+  }
+  // the gradient reaching every sequence's tail values
+  e = launch_conv_tails(a, io, true, st);
+  if (e != cudaSuccess) return cuda_fail(e, "conv tails launch");
   CUtensorMap mx, mdu;
   std::memset(&mx, 0, sizeof(mx));
   std::memset(&mdu, 0, sizeof(mdu));

@@ -85,7 +85,9 @@ struct ConvTileSmem {
 };
 
 // Forward: u[t] = SiLU(bias + sum_k w[W-1-k] x[t-k] [pos[t] >= k]) for the tile.
-template <typename T, int W>
+// kTail: the call passes tail values (x_init) for the first W-1 tokens of a
+// sequence; without them the kernel carries no code for them.
+template <typename T, int W, bool kTail>
 __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                             ConvArgs a) {
   using SM = ConvTileSmem<T, W>;
@@ -131,13 +133,20 @@ __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_cons
     const int tl = kTokPerWarp * wp + j;
     lds4<T>(sm.x() + (tl + W - 1) * bx + c, xw[W - 1]);
     const int p = sm.pos[tl];
+    // a tap reaching before the sequence start reads the sequence's tail value
+    const float* trow = nullptr;
+    if constexpr (kTail) {
+      if (p < W - 1 && t0 + tl < a.T) trow = a.x_init + ((int64_t)a.seq[t0 + tl] * a.D + c0 + c) * (W - 1);
+    }
     float o[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       float pre = fmaf(w[W - 1][v], xw[W - 1][v], bb[v]);
 #pragma unroll
-      for (int k = 1; k < W; ++k)
+      for (int k = 1; k < W; ++k) {
         if (p >= k) pre = fmaf(w[W - 1 - k][v], xw[W - 1 - k][v], pre);
+        else if (kTail && trow) pre = fmaf(w[W - 1 - k][v], __ldg(trow + v * (W - 1) + W - 1 + p - k), pre);
+      }
       o[v] = a.apply_silu ? siluf(pre) : pre;
     }
     if (t0 + tl < a.T) stg4<T>(u + (t0 + tl) * (int64_t)a.D + c0 + c, o);
@@ -153,7 +162,10 @@ __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_cons
 // dbias partials of the tile's own tokens, summed over the 8 warps in a fixed
 // order into one partial row per tile row.  A warp's lanes share their token,
 // so every mask is warp-uniform; the 4 channels of a lane run as 2 packed pairs.
-template <typename T, int W>
+// kTail: the call passes tail values (x_init) and/or gradients reaching
+// sequences' last W-1 inputs (dx_last); without them the kernel carries no
+// code for them.
+template <typename T, int W, bool kTail>
 __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                                const __grid_constant__ CUtensorMap tm_du,
                                                                ConvArgs a) {
@@ -226,12 +238,24 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
       lds4<T>(sm.du() + tl * bx + c, dv);
       const int p = sm.pos[tl];
       pw[W - 1] = p;
+      // taps reaching before the sequence start read the sequence's tail values
+      const float* trow = nullptr;
+      if constexpr (kTail) {
+        if (a.x_init && p < W - 1 && t0 + tl < a.T)
+          trow = a.x_init + ((int64_t)a.seq[t0 + tl] * a.D + c0 + c) * (W - 1);
+      }
+      auto tail2 = [&](int h, int k) {  // the tail pair for tap k (k > p) of channels c+2h, c+2h+1
+        return make_float2(__ldg(trow + (2 * h) * (W - 1) + W - 1 + p - k),
+                           __ldg(trow + (2 * h + 1) * (W - 1) + W - 1 + p - k));
+      };
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float2 pre = fma2(w[W - 1][h], xw[W - 1][h], bb[h]);
 #pragma unroll
-        for (int k = 1; k < W; ++k)
+        for (int k = 1; k < W; ++k) {
           if (p >= k) pre = fma2(w[W - 1 - k][h], xw[W - 1 - k][h], pre);
+          else if (kTail && trow) pre = fma2(w[W - 1 - k][h], tail2(h, k), pre);
+        }
         // rows past T are zero-filled, so g = 0 there
         const float2 dv2 = make_float2(dv[2 * h], dv[2 * h + 1]);
         const float2 g = a.apply_silu ? mul2(dv2, make_float2(silu_grad(pre.x), silu_grad(pre.y))) : dv2;
@@ -239,8 +263,10 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
         if (j < kTokPerWarp) {
           db[h] = __fadd2_rn(db[h], g);
 #pragma unroll
-          for (int k = 0; k < W; ++k)
+          for (int k = 0; k < W; ++k) {
             if (p >= k) dw[W - 1 - k][h] = fma2(g, xw[W - 1 - k][h], dw[W - 1 - k][h]);
+            else if (kTail && trow) dw[W - 1 - k][h] = fma2(g, tail2(h, k), dw[W - 1 - k][h]);
+          }
         }
       }
       if (j >= W - 1) {  // dx of token tl - (W-1), which now has g[t .. t+W-1]
@@ -253,6 +279,22 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
             if (pw[k] >= k)
 #pragma unroll
               for (int h = 0; h < 2; ++h) acc[h] = fma2(w[W - 1 - k][h], gw[k][h], acc[h]);
+          if constexpr (kTail) {
+            // token t is W-1-ke from its sequence's end when token t+ke is the next
+            // start (or past T, where pos is 0): the gradient reaching the
+            // sequence's last W-1 inputs from outside adds to its own
+            if (a.dx_last) {
+              int ke = 0;
+#pragma unroll
+              for (int k = W - 1; k >= 1; --k)
+                if (pw[k] == 0) ke = k;
+              if (ke) {
+                const float* drow = a.dx_last + ((int64_t)a.seq[t] * a.D + c0 + c) * (W - 1) + W - 1 - ke;
+                acc[0] = __fadd2_rn(acc[0], make_float2(__ldg(drow), __ldg(drow + (W - 1))));
+                acc[1] = __fadd2_rn(acc[1], make_float2(__ldg(drow + 2 * (W - 1)), __ldg(drow + 3 * (W - 1))));
+              }
+            }
+          }
           const float o[4] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y};
           stg4<T>(dx + t * (int64_t)a.D + c0 + c, o);
         }
@@ -292,31 +334,43 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
   }
 }
 
-template <typename T, int W>
-cudaError_t fwd_tile_w(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t st) {
+template <typename T, int W, bool kTail>
+cudaError_t fwd_tile_k(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t st) {
   const size_t smem = sizeof(ConvTileSmem<T, W>);
-  cudaError_t e = cudaFuncSetAttribute(conv_fwd_tile_kernel<T, W>,
+  cudaError_t e = cudaFuncSetAttribute(conv_fwd_tile_kernel<T, W, kTail>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t cols = (a.D + kCC - 1) / kCC;
   const int64_t rows = (a.T + kCT - 1) / kCT;
   if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
-  conv_fwd_tile_kernel<T, W><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, a);
+  conv_fwd_tile_kernel<T, W, kTail><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, a);
+  return cudaGetLastError();
+}
+
+template <typename T, int W>
+cudaError_t fwd_tile_w(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t st) {
+  return a.x_init ? fwd_tile_k<T, W, true>(a, tm_x, st) : fwd_tile_k<T, W, false>(a, tm_x, st);
+}
+
+template <typename T, int W, bool kTail>
+cudaError_t bwd_tile_k(const ConvArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
+                       cudaStream_t st) {
+  const size_t smem = sizeof(ConvTileSmem<T, W>);
+  cudaError_t e = cudaFuncSetAttribute(conv_bwd_tile_kernel<T, W, kTail>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t cols = (a.D + kCC - 1) / kCC;
+  const int64_t rows = (a.T + kCT - 1) / kCT;
+  if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
+  conv_bwd_tile_kernel<T, W, kTail><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, tm_du, a);
   return cudaGetLastError();
 }
 
 template <typename T, int W>
 cudaError_t bwd_tile_w(const ConvArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
                        cudaStream_t st) {
-  const size_t smem = sizeof(ConvTileSmem<T, W>);
-  cudaError_t e = cudaFuncSetAttribute(conv_bwd_tile_kernel<T, W>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const int64_t cols = (a.D + kCC - 1) / kCC;
-  const int64_t rows = (a.T + kCT - 1) / kCT;
-  if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
-  conv_bwd_tile_kernel<T, W><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, tm_du, a);
-  return cudaGetLastError();
+  return (a.x_init || a.dx_last) ? bwd_tile_k<T, W, true>(a, tm_x, tm_du, st)
+                                 : bwd_tile_k<T, W, false>(a, tm_x, tm_du, st);
 }
 
 template <typename T>
@@ -342,6 +396,58 @@ cudaError_t bwd_t(const ConvArgs& a, const CUtensorMap& tm_x, const CUtensorMap&
 }
 
 }  // namespace
+
+// Conv tails of cut sequences, one block per sequence s (tokens [cu[s],
+// cu[s+1]), length L), threads over channels.  With xe the sequence's inputs
+// preceded by its tail values (x_init, or zeros):
+//   forward:  x_last[s][d][j] = xe[L - (W-1) + j], the tail the sequence's
+//             next part starts from;
+//   backward: dx_init[s][d][j] = the gradient reaching xe[j - (W-1)]: the
+//             taps of the first W-1 tokens that read it (their g recomputed
+//             from x, x_init, the weights and du) plus, for a sequence shorter
+//             than W-1, the part of dx_last that lands there.
+// The tile kernels handle everything that touches the real tokens.
+template <typename T>
+__global__ void __launch_bounds__(256) conv_tail_kernel(ConvArgs a, int bwd) {
+  const int s = blockIdx.x;
+  const int W = a.W;
+  const int64_t start = a.cu[s], L = (int64_t)a.cu[s + 1] - start;
+  const T* x = static_cast<const T*>(a.x);
+  auto xe = [&](int64_t q, int d) {  // q = position in the sequence, from -(W-1)
+    if (q >= 0) return to_f(x[(start + q) * a.D + d]);
+    return a.x_init ? a.x_init[((int64_t)s * a.D + d) * (W - 1) + (W - 1) + q] : 0.0f;
+  };
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    const int64_t row = ((int64_t)s * a.D + d) * (W - 1);
+    if (!bwd) {
+      for (int j = 0; j < W - 1; ++j) a.x_last[row + j] = xe(L - (W - 1) + j, d);
+      continue;
+    }
+    float acc[3] = {0.0f, 0.0f, 0.0f};  // dxe[q] for q = -(W-1) .. -1, W <= 4
+    const T* du = static_cast<const T*>(a.du);
+    for (int64_t p = 0; p < L && p < W - 1; ++p) {
+      float pre = a.bias ? a.bias[d] : 0.0f;
+      for (int k = 0; k < W; ++k) pre = fmaf(a.w[(int64_t)d * W + (W - 1 - k)], xe(p - k, d), pre);
+      const float gu = to_f(du[(start + p) * a.D + d]);
+      const float g = a.apply_silu ? gu * silu_grad(pre) : gu;
+      for (int k = p + 1; k < W; ++k)  // taps reaching q = p - k < 0
+        acc[W - 1 + p - k] = fmaf(a.w[(int64_t)d * W + (W - 1 - k)], g, acc[W - 1 + p - k]);
+    }
+    if (a.dx_last)
+      for (int j = 0; j < W - 1; ++j) {  // x_last[j] was read from xe[L - (W-1) + j]
+        const int64_t q = L - (W - 1) + j;
+        if (q < 0) acc[W - 1 + q] += a.dx_last[row + j];
+      }
+    for (int j = 0; j < W - 1; ++j) a.dx_init[row + j] = acc[j];
+  }
+}
+
+cudaError_t launch_conv_tails(const ConvArgs& a, IO io, bool bwd, cudaStream_t st) {
+  if ((bwd ? (void*)a.dx_init : (void*)a.x_last) == nullptr || a.num_seqs <= 0 || a.W < 2) return cudaSuccess;
+  if (io == IO::F32) conv_tail_kernel<float><<<(unsigned)a.num_seqs, 256, 0, st>>>(a, bwd ? 1 : 0);
+  else conv_tail_kernel<__nv_bfloat16><<<(unsigned)a.num_seqs, 256, 0, st>>>(a, bwd ? 1 : 0);
+  return cudaGetLastError();
+}
 
 int64_t conv_bwd_partial_rows(int64_t T) {
   const int64_t per = kCT;

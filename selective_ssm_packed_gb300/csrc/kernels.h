@@ -36,10 +36,21 @@ struct ConvArgs {
   const void* du;      // bwd only
   void* out;           // fwd: u; bwd: dx
   float* partial;      // bwd: [rows_of_ctas][D*W + D]
+  // conv tails of cut sequences, (num_seqs, D, W-1) f32, all nullable: the
+  // W-1 inputs before each sequence (x_init), its last W-1 inputs (x_last,
+  // fwd), and their gradients (dx_last in, dx_init out, bwd); seq[t] is the
+  // sequence of token t (set whenever one of them is given)
+  const int32_t* seq;
+  const float* x_init;
+  float* x_last;
+  const float* dx_last;
+  float* dx_init;
   int64_t T;
   int D;
   int W;
   int apply_silu;
+  int num_seqs;
+  const int32_t* cu;
 };
 // Number of token-rows of CTAs the backward kernel uses (partial buffer rows).
 int64_t conv_bwd_partial_rows(int64_t T);
@@ -49,6 +60,8 @@ int conv_tile_cols();
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x, cudaStream_t st);
 cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
                               float* dweight, float* dbias, cudaStream_t st);
+// x_last (fwd) or dx_init (bwd) of every sequence, one block per sequence.
+cudaError_t launch_conv_tails(const ConvArgs& a, IO io, bool bwd, cudaStream_t st);
 
 // ---------------------------------------------------------------- selective scan
 constexpr int kFwdChunk = 128;   // tokens per forward work item (look-back granule)

@@ -61,10 +61,11 @@ def test_strerror_and_status_codes(lib):
 
 def _conv_fwd(lib, **kw):
     a = dict(x=16, weight=16, bias=None, cu=16, pos=None, S=1, T=16, D=8, W=4, silu=1, dt=0,
-             u=16, ws=16, wsb=1 << 20, st=None)
+             u=16, x_init=None, x_last=None, ws=16, wsb=1 << 20, st=None)
     a.update(kw)
     return lib.varlen_conv1d_fwd(a["x"], a["weight"], a["bias"], a["cu"], a["pos"], a["S"], a["T"],
-                                 a["D"], a["W"], a["silu"], a["dt"], a["u"], a["ws"], a["wsb"], a["st"])
+                                 a["D"], a["W"], a["silu"], a["dt"], a["u"], a["x_init"], a["x_last"],
+                                 a["ws"], a["wsb"], a["st"])
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -75,6 +76,7 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _conv_fwd(lib, D=6) == -3            # 6 * 4 bytes is not a multiple of 16
     assert _conv_fwd(lib, dt=1, D=4) == -3       # 4 * 2 bytes
     assert _conv_fwd(lib, x=8) == -3             # misaligned pointer
+    assert _conv_fwd(lib, x_init=8) == -3        # misaligned tail array
     assert _conv_fwd(lib, cu=None) == -1
     assert _conv_fwd(lib, wsb=16) == -4
     assert "workspace" in binding.last_error()

@@ -329,6 +329,60 @@ def test_a_cut_sequence_passes_its_state_on_gpu():
     assert_close("d_initial_states", g_1["d_initial_states"], host(g_w["d_initial_states"]), tol)
 
 
+@pytest.mark.parametrize("W,dtype", [(4, "f32"), (4, "bf16"), (2, "f32")])
+def test_conv_tails_fwd_bwd(W, dtype):
+    """Conv tails of cut sequences: x_init read by the taps that reach before
+    a sequence's start, x_last out, and their gradients.  Lengths shorter
+    than W-1, an empty sequence, and starts on and next to the 64-token tile
+    edges."""
+    lengths = [64, 1, 2, 0, 61, 3, 130, 40]
+    D = 136
+    cu_np, T, r = rand_case(lengths, D, 4, dtype, seed=34, W=W)
+    S = len(lengths)
+    rng = np.random.default_rng(35)
+    x0 = rng.standard_normal((S, D, W - 1)).astype(np.float32)
+    dxl = rng.standard_normal((S, D, W - 1)).astype(np.float32)
+    if dtype == "bf16":  # tail values are inputs like x: give them bf16-exact values
+        x0 = torch.from_numpy(x0).to(torch.bfloat16).float().numpy()
+    cu = torch.from_numpy(cu_np).cuda()
+    x = dev(r["x"], dtype)
+    w, b = f32(r["conv_w"]), f32(r["conv_b"])
+    u, xl = vs.varlen_conv1d_fwd(x, w, b, cu, x_init=f32(x0), x_last=True)
+    g = dev(r["dout"], dtype)
+    dx, dw, db, dxi = vs.varlen_conv1d_bwd(x, w, b, g, cu, x_init=f32(x0), dx_last=f32(dxl), dx_init=True)
+    torch.cuda.synchronize()
+    tol = TOL[dtype]
+    u_ref, xl_ref = oracle.conv1d_fwd(r["x"], r["conv_w"], r["conv_b"], cu_np, x_init=x0, return_last=True)
+    assert_close("u", u, u_ref, tol)
+    assert np.array_equal(host(xl), xl_ref)  # plain copies of inputs
+    ref = oracle.conv1d_bwd(r["x"], r["conv_w"], r["conv_b"], host(g), cu_np, x_init=x0, dx_last=dxl,
+                            return_dx_init=True)
+    for name, got, want in zip(("dx", "dweight", "dbias", "dx_init"), (dx, dw, db, dxi), ref):
+        assert_close(name, got, want, tol)
+
+
+def test_a_cut_sequence_passes_its_conv_tail_on_gpu():
+    L, L1, D = 700, 333, 96
+    cu_np, T, r = rand_case([L], D, 4, "f32", seed=36)
+    w, b = f32(r["conv_w"]), f32(r["conv_b"])
+    one = lambda n: torch.tensor([0, n], dtype=torch.int32, device="cuda")  # noqa: E731
+    x, g = f32(r["x"]), f32(r["dout"])
+    u_w = vs.varlen_conv1d_fwd(x, w, b, one(L))
+    dx_w, dw_w, db_w = vs.varlen_conv1d_bwd(x, w, b, g, one(L))
+    u_1, xl_1 = vs.varlen_conv1d_fwd(x[:L1].contiguous(), w, b, one(L1), x_last=True)
+    u_2 = vs.varlen_conv1d_fwd(x[L1:].contiguous(), w, b, one(L - L1), x_init=xl_1)
+    dx_2, dw_2, db_2, dxi_2 = vs.varlen_conv1d_bwd(x[L1:].contiguous(), w, b, g[L1:].contiguous(), one(L - L1),
+                                                   x_init=xl_1, dx_init=True)
+    dx_1, dw_1, db_1 = vs.varlen_conv1d_bwd(x[:L1].contiguous(), w, b, g[:L1].contiguous(), one(L1),
+                                            dx_last=dxi_2)
+    torch.cuda.synchronize()
+    tol = TOL["f32"]
+    assert_close("u", torch.cat([u_1, u_2]), host(u_w), tol)
+    assert_close("dx", torch.cat([dx_1, dx_2]), host(dx_w), tol)
+    assert_close("dweight", dw_1 + dw_2, host(dw_w), tol)
+    assert_close("dbias", db_1 + db_2, host(db_w), tol)
+
+
 @pytest.mark.parametrize("flags", [dict(z=False), dict(skip=False), dict(bias=False),
                                    dict(softplus=False), dict(z=False, skip=False, bias=False)])
 def test_optional_inputs(flags):
