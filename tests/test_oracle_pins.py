@@ -547,3 +547,35 @@ def test_threaded_helpers_match_single_call():
     for p, q in zip(oracle.conv1d_bwd_threaded(v["x"], v["w"], v["b"], v["dout"], v["cu"], threads=3),
                     oracle.conv1d_bwd(v["x"], v["w"], v["b"], v["dout"], v["cu"])):
         np.testing.assert_array_equal(p, q)
+
+
+# ---------------------------------------------------------------- sequence packing
+
+def test_packing_worked_example():
+    # by hand: sequential seals after 5 (4 does not fit) and after 4+3 (4 does
+    # not fit): 3 packs, 8 of 24 tokens padding; local greedy sorts 5,4,4,3 and
+    # fills 5+3 and 4+4
+    lengths, size = [5, 4, 3, 4], 8
+    seq = oracle.pack_sequential(lengths, size)
+    assert seq == [[0], [1, 2], [3]]
+    assert oracle.padding_rate(lengths, seq, size) == pytest.approx(8 / 24)
+    gr = oracle.pack_local_greedy(lengths, size, window=4)
+    assert gr == [[0, 2], [1, 3]]
+    assert oracle.padding_rate(lengths, gr, size) == 0.0
+
+
+@pytest.mark.parametrize("window", [1, 7, 100, 10000])
+def test_packing_invariants(window):
+    rng = _rng(49)
+    size = 4096
+    lengths = [int(v) for v in np.clip(np.exp(rng.normal(np.log(800), 1.0, 3000)), 1, size)]
+    lengths[10:15] = [0] * 5
+    total = sum(lengths)
+    for packs in (oracle.pack_sequential(lengths, size), oracle.pack_local_greedy(lengths, size, window)):
+        flat = [i for p in packs for i in p]
+        assert sorted(flat) == list(range(len(lengths)))           # every sequence once
+        assert all(sum(lengths[i] for i in p) <= size for p in packs)
+        assert len(packs) >= -(-total // size)                      # capacity lower bound
+    assert [i for p in oracle.pack_sequential(lengths, size) for i in p] == list(range(len(lengths)))
+    if window >= len(lengths):  # first fit decreasing over everything: within 11/9 of the bound, + 1
+        assert len(oracle.pack_local_greedy(lengths, size, window)) <= 11 / 9 * -(-total // size) + 1
