@@ -361,6 +361,17 @@ def comparators(args, torch, vs, binding, device, w, step_sec):
         "padding_rate": 1.0 - T_real / T_pad,
         "config": f"long-tail packs ({len(lengths)} sequences, {T_real} tokens), D={Dc}, N=16, bf16, "
                   f"buckets {list(wls.BUCKETS)}; same kernels, fwd+bwd"}
+    # the packer (host side): arrival-order packing against local greedy on the
+    # bench workload's length mix, as the article compares them
+    rng = np.random.default_rng(14)
+    mix = np.clip(np.exp(rng.normal(np.log(800), 1.0, 20000)), 32, 4096).astype(np.int32)
+    pk = {}
+    for name, method, window in (("sequential", "sequential", 1), ("local_greedy_w1000", "local_greedy", 1000)):
+        t0 = time.perf_counter()
+        packs, pad = binding.pack_sequences(mix, 4096, method, window)
+        pk[name] = {"packs": len(packs), "padding_rate": pad, "ms": (time.perf_counter() - t0) * 1e3}
+    pk["config"] = "20000 lengths LogN(ln 800, 1) clipped [32, 4096], packs of 4096 tokens, host C++"
+    res["packing"] = pk
     return res
 
 

@@ -260,7 +260,30 @@ int varlen_selective_scan_fwd_noalloc(const void* u, const void* delta_raw, cons
                                       const float* initial_states, float* final_states,
                                       int32_t* status, void* stream);
 
-/* ------------------------------------------------------------ status, errors, knobs
+/* ------------------------------------------------------------ packing (host)
+ * The article's section 结论与讨论: its pack method takes sequences in
+ * arrival order and seals a pack when the next sequence does not fit (19.1 %
+ * padding on its pretraining data); sorting a portion of the pending
+ * sequences first and then packing greedily brings that down to 0.46 %.
+ *   VSSM_PACK_SEQUENTIAL: arrival order, sealed when the next does not fit;
+ *   VSSM_PACK_LOCAL_GREEDY: the sequences are taken `window` at a time, each
+ *     window sorted longest first (equal lengths in arrival order) and every
+ *     sequence placed in the first of the window's packs with room for it
+ *     (first fit, decreasing); a window's packs are sealed before the next.
+ * Host arrays, caller-allocated: lengths[num_seqs] (0 .. pack_size);
+ * order[num_seqs] receives the sequence indices pack after pack;
+ * pack_offsets[num_seqs + 1]: pack p holds order[pack_offsets[p] ..
+ * pack_offsets[p+1]); *num_packs; *padding_rate = padded tokens / (num_packs
+ * * pack_size).  Returns VSSM_ERR_ARG for a negative length, a length above
+ * pack_size, a non-positive pack_size or (local greedy) window, an unknown
+ * method, or a NULL array.  Runs on the calling thread; no GPU work.
+ */
+enum { VSSM_PACK_SEQUENTIAL = 0, VSSM_PACK_LOCAL_GREEDY = 1 };
+int varlen_pack_sequences(const int32_t* lengths, int32_t num_seqs, int32_t pack_size, int32_t method,
+                          int32_t window, int32_t* order, int32_t* pack_offsets, int32_t* num_packs,
+                          double* padding_rate);
+
+/* ------------------------------------------------------------ status, errors, knobs/* ------------------------------------------------------------ status, errors, knobs
  * vssm_read_status: synchronises `stream`, reads the status word the last call
  * using `workspace` left there, and stores VSSM_OK or a VSSM_ERR_* code in
  * *status.  Returns VSSM_OK or VSSM_ERR_CUDA / VSSM_ERR_ARG.

@@ -7,6 +7,7 @@ the C entry points' names.
 from .binding import (  # noqa: F401
     VssmError,
     chunk_states_shape,
+    pack_sequences,
     read_status,
     varlen_conv1d_bwd,
     varlen_conv1d_fwd,

@@ -53,6 +53,8 @@ SIGNATURES = {
                                                          ctypes.c_float, _i32,
                                                          _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
                                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "varlen_pack_sequences": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp,
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_double)]),
     "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "vssm_last_error": (ctypes.c_char_p, []),
@@ -330,3 +332,23 @@ def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu
         _ptr(g["dz"], "dz", dt), _ptr(g["d_dt_bias"], "d_dt_bias", torch.float32),
         _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_selective_scan_bwd")
     return g
+
+
+# ------------------------------------------------------------------ packing (host)
+PACK_METHODS = {"sequential": 0, "local_greedy": 1}
+
+
+def pack_sequences(lengths, pack_size, method="local_greedy", window=1000):
+    """Packs sequences of the given lengths into packs of at most pack_size
+    tokens (host work, no GPU).  Returns (packs, padding_rate): packs is a
+    list of int32 arrays of sequence indices, in pack order."""
+    import numpy as np
+    L = np.ascontiguousarray(lengths, dtype=np.int32)
+    n = int(L.size)
+    order = np.empty(max(n, 1), dtype=np.int32)
+    offs = np.empty(n + 1, dtype=np.int32)
+    npk, pad = ctypes.c_int32(0), ctypes.c_double(0.0)
+    _check(lib().varlen_pack_sequences(L.ctypes.data if n else None, n, int(pack_size), PACK_METHODS[method],
+                                       int(window), order.ctypes.data, offs.ctypes.data, ctypes.byref(npk),
+                                       ctypes.byref(pad)), "varlen_pack_sequences")
+    return [order[offs[p]:offs[p + 1]].copy() for p in range(npk.value)], pad.value

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libvarlen_ssm.so")
 PROBE_PATH = os.path.join(BUILD_DIR, "libvssm_probe.so")   # ALU throughput probes (benchmark only)
 
-SOURCES = ["api.cu", "misc.cu", "conv.cu", "scan_fwd.cu", "scan_bwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "misc.cu", "conv.cu", "scan_fwd.cu", "scan_bwd.cu", "noalloc.cu", "packer.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
            os.path.join(INCLUDE, "varlen_ssm.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
