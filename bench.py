@@ -52,7 +52,7 @@ def per_token_counts(D, N, e, W=4):
 # capture of a kernel, per token; reset an entry to nothing as soon as the
 # kernel changes (profiles/ keeps the capture summaries).
 LAST_CAPTURE_TRAFFIC = {
-    ("m14b", "scan_bwd"): {"bytes_per_token": (404.029184e6 + 439.640064e6) / 8192,
+    ("m14b", "scan_bwd"): {"bytes_per_token": (404.583936e6 + 439.550464e6) / 8192,
                            "source": "ncu capture of scan_bwd_kernel on m14b_small (T=8192), "
                                      "scaled by tokens; profiles/scan_bwd_m14b_small.md"},
 }
@@ -556,14 +556,45 @@ def run_ours(args):
             torch.cuda.synchronize(device)
             return a.elapsed_time(b) / 1e3
 
+        def host_link(n):
+            """The host link on its own: n steps' input and result copies, both
+            directions at once on the copy streams, with nothing computed.
+            Returns seconds per step: the floor under the end-to-end step."""
+            si, so = sets[0]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            s_in.wait_event(a)
+            s_out.wait_event(a)
+            for _ in range(n):
+                with torch.cuda.stream(s_in):
+                    for name, h in host_in.items():
+                        si[name].copy_(h, non_blocking=True)
+                    si["cu"].copy_(cu_host, non_blocking=True)
+                with torch.cuda.stream(s_out):
+                    for name, h in host_out.items():
+                        h.copy_(so[name], non_blocking=True)
+            ein, eout = torch.cuda.Event(), torch.cuda.Event()
+            ein.record(s_in)
+            eout.record(s_out)
+            stream.wait_event(ein)
+            stream.wait_event(eout)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            return a.elapsed_time(b) / 1e3 / n
+
         run_e2e(2)
         barrier(device)
         esec = run_e2e(args.e2e_steps) / args.e2e_steps
         ev, _ = aggregate(T, esec, world, device)
+        lsec = host_link(max(4, args.e2e_steps // 2))
         e2e = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": esec * 1e3, "steps": args.e2e_steps,
                "copies": "pinned host buffers; input and result copies on their own streams, "
-                         "double-buffered on the device, overlapping the neighbouring steps' compute"}
+                         "double-buffered on the device, overlapping the neighbouring steps' compute",
+               "host_link": {"ms_per_step": lsec * 1e3,
+                             "GB/s_each_way": {"h2d": h2d / lsec / 1e9, "d2h": d2h / lsec / 1e9},
+                             "e2e_frac_of_link_floor": lsec / esec,
+                             "what": "the same copies alone, both directions at once, no compute"}}
         for k in ("sf", "sb"):
             st = binding.read_status(ws[k])
             if st != 0:
