@@ -1,10 +1,10 @@
 // conv.cu -- packed depthwise causal conv1d (width W <= 4), forward and backward.
 //
-// One CTA per tile of 64 tokens x 128 channels.  The x rows of the tile (plus
+// One CTA per tile of 192 tokens x 128 channels.  The x rows of the tile (plus
 // the W-1 rows before it, and for the backward the W-1 after it) and the du
 // rows come into shared memory by 2-D tensor copies, so every row is read from
 // HBM about once; rows before the first token or past the last are zero-filled
-// by the copy.  Warp w owns 8 consecutive tokens of the tile, lane l owns 4
+// by the copy.  Warp w owns 24 consecutive tokens of the tile, lane l owns 4
 // consecutive channels, so stores are whole 256- or 512-byte row segments per
 // warp.  The sequence-boundary mask comes from position_indices: tap k (k
 // tokens back) is used only if pos[t] >= k, and in the backward the tap that
@@ -34,15 +34,21 @@ __device__ __forceinline__ float silu_grad(float x) {
 }
 
 // ------------------------------------------------------------------ tiled kernels
-// One CTA per tile of kCT = 64 tokens x kCC = 128 channels.  The x rows the
-// tile needs (its tokens plus the W-1 before them, and for the backward the
-// W-1 after them) and the du rows arrive by 2-D tensor copies on one mbarrier;
+// One CTA per tile of CT tokens x kCC = 128 channels.  The x rows the tile
+// needs (its tokens plus the W-1 before them, and for the backward the W-1
+// after them) and the du rows arrive by 2-D tensor copies on one mbarrier;
 // rows before the first token or past the last come back as zeros.  Warp w
-// owns tokens 8w .. 8w+7 of the tile, lane l owns channels 4l .. 4l+3, and
-// every row a thread touches after the copies is read from shared memory.
-constexpr int kCT = 64;    // tokens per tile
+// owns tokens (CT/8)w .. (CT/8)(w+1)-1 of the tile, lane l owns channels
+// 4l .. 4l+3, and every row a thread touches after the copies is read from
+// shared memory.  The backward recomputes g for the W-1 tokens after a warp's
+// own, so the longer the warp's run of tokens, the smaller that share (3 of
+// 27 at 24 tokens).  The forward's tile holds only its x rows (bf16: 17 KB
+// at 64 tokens, 50 KB at 192); tiles of 192 tokens measured faster than 128
+// and 64 for both directions.
+// (a tensor-copy box is at most 256 rows: 192 + 2(W-1) fits)
+constexpr int kCTF = 192;  // tokens per forward tile
+constexpr int kCTB = 192;  // tokens per backward tile
 constexpr int kCC = 128;   // channels per tile
-constexpr int kTokPerWarp = kCT / 8;
 
 template <typename T>
 __device__ __forceinline__ void lds4(const T* p, float (&v)[4]) {
@@ -66,12 +72,14 @@ __device__ __forceinline__ void stg4(T* p, const float (&v)[4]) {
   }
 }
 
-template <typename T, int W>
+// kBwd: the backward's tile (x rows on both sides, du rows, and room for the
+// per-warp dweight / dbias partials); the forward's holds its x rows only.
+template <typename T, int W, int CT, bool kBwd>
 struct ConvTileSmem {
-  static constexpr int XR = kCT + 2 * (W - 1);  // x rows t0-(W-1) .. t0+kCT+W-2
-  static constexpr int GR = kCT + W - 1;        // du rows t0 .. t0+kCT+W-2
+  static constexpr int XR = CT + (kBwd ? 2 : 1) * (W - 1);  // x rows from t0-(W-1)
+  static constexpr int GR = kBwd ? CT + W - 1 : 0;          // du rows t0 .. t0+CT+W-2
   static constexpr size_t kIO = sizeof(T) * (size_t)(XR + GR) * kCC;
-  static constexpr size_t kRed = sizeof(float) * 8 * kCC * (W + 1);
+  static constexpr size_t kRed = kBwd ? sizeof(float) * 8 * kCC * (W + 1) : 0;
   // x rows, then du rows (both 256-byte multiples: kCC * sizeof(T)); after
   // the backward's arithmetic, the per-warp dweight / dbias partials
   alignas(128) unsigned char io[kIO > kRed ? kIO : kRed];
@@ -80,7 +88,7 @@ struct ConvTileSmem {
   __device__ float* red() { return reinterpret_cast<float*>(io); }
   alignas(16) float w[W][kCC];
   alignas(16) float b[kCC];
-  int pos[GR];
+  int pos[CT + W - 1];
   alignas(8) uint64_t bar;
 };
 
@@ -90,16 +98,17 @@ struct ConvTileSmem {
 template <typename T, int W, bool kTail>
 __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                             ConvArgs a) {
-  using SM = ConvTileSmem<T, W>;
+  using SM = ConvTileSmem<T, W, kCTF, false>;
+  constexpr int kTokPerWarp = kCTF / 8;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
   const int ncols = (a.D + kCC - 1) / kCC;
   const int64_t row = blockIdx.x / ncols;
   const int c0 = (int)(blockIdx.x - row * ncols) * kCC;
-  const int64_t t0 = row * kCT;
+  const int64_t t0 = row * kCTF;
   const int bx = a.D < kCC ? a.D : kCC;  // row pitch of the staged tile
-  constexpr int FR = kCT + W - 1;        // x rows the forward needs
+  constexpr int FR = SM::XR;             // x rows the forward needs
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
@@ -111,7 +120,7 @@ __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_cons
     sm.w[k][c] = (c0 + c < a.D) ? __ldg(a.w + (int64_t)c0 * W + i) : 0.0f;
   }
   for (int i = tid; i < kCC; i += 256) sm.b[i] = (a.bias && c0 + i < a.D) ? __ldg(a.bias + c0 + i) : 0.0f;
-  for (int i = tid; i < kCT; i += 256) sm.pos[i] = (t0 + i < a.T) ? __ldg(a.pos + t0 + i) : 0;
+  for (int i = tid; i < kCTF; i += 256) sm.pos[i] = (t0 + i < a.T) ? __ldg(a.pos + t0 + i) : 0;
   __syncthreads();
   const int c = 4 * lane;
   const bool active = c < bx && c0 + c < a.D;
@@ -169,14 +178,15 @@ template <typename T, int W, bool kTail>
 __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                                const __grid_constant__ CUtensorMap tm_du,
                                                                ConvArgs a) {
-  using SM = ConvTileSmem<T, W>;
+  using SM = ConvTileSmem<T, W, kCTB, true>;
+  constexpr int kTokPerWarp = kCTB / 8;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
   const int ncols = (a.D + kCC - 1) / kCC;
   const int64_t row = blockIdx.x / ncols;
   const int c0 = (int)(blockIdx.x - row * ncols) * kCC;
-  const int64_t t0 = row * kCT;
+  const int64_t t0 = row * kCTB;
   const int bx = a.D < kCC ? a.D : kCC;
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
@@ -336,12 +346,12 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
 
 template <typename T, int W, bool kTail>
 cudaError_t fwd_tile_k(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t st) {
-  const size_t smem = sizeof(ConvTileSmem<T, W>);
+  const size_t smem = sizeof(ConvTileSmem<T, W, kCTF, false>);
   cudaError_t e = cudaFuncSetAttribute(conv_fwd_tile_kernel<T, W, kTail>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t cols = (a.D + kCC - 1) / kCC;
-  const int64_t rows = (a.T + kCT - 1) / kCT;
+  const int64_t rows = (a.T + kCTF - 1) / kCTF;
   if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
   conv_fwd_tile_kernel<T, W, kTail><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, a);
   return cudaGetLastError();
@@ -355,12 +365,12 @@ cudaError_t fwd_tile_w(const ConvArgs& a, const CUtensorMap& tm_x, cudaStream_t 
 template <typename T, int W, bool kTail>
 cudaError_t bwd_tile_k(const ConvArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_du,
                        cudaStream_t st) {
-  const size_t smem = sizeof(ConvTileSmem<T, W>);
+  const size_t smem = sizeof(ConvTileSmem<T, W, kCTB, true>);
   cudaError_t e = cudaFuncSetAttribute(conv_bwd_tile_kernel<T, W, kTail>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t cols = (a.D + kCC - 1) / kCC;
-  const int64_t rows = (a.T + kCT - 1) / kCT;
+  const int64_t rows = (a.T + kCTB - 1) / kCTB;
   if (rows * cols > 2147483647LL) return cudaErrorInvalidConfiguration;
   conv_bwd_tile_kernel<T, W, kTail><<<(unsigned)(rows * cols), 256, smem, st>>>(tm_x, tm_du, a);
   return cudaGetLastError();
@@ -450,13 +460,13 @@ cudaError_t launch_conv_tails(const ConvArgs& a, IO io, bool bwd, cudaStream_t s
 }
 
 int64_t conv_bwd_partial_rows(int64_t T) {
-  const int64_t per = kCT;
+  const int64_t per = kCTB;
   const int64_t r = (T + per - 1) / per;
   return r > 0 ? r : 1;
 }
 
 int conv_tile_rows(int W, bool bwd, bool x) {
-  return x ? kCT + (bwd ? 2 : 1) * (W - 1) : kCT + W - 1;
+  return x ? (bwd ? kCTB + 2 * (W - 1) : kCTF + W - 1) : kCTB + W - 1;
 }
 int conv_tile_cols() { return kCC; }
 

@@ -220,8 +220,14 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const T* const up = sm.u + tb * kTile + lane;
     float* const dlp = sm.dlt + tb * kTile + lane;
     const float* const bp = Bf + tb * N;
+    // groups of 8 tokens, unrolled; the loop over the groups keeps the body
+    // small enough for the instruction cache (the fully unrolled 16 tokens
+    // of both passes stalled on instruction fetch)
+#pragma unroll 1
+    for (int kg = 0; kg < kK; kg += 8) {
 #pragma unroll
-    for (int k = 0; k < kK; ++k) {
+    for (int e = 0; e < 8; ++e) {
+      const int k = kg + e;
       const float r = to_f(drp[k * kTile]) + bias;
       const float dl = a.delta_softplus ? softplusf(r) : r;
       dlp[k * kTile] = dl;
@@ -236,6 +242,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
       for (int i = 0; i < P; ++i) h[i] = fma2(ex2x2(mul2(dl2, A2[i])), h[i], mul2(du2, Bv[i]));
       sd += dl;
+    }
     }
   } else {
 #pragma unroll 1  // ragged tails and narrow tiles only: kept small for the instruction cache
@@ -437,8 +444,11 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float* const cp = Cf + tb * N;
     T* op = out + (t0 + tb) * a.D + d;
     T* yp = ypre ? ypre + (t0 + tb) * a.D + d : nullptr;
+#pragma unroll 1  // groups of 8 tokens, as in pass 1
+    for (int kg = 0; kg < kK; kg += 8) {
 #pragma unroll
-    for (int k = 0; k < kK; ++k) {
+    for (int e = 0; e < 8; ++e) {
+      const int k = kg + e;
       if ((rm >> k) & 1u) {
         // the previous token ended a sequence (a token of this warp's when k > 0;
         // the warp before stores its own last token's state)
@@ -467,6 +477,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (a.has_z) y *= siluf(to_f(zp[k * kTile])) + a.gate_floor;
       if (valid) *op = from_f<T>(y);
       op += a.D;
+    }
     }
     if constexpr (kStates) {
       if (a.h_final && seq_end(tb + kK - 1)) end_state(h, tb + kK - 1);
