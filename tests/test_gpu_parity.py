@@ -554,6 +554,20 @@ def _sampled_checks(w, r, res, seq_pick):
         assert_close(f"dC[seq {s}]", res["dC"][a:b], g["dC"], 1e-2)
 
 
+def test_workload_m14b_forward_sampled_parity():
+    """The Mamba-1.4B forward-only configuration (its own seed): conv and scan
+    forward at full size, every output of 48 channels against the oracle."""
+    w = workloads.make("m14b_fwd", backward=False, scan_input=False)
+    r = workloads.rounded(w, "bf16")
+    for k in workloads.ACTIVATIONS:
+        w.pop(k, None)
+    res = run_chain(w["cu_seqlens"], w["T"], r, "bf16", with_bwd=False)
+    D = r["A"].shape[0]
+    rng = np.random.default_rng(11)
+    chans = np.unique(np.concatenate([np.arange(0, 8), np.arange(D - 8, D), rng.choice(D, 32, replace=False)]))
+    check_chain(w["cu_seqlens"], r, res, "bf16", with_bwd=False, channels=chans)
+
+
 def test_workload_m14b_fwd_bwd_sampled_parity():
     w, r = _big_case("m14b")
     res = run_chain(w["cu_seqlens"], w["T"], r, "bf16", use_y=True)  # as the bench step runs
