@@ -433,6 +433,10 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  // every inclusive-state word starts as the all-ones NaN (bytes 0xff) that
+  // the kernel reads as "not stored yet": a word is its own flag
+  if (T > 0) e = cudaMemsetAsync(at<char>(workspace, l.incl), 0xff, l.incl_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "filling the look-back states");
   // an empty sequence ends in the state it starts from
   e = launch_empty_sequence_states(cu_seqlens, num_seqs, (int64_t)D * N, initial_states, final_states, st);
   if (e != cudaSuccess) return cuda_fail(e, "empty-sequence states launch");

@@ -200,6 +200,21 @@ __device__ __forceinline__ void st_carry(float2* p, float2 v) {
   asm volatile("st.relaxed.gpu.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(x), "r"(y) : "memory");
 }
 
+// The same for one 32-bit carry word.
+__device__ __forceinline__ float ld_carry1(const float* p) {
+  unsigned x;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
+  return __uint_as_float(x);
+}
+
+__device__ __forceinline__ bool carry_set1(float v) { return __float_as_uint(v) != kCarryUnset; }
+
+__device__ __forceinline__ void st_carry1(float* p, float v) {
+  unsigned x = __float_as_uint(v);
+  x = x == kCarryUnset ? 0x7fffffffu : x;
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(x) : "memory");
+}
+
 // Warp-wide wait on one look-back slot whose carry words are their own flags
 // and whose aggregate is announced by `flag`.  Returns kFlagInclusive once
 // every lane's carry word holds a value (the value in *v), kFlagAggregate once

@@ -170,6 +170,8 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   char* s = static_cast<char*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t ce = cudaMemsetAsync(s, 0, o_pos, st);  // status, ticket, look-back flags
+  // look-back states: all-ones NaN words, read by the kernel as "not stored yet"
+  if (ce == cudaSuccess && T > 0) ce = cudaMemsetAsync(s + o_incl, 0xff, sizeof(float) * slots * N * kTile, st);
   if (ce == cudaSuccess && status) ce = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
   // an empty sequence ends in the state it starts from
   if (ce == cudaSuccess)

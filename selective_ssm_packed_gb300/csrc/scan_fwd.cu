@@ -17,11 +17,13 @@
 //      sub-chunk is then exp2(A*log2e * sum) or exactly 0 if a sequence starts
 //      inside it (the article's SSM_pack zeroes the factor at a start).
 //   4. Exclusive scan of the 8 sub-chunk aggregates per (channel, state) in
-//      shared memory.
-//   5. Decoupled look-back across chunks (warp 0): publish the chunk aggregate
-//      (or, if a sequence starts inside the chunk, the inclusive state at once),
-//      walk back over predecessors' flags to the nearest inclusive state, then
-//      re-apply the aggregates FORWARD from there in chunk order, which gives
+//      shared memory; warp s takes the states n = s (mod 8).
+//   5. Decoupled look-back across chunks, each warp on its own states' chain:
+//      the inclusive state of a chunk is stored word by word, each word its
+//      own "stored" flag (the array starts as all-ones NaNs); an aggregate is
+//      published, behind a fence and the warp's flag, only when a walk has to
+//      go past it.  The walk goes back to the nearest inclusive state and
+//      re-applies the aggregates FORWARD from there in chunk order, which gives
 //      the same floating-point result whatever the timing (bitwise repeatable).
 //      Work items take chunk ids from an atomic ticket, so a CTA only ever waits
 //      on items already running; every wait is time-bounded and a timeout is
@@ -53,7 +55,6 @@ struct FwdSmem {
   alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
   alignas(16) float dlt[kL * kTile];
   alignas(16) float aggH[kS * N * kTile];
-  float totH[N * kTile];
   float hin[N * kTile];
   float aggSD[kS * kTile];
   alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
@@ -274,33 +275,57 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   if (lane == 0) sm.aggRS[s] = rs;
   __syncthreads();
 
-  // Warp 0 acquires the previous chunk's flag and reads its inclusive state
-  // now; the loads land during the scan below.  (That chunk started long
-  // before this one: its state is nearly always published by now.  The reads
-  // follow the acquire in program order, so they see what the flag publishes.)
-  int early_f = kFlagNone;
-  float early_x[N];
-  if (s == 0 && chunk > 0 && pos_at(0) != 0) {
-    const int64_t jslot = (int64_t)tile * a.n_chunks + chunk - 1;
-    early_f = ld_acquire_gpu(a.flags + jslot * kTile + lane);
-    const float* inc = a.incl + jslot * (N * kTile);
-#pragma unroll
-    for (int n = 0; n < N; ++n) early_x[n] = __ldcg(inc + n * kTile + lane);
+  // ---- steps 4-5, per warp: warp s owns the state chains n = s (and s + kS
+  //      when N = 16); with N = 4 only warps 0-3 own one.  For each of its
+  //      states it runs the exclusive scan over the 8 sub-chunk aggregates,
+  //      then the decoupled look-back across chunks on its own chain.  Each
+  //      (chunk, state, channel) word of the inclusive array holds kCarryUnset
+  //      until its value is stored (the call fills the array before the
+  //      launch), so a word is its own flag: no fence, and no flag for the
+  //      common case.  Only the aggregate of a chunk, published when a walk
+  //      must go past it, is announced by the warp's flag after a fence.
+  constexpr bool kTwo = N > kS;     // two states per warp
+  const bool own = s < N;           // the warp owns at least one state
+  const int n0 = s, n1 = kTwo ? s + kS : s;
+  const bool need_in = chunk > 0 && pos_at(0) != 0;  // a state enters from the previous chunk
+  const int64_t base = (int64_t)tile * a.n_chunks;
+  // the chain word of state n for chunk j, this lane's channel
+  auto word = [&](int64_t j, int n) { return (base + j) * (N * kTile) + n * kTile + lane; };
+  // early look at the previous chunk's inclusive state: that chunk started
+  // long before this one and has nearly always stored it by now; the loads
+  // land during the scan below
+  float2 early = make_float2(0.0f, 0.0f);
+  if (own && need_in) {
+    early.x = ld_carry1(a.incl + word(chunk - 1, n0));
+    if (kTwo) early.y = ld_carry1(a.incl + word(chunk - 1, n1));
   }
-
-  // ---- step 4: exclusive scan over sub-chunks; chain (lane, n) with n % kS == s
-  {
+  if (own) {
     float sdj[kS];
     int rsj[kS];
+    int rs_any = 0;
+    float sd_tot = 0.0f;
 #pragma unroll
     for (int j = 0; j < kS; ++j) {
       sdj[j] = sm.aggSD[j * kTile + lane];
       rsj[j] = sm.aggRS[j];
+      rs_any |= rsj[j];
+      sd_tot += sdj[j];
     }
+    // exclusive scan per state; the chunk's totals stay in registers
+    // A*log2e of the warp's states, picked with compile-time register indices
+    float2 a2w = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      if (n % kS != s) continue;
-      const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
+    for (int i = 0; i < P; ++i) {
+      if (2 * i == n0) a2w.x = A2[i].x;
+      if (2 * i + 1 == n0) a2w.x = A2[i].y;
+      if (2 * i == n1) a2w.y = A2[i].x;
+      if (2 * i + 1 == n1) a2w.y = A2[i].y;
+    }
+    float2 tot = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < (kTwo ? 2 : 1); ++q) {
+      const int n = q ? n1 : n0;
+      const float a2 = q ? a2w.y : a2w.x;
       float Pj[kS], Hj[kS];
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
@@ -313,102 +338,80 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         sm.aggH[(j * N + n) * kTile + lane] = x;
         x = fmaf(Pj[j], x, Hj[j]);
       }
-      sm.totH[n * kTile + lane] = x;
+      if (q) tot.y = x;
+      else tot.x = x;
     }
-  }
-  __syncthreads();
-
-  // ---- step 5: decoupled look-back (warp 0)
-  bool release_incl = false;  // warp 0: inclusive state stored, flag not yet released
-  if (s == 0) {
-    int rs_any = 0;
-    float sd_tot = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kS; ++j) {
-      rs_any |= sm.aggRS[j];
-      sd_tot += sm.aggSD[j * kTile + lane];
-    }
-    const int64_t slot = (int64_t)tile * a.n_chunks + chunk;
     const bool publish = (long long)tk != a.drop_ticket;
-    float* my_agg = a.agg + slot * (N * kTile);
-    float* my_inc = a.incl + slot * (N * kTile);
-    // every lane is its own chain (one channel): it publishes its payload and
-    // then its own flag with a release store, and readers acquire that flag
-    int* my_flag = a.flags + slot * kTile + lane;
-    if (rs_any) {
-      // a sequence starts in this chunk: the state leaving it does not depend
-      // on the state entering, publish it at once
-#pragma unroll
-      for (int n = 0; n < N; ++n) my_inc[n * kTile + lane] = sm.totH[n * kTile + lane];
-      if (publish) st_release_gpu(my_flag, kFlagInclusive);
-    }
-    float x[N];
-#pragma unroll
-    for (int n = 0; n < N; ++n) x[n] = 0.0f;
-    // no entering state is needed when a sequence starts at the first token
-    if (chunk > 0 && pos_at(0) != 0) {
-      // the previous chunk of the tile started long before this one and has
-      // usually published its inclusive state: look first, and publish this
-      // chunk's aggregate only when the walk has to go further
-      const int64_t base = (int64_t)tile * a.n_chunks;
+    int* const my_flag = a.flags + (base + chunk) * kS + s;
+    auto store_incl = [&](float2 v) {
+      st_carry1(a.incl + word(chunk, n0), v.x);
+      if (kTwo) st_carry1(a.incl + word(chunk, n1), v.y);
+    };
+    // a sequence starts in this chunk: the state leaving it does not depend
+    // on the state entering, store it at once
+    if (rs_any && publish) store_incl(tot);
+    float2 x = make_float2(0.0f, 0.0f);
+    if (need_in) {
       int j = chunk - 1, found = -1, timed_out = 0;
-      bool have_x = false;
-      if (early_f == kFlagInclusive) {
-        found = j;
-        have_x = true;
-#pragma unroll
-        for (int n = 0; n < N; ++n) x[n] = early_x[n];
-      } else if (ld_acquire_gpu(a.flags + (base + j) * kTile + lane) == kFlagInclusive) {
+      float2 v = early;
+      if (__all_sync(0xffffffffu, carry_set1(v.x) && (!kTwo || carry_set1(v.y)))) {
         found = j;
       } else {
         if (!rs_any) {
-#pragma unroll
-          for (int n = 0; n < N; ++n) my_agg[n * kTile + lane] = sm.totH[n * kTile + lane];
-          a.agg_sd[slot * kTile + lane] = sd_tot;
-          if (publish) st_release_gpu(my_flag, kFlagAggregate);
+          // publish this chunk's aggregate for walks that must go past it;
+          // every warp stores the same sum of delta, its flag covers its own
+          a.agg[word(chunk, n0)] = tot.x;
+          if (kTwo) a.agg[word(chunk, n1)] = tot.y;
+          a.agg_sd[(base + chunk) * kTile + lane] = sd_tot;
+          fence_acq_rel_gpu();
+          __syncwarp();
+          if (lane == 0 && publish) st_relaxed_gpu(my_flag, kFlagAggregate);
         }
+        const uint64_t t_start = globaltimer_ns();
         while (j >= 0) {
-          const int f = wait_flag(a.flags + (base + j) * kTile + lane, a.wait_ns);
+          // wait for chunk j: its inclusive words, or its aggregate flag
+          unsigned backoff = 32;
+          int f = kFlagNone;
+          for (;;) {
+            v.x = ld_carry1(a.incl + word(j, n0));
+            if (kTwo) v.y = ld_carry1(a.incl + word(j, n1));
+            if (__all_sync(0xffffffffu, carry_set1(v.x) && (!kTwo || carry_set1(v.y)))) {
+              f = kFlagInclusive;
+              break;
+            }
+            if (__all_sync(0xffffffffu, ld_acquire_gpu(a.flags + (base + j) * kS + s) == kFlagAggregate)) {
+              f = kFlagAggregate;
+              break;
+            }
+            if (__shfl_sync(0xffffffffu, globaltimer_ns() - t_start > a.wait_ns, 0)) break;
+            __nanosleep(backoff);
+            if (backoff < 1024) backoff <<= 1;
+          }
           if (f == kFlagInclusive) { found = j; break; }
           if (f == kFlagNone) { timed_out = 1; break; }
           --j;
         }
       }
       if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
+      // forward re-evaluation from the nearest inclusive state, in chunk order
       int first = j + 1;
       if (found >= 0) {
-        if (!have_x) {
-          const float* inc = a.incl + (base + found) * (N * kTile);
-#pragma unroll
-          for (int n = 0; n < N; ++n) x[n] = __ldcg(inc + n * kTile + lane);
-        }
+        x = v;
         first = found + 1;
       }
       for (int i = first; i < chunk; ++i) {
-        const float* ag = a.agg + (base + i) * (N * kTile);
         const float sdi = __ldcg(a.agg_sd + (base + i) * kTile + lane);
-#pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-          x[n] = fmaf(ex2(a2 * sdi), x[n], __ldcg(ag + n * kTile + lane));
-        }
+        x.x = fmaf(ex2(a2w.x * sdi), x.x, __ldcg(a.agg + word(i, n0)));
+        if (kTwo) x.y = fmaf(ex2(a2w.y * sdi), x.y, __ldcg(a.agg + word(i, n1)));
       }
     }
-#pragma unroll
-    for (int n = 0; n < N; ++n) sm.hin[n * kTile + lane] = x[n];
-    if (!rs_any) {
-      // payload now, flag after the barrier below, when these stores have drained
-#pragma unroll
-      for (int n = 0; n < N; ++n) {
-        const float a2 = (n & 1) ? A2[n / 2].y : A2[n / 2].x;
-        my_inc[n * kTile + lane] = fmaf(ex2(a2 * sd_tot), x[n], sm.totH[n * kTile + lane]);
-      }
-      release_incl = publish;
-    }
+    // stored at once: the next chunk of the tile may already be waiting
+    if (!rs_any && publish)
+      store_incl(make_float2(fmaf(ex2(a2w.x * sd_tot), x.x, tot.x), fmaf(ex2(a2w.y * sd_tot), x.y, tot.y)));
+    sm.hin[n0 * kTile + lane] = x.x;
+    if (kTwo) sm.hin[n1 * kTile + lane] = x.y;
   }
   __syncthreads();
-  if (release_incl)
-    st_release_gpu(a.flags + ((int64_t)tile * a.n_chunks + chunk) * kTile + lane, kFlagInclusive);
 
   // ---- step 6: exact start state, pass 2
   int rs_pre = 0;
