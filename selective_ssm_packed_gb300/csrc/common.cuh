@@ -337,9 +337,23 @@ __device__ __forceinline__ const float* widen_rows(const T* src, float* dst, int
   if constexpr (sizeof(T) == 4) {
     return reinterpret_cast<const float*>(src);
   } else {
+    int done = 0;  // values widened by the 16-byte path
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0) {
+      // 8 values per 16-byte load; a bf16 is the upper half of the float it rounds
+      const uint4* s8 = reinterpret_cast<const uint4*>(src);
+      float4* d4 = reinterpret_cast<float4*>(dst);
+      for (int i = tid; i < count / 8; i += nthreads) {
+        const uint4 q = s8[i];
+        d4[2 * i] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                                __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+        d4[2 * i + 1] = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xffff0000u),
+                                    __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xffff0000u));
+      }
+      done = count & ~7;
+    }
     const __nv_bfloat162* s2 = reinterpret_cast<const __nv_bfloat162*>(src);
     float2* d2 = reinterpret_cast<float2*>(dst);
-    for (int i = tid; i < count / 2; i += nthreads) d2[i] = __bfloat1622float2(s2[i]);
+    for (int i = done / 2 + tid; i < count / 2; i += nthreads) d2[i] = __bfloat1622float2(s2[i]);
     return dst;
   }
 }

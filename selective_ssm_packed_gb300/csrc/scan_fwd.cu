@@ -119,12 +119,15 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   __syncthreads();
 
-  // Persistent loop: one work item per pass.  The inputs are read until the
-  // end of pass 2, so the next ticket is drawn and its copies requested there;
-  // an earlier draw would hold tickets back from the look-back chains (an
-  // item whose neighbour sits reserved behind a running item waits for both).
-  // Items only ever wait on items with smaller tickets, all of which are done
-  // or in hand of a running CTA, so the loop cannot deadlock.
+  // Persistent loop: one work item per pass.  The next ticket is drawn when
+  // pass 2 starts, so that the atomic's round trip overlaps pass 2, and its
+  // copies are requested at the end of pass 2, when the inputs are free.  A
+  // draw at the start of the item would hold tickets back from the look-back
+  // chains (an item whose neighbour sits reserved behind a running item waits
+  // for both); pass 2 waits on nothing, so a ticket held through it is not
+  // held back long.  Items only ever wait on items with smaller tickets, all
+  // of which are done or in hand of a running CTA, so the loop cannot
+  // deadlock.
   for (uint32_t it = 0;; ++it) {
   // the barrier's completion also publishes thread 0's write of sm.ticket
   if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
@@ -414,6 +417,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   __syncthreads();
 
   // ---- step 6: exact start state, pass 2
+  int next = 0;  // thread 0: the next ticket, used once pass 2 is done
+  if (tid == 0) next = (int)atomicAdd(a.ticket, 1u);
   int rs_pre = 0;
   float sd_pre = 0.0f;
   for (int j = 0; j < s; ++j) {
@@ -513,10 +518,9 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   }
 
-  // every input of this item has been read: draw the next one
+  // every input of this item has been read: request the next one's
   __syncthreads();
   if (tid == 0) {
-    const int next = (int)atomicAdd(a.ticket, 1u);
     sm.ticket = next;
     issue(next);
   }
