@@ -524,10 +524,13 @@ def run_ours(args):
 
         def run_e2e(n):
             """n steps; returns seconds for all of them (events on the compute stream,
-            which waits for the last copies before its end event)."""
-            copied = [torch.cuda.Event() for _ in range(n)]    # inputs of step k on the device
-            computed = [torch.cuda.Event() for _ in range(n)]  # results of step k ready
-            drained = [torch.cuda.Event() for _ in range(n)]   # results of step k on the host
+            which waits for the last copies before its end event) and each stream's
+            mean busy time per step in ms (from the moment its waits are met)."""
+            ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+            copied = [ev() for _ in range(n)]    # inputs of step k on the device
+            computed = [ev() for _ in range(n)]  # results of step k ready
+            drained = [ev() for _ in range(n)]   # results of step k on the host
+            in0, c0, o0 = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             s_in.wait_event(a)
@@ -537,6 +540,7 @@ def run_ours(args):
                 with torch.cuda.stream(s_in):
                     if k >= 2:
                         s_in.wait_event(computed[k - 2])       # set k%2 no longer read by compute
+                    in0[k].record(s_in)
                     for name, h in host_in.items():
                         si[name].copy_(h, non_blocking=True)
                     si["cu"].copy_(cu_host, non_blocking=True)
@@ -544,17 +548,21 @@ def run_ours(args):
                 stream.wait_event(copied[k])
                 if k >= 2:
                     stream.wait_event(drained[k - 2])          # results of set k%2 copied out
+                c0[k].record(stream)
                 compute(si, so)
                 computed[k].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(computed[k])
+                    o0[k].record(s_out)
                     for name, h in host_out.items():
                         h.copy_(so[name], non_blocking=True)
                     drained[k].record(s_out)
             stream.wait_event(drained[n - 1])
             b.record(stream)
             torch.cuda.synchronize(device)
-            return a.elapsed_time(b) / 1e3
+            busy = {name: sum(x.elapsed_time(y) for x, y in zip(s0, s1)) / n
+                    for name, s0, s1 in (("h2d", in0, copied), ("compute", c0, computed), ("d2h", o0, drained))}
+            return a.elapsed_time(b) / 1e3, busy
 
         def host_link(n):
             """The host link on its own: n steps' input and result copies, both
@@ -586,12 +594,14 @@ def run_ours(args):
         nl = max(4, args.e2e_steps // 2)
         l0 = host_link(nl)  # the link is shared with the host's other work: timed on both sides
         barrier(device)
-        esec = run_e2e(args.e2e_steps) / args.e2e_steps
+        esec, busy = run_e2e(args.e2e_steps)
+        esec /= args.e2e_steps
         ev, _ = aggregate(T, esec, world, device)
         l1 = host_link(nl)
         lsec = min(l0, l1)
         e2e = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": esec * 1e3, "steps": args.e2e_steps,
+               "stream_busy_ms_per_step": busy,
                "copies": "pinned host buffers; input and result copies on their own streams, "
                          "double-buffered on the device, overlapping the neighbouring steps' compute",
                "host_link": {"ms_per_step": lsec * 1e3,

@@ -303,14 +303,17 @@ def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu
     N = A.shape[1]
     dt = u.dtype
     g = dict(grads or {})
-    g.setdefault("du", torch.empty_like(u))
-    g.setdefault("ddelta_raw", torch.empty_like(u))
-    g.setdefault("dA", torch.empty_like(A))
-    g.setdefault("dB", torch.empty((T, N), dtype=torch.float32, device=u.device))
-    g.setdefault("dC", torch.empty((T, N), dtype=torch.float32, device=u.device))
-    g.setdefault("dDskip", torch.empty_like(Dskip) if Dskip is not None else None)
-    g.setdefault("dz", torch.empty_like(z) if z is not None else None)
-    g.setdefault("d_dt_bias", torch.empty_like(dt_bias) if dt_bias is not None else None)
+    # outputs the caller did not pass are allocated here (only those)
+    make = {"du": lambda: torch.empty_like(u), "ddelta_raw": lambda: torch.empty_like(u),
+            "dA": lambda: torch.empty_like(A),
+            "dB": lambda: torch.empty((T, N), dtype=torch.float32, device=u.device),
+            "dC": lambda: torch.empty((T, N), dtype=torch.float32, device=u.device),
+            "dDskip": lambda: torch.empty_like(Dskip) if Dskip is not None else None,
+            "dz": lambda: torch.empty_like(z) if z is not None else None,
+            "d_dt_bias": lambda: torch.empty_like(dt_bias) if dt_bias is not None else None}
+    for k, f in make.items():
+        if k not in g:
+            g[k] = f()
     if d_initial_states is True:
         d_initial_states = torch.empty((cu_seqlens.numel() - 1, D, N), dtype=torch.float32, device=u.device)
     elif d_initial_states is False:
