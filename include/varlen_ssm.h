@@ -296,9 +296,15 @@ const char* vssm_last_error(void);      /* thread-local; "" if none */
  * ticket never publishes its look-back flag (-1 = off), so the waits behind it
  * run out of time and report VSSM_ERR_LOOKBACK_TIMEOUT instead of hanging.
  * VSSM_DBG_WAIT_NS: the time limit of each look-back wait in nanoseconds
- * (default 1e9).  Returns VSSM_OK or VSSM_ERR_ARG. */
+ * (default 1e9).  VSSM_DBG_DELAY_ITEM: the scan work item with this ticket
+ * sleeps VSSM_DBG_DELAY_NS nanoseconds (default 2e5, at most 1e7) before it
+ * stores its inclusive state (-1 = off), so the items after it must walk back
+ * past published aggregates; the results do not change, bit for bit.
+ * Returns VSSM_OK or VSSM_ERR_ARG. */
 #define VSSM_DBG_DROP_FLAG 1
 #define VSSM_DBG_WAIT_NS 2
+#define VSSM_DBG_DELAY_ITEM 3
+#define VSSM_DBG_DELAY_NS 4
 int vssm_debug_set(int knob, int64_t value);
 
 #ifdef __cplusplus

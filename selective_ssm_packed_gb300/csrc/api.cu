@@ -20,6 +20,8 @@ namespace {
 thread_local std::string g_last_error;
 std::atomic<long long> g_drop_ticket{-1};
 std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+std::atomic<long long> g_delay_ticket{-1};
+std::atomic<unsigned long long> g_delay_ns{200000ull};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -231,6 +233,12 @@ int vssm_debug_set(int knob, int64_t value) {
   if (knob == VSSM_DBG_WAIT_NS) {
     if (value <= 0) return fail(VSSM_ERR_ARG, "wait limit must be positive");
     g_wait_ns.store((unsigned long long)value);
+    return VSSM_OK;
+  }
+  if (knob == VSSM_DBG_DELAY_ITEM) { g_delay_ticket.store(value); return VSSM_OK; }
+  if (knob == VSSM_DBG_DELAY_NS) {
+    if (value <= 0 || value > 10000000) return fail(VSSM_ERR_ARG, "delay must be in (0, 1e7] ns");
+    g_delay_ns.store((unsigned long long)value);
     return VSSM_OK;
   }
   return fail(VSSM_ERR_ARG, "unknown debug knob %d", knob);
@@ -472,6 +480,8 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   a.box_y = T < kFwdChunk ? (int)T : kFwdChunk;
   a.drop_ticket = g_drop_ticket.load();
   a.wait_ns = g_wait_ns.load();
+  a.delay_ticket = g_delay_ticket.load();
+  a.delay_ns = g_delay_ns.load();
   CUtensorMap mu, mdr, mz;
   VSSM_TRY(make_map(&mu, u, io, T, D, a.box_x, a.box_y));
   VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
@@ -557,6 +567,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.box_y = T < kBwdChunk ? (int)T : kBwdChunk;
   a.drop_ticket = g_drop_ticket.load();
   a.wait_ns = g_wait_ns.load();
+  a.delay_ticket = g_delay_ticket.load();
+  a.delay_ns = g_delay_ns.load();
   CUtensorMap mu, mdr, mz, mdo, mcs, my;
   std::memset(&my, 0, sizeof(my));
   std::memset(&mu, 0, sizeof(mu));

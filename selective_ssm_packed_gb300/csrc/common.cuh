@@ -175,6 +175,12 @@ __device__ __forceinline__ int wait_flag(const int* flag, uint64_t limit_ns) {
   }
 }
 
+// Sleeps about `ns` nanoseconds (a test knob's delay; always ends).
+__device__ __forceinline__ void sleep_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
 // A carry word that holds no value yet: the all-ones NaN.  The caller fills a
 // carry array with it before the launch.  FP32 arithmetic never yields it (a
 // NaN result is the canonical 0x7fffffff) and st_carry turns it into that NaN

@@ -124,6 +124,8 @@ struct ScanArgs {
   int box_y;                  // tile rows: min(chunk, T)
   long long drop_ticket;
   unsigned long long wait_ns;
+  long long delay_ticket;       // test knob: this item sleeps delay_ns before storing its inclusive state
+  unsigned long long delay_ns;
 };
 
 cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,

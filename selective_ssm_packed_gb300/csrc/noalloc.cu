@@ -216,6 +216,8 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   a.box_y = T < kFwdChunk ? (int)T : kFwdChunk;
   a.drop_ticket = -1;
   a.wait_ns = 1000000000ull;
+  a.delay_ticket = -1;
+  a.delay_ns = 0;
   CUtensorMap mu, mdr, mz;
   int r = map2d(&mu, u, io, T, D, a.box_x, a.box_y);
   if (r == VSSM_OK) r = map2d(&mdr, delta_raw, io, T, D, a.box_x, a.box_y);

@@ -408,6 +408,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // a sequence starts in this chunk: E = 0 exactly, and the carry leaving
     // to the left does not depend on what enters from the right
     const bool rs_any = (rst & (rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u))) != 0u;
+    if ((long long)tk == a.delay_ticket) sleep_ns(a.delay_ns);  // test knob
     if (rs_any && publish) st_carry(inc + wslot * 32 + lane, tot);
     if (chunk < a.n_chunks - 1) {
       // the next chunk of the tile started long before this one and has

@@ -350,6 +350,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       st_carry1(a.incl + word(chunk, n0), v.x);
       if (kTwo) st_carry1(a.incl + word(chunk, n1), v.y);
     };
+    if ((long long)tk == a.delay_ticket) sleep_ns(a.delay_ns);  // test knob
     // a sequence starts in this chunk: the state leaving it does not depend
     // on the state entering, store it at once
     if (rs_any && publish) store_incl(tot);

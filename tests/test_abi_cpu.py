@@ -105,3 +105,7 @@ def test_debug_knobs(lib):
     assert lib.vssm_debug_set(binding.VSSM_DBG_WAIT_NS, 0) == -1
     assert lib.vssm_debug_set(binding.VSSM_DBG_WAIT_NS, 10**9) == 0
     assert lib.vssm_debug_set(binding.VSSM_DBG_DROP_FLAG, -1) == 0
+    assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_NS, 0) == -1
+    assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_NS, 10**8) == -1
+    assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_NS, 200_000) == 0
+    assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_ITEM, -1) == 0

@@ -333,9 +333,10 @@ def test_a_cut_sequence_passes_its_state_on_gpu():
 def test_conv_tails_fwd_bwd(W, dtype):
     """Conv tails of cut sequences: x_init read by the taps that reach before
     a sequence's start, x_last out, and their gradients.  Lengths shorter
-    than W-1, an empty sequence, and starts on and next to the 64-token tile
-    edges."""
-    lengths = [64, 1, 2, 0, 61, 3, 130, 40]
+    than W-1, an empty sequence, and starts just before, on and just after the
+    192-token tile edges (190, 192, 193; 384, 386, 387), with a ragged last
+    tile."""
+    lengths = [190, 2, 1, 0, 191, 2, 1, 130, 40]
     D = 136
     cu_np, T, r = rand_case(lengths, D, 4, dtype, seed=34, W=W)
     S = len(lengths)
@@ -517,6 +518,44 @@ def test_lookback_wait_timeout_is_reported_not_hung():
     # and the context is still healthy
     vs.varlen_selective_scan_fwd(u, u, A, B, B, None, None, None, cu, workspace=ws)
     assert binding.read_status(ws) == 0
+
+
+def test_lookback_walk_past_aggregates_is_bitwise_identical():
+    """One work item sleeps before it stores its inclusive state, so the items
+    after it on the same chain publish their aggregates and later items walk
+    back past them to the delayed one and re-evaluate forward.  The results
+    must equal, bit for bit, those of a run where every item finds its
+    neighbour's inclusive state, and match the oracle."""
+    lengths = [700, 1, 1100]  # long chains: few chunks hold a sequence start
+    D, N = 32, 16             # one channel tile: every chunk is on the same chain
+    cu_np, T, r = rand_case(lengths, D, N, "f32", seed=41)
+    base = run_chain(cu_np, T, r, "f32")
+    try:
+        binding.debug_set(binding.VSSM_DBG_DELAY_NS, 300_000)
+        # forward ticket 2 = chunk 2 of 15 (tokens 256..383); backward ticket 9 =
+        # chunk 47 of 57, the backward counting from the top (tokens 1504..1535);
+        # neither holds a sequence start (those are at tokens 700 and 701)
+        binding.debug_set(binding.VSSM_DBG_DELAY_ITEM, 2)
+        fwd_delayed = run_chain(cu_np, T, r, "f32", with_bwd=False)
+        # and the walk did go past aggregates: some warp published one (the
+        # workspace holds a 256-byte header, then the int32 look-back flags)
+        ws = torch.empty(binding.scan_fwd_workspace_size(T, D, N), dtype=torch.uint8, device="cuda")
+        vs.varlen_selective_scan_fwd(fwd_delayed["u"], f32(r["delta_raw"]), f32(r["A"]), f32(r["B"]), f32(r["C"]),
+                                     f32(r["Dskip"]), f32(r["z"]), f32(r["dt_bias"]), torch.from_numpy(cu_np).cuda(),
+                                     workspace=ws)
+        n_chunks = (T + 127) // 128
+        flags = ws[256:256 + 4 * n_chunks * 32].view(torch.int32)
+        assert int((flags == 1).sum()) > 0
+        binding.debug_set(binding.VSSM_DBG_DELAY_ITEM, 9)
+        bwd_delayed = run_chain(cu_np, T, r, "f32")
+    finally:
+        binding.debug_set(binding.VSSM_DBG_DELAY_ITEM, -1)
+    for k in ("u", "out", "states"):
+        assert torch.equal(fwd_delayed[k], base[k]), k
+    for k in base:
+        if isinstance(base[k], torch.Tensor):
+            assert torch.equal(bwd_delayed[k], base[k]), k
+    check_chain(cu_np, r, bwd_delayed, "f32")
 
 
 # ------------------------------------------------------------------ the named workloads
