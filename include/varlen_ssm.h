@@ -299,7 +299,10 @@ const char* vssm_last_error(void);      /* thread-local; "" if none */
  * (default 1e9).  VSSM_DBG_DELAY_ITEM: the scan work item with this ticket
  * sleeps VSSM_DBG_DELAY_NS nanoseconds (default 2e5, at most 1e7) before it
  * stores its inclusive state (-1 = off), so the items after it must walk back
- * past published aggregates; the results do not change, bit for bit.
+ * past published aggregates; the results do not change, bit for bit.  The
+ * delay applies to fp32 scan calls with N = 16 and no sequence states, which
+ * then run a build of the kernels of their own (the other builds carry no
+ * code for it); other calls ignore it.
  * Returns VSSM_OK or VSSM_ERR_ARG. */
 #define VSSM_DBG_DROP_FLAG 1
 #define VSSM_DBG_WAIT_NS 2
