@@ -320,7 +320,6 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       rs_any |= rsj[j];
       sd_tot += sdj[j];
     }
-    // exclusive scan per state; the chunk's totals stay in registers
     // A*log2e of the warp's states, picked with compile-time register indices
     float2 a2w = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -330,6 +329,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (2 * i == n1) a2w.y = A2[i].x;
       if (2 * i + 1 == n1) a2w.y = A2[i].y;
     }
+    // exclusive scan per state; the chunk's totals stay in registers
     float2 tot = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int q = 0; q < (kTwo ? 2 : 1); ++q) {
