@@ -100,6 +100,13 @@ __global__ void __launch_bounds__(256) sum_row_groups_kernel(float* __restrict__
   float* p = in + m;
   float acc = 0.0f;
   int64_t r = r0;
+  for (; r + 8 <= r1; r += 8) {  // 8 loads in flight, added in row order
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = __ldcs(p + (r + q) * ld);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc += v[q];
+  }
   for (; r + 4 <= r1; r += 4) {
     const float a0 = __ldcs(p + (r + 0) * ld), a1 = __ldcs(p + (r + 1) * ld);
     const float a2 = __ldcs(p + (r + 2) * ld), a3 = __ldcs(p + (r + 3) * ld);

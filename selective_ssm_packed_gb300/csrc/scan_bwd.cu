@@ -602,7 +602,15 @@ __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restri
   const int64_t M = T * 2 * N;
   if (i >= M) return;
   float acc = 0.0f;
-  for (int k = 0; k < n_tiles; ++k) acc += __ldcs(part + (int64_t)k * M + i);
+  int k = 0;
+  for (; k + 8 <= n_tiles; k += 8) {  // 8 loads in flight, added in tile order
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = __ldcs(part + (int64_t)(k + q) * M + i);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc += v[q];
+  }
+  for (; k < n_tiles; ++k) acc += __ldcs(part + (int64_t)k * M + i);
   const int64_t v = i / T;
   const int64_t t = i - v * T;
   if (v < N) dB[t * N + v] = acc; else dC[t * N + (v - N)] = acc;
