@@ -242,9 +242,10 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
  *     VSSM_ERR_WORKSPACE and a message naming both sizes, before anything is
  *     launched.
  *   - Every call on a device shares the array and finds the previous call's
- *     contents; the call clears what must start at zero (status, ticket,
- *     look-back flags) on `stream` before its kernels.  Calls that overlap on
- *     the GPU (other streams, other host threads) race on the array.
+ *     contents; on `stream`, before its kernels, the call clears what must
+ *     start at zero (status, ticket, look-back flags) and fills the look-back
+ *     states with all-ones words.  Calls that overlap on the GPU (other
+ *     streams, other host threads) race on the array.
  *   - status: nullable device int32 the call zeroes and into which device-side
  *     errors are OR-ed (decode with vssm_status_code); NULL keeps them in the
  *     scratch, where they cannot be read back.

@@ -13,10 +13,11 @@
 // The scratch is one file-scope __device__ array of VSSM_NOALLOC_SCRATCH_BYTES
 // (64 MiB).  Every GPU that loads this part of the library keeps it until the
 // process exits, and every call on a device uses the same array, which keeps
-// whatever the previous call left: the call clears the part that must start at
-// zero (status, work ticket, look-back flags) before launching, and calls that
-// overlap on the GPU (two streams, or two host threads on one device) race on
-// it.
+// whatever the previous call left: before launching, the call clears the part
+// that must start at zero (status, work ticket, look-back flags) and fills the
+// look-back states with the all-ones word that reads as "not stored yet".
+// Calls that overlap on the GPU (two streams, or two host threads on one
+// device) race on it.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
