@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace vssm {
@@ -240,6 +242,44 @@ __device__ __forceinline__ int wait_carry(const float2* carry, const int* flag, 
   }
 }
 
+// The same for a 128-bit carry (four 32-bit words, each single-copy atomic).
+__device__ __forceinline__ float4 ld_carry4(const float4* p) {
+  unsigned x, y, z, w;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "l"(p) : "memory");
+  return make_float4(__uint_as_float(x), __uint_as_float(y), __uint_as_float(z), __uint_as_float(w));
+}
+
+__device__ __forceinline__ bool carry_set4(float4 v) {
+  return __float_as_uint(v.x) != kCarryUnset && __float_as_uint(v.y) != kCarryUnset &&
+         __float_as_uint(v.z) != kCarryUnset && __float_as_uint(v.w) != kCarryUnset;
+}
+
+__device__ __forceinline__ void st_carry4(float4* p, float4 v) {
+  unsigned x = __float_as_uint(v.x), y = __float_as_uint(v.y), z = __float_as_uint(v.z), w = __float_as_uint(v.w);
+  x = x == kCarryUnset ? 0x7fffffffu : x;
+  y = y == kCarryUnset ? 0x7fffffffu : y;
+  z = z == kCarryUnset ? 0x7fffffffu : z;
+  w = w == kCarryUnset ? 0x7fffffffu : w;
+  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
+// wait_carry for 128-bit carries.
+__device__ __forceinline__ int wait_carry4(const float4* carry, const int* flag, uint64_t limit_ns,
+                                           float4* v) {
+  const uint64_t t0 = globaltimer_ns();
+  unsigned backoff = 32;
+  for (;;) {
+    *v = ld_carry4(carry);
+    if (__all_sync(0xffffffffu, carry_set4(*v))) return kFlagInclusive;
+    if (__all_sync(0xffffffffu, ld_acquire_gpu(flag) == kFlagAggregate)) return kFlagAggregate;
+    if (__shfl_sync(0xffffffffu, globaltimer_ns() - t0 > limit_ns, 0)) return kFlagNone;
+    __nanosleep(backoff);
+    if (backoff < 1024) backoff <<= 1;
+  }
+}
+
 // ------------------------------------------------------------------ mbarrier + TMA
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -306,6 +346,81 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
       : "memory");
 }
 
+// ------------------------------------------------------------------ tensor memory (TMEM)
+// Tensor memory is 128 lanes x 512 columns of 32-bit words per SM.  A CTA
+// allocates columns (a power of two >= 32) with one warp; warp w of the CTA
+// can then read and write the lanes 32 (w % 4) .. 32 (w % 4) + 31 of those
+// columns, one lane per thread (the .32x32b shape).  Loads and stores are
+// asynchronous: tcgen05.wait::ld / wait::st complete them.  The waits below
+// name the registers involved as in-out operands, so that the compiler can
+// neither read a loaded register before the wait nor reuse a stored one
+// before the store has taken it.
+__device__ __forceinline__ void tmem_alloc128(uint32_t* dst) {  // warp-collective
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(dst))
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc128(uint32_t taddr) {  // warp-collective
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(taddr) : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st16(uint32_t (&v)[16]) {
+  asm volatile("tcgen05.wait::st.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                 "+r"(v[14]), "+r"(v[15])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                 "+r"(v[14]), "+r"(v[15])
+               :
+               : "memory");
+}
+
+// ------------------------------------------------------------------ pairs of io values
+__device__ __forceinline__ float2 ld_io2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 ld_io2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void st_io2(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+__device__ __forceinline__ void st_io2(__nv_bfloat16* p, float2 v) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(v);
+}
+
 // ------------------------------------------------------------------ vector loads of N values
 // Loads N consecutive io values from shared memory (16-byte aligned) as floats.
 template <int N>
@@ -365,15 +480,48 @@ __device__ __forceinline__ const float* widen_rows(const T* src, float* dst, int
 }
 
 // ------------------------------------------------------------------ launch shape
-// Grid of a persistent kernel: as many CTAs as fit on the device at once (all
-// SMs x resident CTAs per SM), never more than there are work items.
+// CTAs of `kernel` that fit on one SM at once, from its registers and shared
+// memory and the SM's limits.  The kernels that allocate tensor memory use
+// this instead of the runtime's occupancy query, which answers 1 for them
+// (it cannot know how many columns a CTA takes); their callers cap the count
+// by the columns each CTA allocates.
 template <typename K>
-inline cudaError_t persistent_grid(K kernel, int threads, size_t smem, int64_t items, int* grid) {
+inline cudaError_t resident_ctas_per_sm(K kernel, int threads, size_t smem, int* per_sm) {
+  cudaFuncAttributes fa;
+  int dev = 0, regs_sm = 0, smem_sm = 0, reserved = 0, thr_sm = 0, blk_sm = 0;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev);
+  if (e != cudaSuccess) return e;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp in units of 256
+  int n = blk_sm;
+  if (regs_warp > 0) n = std::min(n, regs_sm / (regs_warp * warps));
+  n = std::min(n, smem_sm / (int)(smem + fa.sharedSizeBytes + (size_t)reserved));
+  n = std::min(n, thr_sm / threads);
+  *per_sm = n;
+  return cudaSuccess;
+}
+
+// Grid of a persistent kernel: as many CTAs as fit on the device at once (all
+// SMs x resident CTAs per SM), never more than there are work items.  With
+// max_per_sm > 0 the count per SM comes from resident_ctas_per_sm and is
+// capped at max_per_sm.
+template <typename K>
+inline cudaError_t persistent_grid(K kernel, int threads, size_t smem, int64_t items, int* grid,
+                                   int max_per_sm = 0) {
   int dev = 0, n_sm = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (e == cudaSuccess)
+    e = max_per_sm > 0 ? resident_ctas_per_sm(kernel, threads, smem, &per_sm)
+                       : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
   if (e != cudaSuccess) return e;
+  if (max_per_sm > 0 && per_sm > max_per_sm) per_sm = max_per_sm;
   const int64_t cap = (int64_t)(per_sm > 0 ? per_sm : 1) * (n_sm > 0 ? n_sm : 1);
   *grid = (int)(items < cap ? items : cap);
   return cudaSuccess;

@@ -7,10 +7,12 @@
 // looping over tickets); one thread requests each item's inputs with tensor /
 // bulk copies on one mbarrier while the previous item finishes.
 //
-// CTA = N/2 warps.  Warp w owns the state pair (2w, 2w+1) for ALL 32 tokens
-// of the item, lane l owns channel d0 + l.  The forward states therefore need
-// no scan inside the CTA: every warp starts from the saved state of the chunk
-// (chunk_states, written by the forward call) and walks its 32 tokens.
+// CTA = N/4 warps.  A thread owns one channel PAIR (lane % 16: channels 2c,
+// 2c+1 of the tile) and one state pair (warp w, lane / 16: states 2p, 2p+1,
+// p = 2w + lane / 16): four (channel, state) chains.  The paired FP32
+// instructions run over the channel pair, so the per-(token, channel) values
+// (delta, delta u, g) are used as loaded and the per-(token, state) values (B,
+// C) come from shared memory already doubled (x, x).
 //
 // With a_t = exp(delta_t A) (0 at a sequence start), b_t = delta_t u_t B_t,
 // g_t = dout_t (SiLU(z_t) + gate floor):
@@ -18,33 +20,34 @@
 //   dh_t = C_t g_t + a_{t+1} dh_{t+1}              (reverse walk; a_{t+1} = 0
 //                                                   at a sequence start, so the
 //                                                   scan resets at sequence ends)
-// The carry handed to the previous chunk is a_{t0} dh_{t0} = sum_t E_t C_t g_t
-// + E_last * (carry from the next chunk), with E_t = a_{t0} ... a_t: both terms
-// are accumulated during the FORWARD walk, so the look-back needs no extra
-// pass and no extra exponential.
+//   du_t     = delta_t sum_n dh_t B_t + Dskip g_t
+//   d delta_t = u_t sum_n dh_t B_t + sum_n A dh_t p_t,   p_t = a_t h_{t-1}
+//   dA       = sum_t delta_t dh_t p_t,  dB_t = sum_d dh_t delta_t u_t,  dC_t = sum_d g_t h_t
 //
-//   1. Per-(token, channel) values once per item, by all threads: delta,
-//      delta u, g, d delta / d delta_raw, in [channel][token] arrays; B and C
-//      transposed to [state][token] (fp32).
-//   2. Forward walk per warp: states h_t kept in registers (32 tokens x 2
-//      states); E and the carry aggregate accumulated; dC_t[n] contributions
-//      g_t h_t summed over the tile's channels (ColSum16 shuffle butterflies,
-//      fed token by token); C_t.h_t partials for y.
-//   3. Decoupled look-back per warp towards HIGHER chunks for the carry
+//   1. Per-(token, channel) values once per item: delta (softplus), delta u,
+//      g, d delta / d delta_raw into [channel pair][token] arrays, and dz from
+//      the forward's pre-gate output y (so the gate is evaluated once); B and C
+//      doubled per state pair; a per-token exponent offset (-inf at a start).
+//   2. Forward walk per thread from the saved state of the chunk: p_t goes to
+//      TENSOR MEMORY (4 words per token, 128 columns per warp) for the reverse
+//      walk, so the history costs no registers; the left-going carry aggregate
+//      sum_t E_t C_t g_t (E_t = a_t0 ... a_t) is accumulated on the way; dC
+//      sums over the tile's channels by shuffle butterflies.
+//   3. Decoupled look-back per thread towards HIGHER chunks for the carry
 //      entering from the right; aggregates re-applied in a fixed order
 //      (bitwise repeatable); time-bounded waits.  An inclusive carry is its
-//      own flag (the carry array starts filled with a NaN word that no
-//      stored value equals), so it is stored and read with no fence; only an
-//      aggregate is announced by a flag, behind a fence.
-//   4. Reverse walk per warp in blocks of 8 tokens: dA (per thread), dB
-//      contributions (ColSum16), partial sums over the warp's states
-//      for du and d delta; after each block all threads add the warps'
-//      partials in a fixed order and write du, d delta_raw and dz (with
-//      y = the forward's pre-gate output when the call passes it, else the
-//      warps' C.h partials + Dskip u).
-//   5. dA partials per chunk; fixed-order CTA sums for dDskip, d_dt_bias.
+//      own flag (the carry array starts filled with a NaN word that no stored
+//      value equals); only an aggregate is announced by a flag, behind a fence.
+//   4. Reverse walk in blocks of 4 tokens, reading p_t back from tensor
+//      memory: dA per thread, dB by shuffle butterflies, and per-thread
+//      partial sums over its 2 states of sum_n dh B and sum_n A dh p, added
+//      over the state pairs after each block (fixed order) into du and
+//      d delta_raw.
+//   5. dA partials per chunk; fixed-order CTA sums for dDskip and d_dt_bias.
 // Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
 // and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,14 +56,15 @@ namespace vssm {
 namespace {
 
 constexpr int kL = kBwdChunk;   // 32 tokens per work item
-constexpr int kP = kL + 4;      // row pitch of the [channel][token] arrays
-constexpr int kPP = kL + 2;     // token pitch (in pairs) of the paired B / C arrays
-constexpr int kRB = 8;          // tokens per block of the reverse walk
+constexpr int kCP = kTile / 2;  // 16 channel pairs per item
+constexpr int kPT = kL + 2;     // token pitch (in pairs) of the [channel pair][token] arrays
+constexpr int kRB = 4;          // tokens per block of the reverse walk
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <typename T, int N>
+template <typename T, int N, bool kRecY>
 struct BwdSmem {
-  static constexpr int W = N / 2;  // warps = state pairs
+  static constexpr int NW = N / 4;   // warps
+  static constexpr int NSP = N / 2;  // state pairs
   // ---- inputs of one work item, written by tensor / bulk copies and refilled
   //      for the next item once this one has read them for the last time
   alignas(128) T u[kL * kTile];
@@ -75,48 +79,53 @@ struct BwdSmem {
   alignas(16) float bias[kTile];
   alignas(16) float dsk[kTile];
   alignas(16) int pos[kL];
-  // ---- per-(token, channel) values, [channel][token] with pitch kP: a lane
-  //      reads 4 tokens of its channel with one conflict-free 16-byte access
-  alignas(16) float dl[kTile * kP];   // delta
-  alignas(16) float dlu[kTile * kP];  // delta * u
-  alignas(16) float g[kTile * kP];    // dout * SiLU(z)
-  alignas(16) float sg[kTile * kP];   // d delta / d delta_raw
-  // ---- B, C paired per warp, fp32 (zero past the last token): entry
-  //      [o][w][t] of BP is (B_t[2w], B_t[2w+1]) for o = 0 and the swapped
-  //      pair for o = 1, so a lane loads its state pair, in its own order,
-  //      for 2 tokens with one 16-byte access and feeds it to the paired FP32
-  //      instructions as loaded; the pitch kPP keeps the stores conflict-free
-  alignas(16) float BP[2 * W * kPP * 2];
-  alignas(16) float CP[2 * W * kPP * 2];
-  // ---- exponent offset per token: -inf at a sequence start, else 0
-  alignas(16) float off[kL];
-  // ---- cross-warp partials: C.h of each warp's state pair [W][kL][kTile]
-  //      from the forward walk, and (du, d delta) partials
-  //      [2][W][kRB][kTile] float2 from each block of the reverse walk
-  alignas(16) float ypart[W * kL * kTile];
-  alignas(16) float part[W * kL * kTile];
-  float redD[W * kTile];
-  float redB[W * kTile];
+  // ---- per-(token, channel pair) values, [channel pair][token] float2 with
+  //      token pitch kPT: a lane reads 2 tokens of its pair with one 16-byte
+  //      access, the 8 lanes of an access phase in distinct banks
+  alignas(16) float2 dl[kCP * kPT];   // delta
+  alignas(16) float2 dlu[kCP * kPT];  // delta * u
+  alignas(16) float2 g[kCP * kPT];    // dout * (SiLU(z) + gate floor)
+  alignas(16) float2 sg[kCP * kPT];   // d delta / d delta_raw
+  alignas(16) float2 dzf[kRecY ? kCP * kPT : 2];  // d out / d y, when y is recomputed
+  // ---- B and C doubled, [token][state pair][order] float4: order 0 holds
+  //      (B[2p], B[2p], B[2p+1], B[2p+1]), order 1 the two states swapped, the
+  //      order the lanes with bit 3 set keep (see ColSum8); zero past the last
+  //      token.  Token-major, so that the four entries a warp reads for a
+  //      token are adjacent (one bank-conflict-free access)
+  alignas(16) float4 BD[kL * NSP * 2];
+  alignas(16) float4 CD[kL * NSP * 2];
+  // ---- exponent offset per token pair (off_t, off_t, off_t+1, off_t+1): -inf
+  //      at a sequence start, else 0
+  alignas(16) float4 off[kL / 2];
+  // ---- partial sums over each thread's state pair from the reverse walk,
+  //      [buffer][token of the block][state pair][channel pair] float4 =
+  //      (sum dh B for the pair's two channels, sum A dh p for them)
+  alignas(16) float4 nred[2 * kRB * NSP * kCP];
+  alignas(16) float2 nY[kRecY ? 2 * kRB * NSP * kCP : 2];  // C.h partials, when y is recomputed
+  alignas(16) float2 redD[32 * NW];
+  alignas(16) float2 redB[32 * NW];
+  uint32_t taddr;
   int ticket;
   alignas(8) uint64_t bar;
 };
 
-// Column sums over the 32 lanes of a warp (lane = channel) for groups of 16
-// tokens x 2 states, fed one token at a time by shuffle butterflies.  A lane
-// keeps its state pair in its own order, the "first" state being n0 + bit4:
-//   level 1 (every token): lanes l, l^16 exchange the state the other keeps,
-//   level 2 (every token pair): lanes l, l^8 exchange the token the other
-//     keeps (bit 3 picks the odd token),
-//   levels 3, 4, 5 likewise over lane bits 2, 1, 0 for pairs of pairs, ...
-// After the 16th token, lane l holds the sum over all 32 lanes for token
-// 8 b0 + 4 b1 + 2 b2 + b3 of the group (b_i = bit i of l) and its first
-// state.  The pairing is fixed, so the sums are bitwise repeatable; tokens may
-// come in ascending or descending order.
-struct ColSum16 {
-  float p1[2], p2[2], p3[2], p4[2];  // pending sums, by the parity of the token group at each level
+// Column sums over the 16 lanes of a half warp (lane % 16 = channel pair) for
+// groups of 8 tokens x 2 states, fed one token at a time by shuffle
+// butterflies.  A lane keeps its state pair in its own order, the "first"
+// state being 2p + bit3(lane):
+//   level 1 (every token): lanes l, l^8 exchange the state the other keeps,
+//   level 2 (every token pair): lanes l, l^4 exchange the token the other
+//     keeps (bit 2 picks the odd token),
+//   levels 3, 4 likewise over lane bits 1, 0 for pairs of pairs, ...
+// After the 8th token, lane l holds the sum over the half warp for token
+// 4 b0 + 2 b1 + b2 of the group (b_i = bit i of l) and its first state.  The
+// pairing is fixed, so the sums are bitwise repeatable; tokens may come in
+// ascending or descending order.
+struct ColSum8 {
+  float p1[2], p2[2], p3[2];  // pending sums, by the parity of the token group at each level
 
   static __device__ __forceinline__ int token(int lane) {
-    return 8 * (lane & 1) + 4 * ((lane >> 1) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 3) & 1);
+    return 4 * (lane & 1) + 2 * ((lane >> 1) & 1) + ((lane >> 2) & 1);
   }
 
   static __device__ __forceinline__ float combine(float lo, float hi, int lane, int mask) {
@@ -124,21 +133,29 @@ struct ColSum16 {
     return (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, mask);
   }
 
-  // Token c (0..15) of the group with this lane's values in its state order;
-  // returns true once the group is complete (*sum then holds the lane's result).
-  __device__ __forceinline__ bool feed(int c, bool ascending, float2 v, int lane, float* sum) {
-    p1[c & 1] = v.x + __shfl_xor_sync(0xffffffffu, v.y, 16);
+  // Token c (0..7) of the group with this lane's two values in its state
+  // order; returns true once the group is complete (*sum then holds the result).
+  __device__ __forceinline__ bool feed(int c, bool ascending, float vF, float vS, int lane, float* sum) {
+    p1[c & 1] = vF + __shfl_xor_sync(0xffffffffu, vS, 8);
     if ((c & 1) != (ascending ? 1 : 0)) return false;
-    p2[(c >> 1) & 1] = combine(p1[0], p1[1], lane, 8);
+    p2[(c >> 1) & 1] = combine(p1[0], p1[1], lane, 4);
     if ((c & 3) != (ascending ? 3 : 0)) return false;
-    p3[(c >> 2) & 1] = combine(p2[0], p2[1], lane, 4);
+    p3[(c >> 2) & 1] = combine(p2[0], p2[1], lane, 2);
     if ((c & 7) != (ascending ? 7 : 0)) return false;
-    p4[(c >> 3) & 1] = combine(p3[0], p3[1], lane, 2);
-    if ((c & 15) != (ascending ? 15 : 0)) return false;
-    *sum = combine(p4[0], p4[1], lane, 1);
+    *sum = combine(p3[0], p3[1], lane, 1);
     return true;
   }
 };
+
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  const float2 l = __fadd2_rn(lo2(a), lo2(b)), h = __fadd2_rn(hi2(a), hi2(b));
+  return make_float4(l.x, l.y, h.x, h.y);
+}
+__device__ __forceinline__ float hsum(float2 v) { return v.x + v.y; }
+__device__ __forceinline__ uint32_t fbits(float v) { return __float_as_uint(v); }
+__device__ __forceinline__ float bitsf(uint32_t v) { return __uint_as_float(v); }
 
 // Publishes a warp's look-back payload: every lane has stored its part; the
 // fence orders each lane's stores before the barrier, and lane 0 then sets the
@@ -151,23 +168,30 @@ __device__ __forceinline__ void publish_flag(int* flag, int value, bool publish,
 
 // kStates: the call passes sequence states (initial states, final-state or
 // starting-state gradients); without them the kernel carries no code for them.
-template <typename T, int N, bool kStates, bool kKnob>
-__global__ void __launch_bounds__(16 * N, 512 / (16 * N))
+// kRecY: the call has z but no y, so dz needs y = C.h + Dskip u recomputed
+// (the reverse walk adds C.h partials).
+template <typename T, int N, bool kStates, bool kRecY, bool kKnob>
+__global__ void __launch_bounds__(8 * N, N == 16 ? 3 : 4)
 scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
                 const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_y,
                 const ScanArgs a) {
-  using SM = BwdSmem<T, N>;
-  constexpr int W = SM::W;
-  constexpr int kThr = 32 * W;
+  using SM = BwdSmem<T, N, kRecY>;
+  constexpr int NW = SM::NW, NSP = SM::NSP;
+  constexpr int kThr = 32 * NW;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int n_items = a.n_chunks * a.n_tiles;
+  const int cp = lane & 15;                        // channel pair of the tile
+  const int sp = 2 * w + (lane >> 4);              // state pair
+  const int o = (lane >> 3) & 1;                   // this lane's state order
+  const int nF = 2 * sp + o, nS = 2 * sp + 1 - o;  // its "first" and "second" state
+  const int c0 = 2 * cp;                           // first channel of the pair (in the tile)
 
   // Requests every input of work item `tkn` on the barrier: u, delta_raw,
-  // dout, z (and y) tiles; B and C rows; A rows, dt_bias, Dskip and the saved states
-  // of the tile's channels; position indices (whole groups of 4 tokens).
+  // dout, z (and y) tiles; B and C rows; A rows, dt_bias, Dskip and the saved
+  // states of the tile's channels; position indices (whole groups of 4 tokens).
   auto issue = [&](int tkn) {
     const int rv = tkn / a.n_tiles;
     const int tl = tkn - rv * a.n_tiles;
@@ -196,6 +220,9 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
   };
 
+  // tensor memory for the forward walk's history: 128 columns, warp w on the
+  // lanes 32 (w % 4) .. +31 (the CTA has at most 4 warps)
+  if (w == 0) tmem_alloc128(&sm.taddr);
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
@@ -203,20 +230,23 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     sm.ticket = first;
     if (first < n_items) issue(first);
   }
+  tmem_fence_before_sync();
   __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t thist = sm.taddr + ((uint32_t)(32 * (w & 3)) << 16);
 
-  // Persistent loop: one work item per pass.  The next ticket is drawn once
-  // this item has read its inputs for the last time and its copies land while
-  // this item writes its last partials.  An earlier draw would hold tickets
-  // back from the look-back chains (an item whose neighbour sits reserved
-  // behind a running item waits for both).  Items only ever wait on items
-  // with smaller tickets, all of which are done or in hand of a running CTA,
-  // so the loop cannot deadlock.
+  // Persistent loop: one work item per pass.  The next ticket is drawn in
+  // the last block of the reverse walk and its inputs are requested once this
+  // item has read its own for the last time.  An earlier draw would hold
+  // tickets back from the look-back chains (an item whose neighbour sits
+  // reserved behind a running item waits for both).  Items only ever wait on
+  // items with smaller tickets, all of which are done or in hand of a running
+  // CTA, so the loop cannot deadlock.
   for (uint32_t it = 0;; ++it) {
   const int tk = sm.ticket;
   if (tk >= n_items) break;
   // test knob (its own instantiation, so the others carry no code for it):
-  // this item starts late, so its inclusive state is stored late and the
+  // this item starts late, so its inclusive carry is stored late and the
   // items after it on the chain walk back past their aggregates
   if constexpr (kKnob) {
     if ((long long)tk == a.delay_ticket) sleep_ns(a.delay_ns);
@@ -229,98 +259,84 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const int rows4 = rows & ~3;
   const int d0 = tile * kTile;
   const int bx = a.box_x;
-  const int d = d0 + lane;
-  const bool valid = lane < bx && d < a.D;
+  const int d = d0 + c0;                       // first channel of this thread's pair
+  const bool valid = c0 < bx && d < a.D;       // D is even, so the pair is whole
 
   if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
+    // the copies did not land within the limit: report it, give them a
+    // second limit to complete (so that no copy is left writing into this
+    // CTA's shared memory once it has exited), and stop
     if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
+    mbar_wait(&sm.bar, it & 1u, a.wait_ns);
     break;
   }
 
-  // ---- 1. per-(token, channel) values; all zero past the last token and on
-  //         channels past D (a = 1, b = 0, g = 0 there), so that those feed
-  //         exactly 0 into every sum they enter
-  // a warp's 32 lanes take 8 channels x 4 tokens: the [channel][token]
-  // stores then hit 32 different banks.  Straight-line code over the thread's
-  // kPer elements (no per-element branches), so their exp / log chains overlap;
-  // out-of-range elements are computed on whatever the buffers hold and then
-  // replaced by zeros with selects.
+  // ---- 1. per-(token, channel pair) values; all zero past the last token and
+  //         on channels past D (a = 1, b = 0, g = 0 there), so that those feed
+  //         exactly 0 into every sum they enter.  Lanes take 16 pairs x 2
+  //         tokens; a thread keeps the same pair (tid % 16) throughout.
+  float2 accD = make_float2(0.0f, 0.0f);  // dDskip partial: sum g u of this thread's pair
   {
-    constexpr int kPer = kL * kTile / kThr;
-    float rv[kPer], uv[kPer], gov[kPer], dlv[kPer], sgv[kPer], gv[kPer];
-    int cs[kPer], ts[kPer];
-    bool ok[kPer];
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int i = tid + q * kThr;
-      const int b = i >> 5, l = i & 31;
-      const int c = 8 * (b & 3) + (l >> 2), t = 4 * (b >> 2) + (l & 3);
-      cs[q] = c;
-      ts[q] = t;
-      ok[q] = t < rows && c < bx && d0 + c < a.D;
-      rv[q] = to_f(sm.dr[t * bx + c]) + (a.dt_bias ? sm.bias[c] : 0.0f);
-      uv[q] = to_f(sm.u[t * bx + c]);
-      gov[q] = to_f(sm.dout[t * bx + c]);
-      gv[q] = a.has_z ? to_f(sm.z[t * bx + c]) : 0.0f;
-    }
-    if (a.delta_softplus) {
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) dlv[q] = softplus_sig(rv[q], &sgv[q]);
-    } else {
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        dlv[q] = rv[q];
-        sgv[q] = 1.0f;
+    T* gdz = static_cast<T*>(a.dz);
+    const float2 bias2 = a.dt_bias ? make_float2(sm.bias[c0 & 31], sm.bias[(c0 + 1) & 31]) : make_float2(0.0f, 0.0f);
+#pragma unroll 2
+    for (int i = tid; i < kL * kCP; i += kThr) {
+      const int t = i >> 4;
+      const int at = t * bx + c0;  // raw tiles are [token][bx]
+      const bool ok = t < rows && valid;
+      const float2 rr = __fadd2_rn(ld_io2(sm.dr + at), bias2);
+      const float2 uu = ld_io2(sm.u + at);
+      const float2 go = ld_io2(sm.dout + at);
+      float2 dl2, sg2;
+      if (a.delta_softplus) {
+        dl2.x = softplus_sig(rr.x, &sg2.x);
+        dl2.y = softplus_sig(rr.y, &sg2.y);
+      } else {
+        dl2 = rr;
+        sg2 = make_float2(1.0f, 1.0f);
       }
-    }
-    if (a.has_z) {
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) gv[q] = gov[q] * (siluf(gv[q]) + a.gate_floor);
-    } else {
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) gv[q] = gov[q];
-    }
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int at = cs[q] * kP + ts[q];
-      const float dl_q = ok[q] ? dlv[q] : 0.0f;
-      sm.dl[at] = dl_q;
-      sm.dlu[at] = ok[q] ? dl_q * uv[q] : 0.0f;
-      sm.g[at] = ok[q] ? gv[q] : 0.0f;
-      sm.sg[at] = ok[q] ? sgv[q] : 0.0f;
+      float2 gv = go;
+      if (a.has_z) {
+        const float2 zz = ld_io2(sm.z + at);
+        const float2 s = make_float2(sigmoidf_fast(zz.x), sigmoidf_fast(zz.y));
+        gv = mul2(go, fma2(zz, s, splat2(a.gate_floor)));
+        // d out / d y, and dz = dout SiLU'(z) y (SiLU'(z) = s (1 + z (1 - s)))
+        const float2 f = mul2(mul2(go, s), fma2(zz, make_float2(1.0f - s.x, 1.0f - s.y), splat2(1.0f)));
+        if (a.has_y) {
+          if (ok) st_io2(gdz + (t0 + t) * a.D + d, mul2(f, ld_io2(sm.y + at)));
+        } else if constexpr (kRecY) {
+          sm.dzf[cp * kPT + t] = ok ? f : make_float2(0.0f, 0.0f);
+        }
+      }
+      const float2 z0 = make_float2(0.0f, 0.0f);
+      sm.dl[cp * kPT + t] = ok ? dl2 : z0;
+      sm.dlu[cp * kPT + t] = ok ? mul2(dl2, uu) : z0;
+      sm.g[cp * kPT + t] = ok ? gv : z0;
+      sm.sg[cp * kPT + t] = ok ? sg2 : z0;
+      if (ok) accD = fma2(gv, uu, accD);
     }
   }
-#pragma unroll
-  for (int i = tid; i < N * kL; i += kThr) {
-    const int t = i / N, n = i - t * N;  // consecutive lanes: consecutive states
-    const int pw = n >> 1, e = n & 1;
-    const float bv = t < rows ? to_f(sm.B[t * N + n]) : 0.0f;
-    const float cv = t < rows ? to_f(sm.C[t * N + n]) : 0.0f;
-    sm.BP[(pw * kPP + t) * 2 + e] = bv;
-    sm.BP[((W + pw) * kPP + t) * 2 + 1 - e] = bv;
-    sm.CP[(pw * kPP + t) * 2 + e] = cv;
-    sm.CP[((W + pw) * kPP + t) * 2 + 1 - e] = cv;
+  // one (token, state pair) per thread: consecutive lanes read consecutive
+  // pairs of a row and write adjacent entries
+  for (int i = tid; i < kL * NSP; i += kThr) {
+    const int t = i / NSP, pn = i - t * NSP;
+    const bool in = t < rows;
+    const float2 b = in ? ld_io2(sm.B + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
+    const float2 c = in ? ld_io2(sm.C + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
+    sm.BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
+    sm.BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
+    sm.CD[2 * i] = make_float4(c.x, c.x, c.y, c.y);
+    sm.CD[2 * i + 1] = make_float4(c.y, c.y, c.x, c.x);
   }
   // bit t: token t starts a sequence
   const unsigned rst =
       __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
-  // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
-  if (w == 0) sm.off[lane] = ((rst >> lane) & 1u) ? -INFINITY : 0.0f;
-  // the warp's state pair, in this lane's order: "first" = n0 + bit4(lane)
-  // (the column-sum butterflies keep a lane's first state)
-  const int n0 = 2 * w;
-  const int nF = n0 + ((lane >> 4) & 1), nS = n0 + 1 - ((lane >> 4) & 1);
-  const float* const bp = sm.BP + ((((lane >> 4) & 1) * W + w) * kPP) * 2;  // this lane's pairs
-  const float* const cp = sm.CP + ((((lane >> 4) & 1) * W + w) * kPP) * 2;
-  float2 A2 = make_float2(0.0f, 0.0f), h = make_float2(0.0f, 0.0f);
-  if (valid) {
-    A2 = make_float2(sm.Araw[lane * N + nF], sm.Araw[lane * N + nS]);
-    // the rows hold A or A_log (A = -exp(A_log)); kept scaled by log2 e for ex2
-    if (a.a_log) A2 = make_float2(-ex2(A2.x * kLog2e), -ex2(A2.y * kLog2e));
-    A2 = make_float2(A2.x * kLog2e, A2.y * kLog2e);
-    h = make_float2(sm.H[nF * bx + lane], sm.H[nS * bx + lane]);
+  if (w == 0 && lane < kL / 2) {
+    // ex2(-inf) = 0: the transition factor of a sequence's first token, for any A
+    const float o0 = ((rst >> (2 * lane)) & 1u) ? -INFINITY : 0.0f;
+    const float o1 = ((rst >> (2 * lane + 1)) & 1u) ? -INFINITY : 0.0f;
+    sm.off[lane] = make_float4(o0, o0, o1, o1);
   }
-  const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
   // Sequence-state events of this item, bit t for token t of the chunk:
   //   evH: a sequence starts from a given initial state,
   //   evG: a sequence starts and the gradient reaching its initial state is asked for,
@@ -338,100 +354,138 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       evF = ends & live;
     }
   }
-  // the (nF, nS) entries of a sequence-state row for token t's sequence
-  auto state_pair = [&](const float* st, int t) {
+  // a sequence-state row entry pair (channels d, d+1) of state n for token t's sequence
+  auto state_pair = [&](const float* st, int t, int n) {
     if (!valid) return make_float2(0.0f, 0.0f);
-    const float2 v = __ldg(reinterpret_cast<const float2*>(st + ((int64_t)a.seq[t0 + t] * a.D + d) * N + n0));
-    return (lane & 16) ? make_float2(v.y, v.x) : v;
+    const float* row = st + ((int64_t)a.seq[t0 + t] * a.D + d) * N + n;
+    return make_float2(__ldg(row), __ldg(row + N));
   };
   __syncthreads();
 
-  // ---- 2. forward walk over the 32 tokens (state pair n0, n0+1)
-  float2 hist[kL];
-  float2 E = make_float2(1.0f, 1.0f), tot = make_float2(0.0f, 0.0f);
-  ColSum16 colsum;
-  // the forward walk's dC sums (one per lane and 16-token group), stored only
-  // after the look-back, so that a fence there does not wait for them
-  float dcs[kL / 16];
+  // the thread's A pairs (A * log2 e for ex2; the rows hold A or A_log) and
+  // the saved states at the chunk start
+  float2 AF = make_float2(0.0f, 0.0f), AS = make_float2(0.0f, 0.0f);
+  float2 hF = make_float2(0.0f, 0.0f), hS = make_float2(0.0f, 0.0f);
+  if (valid) {
+    AF = make_float2(sm.Araw[c0 * N + nF], sm.Araw[(c0 + 1) * N + nF]);
+    AS = make_float2(sm.Araw[c0 * N + nS], sm.Araw[(c0 + 1) * N + nS]);
+    if (a.a_log) {
+      AF = make_float2(-ex2(AF.x * kLog2e), -ex2(AF.y * kLog2e));
+      AS = make_float2(-ex2(AS.x * kLog2e), -ex2(AS.y * kLog2e));
+    }
+    AF = mul2(AF, splat2(kLog2e));
+    AS = mul2(AS, splat2(kLog2e));
+    hF = *reinterpret_cast<const float2*>(sm.H + nF * bx + c0);
+    hS = *reinterpret_cast<const float2*>(sm.H + nS * bx + c0);
+  }
+  const float2* const dlr = sm.dl + cp * kPT;
+  const float2* const dur = sm.dlu + cp * kPT;
+  const float2* const gr = sm.g + cp * kPT;
+  const float4* const bdr = sm.BD + sp * 2 + o;  // entry of token t at [t * 2 NSP]
+  const float4* const cdr = sm.CD + sp * 2 + o;
+  float* const pdB = a.part_dBC + ((int64_t)tile * 2 * N + nF) * a.T + t0;
+  float* const pdC = a.part_dBC + ((int64_t)tile * 2 * N + N + nF) * a.T + t0;
+
+  // ---- 2. forward walk over the 32 tokens; p_t = a_t h_{t-1} to tensor memory
+  float2 EF = make_float2(1.0f, 1.0f), ES = make_float2(1.0f, 1.0f);
+  float2 totF = make_float2(0.0f, 0.0f), totS = make_float2(0.0f, 0.0f);
   {
-    constexpr bool kEv = kStates;
-    const float* rowc = sm.dl + lane * kP;
+    ColSum8 colsum;
+#pragma unroll 1
+    for (int g8 = 0; g8 < kL / 8; ++g8) {
+      uint32_t hist[16];
 #pragma unroll
-    for (int kb = 0; kb < kL / 4; ++kb) {
-      const float4 dl4 = *reinterpret_cast<const float4*>(rowc + 4 * kb);
-      const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
-      const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
-      const float4 b01 = *reinterpret_cast<const float4*>(bp + 8 * kb);
-      const float4 b23 = *reinterpret_cast<const float4*>(bp + 8 * kb + 4);
-      const float4 c01 = *reinterpret_cast<const float4*>(cp + 8 * kb);
-      const float4 c23 = *reinterpret_cast<const float4*>(cp + 8 * kb + 4);
-      const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
-      const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
-      const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
-      const float dua[4] = {du4.x, du4.y, du4.z, du4.w};
-      const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
-      const float2 Ba[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w), make_float2(b23.x, b23.y),
-                            make_float2(b23.z, b23.w)};
-      const float2 Ca[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
-                            make_float2(c23.z, c23.w)};
+      for (int e = 0; e < 8; e += 2) {
+        const int t = 8 * g8 + e;
+        const float4 dl4 = *reinterpret_cast<const float4*>(dlr + t);
+        const float4 du4 = *reinterpret_cast<const float4*>(dur + t);
+        const float4 g4 = *reinterpret_cast<const float4*>(gr + t);
+        const float4 of4 = sm.off[t >> 1];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = 4 * kb + e;
-        const float2 at = make_float2(ex2(fmaf(dla[e], A2.x, ofa[e])), ex2(fmaf(dla[e], A2.y, ofa[e])));
-        const float2 Ct = Ca[e];
-        h = fma2(at, h, mul2(splat2(dua[e]), Ba[e]));
-        if constexpr (kEv) {
-          if ((evH >> t) & 1u)  // a start from a given state: h = a h_init + b, a's own value
-            h = fma2(make_float2(ex2(dla[e] * A2.x), ex2(dla[e] * A2.y)), state_pair(a.h_init, t), h);
+        for (int j = 0; j < 2; ++j) {
+          const int tt = t + j, e2 = e + j;
+          const float2 dlp = j ? hi2(dl4) : lo2(dl4);
+          const float2 dup = j ? hi2(du4) : lo2(du4);
+          const float2 gp = j ? hi2(g4) : lo2(g4);
+          const float2 ofp = j ? hi2(of4) : lo2(of4);
+          const float4 bd = bdr[tt * 2 * NSP], cd = cdr[tt * 2 * NSP];
+          const float2 aF = ex2x2(fma2(dlp, AF, ofp)), aS = ex2x2(fma2(dlp, AS, ofp));
+          float2 pF = mul2(aF, hF), pS = mul2(aS, hS);
+          if constexpr (kStates) {
+            if ((evH >> tt) & 1u) {  // a start from a given state: p = a h_init, a's own value
+              pF = mul2(ex2x2(mul2(dlp, AF)), state_pair(a.h_init, tt, nF));
+              pS = mul2(ex2x2(mul2(dlp, AS)), state_pair(a.h_init, tt, nS));
+            }
+          }
+          hF = fma2(dup, lo2(bd), pF);
+          hS = fma2(dup, hi2(bd), pS);
+          EF = mul2(EF, aF);
+          ES = mul2(ES, aS);
+          totF = fma2(EF, mul2(lo2(cd), gp), totF);
+          totS = fma2(ES, mul2(hi2(cd), gp), totS);
+          if constexpr (kStates) {
+            // the gradient reaching a final state joins dh_t, and the left carry through E_t
+            if ((evF >> tt) & 1u) {
+              totF = fma2(EF, state_pair(a.dh_final, tt, nF), totF);
+              totS = fma2(ES, state_pair(a.dh_final, tt, nS), totS);
+            }
+          }
+          const int hw = 4 * (e2 & 3);
+          hist[hw + 0] = fbits(pF.x);
+          hist[hw + 1] = fbits(pF.y);
+          hist[hw + 2] = fbits(pS.x);
+          hist[hw + 3] = fbits(pS.y);
+          // dC contributions g_t h_t over the pair's channels, then over the tile's
+          float sum;
+          if (colsum.feed(e2, true, hsum(mul2(gp, hF)), hsum(mul2(gp, hS)), lane, &sum)) {
+            const int ts = 8 * g8 + ColSum8::token(lane);
+            if (ts < rows) pdC[ts] = sum;
+          }
+          if ((e2 & 3) == 3) {
+            __syncwarp();  // the tensor-memory instructions are warp-collective
+            tmem_st16(thist + (uint32_t)(4 * (tt & ~3)), hist);
+            tmem_wait_st16(hist);
+          }
         }
-        hist[t] = h;
-        E = mul2(E, at);
-        tot = fma2(E, mul2(Ct, splat2(ga[e])), tot);
-        if constexpr (kEv) {
-          // the gradient reaching a final state joins dh_t, and the left carry through E_t
-          if ((evF >> t) & 1u) tot = fma2(E, state_pair(a.dh_final, t), tot);
-        }
-        if (a.has_z && !a.has_y) sm.ypart[(w * kL + t) * kTile + lane] = fmaf(Ct.x, h.x, Ct.y * h.y);
-        // dC contributions g_t h_t, summed over the tile's channels
-        colsum.feed(t & 15, true, mul2(splat2(ga[e]), h), lane, &dcs[t >> 4]);
       }
     }
   }
 
-  // ---- 3. decoupled look-back towards higher chunks (every warp for its pair)
-  float2 x = make_float2(0.0f, 0.0f);
+  // ---- 3. decoupled look-back towards higher chunks (one chain per thread)
+  float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   {
     const int64_t base = (int64_t)tile * a.n_chunks;
-    const int64_t wslot = (base + chunk) * W + w;
+    const int64_t wslot = (base + chunk) * kThr + tid;
     const bool publish = (long long)tk != a.drop_ticket;
-    float2* const agg = reinterpret_cast<float2*>(a.agg);
-    float2* const aggp = reinterpret_cast<float2*>(a.agg_sd);
-    float2* const inc = reinterpret_cast<float2*>(a.incl);
+    float4* const agg = reinterpret_cast<float4*>(a.agg);
+    float4* const aggp = reinterpret_cast<float4*>(a.agg_sd);
+    float4* const inc = reinterpret_cast<float4*>(a.incl);
     // the carry words are their own flags (filled with kCarryUnset before the
     // launch); only an aggregate, published when the walk must go further,
     // is announced by the warp's flag
-    int* const my_flag = a.flags + wslot;
+    int* const my_flag = a.flags + (base + chunk) * NW + w;
+    const float4 tot = make_float4(totF.x, totF.y, totS.x, totS.y);
+    const float4 E = make_float4(EF.x, EF.y, ES.x, ES.y);
     // a sequence starts in this chunk: E = 0 exactly, and the carry leaving
     // to the left does not depend on what enters from the right
     const bool rs_any = (rst & (rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u))) != 0u;
-    if (rs_any && publish) st_carry(inc + wslot * 32 + lane, tot);
+    if (rs_any && publish) st_carry4(inc + wslot, tot);
     if (chunk < a.n_chunks - 1) {
       // the next chunk of the tile started long before this one and has
       // usually stored its inclusive carry: look first, and publish this
       // chunk's aggregate only when the walk has to go further
       int j = chunk + 1, found = -1, timed_out = 0;
-      float2 v = ld_carry(inc + ((base + j) * W + w) * 32 + lane);
-      if (__all_sync(0xffffffffu, carry_set(v))) {
+      float4 v = ld_carry4(inc + (base + j) * kThr + tid);
+      if (__all_sync(0xffffffffu, carry_set4(v))) {
         found = j;
       } else {
         if (!rs_any) {
-          agg[wslot * 32 + lane] = tot;
-          aggp[wslot * 32 + lane] = E;
+          agg[wslot] = tot;
+          aggp[wslot] = E;
           publish_flag(my_flag, kFlagAggregate, publish, lane);
         }
         while (j < a.n_chunks) {
-          const int f = wait_carry(inc + ((base + j) * W + w) * 32 + lane, a.flags + (base + j) * W + w,
-                                   a.wait_ns, &v);
+          const int f = wait_carry4(inc + (base + j) * kThr + tid, a.flags + (base + j) * NW + w, a.wait_ns, &v);
           if (f == kFlagInclusive) { found = j; break; }
           if (f == kFlagNone) { timed_out = 1; break; }
           ++j;
@@ -444,152 +498,196 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         last = found - 1;
       }
       for (int i = last; i > chunk; --i) {
-        const int64_t ws = ((base + i) * W + w) * 32 + lane;
-        x = fma2(__ldcg(aggp + ws), x, __ldcg(agg + ws));
+        const int64_t ws = (base + i) * kThr + tid;
+        const float4 p = __ldcg(aggp + ws), q = __ldcg(agg + ws);
+        const float2 lo = fma2(lo2(p), lo2(x), lo2(q)), hi = fma2(hi2(p), hi2(x), hi2(q));
+        x = make_float4(lo.x, lo.y, hi.x, hi.y);
       }
     }
     // stored at once: the previous chunk of the tile may already be waiting,
     // and every link of that chain adds this item's delay
-    if (!rs_any && publish) st_carry(inc + wslot * 32 + lane, fma2(E, x, tot));
-  }
-#pragma unroll
-  for (int q = 0; q < kL / 16; ++q) {
-    const int tt = 16 * q + ColSum16::token(lane);
-    if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + N + nF) * a.T + t0 + tt] = dcs[q];
-  }
-  // no barrier here: the reverse walk writes only its own partial buffers,
-  // and the block barriers below order every cross-warp read
-
-  // ---- 5. reverse walk in blocks of kRB tokens
-  float2 dA = make_float2(0.0f, 0.0f);
-  int next = 0;  // thread 0: the next ticket, drawn before the last block
-  float sDD = 0.0f, sDB = 0.0f;
-  {
-    float2* const part2 = reinterpret_cast<float2*>(sm.part);  // [2][W][kRB][kTile]
-    T* gdu = static_cast<T*>(a.du);
-    T* gddr = static_cast<T*>(a.ddr);
-    T* gdz = static_cast<T*>(a.dz);
-    float2 r = x;  // carry entering the current token from the right
-    constexpr bool kEv = kStates;
-#pragma unroll
-    for (int blk = kL / kRB - 1; blk >= 0; --blk) {
-      const int buf = blk & 1;
-      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
-#pragma unroll
-      for (int kb = (blk + 1) * kRB / 4 - 1; kb >= blk * kRB / 4; --kb) {
-        const float4 dl4 = *reinterpret_cast<const float4*>(sm.dl + lane * kP + 4 * kb);
-        const float4 du4 = *reinterpret_cast<const float4*>(sm.dlu + lane * kP + 4 * kb);
-        const float4 g4 = *reinterpret_cast<const float4*>(sm.g + lane * kP + 4 * kb);
-        const float4 b01 = *reinterpret_cast<const float4*>(bp + 8 * kb);
-        const float4 b23 = *reinterpret_cast<const float4*>(bp + 8 * kb + 4);
-        const float4 c01 = *reinterpret_cast<const float4*>(cp + 8 * kb);
-        const float4 c23 = *reinterpret_cast<const float4*>(cp + 8 * kb + 4);
-        const float4 of4 = *reinterpret_cast<const float4*>(sm.off + 4 * kb);
-        const float ofa[4] = {of4.x, of4.y, of4.z, of4.w};
-        const float dla[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
-        const float dua[4] = {du4.x, du4.y, du4.z, du4.w};
-        const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
-        const float2 Ba[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w), make_float2(b23.x, b23.y),
-                              make_float2(b23.z, b23.w)};
-        const float2 Ca[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
-                              make_float2(c23.z, c23.w)};
-#pragma unroll
-        for (int e = 3; e >= 0; --e) {
-          const int t = 4 * kb + e;
-          const float2 at = make_float2(ex2(fmaf(dla[e], A2.x, ofa[e])), ex2(fmaf(dla[e], A2.y, ofa[e])));
-          const float2 Bt = Ba[e];
-          float2 dh = fma2(Ca[e], splat2(ga[e]), r);  // total gradient w.r.t. h_t
-          if constexpr (kEv) {
-            if ((evF >> t) & 1u) dh = __fadd2_rn(dh, state_pair(a.dh_final, t));
-          }
-          // a_t h_{t-1} = h_t - delta u B: no need for the previous state
-          const float2 dhq = mul2(dh, fma2(splat2(-dua[e]), Bt, hist[t]));
-          dA = fma2(splat2(dla[e]), dhq, dA);
-          part2[((buf * W + w) * kRB + (t - blk * kRB)) * kTile + lane] =
-              make_float2(fmaf(dh.x, Bt.x, dh.y * Bt.y), fmaf(A2.x, dhq.x, A2.y * dhq.y));
-          float sum;  // dB contributions dh_t delta u, summed over the tile's channels
-          if (colsum.feed(t & 15, false, mul2(dh, splat2(dua[e])), lane, &sum)) {
-            const int tt = t + ColSum16::token(lane);
-            if (tt < rows) a.part_dBC[((int64_t)tile * 2 * N + nF) * a.T + t0 + tt] = sum;
-          }
-          if constexpr (kEv) {
-            if (((evG >> t) & 1u) && valid) {
-              // the gradient reaching the starting state: dh_t times a's own value
-              const float2 g0 = mul2(dh, make_float2(ex2(dla[e] * A2.x), ex2(dla[e] * A2.y)));
-              float2* row = reinterpret_cast<float2*>(a.dh_init + ((int64_t)a.seq[t0 + t] * a.D + d) * N + n0);
-              *row = (lane & 16) ? make_float2(g0.y, g0.x) : g0;
-            }
-          }
-          r = mul2(dh, at);  // carry to h_{t-1}
-        }
-      }
-      __syncthreads();  // the block's partials are complete
-      // du, d delta_raw and dz of the block: thread i takes token
-      // blk*kRB + i / kTile, channel i % kTile (= lane), and adds the warps'
-      // partials in order
-      for (int i = tid; i < kRB * kTile; i += kThr) {
-        const int e = i / kTile;
-        const int t = blk * kRB + e;
-        float2 sp = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int v = 0; v < W; ++v) sp = __fadd2_rn(sp, part2[((buf * W + v) * kRB + e) * kTile + lane]);
-        float y = 0.0f;  // C.h, for dz, when the call has no y to read
-        if (a.has_z && !a.has_y) {
-#pragma unroll
-          for (int v = 0; v < W; ++v) y += sm.ypart[(v * kL + t) * kTile + lane];
-        }
-        const float dlt = sm.dl[lane * kP + t], gt = sm.g[lane * kP + t];
-        const float uv = to_f(sm.u[t * bx + lane]);
-        const float gdu_t = fmaf(dlt, sp.x, Dsk * gt);
-        const float gdr_t = fmaf(uv, sp.x, sp.y * kLn2) * sm.sg[lane * kP + t];
-        if (t < rows && valid) {
-          const int64_t at_td = (t0 + t) * a.D + d;
-          gdu[at_td] = from_f<T>(gdu_t);
-          gddr[at_td] = from_f<T>(gdr_t);
-          if (a.has_z) {
-            const float go = to_f(sm.dout[t * bx + lane]);
-            const float zz = to_f(sm.z[t * bx + lane]);
-            const float sz = sigmoidf_fast(zz);
-            const float yf = a.has_y ? to_f(sm.y[t * bx + lane]) : fmaf(Dsk, uv, y);
-            gdz[at_td] = from_f<T>(go * sz * fmaf(zz, 1.0f - sz, 1.0f) * yf);
-          }
-          sDD = fmaf(gt, uv, sDD);
-          sDB += gdr_t;
-        }
-      }
+    if (!rs_any && publish) {
+      const float2 lo = fma2(lo2(E), lo2(x), lo2(tot)), hi = fma2(hi2(E), hi2(x), hi2(tot));
+      st_carry4(inc + wslot, make_float4(lo.x, lo.y, hi.x, hi.y));
     }
   }
 
-  // ---- 6. dA partials of the chunk ([chunk][n][d]); fixed-order CTA sums of
+  // ---- 4. reverse walk in blocks of kRB tokens, p_t read back from tensor memory
+  float2 dAF = make_float2(0.0f, 0.0f), dAS = make_float2(0.0f, 0.0f);
+  float2 accB = make_float2(0.0f, 0.0f);  // d_dt_bias partial of this thread's finalize pair
+  int next = 0;  // thread 0: the next ticket, drawn in the last block
+  {
+    T* gdu = static_cast<T*>(a.du);
+    T* gddr = static_cast<T*>(a.ddr);
+    T* gdz = static_cast<T*>(a.dz);
+    float2 rF = lo2(x), rS = hi2(x);  // carry entering the current token from the right
+    ColSum8 colsum;
+    // One block of 4 tokens (descending) with its history in hb, then the
+    // block's du and d delta_raw once every state pair has added its partials.
+    auto block = [&](auto parity, int bp, uint32_t (&hb)[16]) {
+      constexpr int buf = decltype(parity)::value;  // blocks 2 bp + 1 and 2 bp form one 8-token group
+      const int blk = 2 * bp + buf;
+      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
+#pragma unroll
+      for (int e = kRB - 2; e >= 0; e -= 2) {
+        const int t = blk * kRB + e;
+        const float4 dl4 = *reinterpret_cast<const float4*>(dlr + t);
+        const float4 du4 = *reinterpret_cast<const float4*>(dur + t);
+        const float4 g4 = *reinterpret_cast<const float4*>(gr + t);
+        const float4 of4 = sm.off[t >> 1];
+#pragma unroll
+        for (int j = 1; j >= 0; --j) {
+          const int tt = t + j, e2 = e + j;
+          const float2 dlp = j ? hi2(dl4) : lo2(dl4);
+          const float2 dup = j ? hi2(du4) : lo2(du4);
+          const float2 gp = j ? hi2(g4) : lo2(g4);
+          const float2 ofp = j ? hi2(of4) : lo2(of4);
+          const float4 bd = bdr[tt * 2 * NSP], cd = cdr[tt * 2 * NSP];
+          const float2 pF = make_float2(bitsf(hb[4 * e2]), bitsf(hb[4 * e2 + 1]));
+          const float2 pS = make_float2(bitsf(hb[4 * e2 + 2]), bitsf(hb[4 * e2 + 3]));
+          const float2 aF = ex2x2(fma2(dlp, AF, ofp)), aS = ex2x2(fma2(dlp, AS, ofp));
+          float2 dhF = fma2(lo2(cd), gp, rF);  // total gradient w.r.t. h_t
+          float2 dhS = fma2(hi2(cd), gp, rS);
+          if constexpr (kStates) {
+            if ((evF >> tt) & 1u) {
+              dhF = __fadd2_rn(dhF, state_pair(a.dh_final, tt, nF));
+              dhS = __fadd2_rn(dhS, state_pair(a.dh_final, tt, nS));
+            }
+          }
+          const float2 qF = mul2(dhF, pF), qS = mul2(dhS, pS);
+          dAF = fma2(dlp, qF, dAF);
+          dAS = fma2(dlp, qS, dAS);
+          const float2 s1 = fma2(dhS, hi2(bd), mul2(dhF, lo2(bd)));
+          const float2 s2 = fma2(AS, qS, mul2(AF, qF));
+          sm.nred[((buf * kRB + e2) * NSP + sp) * kCP + cp] = make_float4(s1.x, s1.y, s2.x, s2.y);
+          if constexpr (kRecY) {  // C.h_t partials for y, h_t = p_t + delta u B
+            const float2 yv = fma2(hi2(cd), fma2(dup, hi2(bd), pS), mul2(lo2(cd), fma2(dup, lo2(bd), pF)));
+            sm.nY[((buf * kRB + e2) * NSP + sp) * kCP + cp] = yv;
+          }
+          // dB contributions dh_t delta u over the pair's channels, then over the tile's
+          float sum;
+          if (colsum.feed(4 * buf + e2, false, hsum(mul2(dup, dhF)), hsum(mul2(dup, dhS)), lane, &sum)) {
+            const int ts = tt + ColSum8::token(lane);
+            if (ts < rows) pdB[ts] = sum;
+          }
+          if constexpr (kStates) {
+            if (((evG >> tt) & 1u) && valid) {
+              // the gradient reaching the starting state: dh_t times a's own value
+              const float2 gF = mul2(dhF, ex2x2(mul2(dlp, AF))), gS = mul2(dhS, ex2x2(mul2(dlp, AS)));
+              float* row = a.dh_init + ((int64_t)a.seq[t0 + tt] * a.D + d) * N;
+              row[nF] = gF.x;
+              row[N + nF] = gF.y;
+              row[nS] = gS.x;
+              row[N + nS] = gS.y;
+            }
+          }
+          rF = mul2(dhF, aF);  // carry to h_{t-1}
+          rS = mul2(dhS, aS);
+        }
+      }
+    };
+    // du and d delta_raw (and dz when y is recomputed) of block blk: 64
+    // (token, channel pair) items, taken by warps 0-1 for even blocks and
+    // 2-3 for odd ones when the CTA has 4 warps; the state pairs' partials are
+    // added in order
+    auto finalize = [&](int blk) {
+      const int buf = blk & 1;
+      constexpr int kFin = kThr >= 128 ? 64 : kThr;
+      const bool mine = kThr >= 128 ? ((tid >> 6) == (blk & 1)) : true;
+      if (!mine) return;
+      for (int i = tid & (kFin - 1); i < kRB * kCP; i += kFin) {
+        const int e = i >> 4, q = i & 15;
+        const int t = blk * kRB + e;
+        const float4* np = sm.nred + (buf * kRB + e) * NSP * kCP + q;
+        float4 s = np[0];
+#pragma unroll
+        for (int v = 1; v < NSP; ++v) s = add4(s, np[v * kCP]);
+        const float2 dlv = sm.dl[q * kPT + t], gv = sm.g[q * kPT + t], sgv = sm.sg[q * kPT + t];
+        const int at = t * bx + 2 * q;
+        const float2 uv = ld_io2(sm.u + at);
+        const float2 dsk = a.Dskip ? make_float2(sm.dsk[(2 * q) & 31], sm.dsk[(2 * q + 1) & 31]) : make_float2(0.0f, 0.0f);
+        const float2 du = fma2(dlv, lo2(s), mul2(dsk, gv));
+        const float2 ddr = mul2(fma2(uv, lo2(s), mul2(hi2(s), splat2(kLn2))), sgv);
+        const bool ok = t < rows && 2 * q < bx && d0 + 2 * q < a.D;
+        if (ok) {
+          const int64_t o2 = (t0 + t) * a.D + d0 + 2 * q;
+          st_io2(gdu + o2, du);
+          st_io2(gddr + o2, ddr);
+          if constexpr (kRecY) {
+            const float2* yp = sm.nY + (buf * kRB + e) * NSP * kCP + q;
+            float2 ys = yp[0];
+#pragma unroll
+            for (int v = 1; v < NSP; ++v) ys = __fadd2_rn(ys, yp[v * kCP]);
+            st_io2(gdz + o2, mul2(sm.dzf[q * kPT + t], fma2(dsk, uv, ys)));
+          }
+        }
+        accB = __fadd2_rn(accB, ddr);  // zero past the last token and on missing channels
+      }
+    };
+    // (the tensor-memory instructions are warp-collective: each follows a
+    // __syncwarp so that the warp is converged)
+    uint32_t hb0[16], hb1[16];
+    __syncwarp();
+    tmem_ld16(thist + 4 * kRB * (kL / kRB - 1), hb1);
+    tmem_wait_ld16(hb1);
+#pragma unroll 1
+    for (int bp = kL / (2 * kRB) - 1; bp >= 0; --bp) {
+      // block 2 bp + 1 from hb1, while block 2 bp's history loads into hb0
+      __syncwarp();
+      tmem_ld16(thist + 4 * kRB * (2 * bp), hb0);
+      block(std::integral_constant<int, 1>{}, bp, hb1);
+      __syncwarp();
+      tmem_wait_ld16(hb0);
+      __syncthreads();  // the block's partials are complete
+      finalize(2 * bp + 1);
+      __syncwarp();
+      if (bp > 0) tmem_ld16(thist + 4 * kRB * (2 * bp - 1), hb1);
+      block(std::integral_constant<int, 0>{}, bp, hb0);
+      __syncwarp();
+      if (bp > 0) tmem_wait_ld16(hb1);
+      __syncthreads();
+      finalize(2 * bp);
+    }
+  }
+
+  // ---- 5. dA partials of the chunk ([chunk][n][d]); fixed-order CTA sums of
   //         the dDskip and d_dt_bias partials
   if (valid) {
     // for A_log the chain rule gives dA_log = dA * A (A = A2 ln 2), applied to
     // every chunk's partial before the fixed-order sum
-    const float2 s = a.a_log ? make_float2(A2.x * kLn2, A2.y * kLn2) : make_float2(1.0f, 1.0f);
-    a.part_dA[((int64_t)chunk * N + nF) * a.D + d] = dA.x * s.x;
-    a.part_dA[((int64_t)chunk * N + nS) * a.D + d] = dA.y * s.y;
+    const float2 sF = a.a_log ? mul2(AF, splat2(kLn2)) : make_float2(1.0f, 1.0f);
+    const float2 sS = a.a_log ? mul2(AS, splat2(kLn2)) : make_float2(1.0f, 1.0f);
+    *reinterpret_cast<float2*>(a.part_dA + ((int64_t)chunk * N + nF) * a.D + d) = mul2(dAF, sF);
+    *reinterpret_cast<float2*>(a.part_dA + ((int64_t)chunk * N + nS) * a.D + d) = mul2(dAS, sS);
   }
-  sm.redD[w * kTile + lane] = sDD;
-  sm.redB[w * kTile + lane] = sDB;
+  sm.redD[tid] = accD;
+  sm.redB[tid] = accB;
   __syncthreads();
-  // no input buffer is read any more: draw the next item and request its
-  // inputs, which land while this item writes its last partials
+  // no input buffer is read any more: request the next item's inputs, which
+  // land while this item writes its last partials
   if (tid == 0) {
     sm.ticket = next;
     if (next < n_items) issue(next);
   }
-  if (w == 0 && valid) {
-    float accD = 0.0f, accB = 0.0f;
-#pragma unroll
-    for (int v = 0; v < W; ++v) {
-      accD += sm.redD[v * kTile + lane];
-      accB += sm.redB[v * kTile + lane];
+  if (tid < kCP && d0 + 2 * tid < a.D && 2 * tid < bx) {
+    float2 sD = make_float2(0.0f, 0.0f), sB = make_float2(0.0f, 0.0f);
+    for (int v = tid; v < kThr; v += kCP) {
+      sD = __fadd2_rn(sD, sm.redD[v]);
+      sB = __fadd2_rn(sB, sm.redB[v]);
     }
-    a.part_dD[(int64_t)chunk * a.D + d] = accD;
-    a.part_dbias[(int64_t)chunk * a.D + d] = accB;
+    *reinterpret_cast<float2*>(a.part_dD + (int64_t)chunk * a.D + d0 + 2 * tid) = sD;
+    *reinterpret_cast<float2*>(a.part_dbias + (int64_t)chunk * a.D + d0 + 2 * tid) = sB;
   }
   __syncthreads();  // redD / redB and the ticket are consumed before the next pass
   }  // persistent loop
+
+  // every warp's tensor-memory accesses are complete (waited) before the free
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (w == 0) {
+    tmem_fence_after_sync();
+    tmem_dealloc128(sm.taddr);
+  }
 }
 
 // dB[t][n] = sum over tiles of part[tile][n][t]; dC[t][n] likewise from
@@ -616,31 +714,41 @@ __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restri
   if (v < N) dB[t * N + v] = acc; else dC[t * N + (v - N)] = acc;
 }
 
-template <typename T, int N, bool kStates, bool kKnob = false>
+template <typename T, int N, bool kStates, bool kRecY, bool kKnob = false>
 cudaError_t launch_k(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
                      const CUtensorMap& tm_y, cudaStream_t st) {
-  const size_t smem = sizeof(BwdSmem<T, N>);
-  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, kStates, kKnob>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = scan_bwd_kernel<T, N, kStates, kRecY, kKnob>;
+  const size_t smem = sizeof(BwdSmem<T, N, kRecY>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
   int grid = 0;
-  e = persistent_grid(scan_bwd_kernel<T, N, kStates, kKnob>, 16 * N, smem, items, &grid);
+  // every CTA holds 128 of the SM's 512 tensor-memory columns: at most 4 per SM
+  e = persistent_grid(kern, 8 * N, smem, items, &grid, 4);
   if (e != cudaSuccess) return e;
-  scan_bwd_kernel<T, N, kStates, kKnob><<<grid, 16 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, a);
+  kern<<<grid, 8 * N, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, a);
   return cudaGetLastError();
+}
+
+template <typename T, int N, bool kRecY>
+cudaError_t launch_y(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                     const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                     const CUtensorMap& tm_y, cudaStream_t st) {
+  if constexpr (sizeof(T) == 4 && N == 16 && kRecY) {  // the delay knob's instantiation
+    if (a.delay_ticket >= 0 && !a.seq)
+      return launch_k<T, N, false, kRecY, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  }
+  return a.seq ? launch_k<T, N, true, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+               : launch_k<T, N, false, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
 }
 
 template <typename T, int N>
 cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
                      const CUtensorMap& tm_y, cudaStream_t st) {
-  if constexpr (sizeof(T) == 4 && N == 16) {  // the delay knob's instantiation
-    if (a.delay_ticket >= 0 && !a.seq) return launch_k<T, N, false, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
-  }
-  return a.seq ? launch_k<T, N, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
-               : launch_k<T, N, false>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  return (a.has_z && !a.has_y) ? launch_y<T, N, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+                               : launch_y<T, N, false>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
 }
 
 template <typename T>
