@@ -52,29 +52,35 @@ struct Layout {
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
 
+// Channels per work item of a scan call: the backward with N = 16 takes 64
+// (two 32-channel groups per CTA), every other call 32.
+int scan_tile(int N, bool bwd) { return (bwd && N == 16) ? 2 * kTile : kTile; }
+
 Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   Layout l;
-  const int64_t n_tiles = cdiv(D, kTile);
+  const int tw = scan_tile(N, bwd);
+  const int64_t n_tiles = cdiv(D, tw);
   const int64_t n_chunks = cdiv(T, chunk);
   const int64_t slots = n_tiles * n_chunks;
   size_t off = kAlign;
   l.flags = off;
-  off += up(sizeof(int) * (size_t)slots * kTile);
+  off += up(sizeof(int) * (size_t)slots * tw);
   l.clear_bytes = off;
   l.pos = off;
   off += up(sizeof(int32_t) * (size_t)T);
   l.seq = off;
   off += up(sizeof(int32_t) * (size_t)T);
   l.agg = off;
-  off += up(sizeof(float) * (size_t)slots * N * kTile);
+  off += up(sizeof(float) * (size_t)slots * N * tw);
   l.agg_sd = off;
-  off += up(sizeof(float) * (size_t)slots * (bwd ? N : 1) * kTile);
+  off += up(sizeof(float) * (size_t)slots * (bwd ? N : 1) * tw);
   l.incl = off;
-  l.incl_bytes = sizeof(float) * (size_t)slots * N * kTile;
+  l.incl_bytes = sizeof(float) * (size_t)slots * N * tw;
   off += up(l.incl_bytes);
   if (bwd) {
+    // dB / dC partials: one row group per 32 channels
     l.part_bc = off;
-    off += up(sizeof(float) * (size_t)n_tiles * T * 2 * N);
+    off += up(sizeof(float) * (size_t)n_tiles * (tw / kTile) * T * 2 * N);
     l.part_a = off;
     off += up(sizeof(float) * (size_t)n_chunks * D * N);
     l.part_d = off;
@@ -555,7 +561,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.part_dD = at<float>(workspace, l.part_d);
   a.part_dbias = at<float>(workspace, l.part_b);
   a.T = T; a.D = D; a.N = N;
-  a.n_tiles = (int)cdiv(D, kTile);
+  const int tw = scan_tile(N, true);
+  a.n_tiles = (int)cdiv(D, tw);
   a.n_chunks = (int)cdiv(T, kBwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
   a.gate_floor = gate_floor;
@@ -563,7 +570,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.has_z = z ? 1 : 0;
   a.has_y = (z && y) ? 1 : 0;
   a.has_skip = Dskip ? 1 : 0;
-  a.box_x = D < kTile ? D : kTile;
+  a.box_x = D < tw ? D : tw;
   a.box_y = T < kBwdChunk ? (int)T : kBwdChunk;
   a.drop_ticket = g_drop_ticket.load();
   a.wait_ns = g_wait_ns.load();

@@ -690,6 +690,635 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
 }
 
+// ============================================================================
+// N = 16: a thread owns two channel pairs and one state pair
+// ============================================================================
+// Work item = 32 tokens x kTW = 64 channels; CTA = 4 warps in two channel
+// groups (warps 2g, 2g+1 take the channels 32g .. 32g+31).  A thread owns the
+// channel quad q = 8g + lane % 8 (channels 4q .. 4q+3: two pairs for the
+// paired FP32 instructions) and the state pair p = 4 (w % 2) + lane / 8: eight
+// (channel, state) chains.  Against the pair-by-pair layout above, every
+// per-token value a thread loads serves twice the chains, the channel sums for
+// dB / dC start over 4 channels in registers, and the history takes 8 words
+// per token (256 tensor-memory columns per warp, 2 CTAs per SM).  The partial
+// sums over state pairs for du / d delta_raw come from the two warps of a
+// channel group only, so a block's epilogue waits on a 64-thread named
+// barrier, not on the whole CTA.
+constexpr int kTW = 2 * kTile;  // 64 channels per work item
+constexpr int kCQ = kTW / 4;    // 16 channel quads
+constexpr int kQT = kL + 1;     // token pitch (float4) of the [channel quad][token] arrays
+constexpr int kSP = 8;          // state pairs
+
+template <typename T, bool kRecY>
+struct Bwd16Smem {
+  alignas(128) T u[kL * kTW];
+  alignas(128) T dr[kL * kTW];
+  alignas(128) T z[kL * kTW];
+  alignas(128) T dout[kL * kTW];
+  alignas(128) T y[kL * kTW];
+  alignas(128) T B[kL * 16];
+  alignas(128) T C[kL * 16];
+  alignas(16) float Araw[kTW * 16];
+  alignas(128) float H[16 * kTW];  // saved states at the chunk start, [n][channel]
+  alignas(16) float bias[kTW];
+  alignas(16) float dsk[kTW];
+  alignas(16) int pos[kL];
+  // ---- per-(token, channel quad) values, [quad][token] float4 with token
+  //      pitch kQT: the 8 quads a warp reads for a token are in distinct banks
+  alignas(16) float4 dl[kCQ * kQT];   // delta
+  alignas(16) float4 dlu[kCQ * kQT];  // delta * u
+  alignas(16) float4 g[kCQ * kQT];    // dout * (SiLU(z) + gate floor)
+  alignas(16) float4 dzf[kRecY ? kCQ * kQT : 1];  // d out / d y, when y is recomputed
+  // ---- B and C doubled, [token][state pair][order] float4 (as above)
+  alignas(16) float4 BD[kL * kSP * 2];
+  alignas(16) float4 CD[kL * kSP * 2];
+  alignas(16) float4 off[kL / 2];
+  // ---- partial sums over each thread's state pair from the reverse walk,
+  //      [buffer][token of the block][state pair][channel pair parity][quad]
+  //      float4 = (sum dh B for the pair's two channels, sum A dh p for them)
+  alignas(16) float4 nred[2 * kRB * kSP * 2 * kCQ];
+  alignas(16) float2 nY[kRecY ? 2 * kRB * kSP * 2 * kCQ : 2];  // C.h partials, when y is recomputed
+  alignas(16) float4 redD[128];
+  alignas(16) float2 redB[128];
+  uint32_t taddr;
+  int ticket;
+  alignas(8) uint64_t bar;
+};
+
+// Column sums over the 8 lanes of a warp that share a state pair (lane % 8 =
+// channel quad) for groups of 4 tokens x 2 states, by shuffle butterflies: level
+// 1 exchanges states over lane bit 2 (a lane keeps the state 2p + bit2), levels
+// 2 and 3 pair tokens over lane bits 1 and 0.  After the 4th token, lane l
+// holds the sum over the 8 lanes for token bit1(l) + 2 bit0(l) of the group.
+struct ColSum4 {
+  float p2[2], p3[2];
+
+  static __device__ __forceinline__ int token(int lane) { return ((lane >> 1) & 1) + 2 * (lane & 1); }
+
+  __device__ __forceinline__ bool feed(int c, bool ascending, float vF, float vS, int lane, float* sum) {
+    p2[c & 1] = vF + __shfl_xor_sync(0xffffffffu, vS, 4);
+    if ((c & 1) != (ascending ? 1 : 0)) return false;
+    p3[(c >> 1) & 1] = ColSum8::combine(p2[0], p2[1], lane, 2);
+    if ((c & 3) != (ascending ? 3 : 0)) return false;
+    *sum = ColSum8::combine(p3[0], p3[1], lane, 1);
+    return true;
+  }
+};
+
+__device__ __forceinline__ void st_io4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st_io4(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v.x, v.y));
+  const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(v.z, v.w));
+  uint2 q;
+  q.x = *reinterpret_cast<const uint32_t*>(&a);
+  q.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = q;
+}
+__device__ __forceinline__ float4 mk4(float2 lo, float2 hi) { return make_float4(lo.x, lo.y, hi.x, hi.y); }
+
+template <typename T, bool kStates, bool kRecY, bool kKnob>
+__global__ void __launch_bounds__(128, 2)
+scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dout,
+                  const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_y,
+                  const ScanArgs a) {
+  constexpr int N = 16;
+  constexpr int kThr = 128;
+  using SM = Bwd16Smem<T, kRecY>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int n_items = a.n_chunks * a.n_tiles;
+  const int grp = w >> 1;                          // channel group
+  const int cq = 8 * grp + (lane & 7);             // channel quad of the tile
+  const int sp = 4 * (w & 1) + (lane >> 3);        // state pair
+  const int o = (lane >> 2) & 1;                   // this lane's state order
+  const int nF = 2 * sp + o, nS = 2 * sp + 1 - o;  // its "first" and "second" state
+  const int c0 = 4 * cq;                           // first channel of the quad (in the tile)
+
+  auto issue = [&](int tkn) {
+    const int rv = tkn / a.n_tiles;
+    const int tl = tkn - rv * a.n_tiles;
+    const int ch = a.n_chunks - 1 - rv;
+    const int64_t tt0 = (int64_t)ch * kL;
+    const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
+    const int dd0 = tl * kTW;
+    const uint32_t nval = (uint32_t)(a.D - dd0 < kTW ? a.D - dd0 : kTW);
+    const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
+    const uint32_t rows4 = (uint32_t)nrows & ~3u;
+    const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
+    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bc + nval * N * 4u +
+                                       (uint32_t)a.box_x * N * 4u + rows4 * 4u +
+                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
+    tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+    tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
+    tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
+    if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+    if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
+    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
+    tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
+    if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
+    if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
+    if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
+  };
+
+  // tensor memory for the forward walk's history: 256 columns, warp w on the
+  // lanes 32 w .. 32 w + 31
+  if (w == 0) tmem_alloc256(&sm.taddr);
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+    const int first = (int)atomicAdd(a.ticket, 1u);
+    sm.ticket = first;
+    if (first < n_items) issue(first);
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t thist = sm.taddr + ((uint32_t)(32 * w) << 16);
+
+  for (uint32_t it = 0;; ++it) {
+  const int tk = sm.ticket;
+  if (tk >= n_items) break;
+  if constexpr (kKnob) {
+    if ((long long)tk == a.delay_ticket) sleep_ns(a.delay_ns);
+  }
+  const int rev = tk / a.n_tiles;
+  const int tile = tk - rev * a.n_tiles;
+  const int chunk = a.n_chunks - 1 - rev;
+  const int64_t t0 = (int64_t)chunk * kL;
+  const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
+  const int rows4 = rows & ~3;
+  const int d0 = tile * kTW;
+  const int bx = a.box_x;
+  const int d = d0 + c0;                   // first channel of this thread's quad
+  const bool valid = c0 < bx && d < a.D;   // D is a multiple of 4: the quad is whole
+
+  if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
+    // see scan_bwd_kernel: report, give the copies a second limit, stop
+    if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
+    mbar_wait(&sm.bar, it & 1u, a.wait_ns);
+    break;
+  }
+
+  // ---- 1. per-(token, channel quad) values (zero past the last token and on
+  //         channels past D), and dz from the pre-gate output y
+  float4 accD = make_float4(0.0f, 0.0f, 0.0f, 0.0f);  // dDskip partial of quad tid % 16
+  {
+    T* gdz = static_cast<T*>(a.dz);
+    const int q = tid & 15;
+    const float4 bias4 = a.dt_bias ? *reinterpret_cast<const float4*>(sm.bias + 4 * q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 2
+    for (int i = tid; i < kL * kCQ; i += kThr) {
+      const int t = i >> 4;
+      const int at = t * bx + 4 * q;
+      const bool ok = t < rows && 4 * q < bx && d0 + 4 * q < a.D;
+      const float4 r4 = ld_io4(sm.dr + at);
+      const float4 u4 = ld_io4(sm.u + at);
+      const float4 go = ld_io4(sm.dout + at);
+      const float2 rlo = __fadd2_rn(lo2(r4), lo2(bias4)), rhi = __fadd2_rn(hi2(r4), hi2(bias4));
+      float4 dl4;
+      if (a.delta_softplus) {
+        float sgd;
+        dl4 = make_float4(softplus_sig(rlo.x, &sgd), softplus_sig(rlo.y, &sgd), softplus_sig(rhi.x, &sgd),
+                          softplus_sig(rhi.y, &sgd));
+      } else {
+        dl4 = mk4(rlo, rhi);
+      }
+      float4 gv = go;
+      if (a.has_z) {
+        const float4 z4 = ld_io4(sm.z + at);
+        const float4 s4 = make_float4(sigmoidf_fast(z4.x), sigmoidf_fast(z4.y), sigmoidf_fast(z4.z),
+                                      sigmoidf_fast(z4.w));
+        const float2 glo = mul2(lo2(go), fma2(lo2(z4), lo2(s4), splat2(a.gate_floor)));
+        const float2 ghi = mul2(hi2(go), fma2(hi2(z4), hi2(s4), splat2(a.gate_floor)));
+        gv = mk4(glo, ghi);
+        // d out / d y = dout SiLU'(z), SiLU'(z) = s (1 + z (1 - s))
+        const float2 flo = mul2(mul2(lo2(go), lo2(s4)),
+                                fma2(lo2(z4), make_float2(1.0f - s4.x, 1.0f - s4.y), splat2(1.0f)));
+        const float2 fhi = mul2(mul2(hi2(go), hi2(s4)),
+                                fma2(hi2(z4), make_float2(1.0f - s4.z, 1.0f - s4.w), splat2(1.0f)));
+        if (a.has_y) {
+          if (ok) {
+            const float4 y4 = ld_io4(sm.y + at);
+            st_io4(gdz + (t0 + t) * a.D + d0 + 4 * q, mk4(mul2(flo, lo2(y4)), mul2(fhi, hi2(y4))));
+          }
+        } else if constexpr (kRecY) {
+          sm.dzf[q * kQT + t] = ok ? mk4(flo, fhi) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+      }
+      const float4 z0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      sm.dl[q * kQT + t] = ok ? dl4 : z0;
+      sm.dlu[q * kQT + t] = ok ? mk4(mul2(lo2(dl4), lo2(u4)), mul2(hi2(dl4), hi2(u4))) : z0;
+      sm.g[q * kQT + t] = ok ? gv : z0;
+      if (ok) accD = mk4(fma2(lo2(gv), lo2(u4), lo2(accD)), fma2(hi2(gv), hi2(u4), hi2(accD)));
+    }
+  }
+  for (int i = tid; i < kL * kSP; i += kThr) {
+    const int t = i / kSP, pn = i - t * kSP;
+    const bool in = t < rows;
+    const float2 b = in ? ld_io2(sm.B + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
+    const float2 c = in ? ld_io2(sm.C + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
+    sm.BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
+    sm.BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
+    sm.CD[2 * i] = make_float4(c.x, c.x, c.y, c.y);
+    sm.CD[2 * i + 1] = make_float4(c.y, c.y, c.x, c.x);
+  }
+  const unsigned rst =
+      __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
+  if (w == 0 && lane < kL / 2) {
+    const float o0 = ((rst >> (2 * lane)) & 1u) ? -INFINITY : 0.0f;
+    const float o1 = ((rst >> (2 * lane + 1)) & 1u) ? -INFINITY : 0.0f;
+    sm.off[lane] = make_float4(o0, o0, o1, o1);
+  }
+  unsigned evH = 0u, evG = 0u, evF = 0u;
+  if (kStates && a.seq) {
+    const unsigned live = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
+    const unsigned starts = rst & live;
+    evH = a.h_init ? starts : 0u;
+    evG = a.dh_init ? starts : 0u;
+    if (a.dh_final) {
+      unsigned ends = starts >> 1;
+      if (t0 + rows >= a.T || (rows == 32 && __ldg(a.pos + t0 + 32) == 0)) ends |= 1u << (rows - 1);
+      evF = ends & live;
+    }
+  }
+  // sequence-state entries (channels d + 2j, d + 2j + 1) of state n for token t's sequence
+  auto state_pair = [&](const float* st, int t, int n, int j) {
+    if (!valid) return make_float2(0.0f, 0.0f);
+    const float* row = st + ((int64_t)a.seq[t0 + t] * a.D + d + 2 * j) * N + n;
+    return make_float2(__ldg(row), __ldg(row + N));
+  };
+  __syncthreads();
+
+  // A * log2 e pairs [state F / S][channel pair] and the saved states
+  float2 A[2][2], h[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int n = q ? nS : nF;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      A[q][j] = make_float2(0.0f, 0.0f);
+      h[q][j] = make_float2(0.0f, 0.0f);
+      if (valid) {
+        float2 v = make_float2(sm.Araw[(c0 + 2 * j) * N + n], sm.Araw[(c0 + 2 * j + 1) * N + n]);
+        if (a.a_log) v = make_float2(-ex2(v.x * kLog2e), -ex2(v.y * kLog2e));
+        A[q][j] = mul2(v, splat2(kLog2e));
+        h[q][j] = *reinterpret_cast<const float2*>(sm.H + n * bx + c0 + 2 * j);
+      }
+    }
+  }
+  const float4* const dlr = sm.dl + cq * kQT;
+  const float4* const dur = sm.dlu + cq * kQT;
+  const float4* const gr = sm.g + cq * kQT;
+  const float4* const bdr = sm.BD + sp * 2 + o;  // entry of token t at [t * 2 kSP]
+  const float4* const cdr = sm.CD + sp * 2 + o;
+  const int part = 2 * tile + grp;               // 32-channel partial row group
+  float* const pdB = a.part_dBC + ((int64_t)part * 2 * N + nF) * a.T + t0;
+  float* const pdC = a.part_dBC + ((int64_t)part * 2 * N + N + nF) * a.T + t0;
+
+  // ---- 2. forward walk; p_t = a_t h_{t-1} (8 words per token) to tensor memory
+  float2 E[2][2], tot[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      E[q][j] = make_float2(1.0f, 1.0f);
+      tot[q][j] = make_float2(0.0f, 0.0f);
+    }
+  {
+    ColSum4 colsum;
+    // the group's dC sum is stored during the next group, once its shuffles
+    // have long completed (no stall on them)
+    float pend = 0.0f;
+    int pend_t = kL;
+#pragma unroll 1
+    for (int g4 = 0; g4 < kL / 4; ++g4) {
+      uint32_t hist[32];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tt = 4 * g4 + e;
+        if (e == 2 && pend_t < rows) pdC[pend_t] = pend;
+        const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
+        const float4 of4 = sm.off[tt >> 1];
+        const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
+        const float4 bd = bdr[tt * 2 * kSP], cd = cdr[tt * 2 * kSP];
+        const float2 dlp[2] = {lo2(dl4), hi2(dl4)}, dup[2] = {lo2(du4), hi2(du4)}, gp[2] = {lo2(gq), hi2(gq)};
+        float v[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float2 Bq = q ? hi2(bd) : lo2(bd), Cq = q ? hi2(cd) : lo2(cd);
+          const int n = q ? nS : nF;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 at = ex2x2(fma2(dlp[j], A[q][j], ofp));
+            float2 p = mul2(at, h[q][j]);
+            if constexpr (kStates) {
+              if ((evH >> tt) & 1u) p = mul2(ex2x2(mul2(dlp[j], A[q][j])), state_pair(a.h_init, tt, n, j));
+            }
+            h[q][j] = fma2(dup[j], Bq, p);
+            E[q][j] = mul2(E[q][j], at);
+            tot[q][j] = fma2(E[q][j], mul2(Cq, gp[j]), tot[q][j]);
+            if constexpr (kStates) {
+              if ((evF >> tt) & 1u) tot[q][j] = fma2(E[q][j], state_pair(a.dh_final, tt, n, j), tot[q][j]);
+            }
+            hist[8 * e + 4 * q + 2 * j] = fbits(p.x);
+            hist[8 * e + 4 * q + 2 * j + 1] = fbits(p.y);
+          }
+          v[q] = hsum(fma2(gp[1], h[q][1], mul2(gp[0], h[q][0])));
+        }
+        // dC contributions g_t h_t over the quad's channels, then over the group's
+        if (colsum.feed(e, true, v[0], v[1], lane, &pend)) pend_t = 4 * g4 + ColSum4::token(lane);
+      }
+      // the store reads its registers when it issues; the reverse walk waits
+      // for the stores to land before its first load
+      __syncwarp();
+      tmem_st32(thist + (uint32_t)(32 * g4), hist);
+    }
+    if (pend_t < rows) pdC[pend_t] = pend;
+    tmem_wait_st();
+  }
+
+  // ---- 3. decoupled look-back towards higher chunks (one chain per thread, 8 words)
+  float4 xlo = make_float4(0.0f, 0.0f, 0.0f, 0.0f), xhi = xlo;
+  {
+    const int64_t base = (int64_t)tile * a.n_chunks;
+    const int64_t wslot = ((base + chunk) * kThr + tid) * 2;
+    const bool publish = (long long)tk != a.drop_ticket;
+    float4* const agg = reinterpret_cast<float4*>(a.agg);
+    float4* const aggp = reinterpret_cast<float4*>(a.agg_sd);
+    float4* const inc = reinterpret_cast<float4*>(a.incl);
+    int* const my_flag = a.flags + (base + chunk) * 4 + w;
+    const float4 tlo = mk4(tot[0][0], tot[0][1]), thi = mk4(tot[1][0], tot[1][1]);
+    const float4 elo = mk4(E[0][0], E[0][1]), ehi = mk4(E[1][0], E[1][1]);
+    const bool rs_any = (rst & (rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u))) != 0u;
+    if (rs_any && publish) {
+      st_carry4(inc + wslot, tlo);
+      st_carry4(inc + wslot + 1, thi);
+    }
+    auto combine8 = [&](float4 p_lo, float4 p_hi, float4 q_lo, float4 q_hi) {
+      xlo = mk4(fma2(lo2(p_lo), lo2(xlo), lo2(q_lo)), fma2(hi2(p_lo), hi2(xlo), hi2(q_lo)));
+      xhi = mk4(fma2(lo2(p_hi), lo2(xhi), lo2(q_hi)), fma2(hi2(p_hi), hi2(xhi), hi2(q_hi)));
+    };
+    if (chunk < a.n_chunks - 1) {
+      int j = chunk + 1, found = -1, timed_out = 0;
+      const int64_t js = ((base + j) * kThr + tid) * 2;
+      float4 vlo = ld_carry4(inc + js), vhi = ld_carry4(inc + js + 1);
+      if (__all_sync(0xffffffffu, carry_set4(vlo) && carry_set4(vhi))) {
+        found = j;
+      } else {
+        if (!rs_any) {
+          agg[wslot] = tlo;
+          agg[wslot + 1] = thi;
+          aggp[wslot] = elo;
+          aggp[wslot + 1] = ehi;
+          publish_flag(my_flag, kFlagAggregate, publish, lane);
+        }
+        const uint64_t t_start = globaltimer_ns();
+        while (j < a.n_chunks) {
+          const int64_t ks = ((base + j) * kThr + tid) * 2;
+          unsigned backoff = 32;
+          int f = kFlagNone;
+          for (;;) {
+            vlo = ld_carry4(inc + ks);
+            vhi = ld_carry4(inc + ks + 1);
+            if (__all_sync(0xffffffffu, carry_set4(vlo) && carry_set4(vhi))) { f = kFlagInclusive; break; }
+            if (__all_sync(0xffffffffu, ld_acquire_gpu(a.flags + (base + j) * 4 + w) == kFlagAggregate)) {
+              f = kFlagAggregate;
+              break;
+            }
+            if (__shfl_sync(0xffffffffu, globaltimer_ns() - t_start > a.wait_ns, 0)) break;
+            __nanosleep(backoff);
+            if (backoff < 1024) backoff <<= 1;
+          }
+          if (f == kFlagInclusive) { found = j; break; }
+          if (f == kFlagNone) { timed_out = 1; break; }
+          ++j;
+        }
+      }
+      if (timed_out) atomicOr(a.status, kStatusLookbackTimeout);
+      int last = j - 1;
+      if (found >= 0) {
+        xlo = vlo;
+        xhi = vhi;
+        last = found - 1;
+      }
+      for (int i = last; i > chunk; --i) {
+        const int64_t ws = ((base + i) * kThr + tid) * 2;
+        combine8(__ldcg(aggp + ws), __ldcg(aggp + ws + 1), __ldcg(agg + ws), __ldcg(agg + ws + 1));
+      }
+    }
+    if (!rs_any && publish) {
+      st_carry4(inc + wslot, mk4(fma2(lo2(elo), lo2(xlo), lo2(tlo)), fma2(hi2(elo), hi2(xlo), hi2(tlo))));
+      st_carry4(inc + wslot + 1, mk4(fma2(lo2(ehi), lo2(xhi), lo2(thi)), fma2(hi2(ehi), hi2(xhi), hi2(thi))));
+    }
+  }
+
+  // ---- 4. reverse walk in blocks of kRB tokens
+  float2 dA[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) dA[q][j] = make_float2(0.0f, 0.0f);
+  float2 accB = make_float2(0.0f, 0.0f);  // d_dt_bias partial of this thread's epilogue pair
+  int next = 0;
+  {
+    T* gdu = static_cast<T*>(a.du);
+    T* gddr = static_cast<T*>(a.ddr);
+    T* gdz = static_cast<T*>(a.dz);
+    float2 r[2][2] = {{lo2(xlo), hi2(xlo)}, {lo2(xhi), hi2(xhi)}};
+    float pendB = 0.0f;
+    int pendB_t = kL;
+    auto block = [&](auto parity, int bp, uint32_t (&hb)[32]) {
+      constexpr int buf = decltype(parity)::value;
+      const int blk = 2 * bp + buf;
+      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
+      ColSum4 colsum;
+#pragma unroll
+      for (int e = kRB - 1; e >= 0; --e) {
+        const int tt = blk * kRB + e;
+        const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
+        const float4 of4 = sm.off[tt >> 1];
+        const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
+        const float4 bd = bdr[tt * 2 * kSP], cd = cdr[tt * 2 * kSP];
+        const float2 dlp[2] = {lo2(dl4), hi2(dl4)}, dup[2] = {lo2(du4), hi2(du4)}, gp[2] = {lo2(gq), hi2(gq)};
+        float2 dh[2][2], qq[2][2], at[2][2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float2 Cq = q ? hi2(cd) : lo2(cd);
+          const int n = q ? nS : nF;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 p = make_float2(bitsf(hb[8 * e + 4 * q + 2 * j]), bitsf(hb[8 * e + 4 * q + 2 * j + 1]));
+            at[q][j] = ex2x2(fma2(dlp[j], A[q][j], ofp));
+            dh[q][j] = fma2(Cq, gp[j], r[q][j]);
+            if constexpr (kStates) {
+              if ((evF >> tt) & 1u) dh[q][j] = __fadd2_rn(dh[q][j], state_pair(a.dh_final, tt, n, j));
+            }
+            qq[q][j] = mul2(dh[q][j], p);
+            dA[q][j] = fma2(dlp[j], qq[q][j], dA[q][j]);
+          }
+        }
+        const float2 BF = lo2(bd), BS = hi2(bd);
+        float4* np = sm.nred + ((buf * kRB + e) * kSP + sp) * 2 * kCQ + cq;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float2 s1 = fma2(dh[1][j], BS, mul2(dh[0][j], BF));
+          const float2 s2 = fma2(A[1][j], qq[1][j], mul2(A[0][j], qq[0][j]));
+          np[j * kCQ] = mk4(s1, s2);
+        }
+        if constexpr (kRecY) {  // C.h_t partials for y, h_t = p_t + delta u B
+          float2* yp = sm.nY + ((buf * kRB + e) * kSP + sp) * 2 * kCQ + cq;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 pF = make_float2(bitsf(hb[8 * e + 2 * j]), bitsf(hb[8 * e + 2 * j + 1]));
+            const float2 pS = make_float2(bitsf(hb[8 * e + 4 + 2 * j]), bitsf(hb[8 * e + 4 + 2 * j + 1]));
+            yp[j * kCQ] = fma2(hi2(cd), fma2(dup[j], BS, pS), mul2(lo2(cd), fma2(dup[j], BF, pF)));
+          }
+        }
+        float wv[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) wv[q] = hsum(fma2(dup[1], dh[q][1], mul2(dup[0], dh[q][0])));
+        // dB contributions dh_t delta u over the quad's channels, then over the
+        // group's; stored after the block's barrier (no stall on the shuffles)
+        if (colsum.feed(e, false, wv[0], wv[1], lane, &pendB)) pendB_t = blk * kRB + ColSum4::token(lane);
+        if constexpr (kStates) {
+          if (((evG >> tt) & 1u) && valid) {
+            float* row = a.dh_init + ((int64_t)a.seq[t0 + tt] * a.D + d) * N;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int n = q ? nS : nF;
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float2 gq2 = mul2(dh[q][j], ex2x2(mul2(dlp[j], A[q][j])));
+                row[(2 * j) * N + n] = gq2.x;
+                row[(2 * j + 1) * N + n] = gq2.y;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) r[q][j] = mul2(dh[q][j], at[q][j]);
+      }
+    };
+    // du and d delta_raw (and dz when y is recomputed) of block blk for this
+    // thread's channel group: item (token e, channel pair) per thread of the
+    // group; the state pairs' partials are added in order
+    auto finalize = [&](int blk) {
+      const int buf = blk & 1;
+      const int tg = tid & 63;
+      const int e = tg >> 4, cpl = tg & 15;
+      const int cp = 16 * grp + cpl, hh = cp & 1, qd = cp >> 1;
+      const int t = blk * kRB + e;
+      if (pendB_t < rows) pdB[pendB_t] = pendB;
+      pendB_t = kL;
+      const float4* np = sm.nred + (buf * kRB + e) * kSP * 2 * kCQ + hh * kCQ + qd;
+      float4 pv[kSP];
+#pragma unroll
+      for (int v = 0; v < kSP; ++v) pv[v] = np[v * 2 * kCQ];
+      // fixed pairwise tree over the 8 state pairs
+      const float4 s = add4(add4(add4(pv[0], pv[1]), add4(pv[2], pv[3])), add4(add4(pv[4], pv[5]), add4(pv[6], pv[7])));
+      const float2 dlv = reinterpret_cast<const float2*>(sm.dl + qd * kQT + t)[hh];
+      const float2 gv = reinterpret_cast<const float2*>(sm.g + qd * kQT + t)[hh];
+      const int at = t * bx + 2 * cp;
+      const float2 uv = ld_io2(sm.u + at);
+      float2 sgv = make_float2(1.0f, 1.0f);
+      if (a.delta_softplus) {  // d softplus / dx = sigmoid(delta_raw + dt_bias)
+        const float2 rr = __fadd2_rn(ld_io2(sm.dr + at), a.dt_bias ? *reinterpret_cast<const float2*>(sm.bias + 2 * cp)
+                                                                   : make_float2(0.0f, 0.0f));
+        sgv = make_float2(sigmoidf_fast(rr.x), sigmoidf_fast(rr.y));
+      }
+      const float2 dsk = a.Dskip ? *reinterpret_cast<const float2*>(sm.dsk + 2 * cp) : make_float2(0.0f, 0.0f);
+      const float2 du = fma2(dlv, lo2(s), mul2(dsk, gv));
+      const bool ok = t < rows && 2 * cp < bx && d0 + 2 * cp < a.D;
+      const float2 ddr = ok ? mul2(fma2(uv, lo2(s), mul2(hi2(s), splat2(kLn2))), sgv) : make_float2(0.0f, 0.0f);
+      if (ok) {
+        const int64_t o2 = (t0 + t) * a.D + d0 + 2 * cp;
+        st_io2(gdu + o2, du);
+        st_io2(gddr + o2, ddr);
+        if constexpr (kRecY) {
+          const float2* yp = sm.nY + (buf * kRB + e) * kSP * 2 * kCQ + hh * kCQ + qd;
+          float2 ys = yp[0];
+#pragma unroll
+          for (int v = 1; v < kSP; ++v) ys = __fadd2_rn(ys, yp[v * 2 * kCQ]);
+          const float2 f = reinterpret_cast<const float2*>(sm.dzf + qd * kQT + t)[hh];
+          st_io2(gdz + o2, mul2(f, fma2(dsk, uv, ys)));
+        }
+      }
+      accB = __fadd2_rn(accB, ddr);
+    };
+    uint32_t hb0[32], hb1[32];
+    __syncwarp();
+    tmem_ld32(thist + 32 * (kL / kRB - 1), hb1);
+    tmem_wait_ld32(hb1);
+#pragma unroll 1
+    for (int bp = kL / (2 * kRB) - 1; bp >= 0; --bp) {
+      __syncwarp();
+      tmem_ld32(thist + 32 * (2 * bp), hb0);
+      block(std::integral_constant<int, 1>{}, bp, hb1);
+      __syncwarp();
+      tmem_wait_ld32(hb0);
+      named_barrier(1 + grp, 64);  // the group's partials of the block are complete
+      finalize(2 * bp + 1);
+      __syncwarp();
+      if (bp > 0) tmem_ld32(thist + 32 * (2 * bp - 1), hb1);
+      block(std::integral_constant<int, 0>{}, bp, hb0);
+      __syncwarp();
+      if (bp > 0) tmem_wait_ld32(hb1);
+      named_barrier(1 + grp, 64);
+      finalize(2 * bp);
+    }
+  }
+
+  // ---- 5. dA partials ([chunk][n][d]); fixed-order CTA sums of dDskip, d_dt_bias
+  if (valid) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int n = q ? nS : nF;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float2 sc = a.a_log ? mul2(A[q][j], splat2(kLn2)) : make_float2(1.0f, 1.0f);
+        *reinterpret_cast<float2*>(a.part_dA + ((int64_t)chunk * N + n) * a.D + d + 2 * j) = mul2(dA[q][j], sc);
+      }
+    }
+  }
+  sm.redD[tid] = accD;
+  sm.redB[tid] = accB;
+  __syncthreads();
+  if (tid == 0) {
+    sm.ticket = next;
+    if (next < n_items) issue(next);
+  }
+  if (tid < kCQ && 4 * tid < bx && d0 + 4 * tid < a.D) {
+    // dDskip: phase-1 quad q = tid % 16 of every thread, in thread order
+    float4 sD = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int v = tid; v < kThr; v += kCQ) sD = add4(sD, sm.redD[v]);
+    *reinterpret_cast<float4*>(a.part_dD + (int64_t)chunk * a.D + d0 + 4 * tid) = sD;
+  }
+  if (tid < 2 * kCQ && 2 * tid < bx && d0 + 2 * tid < a.D) {
+    // d_dt_bias: channel pair cp = 16 g + cpl was finalized by the threads
+    // 64 g + 16 e + cpl, e = 0..3
+    const int g = tid >> 4, cpl = tid & 15;
+    float2 sB = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int e = 0; e < kRB; ++e) sB = __fadd2_rn(sB, sm.redB[64 * g + 16 * e + cpl]);
+    *reinterpret_cast<float2*>(a.part_dbias + (int64_t)chunk * a.D + d0 + 2 * tid) = sB;
+  }
+  __syncthreads();
+  }  // persistent loop
+
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (w == 0) {
+    tmem_fence_after_sync();
+    tmem_dealloc256(sm.taddr);
+  }
+}
+
 // dB[t][n] = sum over tiles of part[tile][n][t]; dC[t][n] likewise from
 // part[tile][N + n][t].  One thread per output, tiles summed in order.
 __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restrict__ part,
@@ -714,6 +1343,23 @@ __global__ void __launch_bounds__(256) sum_tiles_bc_kernel(const float* __restri
   if (v < N) dB[t * N + v] = acc; else dC[t * N + (v - N)] = acc;
 }
 
+template <typename T, bool kStates, bool kRecY, bool kKnob = false>
+cudaError_t launch_k16(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
+                       const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
+                       const CUtensorMap& tm_y, cudaStream_t st) {
+  auto kern = scan_bwd16_kernel<T, kStates, kRecY, kKnob>;
+  const size_t smem = sizeof(Bwd16Smem<T, kRecY>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
+  int grid = 0;
+  // every CTA holds 256 of the SM's 512 tensor-memory columns: at most 2 per SM
+  e = persistent_grid(kern, 128, smem, items, &grid, 2);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 128, smem, st>>>(tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, a);
+  return cudaGetLastError();
+}
+
 template <typename T, int N, bool kStates, bool kRecY, bool kKnob = false>
 cudaError_t launch_k(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
@@ -735,12 +1381,17 @@ template <typename T, int N, bool kRecY>
 cudaError_t launch_y(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, const CUtensorMap& tm_dout, const CUtensorMap& tm_cs,
                      const CUtensorMap& tm_y, cudaStream_t st) {
-  if constexpr (sizeof(T) == 4 && N == 16 && kRecY) {  // the delay knob's instantiation
-    if (a.delay_ticket >= 0 && !a.seq)
-      return launch_k<T, N, false, kRecY, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  if constexpr (N == 16) {
+    if constexpr (sizeof(T) == 4 && kRecY) {  // the delay knob's instantiation
+      if (a.delay_ticket >= 0 && !a.seq)
+        return launch_k16<T, false, kRecY, true>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+    }
+    return a.seq ? launch_k16<T, true, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+                 : launch_k16<T, false, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  } else {
+    return a.seq ? launch_k<T, N, true, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+                 : launch_k<T, N, false, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
   }
-  return a.seq ? launch_k<T, N, true, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
-               : launch_k<T, N, false, kRecY>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
 }
 
 template <typename T, int N>
@@ -779,8 +1430,9 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                                 : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
   if (e != cudaSuccess) return e;
   const int64_t M = a.T * 2 * a.N;
-  sum_tiles_bc_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(a.part_dBC, a.n_tiles, a.T, a.N,
-                                                                   dB, dC);
+  // partial rows come in groups of 32 channels: two per tile when N = 16
+  const int parts = a.n_tiles * (a.N == 16 ? 2 : 1);
+  sum_tiles_bc_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(a.part_dBC, parts, a.T, a.N, dB, dC);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // part_dA is [chunk][n][d]: sum over chunks, written out as dA[d][n]
