@@ -235,7 +235,10 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
  * and output.
  *   - The first call made with a given device current looks up the array's
  *     device address (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture on that device.
+ *     before any stream capture on that device.  The cached address belongs to
+ *     the device's primary context: after cudaDeviceReset (or anything else
+ *     that destroys that context) it is stale, and the process must not call
+ *     this entry point on that device again.
  *   - A problem whose scratch would not fit (about T*D*(N+1)/16 + 8*T
  *     bytes: T = 8192 tokens at D = 4096, N = 16 needs 36 MB and fits;
  *     T = 16384 needs 69 MB and does not) is rejected with
@@ -249,6 +252,8 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
  *   - status: nullable device int32 the call zeroes and into which device-side
  *     errors are OR-ed (decode with vssm_status_code); NULL keeps them in the
  *     scratch, where they cannot be read back.
+ *   - The test knobs of vssm_debug_set apply as they do to
+ *     varlen_selective_scan_fwd.
  */
 #define VSSM_NOALLOC_SCRATCH_BYTES (64u << 20)
 int varlen_selective_scan_fwd_noalloc(const void* u, const void* delta_raw, const float* A,
@@ -284,7 +289,7 @@ int varlen_pack_sequences(const int32_t* lengths, int32_t num_seqs, int32_t pack
                           int32_t window, int32_t* order, int32_t* pack_offsets, int32_t* num_packs,
                           double* padding_rate);
 
-/* ------------------------------------------------------------ status, errors, knobs/* ------------------------------------------------------------ status, errors, knobs
+/* ------------------------------------------------------------ status, errors, knobs
  * vssm_read_status: synchronises `stream`, reads the status word the last call
  * using `workspace` left there, and stores VSSM_OK or a VSSM_ERR_* code in
  * *status.  Returns VSSM_OK or VSSM_ERR_CUDA / VSSM_ERR_ARG.

@@ -208,6 +208,25 @@ int vssm::record_error(int code, const char* message) {
   return code;
 }
 
+vssm::ScanLayout vssm::scan_workspace_layout(int64_t T, int D, int N, int chunk, bool bwd) {
+  const Layout l = scan_layout(T, D, N, chunk, bwd);
+  ScanLayout o;
+  o.flags = l.flags; o.pos = l.pos; o.seq = l.seq; o.agg = l.agg; o.agg_sd = l.agg_sd; o.incl = l.incl;
+  o.part_bc = l.part_bc; o.part_a = l.part_a; o.part_d = l.part_d; o.part_b = l.part_b;
+  o.clear_bytes = l.clear_bytes; o.incl_bytes = l.incl_bytes; o.total = l.total;
+  return o;
+}
+
+int vssm::scan_tile_width(int N, bool bwd) { return scan_tile(N, bwd); }
+
+int vssm::encode_tile_map(CUtensorMap* m, const void* base, IO io, int64_t T, int D, int box_x, int box_y) {
+  return make_map(m, base, io, T, D, box_x, box_y);
+}
+
+vssm::DebugKnobs vssm::debug_knobs() {
+  return DebugKnobs{g_drop_ticket.load(), g_wait_ns.load(), g_delay_ticket.load(), g_delay_ns.load()};
+}
+
 // ============================================================================ C ABI
 extern "C" {
 

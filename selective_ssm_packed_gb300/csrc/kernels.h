@@ -93,7 +93,7 @@ struct ScanArgs {
   void* du;                   // bwd
   void* ddr;                  // bwd
   void* dz;                   // bwd (nullable)
-  float* part_dBC;            // bwd [n_tiles][2N][T]
+  float* part_dBC;            // bwd [32-channel group][2N][T]
   float* part_dA;             // bwd [n_chunks][N][D]
   float* part_dD;             // bwd [n_chunks][D]
   float* part_dbias;          // bwd [n_chunks][D]
@@ -101,10 +101,11 @@ struct ScanArgs {
   unsigned* ticket;
   // look-back state.  fwd: one chain per channel, flags [n_tiles][n_chunks][kTile],
   // agg / incl [n_tiles][n_chunks][N][kTile], agg_sd [n_tiles][n_chunks][kTile]
-  // (sum of delta).  bwd: one chain per (warp = state pair, channel), flags
-  // [n_tiles][n_chunks][N/2], agg / incl / agg_sd [n_tiles][n_chunks][N/2][kTile]
-  // float2, agg_sd holding the products of the transition factors; the flags
-  // announce aggregates only, and incl starts filled with kCarryUnset words.
+  // (sum of delta).  bwd: one chain per thread (its 4 or 8 (channel, state)
+  // words), flags [n_tiles][n_chunks][warp], agg / incl / agg_sd
+  // [n_tiles][n_chunks][thread][words], agg_sd holding the products of the
+  // transition factors; the flags announce aggregates only, and incl starts
+  // filled with kCarryUnset words.
   int* flags;
   float* agg;
   float* agg_sd;
@@ -120,7 +121,7 @@ struct ScanArgs {
   int has_z;
   int has_y;                  // bwd: dz from the given y instead of recomputed C.h + Dskip u
   int has_skip;
-  int box_x;                  // tile row pitch in elements: min(kTile, D)
+  int box_x;                  // tile row pitch in elements: min(tile width, D)
   int box_y;                  // tile rows: min(chunk, T)
   long long drop_ticket;
   unsigned long long wait_ns;
@@ -138,6 +139,33 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
 
 // Sets the message vssm_last_error() returns on this thread; returns `code`.
 int record_error(int code, const char* message);
+
+// ---------------------------------------------------------------- shared host helpers (api.cu)
+// Byte offsets of a scan call's workspace: [header 256 B: status int @0,
+// ticket uint @4][look-back flags][position indices][sequence index]
+// [aggregates][aggregate factors][inclusive states][backward partials].
+// The header and flags (clear_bytes) start at zero; the inclusive states
+// (incl, incl_bytes) start as all-ones words.
+struct ScanLayout {
+  size_t flags = 0, pos = 0, seq = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0;
+  size_t clear_bytes = 0, incl_bytes = 0, total = 0;
+};
+// chunk = tokens per work item (kFwdChunk / kBwdChunk).
+ScanLayout scan_workspace_layout(int64_t T, int D, int N, int chunk, bool bwd);
+// Channels per work item of a scan call (64 for the backward with N = 16, else 32).
+int scan_tile_width(int N, bool bwd);
+// 2-D tensor map over a (T, D) row-major tensor, box = box_x channels x
+// box_y tokens; returns VSSM_OK or a VSSM_ERR_* code (message recorded).
+int encode_tile_map(CUtensorMap* m, const void* base, IO io, int64_t T, int D, int box_x, int box_y);
+// The test knobs set by vssm_debug_set, as the kernels take them.
+struct DebugKnobs {
+  long long drop_ticket;
+  unsigned long long wait_ns;
+  long long delay_ticket;
+  unsigned long long delay_ns;
+};
+DebugKnobs debug_knobs();
 
 // ---------------------------------------------------------------- reductions
 // out[m] = sum_{p < P} in[p * ld + m] for m < M, in a fixed order (rows in

@@ -18,8 +18,6 @@
 // look-back states with the all-ones word that reads as "not stored yet".
 // Calls that overlap on the GPU (two streams, or two host threads on one
 // device) race on it.
-#include <cudaTypedefs.h>
-
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -31,7 +29,6 @@ namespace vssm {
 namespace {
 
 constexpr size_t kScratchBytes = VSSM_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kAlign = 256;
 constexpr int kMaxDevices = 64;
 
 }  // namespace
@@ -46,9 +43,6 @@ namespace {
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
-size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
 int err(int code, const char* fmt, long long a = 0, long long b = 0) {
   char buf[256];
   snprintf(buf, sizeof(buf), fmt, a, b);
@@ -56,7 +50,10 @@ int err(int code, const char* fmt, long long a = 0, long long b = 0) {
 }
 
 // Device address of the scratch on the current device, looked up on the first
-// call made with that device current and cached per device afterwards.
+// call made with that device current and cached per device afterwards.  The
+// cache outlives nothing but the device's context: after cudaDeviceReset (or
+// anything else that destroys the primary context) the cached address is
+// stale, and the process must not call the entry point on that device again.
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -78,38 +75,8 @@ int scratch_address(void** out) {
   return VSSM_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-int map2d(CUtensorMap* m, const void* base, IO io, int64_t T, int D, int bx, int by) {
-  std::memset(m, 0, sizeof(*m));
-  if (!base) return VSSM_OK;
-  auto enc = encoder();
-  if (!enc) return record_error(VSSM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)T};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * (cuuint64_t)io_bytes(io)};
-  const cuuint32_t box[2] = {(cuuint32_t)bx, (cuuint32_t)by};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, io == IO::F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         2, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return err(VSSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%lld)", (long long)r);
-  return VSSM_OK;
-}
-
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 }  // namespace vssm
@@ -149,30 +116,22 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
                         "z, y, chunk_states, A, Dskip, dt_bias, position_indices, initial_states and "
                         "final_states must be 16-byte aligned");
 
-  // ---- scratch layout: [header: status, ticket][flags][pos][seq][agg][agg_sd][incl]
-  const int64_t n_tiles = cdiv(D, kTile), n_chunks = cdiv(T, kFwdChunk);
-  const size_t slots = (size_t)(n_tiles * n_chunks);
-  const size_t o_flags = kAlign;
-  const size_t o_pos = o_flags + up(sizeof(int) * slots * kTile);
-  const size_t o_seq = o_pos + up(sizeof(int32_t) * (size_t)T);
-  const size_t o_agg = o_seq + up(sizeof(int32_t) * (size_t)T);
-  const size_t o_sd = o_agg + up(sizeof(float) * slots * N * kTile);
-  const size_t o_incl = o_sd + up(sizeof(float) * slots * kTile);
-  const size_t need = o_incl + up(sizeof(float) * slots * N * kTile);
-  if (need > kScratchBytes)
+  // ---- the forward call's own workspace layout, placed in the built-in scratch
+  const ScanLayout l = scan_workspace_layout(T, D, N, kFwdChunk, false);
+  if (l.total > kScratchBytes)
     return err(VSSM_ERR_WORKSPACE,
                "this problem needs %lld bytes of scratch but the built-in scratch holds %lld bytes; "
                "use varlen_selective_scan_fwd with a caller-allocated workspace",
-               (long long)need, (long long)kScratchBytes);
+               (long long)l.total, (long long)kScratchBytes);
 
   void* base = nullptr;
   const int rc = scratch_address(&base);
   if (rc != VSSM_OK) return rc;
   char* s = static_cast<char*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t ce = cudaMemsetAsync(s, 0, o_pos, st);  // status, ticket, look-back flags
+  cudaError_t ce = cudaMemsetAsync(s, 0, l.clear_bytes, st);  // status, ticket, look-back flags
   // look-back states: all-ones NaN words, read by the kernel as "not stored yet"
-  if (ce == cudaSuccess && T > 0) ce = cudaMemsetAsync(s + o_incl, 0xff, sizeof(float) * slots * N * kTile, st);
+  if (ce == cudaSuccess && T > 0) ce = cudaMemsetAsync(s + l.incl, 0xff, l.incl_bytes, st);
   if (ce == cudaSuccess && status) ce = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
   // an empty sequence ends in the state it starts from
   if (ce == cudaSuccess)
@@ -182,47 +141,50 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   int32_t* status_word = status ? status : reinterpret_cast<int32_t*>(s);
   const int32_t* seq = nullptr;
   if (initial_states || final_states) {
-    ce = launch_sequence_index(cu_seqlens, num_seqs, T, reinterpret_cast<int32_t*>(s + o_seq), st);
+    ce = launch_sequence_index(cu_seqlens, num_seqs, T, reinterpret_cast<int32_t*>(s + l.seq), st);
     if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
-    seq = reinterpret_cast<int32_t*>(s + o_seq);
+    seq = reinterpret_cast<int32_t*>(s + l.seq);
   }
 
   const int32_t* pos = position_indices;
   if (!pos) {
-    int32_t* p = reinterpret_cast<int32_t*>(s + o_pos);
+    int32_t* p = reinterpret_cast<int32_t*>(s + l.pos);
     ce = launch_position_indices(cu_seqlens, num_seqs, T, p, status_word, st);
     if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
     pos = p;
   }
 
+  const int tw = scan_tile_width(N, false);
+  const DebugKnobs kn = debug_knobs();
   ScanArgs a{};
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
   a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
   a.status = status_word;
   a.ticket = reinterpret_cast<unsigned*>(s + 4);
-  a.flags = reinterpret_cast<int*>(s + o_flags);
-  a.agg = reinterpret_cast<float*>(s + o_agg);
-  a.agg_sd = reinterpret_cast<float*>(s + o_sd);
-  a.incl = reinterpret_cast<float*>(s + o_incl);
+  a.flags = reinterpret_cast<int*>(s + l.flags);
+  a.agg = reinterpret_cast<float*>(s + l.agg);
+  a.agg_sd = reinterpret_cast<float*>(s + l.agg_sd);
+  a.incl = reinterpret_cast<float*>(s + l.incl);
   a.T = T; a.D = D; a.N = N;
-  a.n_tiles = (int)n_tiles;
-  a.n_chunks = (int)n_chunks;
+  a.n_tiles = (int)cdiv(D, tw);
+  a.n_chunks = (int)cdiv(T, kFwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
   a.gate_floor = gate_floor;
   a.a_log = a_log ? 1 : 0;
   a.has_z = z ? 1 : 0;
   a.has_skip = Dskip ? 1 : 0;
-  a.box_x = D < kTile ? D : kTile;
+  a.box_x = D < tw ? D : tw;
   a.box_y = T < kFwdChunk ? (int)T : kFwdChunk;
-  a.drop_ticket = -1;
-  a.wait_ns = 1000000000ull;
-  a.delay_ticket = -1;
-  a.delay_ns = 0;
+  // the test knobs of vssm_debug_set apply here as in the workspace entry point
+  a.drop_ticket = kn.drop_ticket;
+  a.wait_ns = kn.wait_ns;
+  a.delay_ticket = kn.delay_ticket;
+  a.delay_ns = kn.delay_ns;
   CUtensorMap mu, mdr, mz;
-  int r = map2d(&mu, u, io, T, D, a.box_x, a.box_y);
-  if (r == VSSM_OK) r = map2d(&mdr, delta_raw, io, T, D, a.box_x, a.box_y);
-  if (r == VSSM_OK) r = map2d(&mz, z, io, T, D, a.box_x, a.box_y);
+  int r = encode_tile_map(&mu, u, io, T, D, a.box_x, a.box_y);
+  if (r == VSSM_OK) r = encode_tile_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y);
+  if (r == VSSM_OK) r = encode_tile_map(&mz, z, io, T, D, a.box_x, a.box_y);
   if (r != VSSM_OK) return r;
   ce = launch_scan_fwd(a, io, mu, mdr, mz, st);
   if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));

@@ -25,7 +25,10 @@ log-normal mixes instead of a real corpus):
 Values: x (conv input), u (scan input when the scan is run alone), z, B, C,
 dout ~ N(0, 1); delta_raw ~ N(0, 0.5^2); dt_bias = inverse-softplus of
 dt ~ logU[1e-3, 1e-1] per channel; A[d, n] = -(n + 1); Dskip = 1; conv
-weight and bias ~ U(-1/sqrt(W), 1/sqrt(W)).
+weight and bias ~ U(-1/sqrt(W), 1/sqrt(W)).  With params="general" (the
+parity cases) A and Dskip are drawn instead, as a learned layer holds them:
+A[d, n] = -U(0.05, 4) per entry and Dskip ~ N(0, 1), from a generator of
+their own, so every other value is the same as with the default.
 """
 from __future__ import annotations
 
@@ -133,16 +136,24 @@ def padded_layout(lengths):
 
 
 def draw_values(T: int, D: int, N: int, W: int, seed: int, backward: bool = True,
-                scan_input: bool = True) -> dict:
+                scan_input: bool = True, params: str = "s4d") -> dict:
     """Seeded float32 values for one pack of T tokens (see module docstring).
     Keys: x, u, delta_raw, z, B, C, dout (activations); A, Dskip, dt_bias,
-    conv_w, conv_b (parameters)."""
+    conv_w, conv_b (parameters).  params: "s4d" (A = -(n+1), Dskip = 1) or
+    "general" (A = -U(0.05, 4), Dskip ~ N(0, 1))."""
     rng = np.random.default_rng(seed + 1_000_003)
     f32 = np.float32
     v = {}
     # parameters first so that they do not depend on T
-    v["A"] = np.tile(-(np.arange(N, dtype=f32) + 1.0), (D, 1)).astype(f32)
-    v["Dskip"] = np.ones(D, dtype=f32)
+    if params == "s4d":
+        v["A"] = np.tile(-(np.arange(N, dtype=f32) + 1.0), (D, 1)).astype(f32)
+        v["Dskip"] = np.ones(D, dtype=f32)
+    elif params == "general":
+        prng = np.random.default_rng(seed + 2_000_003)
+        v["A"] = (-prng.uniform(0.05, 4.0, size=(D, N))).astype(f32)
+        v["Dskip"] = prng.standard_normal(D).astype(f32)
+    else:
+        raise ValueError(f"params must be 's4d' or 'general', got {params!r}")
     dt = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=D))
     v["dt_bias"] = (dt + np.log(-np.expm1(-dt))).astype(f32)
     bound = 1.0 / math.sqrt(W)

@@ -58,9 +58,15 @@ def test_parse_clocks():
 
 
 def test_per_token_counts_match_the_stated_totals():
+    """The step's algorithmic counts: 16eD + 4eN + 8N + 16 bytes, D(17N + 59)
+    FP32-pipe ops and D(2N + 14) MUFU ops per token, i.e. 131,344 B,
+    1,355,776 and 188,416 at the Mamba-1.4B shape (D = 4096, N = 16, bf16)."""
     D, N, e = 4096, 16, 2
     c = bench.per_token_counts(D, N, e)
     tot = {k: sum(s[k] for s in c.values()) for k in ("bytes", "fp32", "mufu")}
-    assert tot["bytes"] == 18 * e * D + 4 * e * N + 8 * N + 16
-    assert tot["fp32"] == D * (16 * N + 59)
-    assert tot["mufu"] == D * (2 * N + 14)
+    assert tot["bytes"] == 16 * e * D + 4 * e * N + 8 * N + 16 == 131344
+    assert tot["fp32"] == D * (17 * N + 59) == 1355776
+    assert tot["mufu"] == D * (2 * N + 14) == 188416
+    # forward only: 6eD + 2eN + 8 bytes, D(4N + 17) FP32, D(N + 6) MUFU
+    fwd = {k: c["conv_fwd"][k] + c["scan_fwd"][k] for k in ("bytes", "fp32", "mufu")}
+    assert fwd == {"bytes": 6 * e * D + 2 * e * N + 8, "fp32": D * (4 * N + 17), "mufu": D * (N + 6)}
