@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -35,26 +36,37 @@ if ROOT not in sys.path:
 
 METRIC = "packed tokens/s for varlen conv1d+selective scan fwd+bwd; % of roofline"
 
-# Algorithmic per-token counts of the step (bytes moved, FP32-pipe ops with
-# FMA = 1, MUFU ops), e = bytes per I/O element; see the design doc.  The forward
-# writes the pre-gate output y and the backward reads it for dz (so it does not
-# recompute C.h).
+# Algorithmic per-token counts of each stage (bytes moved, FP32-pipe ops with
+# FMA = 1, MUFU ops), e = bytes per I/O element, as the path's scope defines
+# them: the forward reads u, delta_raw, z and writes out; the backward reads
+# u, delta_raw, z, dout and writes du, d delta_raw, dz; the backward's FP32
+# count is 13 D N + 24 D (the state recompute, the reverse recurrence, the
+# four channel / state sums and the C.h of y).  The roofline fractions use
+# these.
 def per_token_counts(D, N, e, W=4):
     return {
         "conv_fwd": dict(bytes=2 * e * D + 4, fp32=(W + 3) * D, mufu=2 * D),
-        "scan_fwd": dict(bytes=5 * e * D + 2 * e * N + 4, fp32=4 * D * N + 10 * D, mufu=D * N + 4 * D),
-        "scan_bwd": dict(bytes=8 * e * D + 2 * e * N + 8 * N + 4, fp32=12 * D * N + 24 * D, mufu=D * N + 6 * D),
+        "scan_fwd": dict(bytes=4 * e * D + 2 * e * N + 4, fp32=4 * D * N + 10 * D, mufu=D * N + 4 * D),
+        "scan_bwd": dict(bytes=7 * e * D + 2 * e * N + 8 * N + 4, fp32=13 * D * N + 24 * D, mufu=D * N + 6 * D),
         "conv_bwd": dict(bytes=3 * e * D + 4, fp32=(3 * W + 6) * D, mufu=2 * D),
     }
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the last ncu
-# capture of a kernel, per token; reset an entry to nothing as soon as the
-# kernel changes (profiles/ keeps the capture summaries).
+# What this implementation moves on top of those counts, per token: the
+# forward also writes its pre-gate output y (e D bytes) and the backward reads
+# it for dz instead of recomputing C.h (e D bytes, and D N fewer FP32 ops).
+def implementation_extra_bytes(D, e):
+    return {"scan_fwd": e * D, "scan_bwd": e * D}
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the latest
+# ncu capture of a kernel, per token, with the kernel it was taken on; the
+# line reports it only for that kernel.
 LAST_CAPTURE_TRAFFIC = {
-    ("m14b", "scan_bwd"): {"bytes_per_token": (404.583936e6 + 439.550464e6) / 8192,
-                           "source": "ncu capture of scan_bwd_kernel on m14b_small (T=8192), "
-                                     "scaled by tokens; profiles/scan_bwd_m14b_small.md"},
+    ("m14b", "scan_bwd"): {"bytes_per_token": (407.139584e6 + 440.144640e6) / 8192,
+                           "kernel": "scan_bwd16_kernel",
+                           "source": "ncu --set full capture of scan_bwd16_kernel on m14b_small (T=8192), "
+                                     "scaled by tokens"},
 }
 
 
@@ -71,11 +83,15 @@ def parse_args(argv=None):
     p.add_argument("--no-comparators", action="store_true",
                    help="skip the no-reset concat bound and the packed-vs-padded comparison")
     p.add_argument("--comparator-steps", type=int, default=10)
-    p.add_argument("--comparator-d", type=int, default=512,
-                   help="channels for the packed-vs-padded comparison (the padded long-tail layout "
-                        "holds ~2.2 M tokens)")
+    p.add_argument("--comparator-d", type=int, default=4096,
+                   help="channels for the packed-vs-padded comparison (the long-tail workload's width)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip timing the other workloads (m130m and m14b_fwd forward, long-tail fwd+bwd)")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target wall time of the CPU-oracle baseline sample")
+    p.add_argument("--clock-log", default=None,
+                   help="file for the nvidia-smi clock samples of the timed region ({rank} is replaced); "
+                        "default: a temporary file")
     return p.parse_args(argv)
 
 
@@ -240,8 +256,11 @@ def run_reference(args):
             times.append(sec)
     sec = sum(times) / len(times)
     value = T * (ch / D) / sec
+    # ms_per_step is what one timed step took (a channel sample of the step);
+    # the whole step's time is extrapolated from it by D / ch
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * D / ch,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "ms_per_full_step_extrapolated": sec * 1e3 * D / ch, "sample_channels": ch,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(w, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -253,11 +272,11 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our arm
-def probe_alu():
+def probe_alu(n_sm):
     """FP32 / packed-FP32 / MUFU throughput of this GPU (ops/s), or {}."""
-    from selective_ssm_packed_gb300 import build
+    import __graft_entry__
     try:
-        lib = ctypes.CDLL(build.PROBE_PATH)
+        lib = ctypes.CDLL(__graft_entry__.PROBE_PATH)
     except OSError:
         return {}
     fn = lib.vssm_probe_alu
@@ -265,14 +284,19 @@ def probe_alu():
     out = {}
     for kind, name, iters in ((0, "fp32_fma", 20000), (1, "fp32x2_fma", 20000), (2, "mufu_ex2", 5000)):
         v = ctypes.c_double(0.0)
-        if fn(kind, 152 * 8, iters, ctypes.byref(v)) == 0:
+        if fn(kind, n_sm * 8, iters, ctypes.byref(v)) == 0:
             out[name + "_tops"] = v.value / 1e12
     return out
 
 
-def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=None):
-    """Seconds per full step (pos, conv fwd, scan fwd, scan bwd, conv bwd) for
-    the packed layout cu_np, on seeded device-generated inputs (timing only)."""
+def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=None, backward=True,
+              flush=None):
+    """Seconds per step for the packed layout cu_np, on seeded device-generated
+    inputs with the workloads' value distributions (timing only).  A step is
+    pos, conv fwd, scan fwd and, with backward, scan bwd and conv bwd.  With
+    `flush` (a device tensor larger than the L2), the tensor is overwritten
+    before every step, outside the timed events, and the median of the
+    per-step times is returned; otherwise steps run back to back."""
     import numpy as np
     tdt = dtype or torch.bfloat16
     T = int(cu_np[-1])
@@ -311,6 +335,9 @@ def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=No
     def step():
         vs.varlen_position_indices(cu, T, out=pos)
         vs.varlen_conv1d_fwd(x, cw, cb, cu, pos, out=u, workspace=ws["cf"])
+        if not backward:  # a forward pass: no pre-gate output or saved states needed
+            vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, workspace=ws["sf"])
+            return
         vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, chunk_states=states,
                                      workspace=ws["sf"], y=ypre)
         vs.varlen_selective_scan_bwd(u, dr, A, B, C, Dsk, z, dtb, dout, cu, states, pos, grads=grads,
@@ -320,17 +347,30 @@ def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=No
     for _ in range(3):
         step()
     torch.cuda.synchronize(device)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
-    torch.cuda.synchronize(device)
-    for k in ("sf", "sb"):
+    if flush is not None:
+        times = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            torch.cuda.synchronize(device)
+            times.append(a.elapsed_time(b) / 1e3)
+        sec = statistics.median(times)
+    else:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            step()
+        b.record()
+        torch.cuda.synchronize(device)
+        sec = a.elapsed_time(b) / 1e3 / steps
+    for k in ("sf", "sb") if backward else ("sf",):
         st = binding.read_status(ws[k])
         if st != 0:
-            raise RuntimeError(f"device status {binding.ERR.get(st, st)} in a comparator run ({k})")
-    return a.elapsed_time(b) / 1e3 / steps
+            raise RuntimeError(f"device status {binding.ERR.get(st, st)} in a timing run ({k})")
+    return sec
 
 
 def comparators(args, torch, vs, binding, device, w, step_sec):
@@ -349,18 +389,35 @@ def comparators(args, torch, vs, binding, device, w, step_sec):
                               "config": f"{args.workload} with cu_seqlens = [0, {T}] (one sequence)"}
     lengths = wls.pack_lengths("longtail")
     cu_pk = wls.cu_seqlens_from_lengths(lengths)
-    cu_pad, _ = wls.padded_layout(lengths)
+    rows = [wls.bucket_of(L) for L in lengths]
     Dc = args.comparator_d
-    T_real, T_pad = int(cu_pk[-1]), int(cu_pad[-1])
+    T_real, T_pad = int(cu_pk[-1]), int(sum(rows))
     psec = time_case(torch, vs, binding, device, cu_pk, Dc, 16, 4, args.comparator_steps, seed=12)
-    qsec = time_case(torch, vs, binding, device, cu_pad, Dc, 16, 4, max(2, args.comparator_steps // 4),
-                     seed=13)
+    # the right-padded layout (each sequence its own row of its bucket length)
+    # holds ~2.2 M tokens, too many for one call's buffers at D = 4096: its rows
+    # run in groups of at most the packed call's token count, and the groups'
+    # step times add up to the padded step
+    groups, cur, cur_t = [], [], 0
+    for L in sorted(rows):
+        if cur and cur_t + L > T_real:
+            groups.append(cur)
+            cur, cur_t = [], 0
+        cur.append(L)
+        cur_t += L
+    if cur:
+        groups.append(cur)
+    qsec = 0.0
+    for gi, grp in enumerate(groups):
+        qsec += time_case(torch, vs, binding, device, wls.cu_seqlens_from_lengths(grp), Dc, 16, 4,
+                          max(2, args.comparator_steps // 4), seed=13 + gi)
     res["longtail_packed_vs_padded"] = {
         "packed_tokens_per_s": T_real / psec, "padded_real_tokens_per_s": T_real / qsec,
+        "packed_ms_per_step": psec * 1e3, "padded_ms_per_step": qsec * 1e3,
         "speedup": qsec / psec, "real_tokens": T_real, "padded_tokens": T_pad,
-        "padding_rate": 1.0 - T_real / T_pad,
+        "padding_rate": 1.0 - T_real / T_pad, "padded_row_groups": len(groups),
         "config": f"long-tail packs ({len(lengths)} sequences, {T_real} tokens), D={Dc}, N=16, bf16, "
-                  f"buckets {list(wls.BUCKETS)}; same kernels, fwd+bwd"}
+                  f"buckets {list(wls.BUCKETS)}; same kernels, fwd+bwd; padded rows in "
+                  f"{len(groups)} groups of at most {T_real} tokens, times summed"}
     # the packer (host side): arrival-order packing against local greedy on the
     # bench workload's length mix, as the article compares them
     rng = np.random.default_rng(14)
@@ -372,6 +429,57 @@ def comparators(args, torch, vs, binding, device, w, step_sec):
         pk[name] = {"packs": len(packs), "padding_rate": pad, "ms": (time.perf_counter() - t0) * 1e3}
     pk["config"] = "20000 lengths LogN(ln 800, 1) clipped [32, 4096], packs of 4096 tokens, host C++"
     res["packing"] = pk
+    return res
+
+
+def path_bound(counts, stages, T, hbm_gbs, fp32_tops, mufu_tops):
+    """The path roofline of the given stages: per bound, the time T tokens need
+    at the peak, and the slowest of them."""
+    tot = {k: sum(counts[s][k] for s in stages) for k in ("bytes", "fp32", "mufu")}
+    parts = {"hbm": tot["bytes"] * T / (hbm_gbs * 1e9), "fp32": tot["fp32"] * T / (fp32_tops * 1e12)}
+    if mufu_tops:
+        parts["mufu"] = tot["mufu"] * T / (mufu_tops * 1e12)
+    return parts, max(parts.values())
+
+
+def other_configs(args, torch, vs, binding, device, longtail_sec, hbm_gbs, fp32_tops, mufu_tops):
+    """Tokens/s and path-roofline fraction of the other workloads: the
+    Mamba-130M forward (fp32; its tensors fit in the L2, so it is timed both
+    with a 512 MiB write between steps and back to back), the Mamba-1.4B
+    forward, and the long-tail forward + backward (timed by the comparator)."""
+    from selective_ssm_packed_gb300 import workloads as wls
+    res = {}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    for name, flushed in (("m130m", True), ("m14b_fwd", False)):
+        wl = wls.WORKLOADS[name]
+        cu = wls.cu_seqlens_from_lengths(wls.pack_lengths(name))
+        T = int(cu[-1])
+        tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+        e = 4 if wl.dtype == "f32" else 2
+        counts = per_token_counts(wl.D, wl.N, e, wl.W)
+        parts, t_roof = path_bound(counts, ("conv_fwd", "scan_fwd"), T, hbm_gbs, fp32_tops, mufu_tops)
+        entry = {"config": f"{name}: {wl.description}; pos + conv1d fwd + selective scan fwd",
+                 "T": T, "path_bound_ms": {k: v * 1e3 for k, v in parts.items()}}
+        runs = (("l2_flushed", flush), ("back_to_back", None)) if flushed else (("back_to_back", None),)
+        for key, fl in runs:
+            sec = time_case(torch, vs, binding, device, cu, wl.D, wl.N, wl.W, 50, seed=wl.seed, dtype=tdt,
+                            backward=False, flush=fl)
+            entry[key] = {"value": T / sec, "unit": "tokens/s", "ms_per_step": sec * 1e3,
+                          "frac_of_path_roofline": t_roof / sec}
+        if flushed:
+            entry["l2"] = "each (T, D) tensor is 24 MiB and fits in the 129 MB L2: l2_flushed overwrites " \
+                          "a 512 MiB buffer before every step (median of 50 steps)"
+        res[name] = entry
+    if longtail_sec:
+        wl = wls.WORKLOADS["longtail"]
+        T = int(wls.cu_seqlens_from_lengths(wls.pack_lengths("longtail"))[-1])
+        counts = per_token_counts(wl.D, wl.N, 2, wl.W)
+        parts, t_roof = path_bound(counts, tuple(counts), T, hbm_gbs, fp32_tops, mufu_tops)
+        res["longtail"] = {"config": f"longtail: {wl.description}; the whole step",
+                           "T": T, "value": T / longtail_sec, "unit": "tokens/s",
+                           "ms_per_step": longtail_sec * 1e3, "frac_of_path_roofline": t_roof / longtail_sec,
+                           "path_bound_ms": {k: v * 1e3 for k, v in parts.items()}}
+    del flush
     return res
 
 
@@ -455,8 +563,8 @@ def run_ours(args):
             raise RuntimeError(f"device status {binding.ERR.get(st, st)} after warm-up ({k})")
 
     # --- device-resident throughput, per-stage events on the launching stream
-    clocks_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/vssm_clocks_{os.getpid()}.csv"
+    clocks_path = args.clock_log.replace("{rank}", str(rank)) if args.clock_log else \
+        os.path.join(tempfile.gettempdir(), f"vssm_clocks_{os.getpid()}_rank{rank}.csv")
     sampler = ClockSampler(local, clocks_path)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     barrier(device)
@@ -626,8 +734,9 @@ def run_ours(args):
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    fp32_peak_tops = 152 * 128 * sm_max * 1e6 / 1e12         # FP32 pipe, FMA = 1 op
-    probes = probe_alu() if rank == 0 else {}
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+    fp32_peak_tops = n_sm * 128 * sm_max * 1e6 / 1e12         # FP32 pipe, FMA = 1 op
+    probes = probe_alu(n_sm) if rank == 0 else {}
     stages = {}
     for s in ("conv_fwd", "scan_fwd", "scan_bwd", "conv_bwd"):
         c, ms = counts[s], stage_ms[s]
@@ -641,7 +750,7 @@ def run_ours(args):
     if t_alu >= t_hbm:
         roof = {"kernel": dom, "bound": "alu", "achieved": stages[dom]["fp32_Tops/s"], "peak": fp32_peak_tops,
                 "unit": "Tops/s (fp32 pipe, FMA=1)",
-                "peak_source": f"152 SMs x 128 FP32 lanes x {sm_max:.0f} MHz (max SM clock)"}
+                "peak_source": f"{n_sm} SMs x 128 FP32 lanes x {sm_max:.0f} MHz (max SM clock)"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": stages[dom]["GB/s"], "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)"}
@@ -650,20 +759,27 @@ def run_ours(args):
     roof["traffic"] = tr["bytes_per_token"] * T if tr else None
     if tr:
         roof["traffic_source"] = tr["source"]
+        roof["traffic_kernel"] = tr["kernel"]
     roof["algorithmic_per_token"] = c
+    roof["counts"] = ("algorithmic per-token counts of the path's scope; this implementation also moves "
+                      "the pre-gate output y (per token: "
+                      + ", ".join(f"{k} +{v} B" for k, v in implementation_extra_bytes(D, e).items()) + ")")
     # whole-step roofline (the metric's definition): slowest of HBM, FP32, MUFU bounds
-    tot = {k: sum(counts[s][k] for s in counts) for k in ("bytes", "fp32", "mufu")}
     mufu_tops = probes.get("mufu_ex2_tops")
-    t_parts = {"hbm": tot["bytes"] * T / (hbm_peak * 1e9), "fp32": tot["fp32"] * T / (fp32_peak_tops * 1e12)}
-    if mufu_tops:
-        t_parts["mufu"] = tot["mufu"] * T / (mufu_tops * 1e12)
-    t_roof = max(t_parts.values())
+    t_parts, t_roof = path_bound(counts, tuple(counts), T, hbm_peak, fp32_peak_tops, mufu_tops)
     step_ms = sec * 1e3 / args.steps
     path_roofline = {"step_bound_ms": {k: v * 1e3 for k, v in t_parts.items()},
                      "roofline_tokens_per_s": T / t_roof, "frac_of_roofline": t_roof / (step_ms * 1e-3),
                      "alu_probe_tops": probes}
 
-    # --- CPU oracle baseline (rank 0, one GPU only)
+    # --- the other workloads (rank 0, one GPU only)
+    cfgs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        lt = comp["longtail_packed_vs_padded"]["packed_ms_per_step"] / 1e3 \
+            if comp and args.comparator_d == 4096 else None
+        cfgs = other_configs(args, torch, vs, binding, device, lt, hbm_peak, fp32_peak_tops, mufu_tops)
+
+    # --- CPU oracle baseline (rank 0, one GPU only): all host cores, and one core
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         ch = sized_sample(w, r, args.cpu_seconds)
@@ -671,13 +787,19 @@ def run_ours(args):
         cpu = {"value": T * (ch / D) / csec, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{ch} of {D} channels over all {T} tokens (conv1d + selective scan fwd + bwd, "
                          f"double), {csec:.1f} s; tokens/s scaled by {D}/{ch}"}
+        # one core: a sample sized to about 3 s from a 16-channel probe
+        c16, _ = oracle_sample(w, r, 16, threads=1)
+        ch1 = max(16, min(D, int(16 * 3.0 / max(c16, 1e-3)) // 16 * 16))
+        csec1, _ = oracle_sample(w, r, ch1, threads=1)
+        cpu["one_core"] = {"value": T * (ch1 / D) / csec1, "unit": "tokens/s", "cores": 1,
+                           "sample": f"{ch1} of {D} channels over all {T} tokens, {csec1:.1f} s"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": sec_max * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": config_of(w, world), "roofline": roof, "path_roofline": path_roofline,
-                "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "comparators": comp,
+                "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "comparators": comp, "configs": cfgs,
                 "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
     return 0

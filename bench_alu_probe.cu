@@ -1,5 +1,5 @@
-// probe.cu -- throughput probes for the scan's arithmetic units on the local
-// GPU (measurement support for the benchmark; not part of libvarlen_ssm's ABI).
+// bench_alu_probe.cu -- throughput probes for the scan's arithmetic units on the local
+// GPU (measurement support for bench.py; not part of libvarlen_ssm).
 //
 //   kind 0: FP32 FMA        (fma.rn.f32, 8 independent chains per thread)
 //   kind 1: packed FP32 FMA (fma.rn.f32x2, 8 chains, 2 lanes each)

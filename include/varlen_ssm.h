@@ -308,12 +308,17 @@ const char* vssm_last_error(void);      /* thread-local; "" if none */
  * past published aggregates; the results do not change, bit for bit.  The
  * delay applies to fp32 scan calls with N = 16 and no sequence states, which
  * then run a build of the kernels of their own (the other builds carry no
- * code for it); other calls ignore it.
+ * code for it); other calls ignore it.  VSSM_DBG_FORCE_COPY_TIMEOUT: in the
+ * conv calls, the CTA with this index reports its tile-copy wait as timed out
+ * once the copy has landed (-1 = off), so a test sees VSSM_ERR_LOOKBACK_TIMEOUT
+ * in the call's status word without any copy failing; the conv calls' copy
+ * waits also take their limit from VSSM_DBG_WAIT_NS.
  * Returns VSSM_OK or VSSM_ERR_ARG. */
 #define VSSM_DBG_DROP_FLAG 1
 #define VSSM_DBG_WAIT_NS 2
 #define VSSM_DBG_DELAY_ITEM 3
 #define VSSM_DBG_DELAY_NS 4
+#define VSSM_DBG_FORCE_COPY_TIMEOUT 5
 int vssm_debug_set(int knob, int64_t value);
 
 #ifdef __cplusplus

@@ -21,6 +21,7 @@ from . import build as _build
 VSSM_F32, VSSM_BF16 = 0, 1
 VSSM_STATE_CHUNK = 32
 VSSM_DBG_DROP_FLAG, VSSM_DBG_WAIT_NS, VSSM_DBG_DELAY_ITEM, VSSM_DBG_DELAY_NS = 1, 2, 3, 4
+VSSM_DBG_FORCE_COPY_TIMEOUT = 5
 ERR = {0: "VSSM_OK", -1: "VSSM_ERR_ARG", -2: "VSSM_ERR_DTYPE", -3: "VSSM_ERR_ALIGN",
        -4: "VSSM_ERR_WORKSPACE", -5: "VSSM_ERR_CUDA", -6: "VSSM_ERR_UNSUPPORTED",
        -16: "VSSM_ERR_BAD_CU_SEQLENS", -17: "VSSM_ERR_LOOKBACK_TIMEOUT"}

@@ -19,7 +19,6 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libvarlen_ssm.so")
-PROBE_PATH = os.path.join(BUILD_DIR, "libvssm_probe.so")   # ALU throughput probes (benchmark only)
 
 SOURCES = ["api.cu", "misc.cu", "conv.cu", "scan_fwd.cu", "scan_bwd.cu", "noalloc.cu", "packer.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
@@ -79,13 +78,6 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB_PATH)
-    probe_src = os.path.join(CSRC, "probe.cu")
-    if force or _stale(PROBE_PATH, [probe_src]):
-        tmp = PROBE_PATH + f".tmp{os.getpid()}"
-        r = subprocess.run([nvcc, *_flags(), "-shared", probe_src, "-o", tmp], capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"probe build failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, PROBE_PATH)
     return LIB_PATH
 
 

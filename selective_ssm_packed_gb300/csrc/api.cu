@@ -22,6 +22,7 @@ std::atomic<long long> g_drop_ticket{-1};
 std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 std::atomic<long long> g_delay_ticket{-1};
 std::atomic<unsigned long long> g_delay_ns{200000ull};
+std::atomic<long long> g_force_copy_timeout{-1};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -246,7 +247,7 @@ const char* vssm_strerror(int code) {
     case VSSM_ERR_CUDA: return "CUDA runtime or driver error";
     case VSSM_ERR_UNSUPPORTED: return "unsupported N or conv width";
     case VSSM_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens (device check)";
-    case VSSM_ERR_LOOKBACK_TIMEOUT: return "cross-chunk wait timed out (device check)";
+    case VSSM_ERR_LOOKBACK_TIMEOUT: return "a device-side wait timed out: look-back or tile copy (device check)";
   }
   return "unknown status code";
 }
@@ -266,6 +267,7 @@ int vssm_debug_set(int knob, int64_t value) {
     g_delay_ns.store((unsigned long long)value);
     return VSSM_OK;
   }
+  if (knob == VSSM_DBG_FORCE_COPY_TIMEOUT) { g_force_copy_timeout.store(value); return VSSM_OK; }
   return fail(VSSM_ERR_ARG, "unknown debug knob %d", knob);
 }
 
@@ -333,6 +335,9 @@ int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
   a.x = x; a.w = weight; a.bias = bias; a.out = u;
   a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
   a.cu = cu_seqlens; a.num_seqs = num_seqs; a.x_init = W > 1 ? x_init : nullptr; a.x_last = x_last;
+  a.status = at<int>(workspace, 0);
+  a.wait_ns = g_wait_ns.load();
+  a.force_timeout_cta = g_force_copy_timeout.load();
   // every sequence's last W-1 inputs (its tail values when it is shorter)
   e = launch_conv_tails(a, io, false, st);
   if (e != cudaSuccess) return cuda_fail(e, "conv tails launch");
@@ -379,6 +384,9 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
   a.partial = at<float>(workspace, l.conv_part);
   a.T = total_tokens; a.D = D; a.W = W; a.apply_silu = apply_silu ? 1 : 0;
   a.cu = cu_seqlens; a.num_seqs = num_seqs;
+  a.status = at<int>(workspace, 0);
+  a.wait_ns = g_wait_ns.load();
+  a.force_timeout_cta = g_force_copy_timeout.load();
   if (W > 1) { a.x_init = x_init; a.dx_last = dx_last; a.dx_init = dx_init; }
   if (total_tokens > 0 && (a.x_init || a.dx_last)) {
     e = launch_sequence_index(cu_seqlens, num_seqs, total_tokens, at<int32_t>(workspace, l.seq), st);

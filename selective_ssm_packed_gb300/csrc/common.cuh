@@ -316,6 +316,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// After a copy wait has been reported as timed out, a CTA waits this much
+// longer for the copy before it leaves, so that no copy it requested is still
+// writing into its shared memory once another CTA may own that memory.
+constexpr unsigned long long kCopyDrainNs = 1ull << 30;
+
 // Wait for phase `parity` of the barrier; gives up after limit_ns (returns false).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;

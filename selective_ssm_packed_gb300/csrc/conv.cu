@@ -131,7 +131,15 @@ __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_cons
     for (int k = 0; k < W; ++k) w[k][v] = sm.w[k][c + v];
     bb[v] = sm.b[c + v];
   }
-  if (!mbar_wait(&sm.bar, 0, 1000000000ull)) return;  // copies lost: leave the tile (never expected)
+  // the tile copy: a wait that runs out (or the test knob's CTA) is reported in
+  // the status word; the CTA then gives the copy one more, long limit to land
+  // before it leaves, so that nothing it requested still writes into its
+  // shared memory afterwards
+  if (!__syncthreads_and(mbar_wait(&sm.bar, 0, a.wait_ns) && (long long)blockIdx.x != a.force_timeout_cta)) {
+    if (tid == 0 && a.status) atomicOr(a.status, kStatusTmaTimeout);
+    mbar_wait(&sm.bar, 0, kCopyDrainNs);
+    return;
+  }
   if (!active) return;
   T* __restrict__ u = static_cast<T*>(a.out);
   float xw[W][4];  // xw[k] = x[t - (W-1) + k]
@@ -212,7 +220,15 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
     for (int k = 0; k < W; ++k) w[k][h] = make_float2(sm.w[k][c + 2 * h], sm.w[k][c + 2 * h + 1]);
     bb[h] = make_float2(sm.b[c + 2 * h], sm.b[c + 2 * h + 1]);
   }
-  const bool got = mbar_wait(&sm.bar, 0, 1000000000ull);
+  // the tile copies: a wait that runs out (or the test knob's CTA) is reported
+  // in the status word, and the CTA gives the copies one more, long limit to
+  // land; it still reaches the barriers below, with zero contributions
+  const bool got =
+      __syncthreads_and(mbar_wait(&sm.bar, 0, a.wait_ns) && (long long)blockIdx.x != a.force_timeout_cta);
+  if (!got) {
+    if (tid == 0 && a.status) atomicOr(a.status, kStatusTmaTimeout);
+    mbar_wait(&sm.bar, 0, kCopyDrainNs);
+  }
   float2 dw[W][2], db[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {

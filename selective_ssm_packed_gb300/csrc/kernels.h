@@ -51,6 +51,9 @@ struct ConvArgs {
   int apply_silu;
   int num_seqs;
   const int32_t* cu;
+  int* status;                      // device status word (workspace header)
+  unsigned long long wait_ns;       // limit of the tile-copy wait
+  long long force_timeout_cta;      // test knob: this CTA reports its copy wait as timed out
 };
 // Number of token-rows of CTAs the backward kernel uses (partial buffer rows).
 int64_t conv_bwd_partial_rows(int64_t T);

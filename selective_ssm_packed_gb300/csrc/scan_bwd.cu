@@ -267,7 +267,7 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // second limit to complete (so that no copy is left writing into this
     // CTA's shared memory once it has exited), and stop
     if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
-    mbar_wait(&sm.bar, it & 1u, a.wait_ns);
+    mbar_wait(&sm.bar, it & 1u, kCopyDrainNs);
     break;
   }
 
@@ -859,7 +859,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
     // see scan_bwd_kernel: report, give the copies a second limit, stop
     if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
-    mbar_wait(&sm.bar, it & 1u, a.wait_ns);
+    mbar_wait(&sm.bar, it & 1u, kCopyDrainNs);
     break;
   }
 

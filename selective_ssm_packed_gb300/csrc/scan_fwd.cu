@@ -131,7 +131,10 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   for (uint32_t it = 0;; ++it) {
   // the barrier's completion also publishes thread 0's write of sm.ticket
   if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
+    // report, and give the copies one more, long limit to land before the CTA
+    // leaves (nothing it requested may still write into its shared memory)
     if (tid == 0) atomicOr(a.status, kStatusTmaTimeout);
+    mbar_wait(&sm.bar, it & 1u, kCopyDrainNs);
     break;
   }
   const int tk = sm.ticket;

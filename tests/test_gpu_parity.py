@@ -527,6 +527,37 @@ def test_lookback_wait_timeout_is_reported_not_hung(N):
     assert binding.read_status(ws) == 0
 
 
+def test_conv_copy_timeout_is_reported_in_the_call_status():
+    """The conv calls report a tile-copy wait that runs out in their status
+    word.  The test knob makes one CTA treat its wait as timed out once its
+    copy has landed (no copy fails); the call completes, vssm_read_status
+    returns VSSM_ERR_LOOKBACK_TIMEOUT, and the next call is clean and right."""
+    cu_np, T, r = rand_case([300, 1, 40, 700], 64, 4, "f32", seed=45)
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    x, w, b = f32(r["x"]), f32(r["conv_w"]), f32(r["conv_b"])
+    D, W = 64, 4
+    wsf = torch.empty(binding.conv1d_fwd_workspace_size(T, D, W), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(binding.conv1d_bwd_workspace_size(T, D, W), dtype=torch.uint8, device="cuda")
+    try:
+        binding.debug_set(binding.VSSM_DBG_FORCE_COPY_TIMEOUT, 1)
+        u = vs.varlen_conv1d_fwd(x, w, b, cu, pos, workspace=wsf)
+        assert binding.read_status(wsf) == -17
+        vs.varlen_conv1d_bwd(x, w, b, u, cu, pos, workspace=wsb)
+        assert binding.read_status(wsb) == -17
+    finally:
+        binding.debug_set(binding.VSSM_DBG_FORCE_COPY_TIMEOUT, -1)
+    u = vs.varlen_conv1d_fwd(x, w, b, cu, pos, workspace=wsf)
+    assert binding.read_status(wsf) == 0
+    du = f32(r["dout"])
+    dx, dw, db = vs.varlen_conv1d_bwd(x, w, b, du, cu, pos, workspace=wsb)
+    assert binding.read_status(wsb) == 0
+    assert_close("u", u, oracle.conv1d_fwd(r["x"], r["conv_w"], r["conv_b"], cu_np), TOL["f32"])
+    ref = oracle.conv1d_bwd(r["x"], r["conv_w"], r["conv_b"], r["dout"], cu_np)
+    for name, got, want in zip(("dx", "dweight", "dbias"), (dx, dw, db), ref):
+        assert_close(name, got, want, TOL["f32"])
+
+
 def test_lookback_walk_past_aggregates_is_bitwise_identical():
     """One work item sleeps before it stores its inclusive state, so the items
     after it on the same chain publish their aggregates and later items walk
