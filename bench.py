@@ -290,13 +290,14 @@ def probe_alu(n_sm):
 
 
 def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=None, backward=True,
-              flush=None):
+              flush=None, fused=False):
     """Seconds per step for the packed layout cu_np, on seeded device-generated
     inputs with the workloads' value distributions (timing only).  A step is
     pos, conv fwd, scan fwd and, with backward, scan bwd and conv bwd.  With
     `flush` (a device tensor larger than the L2), the tensor is overwritten
     before every step, outside the timed events, and the median of the
-    per-step times is returned; otherwise steps run back to back."""
+    per-step times is returned; otherwise steps run back to back.  With
+    `fused`, the conv1d and scan forwards run as one call (u computed on chip)."""
     import numpy as np
     tdt = dtype or torch.bfloat16
     T = int(cu_np[-1])
@@ -334,12 +335,20 @@ def time_case(torch, vs, binding, device, cu_np, D, N, Wc, steps, seed, dtype=No
 
     def step():
         vs.varlen_position_indices(cu, T, out=pos)
-        vs.varlen_conv1d_fwd(x, cw, cb, cu, pos, out=u, workspace=ws["cf"])
-        if not backward:  # a forward pass: no pre-gate output or saved states needed
-            vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, workspace=ws["sf"])
-            return
-        vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, chunk_states=states,
-                                     workspace=ws["sf"], y=ypre)
+        if fused:
+            # the backward needs u, y and the saved states; a forward pass does not
+            vs.varlen_conv1d_scan_fwd(x, cw, cb, dr, A, B, C, Dsk, z, dtb, cu, pos, u=u if backward else None,
+                                      out=out, chunk_states=states if backward else None, workspace=ws["sf"],
+                                      y=ypre if backward else None)
+            if not backward:
+                return
+        else:
+            vs.varlen_conv1d_fwd(x, cw, cb, cu, pos, out=u, workspace=ws["cf"])
+            if not backward:  # a forward pass: no pre-gate output or saved states needed
+                vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, workspace=ws["sf"])
+                return
+            vs.varlen_selective_scan_fwd(u, dr, A, B, C, Dsk, z, dtb, cu, pos, out=out, chunk_states=states,
+                                         workspace=ws["sf"], y=ypre)
         vs.varlen_selective_scan_bwd(u, dr, A, B, C, Dsk, z, dtb, dout, cu, states, pos, grads=grads,
                                      workspace=ws["sb"], y=ypre)
         vs.varlen_conv1d_bwd(x, cw, cb, grads["du"], cu, pos, dx=dx, dweight=dw, dbias=db, workspace=ws["cb"])
@@ -418,6 +427,18 @@ def comparators(args, torch, vs, binding, device, w, step_sec):
         "config": f"long-tail packs ({len(lengths)} sequences, {T_real} tokens), D={Dc}, N=16, bf16, "
                   f"buckets {list(wls.BUCKETS)}; same kernels, fwd+bwd; padded rows in "
                   f"{len(groups)} groups of at most {T_real} tokens, times summed"}
+    # the fused conv1d + scan forward against the two calls, on the bench
+    # workload's layout: the forward alone and the whole step
+    fz = {}
+    for key, bwd in (("forward", False), ("step", True)):
+        two = time_case(torch, vs, binding, device, w["cu_seqlens"], wl.D, wl.N, wl.W, args.comparator_steps,
+                        seed=15, backward=bwd)
+        one = time_case(torch, vs, binding, device, w["cu_seqlens"], wl.D, wl.N, wl.W, args.comparator_steps,
+                        seed=15, backward=bwd, fused=True)
+        fz[key] = {"two_calls_ms": two * 1e3, "fused_ms": one * 1e3, "speedup": two / one}
+    fz["config"] = (f"{args.workload} layout, D={wl.D}, N={wl.N}; conv1d fwd + scan fwd as two calls vs "
+                    "varlen_conv1d_scan_fwd (u computed on chip; written out only for the backward)")
+    res["fused_conv_scan_fwd"] = fz
     # the packer (host side): arrival-order packing against local greedy on the
     # bench workload's length mix, as the article compares them
     rng = np.random.default_rng(14)

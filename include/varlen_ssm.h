@@ -289,6 +289,34 @@ int varlen_pack_sequences(const int32_t* lengths, int32_t num_seqs, int32_t pack
                           int32_t window, int32_t* order, int32_t* pack_offsets, int32_t* num_packs,
                           double* padding_rate);
 
+/*
+ * varlen_conv1d_scan_fwd: varlen_conv1d_fwd followed by
+ * varlen_selective_scan_fwd in one call, with u computed on chip.  It is the
+ * fusion idea of the memory-efficient path in "从 1 卡到 N 卡 Mamba 分布式训练"
+ * (gsyq.cn), section 显存开关, applied to the two sequence-wise operators of
+ * the article's section "Mamba block 中的步骤": the scan kernel reads the conv
+ * input x (with the W-1 rows before each chunk) instead of u, evaluates
+ * u = SiLU(bias + sum_k weight[d][W-1-k] x[t-k] [pos[t] >= k]) (no SiLU when
+ * apply_silu is 0) in the conv call's arithmetic and order, rounds it to the
+ * I/O type as that call's store does, and scans it.  The results equal the
+ * two calls', bit for bit.
+ *   x, conv_weight (D, W), conv_bias (nullable), W (1..4), apply_silu: as
+ *       varlen_conv1d_fwd (conv_weight and conv_bias 16-byte aligned); the
+ *       calls with conv tails (x_init / x_last) have no fused form.
+ *   u:  nullable (T, D) output receiving the conv output, which the backward
+ *       call needs; NULL when only the forward is wanted.
+ *   every other argument, the workspace (varlen_selective_scan_fwd_workspace_size)
+ *   and the status word are those of varlen_selective_scan_fwd.
+ */
+int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float* conv_bias, int32_t W,
+                           int32_t apply_silu, const void* delta_raw, const float* A, const void* B,
+                           const void* C, const float* Dskip, const void* z, const float* dt_bias,
+                           int32_t delta_softplus, float gate_floor, int32_t a_log,
+                           const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+                           int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* u, void* out,
+                           void* y, float* chunk_states, const float* initial_states, float* final_states,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------ status, errors, knobs
  * vssm_read_status: synchronises `stream`, reads the status word the last call
  * using `workspace` left there, and stores VSSM_OK or a VSSM_ERR_* code in

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     read_status,
     varlen_conv1d_bwd,
     varlen_conv1d_fwd,
+    varlen_conv1d_scan_fwd,
     varlen_position_indices,
     varlen_selective_scan_bwd,
     varlen_selective_scan_fwd,

@@ -44,6 +44,10 @@ SIGNATURES = {
                                                  ctypes.c_float, _i32,
                                                  _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
                                                  _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "varlen_conv1d_scan_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              _i32, ctypes.c_float, _i32,
+                                              _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_int,
+                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "varlen_selective_scan_bwd_workspace_size": (_sz, [_i64, _i32, _i32]),
     "varlen_selective_scan_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                  ctypes.c_float, _i32, _vp,
@@ -286,6 +290,53 @@ def varlen_selective_scan_fwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqle
         _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_selective_scan_fwd")
     res = (out, chunk_states) + ((y,) if want_y else ()) + ((final_states,) if want_final else ())
     return res
+
+
+def varlen_conv1d_scan_fwd(x, conv_weight, conv_bias, delta_raw, A, B, C, Dskip, z, dt_bias, cu_seqlens,
+                           position_indices=None, apply_silu=True, delta_softplus=True, u=True, out=None,
+                           chunk_states=True, workspace=None, stream=None, y=None, gate_floor=0.0,
+                           a_log=False, initial_states=None, final_states=None):
+    """The conv1d forward and the selective-scan forward in one call (u computed
+    on chip; results equal the two calls' bit for bit).  Returns (u, out,
+    chunk_states) plus y and final_states when asked for, as
+    varlen_selective_scan_fwd; u: True allocates the conv output (the backward
+    needs it), None/False skips writing it, a tensor is filled."""
+    T, D = x.shape
+    N = A.shape[1]
+    W = conv_weight.shape[1]
+    out = torch.empty_like(x) if out is None else out
+    if u is True:
+        u = torch.empty_like(x)
+    elif u is False:
+        u = None
+    want_y = y is not None and y is not False
+    if y is True:
+        y = torch.empty_like(x)
+    elif y is False:
+        y = None
+    S = cu_seqlens.numel() - 1
+    want_final = final_states is not None and final_states is not False
+    if final_states is True:
+        final_states = torch.empty((S, D, N), dtype=torch.float32, device=x.device)
+    elif final_states is False:
+        final_states = None
+    if chunk_states is True:
+        chunk_states = torch.empty(chunk_states_shape(T, D, N), dtype=torch.float32, device=x.device)
+    elif chunk_states is False:
+        chunk_states = None
+    ws = _ws(workspace, scan_fwd_workspace_size(T, D, N), x.device)
+    dt = x.dtype
+    _check(lib().varlen_conv1d_scan_fwd(
+        _ptr(x, "x"), _ptr(conv_weight, "conv_weight", torch.float32), _ptr(conv_bias, "conv_bias", torch.float32),
+        W, int(bool(apply_silu)), _ptr(delta_raw, "delta_raw", dt), _ptr(A, "A", torch.float32),
+        _ptr(B, "B", dt), _ptr(C, "C", dt), _ptr(Dskip, "Dskip", torch.float32), _ptr(z, "z", dt),
+        _ptr(dt_bias, "dt_bias", torch.float32), int(bool(delta_softplus)), float(gate_floor), int(bool(a_log)),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(position_indices, "position_indices", torch.int32),
+        cu_seqlens.numel() - 1, T, D, N, _dt(x), _ptr(u, "u", dt), _ptr(out, "out", dt), _ptr(y, "y", dt),
+        _ptr(chunk_states, "chunk_states", torch.float32),
+        _ptr(initial_states, "initial_states", torch.float32), _ptr(final_states, "final_states", torch.float32),
+        _ptr(ws, "workspace"), ws.numel(), _stream(stream)), "varlen_conv1d_scan_fwd")
+    return (u, out, chunk_states) + ((y,) if want_y else ()) + ((final_states,) if want_final else ())
 
 
 def varlen_selective_scan_bwd(u, delta_raw, A, B, C, Dskip, z, dt_bias, dout, cu_seqlens,

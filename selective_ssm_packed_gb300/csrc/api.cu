@@ -523,6 +523,82 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_fwd launch");
 }
 
+int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float* conv_bias, int32_t W,
+                           int32_t apply_silu, const void* delta_raw, const float* A, const void* B,
+                           const void* C, const float* Dskip, const void* z, const float* dt_bias,
+                           int32_t delta_softplus, float gate_floor, int32_t a_log,
+                           const int32_t* cu_seqlens, const int32_t* position_indices, int32_t num_seqs,
+                           int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* u, void* out,
+                           void* y, float* chunk_states, const float* initial_states, float* final_states,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  IO io;
+  // x takes u's place in the scan's checks (same shape, dtype and alignment)
+  VSSM_TRY(scan_common(x, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
+                        num_seqs, total_tokens, D, N, dtype, &io));
+  if (W < 1 || W > 4) return fail(VSSM_ERR_UNSUPPORTED, "conv width %d not in 1..4", W);
+  if (!conv_weight) return fail(VSSM_ERR_ARG, "conv_weight is NULL");
+  if (!aligned16(conv_weight)) return fail(VSSM_ERR_ALIGN, "conv_weight is not 16-byte aligned");
+  if (conv_bias && !aligned16(conv_bias)) return fail(VSSM_ERR_ALIGN, "conv_bias is not 16-byte aligned");
+  VSSM_TRY(check_io(out, "out", total_tokens));
+  if (u) VSSM_TRY(check_io(u, "u", total_tokens));
+  if (y) VSSM_TRY(check_io(y, "y", total_tokens));
+  if (chunk_states && !aligned16(chunk_states))
+    return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
+  VSSM_TRY(check_states(initial_states, "initial_states"));
+  VSSM_TRY(check_states(final_states, "final_states"));
+  const int64_t T = total_tokens;
+  const Layout l = scan_layout(T, D, N, kFwdChunk, false);
+  VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, l.clear_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  if (T > 0) e = cudaMemsetAsync(at<char>(workspace, l.incl), 0xff, l.incl_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "filling the look-back states");
+  e = launch_empty_sequence_states(cu_seqlens, num_seqs, (int64_t)D * N, initial_states, final_states, st);
+  if (e != cudaSuccess) return cuda_fail(e, "empty-sequence states launch");
+  if (T == 0) return VSSM_OK;
+  const int32_t* pos = nullptr;
+  VSSM_TRY(resolve_pos(cu_seqlens, position_indices, num_seqs, T, workspace, l, st, &pos));
+  const int32_t* seq = nullptr;
+  if (initial_states || final_states) {
+    e = launch_sequence_index(cu_seqlens, num_seqs, T, at<int32_t>(workspace, l.seq), st);
+    if (e != cudaSuccess) return cuda_fail(e, "sequence index launch");
+    seq = at<int32_t>(workspace, l.seq);
+  }
+  ScanArgs a{};
+  a.u = x; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
+  a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
+  a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
+  a.conv_w = conv_weight; a.conv_b = conv_bias; a.conv_W = W; a.conv_silu = apply_silu ? 1 : 0; a.u_out = u;
+  a.status = at<int>(workspace, 0);
+  a.ticket = at<unsigned>(workspace, 4);
+  a.flags = at<int>(workspace, l.flags);
+  a.agg = at<float>(workspace, l.agg);
+  a.agg_sd = at<float>(workspace, l.agg_sd);
+  a.incl = at<float>(workspace, l.incl);
+  a.T = T; a.D = D; a.N = N;
+  a.n_tiles = (int)cdiv(D, kTile);
+  a.n_chunks = (int)cdiv(T, kFwdChunk);
+  a.delta_softplus = delta_softplus ? 1 : 0;
+  a.gate_floor = gate_floor;
+  a.a_log = a_log ? 1 : 0;
+  a.has_z = z ? 1 : 0;
+  a.has_skip = Dskip ? 1 : 0;
+  a.box_x = D < kTile ? D : kTile;
+  a.box_y = T < kFwdChunk ? (int)T : kFwdChunk;
+  a.drop_ticket = g_drop_ticket.load();
+  a.wait_ns = g_wait_ns.load();
+  a.delay_ticket = -1;  // the delay knob's build does not carry the fused conv
+  a.delay_ns = g_delay_ns.load();
+  CUtensorMap mx, mdr, mz;
+  // x rows t0 - 3 .. t0 + 127 of every chunk: three rows above the u box
+  VSSM_TRY(make_map(&mx, x, io, T, D, a.box_x, a.box_y + 3));
+  VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
+  VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
+  e = launch_scan_fwd(a, io, mx, mdr, mz, st);
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_scan_fwd launch");
+}
+
 int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
                               const void* B, const void* C, const float* Dskip, const void* z,
                               const float* dt_bias, int32_t delta_softplus, float gate_floor,

@@ -130,6 +130,13 @@ struct ScanArgs {
   unsigned long long wait_ns;
   long long delay_ticket;       // test knob: this item sleeps delay_ns before storing its inclusive state
   unsigned long long delay_ns;
+  // fused conv1d + scan forward (conv_w non-null): u = conv(x) computed in the
+  // kernel from the x the u map then covers; u_out (nullable) receives it
+  const float* conv_w;        // (D, conv_W)
+  const float* conv_b;        // (D) or null
+  int conv_W;
+  int conv_silu;
+  void* u_out;
 };
 
 cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,

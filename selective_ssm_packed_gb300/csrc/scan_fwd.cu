@@ -43,9 +43,17 @@ constexpr int kS = 8;           // sub-chunks (warps)
 constexpr int kK = kL / kS;     // 16 tokens per thread
 constexpr int kThreads = kS * 32;
 
-template <typename T, int N>
+constexpr int kHalo = 3;        // x rows before the chunk a fused conv of width <= 4 reads
+constexpr int kMaxW = 4;        // widest fused conv
+
+template <typename T, int N, bool kConv>
 struct FwdSmem {
   alignas(128) T u[kL * kTile];
+  // fused conv1d: x rows t0 - 3 .. t0 + 127 (by one tensor copy; rows before
+  // the first token come back zero), the tile's weights (D, W) and bias
+  alignas(128) T x[kConv ? (kL + kHalo) * kTile : 8];
+  alignas(16) float cw[kConv ? kTile * kMaxW : 4];
+  alignas(16) float cb[kConv ? kTile : 4];
   alignas(128) T dr[kL * kTile];
   alignas(128) T z[kL * kTile];
   alignas(128) T B[kL * N];
@@ -67,12 +75,18 @@ struct FwdSmem {
 };
 
 // kStates: the call passes sequence states (initial and/or final); without
-// them the kernel carries no code for them.
-template <typename T, int N, bool kStates, bool kKnob>
+// them the kernel carries no code for them.  kConv: the call passes the conv1d
+// input x instead of u (tm_u maps x), and the kernel computes
+// u = SiLU(bias + sum_k w[W-1-k] x[t-k] [pos[t] >= k]) itself in pass 1, with
+// the conv kernel's arithmetic in the conv kernel's order, rounding u to the
+// I/O type as that kernel's store does (so the results equal the two calls'
+// bit for bit); u goes to a.u_out when the call asks for it (the backward
+// needs it).
+template <typename T, int N, bool kStates, bool kKnob, bool kConv>
 __global__ void __launch_bounds__(kThreads, 2)
 scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dr,
                 const __grid_constant__ CUtensorMap tm_z, const ScanArgs a) {
-  using SM = FwdSmem<T, N>;
+  using SM = FwdSmem<T, N, kConv>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, s = tid >> 5;
@@ -97,9 +111,18 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (a.has_z ? 3u : 2u) + 2u * bc + nval * N * 4u + rows4 * 4u +
-                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
-    tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+    // the fused conv's x box has kHalo more rows, and its weights and bias come along
+    const uint32_t ubox = kConv ? (uint32_t)a.box_x * (uint32_t)(a.box_y + kHalo) * sizeof(T) : box;
+    const uint32_t conv_bytes = kConv ? nval * (uint32_t)a.conv_W * 4u + (a.conv_b ? nval * 4u : 0u) : 0u;
+    mbar_arrive_expect_tx(&sm.bar, ubox + box * (a.has_z ? 2u : 1u) + 2u * bc + nval * N * 4u + rows4 * 4u +
+                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u) + conv_bytes);
+    if constexpr (kConv) {
+      tma_load_2d(sm.x, &tm_u, dd0, (int)tt0 - kHalo, &sm.bar);
+      bulk_load_1d(sm.cw, a.conv_w + (int64_t)dd0 * a.conv_W, nval * (uint32_t)a.conv_W * 4u, &sm.bar);
+      if (a.conv_b) bulk_load_1d(sm.cb, a.conv_b + dd0, nval * 4u, &sm.bar);
+    } else {
+      tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+    }
     tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
     if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
     bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
@@ -160,6 +183,26 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // position index of token t < rows of the chunk (the last chunk's ragged
   // tail, past the last whole group of 4, is read from global memory)
   auto pos_at = [&](int t) { return t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t); };
+  // fused conv1d: tap k (k tokens back) of this lane's channel; zero past W
+  float tapw[kMaxW], cbias = 0.0f;
+  if constexpr (kConv) {
+#pragma unroll
+    for (int k = 0; k < kMaxW; ++k) tapw[k] = (valid && k < a.conv_W) ? sm.cw[lane * a.conv_W + a.conv_W - 1 - k] : 0.0f;
+    cbias = (valid && a.conv_b) ? sm.cb[lane] : 0.0f;
+  }
+  // u of chunk token t (< rows) for this lane's channel, computed from the x
+  // tile: kept in the u tile for both passes and stored for the caller when asked
+  auto conv_u = [&](int t) {
+    const T* xr = sm.x + (t + kHalo) * bx + lane;
+    const int p = pos_at(t);
+    float pre = fmaf(tapw[0], to_f(xr[0]), cbias);
+#pragma unroll
+    for (int k = 1; k < kMaxW; ++k)
+      if (k < a.conv_W && p >= k) pre = fmaf(tapw[k], to_f(xr[-k * bx]), pre);
+    const T ot = from_f<T>(a.conv_silu ? siluf(pre) : pre);
+    sm.u[t * bx + lane] = ot;
+    if (a.u_out && valid) static_cast<T*>(a.u_out)[(t0 + t) * a.D + d] = ot;
+  };
   // the state a sequence starting at token t (of the chunk) starts from: its
   // row of the initial states, or zero
   auto start_state = [&](float2 (&hs)[N / 2], int t) {
@@ -213,6 +256,14 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   } else {
 #pragma unroll
     for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
+  }
+
+  // fused conv1d: this thread's 16 u values first, in a loop of independent
+  // iterations (kept out of the walk's dependency chain), into the u tile
+  if constexpr (kConv) {
+#pragma unroll 4
+    for (int k = 0; k < kK; ++k)
+      if (tb + k < rows) conv_u(tb + k);
   }
 
   // ---- steps 2-3: delta for my tokens (kept for pass 2) and pass 1, the
@@ -536,24 +587,27 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }  // persistent loop
 }
 
-template <typename T, int N, bool kStates, bool kKnob = false>
+template <typename T, int N, bool kStates, bool kKnob = false, bool kConv = false>
 cudaError_t launch_k(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, cudaStream_t st) {
-  const size_t smem = sizeof(FwdSmem<T, N>);
-  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<T, N, kStates, kKnob>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = scan_fwd_kernel<T, N, kStates, kKnob, kConv>;
+  const size_t smem = sizeof(FwdSmem<T, N, kConv>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.n_chunks * a.n_tiles;
   int grid = 0;
-  e = persistent_grid(scan_fwd_kernel<T, N, kStates, kKnob>, kThreads, smem, items, &grid);
+  e = persistent_grid(kern, kThreads, smem, items, &grid);
   if (e != cudaSuccess) return e;
-  scan_fwd_kernel<T, N, kStates, kKnob><<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
+  kern<<<grid, kThreads, smem, st>>>(tm_u, tm_dr, tm_z, a);
   return cudaGetLastError();
 }
 
 template <typename T, int N>
 cudaError_t launch_n(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorMap& tm_dr,
                      const CUtensorMap& tm_z, cudaStream_t st) {
+  if (a.conv_w)  // the fused conv1d + scan forward
+    return a.seq ? launch_k<T, N, true, false, true>(a, tm_u, tm_dr, tm_z, st)
+                 : launch_k<T, N, false, false, true>(a, tm_u, tm_dr, tm_z, st);
   if constexpr (sizeof(T) == 4 && N == 16) {  // the delay knob's instantiation
     if (a.delay_ticket >= 0 && !a.seq) return launch_k<T, N, false, true>(a, tm_u, tm_dr, tm_z, st);
   }

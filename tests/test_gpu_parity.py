@@ -265,6 +265,45 @@ def test_gate_floor_and_a_log_variants(N, dtype):
         assert_close(k, g[k], ref[k], tol)
 
 
+@pytest.mark.parametrize("lengths,D,N,W,dtype,silu,bias", [
+    ([1, 1, 2, 3, 700, 1, 40, 129, 5], 40, 4, 4, "f32", True, True),
+    ([129, 1, 1, 1, 640, 77], 104, 16, 4, "bf16", True, True),
+    ([300, 0, 1, 257, 33, 2], 72, 8, 2, "f32", True, False),
+    ([5, 90, 1, 200], 64, 16, 1, "f32", False, True),
+    ([700, 3, 1, 290, 33, 1000], 256, 16, 3, "bf16", True, True),
+])
+def test_fused_conv_scan_forward_equals_the_two_calls(lengths, D, N, W, dtype, silu, bias):
+    """varlen_conv1d_scan_fwd computes u on chip in the conv call's arithmetic
+    and order, rounded as its store rounds: u, out, y, the saved states and the
+    final states equal those of conv1d_fwd followed by selective_scan_fwd bit
+    for bit, and match the oracle's conv1d -> selective scan."""
+    cu_np, T, r = rand_case(lengths, D, N, dtype, seed=sum(lengths) + 3 * W, W=W)
+    S = len(lengths)
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    x = dev(r["x"], dtype)
+    cw, cb = f32(r["conv_w"]), (f32(r["conv_b"]) if bias else None)
+    h0 = f32(np.random.default_rng(7).standard_normal((S, D, N)))
+    sargs = dict(delta_raw=dev(r["delta_raw"], dtype), A=f32(r["A"]), B=dev(r["B"], dtype),
+                 C=dev(r["C"], dtype), Dskip=f32(r["Dskip"]), z=dev(r["z"], dtype), dt_bias=f32(r["dt_bias"]))
+    u_ref = vs.varlen_conv1d_fwd(x, cw, cb, cu, pos, apply_silu=silu)
+    ref = vs.varlen_selective_scan_fwd(u_ref, **sargs, cu_seqlens=cu, position_indices=pos, y=True,
+                                       initial_states=h0, final_states=True)
+    got = vs.varlen_conv1d_scan_fwd(x, cw, cb, **sargs, cu_seqlens=cu, position_indices=pos, apply_silu=silu,
+                                    y=True, initial_states=h0, final_states=True)
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], u_ref), "u"
+    for name, g, e in zip(("out", "chunk_states", "y", "final_states"), got[1:], ref):
+        assert torch.equal(g, e), name
+    # and against the oracle: conv1d, the u the device holds, selective scan
+    u_o = oracle.conv1d_fwd(r["x"], r["conv_w"], r["conv_b"] if bias else np.zeros(D, np.float32), cu_np,
+                            apply_silu=silu)
+    assert_close("u", got[0], u_o, TOL[dtype])
+    out_o = oracle.scan_fwd(host(got[0]), r["delta_raw"], r["A"], r["B"], r["C"], r["Dskip"], r["z"],
+                            r["dt_bias"], cu_np, h_init=host(h0))
+    assert_close("out", got[1], out_o, TOL[dtype])
+
+
 @pytest.mark.parametrize("D,N,dtype", [(72, 8, "f32"), (104, 16, "bf16")])
 def test_sequence_states_fwd_bwd(D, N, dtype):
     """Per-sequence initial states in, final states out, and their gradients
