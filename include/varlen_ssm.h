@@ -77,7 +77,9 @@ typedef enum { VSSM_F32 = 0, VSSM_BF16 = 1 } vssm_dtype;
 #define VSSM_ERR_CUDA (-5)             /* a CUDA runtime / driver call failed */
 #define VSSM_ERR_UNSUPPORTED (-6)      /* N or W outside the supported set */
 #define VSSM_ERR_BAD_CU_SEQLENS (-16)  /* cu_seqlens[0] != 0, decreasing, or cu[S] != T */
-#define VSSM_ERR_LOOKBACK_TIMEOUT (-17)/* a cross-chunk wait gave up; results invalid */
+#define VSSM_ERR_LOOKBACK_TIMEOUT (-17)/* a cross-chunk or tile-copy wait gave up; results invalid */
+#define VSSM_ERR_NONFINITE (-18)        /* an output holds a NaN / inf (VSSM_DBG_CHECK_FINITE on) */
+#define VSSM_ERR_DEVICE_CHECK (-19)     /* a device index check failed (VSSM_CHECKS=1 build only) */
 
 /* Tokens per saved scan-state chunk: the forward scan can save the state at
  * every multiple of this many tokens for the backward scan. */
@@ -325,6 +327,14 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
 int vssm_read_status(const void* workspace, void* stream, int* status);
 const char* vssm_strerror(int code);
 const char* vssm_last_error(void);      /* thread-local; "" if none */
+/* 1 when this library is the checked build (compiled with VSSM_CHECKS=1):
+ * its kernels check the sequence-state rows they index by a token's sequence
+ * (rows a malformed cu_seqlens could push past num_seqs) and skip a failing
+ * access, ORing a bit into the status word instead (vssm_read_status then
+ * returns VSSM_ERR_DEVICE_CHECK; nothing traps), and calls given position
+ * indices check them against cu_seqlens (VSSM_ERR_BAD_CU_SEQLENS).  0 in the
+ * ordinary build, where neither check runs. */
+int vssm_checks_build(void);
 
 /* Test knobs (process-wide).  VSSM_DBG_DROP_FLAG: the scan work item with this
  * ticket never publishes its look-back flag (-1 = off), so the waits behind it
@@ -347,6 +357,14 @@ const char* vssm_last_error(void);      /* thread-local; "" if none */
 #define VSSM_DBG_DELAY_ITEM 3
 #define VSSM_DBG_DELAY_NS 4
 #define VSSM_DBG_FORCE_COPY_TIMEOUT 5
+/* VSSM_DBG_CHECK_FINITE: 1 makes every conv / scan call check its outputs
+ * after its kernels and OR a bit into its status word when any output holds a
+ * NaN or an infinity (vssm_read_status then returns VSSM_ERR_NONFINITE); 0
+ * (the default) skips the check.  It makes a run whose values have gone bad
+ * fail loudly: the aimodeling.com page on near-zero embedding rows stalling
+ * the training of gated models describes how such a failure otherwise stays
+ * silent until the loss shows it. */
+#define VSSM_DBG_CHECK_FINITE 6
 int vssm_debug_set(int knob, int64_t value);
 
 #ifdef __cplusplus

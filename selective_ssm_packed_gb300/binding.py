@@ -21,10 +21,11 @@ from . import build as _build
 VSSM_F32, VSSM_BF16 = 0, 1
 VSSM_STATE_CHUNK = 32
 VSSM_DBG_DROP_FLAG, VSSM_DBG_WAIT_NS, VSSM_DBG_DELAY_ITEM, VSSM_DBG_DELAY_NS = 1, 2, 3, 4
-VSSM_DBG_FORCE_COPY_TIMEOUT = 5
+VSSM_DBG_FORCE_COPY_TIMEOUT, VSSM_DBG_CHECK_FINITE = 5, 6
 ERR = {0: "VSSM_OK", -1: "VSSM_ERR_ARG", -2: "VSSM_ERR_DTYPE", -3: "VSSM_ERR_ALIGN",
        -4: "VSSM_ERR_WORKSPACE", -5: "VSSM_ERR_CUDA", -6: "VSSM_ERR_UNSUPPORTED",
-       -16: "VSSM_ERR_BAD_CU_SEQLENS", -17: "VSSM_ERR_LOOKBACK_TIMEOUT"}
+       -16: "VSSM_ERR_BAD_CU_SEQLENS", -17: "VSSM_ERR_LOOKBACK_TIMEOUT", -18: "VSSM_ERR_NONFINITE",
+       -19: "VSSM_ERR_DEVICE_CHECK"}
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
@@ -63,6 +64,7 @@ SIGNATURES = {
     "vssm_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "vssm_last_error": (ctypes.c_char_p, []),
+    "vssm_checks_build": (ctypes.c_int, []),
     "vssm_debug_set": (ctypes.c_int, [ctypes.c_int, _i64]),
 }
 
@@ -76,7 +78,9 @@ class VssmError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The library this process loads: the checked build when VSSM_CHECKS=1
+    is set in the environment, else the ordinary one."""
+    return _build.lib_path()
 
 
 def lib():

@@ -4,6 +4,13 @@ Each .cu file compiles in parallel to an object in ``_build/``; the objects
 link into ``_build/libvarlen_ssm.so`` (CUDA runtime linked statically).  A
 rebuild happens only when a source or header is newer than the library.
 Set VSSM_PTXAS_VERBOSE=1 to print register / spill / shared-memory usage.
+
+``build(checks=True)`` (or VSSM_CHECKS=1 in the environment) builds the
+checked variant instead, ``_build_checks/libvarlen_ssm_checks.so``: the same
+sources with -DVSSM_CHECKS=1, whose kernels verify the indices that input
+data can push out of range and report a failure in the call's status word
+(VSSM_ERR_DEVICE_CHECK) instead of making the access; the calls also verify
+caller-supplied position indices against cu_seqlens.
 """
 from __future__ import annotations
 
@@ -19,6 +26,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libvarlen_ssm.so")
+CHECKS_BUILD_DIR = os.path.join(HERE, "_build_checks")
+CHECKS_LIB_PATH = os.path.join(CHECKS_BUILD_DIR, "libvarlen_ssm_checks.so")
 
 SOURCES = ["api.cu", "misc.cu", "conv.cu", "scan_fwd.cu", "scan_bwd.cu", "noalloc.cu", "packer.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
@@ -35,9 +44,22 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found (set NVCC or CUDA_HOME)")
 
 
-def _flags():
+def checks_requested() -> bool:
+    """Whether the environment asks for the checked build (VSSM_CHECKS=1)."""
+    return os.environ.get("VSSM_CHECKS", "0") not in ("", "0")
+
+
+def lib_path(checks: bool | None = None) -> str:
+    if checks is None:
+        checks = checks_requested()
+    return CHECKS_LIB_PATH if checks else LIB_PATH
+
+
+def _flags(checks: bool = False):
     f = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
+    if checks:
+        f.append("-DVSSM_CHECKS=1")
     if os.environ.get("VSSM_PTXAS_VERBOSE"):
         f += ["-Xptxas", "-v"]
     return f
@@ -50,16 +72,21 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checks: bool | None = None) -> str:
+    """Builds the library (the checked variant when checks is true, or when it
+    is None and VSSM_CHECKS=1 is set) and returns its path."""
+    if checks is None:
+        checks = checks_requested()
+    build_dir, out_path = (CHECKS_BUILD_DIR, CHECKS_LIB_PATH) if checks else (BUILD_DIR, LIB_PATH)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = nvcc_path()
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s, *HEADERS]):
-            jobs.append([nvcc, *_flags(), "-c", s, "-o", o])
+            jobs.append([nvcc, *_flags(checks), "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -72,14 +99,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or jobs or _stale(out_path, objs):
+        tmp = out_path + f".tmp{os.getpid()}"
         r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, out_path)
+    return out_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checks="--checks" in sys.argv or None))

@@ -2,8 +2,10 @@
 // argument validation, workspace layout, TMA descriptors, kernel launches,
 // device status words and error reporting.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -23,6 +25,14 @@ std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 std::atomic<long long> g_delay_ticket{-1};
 std::atomic<unsigned long long> g_delay_ns{200000ull};
 std::atomic<long long> g_force_copy_timeout{-1};
+std::atomic<int> g_check_finite{0};
+
+// An NVTX range over a C-ABI call (host side: the call's enqueue), named
+// after the call, for timelines taken with a profiler.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -178,9 +188,14 @@ int check_ws(const void* ws, size_t have, size_t need) {
 
 // Resolves the position indices a call uses: the caller's array, or one built
 // in the workspace from cu_seqlens (status bits land in the workspace header).
+int check_caller_pos(const int32_t* cu, int32_t S, int64_t T, const int32_t* pos, int32_t* status,
+                     cudaStream_t st);
 int resolve_pos(const int32_t* cu, const int32_t* pos_in, int32_t S, int64_t T, void* ws,
                 const Layout& l, cudaStream_t st, const int32_t** pos_out) {
-  if (pos_in) { *pos_out = pos_in; return VSSM_OK; }
+  if (pos_in) {
+    *pos_out = pos_in;
+    return check_caller_pos(cu, S, T, pos_in, at<int32_t>(ws, 0), st);
+  }
   int32_t* p = at<int32_t>(ws, l.pos);
   cudaError_t e = launch_position_indices(cu, S, T, p, at<int32_t>(ws, 0), st);
   if (e != cudaSuccess) return cuda_fail(e, "position_indices launch");
@@ -188,9 +203,43 @@ int resolve_pos(const int32_t* cu, const int32_t* pos_in, int32_t S, int64_t T, 
   return VSSM_OK;
 }
 
+// With the VSSM_DBG_CHECK_FINITE knob on, ORs kStatusNonFinite into the
+// call's status word when any output holds a NaN or an infinity.
+struct OutSpan {
+  const void* p;
+  int64_t n;
+  bool f32;
+};
+int check_outputs(int32_t* status, cudaStream_t st, std::initializer_list<OutSpan> outs) {
+  if (!g_check_finite.load()) return VSSM_OK;
+  for (const OutSpan& o : outs) {
+    const cudaError_t e = launch_nonfinite_check(o.p, o.n, o.f32, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
+  }
+  return VSSM_OK;
+}
+
+// In the checks build, a caller's position indices are verified against
+// cu_seqlens (kStatusBadCu in the status word when they disagree).
+int check_caller_pos(const int32_t* cu, int32_t S, int64_t T, const int32_t* pos, int32_t* status,
+                     cudaStream_t st) {
+  if (!VSSM_CHECKS || !pos || T <= 0) return VSSM_OK;
+  const cudaError_t e = launch_position_check(cu, S, T, pos, status, st);
+  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "position check launch");
+}
+
 // A (num_seqs, D, N) f32 sequence-state array: nullable, 16-byte aligned.
 int check_states(const float* p, const char* name) {
   if (p && !aligned16(p)) return fail(VSSM_ERR_ALIGN, "%s is not 16-byte aligned", name);
+  return VSSM_OK;
+}
+
+// Sequence states (or conv tails) of a call with tokens need at least one
+// sequence to hold them.
+int check_states_rows(bool any_states, int32_t num_seqs, int64_t T) {
+  if (any_states && T > 0 && num_seqs < 1)
+    return fail(VSSM_ERR_ARG, "sequence states or tails given for %lld tokens but num_seqs = %d", (long long)T,
+                num_seqs);
   return VSSM_OK;
 }
 
@@ -209,6 +258,16 @@ int vssm::record_error(int code, const char* message) {
   return code;
 }
 
+int vssm::check_outputs_finite(int32_t* status, cudaStream_t st, const void* const* ptrs, const int64_t* counts,
+                               const bool* f32, int n) {
+  if (!g_check_finite.load()) return VSSM_OK;
+  for (int i = 0; i < n; ++i) {
+    const cudaError_t e = launch_nonfinite_check(ptrs[i], counts[i], f32[i], status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
+  }
+  return VSSM_OK;
+}
+
 vssm::ScanLayout vssm::scan_workspace_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   const Layout l = scan_layout(T, D, N, chunk, bwd);
   ScanLayout o;
@@ -225,7 +284,8 @@ int vssm::encode_tile_map(CUtensorMap* m, const void* base, IO io, int64_t T, in
 }
 
 vssm::DebugKnobs vssm::debug_knobs() {
-  return DebugKnobs{g_drop_ticket.load(), g_wait_ns.load(), g_delay_ticket.load(), g_delay_ns.load()};
+  return DebugKnobs{g_drop_ticket.load(), g_wait_ns.load(), g_delay_ticket.load(), g_delay_ns.load(),
+                    g_check_finite.load() != 0};
 }
 
 // ============================================================================ C ABI
@@ -234,6 +294,8 @@ extern "C" {
 int vssm_status_code(int32_t w) {
   if (w & kStatusBadCu) return VSSM_ERR_BAD_CU_SEQLENS;
   if (w & (kStatusLookbackTimeout | kStatusTmaTimeout)) return VSSM_ERR_LOOKBACK_TIMEOUT;
+  if (w & kStatusDeviceCheck) return VSSM_ERR_DEVICE_CHECK;
+  if (w & kStatusNonFinite) return VSSM_ERR_NONFINITE;
   return VSSM_OK;
 }
 
@@ -246,13 +308,17 @@ const char* vssm_strerror(int code) {
     case VSSM_ERR_WORKSPACE: return "workspace missing or too small";
     case VSSM_ERR_CUDA: return "CUDA runtime or driver error";
     case VSSM_ERR_UNSUPPORTED: return "unsupported N or conv width";
-    case VSSM_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens (device check)";
+    case VSSM_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens, or position indices that disagree with it (device check)";
     case VSSM_ERR_LOOKBACK_TIMEOUT: return "a device-side wait timed out: look-back or tile copy (device check)";
+    case VSSM_ERR_NONFINITE: return "an output holds a NaN or an infinity (VSSM_DBG_CHECK_FINITE)";
+    case VSSM_ERR_DEVICE_CHECK: return "a device-side index check failed (VSSM_CHECKS build)";
   }
   return "unknown status code";
 }
 
 const char* vssm_last_error(void) { return g_last_error.c_str(); }
+
+int vssm_checks_build(void) { return VSSM_CHECKS ? 1 : 0; }
 
 int vssm_debug_set(int knob, int64_t value) {
   if (knob == VSSM_DBG_DROP_FLAG) { g_drop_ticket.store(value); return VSSM_OK; }
@@ -268,6 +334,11 @@ int vssm_debug_set(int knob, int64_t value) {
     return VSSM_OK;
   }
   if (knob == VSSM_DBG_FORCE_COPY_TIMEOUT) { g_force_copy_timeout.store(value); return VSSM_OK; }
+  if (knob == VSSM_DBG_CHECK_FINITE) {
+    if (value != 0 && value != 1) return fail(VSSM_ERR_ARG, "VSSM_DBG_CHECK_FINITE takes 0 or 1");
+    g_check_finite.store((int)value);
+    return VSSM_OK;
+  }
   return fail(VSSM_ERR_ARG, "unknown debug knob %d", knob);
 }
 
@@ -285,6 +356,7 @@ int vssm_read_status(const void* workspace, void* stream, int* status) {
 // ---------------------------------------------------------------- position indices
 int varlen_position_indices(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                             int32_t* position_indices, int32_t* status, void* stream) {
+  NvtxRange nvtx_("varlen_position_indices");
   VSSM_TRY(check_shape(total_tokens, 1, num_seqs, cu_seqlens));
   if (total_tokens > 0 && !position_indices) return fail(VSSM_ERR_ARG, "position_indices is NULL");
   cudaError_t e = launch_position_indices(cu_seqlens, num_seqs, total_tokens, position_indices,
@@ -321,11 +393,13 @@ int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
                       int64_t total_tokens, int32_t D, int32_t W, int32_t apply_silu,
                       vssm_dtype dtype, void* u, const float* x_init, float* x_last,
                       void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_("varlen_conv1d_fwd");
   IO io;
   VSSM_TRY(conv_common(x, weight, cu_seqlens, num_seqs, total_tokens, D, W, dtype, &io));
   VSSM_TRY(check_io(u, "u", total_tokens));
   VSSM_TRY(check_states(x_init, "x_init"));
   VSSM_TRY(check_states(x_last, "x_last"));
+  VSSM_TRY(check_states_rows(x_init || x_last, num_seqs, total_tokens));
   const Layout l = conv_layout(total_tokens, D, W, false);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -354,7 +428,9 @@ int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
   CUtensorMap mx;
   VSSM_TRY(make_map(&mx, x, io, total_tokens, D, bx, conv_tile_rows(W, false, true)));
   e = launch_conv1d_fwd(a, io, mx, st);
-  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_fwd launch");
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d_fwd launch");
+  const bool f = io == IO::F32;
+  return check_outputs(a.status, st, {{u, total_tokens * D, f}});
 }
 
 int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, const void* du,
@@ -363,6 +439,7 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
                       vssm_dtype dtype, void* dx, float* dweight, float* dbias,
                       const float* x_init, const float* dx_last, float* dx_init,
                       void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_("varlen_conv1d_bwd");
   IO io;
   VSSM_TRY(conv_common(x, weight, cu_seqlens, num_seqs, total_tokens, D, W, dtype, &io));
   VSSM_TRY(check_io(du, "du", total_tokens));
@@ -371,6 +448,7 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
   VSSM_TRY(check_states(x_init, "x_init"));
   VSSM_TRY(check_states(dx_last, "dx_last"));
   VSSM_TRY(check_states(dx_init, "dx_init"));
+  VSSM_TRY(check_states_rows(x_init || dx_last || dx_init, num_seqs, total_tokens));
   const Layout l = conv_layout(total_tokens, D, W, true);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -405,7 +483,9 @@ int varlen_conv1d_bwd(const void* x, const float* weight, const float* bias, con
     VSSM_TRY(make_map(&mdu, du, io, total_tokens, D, bx, conv_tile_rows(W, true, false)));
   }
   e = launch_conv1d_bwd(a, io, mx, mdu, dweight, dbias, st);
-  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_bwd launch");
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d_bwd launch");
+  return check_outputs(a.status, st, {{dx, total_tokens * D, io == IO::F32}, {dweight, (int64_t)D * W, true},
+                                      {dbias, dbias ? (int64_t)D : 0, true}});
 }
 
 // ---------------------------------------------------------------- selective scan
@@ -459,6 +539,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
                               vssm_dtype dtype, void* out, void* y, float* chunk_states,
                               const float* initial_states, float* final_states,
                               void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_("varlen_selective_scan_fwd");
   IO io;
   VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
                         num_seqs, total_tokens, D, N, dtype, &io));
@@ -468,6 +549,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
     return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
   VSSM_TRY(check_states(initial_states, "initial_states"));
   VSSM_TRY(check_states(final_states, "final_states"));
+  VSSM_TRY(check_states_rows(initial_states || final_states, num_seqs, total_tokens));
   const int64_t T = total_tokens;
   const Layout l = scan_layout(T, D, N, kFwdChunk, false);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
@@ -501,7 +583,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   a.agg = at<float>(workspace, l.agg);
   a.agg_sd = at<float>(workspace, l.agg_sd);
   a.incl = at<float>(workspace, l.incl);
-  a.T = T; a.D = D; a.N = N;
+  a.T = T; a.D = D; a.N = N; a.num_seqs = num_seqs;
   a.n_tiles = (int)cdiv(D, kTile);
   a.n_chunks = (int)cdiv(T, kFwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
@@ -520,7 +602,9 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
   VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
   e = launch_scan_fwd(a, io, mu, mdr, mz, st);
-  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_fwd launch");
+  if (e != cudaSuccess) return cuda_fail(e, "selective_scan_fwd launch");
+  return check_outputs(a.status, st, {{out, T * D, io == IO::F32}, {y, y ? T * D : 0, io == IO::F32},
+                                      {final_states, final_states ? (int64_t)num_seqs * D * N : 0, true}});
 }
 
 int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float* conv_bias, int32_t W,
@@ -531,6 +615,7 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
                            int64_t total_tokens, int32_t D, int32_t N, vssm_dtype dtype, void* u, void* out,
                            void* y, float* chunk_states, const float* initial_states, float* final_states,
                            void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_("varlen_conv1d_scan_fwd");
   IO io;
   // x takes u's place in the scan's checks (same shape, dtype and alignment)
   VSSM_TRY(scan_common(x, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
@@ -546,6 +631,7 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
     return fail(VSSM_ERR_ALIGN, "chunk_states is not 16-byte aligned");
   VSSM_TRY(check_states(initial_states, "initial_states"));
   VSSM_TRY(check_states(final_states, "final_states"));
+  VSSM_TRY(check_states_rows(initial_states || final_states, num_seqs, total_tokens));
   const int64_t T = total_tokens;
   const Layout l = scan_layout(T, D, N, kFwdChunk, false);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
@@ -576,7 +662,7 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
   a.agg = at<float>(workspace, l.agg);
   a.agg_sd = at<float>(workspace, l.agg_sd);
   a.incl = at<float>(workspace, l.incl);
-  a.T = T; a.D = D; a.N = N;
+  a.T = T; a.D = D; a.N = N; a.num_seqs = num_seqs;
   a.n_tiles = (int)cdiv(D, kTile);
   a.n_chunks = (int)cdiv(T, kFwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
@@ -596,7 +682,10 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
   VSSM_TRY(make_map(&mdr, delta_raw, io, T, D, a.box_x, a.box_y));
   VSSM_TRY(make_map(&mz, z, io, T, D, a.box_x, a.box_y));
   e = launch_scan_fwd(a, io, mx, mdr, mz, st);
-  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "conv1d_scan_fwd launch");
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d_scan_fwd launch");
+  return check_outputs(a.status, st, {{u, u ? T * D : 0, io == IO::F32}, {out, T * D, io == IO::F32},
+                                      {y, y ? T * D : 0, io == IO::F32},
+                                      {final_states, final_states ? (int64_t)num_seqs * D * N : 0, true}});
 }
 
 int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float* A,
@@ -611,6 +700,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
                               void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
                               float* dDskip, void* dz, float* d_dt_bias,
                               void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_("varlen_selective_scan_bwd");
   IO io;
   VSSM_TRY(scan_common(u, delta_raw, A, B, C, z, Dskip, dt_bias, position_indices, cu_seqlens,
                         num_seqs, total_tokens, D, N, dtype, &io));
@@ -628,6 +718,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   VSSM_TRY(check_states(initial_states, "initial_states"));
   VSSM_TRY(check_states(d_final_states, "d_final_states"));
   VSSM_TRY(check_states(d_initial_states, "d_initial_states"));
+  VSSM_TRY(check_states_rows(initial_states || d_final_states || d_initial_states, num_seqs, total_tokens));
   const Layout l = scan_layout(T, D, N, kBwdChunk, true);
   VSSM_TRY(check_ws(workspace, workspace_bytes, l.total));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -663,7 +754,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.part_dA = at<float>(workspace, l.part_a);
   a.part_dD = at<float>(workspace, l.part_d);
   a.part_dbias = at<float>(workspace, l.part_b);
-  a.T = T; a.D = D; a.N = N;
+  a.T = T; a.D = D; a.N = N; a.num_seqs = num_seqs;
   const int tw = scan_tile(N, true);
   a.n_tiles = (int)cdiv(D, tw);
   a.n_chunks = (int)cdiv(T, kBwdChunk);
@@ -700,7 +791,13 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
     VSSM_TRY(make_map(&mcs, chunk_states, IO::F32, cdiv(T, kStateChunk) * N, D, a.box_x, N));
   }
   e = launch_scan_bwd(a, io, mu, mdr, mz, mdo, mcs, my, dA, dB, dC, dDskip, d_dt_bias, st);
-  return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "selective_scan_bwd launch");
+  if (e != cudaSuccess) return cuda_fail(e, "selective_scan_bwd launch");
+  const bool f = io == IO::F32;
+  return check_outputs(a.status, st, {{du, T * D, f}, {ddelta_raw, T * D, f}, {a.dz, a.dz ? T * D : 0, f},
+                                      {dA, (int64_t)D * N, true}, {dB, T * N, true}, {dC, T * N, true},
+                                      {dDskip, dDskip ? (int64_t)D : 0, true},
+                                      {d_dt_bias, d_dt_bias ? (int64_t)D : 0, true},
+                                      {d_initial_states, d_initial_states ? (int64_t)num_seqs * D * N : 0, true}});
 }
 
 }  // extern "C"

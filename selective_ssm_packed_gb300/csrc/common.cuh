@@ -14,6 +14,20 @@ namespace vssm {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Device checks of the VSSM_CHECKS=1 build: VSSM_CHECKED(cond, status) is
+// cond, and when cond fails it ORs kStatusDeviceCheck into *status, so that
+// the caller can skip the access it guards; in the ordinary build it is the
+// constant true and costs nothing.  Nothing traps.
+__device__ __forceinline__ bool device_check(bool cond, int* status) {
+  if (!cond && status) atomicOr(status, kStatusDeviceCheck);
+  return cond;
+}
+#if VSSM_CHECKS
+#define VSSM_CHECKED(cond, status) ::vssm::device_check((cond), (status))
+#else
+#define VSSM_CHECKED(cond, status) true
+#endif
+
 // look-back flag values
 enum : int { kFlagNone = 0, kFlagAggregate = 1, kFlagInclusive = 2 };
 
@@ -584,6 +598,23 @@ inline cudaError_t resident_ctas_per_sm(K kernel, int threads, size_t smem, int*
   n = std::min(n, thr_sm / threads);
   *per_sm = n;
   return cudaSuccess;
+}
+
+// The current device's SM count (1 when the query fails).
+inline int device_sm_count() {
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess || n_sm < 1)
+    return 1;
+  return n_sm;
+}
+
+// Blocks of a grid-stride kernel of 256-thread blocks over `work` items: one
+// item per thread, at most the 8 blocks per SM that fill the device once.
+inline int64_t grid_stride_blocks(int64_t work) {
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int64_t b = (work + 255) / 256;
+  return b < cap ? b : cap;
 }
 
 // Grid of a persistent kernel: as many CTAs as fit on the device at once (all

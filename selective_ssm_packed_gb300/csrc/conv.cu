@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(256, 4) conv_fwd_tile_kernel(const __grid_cons
     // a tap reaching before the sequence start reads the sequence's tail value
     const float* trow = nullptr;
     if constexpr (kTail) {
-      if (p < W - 1 && t0 + tl < a.T) trow = a.x_init + ((int64_t)a.seq[t0 + tl] * a.D + c0 + c) * (W - 1);
+      if (p < W - 1 && t0 + tl < a.T &&
+          VSSM_CHECKED((unsigned)a.seq[t0 + tl] < (unsigned)a.num_seqs, a.status))
+        trow = a.x_init + ((int64_t)a.seq[t0 + tl] * a.D + c0 + c) * (W - 1);
     }
     float o[4];
 #pragma unroll
@@ -267,7 +269,8 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
       // taps reaching before the sequence start read the sequence's tail values
       const float* trow = nullptr;
       if constexpr (kTail) {
-        if (a.x_init && p < W - 1 && t0 + tl < a.T)
+        if (a.x_init && p < W - 1 && t0 + tl < a.T &&
+            VSSM_CHECKED((unsigned)a.seq[t0 + tl] < (unsigned)a.num_seqs, a.status))
           trow = a.x_init + ((int64_t)a.seq[t0 + tl] * a.D + c0 + c) * (W - 1);
       }
       auto tail2 = [&](int h, int k) {  // the tail pair for tap k (k > p) of channels c+2h, c+2h+1
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(256, 2) conv_bwd_tile_kernel(const __grid_cons
 #pragma unroll
               for (int k = W - 1; k >= 1; --k)
                 if (pw[k] == 0) ke = k;
-              if (ke) {
+              if (ke && VSSM_CHECKED((unsigned)a.seq[t] < (unsigned)a.num_seqs, a.status)) {
                 const float* drow = a.dx_last + ((int64_t)a.seq[t] * a.D + c0 + c) * (W - 1) + W - 1 - ke;
                 acc[0] = __fadd2_rn(acc[0], make_float2(__ldg(drow), __ldg(drow + (W - 1))));
                 acc[1] = __fadd2_rn(acc[1], make_float2(__ldg(drow + 2 * (W - 1)), __ldg(drow + 3 * (W - 1))));

@@ -6,6 +6,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// 1 in the checked build (-DVSSM_CHECKS=1): kernels check the sequence-state
+// rows they index and the calls check caller-supplied position indices.
+#ifndef VSSM_CHECKS
+#define VSSM_CHECKS 0
+#endif
+
 namespace vssm {
 
 enum class IO { F32 = 0, BF16 = 1 };
@@ -15,7 +21,8 @@ inline int io_bytes(IO t) { return t == IO::F32 ? 4 : 2; }
 constexpr int kStateChunk = 32;  // tokens per saved scan-state chunk
 
 // status-word bits written by kernels (the host maps them to VSSM_ERR_* codes)
-enum : int { kStatusBadCu = 1, kStatusLookbackTimeout = 2, kStatusTmaTimeout = 4 };
+enum : int { kStatusBadCu = 1, kStatusLookbackTimeout = 2, kStatusTmaTimeout = 4, kStatusNonFinite = 8,
+             kStatusDeviceCheck = 16 };
 
 // ---------------------------------------------------------------- position indices
 // seq[t] = the sequence holding token t (read where sequences start or end).
@@ -26,6 +33,13 @@ cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, in
                                          const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st);
+// ORs kStatusNonFinite into *status when any of the n values at p (io type,
+// or f32 when f32 is true) is a NaN or an infinity.
+cudaError_t launch_nonfinite_check(const void* p, int64_t n, bool f32, int32_t* status, cudaStream_t st);
+// ORs kStatusBadCu into *status when a caller's position indices disagree
+// with cu_seqlens (pos[t] != t - cu[s] for the sequence s holding t).
+cudaError_t launch_position_check(const int32_t* cu, int32_t num_seqs, int64_t T, const int32_t* pos,
+                                  int32_t* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- conv1d
 struct ConvArgs {
@@ -89,6 +103,7 @@ struct ScanArgs {
   // writes h_final; bwd reads h_init and dh_final and writes dh_init.  seq[t]
   // is the sequence of token t (set whenever one of them is given).
   const int32_t* seq;
+  int num_seqs;
   const float* h_init;
   float* h_final;
   const float* dh_final;
@@ -174,8 +189,13 @@ struct DebugKnobs {
   unsigned long long wait_ns;
   long long delay_ticket;
   unsigned long long delay_ns;
+  bool check_finite;
 };
 DebugKnobs debug_knobs();
+// With the VSSM_DBG_CHECK_FINITE knob on, checks the n outputs (pointer,
+// value count, f32 or io bf16) for NaNs and infinities into *status.
+int check_outputs_finite(int32_t* status, cudaStream_t st, const void* const* ptrs, const int64_t* counts,
+                         const bool* f32, int n);
 
 // ---------------------------------------------------------------- reductions
 // out[m] = sum_{p < P} in[p * ld + m] for m < M, in a fixed order (rows in

@@ -32,16 +32,76 @@ __global__ void __launch_bounds__(256) position_indices_kernel(const int32_t* __
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st) {
   const int64_t work = T > (int64_t)num_seqs + 1 ? T : (int64_t)num_seqs + 1;
-  int64_t blocks = (work + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  int64_t blocks = grid_stride_blocks(work);
   if (blocks < 1) blocks = 1;
   position_indices_kernel<<<(unsigned)blocks, 256, 0, st>>>(cu, num_seqs, T, pos, status);
+  return cudaGetLastError();
+}
+
+// A value is NaN or infinite when its exponent bits are all ones: bits
+// 0x7f800000 of an f32, 0x7f80 of a bf16 (two bf16 values per 32-bit word).
+__global__ void __launch_bounds__(256) nonfinite_kernel(const uint32_t* __restrict__ p, int64_t words,
+                                                        int bf16, int32_t* status) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  bool bad = false;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += stride) {
+    const uint32_t v = __ldg(p + i);
+    bad |= (v & 0x7f800000u) == 0x7f800000u;
+    if (bf16) bad |= (v & 0x7f80u) == 0x7f80u;
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusNonFinite);
+}
+
+// The last value of an odd count of bf16 values, which has no word of its own.
+__global__ void nonfinite_bf16_tail_kernel(const uint16_t* __restrict__ p, int32_t* status) {
+  if ((p[0] & 0x7f80u) == 0x7f80u) atomicOr(status, kStatusNonFinite);
+}
+
+cudaError_t launch_nonfinite_check(const void* p, int64_t n, bool f32, int32_t* status, cudaStream_t st) {
+  if (!p || n <= 0) return cudaSuccess;
+  const int64_t words = f32 ? n : n / 2;
+  const int64_t blocks = grid_stride_blocks(words);
+  if (blocks > 0)
+    nonfinite_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint32_t*>(p), words, f32 ? 0 : 1, status);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && !f32 && (n & 1)) {
+    nonfinite_bf16_tail_kernel<<<1, 1, 0, st>>>(static_cast<const uint16_t*>(p) + (n - 1), status);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+// pos[t] must be t - cu[s] for the sequence s holding token t.
+__global__ void __launch_bounds__(256) position_check_kernel(const int32_t* __restrict__ cu, int32_t S,
+                                                             int64_t T, const int32_t* __restrict__ pos,
+                                                             int32_t* status) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  bool bad = false;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += stride) {
+    int32_t lo = 0, hi = S;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    bad |= (int64_t)pos[t] != t - (int64_t)cu[lo];
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusBadCu);
+}
+
+cudaError_t launch_position_check(const int32_t* cu, int32_t num_seqs, int64_t T, const int32_t* pos,
+                                  int32_t* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int64_t blocks = grid_stride_blocks(T);
+  position_check_kernel<<<(unsigned)blocks, 256, 0, st>>>(cu, num_seqs, T, pos, status);
   return cudaGetLastError();
 }
 
 // seq[t] = the sequence holding token t: the largest s with cu[s] <= t (the
 // same upper-bound search, so zero-length sequences hold no token).  The scan
 // calls read it only where a sequence starts or ends, to find its state row.
+// A malformed cu_seqlens (reported through the status word) can leave tokens
+// past cu[S]; they are given the last sequence, so that every state row the
+// kernels touch exists.
 __global__ void __launch_bounds__(256) sequence_index_kernel(const int32_t* __restrict__ cu,
                                                              int32_t S, int64_t T,
                                                              int32_t* __restrict__ seq) {
@@ -52,14 +112,13 @@ __global__ void __launch_bounds__(256) sequence_index_kernel(const int32_t* __re
       const int32_t mid = (lo + hi + 1) >> 1;
       if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
     }
-    seq[t] = lo;
+    seq[t] = lo < S ? lo : S - 1;
   }
 }
 
 cudaError_t launch_sequence_index(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* seq,
                                   cudaStream_t st) {
-  int64_t blocks = (T + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  const int64_t blocks = grid_stride_blocks(T);
   if (blocks < 1) return cudaSuccess;
   sequence_index_kernel<<<(unsigned)blocks, 256, 0, st>>>(cu, num_seqs, T, seq);
   return cudaGetLastError();

@@ -97,6 +97,8 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   if (T < 0 || T > 2147483647LL) return err(VSSM_ERR_ARG, "total_tokens %lld out of range", T);
   if (D <= 0) return err(VSSM_ERR_ARG, "D must be positive (got %lld)", D);
   if (num_seqs < 0 || !cu_seqlens) return record_error(VSSM_ERR_ARG, "bad num_seqs or NULL cu_seqlens");
+  if ((initial_states || final_states) && T > 0 && num_seqs < 1)
+    return record_error(VSSM_ERR_ARG, "sequence states given for tokens but num_seqs = 0");
   if (N != 4 && N != 8 && N != 16) return err(VSSM_ERR_UNSUPPORTED, "N = %lld not in {4, 8, 16}", N);
   const int e = io_bytes(io);
   if (((int64_t)D * e) % 16 != 0 || (N * e) % 16 != 0)
@@ -147,6 +149,10 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   }
 
   const int32_t* pos = position_indices;
+  if (VSSM_CHECKS && pos) {  // the checked build verifies the caller's indices
+    ce = launch_position_check(cu_seqlens, num_seqs, T, pos, status_word, st);
+    if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
+  }
   if (!pos) {
     int32_t* p = reinterpret_cast<int32_t*>(s + l.pos);
     ce = launch_position_indices(cu_seqlens, num_seqs, T, p, status_word, st);
@@ -166,7 +172,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   a.agg = reinterpret_cast<float*>(s + l.agg);
   a.agg_sd = reinterpret_cast<float*>(s + l.agg_sd);
   a.incl = reinterpret_cast<float*>(s + l.incl);
-  a.T = T; a.D = D; a.N = N;
+  a.T = T; a.D = D; a.N = N; a.num_seqs = num_seqs;
   a.n_tiles = (int)cdiv(D, tw);
   a.n_chunks = (int)cdiv(T, kFwdChunk);
   a.delta_softplus = delta_softplus ? 1 : 0;
@@ -188,5 +194,9 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   if (r != VSSM_OK) return r;
   ce = launch_scan_fwd(a, io, mu, mdr, mz, st);
   if (ce != cudaSuccess) return record_error(VSSM_ERR_CUDA, cudaGetErrorString(ce));
-  return VSSM_OK;
+  // with the VSSM_DBG_CHECK_FINITE knob on: NaNs or infinities in the outputs
+  const void* outs[] = {out, y};
+  const int64_t counts[] = {T * D, y ? T * D : 0};
+  const bool f32[] = {io == IO::F32, io == IO::F32};
+  return check_outputs_finite(status_word, st, outs, counts, f32, 2);
 }

@@ -356,7 +356,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   // a sequence-state row entry pair (channels d, d+1) of state n for token t's sequence
   auto state_pair = [&](const float* st, int t, int n) {
-    if (!valid) return make_float2(0.0f, 0.0f);
+    if (!valid || !VSSM_CHECKED((unsigned)a.seq[t0 + t] < (unsigned)a.num_seqs, a.status))
+      return make_float2(0.0f, 0.0f);
     const float* row = st + ((int64_t)a.seq[t0 + t] * a.D + d) * N + n;
     return make_float2(__ldg(row), __ldg(row + N));
   };
@@ -571,7 +572,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             if (ts < rows) pdB[ts] = sum;
           }
           if constexpr (kStates) {
-            if (((evG >> tt) & 1u) && valid) {
+            if (((evG >> tt) & 1u) && valid &&
+                VSSM_CHECKED((unsigned)a.seq[t0 + tt] < (unsigned)a.num_seqs, a.status)) {
               // the gradient reaching the starting state: dh_t times a's own value
               const float2 gF = mul2(dhF, ex2x2(mul2(dlp, AF))), gS = mul2(dhS, ex2x2(mul2(dlp, AS)));
               float* row = a.dh_init + ((int64_t)a.seq[t0 + tt] * a.D + d) * N;
@@ -947,7 +949,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   }
   // sequence-state entries (channels d + 2j, d + 2j + 1) of state n for token t's sequence
   auto state_pair = [&](const float* st, int t, int n, int j) {
-    if (!valid) return make_float2(0.0f, 0.0f);
+    if (!valid || !VSSM_CHECKED((unsigned)a.seq[t0 + t] < (unsigned)a.num_seqs, a.status))
+      return make_float2(0.0f, 0.0f);
     const float* row = st + ((int64_t)a.seq[t0 + t] * a.D + d + 2 * j) * N + n;
     return make_float2(__ldg(row), __ldg(row + N));
   };
@@ -1185,7 +1188,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         // group's; stored after the block's barrier (no stall on the shuffles)
         if (colsum.feed(e, false, wv[0], wv[1], lane, &pendB)) pendB_t = blk * kRB + ColSum4::token(lane);
         if constexpr (kStates) {
-          if (((evG >> tt) & 1u) && valid) {
+          if (((evG >> tt) & 1u) && valid &&
+              VSSM_CHECKED((unsigned)a.seq[t0 + tt] < (unsigned)a.num_seqs, a.status)) {
             float* row = a.dh_init + ((int64_t)a.seq[t0 + tt] * a.D + d) * N;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {

@@ -206,7 +206,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // the state a sequence starting at token t (of the chunk) starts from: its
   // row of the initial states, or zero
   auto start_state = [&](float2 (&hs)[N / 2], int t) {
-    if (kStates && a.h_init && valid) {
+    if (kStates && a.h_init && valid &&
+        VSSM_CHECKED((unsigned)a.seq[t0 + t] < (unsigned)a.num_seqs, a.status)) {
       const float4* row = reinterpret_cast<const float4*>(a.h_init + ((int64_t)a.seq[t0 + t] * a.D + d) * N);
 #pragma unroll
       for (int i = 0; i < N / 4; ++i) {
@@ -222,7 +223,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // the state after the last token t (of the chunk) of a sequence, into its
   // row of the final states
   auto end_state = [&](const float2 (&hs)[N / 2], int t) {
-    if (valid) {
+    if (valid && VSSM_CHECKED((unsigned)a.seq[t0 + t] < (unsigned)a.num_seqs, a.status)) {
       float4* row = reinterpret_cast<float4*>(a.h_final + ((int64_t)a.seq[t0 + t] * a.D + d) * N);
 #pragma unroll
       for (int i = 0; i < N / 4; ++i)

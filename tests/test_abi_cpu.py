@@ -57,6 +57,21 @@ def test_strerror_and_status_codes(lib):
     assert binding.status_code(0) == 0
     assert binding.status_code(1) == -16
     assert binding.status_code(2) == -17
+    assert binding.status_code(4) == -17          # a tile-copy wait ran out
+    assert binding.status_code(8) == -18          # a non-finite output (VSSM_DBG_CHECK_FINITE)
+    assert binding.status_code(16) == -19         # a device index check (checked build)
+    assert binding.status_code(1 | 8 | 16) == -16  # malformed input outranks what follows from it
+    assert lib.vssm_checks_build() == 0           # the ordinary build
+
+
+def test_checked_build_compiles_and_reports_itself():
+    """The VSSM_CHECKS=1 variant builds beside the ordinary library (nvcc
+    cross-compiles here) and says which build it is."""
+    import ctypes
+    path = build.build(checks=True)
+    assert path == build.CHECKS_LIB_PATH != build.LIB_PATH
+    L = ctypes.CDLL(path)
+    assert L.vssm_checks_build() == 1
 
 
 def _conv_fwd(lib, **kw):
@@ -96,6 +111,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     args[21] = 8
     assert scan(*args) == -3                     # misaligned initial_states
     args[21] = None
+    args[13] = 0
+    args[21] = 16
+    assert scan(*args) == -1                     # initial states for 16 tokens but no sequence
+    args[13] = 1
+    args[21] = None
     args[23] = None
     assert scan(*args) == -4
 
@@ -109,3 +129,6 @@ def test_debug_knobs(lib):
     assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_NS, 10**8) == -1
     assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_NS, 200_000) == 0
     assert lib.vssm_debug_set(binding.VSSM_DBG_DELAY_ITEM, -1) == 0
+    assert lib.vssm_debug_set(binding.VSSM_DBG_FORCE_COPY_TIMEOUT, -1) == 0
+    assert lib.vssm_debug_set(binding.VSSM_DBG_CHECK_FINITE, 2) == -1
+    assert lib.vssm_debug_set(binding.VSSM_DBG_CHECK_FINITE, 0) == 0
