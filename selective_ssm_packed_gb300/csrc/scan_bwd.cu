@@ -696,10 +696,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // N = 16: a thread owns two channel pairs and one state pair
 // ============================================================================
 // Work item = 32 tokens x kTW = 64 channels; CTA = 4 warps in two channel
-// groups (warps 2g, 2g+1 take the channels 32g .. 32g+31).  A thread owns the
-// channel quad q = 8g + lane % 8 (channels 4q .. 4q+3: two pairs for the
-// paired FP32 instructions) and the state pair p = 4 (w % 2) + lane / 8: eight
-// (channel, state) chains.  Against the pair-by-pair layout above, every
+// groups (warps 2g, 2g+1 take the channels 32g .. 32g+31).  A thread owns a
+// channel quad q of its group (channels 4q .. 4q+3: two pairs for the paired
+// FP32 instructions) and a state pair p of its warp's four (p = 4 (w % 2) ..
+// +3): eight (channel, state) chains; the lane map is given in the kernel.  Against the pair-by-pair layout above, every
 // per-token value a thread loads serves twice the chains, the channel sums for
 // dB / dC start over 4 channels in registers, and the history takes 8 words
 // per token (256 tensor-memory columns per warp, 2 CTAs per SM).  The partial
@@ -747,25 +747,45 @@ struct Bwd16Smem {
   alignas(8) uint64_t bar;
 };
 
-// Column sums over the 8 lanes of a warp that share a state pair (lane % 8 =
-// channel quad) for groups of 4 tokens x 2 states, by shuffle butterflies: level
-// 1 exchanges states over lane bit 2 (a lane keeps the state 2p + bit2), levels
-// 2 and 3 pair tokens over lane bits 1 and 0.  After the 4th token, lane l
-// holds the sum over the 8 lanes for token bit1(l) + 2 bit0(l) of the group.
+// Column sums over the 8 lanes of a warp that share a state pair for groups
+// of 4 tokens x 2 states, by shuffle butterflies.  The 8 lanes differ in lane
+// bits 0 and 1 (channel quads) and in bits 3 and 4 together (the quarter-warps
+// k and k ^ 3).  Level 1 exchanges states over lane bit 0 (a lane keeps its
+// first state, 2p + bit 0: lanes l and l ^ 1 hold the pair in opposite
+// orders), level 2 pairs tokens over bit 1, level 3 over the quarter pair
+// (xor 24, the upper quarter of the two keeping the odd pair).  After the 4th
+// token, lane l holds the sum over the 8 lanes for token bit1(l) + 2 bit4(l)
+// of the group.
 struct ColSum4 {
   float p2[2], p3[2];
 
-  static __device__ __forceinline__ int token(int lane) { return ((lane >> 1) & 1) + 2 * (lane & 1); }
+  static __device__ __forceinline__ int token(int lane) { return ((lane >> 1) & 1) + 2 * ((lane >> 4) & 1); }
+
+  // lo + hi over the lane pair (l, l ^ xor_mask): the lane with up_bit set
+  // keeps the hi sum, its partner the lo sum
+  static __device__ __forceinline__ float combine(float lo, float hi, int lane, int xor_mask, int up_bit) {
+    const bool up = (lane & up_bit) != 0;
+    return (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, xor_mask);
+  }
 
   __device__ __forceinline__ bool feed(int c, bool ascending, float vF, float vS, int lane, float* sum) {
-    p2[c & 1] = vF + __shfl_xor_sync(0xffffffffu, vS, 4);
+    p2[c & 1] = vF + __shfl_xor_sync(0xffffffffu, vS, 1);
     if ((c & 1) != (ascending ? 1 : 0)) return false;
-    p3[(c >> 1) & 1] = ColSum8::combine(p2[0], p2[1], lane, 2);
+    p3[(c >> 1) & 1] = combine(p2[0], p2[1], lane, 2, 2);
     if ((c & 3) != (ascending ? 3 : 0)) return false;
-    *sum = ColSum8::combine(p3[0], p3[1], lane, 1);
+    *sum = combine(p3[0], p3[1], lane, 24, 16);
     return true;
   }
 };
+
+// Index (float4 or float2 units) of the n-sum partial of state pair sp,
+// channel pair j of quad cq, token e of buffer buf.  The quad is swizzled by
+// the parity of j and sp so that the walk's stores (a quarter-warp: 4 quads x
+// 2 state pairs, fixed j) and the finalize's loads (a quarter-warp: 4 quads x
+// 2 pairs j, fixed sp) each hit 8 distinct 16-byte bank groups.
+__device__ __forceinline__ int nred_at(int buf, int e, int sp, int j, int cq) {
+  return ((buf * kRB + e) * kSP + sp) * 2 * kCQ + j * kCQ + (cq ^ (4 * (j ^ (sp & 1))));
+}
 
 __device__ __forceinline__ void st_io4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void st_io4(__nv_bfloat16* p, float4 v) {
@@ -791,10 +811,17 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int n_items = a.n_chunks * a.n_tiles;
+  // Lane map: quarter-warp k = lane / 8 holds 4 channel quads x 2 state pairs,
+  // the quads 4 (k % 2) .. +3 of the group and the state pairs
+  // 2 ((k % 2) ^ (k / 2)) .. +1 of the warp's four.  The two quarters of a
+  // half-warp then read disjoint quads (per-(token, channel) values) and
+  // disjoint state pairs (B, C), so a 16-byte load of either kind is two
+  // shared-memory wavefronts per warp, not four.
   const int grp = w >> 1;                          // channel group
-  const int cq = 8 * grp + (lane & 7);             // channel quad of the tile
-  const int sp = 4 * (w & 1) + (lane >> 3);        // state pair
-  const int o = (lane >> 2) & 1;                   // this lane's state order
+  const int qk = lane >> 3, qr = lane & 7;
+  const int cq = 8 * grp + 4 * (qk & 1) + (qr & 3);                 // channel quad of the tile
+  const int sp = 4 * (w & 1) + 2 * ((qk & 1) ^ (qk >> 1)) + (qr >> 2);  // state pair
+  const int o = lane & 1;                          // this lane's state order
   const int nF = 2 * sp + o, nS = 2 * sp + 1 - o;  // its "first" and "second" state
   const int c0 = 4 * cq;                           // first channel of the quad (in the tile)
 
@@ -1165,20 +1192,18 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
           }
         }
         const float2 BF = lo2(bd), BS = hi2(bd);
-        float4* np = sm.nred + ((buf * kRB + e) * kSP + sp) * 2 * kCQ + cq;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const float2 s1 = fma2(dh[1][j], BS, mul2(dh[0][j], BF));
           const float2 s2 = fma2(A[1][j], qq[1][j], mul2(A[0][j], qq[0][j]));
-          np[j * kCQ] = mk4(s1, s2);
+          sm.nred[nred_at(buf, e, sp, j, cq)] = mk4(s1, s2);
         }
         if constexpr (kRecY) {  // C.h_t partials for y, h_t = p_t + delta u B
-          float2* yp = sm.nY + ((buf * kRB + e) * kSP + sp) * 2 * kCQ + cq;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const float2 pF = make_float2(bitsf(hb[8 * e + 2 * j]), bitsf(hb[8 * e + 2 * j + 1]));
             const float2 pS = make_float2(bitsf(hb[8 * e + 4 + 2 * j]), bitsf(hb[8 * e + 4 + 2 * j + 1]));
-            yp[j * kCQ] = fma2(hi2(cd), fma2(dup[j], BS, pS), mul2(lo2(cd), fma2(dup[j], BF, pF)));
+            sm.nY[nred_at(buf, e, sp, j, cq)] = fma2(hi2(cd), fma2(dup[j], BS, pS), mul2(lo2(cd), fma2(dup[j], BF, pF)));
           }
         }
         float wv[2];
@@ -1220,10 +1245,9 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       const int t = blk * kRB + e;
       if (pendB_t < rows) pdB[pendB_t] = pendB;
       pendB_t = kL;
-      const float4* np = sm.nred + (buf * kRB + e) * kSP * 2 * kCQ + hh * kCQ + qd;
       float4 pv[kSP];
 #pragma unroll
-      for (int v = 0; v < kSP; ++v) pv[v] = np[v * 2 * kCQ];
+      for (int v = 0; v < kSP; ++v) pv[v] = sm.nred[nred_at(buf, e, v, hh, qd)];
       // fixed pairwise tree over the 8 state pairs
       const float4 s = add4(add4(add4(pv[0], pv[1]), add4(pv[2], pv[3])), add4(add4(pv[4], pv[5]), add4(pv[6], pv[7])));
       const float2 dlv = reinterpret_cast<const float2*>(sm.dl + qd * kQT + t)[hh];
@@ -1245,10 +1269,9 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         st_io2(gdu + o2, du);
         st_io2(gddr + o2, ddr);
         if constexpr (kRecY) {
-          const float2* yp = sm.nY + (buf * kRB + e) * kSP * 2 * kCQ + hh * kCQ + qd;
-          float2 ys = yp[0];
+          float2 ys = sm.nY[nred_at(buf, e, 0, hh, qd)];
 #pragma unroll
-          for (int v = 1; v < kSP; ++v) ys = __fadd2_rn(ys, yp[v * 2 * kCQ]);
+          for (int v = 1; v < kSP; ++v) ys = __fadd2_rn(ys, sm.nY[nred_at(buf, e, v, hh, qd)]);
           const float2 f = reinterpret_cast<const float2*>(sm.dzf + qd * kQT + t)[hh];
           st_io2(gdz + o2, mul2(f, fma2(dsk, uv, ys)));
         }
