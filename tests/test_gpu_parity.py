@@ -535,15 +535,17 @@ def test_right_padded_layout_matches_packed_on_real_tokens():
 
 # ------------------------------------------------------------------ failure reporting
 
-@pytest.mark.parametrize("N", [8, 16])
-def test_lookback_wait_timeout_is_reported_not_hung(N):
+@pytest.mark.parametrize("N,dtype", [(8, "f32"), (16, "f32"), (16, "bf16")])
+def test_lookback_wait_timeout_is_reported_not_hung(N, dtype):
     """A work item that never publishes its flag makes the next one's wait run
-    out (after 1 ms); the call still completes and reports the timeout."""
+    out (after 1 ms); the call still completes and reports the timeout (each
+    forward and backward kernel: bf16 with N = 16 runs the channel-pair
+    forward)."""
     cu_np = np.array([0, 1024], dtype=np.int32)
     T, D = 1024, 32
     rng = np.random.default_rng(1)
-    u = f32(rng.standard_normal((T, D)))
-    B = f32(rng.standard_normal((T, N)))
+    u = dev(rng.standard_normal((T, D)), dtype)
+    B = dev(rng.standard_normal((T, N)), dtype)
     A = -torch.ones(D, N, device="cuda")
     cu = torch.from_numpy(cu_np).cuda()
     ws = torch.empty(binding.scan_fwd_workspace_size(T, D, N), dtype=torch.uint8, device="cuda")

@@ -143,3 +143,29 @@ def test_noalloc_refuses_a_problem_larger_than_its_scratch(lib):
     assert rc == -4
     msg = binding.last_error()
     assert "scratch" in msg and str(64 << 20) in msg
+
+
+def test_noalloc_reports_a_lookback_wait_that_runs_out(lib):
+    """The test knobs of vssm_debug_set apply to this entry point too: a work
+    item that never publishes its look-back state makes the next one's wait
+    run out (after 1 ms); the call completes and its status word reports the
+    timeout, and the next call is clean and equals the workspace entry point
+    bit for bit."""
+    T, t, r, cu = _case([1024], 32, 16, "f32", 45)
+    out = torch.empty_like(t["u"])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        binding.debug_set(binding.VSSM_DBG_WAIT_NS, 1_000_000)
+        binding.debug_set(binding.VSSM_DBG_DROP_FLAG, 3)
+        assert _noalloc(lib, t, T, 32, 16, "f32", out, None, status) == 0, binding.last_error()
+        torch.cuda.synchronize()
+        assert binding.status_code(int(status.item())) == -17
+    finally:
+        binding.debug_set(binding.VSSM_DBG_DROP_FLAG, -1)
+        binding.debug_set(binding.VSSM_DBG_WAIT_NS, 1_000_000_000)
+    assert _noalloc(lib, t, T, 32, 16, "f32", out, None, status) == 0, binding.last_error()
+    torch.cuda.synchronize()
+    assert binding.status_code(int(status.item())) == 0
+    ref = vs.varlen_selective_scan_fwd(t["u"], t["delta_raw"], t["A"], t["B"], t["C"], t["Dskip"], t["z"],
+                                       t["dt_bias"], t["cu"], chunk_states=False)
+    assert torch.equal(out, ref[0])
