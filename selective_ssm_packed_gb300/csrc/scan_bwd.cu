@@ -730,7 +730,6 @@ struct Bwd16Smem {
   alignas(16) float4 dl[kCQ * kQT];   // delta
   alignas(16) float4 dlu[kCQ * kQT];  // delta * u
   alignas(16) float4 g[kCQ * kQT];    // dout * (SiLU(z) + gate floor)
-  alignas(16) float4 dzf[kRecY ? kCQ * kQT : 1];  // d out / d y, when y is recomputed
   // ---- B and C doubled, [token][state pair][order] float4 (as above)
   alignas(16) float4 BD[kL * kSP * 2];
   alignas(16) float4 CD[kL * kSP * 2];
@@ -739,7 +738,10 @@ struct Bwd16Smem {
   //      [buffer][token of the block][state pair][channel pair parity][quad]
   //      float4 = (sum dh B for the pair's two channels, sum A dh p for them)
   alignas(16) float4 nred[2 * kRB * kSP * 2 * kCQ];
-  alignas(16) float2 nY[kRecY ? 2 * kRB * kSP * 2 * kCQ : 2];  // C.h partials, when y is recomputed
+  // C.h partials, when y is recomputed: [buffer][token of the block][warp of
+  // the group][group][channel of the group], each summed over the warp's
+  // four state pairs
+  alignas(16) float ysum[kRecY ? 2 * kRB * 2 * 2 * kTile : 2];
   alignas(16) float4 redD[128];
   alignas(16) float2 redB[128];
   uint32_t taddr;
@@ -934,8 +936,6 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
             const float4 y4 = ld_io4(sm.y + at);
             st_io4(gdz + (t0 + t) * a.D + d0 + 4 * q, mk4(mul2(flo, lo2(y4)), mul2(fhi, hi2(y4))));
           }
-        } else if constexpr (kRecY) {
-          sm.dzf[q * kQT + t] = ok ? mk4(flo, fhi) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
       }
       const float4 z0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -1198,13 +1198,27 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
           const float2 s2 = fma2(A[1][j], qq[1][j], mul2(A[0][j], qq[0][j]));
           sm.nred[nred_at(buf, e, sp, j, cq)] = mk4(s1, s2);
         }
-        if constexpr (kRecY) {  // C.h_t partials for y, h_t = p_t + delta u B
+        if constexpr (kRecY) {
+          // C.h_t over this thread's two states (h_t = p_t + delta u B), for
+          // the quad's channel pairs; summed over the warp's four state pairs
+          // of the quad (lanes l ^ 4, l ^ 16) so that lane l keeps channel
+          // 2 bit2(l) + bit4(l) of its quad
+          float2 yv[2];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const float2 pF = make_float2(bitsf(hb[8 * e + 2 * j]), bitsf(hb[8 * e + 2 * j + 1]));
             const float2 pS = make_float2(bitsf(hb[8 * e + 4 + 2 * j]), bitsf(hb[8 * e + 4 + 2 * j + 1]));
-            sm.nY[nred_at(buf, e, sp, j, cq)] = fma2(hi2(cd), fma2(dup[j], BS, pS), mul2(lo2(cd), fma2(dup[j], BF, pF)));
+            yv[j] = fma2(hi2(cd), fma2(dup[j], BS, pS), mul2(lo2(cd), fma2(dup[j], BF, pF)));
           }
+          const bool b2 = (lane & 4) != 0, b4 = (lane & 16) != 0;
+          float2 keep = b2 ? yv[1] : yv[0];
+          const float2 send = b2 ? yv[0] : yv[1];
+          keep.x += __shfl_xor_sync(0xffffffffu, send.x, 4);
+          keep.y += __shfl_xor_sync(0xffffffffu, send.y, 4);
+          float k1 = b4 ? keep.y : keep.x;
+          k1 += __shfl_xor_sync(0xffffffffu, b4 ? keep.x : keep.y, 16);
+          sm.ysum[((buf * kRB + e) * 2 + (w & 1)) * (2 * kTile) + grp * kTile + 4 * (cq - 8 * grp) + 2 * (b2 ? 1 : 0) +
+                  (b4 ? 1 : 0)] = k1;
         }
         float wv[2];
 #pragma unroll
@@ -1269,10 +1283,14 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         st_io2(gdu + o2, du);
         st_io2(gddr + o2, ddr);
         if constexpr (kRecY) {
-          float2 ys = sm.nY[nred_at(buf, e, 0, hh, qd)];
-#pragma unroll
-          for (int v = 1; v < kSP; ++v) ys = __fadd2_rn(ys, sm.nY[nred_at(buf, e, v, hh, qd)]);
-          const float2 f = reinterpret_cast<const float2*>(sm.dzf + qd * kQT + t)[hh];
+          // y = C.h (the two warps' sums, in warp order) + Dskip u, and
+          // d out / d y = dout SiLU'(z), SiLU'(z) = s (1 + z (1 - s))
+          const float* yr = sm.ysum + (buf * kRB + e) * 2 * (2 * kTile) + grp * kTile + 2 * cpl;
+          const float2 ys = __fadd2_rn(*reinterpret_cast<const float2*>(yr),
+                                       *reinterpret_cast<const float2*>(yr + 2 * kTile));
+          const float2 zz = ld_io2(sm.z + at), go = ld_io2(sm.dout + at);
+          const float2 sz = make_float2(sigmoidf_fast(zz.x), sigmoidf_fast(zz.y));
+          const float2 f = mul2(mul2(go, sz), fma2(zz, make_float2(1.0f - sz.x, 1.0f - sz.y), splat2(1.0f)));
           st_io2(gdz + o2, mul2(f, fma2(dsk, uv, ys)));
         }
       }
