@@ -58,7 +58,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // [header 256 B: status int @0, ticket uint @4][flags, one per (slot, lane)][pos][...call specific]
 // header + flags are cleared by one memset at the start of every call.
 struct Layout {
-  size_t flags = 0, pos = 0, seq = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t flags = 0, pos = 0, seq = 0, bcf = 0, agg = 0, agg_sd = 0, incl = 0;
   size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, conv_part = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
@@ -81,6 +81,10 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   off += up(sizeof(int32_t) * (size_t)T);
   l.seq = off;
   off += up(sizeof(int32_t) * (size_t)T);
+  if (!bwd) {  // B and C as fp32 for bf16 I/O, widened once per call
+    l.bcf = off;
+    off += up(sizeof(float) * (size_t)T * N * 2);
+  }
   l.agg = off;
   off += up(sizeof(float) * (size_t)slots * N * tw);
   l.agg_sd = off;
@@ -271,7 +275,8 @@ int vssm::check_outputs_finite(int32_t* status, cudaStream_t st, const void* con
 vssm::ScanLayout vssm::scan_workspace_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   const Layout l = scan_layout(T, D, N, chunk, bwd);
   ScanLayout o;
-  o.flags = l.flags; o.pos = l.pos; o.seq = l.seq; o.agg = l.agg; o.agg_sd = l.agg_sd; o.incl = l.incl;
+  o.flags = l.flags; o.pos = l.pos; o.seq = l.seq; o.bcf = l.bcf; o.agg = l.agg; o.agg_sd = l.agg_sd;
+  o.incl = l.incl;
   o.part_bc = l.part_bc; o.part_a = l.part_a; o.part_d = l.part_d; o.part_b = l.part_b;
   o.clear_bytes = l.clear_bytes; o.incl_bytes = l.incl_bytes; o.total = l.total;
   return o;
@@ -577,6 +582,10 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
   a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
+  if (io == IO::BF16) {
+    a.Bf32 = at<float>(workspace, l.bcf);
+    a.Cf32 = a.Bf32 + T * N;
+  }
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);
   a.flags = at<int>(workspace, l.flags);
@@ -655,6 +664,10 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
   a.u = x; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
   a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
+  if (io == IO::BF16) {
+    a.Bf32 = at<float>(workspace, l.bcf);
+    a.Cf32 = a.Bf32 + T * N;
+  }
   a.conv_w = conv_weight; a.conv_b = conv_bias; a.conv_W = W; a.conv_silu = apply_silu ? 1 : 0; a.u_out = u;
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);

@@ -33,6 +33,8 @@ cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, in
                                          const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st);
+// dst[i] = the bf16 value src[i] as fp32, i < n.
+cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // ORs kStatusNonFinite into *status when any of the n values at p (io type,
 // or f32 when f32 is true) is a NaN or an infinity.
 cudaError_t launch_nonfinite_check(const void* p, int64_t n, bool f32, int32_t* status, cudaStream_t st);
@@ -91,6 +93,10 @@ struct ScanArgs {
   const float* A;
   const void* B;
   const void* C;
+  // fwd with bf16 I/O: B and C widened to fp32 once per call, (T, N) each
+  // (null for fp32 I/O, where the kernel reads B and C themselves)
+  const float* Bf32;
+  const float* Cf32;
   const float* Dskip;
   const void* z;
   const float* dt_bias;
@@ -168,11 +174,12 @@ int record_error(int code, const char* message);
 // ---------------------------------------------------------------- shared host helpers (api.cu)
 // Byte offsets of a scan call's workspace: [header 256 B: status int @0,
 // ticket uint @4][look-back flags][position indices][sequence index]
-// [aggregates][aggregate factors][inclusive states][backward partials].
+// [fwd: B and C as fp32][aggregates][aggregate factors][inclusive states]
+// [backward partials].
 // The header and flags (clear_bytes) start at zero; the inclusive states
 // (incl, incl_bytes) start as all-ones words.
 struct ScanLayout {
-  size_t flags = 0, pos = 0, seq = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t flags = 0, pos = 0, seq = 0, bcf = 0, agg = 0, agg_sd = 0, incl = 0;
   size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };

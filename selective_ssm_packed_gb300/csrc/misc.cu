@@ -38,6 +38,31 @@ cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t
   return cudaGetLastError();
 }
 
+// dst[i] = src[i] widened from bf16 (the upper half of the fp32 word), eight
+// values per thread and 16-byte access where the arrays allow it.
+__global__ void __launch_bounds__(256) widen_bf16_kernel(const uint16_t* __restrict__ src,
+                                                         float* __restrict__ dst, int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t n8 = n / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 q = reinterpret_cast<const uint4*>(src)[i];
+    float4* d = reinterpret_cast<float4*>(dst) + 2 * i;
+    d[0] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                       __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+    d[1] = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xffff0000u),
+                       __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xffff0000u));
+  }
+  for (int64_t i = 8 * n8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = __uint_as_float((uint32_t)src[i] << 16);
+}
+
+cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = grid_stride_blocks((n + 7) / 8);
+  widen_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(src), dst, n);
+  return cudaGetLastError();
+}
+
 // A value is NaN or infinite when its exponent bits are all ones: bits
 // 0x7f800000 of an f32, 0x7f80 of a bf16 (two bf16 values per 32-bit word).
 __global__ void __launch_bounds__(256) nonfinite_kernel(const uint32_t* __restrict__ p, int64_t words,

@@ -166,6 +166,10 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
   a.u = u; a.dr = delta_raw; a.A = A; a.B = B; a.C = C; a.Dskip = Dskip; a.z = z;
   a.dt_bias = dt_bias; a.pos = pos; a.chunk_states = chunk_states; a.out = out; a.y = y;
   a.seq = seq; a.h_init = initial_states; a.h_final = final_states;
+  if (io == IO::BF16) {
+    a.Bf32 = reinterpret_cast<float*>(s + l.bcf);
+    a.Cf32 = a.Bf32 + T * N;
+  }
   a.status = status_word;
   a.ticket = reinterpret_cast<unsigned*>(s + 4);
   a.flags = reinterpret_cast<int*>(s + l.flags);

@@ -56,11 +56,9 @@ struct FwdSmem {
   alignas(16) float cb[kConv ? kTile : 4];
   alignas(128) T dr[kL * kTile];
   alignas(128) T z[kL * kTile];
-  alignas(128) T B[kL * N];
-  alignas(128) T C[kL * N];
-  // B and C widened to fp32 once per work item (bf16 I/O only)
-  alignas(16) float Bf[sizeof(T) == 2 ? kL * N : 4];
-  alignas(16) float Cf[sizeof(T) == 2 ? kL * N : 4];
+  // B and C rows as fp32 (for bf16 I/O widened once per call, before the kernel)
+  alignas(128) float B[kL * N];
+  alignas(128) float C[kL * N];
   alignas(16) float dlt[kL * kTile];
   alignas(16) float aggH[kS * N * kTile];
   float hin[N * kTile];
@@ -108,7 +106,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
     const int dd0 = tl * kTile;
     const uint32_t nval = (uint32_t)(a.D - dd0 < kTile ? a.D - dd0 : kTile);
-    const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
+    const uint32_t bc = (uint32_t)nrows * N * 4u;
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
     // the fused conv's x box has kHalo more rows, and its weights and bias come along
@@ -125,8 +123,10 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
     if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
-    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
+    const float* Bsrc = sizeof(T) == 4 ? static_cast<const float*>(a.B) : a.Bf32;
+    const float* Csrc = sizeof(T) == 4 ? static_cast<const float*>(a.C) : a.Cf32;
+    bulk_load_1d(sm.B, Bsrc + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C, Csrc + tt0 * N, bc, &sm.bar);
     bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
     if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
     if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
@@ -239,12 +239,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   };
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
-  // B and C rows of this warp's own tokens, widened to fp32 by the warp: no
-  // other warp reads them, so a warp barrier is enough
-  const int wr0 = tb < rows ? tb : rows, wr1 = tb + kK < rows ? tb + kK : rows;
-  const float* Bf = widen_rows<T>(sm.B + wr0 * N, sm.Bf + wr0 * N, (wr1 - wr0) * N, lane, 32) - wr0 * N;
-  const float* Cf = widen_rows<T>(sm.C + wr0 * N, sm.Cf + wr0 * N, (wr1 - wr0) * N, lane, 32) - wr0 * N;
-  __syncwarp();
+  const float* Bf = sm.B;
+  const float* Cf = sm.C;
   float2 A2[P];
   if (valid) {
     load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, a.a_log ? 1.0f : kLog2e);
@@ -631,6 +627,12 @@ cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
 cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
+  if (io == IO::BF16) {  // every work item then copies fp32 B and C rows as they are
+    if (!a.Bf32 || !a.Cf32) return cudaErrorInvalidValue;
+    cudaError_t e = launch_widen_bf16(a.B, const_cast<float*>(a.Bf32), a.T * a.N, st);
+    if (e == cudaSuccess) e = launch_widen_bf16(a.C, const_cast<float*>(a.Cf32), a.T * a.N, st);
+    if (e != cudaSuccess) return e;
+  }
   return io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, st)
                        : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, st);
 }
