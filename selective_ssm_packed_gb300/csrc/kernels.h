@@ -33,6 +33,9 @@ cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, in
                                          const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st);
+// The backward's doubled B and C (see ScanArgs::BD) for tokens 0 .. T_pad-1.
+cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, float4* BD,
+                             float4* CD, cudaStream_t st);
 // dst[i] = the bf16 value src[i] as fp32, i < n.
 cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // ORs kStatusNonFinite into *status when any of the n values at p (io type,
@@ -97,6 +100,11 @@ struct ScanArgs {
   // (null for fp32 I/O, where the kernel reads B and C themselves)
   const float* Bf32;
   const float* Cf32;
+  // bwd: B and C doubled, [token][state pair][order] float4 (order 0 holds
+  // (B[2p], B[2p], B[2p+1], B[2p+1]), order 1 the two states swapped), built
+  // once per call for whole 32-token chunks (zero past the last token)
+  const float4* BD;
+  const float4* CD;
   const float* Dskip;
   const void* z;
   const float* dt_bias;
@@ -180,7 +188,7 @@ int record_error(int code, const char* message);
 // (incl, incl_bytes) start as all-ones words.
 struct ScanLayout {
   size_t flags = 0, pos = 0, seq = 0, bcf = 0, agg = 0, agg_sd = 0, incl = 0;
-  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0;
+  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
 // chunk = tokens per work item (kFwdChunk / kBwdChunk).

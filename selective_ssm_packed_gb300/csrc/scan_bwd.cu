@@ -72,8 +72,6 @@ struct BwdSmem {
   alignas(128) T z[kL * kTile];
   alignas(128) T dout[kL * kTile];
   alignas(128) T y[kL * kTile];  // the forward's pre-gate output, when the call has it
-  alignas(128) T B[kL * N];
-  alignas(128) T C[kL * N];
   alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
   alignas(128) float H[N * kTile];    // saved states at the chunk start, [n][channel]
   alignas(16) float bias[kTile];
@@ -200,10 +198,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
     const int dd0 = tl * kTile;
     const uint32_t nval = (uint32_t)(a.D - dd0 < kTile ? a.D - dd0 : kTile);
-    const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
+    const uint32_t bcd = (uint32_t)kL * N * 16u;  // the chunk's doubled B (or C) rows
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bc + nval * N * 4u +
+    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bcd + nval * N * 4u +
                                        (uint32_t)a.box_x * N * 4u + rows4 * 4u +
                                        (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
     tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
@@ -211,8 +209,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
     if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
     if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
-    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.BD, a.BD + tt0 * N, bcd, &sm.bar);
+    bulk_load_1d(sm.CD, a.CD + tt0 * N, bcd, &sm.bar);
     bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
     tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
     if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
@@ -315,18 +313,6 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       sm.sg[cp * kPT + t] = ok ? sg2 : z0;
       if (ok) accD = fma2(gv, uu, accD);
     }
-  }
-  // one (token, state pair) per thread: consecutive lanes read consecutive
-  // pairs of a row and write adjacent entries
-  for (int i = tid; i < kL * NSP; i += kThr) {
-    const int t = i / NSP, pn = i - t * NSP;
-    const bool in = t < rows;
-    const float2 b = in ? ld_io2(sm.B + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
-    const float2 c = in ? ld_io2(sm.C + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
-    sm.BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
-    sm.BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
-    sm.CD[2 * i] = make_float4(c.x, c.x, c.y, c.y);
-    sm.CD[2 * i + 1] = make_float4(c.y, c.y, c.x, c.x);
   }
   // bit t: token t starts a sequence
   const unsigned rst =
@@ -718,8 +704,6 @@ struct Bwd16Smem {
   alignas(128) T z[kL * kTW];
   alignas(128) T dout[kL * kTW];
   alignas(128) T y[kL * kTW];
-  alignas(128) T B[kL * 16];
-  alignas(128) T C[kL * 16];
   alignas(16) float Araw[kTW * 16];
   alignas(128) float H[16 * kTW];  // saved states at the chunk start, [n][channel]
   alignas(16) float bias[kTW];
@@ -835,10 +819,10 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
     const int dd0 = tl * kTW;
     const uint32_t nval = (uint32_t)(a.D - dd0 < kTW ? a.D - dd0 : kTW);
-    const uint32_t bc = (uint32_t)nrows * N * sizeof(T);
+    const uint32_t bcd = (uint32_t)kL * N * 16u;  // the chunk's doubled B (or C) rows
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bc + nval * N * 4u +
+    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bcd + nval * N * 4u +
                                        (uint32_t)a.box_x * N * 4u + rows4 * 4u +
                                        (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
     tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
@@ -846,8 +830,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
     if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
     if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
-    bulk_load_1d(sm.B, static_cast<const T*>(a.B) + tt0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C, static_cast<const T*>(a.C) + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.BD, a.BD + tt0 * N, bcd, &sm.bar);
+    bulk_load_1d(sm.CD, a.CD + tt0 * N, bcd, &sm.bar);
     bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
     tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
     if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
@@ -944,16 +928,6 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       sm.g[q * kQT + t] = ok ? gv : z0;
       if (ok) accD = mk4(fma2(lo2(gv), lo2(u4), lo2(accD)), fma2(hi2(gv), hi2(u4), hi2(accD)));
     }
-  }
-  for (int i = tid; i < kL * kSP; i += kThr) {
-    const int t = i / kSP, pn = i - t * kSP;
-    const bool in = t < rows;
-    const float2 b = in ? ld_io2(sm.B + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
-    const float2 c = in ? ld_io2(sm.C + t * N + 2 * pn) : make_float2(0.0f, 0.0f);
-    sm.BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
-    sm.BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
-    sm.CD[2 * i] = make_float4(c.x, c.x, c.y, c.y);
-    sm.CD[2 * i + 1] = make_float4(c.y, c.y, c.x, c.x);
   }
   const unsigned rst =
       __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
@@ -1471,8 +1445,12 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
     if (e == cudaSuccess && d_dt_bias) e = cudaMemsetAsync(d_dt_bias, 0, sizeof(float) * a.D, st);
     return e;
   }
-  cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
-                                : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  // B and C doubled once per call; every work item copies its chunk's rows
+  cudaError_t e = launch_double_bc(a.B, a.C, io, a.T, (int64_t)a.n_chunks * kBwdChunk, a.N,
+                                   const_cast<float4*>(a.BD), const_cast<float4*>(a.CD), st);
+  if (e != cudaSuccess) return e;
+  e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
+                    : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
   if (e != cudaSuccess) return e;
   const int64_t M = a.T * 2 * a.N;
   // partial rows come in groups of 32 channels: two per tile when N = 16
