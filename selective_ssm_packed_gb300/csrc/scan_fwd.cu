@@ -28,6 +28,9 @@
 //      Work items take chunk ids from an atomic ticket, so a CTA only ever waits
 //      on items already running; every wait is time-bounded and a timeout is
 //      reported through the status word instead of hanging.
+//      Once the entering state is known, the owning warp turns each sub-chunk's
+//      prefix into its exact start state (prefix + entering state times the
+//      product of the factors of the sub-chunks before it).
 //   6. Pass 2: each thread starts from its exact state, recomputes its K tokens
 //      and writes out = (C.h + Dskip u) * SiLU(z); states at multiples of 32
 //      tokens go to chunk_states for the backward pass.
@@ -61,7 +64,6 @@ struct FwdSmem {
   alignas(128) float C[kL * N];
   alignas(16) float dlt[kL * kTile];
   alignas(16) float aggH[kS * N * kTile];
-  float hin[N * kTile];
   float aggSD[kS * kTile];
   alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
   alignas(16) float bias[kTile];
@@ -380,23 +382,25 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (2 * i == n1) a2w.y = A2[i].x;
       if (2 * i + 1 == n1) a2w.y = A2[i].y;
     }
-    // exclusive scan per state; the chunk's totals stay in registers
+    // exclusive scan per state; the chunk's totals, the prefixes and the
+    // sub-chunks' factors stay in registers until the entering state is known
     float2 tot = make_float2(0.0f, 0.0f);
+    float Pj[2][kS], Ej[2][kS];
 #pragma unroll
     for (int q = 0; q < (kTwo ? 2 : 1); ++q) {
       const int n = q ? n1 : n0;
       const float a2 = q ? a2w.y : a2w.x;
-      float Pj[kS], Hj[kS];
+      float Hj[kS];
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
-        Pj[j] = rsj[j] ? 0.0f : ex2(a2 * sdj[j]);
+        Pj[q][j] = rsj[j] ? 0.0f : ex2(a2 * sdj[j]);
         Hj[j] = sm.aggH[(j * N + n) * kTile + lane];
       }
       float x = 0.0f;
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
-        sm.aggH[(j * N + n) * kTile + lane] = x;
-        x = fmaf(Pj[j], x, Hj[j]);
+        Ej[q][j] = x;
+        x = fmaf(Pj[q][j], x, Hj[j]);
       }
       if (q) tot.y = x;
       else tot.x = x;
@@ -468,26 +472,29 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // stored at once: the next chunk of the tile may already be waiting
     if (!rs_any && publish)
       store_incl(make_float2(fmaf(ex2(a2w.x * sd_tot), x.x, tot.x), fmaf(ex2(a2w.y * sd_tot), x.y, tot.y)));
-    sm.hin[n0 * kTile + lane] = x.x;
-    if (kTwo) sm.hin[n1 * kTile + lane] = x.y;
+    // the exact state each sub-chunk starts from: its prefix plus the entering
+    // state carried over the sub-chunks before it (their factors' product, 0
+    // past a sequence start)
+#pragma unroll
+    for (int q = 0; q < (kTwo ? 2 : 1); ++q) {
+      const int n = q ? n1 : n0;
+      const float xin = q ? x.y : x.x;
+      float pp = 1.0f;
+#pragma unroll
+      for (int j = 0; j < kS; ++j) {
+        sm.aggH[(j * N + n) * kTile + lane] = fmaf(pp, xin, Ej[q][j]);
+        pp *= Pj[q][j];
+      }
+    }
   }
   __syncthreads();
 
   // ---- step 6: exact start state, pass 2
   int next = 0;  // thread 0: the next ticket, used once pass 2 is done
   if (tid == 0) next = (int)atomicAdd(a.ticket, 1u);
-  int rs_pre = 0;
-  float sd_pre = 0.0f;
-  for (int j = 0; j < s; ++j) {
-    rs_pre |= sm.aggRS[j];
-    sd_pre += sm.aggSD[j * kTile + lane];
-  }
 #pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const float2 E = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
-    const float2 R = make_float2(sm.hin[(2 * i) * kTile + lane], sm.hin[(2 * i + 1) * kTile + lane]);
-    h[i] = rs_pre ? E : fma2(ex2x2(mul2(A2[i], splat2(sd_pre))), R, E);
-  }
+  for (int i = 0; i < P; ++i)
+    h[i] = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
   const int64_t ts = t0 + tb;
   if (a.chunk_states && valid && ts < a.T && (ts % kStateChunk) == 0) {
     // layout [chunk][n][d]: the 32 lanes store 32 consecutive floats per state
