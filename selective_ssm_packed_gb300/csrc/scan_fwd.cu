@@ -49,26 +49,34 @@ constexpr int kThreads = kS * 32;
 constexpr int kHalo = 3;        // x rows before the chunk a fused conv of width <= 4 reads
 constexpr int kMaxW = 4;        // widest fused conv
 
+// Buffers of the inputs pass 2 reads (u, z, B, C, positions): two for bf16
+// I/O without the fused conv, so that the next work item's copies land while
+// pass 2 runs; one otherwise (the fp32 tiles and the conv's x tile leave no
+// room for a second CTA per SM with two).
+template <typename T, bool kConv>
+constexpr int fwd_buffers() { return (sizeof(T) == 2 && !kConv) ? 2 : 1; }
+
 template <typename T, int N, bool kConv>
 struct FwdSmem {
-  alignas(128) T u[kL * kTile];
+  static constexpr int NB = fwd_buffers<T, kConv>();
+  alignas(128) T u[NB][kL * kTile];
   // fused conv1d: x rows t0 - 3 .. t0 + 127 (by one tensor copy; rows before
   // the first token come back zero), the tile's weights (D, W) and bias
   alignas(128) T x[kConv ? (kL + kHalo) * kTile : 8];
   alignas(16) float cw[kConv ? kTile * kMaxW : 4];
   alignas(16) float cb[kConv ? kTile : 4];
   alignas(128) T dr[kL * kTile];
-  alignas(128) T z[kL * kTile];
+  alignas(128) T z[NB][kL * kTile];
   // B and C rows as fp32 (for bf16 I/O widened once per call, before the kernel)
-  alignas(128) float B[kL * N];
-  alignas(128) float C[kL * N];
+  alignas(128) float B[NB][kL * N];
+  alignas(128) float C[NB][kL * N];
   alignas(16) float dlt[kL * kTile];
   alignas(16) float aggH[kS * N * kTile];
   float aggSD[kS * kTile];
   alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
   alignas(16) float bias[kTile];
   alignas(16) float dsk[kTile];
-  alignas(16) int pos[kL];
+  alignas(16) int pos[NB][kL];
   int aggRS[kS];
   int ticket;
   alignas(8) uint64_t bar;
@@ -97,7 +105,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   // tiles; B and C rows; A rows, dt_bias, Dskip; position indices (whole
   // groups of 4 tokens).  With no item left, thread 0 arrives without data so
   // that the barrier still completes and tells every thread to stop.
-  auto issue = [&](int tkn) {
+  auto issue = [&](int tkn, int buf) {
     if (tkn >= n_items) {
       mbar_arrive(&sm.bar);
       return;
@@ -121,18 +129,18 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       bulk_load_1d(sm.cw, a.conv_w + (int64_t)dd0 * a.conv_W, nval * (uint32_t)a.conv_W * 4u, &sm.bar);
       if (a.conv_b) bulk_load_1d(sm.cb, a.conv_b + dd0, nval * 4u, &sm.bar);
     } else {
-      tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+      tma_load_2d(sm.u[buf], &tm_u, dd0, (int)tt0, &sm.bar);
     }
     tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
-    if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+    if (a.has_z) tma_load_2d(sm.z[buf], &tm_z, dd0, (int)tt0, &sm.bar);
     const float* Bsrc = sizeof(T) == 4 ? static_cast<const float*>(a.B) : a.Bf32;
     const float* Csrc = sizeof(T) == 4 ? static_cast<const float*>(a.C) : a.Cf32;
-    bulk_load_1d(sm.B, Bsrc + tt0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C, Csrc + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.B[buf], Bsrc + tt0 * N, bc, &sm.bar);
+    bulk_load_1d(sm.C[buf], Csrc + tt0 * N, bc, &sm.bar);
     bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
     if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
     if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
-    if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
+    if (rows4) bulk_load_1d(sm.pos[buf], a.pos + tt0, rows4 * 4u, &sm.bar);
   };
 
   if (tid == 0) {
@@ -140,13 +148,14 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     fence_mbar_init();
     const int first = (int)atomicAdd(a.ticket, 1u);
     sm.ticket = first;
-    issue(first);
+    issue(first, 0);
   }
   __syncthreads();
 
   // Persistent loop: one work item per pass.  The next ticket is drawn when
   // pass 2 starts, so that the atomic's round trip overlaps pass 2, and its
-  // copies are requested at the end of pass 2, when the inputs are free.  A
+  // copies are requested halfway through pass 2 into the other buffer set
+  // (two buffers), or at the end of pass 2, when the inputs are free (one).  A
   // draw at the start of the item would hold tickets back from the look-back
   // chains (an item whose neighbour sits reserved behind a running item waits
   // for both); pass 2 waits on nothing, so a ticket held through it is not
@@ -173,6 +182,12 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const int chunk = tk / a.n_tiles;
   const int tile = tk - chunk * a.n_tiles;
   const int64_t t0 = (int64_t)chunk * kL;
+  // this item's buffers of the double-buffered inputs
+  constexpr int kNB = SM::NB;
+  const int buf = kNB == 2 ? (int)(it & 1u) : 0;
+  T* const su = sm.u[buf];
+  const T* const sz = sm.z[buf];
+  const int* const spos = sm.pos[buf];
   const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
   const int rows4 = rows & ~3;
   const int d0 = tile * kTile;
@@ -184,9 +199,9 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const float Dsk = (valid && a.Dskip) ? sm.dsk[lane] : 0.0f;
   // position index of token t < rows of the chunk (the last chunk's ragged
   // tail, past the last whole group of 4, is read from global memory)
-  auto pos_at = [&](int t) { return t < rows4 ? sm.pos[t] : __ldg(a.pos + t0 + t); };
+  auto pos_at = [&](int t) { return t < rows4 ? spos[t] : __ldg(a.pos + t0 + t); };
   // fused conv1d: tap k (k tokens back) of this lane's channel; zero past W
-  float tapw[kMaxW], cbias = 0.0f;
+  float tapw[kMaxW] = {0.0f, 0.0f, 0.0f, 0.0f}, cbias = 0.0f;
   if constexpr (kConv) {
 #pragma unroll
     for (int k = 0; k < kMaxW; ++k) tapw[k] = (valid && k < a.conv_W) ? sm.cw[lane * a.conv_W + a.conv_W - 1 - k] : 0.0f;
@@ -202,7 +217,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     for (int k = 1; k < kMaxW; ++k)
       if (k < a.conv_W && p >= k) pre = fmaf(tapw[k], to_f(xr[-k * bx]), pre);
     const T ot = from_f<T>(a.conv_silu ? siluf(pre) : pre);
-    sm.u[t * bx + lane] = ot;
+    su[t * bx + lane] = ot;
     if (a.u_out && valid) static_cast<T*>(a.u_out)[(t0 + t) * a.D + d] = ot;
   };
   // the state a sequence starting at token t (of the chunk) starts from: its
@@ -241,8 +256,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   };
 
   const int tb = s * kK;  // first token (within the chunk) of this thread
-  const float* Bf = sm.B;
-  const float* Cf = sm.C;
+  const float* Bf = sm.B[buf];
+  const float* Cf = sm.C[buf];
   float2 A2[P];
   if (valid) {
     load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, a.a_log ? 1.0f : kLog2e);
@@ -280,7 +295,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const bool whole = tb + kK <= rows && bx == kTile;
   if (whole) {
     const T* const drp = sm.dr + tb * kTile + lane;
-    const T* const up = sm.u + tb * kTile + lane;
+    const T* const up = su + tb * kTile + lane;
     float* const dlp = sm.dlt + tb * kTile + lane;
     const float* const bp = Bf + tb * N;
     // groups of 8 tokens, unrolled; the loop over the groups keeps the body
@@ -320,7 +335,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       sd = 0.0f;
       rs = 1;
     }
-    const float2 dl2 = splat2(dl), du2 = splat2(dl * to_f(sm.u[t * bx + lane]));
+    const float2 dl2 = splat2(dl), du2 = splat2(dl * to_f(su[t * bx + lane]));
     float2 Bv[P];
     lds_pairs<N>(Bv, Bf + t * N);
 #pragma unroll
@@ -490,8 +505,20 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   __syncthreads();
 
   // ---- step 6: exact start state, pass 2
-  int next = 0;  // thread 0: the next ticket, used once pass 2 is done
+  int next = 0;  // thread 0: the next ticket
   if (tid == 0) next = (int)atomicAdd(a.ticket, 1u);
+  // with two buffers, thread 0 requests the next item's inputs halfway
+  // through pass 2 (the ticket's round trip is over by then): the single
+  // buffers (delta_raw, A rows, dt_bias, Dskip) were read before pass 2, the
+  // other buffer set by the item before this one
+  bool issued = false;
+  auto issue_next = [&]() {
+    if (kNB == 2 && tid == 0 && !issued) {
+      sm.ticket = next;
+      issue(next, buf ^ 1);
+      issued = true;
+    }
+  };
 #pragma unroll
   for (int i = 0; i < P; ++i)
     h[i] = make_float2(sm.aggH[(s * N + 2 * i) * kTile + lane], sm.aggH[(s * N + 2 * i + 1) * kTile + lane]);
@@ -509,8 +536,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   T* out = static_cast<T*>(a.out);
   T* ypre = static_cast<T*>(a.y);  // the output before the gate (nullable)
   if (whole) {
-    const T* const up = sm.u + tb * kTile + lane;
-    const T* const zp = sm.z + tb * kTile + lane;
+    const T* const up = su + tb * kTile + lane;
+    const T* const zp = sz + tb * kTile + lane;
     const float* const dlp = sm.dlt + tb * kTile + lane;
     const float* const bp = Bf + tb * N;
     const float* const cp = Cf + tb * N;
@@ -550,6 +577,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       if (valid) *op = from_f<T>(y);
       op += a.D;
     }
+    if (kg == 0) issue_next();
     }
     if constexpr (kStates) {
       if (a.h_final && seq_end(tb + kK - 1)) end_state(h, tb + kK - 1);
@@ -561,7 +589,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (t >= rows) break;
     if (pos_at(t) == 0) start_state(h, t);
     const float dl = sm.dlt[t * kTile + lane];
-    const float uu = to_f(sm.u[t * bx + lane]);
+    const float uu = to_f(su[t * bx + lane]);
     const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
     float2 Bv[P], Cv[P];
     lds_pairs<N>(Bv, Bf + t * N);
@@ -574,7 +602,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     float y = fmaf(Dsk, uu, y2.x + y2.y);
     if (ypre && valid) ypre[(t0 + t) * a.D + d] = from_f<T>(y);
-    if (a.has_z) y *= siluf(to_f(sm.z[t * bx + lane])) + a.gate_floor;
+    if (a.has_z) y *= siluf(to_f(sz[t * bx + lane])) + a.gate_floor;
     if (valid) out[(t0 + t) * a.D + d] = from_f<T>(y);
     if constexpr (kStates) {
       if (a.h_final && seq_end(t)) end_state(h, t);
@@ -582,11 +610,15 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   }
   }
 
-  // every input of this item has been read: request the next one's
-  __syncthreads();
-  if (tid == 0) {
-    sm.ticket = next;
-    issue(next);
+  if constexpr (kNB == 2) {
+    issue_next();  // the ragged paths: at the end of pass 2
+  } else {
+    // every input of this item has been read: request the next one's
+    __syncthreads();
+    if (tid == 0) {
+      sm.ticket = next;
+      issue(next, 0);
+    }
   }
   }  // persistent loop
 }
