@@ -26,8 +26,9 @@
 //
 //   1. Per-(token, channel) values once per item: delta (softplus), delta u,
 //      g, d delta / d delta_raw into [channel pair][token] arrays, and dz from
-//      the forward's pre-gate output y (so the gate is evaluated once); B and C
-//      doubled per state pair; a per-token exponent offset (-inf at a start).
+//      the forward's pre-gate output y (so the gate is evaluated once); a
+//      per-token exponent offset (-inf at a start).  B and C arrive doubled
+//      per state pair, built once per call for every item (launch_double_bc).
 //   2. Forward walk per thread from the saved state of the chunk: p_t goes to
 //      TENSOR MEMORY (4 words per token, 128 columns per warp) for the reverse
 //      walk, so the history costs no registers; the left-going carry aggregate
