@@ -365,7 +365,22 @@ int vssm_checks_build(void);
  * the training of gated models describes how such a failure otherwise stays
  * silent until the loss shows it. */
 #define VSSM_DBG_CHECK_FINITE 6
+/* VSSM_DBG_KERNEL_EVENTS: 1 makes the conv and scan calls record a CUDA event
+ * pair on their stream around their main kernel (the conv1d tile kernel, the
+ * scan kernel; not the calls' memsets, operand staging or fixed-order sums),
+ * so that a benchmark can time the kernels alone while it times the calls; 0
+ * (the default) records nothing and drops what was recorded.  Read the
+ * totals with vssm_kernel_time. */
+#define VSSM_DBG_KERNEL_EVENTS 7
 int vssm_debug_set(int knob, int64_t value);
+
+/* Total device time (ms) and number of launches of the main kernel of one
+ * kind of call since the last read, from the events VSSM_DBG_KERNEL_EVENTS
+ * records: kind 0 varlen_conv1d_fwd, 1 varlen_selective_scan_fwd (and the
+ * fused call), 2 varlen_selective_scan_bwd, 3 varlen_conv1d_bwd.  Waits for
+ * the recorded events to complete, then forgets them.  Returns VSSM_OK,
+ * VSSM_ERR_ARG (bad kind or NULL pointers) or VSSM_ERR_CUDA. */
+int vssm_kernel_time(int kind, double* total_ms, int64_t* launches);
 
 #ifdef __cplusplus
 }

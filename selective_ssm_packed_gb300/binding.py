@@ -21,7 +21,9 @@ from . import build as _build
 VSSM_F32, VSSM_BF16 = 0, 1
 VSSM_STATE_CHUNK = 32
 VSSM_DBG_DROP_FLAG, VSSM_DBG_WAIT_NS, VSSM_DBG_DELAY_ITEM, VSSM_DBG_DELAY_NS = 1, 2, 3, 4
-VSSM_DBG_FORCE_COPY_TIMEOUT, VSSM_DBG_CHECK_FINITE = 5, 6
+VSSM_DBG_FORCE_COPY_TIMEOUT, VSSM_DBG_CHECK_FINITE, VSSM_DBG_KERNEL_EVENTS = 5, 6, 7
+# the call kinds vssm_kernel_time reports
+KERNEL_KINDS = {"conv_fwd": 0, "scan_fwd": 1, "scan_bwd": 2, "conv_bwd": 3}
 ERR = {0: "VSSM_OK", -1: "VSSM_ERR_ARG", -2: "VSSM_ERR_DTYPE", -3: "VSSM_ERR_ALIGN",
        -4: "VSSM_ERR_WORKSPACE", -5: "VSSM_ERR_CUDA", -6: "VSSM_ERR_UNSUPPORTED",
        -16: "VSSM_ERR_BAD_CU_SEQLENS", -17: "VSSM_ERR_LOOKBACK_TIMEOUT", -18: "VSSM_ERR_NONFINITE",
@@ -65,6 +67,8 @@ SIGNATURES = {
     "vssm_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "vssm_last_error": (ctypes.c_char_p, []),
     "vssm_checks_build": (ctypes.c_int, []),
+    "vssm_kernel_time": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_int64)]),
     "vssm_debug_set": (ctypes.c_int, [ctypes.c_int, _i64]),
 }
 
@@ -154,6 +158,14 @@ def read_status(workspace: torch.Tensor, stream=None) -> int:
     _check(lib().vssm_read_status(_ptr(workspace, "workspace"), _stream(stream), ctypes.byref(st)),
            "vssm_read_status")
     return st.value
+
+
+def kernel_time(kind: str):
+    """(total ms, launches) of one kind of call's main kernel since the last
+    read, from the events VSSM_DBG_KERNEL_EVENTS records."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_int64(0)
+    _check(lib().vssm_kernel_time(KERNEL_KINDS[kind], ctypes.byref(ms), ctypes.byref(n)), "vssm_kernel_time")
+    return ms.value, n.value
 
 
 def status_code(word: int) -> int:

@@ -11,6 +11,8 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "kernels.h"
 #include "varlen_ssm.h"
@@ -26,6 +28,32 @@ std::atomic<long long> g_delay_ticket{-1};
 std::atomic<unsigned long long> g_delay_ns{200000ull};
 std::atomic<long long> g_force_copy_timeout{-1};
 std::atomic<int> g_check_finite{0};
+std::atomic<int> g_kernel_events{0};
+
+// The recorded event pairs of each kind of main kernel, and a pool of events
+// to reuse (created on first use).
+struct KernelTimer {
+  std::mutex mu;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pairs[vssm::kTimeKinds];
+  cudaEvent_t open[vssm::kTimeKinds] = {};
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t take() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+  }
+  void give(cudaEvent_t e) {
+    if (e) pool.push_back(e);
+  }
+};
+KernelTimer& kernel_timer() {
+  static KernelTimer t;
+  return t;
+}
 
 // An NVTX range over a C-ABI call (host side: the call's enqueue), named
 // after the call, for timelines taken with a profiler.
@@ -258,6 +286,27 @@ int check_states_rows(bool any_states, int32_t num_seqs, int64_t T) {
 
 }  // namespace
 
+void vssm::kernel_timer_mark(int kind, bool begin, cudaStream_t st) {
+  if (!g_kernel_events.load() || kind < 0 || kind >= kTimeKinds) return;
+  KernelTimer& kt = kernel_timer();
+  std::lock_guard<std::mutex> lock(kt.mu);
+  cudaEvent_t e = kt.take();
+  if (!e) return;
+  if (cudaEventRecord(e, st) != cudaSuccess) {
+    kt.give(e);
+    return;
+  }
+  if (begin) {
+    kt.give(kt.open[kind]);  // an unmatched begin is dropped
+    kt.open[kind] = e;
+  } else if (kt.open[kind]) {
+    kt.pairs[kind].emplace_back(kt.open[kind], e);
+    kt.open[kind] = nullptr;
+  } else {
+    kt.give(e);
+  }
+}
+
 // Lets other translation units of the library report a host-side error
 // through vssm_last_error().
 int vssm::record_error(int code, const char* message) {
@@ -328,6 +377,32 @@ const char* vssm_last_error(void) { return g_last_error.c_str(); }
 
 int vssm_checks_build(void) { return VSSM_CHECKS ? 1 : 0; }
 
+int vssm_kernel_time(int kind, double* total_ms, int64_t* launches) {
+  if (kind < 0 || kind >= kTimeKinds || !total_ms || !launches) return fail(VSSM_ERR_ARG, "bad kind or NULL output");
+  KernelTimer& kt = kernel_timer();
+  std::lock_guard<std::mutex> lock(kt.mu);
+  double ms = 0.0;
+  int64_t n = 0;
+  cudaError_t err = cudaSuccess;
+  for (auto& pr : kt.pairs[kind]) {
+    float t = 0.0f;
+    cudaError_t e = cudaEventSynchronize(pr.second);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, pr.first, pr.second);
+    if (e == cudaSuccess) {
+      ms += t;
+      ++n;
+    } else if (err == cudaSuccess) {
+      err = e;
+    }
+    kt.give(pr.first);
+    kt.give(pr.second);
+  }
+  kt.pairs[kind].clear();
+  *total_ms = ms;
+  *launches = n;
+  return err == cudaSuccess ? VSSM_OK : cuda_fail(err, "kernel event timing");
+}
+
 int vssm_debug_set(int knob, int64_t value) {
   if (knob == VSSM_DBG_DROP_FLAG) { g_drop_ticket.store(value); return VSSM_OK; }
   if (knob == VSSM_DBG_WAIT_NS) {
@@ -342,6 +417,24 @@ int vssm_debug_set(int knob, int64_t value) {
     return VSSM_OK;
   }
   if (knob == VSSM_DBG_FORCE_COPY_TIMEOUT) { g_force_copy_timeout.store(value); return VSSM_OK; }
+  if (knob == VSSM_DBG_KERNEL_EVENTS) {
+    if (value != 0 && value != 1) return fail(VSSM_ERR_ARG, "VSSM_DBG_KERNEL_EVENTS takes 0 or 1");
+    g_kernel_events.store((int)value);
+    if (!value) {  // drop what was recorded (completed or not: events are reusable once recorded over)
+      KernelTimer& kt = kernel_timer();
+      std::lock_guard<std::mutex> lock(kt.mu);
+      for (int k = 0; k < kTimeKinds; ++k) {
+        for (auto& pr : kt.pairs[k]) {
+          kt.give(pr.first);
+          kt.give(pr.second);
+        }
+        kt.pairs[k].clear();
+        kt.give(kt.open[k]);
+        kt.open[k] = nullptr;
+      }
+    }
+    return VSSM_OK;
+  }
   if (knob == VSSM_DBG_CHECK_FINITE) {
     if (value != 0 && value != 1) return fail(VSSM_ERR_ARG, "VSSM_DBG_CHECK_FINITE takes 0 or 1");
     g_check_finite.store((int)value);
@@ -435,7 +528,9 @@ int varlen_conv1d_fwd(const void* x, const float* weight, const float* bias,
   const int bx = D < conv_tile_cols() ? D : conv_tile_cols();
   CUtensorMap mx;
   VSSM_TRY(make_map(&mx, x, io, total_tokens, D, bx, conv_tile_rows(W, false, true)));
+  kernel_timer_mark(kTimeConvFwd, true, st);
   e = launch_conv1d_fwd(a, io, mx, st);
+  kernel_timer_mark(kTimeConvFwd, false, st);
   if (e != cudaSuccess) return cuda_fail(e, "conv1d_fwd launch");
   const bool f = io == IO::F32;
   return check_outputs(a.status, st, {{u, total_tokens * D, f}});

@@ -498,7 +498,9 @@ cudaError_t launch_conv1d_bwd(const ConvArgs& a, IO io, const CUtensorMap& tm_x,
                               float* dweight, float* dbias, cudaStream_t st) {
   const int64_t P = conv_bwd_partial_rows(a.T);
   if (a.T > 0) {
+    kernel_timer_mark(kTimeConvBwd, true, st);
     cudaError_t e = io == IO::F32 ? bwd_t<float>(a, tm_x, tm_du, st) : bwd_t<__nv_bfloat16>(a, tm_x, tm_du, st);
+    kernel_timer_mark(kTimeConvBwd, false, st);
     if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = cudaMemsetAsync(a.partial, 0, sizeof(float) * (size_t)a.D * (a.W + 1), st);

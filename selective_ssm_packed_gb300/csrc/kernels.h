@@ -176,6 +176,12 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_y, float* dA,
                             float* dB, float* dC, float* dDskip, float* d_dt_bias, cudaStream_t st);
 
+// Kernel timing (VSSM_DBG_KERNEL_EVENTS): when it is on, the calls record a
+// CUDA event pair on their stream around their main kernel, kind 0 conv1d
+// fwd, 1 scan fwd, 2 scan bwd, 3 conv1d bwd.  No-ops when off.
+enum : int { kTimeConvFwd = 0, kTimeScanFwd = 1, kTimeScanBwd = 2, kTimeConvBwd = 3, kTimeKinds = 4 };
+void kernel_timer_mark(int kind, bool begin, cudaStream_t st);
+
 // Sets the message vssm_last_error() returns on this thread; returns `code`.
 int record_error(int code, const char* message);
 

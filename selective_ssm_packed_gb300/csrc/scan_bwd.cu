@@ -1450,8 +1450,10 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
   cudaError_t e = launch_double_bc(a.B, a.C, io, a.T, (int64_t)a.n_chunks * kBwdChunk, a.N,
                                    const_cast<float4*>(a.BD), const_cast<float4*>(a.CD), st);
   if (e != cudaSuccess) return e;
+  kernel_timer_mark(kTimeScanBwd, true, st);
   e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
                     : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st);
+  kernel_timer_mark(kTimeScanBwd, false, st);
   if (e != cudaSuccess) return e;
   const int64_t M = a.T * 2 * a.N;
   // partial rows come in groups of 32 channels: two per tile when N = 16

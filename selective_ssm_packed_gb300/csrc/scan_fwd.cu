@@ -672,8 +672,11 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
     if (e == cudaSuccess) e = launch_widen_bf16(a.C, const_cast<float*>(a.Cf32), a.T * a.N, st);
     if (e != cudaSuccess) return e;
   }
-  return io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, st)
-                       : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, st);
+  kernel_timer_mark(kTimeScanFwd, true, st);
+  const cudaError_t e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, st)
+                                      : launch_t<__nv_bfloat16>(a, tm_u, tm_dr, tm_z, st);
+  kernel_timer_mark(kTimeScanFwd, false, st);
+  return e;
 }
 
 }  // namespace vssm

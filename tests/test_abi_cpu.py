@@ -132,3 +132,9 @@ def test_debug_knobs(lib):
     assert lib.vssm_debug_set(binding.VSSM_DBG_FORCE_COPY_TIMEOUT, -1) == 0
     assert lib.vssm_debug_set(binding.VSSM_DBG_CHECK_FINITE, 2) == -1
     assert lib.vssm_debug_set(binding.VSSM_DBG_CHECK_FINITE, 0) == 0
+    assert lib.vssm_debug_set(binding.VSSM_DBG_KERNEL_EVENTS, 3) == -1
+    assert lib.vssm_debug_set(binding.VSSM_DBG_KERNEL_EVENTS, 0) == 0
+    assert binding.kernel_time("scan_bwd") == (0.0, 0)  # nothing recorded
+    import ctypes
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    assert lib.vssm_kernel_time(9, ctypes.byref(ms), ctypes.byref(n)) == -1

@@ -120,3 +120,39 @@ def test_checked_build_gives_the_same_results_and_reports_bad_position_indices()
     r = subprocess.run([sys.executable, os.path.join(HERE, "checked_build_child.py")], env=env,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout[-3000:] + r.stderr[-3000:]
+
+
+def test_kernel_event_timing_counts_each_main_kernel():
+    """VSSM_DBG_KERNEL_EVENTS: each call records one event pair around its
+    main kernel; vssm_kernel_time returns the launches and their time, then
+    forgets them; with the knob off nothing is recorded."""
+    lengths = [300, 1, 77]
+    D, N, W = 64, 16, 4
+    cu_np = workloads.cu_seqlens_from_lengths(lengths)
+    T = int(cu_np[-1])
+    r = workloads.draw_values(T, D, N, W, 63, scan_input=True, params="general")
+    cu = torch.from_numpy(cu_np).cuda()
+    pos = vs.varlen_position_indices(cu, T)
+    bf = lambda k: _dv(r[k]).to(torch.bfloat16)  # noqa: E731
+    args = dict(delta_raw=bf("delta_raw"), A=_dv(r["A"]), B=bf("B"), C=bf("C"), Dskip=_dv(r["Dskip"]),
+                z=bf("z"), dt_bias=_dv(r["dt_bias"]))
+    try:
+        binding.debug_set(binding.VSSM_DBG_KERNEL_EVENTS, 1)
+        for _ in range(3):
+            out, states = vs.varlen_selective_scan_fwd(bf("u"), **args, cu_seqlens=cu, position_indices=pos)
+        vs.varlen_selective_scan_bwd(bf("u"), **args, dout=bf("dout"), cu_seqlens=cu, chunk_states=states,
+                                     position_indices=pos)
+        vs.varlen_conv1d_fwd(bf("x"), _dv(r["conv_w"]), _dv(r["conv_b"]), cu, pos)
+        ms, n = binding.kernel_time("scan_fwd")
+        assert n == 3 and ms > 0.0
+        ms, n = binding.kernel_time("scan_bwd")
+        assert n == 1 and ms > 0.0
+        ms, n = binding.kernel_time("conv_fwd")
+        assert n == 1 and ms > 0.0
+        assert binding.kernel_time("scan_fwd") == (0.0, 0)  # read and forgotten
+        assert binding.kernel_time("conv_bwd") == (0.0, 0)  # never launched
+    finally:
+        binding.debug_set(binding.VSSM_DBG_KERNEL_EVENTS, 0)
+    vs.varlen_selective_scan_fwd(bf("u"), **args, cu_seqlens=cu, position_indices=pos)
+    torch.cuda.synchronize()
+    assert binding.kernel_time("scan_fwd") == (0.0, 0)
