@@ -1144,6 +1144,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
 #pragma unroll
       for (int e = kRB - 1; e >= 0; --e) {
         const int tt = blk * kRB + e;
+        // the previous block's dB sum, long since complete
+        if (e == kRB - 2 && pendB_t < rows) pdB[pendB_t] = pendB;
         const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
         const float4 of4 = sm.off[tt >> 1];
         const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
@@ -1199,7 +1201,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
 #pragma unroll
         for (int q = 0; q < 2; ++q) wv[q] = hsum(fma2(dup[1], dh[q][1], mul2(dup[0], dh[q][0])));
         // dB contributions dh_t delta u over the quad's channels, then over the
-        // group's; stored after the block's barrier (no stall on the shuffles)
+        // group's; stored during the next block (no stall on the shuffles)
         if (colsum.feed(e, false, wv[0], wv[1], lane, &pendB)) pendB_t = blk * kRB + ColSum4::token(lane);
         if constexpr (kStates) {
           if (((evG >> tt) & 1u) && valid &&
@@ -1232,8 +1234,6 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       const int e = tg >> 4, cpl = tg & 15;
       const int cp = 16 * grp + cpl, hh = cp & 1, qd = cp >> 1;
       const int t = blk * kRB + e;
-      if (pendB_t < rows) pdB[pendB_t] = pendB;
-      pendB_t = kL;
       float4 pv[kSP];
 #pragma unroll
       for (int v = 0; v < kSP; ++v) pv[v] = sm.nred[nred_at(buf, e, v, hh, qd)];
@@ -1271,27 +1271,37 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       }
       accB = __fadd2_rn(accB, ddr);
     };
-    uint32_t hb0[32], hb1[32];
+    // one block of history in registers: the next block's load is issued once
+    // the walk has used the current one.  Block k + 1 is finalized after the
+    // walk over block k (its n-sums are complete since the barrier that ended
+    // that walk's predecessor); the barrier after the finalize also frees
+    // block k + 1's n-sum buffer for block k - 1.
+    uint32_t hb[32];
     __syncwarp();
-    tmem_ld32(thist + 32 * (kL / kRB - 1), hb1);
-    tmem_wait_ld32(hb1);
+    tmem_ld32(thist + 32 * (kL / kRB - 1), hb);
+    tmem_wait_ld32(hb);
+    block(std::integral_constant<int, 1>{}, kL / (2 * kRB) - 1, hb);
+    __syncwarp();
+    tmem_ld32(thist + 32 * (kL / kRB - 2), hb);
+    named_barrier(1 + grp, 64);
 #pragma unroll 1
     for (int bp = kL / (2 * kRB) - 1; bp >= 0; --bp) {
+      tmem_wait_ld32(hb);
+      block(std::integral_constant<int, 0>{}, bp, hb);
       __syncwarp();
-      tmem_ld32(thist + 32 * (2 * bp), hb0);
-      block(std::integral_constant<int, 1>{}, bp, hb1);
-      __syncwarp();
-      tmem_wait_ld32(hb0);
-      named_barrier(1 + grp, 64);  // the group's partials of the block are complete
+      if (bp > 0) tmem_ld32(thist + 32 * (2 * bp - 1), hb);
       finalize(2 * bp + 1);
-      __syncwarp();
-      if (bp > 0) tmem_ld32(thist + 32 * (2 * bp - 1), hb1);
-      block(std::integral_constant<int, 0>{}, bp, hb0);
-      __syncwarp();
-      if (bp > 0) tmem_wait_ld32(hb1);
       named_barrier(1 + grp, 64);
+      if (bp == 0) break;
+      tmem_wait_ld32(hb);
+      block(std::integral_constant<int, 1>{}, bp - 1, hb);
+      __syncwarp();
+      tmem_ld32(thist + 32 * (2 * bp - 2), hb);
       finalize(2 * bp);
+      named_barrier(1 + grp, 64);
     }
+    finalize(0);
+    if (pendB_t < rows) pdB[pendB_t] = pendB;
   }
 
   // ---- 5. dA partials ([chunk][n][d]); fixed-order CTA sums of dDskip, d_dt_bias
