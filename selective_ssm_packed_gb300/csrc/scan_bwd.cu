@@ -686,13 +686,16 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // groups (warps 2g, 2g+1 take the channels 32g .. 32g+31).  A thread owns a
 // channel quad q of its group (channels 4q .. 4q+3: two pairs for the paired
 // FP32 instructions) and a state pair p of its warp's four (p = 4 (w % 2) ..
-// +3): eight (channel, state) chains; the lane map is given in the kernel.  Against the pair-by-pair layout above, every
-// per-token value a thread loads serves twice the chains, the channel sums for
-// dB / dC start over 4 channels in registers, and the history takes 8 words
-// per token (256 tensor-memory columns per warp, 2 CTAs per SM).  The partial
+// +3): eight (channel, state) chains; the lane map is given in the kernel.
+// Against the pair-by-pair layout above, every per-token value a thread
+// loads serves twice the chains, the channel sums for dB / dC start over 4
+// channels in registers, and the history takes 8 words per token (256
+// tensor-memory columns per warp, 2 CTAs per SM).  The partial
 // sums over state pairs for du / d delta_raw come from the two warps of a
 // channel group only, so a block's epilogue waits on a 64-thread named
-// barrier, not on the whole CTA.
+// barrier, not on the whole CTA; each block is finalized after the walk over
+// the next one.  The next item's copies are split over the four warps (the
+// barrier takes four arrivals).
 constexpr int kTW = 2 * kTile;  // 64 channels per work item
 constexpr int kCQ = kTW / 4;    // 16 channel quads
 constexpr int kQT = kL + 1;     // token pitch (float4) of the [channel quad][token] arrays
@@ -812,7 +815,11 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   const int nF = 2 * sp + o, nS = 2 * sp + 1 - o;  // its "first" and "second" state
   const int c0 = 4 * cq;                           // first channel of the quad (in the tile)
 
-  auto issue = [&](int tkn) {
+  // The item's twelve copies, split over the four warps: lane 0 of warp wq
+  // posts its share's bytes on the barrier (which expects four arrivals) and
+  // issues its three copies.  One thread issuing all twelve in turn spent
+  // about 1.4k cycles on them while the rest of the CTA waited.
+  auto issue = [&](int tkn, int wq) {
     const int rv = tkn / a.n_tiles;
     const int tl = tkn - rv * a.n_tiles;
     const int ch = a.n_chunks - 1 - rv;
@@ -823,36 +830,41 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     const uint32_t bcd = (uint32_t)kL * N * 16u;  // the chunk's doubled B (or C) rows
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    mbar_arrive_expect_tx(&sm.bar, box * (3u + (a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + 2u * bcd + nval * N * 4u +
-                                       (uint32_t)a.box_x * N * 4u + rows4 * 4u +
-                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
-    tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
-    tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
-    tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
-    if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
-    if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
-    bulk_load_1d(sm.BD, a.BD + tt0 * N, bcd, &sm.bar);
-    bulk_load_1d(sm.CD, a.CD + tt0 * N, bcd, &sm.bar);
-    bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
-    tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
-    if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
-    if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
-    if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
+    if (wq == 0) {
+      mbar_arrive_expect_tx(&sm.bar, 3u * box);
+      tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
+      tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
+      tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
+    } else if (wq == 1) {
+      mbar_arrive_expect_tx(&sm.bar, box * ((a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + (uint32_t)a.box_x * N * 4u);
+      if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+      if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
+      tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
+    } else if (wq == 2) {
+      mbar_arrive_expect_tx(&sm.bar, 2u * bcd + rows4 * 4u);
+      bulk_load_1d(sm.BD, a.BD + tt0 * N, bcd, &sm.bar);
+      bulk_load_1d(sm.CD, a.CD + tt0 * N, bcd, &sm.bar);
+      if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
+    } else {
+      mbar_arrive_expect_tx(&sm.bar, nval * N * 4u + (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
+      bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
+      if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
+      if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
+    }
   };
 
   // tensor memory for the forward walk's history: 256 columns, warp w on the
   // lanes 32 w .. 32 w + 31
   if (w == 0) tmem_alloc256(&sm.taddr);
   if (tid == 0) {
-    mbar_init(&sm.bar, 1);
+    mbar_init(&sm.bar, 4);
     fence_mbar_init();
-    const int first = (int)atomicAdd(a.ticket, 1u);
-    sm.ticket = first;
-    if (first < n_items) issue(first);
+    sm.ticket = (int)atomicAdd(a.ticket, 1u);
   }
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
+  if (lane == 0 && sm.ticket < n_items) issue(sm.ticket, w);
   const uint32_t thist = sm.taddr + ((uint32_t)(32 * w) << 16);
 
   for (uint32_t it = 0;; ++it) {
@@ -1139,7 +1151,9 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     auto block = [&](auto parity, int bp, uint32_t (&hb)[32]) {
       constexpr int buf = decltype(parity)::value;
       const int blk = 2 * bp + buf;
-      if (blk == 0 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
+      // the next ticket, drawn a block ahead of the tail so that its round
+      // trip is over when the tail hands it to the copies
+      if (blk == 1 && tid == 0) next = (int)atomicAdd(a.ticket, 1u);
       ColSum4 colsum;
 #pragma unroll
       for (int e = kRB - 1; e >= 0; --e) {
@@ -1155,7 +1169,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const float2 Cq = q ? hi2(cd) : lo2(cd);
-          const int n = q ? nS : nF;
+          [[maybe_unused]] const int n = q ? nS : nF;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const float2 p = make_float2(bitsf(hb[8 * e + 4 * q + 2 * j]), bitsf(hb[8 * e + 4 * q + 2 * j + 1]));
@@ -1318,11 +1332,9 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   }
   sm.redD[tid] = accD;
   sm.redB[tid] = accB;
+  if (tid == 0) sm.ticket = next;
   __syncthreads();
-  if (tid == 0) {
-    sm.ticket = next;
-    if (next < n_items) issue(next);
-  }
+  if (lane == 0 && sm.ticket < n_items) issue(sm.ticket, w);
   if (tid < kCQ && 4 * tid < bx && d0 + 4 * tid < a.D) {
     // dDskip: phase-1 quad q = tid % 16 of every thread, in thread order
     float4 sD = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
