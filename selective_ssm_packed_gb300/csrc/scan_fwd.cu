@@ -101,11 +101,16 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
   const int n_items = a.n_chunks * a.n_tiles;
 
-  // Requests every input of work item `tkn` on the barrier: u, delta_raw, z
-  // tiles; B and C rows; A rows, dt_bias, Dskip; position indices (whole
-  // groups of 4 tokens).  With no item left, thread 0 arrives without data so
-  // that the barrier still completes and tells every thread to stop.
-  auto issue = [&](int tkn, int buf) {
+  // Requests warp wq's share of the inputs of work item `tkn` on the barrier,
+  // which expects one arrival per warp: lane 0 of each warp posts its share's
+  // bytes and issues its copies (one thread issuing all of them in turn held
+  // its warp, and the CTA behind it, for about a thousand cycles).  Shares:
+  // 0 the u tile (the fused conv: the x tile, weights and bias) and the
+  // position indices (whole groups of 4 tokens), 1 delta_raw, 2 z, 3 B rows,
+  // 4 C rows, 5 A rows, 6 dt_bias, 7 Dskip.  With no item left, every warp
+  // arrives without data, so that the barrier still completes and tells
+  // every thread to stop.
+  auto issue = [&](int tkn, int buf, int wq) {
     if (tkn >= n_items) {
       mbar_arrive(&sm.bar);
       return;
@@ -117,53 +122,67 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int dd0 = tl * kTile;
     const uint32_t nval = (uint32_t)(a.D - dd0 < kTile ? a.D - dd0 : kTile);
     const uint32_t bc = (uint32_t)nrows * N * 4u;
-    const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
-    // the fused conv's x box has kHalo more rows, and its weights and bias come along
-    const uint32_t ubox = kConv ? (uint32_t)a.box_x * (uint32_t)(a.box_y + kHalo) * sizeof(T) : box;
-    const uint32_t conv_bytes = kConv ? nval * (uint32_t)a.conv_W * 4u + (a.conv_b ? nval * 4u : 0u) : 0u;
-    mbar_arrive_expect_tx(&sm.bar, ubox + box * (a.has_z ? 2u : 1u) + 2u * bc + nval * N * 4u + rows4 * 4u +
-                                       (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u) + conv_bytes);
-    if constexpr (kConv) {
-      tma_load_2d(sm.x, &tm_u, dd0, (int)tt0 - kHalo, &sm.bar);
-      bulk_load_1d(sm.cw, a.conv_w + (int64_t)dd0 * a.conv_W, nval * (uint32_t)a.conv_W * 4u, &sm.bar);
-      if (a.conv_b) bulk_load_1d(sm.cb, a.conv_b + dd0, nval * 4u, &sm.bar);
+    if (wq == 0) {
+      const uint32_t rows4 = (uint32_t)nrows & ~3u;
+      if constexpr (kConv) {
+        // the fused conv's x box has kHalo more rows
+        const uint32_t xbox = (uint32_t)a.box_x * (uint32_t)(a.box_y + kHalo) * sizeof(T);
+        const uint32_t wbytes = nval * (uint32_t)a.conv_W * 4u;
+        mbar_arrive_expect_tx(&sm.bar, xbox + wbytes + (a.conv_b ? nval * 4u : 0u) + rows4 * 4u);
+        tma_load_2d(sm.x, &tm_u, dd0, (int)tt0 - kHalo, &sm.bar);
+        bulk_load_1d(sm.cw, a.conv_w + (int64_t)dd0 * a.conv_W, wbytes, &sm.bar);
+        if (a.conv_b) bulk_load_1d(sm.cb, a.conv_b + dd0, nval * 4u, &sm.bar);
+      } else {
+        mbar_arrive_expect_tx(&sm.bar, box + rows4 * 4u);
+        tma_load_2d(sm.u[buf], &tm_u, dd0, (int)tt0, &sm.bar);
+      }
+      if (rows4) bulk_load_1d(sm.pos[buf], a.pos + tt0, rows4 * 4u, &sm.bar);
+    } else if (wq == 1) {
+      mbar_arrive_expect_tx(&sm.bar, box);
+      tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
+    } else if (wq == 2) {
+      mbar_arrive_expect_tx(&sm.bar, a.has_z ? box : 0u);
+      if (a.has_z) tma_load_2d(sm.z[buf], &tm_z, dd0, (int)tt0, &sm.bar);
+    } else if (wq == 3) {
+      mbar_arrive_expect_tx(&sm.bar, bc);
+      bulk_load_1d(sm.B[buf], (sizeof(T) == 4 ? static_cast<const float*>(a.B) : a.Bf32) + tt0 * N, bc, &sm.bar);
+    } else if (wq == 4) {
+      mbar_arrive_expect_tx(&sm.bar, bc);
+      bulk_load_1d(sm.C[buf], (sizeof(T) == 4 ? static_cast<const float*>(a.C) : a.Cf32) + tt0 * N, bc, &sm.bar);
+    } else if (wq == 5) {
+      mbar_arrive_expect_tx(&sm.bar, nval * N * 4u);
+      bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
+    } else if (wq == 6) {
+      mbar_arrive_expect_tx(&sm.bar, a.dt_bias ? nval * 4u : 0u);
+      if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
     } else {
-      tma_load_2d(sm.u[buf], &tm_u, dd0, (int)tt0, &sm.bar);
+      mbar_arrive_expect_tx(&sm.bar, a.Dskip ? nval * 4u : 0u);
+      if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
     }
-    tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
-    if (a.has_z) tma_load_2d(sm.z[buf], &tm_z, dd0, (int)tt0, &sm.bar);
-    const float* Bsrc = sizeof(T) == 4 ? static_cast<const float*>(a.B) : a.Bf32;
-    const float* Csrc = sizeof(T) == 4 ? static_cast<const float*>(a.C) : a.Cf32;
-    bulk_load_1d(sm.B[buf], Bsrc + tt0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.C[buf], Csrc + tt0 * N, bc, &sm.bar);
-    bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
-    if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
-    if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
-    if (rows4) bulk_load_1d(sm.pos[buf], a.pos + tt0, rows4 * 4u, &sm.bar);
   };
+  static_assert(kThreads == 8 * 32, "one share of the copies per warp");
 
   if (tid == 0) {
-    mbar_init(&sm.bar, 1);
+    mbar_init(&sm.bar, kThreads / 32);
     fence_mbar_init();
-    const int first = (int)atomicAdd(a.ticket, 1u);
-    sm.ticket = first;
-    issue(first, 0);
+    sm.ticket = (int)atomicAdd(a.ticket, 1u);
   }
   __syncthreads();
+  if (lane == 0) issue(sm.ticket, 0, s);
 
   // Persistent loop: one work item per pass.  The next ticket is drawn when
-  // pass 2 starts, so that the atomic's round trip overlaps pass 2, and its
-  // copies are requested halfway through pass 2 into the other buffer set
-  // (two buffers), or at the end of pass 2, when the inputs are free (one).  A
-  // draw at the start of the item would hold tickets back from the look-back
-  // chains (an item whose neighbour sits reserved behind a running item waits
-  // for both); pass 2 waits on nothing, so a ticket held through it is not
-  // held back long.  Items only ever wait on items with smaller tickets, all
-  // of which are done or in hand of a running CTA, so the loop cannot
-  // deadlock.
+  // the in-CTA scan starts, so that the atomic's round trip overlaps the scan
+  // and look-back, and published to every warp by the barrier before pass 2;
+  // each warp requests its share of the next item's copies halfway through
+  // its pass 2 into the other buffer set (two buffers), or at the end of
+  // pass 2, when the inputs are free (one).  A draw at the start of the item
+  // would hold tickets back from the look-back chains (an item whose
+  // neighbour sits reserved behind a running item waits for both); pass 2
+  // waits on nothing, so a ticket held through it is not held back long.
+  // Items only ever wait on items with smaller tickets, all of which are done
+  // or in hand of a running CTA, so the loop cannot deadlock.
   for (uint32_t it = 0;; ++it) {
-  // the barrier's completion also publishes thread 0's write of sm.ticket
   if (!__syncthreads_and(mbar_wait(&sm.bar, it & 1u, a.wait_ns))) {
     // report, and give the copies one more, long limit to land before the CTA
     // leaves (nothing it requested may still write into its shared memory)
@@ -361,6 +380,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   //      launch), so a word is its own flag: no fence, and no flag for the
   //      common case.  Only the aggregate of a chunk, published when a walk
   //      must go past it, is announced by the warp's flag after a fence.
+  int next = 0;  // thread 0: the next ticket, stored for every warp before pass 2
+  if (tid == 0) next = (int)atomicAdd(a.ticket, 1u);
   constexpr bool kTwo = N > kS;     // two states per warp
   const bool own = s < N;           // the warp owns at least one state
   const int n0 = s, n1 = kTwo ? s + kS : s;
@@ -502,20 +523,19 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       }
     }
   }
+  // every thread has read this item's ticket at the top of the loop
+  if (tid == 0) sm.ticket = next;
   __syncthreads();
 
   // ---- step 6: exact start state, pass 2
-  int next = 0;  // thread 0: the next ticket
-  if (tid == 0) next = (int)atomicAdd(a.ticket, 1u);
-  // with two buffers, thread 0 requests the next item's inputs halfway
-  // through pass 2 (the ticket's round trip is over by then): the single
-  // buffers (delta_raw, A rows, dt_bias, Dskip) were read before pass 2, the
-  // other buffer set by the item before this one
+  // with two buffers, each warp requests its share of the next item's inputs
+  // halfway through its pass 2: the single buffers (delta_raw, A rows,
+  // dt_bias, Dskip) were read before pass 2, the other buffer set by the
+  // item before this one
   bool issued = false;
   auto issue_next = [&]() {
-    if (kNB == 2 && tid == 0 && !issued) {
-      sm.ticket = next;
-      issue(next, buf ^ 1);
+    if (kNB == 2 && lane == 0 && !issued) {
+      issue(sm.ticket, buf ^ 1, s);
       issued = true;
     }
   };
@@ -615,10 +635,7 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   } else {
     // every input of this item has been read: request the next one's
     __syncthreads();
-    if (tid == 0) {
-      sm.ticket = next;
-      issue(next, 0);
-    }
+    if (lane == 0) issue(sm.ticket, 0, s);
   }
   }  // persistent loop
 }
