@@ -86,7 +86,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // [header 256 B: status int @0, ticket uint @4][flags, one per (slot, lane)][pos][...call specific]
 // header + flags are cleared by one memset at the start of every call.
 struct Layout {
-  size_t flags = 0, pos = 0, seq = 0, bcf = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t flags = 0, pos = 0, seq = 0, bcf = 0, af = 0, agg = 0, agg_sd = 0, incl = 0;
   size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0, conv_part = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
@@ -109,9 +109,11 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   off += up(sizeof(int32_t) * (size_t)T);
   l.seq = off;
   off += up(sizeof(int32_t) * (size_t)T);
-  if (!bwd) {  // B and C as fp32 for bf16 I/O, widened once per call
+  if (!bwd) {  // B and C as fp32 for bf16 I/O, widened once per call; the A rows
     l.bcf = off;
     off += up(sizeof(float) * (size_t)T * N * 2);
+    l.af = off;
+    off += up(sizeof(float) * (size_t)n_tiles * tw * N);
   }
   l.agg = off;
   off += up(sizeof(float) * (size_t)slots * N * tw);
@@ -327,7 +329,7 @@ int vssm::check_outputs_finite(int32_t* status, cudaStream_t st, const void* con
 vssm::ScanLayout vssm::scan_workspace_layout(int64_t T, int D, int N, int chunk, bool bwd) {
   const Layout l = scan_layout(T, D, N, chunk, bwd);
   ScanLayout o;
-  o.flags = l.flags; o.pos = l.pos; o.seq = l.seq; o.bcf = l.bcf; o.agg = l.agg; o.agg_sd = l.agg_sd;
+  o.flags = l.flags; o.pos = l.pos; o.seq = l.seq; o.bcf = l.bcf; o.af = l.af; o.agg = l.agg; o.agg_sd = l.agg_sd;
   o.incl = l.incl;
   o.part_bc = l.part_bc; o.part_a = l.part_a; o.part_d = l.part_d; o.part_b = l.part_b; o.bcd = l.bcd;
   o.clear_bytes = l.clear_bytes; o.incl_bytes = l.incl_bytes; o.total = l.total;
@@ -684,6 +686,7 @@ int varlen_selective_scan_fwd(const void* u, const void* delta_raw, const float*
     a.Bf32 = at<float>(workspace, l.bcf);
     a.Cf32 = a.Bf32 + T * N;
   }
+  a.Af = at<float4>(workspace, l.af);
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);
   a.flags = at<int>(workspace, l.flags);
@@ -766,6 +769,7 @@ int varlen_conv1d_scan_fwd(const void* x, const float* conv_weight, const float*
     a.Bf32 = at<float>(workspace, l.bcf);
     a.Cf32 = a.Bf32 + T * N;
   }
+  a.Af = at<float4>(workspace, l.af);
   a.conv_w = conv_weight; a.conv_b = conv_bias; a.conv_W = W; a.conv_silu = apply_silu ? 1 : 0; a.u_out = u;
   a.status = at<int>(workspace, 0);
   a.ticket = at<unsigned>(workspace, 4);

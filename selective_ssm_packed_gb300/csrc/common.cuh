@@ -104,52 +104,6 @@ __device__ __forceinline__ void lds_pairs(float2 (&v)[N / 2], const float* p) {
   }
 }
 
-// Copies the rows d0 .. d0+31 of a row-major (D, N) fp32 array into shared
-// memory with row pitch N + 4 (coalesced global reads; the padding makes the
-// per-lane 16-byte row reads conflict-free); rows past D are zero.
-template <int N>
-__device__ __forceinline__ void stage_rows(float* dst, const float* src, int d0, int D, int tid,
-                                           int nthreads) {
-  const float* base = src + (int64_t)d0 * N;
-  for (int i = tid; i < 32 * N; i += nthreads) {
-    const int r = i / N, c = i - r * N;
-    dst[r * (N + 4) + c] = (d0 + r < D) ? __ldg(base + i) : 0.0f;
-  }
-}
-
-// Reads one staged row of N values as N/2 pairs, each value times `scale`.
-template <int N>
-__device__ __forceinline__ void load_scaled_pairs(float2 (&v)[N / 2], const float* row, float scale) {
-#pragma unroll
-  for (int i = 0; i < N / 2; i += 2) {
-    const float4 q = *reinterpret_cast<const float4*>(row + 2 * i);
-    v[i] = make_float2(q.x * scale, q.y * scale);
-    v[i + 1] = make_float2(q.z * scale, q.w * scale);
-  }
-}
-
-// Same values from an UNPADDED row-major (rows, N) array in shared memory, one
-// row per lane: each lane fetches its four-value blocks in a lane-rotated
-// order, so that the 8 lanes of a 16-byte access phase hit distinct banks.
-template <int N>
-__device__ __forceinline__ void load_row_pairs_rotated(float2 (&v)[N / 2], const float* row, int lane,
-                                                       float scale) {
-  constexpr int NB = N / 4;                     // 16-byte blocks per row
-  const int r = (lane / (8 / NB)) % NB;         // rotation of this lane
-  float4 q[NB];                                 // q[j] = block (j + r) % NB
-#pragma unroll
-  for (int j = 0; j < NB; ++j) q[j] = *reinterpret_cast<const float4*>(row + 4 * ((j + r) % NB));
-#pragma unroll
-  for (int c = 0; c < NB; ++c) {
-    float4 b = q[c];
-#pragma unroll
-    for (int k = 1; k < NB; ++k)
-      if (r == k) b = q[(c - k + NB) % NB];
-    v[2 * c] = make_float2(b.x * scale, b.y * scale);
-    v[2 * c + 1] = make_float2(b.z * scale, b.w * scale);
-  }
-}
-
 // ------------------------------------------------------------------ timers, memory order
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

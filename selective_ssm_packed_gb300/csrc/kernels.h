@@ -38,6 +38,8 @@ cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int
                              float4* CD, cudaStream_t st);
 // dst[i] = the bf16 value src[i] as fp32, i < n.
 cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
+// The forward's A rows (see ScanArgs::Af) for the ceil(D / 32) channel tiles.
+cudaError_t launch_prep_a(const float* A, int D, int N, bool a_log, float4* Af, cudaStream_t st);
 // ORs kStatusNonFinite into *status when any of the n values at p (io type,
 // or f32 when f32 is true) is a NaN or an infinity.
 cudaError_t launch_nonfinite_check(const void* p, int64_t n, bool f32, int32_t* status, cudaStream_t st);
@@ -100,6 +102,10 @@ struct ScanArgs {
   // (null for fp32 I/O, where the kernel reads B and C themselves)
   const float* Bf32;
   const float* Cf32;
+  // fwd: A * log2 e (A = -exp(A_log) when a_log), per 32-channel tile
+  // [tile][n / 4][channel of the tile] float4 (zero past D), built once per
+  // call, so that lane c of a warp reads channel c's four states n .. n + 3
+  const float4* Af;
   // bwd: B and C doubled, [token][state pair][order] float4 (order 0 holds
   // (B[2p], B[2p], B[2p+1], B[2p+1]), order 1 the two states swapped), built
   // once per call for whole 32-token chunks (zero past the last token)
@@ -188,12 +194,12 @@ int record_error(int code, const char* message);
 // ---------------------------------------------------------------- shared host helpers (api.cu)
 // Byte offsets of a scan call's workspace: [header 256 B: status int @0,
 // ticket uint @4][look-back flags][position indices][sequence index]
-// [fwd: B and C as fp32][aggregates][aggregate factors][inclusive states]
+// [fwd: B and C as fp32, A rows][aggregates][aggregate factors][inclusive states]
 // [backward partials].
 // The header and flags (clear_bytes) start at zero; the inclusive states
 // (incl, incl_bytes) start as all-ones words.
 struct ScanLayout {
-  size_t flags = 0, pos = 0, seq = 0, bcf = 0, agg = 0, agg_sd = 0, incl = 0;
+  size_t flags = 0, pos = 0, seq = 0, bcf = 0, af = 0, agg = 0, agg_sd = 0, incl = 0;
   size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };

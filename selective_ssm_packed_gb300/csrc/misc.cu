@@ -101,6 +101,37 @@ cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream
   return cudaGetLastError();
 }
 
+// The forward's A rows: out[(tile * N/4 + b) * 32 + c] = the states 4b .. 4b+3
+// of channel d = 32 tile + c, each A * log2 e, where A = -exp(A_log) (as
+// -2^(A_log log2 e)) when the rows hold A_log; zero for d >= D.
+__global__ void __launch_bounds__(256) prep_a_kernel(const float* __restrict__ A, int D, int N, int a_log,
+                                                     float4* __restrict__ out, int64_t n) {
+  const int nb = N / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % kTile);
+    const int64_t tb = i / kTile;
+    const int b = (int)(tb % nb);
+    const int64_t d = (tb / nb) * kTile + c;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (d < D) {
+      const float4 r = __ldg(reinterpret_cast<const float4*>(A + d * N) + b);
+      if (a_log)
+        v = make_float4(-ex2(r.x * kLog2e) * kLog2e, -ex2(r.y * kLog2e) * kLog2e, -ex2(r.z * kLog2e) * kLog2e,
+                        -ex2(r.w * kLog2e) * kLog2e);
+      else
+        v = make_float4(r.x * kLog2e, r.y * kLog2e, r.z * kLog2e, r.w * kLog2e);
+    }
+    out[i] = v;
+  }
+}
+
+cudaError_t launch_prep_a(const float* A, int D, int N, bool a_log, float4* Af, cudaStream_t st) {
+  const int64_t n = (int64_t)(D + kTile - 1) / kTile * kTile * (N / 4);
+  if (n <= 0) return cudaSuccess;
+  prep_a_kernel<<<(unsigned)grid_stride_blocks(n), 256, 0, st>>>(A, D, N, a_log ? 1 : 0, Af, n);
+  return cudaGetLastError();
+}
+
 // A value is NaN or infinite when its exponent bits are all ones: bits
 // 0x7f800000 of an f32, 0x7f80 of a bf16 (two bf16 values per 32-bit word).
 __global__ void __launch_bounds__(256) nonfinite_kernel(const uint32_t* __restrict__ p, int64_t words,

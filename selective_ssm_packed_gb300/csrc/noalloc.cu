@@ -170,6 +170,7 @@ extern "C" int varlen_selective_scan_fwd_noalloc(
     a.Bf32 = reinterpret_cast<float*>(s + l.bcf);
     a.Cf32 = a.Bf32 + T * N;
   }
+  a.Af = reinterpret_cast<float4*>(s + l.af);
   a.status = status_word;
   a.ticket = reinterpret_cast<unsigned*>(s + 4);
   a.flags = reinterpret_cast<int*>(s + l.flags);

@@ -73,7 +73,7 @@ struct FwdSmem {
   alignas(16) float dlt[kL * kTile];
   alignas(16) float aggH[kS * N * kTile];
   float aggSD[kS * kTile];
-  alignas(16) float Araw[kTile * N];  // A rows d0 .. d0+31
+  alignas(16) float4 Af[N / 4 * kTile];  // the tile's A rows, prepared once per call (ScanArgs::Af)
   alignas(16) float bias[kTile];
   alignas(16) float dsk[kTile];
   alignas(16) int pos[NB][kL];
@@ -151,8 +151,8 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
       mbar_arrive_expect_tx(&sm.bar, bc);
       bulk_load_1d(sm.C[buf], (sizeof(T) == 4 ? static_cast<const float*>(a.C) : a.Cf32) + tt0 * N, bc, &sm.bar);
     } else if (wq == 5) {
-      mbar_arrive_expect_tx(&sm.bar, nval * N * 4u);
-      bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
+      mbar_arrive_expect_tx(&sm.bar, (uint32_t)kTile * N * 4u);
+      bulk_load_1d(sm.Af, a.Af + (int64_t)tl * (N / 4) * kTile, (uint32_t)kTile * N * 4u, &sm.bar);
     } else if (wq == 6) {
       mbar_arrive_expect_tx(&sm.bar, a.dt_bias ? nval * 4u : 0u);
       if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
@@ -277,18 +277,13 @@ scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
   const int tb = s * kK;  // first token (within the chunk) of this thread
   const float* Bf = sm.B[buf];
   const float* Cf = sm.C[buf];
+  // A * log2 e of this lane's channel (zero past D), as state pairs
   float2 A2[P];
-  if (valid) {
-    load_row_pairs_rotated<N>(A2, sm.Araw + lane * N, lane, a.a_log ? 1.0f : kLog2e);
-    if (a.a_log) {
-      // the rows hold A_log: A = -exp(A_log), kept scaled by log2 e for ex2
 #pragma unroll
-      for (int i = 0; i < P; ++i)
-        A2[i] = make_float2(-ex2(A2[i].x * kLog2e) * kLog2e, -ex2(A2[i].y * kLog2e) * kLog2e);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < P; ++i) A2[i] = make_float2(0.0f, 0.0f);
+  for (int b = 0; b < N / 4; ++b) {
+    const float4 q = sm.Af[b * kTile + lane];
+    A2[2 * b] = make_float2(q.x, q.y);
+    A2[2 * b + 1] = make_float2(q.z, q.w);
   }
 
   // fused conv1d: this thread's 16 u values first, in a loop of independent
@@ -683,6 +678,9 @@ cudaError_t launch_t(const ScanArgs& a, const CUtensorMap& tm_u, const CUtensorM
 cudaError_t launch_scan_fwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
                             const CUtensorMap& tm_dr, const CUtensorMap& tm_z, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
+  if (!a.Af) return cudaErrorInvalidValue;
+  cudaError_t pe = launch_prep_a(a.A, a.D, a.N, a.a_log != 0, const_cast<float4*>(a.Af), st);
+  if (pe != cudaSuccess) return pe;
   if (io == IO::BF16) {  // every work item then copies fp32 B and C rows as they are
     if (!a.Bf32 || !a.Cf32) return cudaErrorInvalidValue;
     cudaError_t e = launch_widen_bf16(a.B, const_cast<float*>(a.Bf32), a.T * a.N, st);
