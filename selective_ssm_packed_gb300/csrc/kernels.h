@@ -33,9 +33,10 @@ cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, in
                                          const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st);
-// The backward's doubled B and C (see ScanArgs::BD) for tokens 0 .. T_pad-1.
-cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, float4* BD,
-                             float4* CD, cudaStream_t st);
+// The backward's doubled B and C (see ScanArgs::BD) for tokens 0 .. T_pad-1;
+// packed: B and C in one array instead (see ScanArgs::BD), CD unused.
+cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, bool packed,
+                             float4* BD, float4* CD, cudaStream_t st);
 // dst[i] = the bf16 value src[i] as fp32, i < n.
 cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // The forward's A rows (see ScanArgs::Af) for the ceil(D / 32) channel tiles.
@@ -108,7 +109,9 @@ struct ScanArgs {
   const float4* Af;
   // bwd: B and C doubled, [token][state pair][order] float4 (order 0 holds
   // (B[2p], B[2p], B[2p+1], B[2p+1]), order 1 the two states swapped), built
-  // once per call for whole 32-token chunks (zero past the last token)
+  // once per call for whole 32-token chunks (zero past the last token).  For
+  // N = 16, B and C packed in BD alone: (B[2p], B[2p+1], C[2p], C[2p+1]) for
+  // order 0, order 1 the two states swapped.
   const float4* BD;
   const float4* CD;
   const float* Dskip;

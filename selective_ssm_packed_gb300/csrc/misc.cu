@@ -41,9 +41,11 @@ cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t
 // BD[(t NSP + p) 2 + o] = (b0, b0, b1, b1) for o = 0 and (b1, b1, b0, b0) for
 // o = 1, with (b0, b1) = (B[t][2p], B[t][2p+1]) as fp32, zero for t >= T; CD
 // likewise from C.  One thread per (token, state pair).
+// packed (CD unused): BD[(t NSP + p) 2 + o] = (b0, b1, c0, c1) for o = 0 and
+// (b1, b0, c1, c0) for o = 1.
 template <typename T>
 __global__ void __launch_bounds__(256) double_bc_kernel(const T* __restrict__ B, const T* __restrict__ C,
-                                                        int64_t nT, int64_t n_items, int N,
+                                                        int64_t nT, int64_t n_items, int N, int packed,
                                                         float4* __restrict__ BD, float4* __restrict__ CD) {
   const int NSP = N / 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -55,24 +57,30 @@ __global__ void __launch_bounds__(256) double_bc_kernel(const T* __restrict__ B,
       b = make_float2(to_f(B[t * N + 2 * p]), to_f(B[t * N + 2 * p + 1]));
       c = make_float2(to_f(C[t * N + 2 * p]), to_f(C[t * N + 2 * p + 1]));
     }
-    BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
-    BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
-    CD[2 * i] = make_float4(c.x, c.x, c.y, c.y);
-    CD[2 * i + 1] = make_float4(c.y, c.y, c.x, c.x);
+    if (packed) {
+      BD[2 * i] = make_float4(b.x, b.y, c.x, c.y);
+      BD[2 * i + 1] = make_float4(b.y, b.x, c.y, c.x);
+    } else {
+      BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
+      BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
+      CD[2 * i] = make_float4(c.x, c.x, c.y, c.y);
+      CD[2 * i + 1] = make_float4(c.y, c.y, c.x, c.x);
+    }
   }
 }
 
-cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, float4* BD,
-                             float4* CD, cudaStream_t st) {
+cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, bool packed,
+                             float4* BD, float4* CD, cudaStream_t st) {
   const int64_t n_items = T_pad * (N / 2);
   if (n_items <= 0) return cudaSuccess;
   const int64_t blocks = grid_stride_blocks(n_items);
   if (io == IO::F32)
     double_bc_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float*>(B),
-                                                              static_cast<const float*>(C), T, n_items, N, BD, CD);
+                                                              static_cast<const float*>(C), T, n_items, N, packed ? 1 : 0, BD, CD);
   else
     double_bc_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), T, n_items, N, BD, CD);
+        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), T, n_items, N, packed ? 1 : 0, BD,
+        CD);
   return cudaGetLastError();
 }
 

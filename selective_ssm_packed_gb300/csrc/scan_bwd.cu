@@ -718,9 +718,9 @@ struct Bwd16Smem {
   alignas(16) float4 dl[kCQ * kQT];   // delta
   alignas(16) float4 dlu[kCQ * kQT];  // delta * u
   alignas(16) float4 g[kCQ * kQT];    // dout * (SiLU(z) + gate floor)
-  // ---- B and C doubled, [token][state pair][order] float4 (as above)
-  alignas(16) float4 BD[kL * kSP * 2];
-  alignas(16) float4 CD[kL * kSP * 2];
+  // ---- B and C packed, [token][state pair][order] float4 = (B_n, B_m, C_n,
+  //      C_m), (n, m) the pair in the thread's order
+  alignas(16) float4 BC[kL * kSP * 2];
   alignas(16) float4 off[kL / 2];
   // ---- partial sums over each thread's state pair from the reverse walk,
   //      [buffer][token of the block][state pair][channel pair parity][quad]
@@ -827,7 +827,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
     const int dd0 = tl * kTW;
     const uint32_t nval = (uint32_t)(a.D - dd0 < kTW ? a.D - dd0 : kTW);
-    const uint32_t bcd = (uint32_t)kL * N * 16u;  // the chunk's doubled B (or C) rows
+    const uint32_t bcd = (uint32_t)kL * N * 16u;  // the chunk's packed B and C rows
     const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
     if (wq == 0) {
@@ -841,9 +841,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
       tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
     } else if (wq == 2) {
-      mbar_arrive_expect_tx(&sm.bar, 2u * bcd + rows4 * 4u);
-      bulk_load_1d(sm.BD, a.BD + tt0 * N, bcd, &sm.bar);
-      bulk_load_1d(sm.CD, a.CD + tt0 * N, bcd, &sm.bar);
+      mbar_arrive_expect_tx(&sm.bar, bcd + rows4 * 4u);
+      bulk_load_1d(sm.BC, a.BD + tt0 * N, bcd, &sm.bar);
       if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
     } else {
       mbar_arrive_expect_tx(&sm.bar, nval * N * 4u + (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
@@ -990,8 +989,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   const float4* const dlr = sm.dl + cq * kQT;
   const float4* const dur = sm.dlu + cq * kQT;
   const float4* const gr = sm.g + cq * kQT;
-  const float4* const bdr = sm.BD + sp * 2 + o;  // entry of token t at [t * 2 kSP]
-  const float4* const cdr = sm.CD + sp * 2 + o;
+  const float4* const bcr = sm.BC + sp * 2 + o;  // entry of token t at [t * 2 kSP]
   const int part = 2 * tile + grp;               // 32-channel partial row group
   float* const pdB = a.part_dBC + ((int64_t)part * 2 * N + nF) * a.T + t0;
   float* const pdC = a.part_dBC + ((int64_t)part * 2 * N + N + nF) * a.T + t0;
@@ -1021,12 +1019,12 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
         const float4 of4 = sm.off[tt >> 1];
         const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
-        const float4 bd = bdr[tt * 2 * kSP], cd = cdr[tt * 2 * kSP];
+        const float4 bc = bcr[tt * 2 * kSP];
         const float2 dlp[2] = {lo2(dl4), hi2(dl4)}, dup[2] = {lo2(du4), hi2(du4)}, gp[2] = {lo2(gq), hi2(gq)};
         float v[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const float2 Bq = q ? hi2(bd) : lo2(bd), Cq = q ? hi2(cd) : lo2(cd);
+          const float2 Bq = splat2(q ? bc.y : bc.x), Cq = splat2(q ? bc.w : bc.z);
           const int n = q ? nS : nF;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -1163,12 +1161,12 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
         const float4 of4 = sm.off[tt >> 1];
         const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
-        const float4 bd = bdr[tt * 2 * kSP], cd = cdr[tt * 2 * kSP];
+        const float4 bc = bcr[tt * 2 * kSP];
         const float2 dlp[2] = {lo2(dl4), hi2(dl4)}, dup[2] = {lo2(du4), hi2(du4)}, gp[2] = {lo2(gq), hi2(gq)};
         float2 dh[2][2], qq[2][2], at[2][2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const float2 Cq = q ? hi2(cd) : lo2(cd);
+          const float2 Cq = splat2(q ? bc.w : bc.z);
           [[maybe_unused]] const int n = q ? nS : nF;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -1182,7 +1180,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
             dA[q][j] = fma2(dlp[j], qq[q][j], dA[q][j]);
           }
         }
-        const float2 BF = lo2(bd), BS = hi2(bd);
+        const float2 BF = splat2(bc.x), BS = splat2(bc.y);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const float2 s1 = fma2(dh[1][j], BS, mul2(dh[0][j], BF));
@@ -1199,7 +1197,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
           for (int j = 0; j < 2; ++j) {
             const float2 pF = make_float2(bitsf(hb[8 * e + 2 * j]), bitsf(hb[8 * e + 2 * j + 1]));
             const float2 pS = make_float2(bitsf(hb[8 * e + 4 + 2 * j]), bitsf(hb[8 * e + 4 + 2 * j + 1]));
-            yv[j] = fma2(hi2(cd), fma2(dup[j], BS, pS), mul2(lo2(cd), fma2(dup[j], BF, pF)));
+            yv[j] = fma2(splat2(bc.w), fma2(dup[j], BS, pS), mul2(splat2(bc.z), fma2(dup[j], BF, pF)));
           }
           const bool b2 = (lane & 4) != 0, b4 = (lane & 16) != 0;
           float2 keep = b2 ? yv[1] : yv[0];
@@ -1469,7 +1467,7 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
     return e;
   }
   // B and C doubled once per call; every work item copies its chunk's rows
-  cudaError_t e = launch_double_bc(a.B, a.C, io, a.T, (int64_t)a.n_chunks * kBwdChunk, a.N,
+  cudaError_t e = launch_double_bc(a.B, a.C, io, a.T, (int64_t)a.n_chunks * kBwdChunk, a.N, a.N == 16,
                                    const_cast<float4*>(a.BD), const_cast<float4*>(a.CD), st);
   if (e != cudaSuccess) return e;
   kernel_timer_mark(kTimeScanBwd, true, st);
