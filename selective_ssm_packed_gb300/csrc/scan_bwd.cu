@@ -721,7 +721,6 @@ struct Bwd16Smem {
   // ---- B and C packed, [token][state pair][order] float4 = (B_n, B_m, C_n,
   //      C_m), (n, m) the pair in the thread's order
   alignas(16) float4 BC[kL * kSP * 2];
-  alignas(16) float4 off[kL / 2];
   // ---- partial sums over each thread's state pair from the reverse walk,
   //      [buffer][token of the block][state pair][channel pair parity][quad]
   //      float4 = (sum dh B for the pair's two channels, sum A dh p for them)
@@ -943,11 +942,6 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   }
   const unsigned rst =
       __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
-  if (w == 0 && lane < kL / 2) {
-    const float o0 = ((rst >> (2 * lane)) & 1u) ? -INFINITY : 0.0f;
-    const float o1 = ((rst >> (2 * lane + 1)) & 1u) ? -INFINITY : 0.0f;
-    sm.off[lane] = make_float4(o0, o0, o1, o1);
-  }
   unsigned evH = 0u, evG = 0u, evF = 0u;
   if (kStates && a.seq) {
     const unsigned live = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
@@ -1017,8 +1011,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         const int tt = 4 * g4 + e;
         if (e == 2 && pend_t < rows) pdC[pend_t] = pend;
         const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
-        const float4 of4 = sm.off[tt >> 1];
-        const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
+        // exponent offset: -inf at a sequence start (the factor is zeroed)
+        const float2 ofp = splat2(((rst >> tt) & 1u) ? -INFINITY : 0.0f);
         const float4 bc = bcr[tt * 2 * kSP];
         const float2 dlp[2] = {lo2(dl4), hi2(dl4)}, dup[2] = {lo2(du4), hi2(du4)}, gp[2] = {lo2(gq), hi2(gq)};
         float v[2];
@@ -1159,8 +1153,8 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         // the previous block's dB sum, long since complete
         if (e == kRB - 2 && pendB_t < rows) pdB[pendB_t] = pendB;
         const float4 dl4 = dlr[tt], du4 = dur[tt], gq = gr[tt];
-        const float4 of4 = sm.off[tt >> 1];
-        const float2 ofp = (e & 1) ? hi2(of4) : lo2(of4);
+        // exponent offset: -inf at a sequence start (the factor is zeroed)
+        const float2 ofp = splat2(((rst >> tt) & 1u) ? -INFINITY : 0.0f);
         const float4 bc = bcr[tt * 2 * kSP];
         const float2 dlp[2] = {lo2(dl4), hi2(dl4)}, dup[2] = {lo2(du4), hi2(du4)}, gp[2] = {lo2(gq), hi2(gq)};
         float2 dh[2][2], qq[2][2], at[2][2];
