@@ -1234,11 +1234,15 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     // du and d delta_raw (and dz when y is recomputed) of block blk for this
     // thread's channel group: item (token e, channel pair) per thread of the
     // group; the state pairs' partials are added in order
+    // this thread's channel pair in every finalize, and its dt_bias / Dskip
+    const int fin_cpl = tid & 15;
+    const int fin_cp = 16 * grp + fin_cpl;
+    const float2 fin_bias = a.dt_bias ? *reinterpret_cast<const float2*>(sm.bias + 2 * fin_cp) : make_float2(0.0f, 0.0f);
+    const float2 fin_dsk = a.Dskip ? *reinterpret_cast<const float2*>(sm.dsk + 2 * fin_cp) : make_float2(0.0f, 0.0f);
     auto finalize = [&](int blk) {
       const int buf = blk & 1;
-      const int tg = tid & 63;
-      const int e = tg >> 4, cpl = tg & 15;
-      const int cp = 16 * grp + cpl, hh = cp & 1, qd = cp >> 1;
+      const int e = (tid & 63) >> 4, cpl = fin_cpl;
+      const int cp = fin_cp, hh = cp & 1, qd = cp >> 1;
       const int t = blk * kRB + e;
       float4 pv[kSP];
 #pragma unroll
@@ -1251,11 +1255,10 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       const float2 uv = ld_io2(sm.u + at);
       float2 sgv = make_float2(1.0f, 1.0f);
       if (a.delta_softplus) {  // d softplus / dx = sigmoid(delta_raw + dt_bias)
-        const float2 rr = __fadd2_rn(ld_io2(sm.dr + at), a.dt_bias ? *reinterpret_cast<const float2*>(sm.bias + 2 * cp)
-                                                                   : make_float2(0.0f, 0.0f));
+        const float2 rr = __fadd2_rn(ld_io2(sm.dr + at), fin_bias);
         sgv = make_float2(sigmoidf_fast(rr.x), sigmoidf_fast(rr.y));
       }
-      const float2 dsk = a.Dskip ? *reinterpret_cast<const float2*>(sm.dsk + 2 * cp) : make_float2(0.0f, 0.0f);
+      const float2 dsk = fin_dsk;
       const float2 du = fma2(dlv, lo2(s), mul2(dsk, gv));
       const bool ok = t < rows && 2 * cp < bx && d0 + 2 * cp < a.D;
       const float2 ddr = ok ? mul2(fma2(uv, lo2(s), mul2(hi2(s), splat2(kLn2))), sgv) : make_float2(0.0f, 0.0f);
