@@ -695,7 +695,10 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // channel group only, so a block's epilogue waits on a 64-thread named
 // barrier, not on the whole CTA; each block is finalized after the walk over
 // the next one.  The next item's copies are split over the four warps (the
-// barrier takes four arrivals).
+// barrier takes four arrivals).  Fewer shared-memory loads pay here even at
+// the cost of register moves: B and C arrive packed, (B_n, B_m, C_n, C_m) in
+// one 16-byte row per token and state pair, each value splatted for the paired
+// instructions, and the exponent offsets are selects on the start ballot.
 constexpr int kTW = 2 * kTile;  // 64 channels per work item
 constexpr int kCQ = kTW / 4;    // 16 channel quads
 constexpr int kQT = kL + 1;     // token pitch (float4) of the [channel quad][token] arrays
