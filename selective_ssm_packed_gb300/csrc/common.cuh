@@ -74,7 +74,7 @@ __device__ __forceinline__ float softplus_sig(float x, float* sig) {
   const float ope = 1.0f + e;
   const float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.33333334f), -0.5f), 1.0f);
   const float l1p = e >= 0.03125f ? lg2(ope) * 0.6931471805599453f : series;
-  const float r = __frcp_rn(ope);
+  const float r = __fdividef(1.0f, ope);  // MUFU reciprocal, relative error ~2^-22
   *sig = x >= 0.0f ? r : e * r;
   return fmaxf(x, 0.0f) + l1p;
 }

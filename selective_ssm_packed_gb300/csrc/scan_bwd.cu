@@ -699,6 +699,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // the cost of register moves: B and C arrive packed, (B_n, B_m, C_n, C_m) in
 // one 16-byte row per token and state pair, each value splatted for the paired
 // instructions, and the exponent offsets are selects on the start ballot.
+// For bf16 I/O step 1 keeps d delta / d delta_raw (a by-product of softplus)
+// for the finalize, which otherwise recomputes it from delta_raw.
 constexpr int kTW = 2 * kTile;  // 64 channels per work item
 constexpr int kCQ = kTW / 4;    // 16 channel quads
 constexpr int kQT = kL + 1;     // token pitch (float4) of the [channel quad][token] arrays
@@ -721,6 +723,9 @@ struct Bwd16Smem {
   alignas(16) float4 dl[kCQ * kQT];   // delta
   alignas(16) float4 dlu[kCQ * kQT];  // delta * u
   alignas(16) float4 g[kCQ * kQT];    // dout * (SiLU(z) + gate floor)
+  // d delta / d delta_raw = sigmoid(delta_raw + dt_bias), for bf16 I/O (the
+  // fp32 tiles leave no room: the finalize recomputes it there)
+  alignas(16) float4 sg[sizeof(T) == 2 ? kCQ * kQT : 1];
   // ---- B and C packed, [token][state pair][order] float4 = (B_n, B_m, C_n,
   //      C_m), (n, m) the pair in the thread's order
   alignas(16) float4 BC[kL * kSP * 2];
@@ -908,14 +913,14 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       const float4 u4 = ld_io4(sm.u + at);
       const float4 go = ld_io4(sm.dout + at);
       const float2 rlo = __fadd2_rn(lo2(r4), lo2(bias4)), rhi = __fadd2_rn(hi2(r4), hi2(bias4));
-      float4 dl4;
+      float4 dl4, sg4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
       if (a.delta_softplus) {
-        float sgd;
-        dl4 = make_float4(softplus_sig(rlo.x, &sgd), softplus_sig(rlo.y, &sgd), softplus_sig(rhi.x, &sgd),
-                          softplus_sig(rhi.y, &sgd));
+        dl4 = make_float4(softplus_sig(rlo.x, &sg4.x), softplus_sig(rlo.y, &sg4.y),
+                          softplus_sig(rhi.x, &sg4.z), softplus_sig(rhi.y, &sg4.w));
       } else {
         dl4 = mk4(rlo, rhi);
       }
+      if constexpr (sizeof(T) == 2) sm.sg[q * kQT + t] = sg4;
       float4 gv = go;
       if (a.has_z) {
         const float4 z4 = ld_io4(sm.z + at);
@@ -1257,7 +1262,9 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       const int at = t * bx + 2 * cp;
       const float2 uv = ld_io2(sm.u + at);
       float2 sgv = make_float2(1.0f, 1.0f);
-      if (a.delta_softplus) {  // d softplus / dx = sigmoid(delta_raw + dt_bias)
+      if constexpr (sizeof(T) == 2) {
+        sgv = reinterpret_cast<const float2*>(sm.sg + qd * kQT + t)[hh];
+      } else if (a.delta_softplus) {  // d softplus / dx = sigmoid(delta_raw + dt_bias)
         const float2 rr = __fadd2_rn(ld_io2(sm.dr + at), fin_bias);
         sgv = make_float2(sigmoidf_fast(rr.x), sigmoidf_fast(rr.y));
       }
