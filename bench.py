@@ -575,10 +575,11 @@ def run_ours(args):
 
     # this library's launches per step: position indices 1; conv fwd 1; scan
     # fwd 1, plus the A-row preparation 1 and 2 to widen B and C for bf16 I/O;
-    # scan bwd 1, plus B/C doubling 1, the dB/dC tile sum 1 and 3 fixed-order
-    # row sums of 2 launches (dA, dDskip, d_dt_bias); conv bwd 1 plus 2 row
-    # sums of 2 (dweight, dbias)
-    KERNELS_PER_STEP = 1 + 1 + (1 + 1 + (2 if wl.dtype == "bf16" else 0)) + (1 + 1 + 1 + 3 * 2) + (1 + 2 * 2)
+    # scan bwd 1, plus the B/C rows 1, the tile parameters 1 (N = 16), the
+    # dB/dC tile sum 1 and 3 fixed-order row sums of 2 launches (dA, dDskip,
+    # d_dt_bias); conv bwd 1 plus 2 row sums of 2 (dweight, dbias)
+    KERNELS_PER_STEP = (1 + 1 + (1 + 1 + (2 if wl.dtype == "bf16" else 0))
+                        + (1 + 1 + (1 if wl.N == 16 else 0) + 1 + 3 * 2) + (1 + 2 * 2))
 
     for _ in range(args.warmup):
         step()

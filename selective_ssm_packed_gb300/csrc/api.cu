@@ -87,7 +87,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // header + flags are cleared by one memset at the start of every call.
 struct Layout {
   size_t flags = 0, pos = 0, seq = 0, bcf = 0, af = 0, agg = 0, agg_sd = 0, incl = 0;
-  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0, conv_part = 0;
+  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0, tpar = 0, conv_part = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
 
@@ -133,8 +133,13 @@ Layout scan_layout(int64_t T, int D, int N, int chunk, bool bwd) {
     l.part_b = off;
     off += up(sizeof(float) * (size_t)n_chunks * D);
     // B and C doubled for whole chunks: [token][state pair][order] float4
+    // (N = 16: packed, with the chunk's position indices, in less room)
     l.bcd = off;
     off += up(sizeof(float) * 4 * (size_t)n_chunks * chunk * N * 2);
+    if (N == 16) {  // the tiles' A rows, dt_bias and Dskip
+      l.tpar = off;
+      off += up(sizeof(float) * (size_t)n_tiles * kBwdTileParams);
+    }
   }
   l.total = off;
   return l;
@@ -331,7 +336,7 @@ vssm::ScanLayout vssm::scan_workspace_layout(int64_t T, int D, int N, int chunk,
   ScanLayout o;
   o.flags = l.flags; o.pos = l.pos; o.seq = l.seq; o.bcf = l.bcf; o.af = l.af; o.agg = l.agg; o.agg_sd = l.agg_sd;
   o.incl = l.incl;
-  o.part_bc = l.part_bc; o.part_a = l.part_a; o.part_d = l.part_d; o.part_b = l.part_b; o.bcd = l.bcd;
+  o.part_bc = l.part_bc; o.part_a = l.part_a; o.part_d = l.part_d; o.part_b = l.part_b; o.bcd = l.bcd; o.tpar = l.tpar;
   o.clear_bytes = l.clear_bytes; o.incl_bytes = l.incl_bytes; o.total = l.total;
   return o;
 }
@@ -871,6 +876,7 @@ int varlen_selective_scan_bwd(const void* u, const void* delta_raw, const float*
   a.part_dbias = at<float>(workspace, l.part_b);
   a.BD = at<float4>(workspace, l.bcd);
   a.CD = a.BD + cdiv(T, kBwdChunk) * kBwdChunk * N;
+  a.tpar = N == 16 ? at<float>(workspace, l.tpar) : nullptr;
   a.T = T; a.D = D; a.N = N; a.num_seqs = num_seqs;
   const int tw = scan_tile(N, true);
   a.n_tiles = (int)cdiv(D, tw);

@@ -34,9 +34,14 @@ cudaError_t launch_empty_sequence_states(const int32_t* cu, int32_t num_seqs, in
 cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t T, int32_t* pos,
                                     int32_t* status, cudaStream_t st);
 // The backward's doubled B and C (see ScanArgs::BD) for tokens 0 .. T_pad-1;
-// packed: B and C in one array instead (see ScanArgs::BD), CD unused.
+// packed (N = 16): per 32-token chunk, B and C in one array (see ScanArgs::BD)
+// followed by the chunk's 32 position indices (zero past T), kBwdChunkRow
+// bytes a chunk; CD unused.
 cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, bool packed,
-                             float4* BD, float4* CD, cudaStream_t st);
+                             const int32_t* pos, float4* BD, float4* CD, cudaStream_t st);
+// The N = 16 backward's tile parameters (see ScanArgs::tpar).
+cudaError_t launch_bwd_tile_params(const float* A, const float* dt_bias, const float* Dskip, int D, bool a_log,
+                                   float* tpar, cudaStream_t st);
 // dst[i] = the bf16 value src[i] as fp32, i < n.
 cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // The forward's A rows (see ScanArgs::Af) for the ceil(D / 32) channel tiles.
@@ -91,6 +96,10 @@ cudaError_t launch_conv_tails(const ConvArgs& a, IO io, bool bwd, cudaStream_t s
 // ---------------------------------------------------------------- selective scan
 constexpr int kFwdChunk = 128;   // tokens per forward work item (look-back granule)
 constexpr int kBwdChunk = 32;    // tokens per backward work item (= saved-state chunk)
+// N = 16 backward: bytes of a chunk's packed B / C rows and position indices,
+// and floats of a 64-channel tile's parameters (A rows, dt_bias, Dskip)
+constexpr int kBwdChunkRow = kBwdChunk * 16 * 16 + kBwdChunk * 4;
+constexpr int kBwdTileParams = 64 * 16 + 64 + 64;
 constexpr int kTile = 32;        // channels per work item
 
 struct ScanArgs {
@@ -114,6 +123,10 @@ struct ScanArgs {
   // order 0, order 1 the two states swapped.
   const float4* BD;
   const float4* CD;
+  // N = 16 bwd: per 64-channel tile, A * log2 e (A = -exp(A_log) when
+  // a_log) as [channel][n], then dt_bias and Dskip (zero when absent or past
+  // D): kBwdTileParams floats per tile, built once per call
+  const float* tpar;
   const float* Dskip;
   const void* z;
   const float* dt_bias;
@@ -203,7 +216,7 @@ int record_error(int code, const char* message);
 // (incl, incl_bytes) start as all-ones words.
 struct ScanLayout {
   size_t flags = 0, pos = 0, seq = 0, bcf = 0, af = 0, agg = 0, agg_sd = 0, incl = 0;
-  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0;
+  size_t part_bc = 0, part_a = 0, part_d = 0, part_b = 0, bcd = 0, tpar = 0;
   size_t clear_bytes = 0, incl_bytes = 0, total = 0;
 };
 // chunk = tokens per work item (kFwdChunk / kBwdChunk).

@@ -41,11 +41,14 @@ cudaError_t launch_position_indices(const int32_t* cu, int32_t num_seqs, int64_t
 // BD[(t NSP + p) 2 + o] = (b0, b0, b1, b1) for o = 0 and (b1, b1, b0, b0) for
 // o = 1, with (b0, b1) = (B[t][2p], B[t][2p+1]) as fp32, zero for t >= T; CD
 // likewise from C.  One thread per (token, state pair).
-// packed (CD unused): BD[(t NSP + p) 2 + o] = (b0, b1, c0, c1) for o = 0 and
-// (b1, b0, c1, c0) for o = 1.
+// packed (N = 16, CD unused): per chunk of kBwdChunk tokens, kBwdChunkRow
+// bytes: first the float4 rows [token][state pair][order] = (b0, b1, c0, c1)
+// for o = 0 and (b1, b0, c1, c0) for o = 1, then the chunk's position
+// indices (zero past T, written by the chunk's first state pair).
 template <typename T>
 __global__ void __launch_bounds__(256) double_bc_kernel(const T* __restrict__ B, const T* __restrict__ C,
                                                         int64_t nT, int64_t n_items, int N, int packed,
+                                                        const int32_t* __restrict__ pos,
                                                         float4* __restrict__ BD, float4* __restrict__ CD) {
   const int NSP = N / 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -58,8 +61,12 @@ __global__ void __launch_bounds__(256) double_bc_kernel(const T* __restrict__ B,
       c = make_float2(to_f(C[t * N + 2 * p]), to_f(C[t * N + 2 * p + 1]));
     }
     if (packed) {
-      BD[2 * i] = make_float4(b.x, b.y, c.x, c.y);
-      BD[2 * i + 1] = make_float4(b.y, b.x, c.y, c.x);
+      const int64_t ch = t / kBwdChunk, tl = t - ch * kBwdChunk;
+      float4* row = BD + ch * (kBwdChunkRow / 16) + (tl * NSP + p) * 2;
+      row[0] = make_float4(b.x, b.y, c.x, c.y);
+      row[1] = make_float4(b.y, b.x, c.y, c.x);
+      if (p == 0)
+        reinterpret_cast<int32_t*>(BD + ch * (kBwdChunkRow / 16) + kBwdChunk * NSP * 2)[tl] = t < nT ? pos[t] : 0;
     } else {
       BD[2 * i] = make_float4(b.x, b.x, b.y, b.y);
       BD[2 * i + 1] = make_float4(b.y, b.y, b.x, b.x);
@@ -70,17 +77,19 @@ __global__ void __launch_bounds__(256) double_bc_kernel(const T* __restrict__ B,
 }
 
 cudaError_t launch_double_bc(const void* B, const void* C, IO io, int64_t T, int64_t T_pad, int N, bool packed,
-                             float4* BD, float4* CD, cudaStream_t st) {
+                             const int32_t* pos, float4* BD, float4* CD, cudaStream_t st) {
+  if (packed && (N != 16 || !pos)) return cudaErrorInvalidValue;
   const int64_t n_items = T_pad * (N / 2);
   if (n_items <= 0) return cudaSuccess;
   const int64_t blocks = grid_stride_blocks(n_items);
   if (io == IO::F32)
     double_bc_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float*>(B),
-                                                              static_cast<const float*>(C), T, n_items, N, packed ? 1 : 0, BD, CD);
+                                                              static_cast<const float*>(C), T, n_items, N, packed ? 1 : 0, pos, BD,
+                                                              CD);
   else
     double_bc_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), T, n_items, N, packed ? 1 : 0, BD,
-        CD);
+        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), T, n_items, N, packed ? 1 : 0, pos,
+        BD, CD);
   return cudaGetLastError();
 }
 
@@ -106,6 +115,43 @@ cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream
   if (n <= 0) return cudaSuccess;
   const int64_t blocks = grid_stride_blocks((n + 7) / 8);
   widen_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(src), dst, n);
+  return cudaGetLastError();
+}
+
+// The N = 16 backward's tile parameters: for each 64-channel tile, A * log2 e
+// as [channel][n] (A = -exp(A_log), as -2^(A_log log2 e), when the rows hold
+// A_log), then dt_bias and Dskip; zero for absent vectors and channels >= D.
+__global__ void __launch_bounds__(256) bwd_tile_params_kernel(const float* __restrict__ A,
+                                                              const float* __restrict__ bias,
+                                                              const float* __restrict__ dsk, int D, int a_log,
+                                                              float* __restrict__ out, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = i / kBwdTileParams;
+    const int k = (int)(i - tile * kBwdTileParams);
+    float v = 0.0f;
+    if (k < 64 * 16) {
+      const int64_t d = tile * 64 + k / 16;
+      if (d < D) {
+        const float r = __ldg(A + d * 16 + k % 16);
+        v = a_log ? -ex2(r * kLog2e) * kLog2e : r * kLog2e;
+      }
+    } else if (k < 64 * 16 + 64) {
+      const int64_t d = tile * 64 + (k - 64 * 16);
+      if (bias && d < D) v = __ldg(bias + d);
+    } else {
+      const int64_t d = tile * 64 + (k - 64 * 16 - 64);
+      if (dsk && d < D) v = __ldg(dsk + d);
+    }
+    out[i] = v;
+  }
+}
+
+cudaError_t launch_bwd_tile_params(const float* A, const float* dt_bias, const float* Dskip, int D, bool a_log,
+                                   float* tpar, cudaStream_t st) {
+  const int64_t n = (int64_t)(D + 63) / 64 * kBwdTileParams;
+  if (n <= 0) return cudaSuccess;
+  bwd_tile_params_kernel<<<(unsigned)grid_stride_blocks(n), 256, 0, st>>>(A, dt_bias, Dskip, D, a_log ? 1 : 0, tpar,
+                                                                          n);
   return cudaGetLastError();
 }
 

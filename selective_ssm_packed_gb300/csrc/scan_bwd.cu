@@ -47,6 +47,7 @@
 //   5. dA partials per chunk; fixed-order CTA sums for dDskip and d_dt_bias.
 // Separate fixed-order kernels sum the partials over channel tiles (dB, dC)
 // and chunks (dA, dDskip, d_dt_bias).  No atomics anywhere in the arithmetic.
+#include <cstddef>
 #include <type_traits>
 
 #include "common.cuh"
@@ -694,8 +695,8 @@ scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // sums over state pairs for du / d delta_raw come from the two warps of a
 // channel group only, so a block's epilogue waits on a 64-thread named
 // barrier, not on the whole CTA; each block is finalized after the walk over
-// the next one.  The next item's copies are split over the four warps (the
-// barrier takes four arrivals).  Fewer shared-memory loads pay here even at
+// the next one.  The next item's copies are split over the four warps, two
+// each (the barrier takes four arrivals).  Fewer shared-memory loads pay here even at
 // the cost of register moves: B and C arrive packed, (B_n, B_m, C_n, C_m) in
 // one 16-byte row per token and state pair, each value splatted for the paired
 // instructions, and the exponent offsets are selects on the start ballot.
@@ -713,11 +714,12 @@ struct Bwd16Smem {
   alignas(128) T z[kL * kTW];
   alignas(128) T dout[kL * kTW];
   alignas(128) T y[kL * kTW];
-  alignas(16) float Araw[kTW * 16];
   alignas(128) float H[16 * kTW];  // saved states at the chunk start, [n][channel]
+  // the tile's parameters as one copy brings them (ScanArgs::tpar): A * log2 e
+  // [channel][n], dt_bias, Dskip
+  alignas(16) float Araw[kTW * 16];
   alignas(16) float bias[kTW];
   alignas(16) float dsk[kTW];
-  alignas(16) int pos[kL];
   // ---- per-(token, channel quad) values, [quad][token] float4 with token
   //      pitch kQT: the 8 quads a warp reads for a token are in distinct banks
   alignas(16) float4 dl[kCQ * kQT];   // delta
@@ -729,6 +731,7 @@ struct Bwd16Smem {
   // ---- B and C packed, [token][state pair][order] float4 = (B_n, B_m, C_n,
   //      C_m), (n, m) the pair in the thread's order
   alignas(16) float4 BC[kL * kSP * 2];
+  alignas(16) int pos[kL];  // the chunk's position indices (zero past T), copied with BC
   // ---- partial sums over each thread's state pair from the reverse walk,
   //      [buffer][token of the block][state pair][channel pair parity][quad]
   //      float4 = (sum dh B for the pair's two channels, sum A dh p for them)
@@ -804,6 +807,14 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   constexpr int N = 16;
   constexpr int kThr = 128;
   using SM = Bwd16Smem<T, kRecY>;
+  // one bulk copy fills each of these runs of shared memory
+  static_assert(offsetof(SM, pos) == offsetof(SM, BC) + sizeof(SM::BC) &&
+                    sizeof(SM::BC) + sizeof(SM::pos) == kBwdChunkRow,
+                "B / C rows and positions must be contiguous");
+  static_assert(offsetof(SM, bias) == offsetof(SM, Araw) + sizeof(SM::Araw) &&
+                    offsetof(SM, dsk) == offsetof(SM, bias) + sizeof(SM::bias) &&
+                    sizeof(SM::Araw) + sizeof(SM::bias) + sizeof(SM::dsk) == kBwdTileParams * 4,
+                "the tile's parameters must be contiguous");
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -822,40 +833,36 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   const int nF = 2 * sp + o, nS = 2 * sp + 1 - o;  // its "first" and "second" state
   const int c0 = 4 * cq;                           // first channel of the quad (in the tile)
 
-  // The item's twelve copies, split over the four warps: lane 0 of warp wq
-  // posts its share's bytes on the barrier (which expects four arrivals) and
-  // issues its three copies.  One thread issuing all twelve in turn spent
-  // about 1.4k cycles on them while the rest of the CTA waited.
+  // The item's eight copies, two per warp: lane 0 of warp wq posts its
+  // share's bytes on the barrier (which expects four arrivals) and issues its
+  // copies.  One thread issuing twelve copies in turn spent about 1.4k cycles
+  // on them while the rest of the CTA waited, and a warp's copies still issue
+  // one after another: the chunk's B / C rows come with its positions, and the
+  // tile's A rows with dt_bias and Dskip, each in one copy (built per call).
   auto issue = [&](int tkn, int wq) {
     const int rv = tkn / a.n_tiles;
     const int tl = tkn - rv * a.n_tiles;
     const int ch = a.n_chunks - 1 - rv;
     const int64_t tt0 = (int64_t)ch * kL;
-    const int nrows = (int)((a.T - tt0) < kL ? (a.T - tt0) : kL);
     const int dd0 = tl * kTW;
-    const uint32_t nval = (uint32_t)(a.D - dd0 < kTW ? a.D - dd0 : kTW);
-    const uint32_t bcd = (uint32_t)kL * N * 16u;  // the chunk's packed B and C rows
-    const uint32_t rows4 = (uint32_t)nrows & ~3u;
     const uint32_t box = (uint32_t)a.box_x * (uint32_t)a.box_y * sizeof(T);
     if (wq == 0) {
-      mbar_arrive_expect_tx(&sm.bar, 3u * box);
+      mbar_arrive_expect_tx(&sm.bar, 2u * box);
       tma_load_2d(sm.u, &tm_u, dd0, (int)tt0, &sm.bar);
       tma_load_2d(sm.dr, &tm_dr, dd0, (int)tt0, &sm.bar);
-      tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
     } else if (wq == 1) {
-      mbar_arrive_expect_tx(&sm.bar, box * ((a.has_z ? 1u : 0u) + (a.has_y ? 1u : 0u)) + (uint32_t)a.box_x * N * 4u);
+      mbar_arrive_expect_tx(&sm.bar, box * (1u + (a.has_z ? 1u : 0u)));
+      tma_load_2d(sm.dout, &tm_dout, dd0, (int)tt0, &sm.bar);
       if (a.has_z) tma_load_2d(sm.z, &tm_z, dd0, (int)tt0, &sm.bar);
+    } else if (wq == 2) {
+      mbar_arrive_expect_tx(&sm.bar, box * (a.has_y ? 1u : 0u) + (uint32_t)a.box_x * N * 4u);
       if (a.has_y) tma_load_2d(sm.y, &tm_y, dd0, (int)tt0, &sm.bar);
       tma_load_2d(sm.H, &tm_cs, dd0, ch * N, &sm.bar);
-    } else if (wq == 2) {
-      mbar_arrive_expect_tx(&sm.bar, bcd + rows4 * 4u);
-      bulk_load_1d(sm.BC, a.BD + tt0 * N, bcd, &sm.bar);
-      if (rows4) bulk_load_1d(sm.pos, a.pos + tt0, rows4 * 4u, &sm.bar);
     } else {
-      mbar_arrive_expect_tx(&sm.bar, nval * N * 4u + (a.dt_bias ? nval * 4u : 0u) + (a.Dskip ? nval * 4u : 0u));
-      bulk_load_1d(sm.Araw, a.A + (int64_t)dd0 * N, nval * N * 4u, &sm.bar);
-      if (a.dt_bias) bulk_load_1d(sm.bias, a.dt_bias + dd0, nval * 4u, &sm.bar);
-      if (a.Dskip) bulk_load_1d(sm.dsk, a.Dskip + dd0, nval * 4u, &sm.bar);
+      // the chunk's B / C rows with its positions, and the tile's parameters
+      mbar_arrive_expect_tx(&sm.bar, (uint32_t)kBwdChunkRow + kBwdTileParams * 4u);
+      bulk_load_1d(sm.BC, a.BD + (int64_t)ch * (kBwdChunkRow / 16), kBwdChunkRow, &sm.bar);
+      bulk_load_1d(sm.Araw, a.tpar + (int64_t)tl * kBwdTileParams, kBwdTileParams * 4u, &sm.bar);
     }
   };
 
@@ -884,7 +891,6 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   const int chunk = a.n_chunks - 1 - rev;
   const int64_t t0 = (int64_t)chunk * kL;
   const int rows = (int)((a.T - t0) < kL ? (a.T - t0) : kL);
-  const int rows4 = rows & ~3;
   const int d0 = tile * kTW;
   const int bx = a.box_x;
   const int d = d0 + c0;                   // first channel of this thread's quad
@@ -948,8 +954,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       if (ok) accD = mk4(fma2(lo2(gv), lo2(u4), lo2(accD)), fma2(hi2(gv), hi2(u4), hi2(accD)));
     }
   }
-  const unsigned rst =
-      __ballot_sync(0xffffffffu, lane < rows && (lane < rows4 ? sm.pos[lane] : __ldg(a.pos + t0 + lane)) == 0);
+  const unsigned rst = __ballot_sync(0xffffffffu, lane < rows && sm.pos[lane] == 0);
   unsigned evH = 0u, evG = 0u, evF = 0u;
   if (kStates && a.seq) {
     const unsigned live = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
@@ -981,9 +986,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
       A[q][j] = make_float2(0.0f, 0.0f);
       h[q][j] = make_float2(0.0f, 0.0f);
       if (valid) {
-        float2 v = make_float2(sm.Araw[(c0 + 2 * j) * N + n], sm.Araw[(c0 + 2 * j + 1) * N + n]);
-        if (a.a_log) v = make_float2(-ex2(v.x * kLog2e), -ex2(v.y * kLog2e));
-        A[q][j] = mul2(v, splat2(kLog2e));
+        A[q][j] = make_float2(sm.Araw[(c0 + 2 * j) * N + n], sm.Araw[(c0 + 2 * j + 1) * N + n]);
         h[q][j] = *reinterpret_cast<const float2*>(sm.H + n * bx + c0 + 2 * j);
       }
     }
@@ -1474,8 +1477,10 @@ cudaError_t launch_scan_bwd(const ScanArgs& a, IO io, const CUtensorMap& tm_u,
     return e;
   }
   // B and C doubled once per call; every work item copies its chunk's rows
-  cudaError_t e = launch_double_bc(a.B, a.C, io, a.T, (int64_t)a.n_chunks * kBwdChunk, a.N, a.N == 16,
+  cudaError_t e = launch_double_bc(a.B, a.C, io, a.T, (int64_t)a.n_chunks * kBwdChunk, a.N, a.N == 16, a.pos,
                                    const_cast<float4*>(a.BD), const_cast<float4*>(a.CD), st);
+  if (e == cudaSuccess && a.N == 16)
+    e = launch_bwd_tile_params(a.A, a.dt_bias, a.Dskip, a.D, a.a_log != 0, const_cast<float*>(a.tpar), st);
   if (e != cudaSuccess) return e;
   kernel_timer_mark(kTimeScanBwd, true, st);
   e = io == IO::F32 ? launch_t<float>(a, tm_u, tm_dr, tm_z, tm_dout, tm_cs, tm_y, st)
