@@ -999,6 +999,15 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
   float* const pdB = a.part_dBC + ((int64_t)part * 2 * N + nF) * a.T + t0;
   float* const pdC = a.part_dBC + ((int64_t)part * 2 * N + N + nF) * a.T + t0;
 
+  // the right neighbour's inclusive carry words, first read two groups before
+  // the walk ends (that chunk started about a fifth of an item earlier and
+  // has nearly always stored them by then), so the read's round trip is over
+  // when the look-back checks them
+  const bool has_right = chunk < a.n_chunks - 1;
+  const float4* const right_carry =
+      reinterpret_cast<const float4*>(a.incl) + (((int64_t)tile * a.n_chunks + chunk + 1) * kThr + tid) * 2;
+  float4 early_lo = make_float4(0.0f, 0.0f, 0.0f, 0.0f), early_hi = early_lo;
+
   // ---- 2. forward walk; p_t = a_t h_{t-1} (8 words per token) to tensor memory
   float2 E[2][2], tot[2][2];
 #pragma unroll
@@ -1016,6 +1025,10 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     int pend_t = kL;
 #pragma unroll 1
     for (int g4 = 0; g4 < kL / 4; ++g4) {
+      if (g4 == kL / 4 - 2 && has_right) {
+        early_lo = ld_carry4(right_carry);
+        early_hi = ld_carry4(right_carry + 1);
+      }
       uint32_t hist[32];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -1084,8 +1097,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     };
     if (chunk < a.n_chunks - 1) {
       int j = chunk + 1, found = -1, timed_out = 0;
-      const int64_t js = ((base + j) * kThr + tid) * 2;
-      float4 vlo = ld_carry4(inc + js), vhi = ld_carry4(inc + js + 1);
+      float4 vlo = early_lo, vhi = early_hi;  // read during the forward walk
       if (__all_sync(0xffffffffu, carry_set4(vlo) && carry_set4(vhi))) {
         found = j;
       } else {
