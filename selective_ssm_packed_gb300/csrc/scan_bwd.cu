@@ -910,7 +910,7 @@ scan_bwd16_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     T* gdz = static_cast<T*>(a.dz);
     const int q = tid & 15;
     const float4 bias4 = a.dt_bias ? *reinterpret_cast<const float4*>(sm.bias + 4 * q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 2
+#pragma unroll 1
     for (int i = tid; i < kL * kCQ; i += kThr) {
       const int t = i >> 4;
       const int at = t * bx + 4 * q;
