@@ -63,7 +63,7 @@ def implementation_extra_bytes(D, e):
 # ncu capture of a kernel, per token, with the kernel it was taken on; the
 # line reports it only for that kernel.
 LAST_CAPTURE_TRAFFIC = {
-    ("m14b", "scan_bwd"): {"bytes_per_token": (412.017664e6 + 445.299968e6) / 8192,
+    ("m14b", "scan_bwd"): {"bytes_per_token": (411.232768e6 + 444.166912e6) / 8192,
                            "kernel": "scan_bwd16_kernel",
                            "source": "ncu --set full capture of scan_bwd16_kernel on m14b_small (T=8192), "
                                      "scaled by tokens"},
